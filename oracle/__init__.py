@@ -1,0 +1,310 @@
+"""fp64 oracle for the block-diffusion denoising step -- TEST INFRASTRUCTURE.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library: the per-position sampler, acceptance rule, stop test, Philox and the
+attention loops live in ``dg_oracle.c`` (plain single-threaded C, fp64); the
+LM-head product uses numpy's float64 matmul as a library step.  bf16 tensors
+are passed as raw ``uint16`` bit patterns and widened exactly to fp64.
+
+Sources, by page title and section:
+  * "DiffusionGemma Lab", section 2, items 1-7 (the sampler as coded).
+  * "DiffusionGemma: Parallel Denoising From an Autoregressive Checkpoint",
+    section "Finding" (entropy-bounded acceptance, temperature annealing,
+    adaptive stopping; causal encoder cache + bidirectional canvas decoder).
+  * Salmon et al., SC'11, for Philox4x32-10.
+
+Parity unpinned: the number of steps a converging block loop takes (no page
+gives one); everything else is pinned by tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dg_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_c_i32 = ctypes.c_int32
+_c_u32 = ctypes.c_uint32
+_c_u64 = ctypes.c_uint64
+_c_i64 = ctypes.c_int64
+_c_dbl = ctypes.c_double
+_c_flt = ctypes.c_float
+_vp = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile dg_oracle.c into liboracle.so with gcc (no fast-math, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        L.orc_philox4x32_10.argtypes = [_vp, _vp, _vp]
+        L.orc_philox4x32_10.restype = None
+        L.orc_gumbel_bits.argtypes = [_c_u64, _c_u32, _c_u32, _c_u32]
+        L.orc_gumbel_bits.restype = _c_u32
+        L.orc_renoise_token.argtypes = [_c_u64, _c_u32, _c_u32, _c_i32]
+        L.orc_renoise_token.restype = _c_i32
+        L.orc_init_token.argtypes = [_c_u64, _c_u32, _c_i32]
+        L.orc_init_token.restype = _c_i32
+        L.orc_init_canvas.argtypes = [_vp, _c_i32, _c_i32, _c_u64]
+        L.orc_init_canvas.restype = None
+        L.orc_logf.argtypes = [_c_flt]
+        L.orc_logf.restype = _c_flt
+        L.orc_uniform_open.argtypes = [_c_u32]
+        L.orc_uniform_open.restype = _c_flt
+        L.orc_gumbel_from_bits.argtypes = [_c_u32]
+        L.orc_gumbel_from_bits.restype = _c_flt
+        L.orc_sampler_row.argtypes = [_vp, _c_i32, _c_dbl, _c_u64, _c_u32, _c_u32,
+                                      _vp, _vp, _vp, _vp, _vp]
+        L.orc_sampler_row.restype = None
+        L.orc_accept_renoise.argtypes = [_vp, _vp, _vp, _vp, _c_i32, _c_i32, _c_dbl,
+                                         _c_u64, _c_u32, _c_u32, _vp, _vp]
+        L.orc_accept_renoise.restype = _c_i32
+        L.orc_stop.argtypes = [_vp, _vp, _vp, _c_i32, _c_i32, _c_dbl, _vp]
+        L.orc_stop.restype = _c_i32
+        L.orc_temperature.argtypes = [_c_i32, _c_i32, _c_dbl, _c_dbl]
+        L.orc_temperature.restype = _c_dbl
+        L.orc_attention_rows.argtypes = [_vp, _vp, _vp, _vp, _vp,
+                                         _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                         _c_dbl, _vp, _c_i64, _vp]
+        L.orc_attention_rows.restype = None
+        L.orc_gumbel_fill.argtypes = [_c_u64, _c_u32, _c_u32, _c_u32, _c_i32, _vp]
+        L.orc_gumbel_fill.restype = None
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(_vp)
+
+
+# ---------------------------------------------------------------- primitives
+def philox4x32_10(ctr: Sequence[int], key: Sequence[int]) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def logf(x: float) -> float:
+    return float(np.float32(lib().orc_logf(float(x))))
+
+
+def uniform_open(bits: int) -> float:
+    return float(np.float32(lib().orc_uniform_open(int(bits))))
+
+
+def gumbel_from_bits(bits: int) -> float:
+    return float(np.float32(lib().orc_gumbel_from_bits(int(bits))))
+
+
+def gumbel_fill(seed: int, row: int, step: int, v0: int, n: int) -> np.ndarray:
+    out = np.zeros(n, dtype=np.float32)
+    lib().orc_gumbel_fill(seed, row, step, v0, n, _ptr(out))
+    return out
+
+
+def gumbel_bits(seed: int, row: int, step: int, v: int) -> int:
+    return int(lib().orc_gumbel_bits(seed, row, step, v))
+
+
+def renoise_token(seed: int, row: int, step: int, V: int) -> int:
+    return int(lib().orc_renoise_token(seed, row, step, V))
+
+
+def init_canvas(n: int, V: int, seed: int) -> np.ndarray:
+    out = np.zeros(n, dtype=np.int32)
+    lib().orc_init_canvas(_ptr(out), n, V, seed)
+    return out
+
+
+def temperature(k: int, N: int, t0: float = 0.8, t1: float = 0.4) -> float:
+    return float(lib().orc_temperature(k, N, t0, t1))
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact widening of raw bf16 bit patterns (uint16) to float64."""
+    a = np.asarray(a, dtype=np.uint16)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- LM head
+def logits(x_bits: np.ndarray, w_bits: np.ndarray, rows: Optional[Sequence[int]] = None,
+           col_chunk: int = 32768) -> np.ndarray:
+    """fp64 logits X[rows] @ W for bf16 X [M, d] and W [d, V] (raw bits).
+
+    The product is numpy's float64 matmul (a library step); columns of W are
+    widened chunk by chunk to bound host memory.
+    """
+    X = bf16_bits_to_f64(x_bits if rows is None else np.asarray(x_bits)[np.asarray(rows)])
+    d, V = w_bits.shape
+    out = np.empty((X.shape[0], V), dtype=np.float64)
+    for c0 in range(0, V, col_chunk):
+        c1 = min(V, c0 + col_chunk)
+        out[:, c0:c1] = X @ bf16_bits_to_f64(w_bits[:, c0:c1])
+    return out
+
+
+# ---------------------------------------------------------------- sampler
+def sampler_row(logits_row: np.ndarray, T: float, seed: int, row: int, step: int) -> dict:
+    lr = np.ascontiguousarray(np.asarray(logits_row, dtype=np.float64))
+    H = ctypes.c_double()
+    smp = ctypes.c_int32()
+    am = ctypes.c_int32()
+    gm = ctypes.c_double()
+    amm = ctypes.c_double()
+    lib().orc_sampler_row(_ptr(lr), lr.shape[0], float(T), seed, row, step,
+                          ctypes.byref(H), ctypes.byref(smp), ctypes.byref(am),
+                          ctypes.byref(gm), ctypes.byref(amm))
+    return dict(H=H.value, sample=smp.value, argmax=am.value,
+                gumbel_margin=gm.value, argmax_margin=amm.value)
+
+
+def sampler(logits_rows: np.ndarray, T: float, seed: int, rows: Sequence[int], step: int) -> dict:
+    """Run sampler_row over a block of logits; rows[i] is the global row id of logits_rows[i]."""
+    n = logits_rows.shape[0]
+    res = dict(H=np.zeros(n), sample=np.zeros(n, np.int32), argmax=np.zeros(n, np.int32),
+               gumbel_margin=np.zeros(n), argmax_margin=np.zeros(n))
+    for t in range(n):
+        r = sampler_row(logits_rows[t], T, seed, int(rows[t]), step)
+        for k in res:
+            res[k][t] = r[k]
+    return res
+
+
+def accept_renoise(H: np.ndarray, sample: np.ndarray, canvas: np.ndarray, V: int, b: float,
+                   seed: int, row_base: int, step: int) -> dict:
+    """One canvas: returns the new canvas, accepted mask, k*, sorted order, boundary gap."""
+    Hf = np.ascontiguousarray(np.asarray(H, dtype=np.float32))
+    sm = np.ascontiguousarray(np.asarray(sample, dtype=np.int32))
+    cv = np.ascontiguousarray(np.array(canvas, dtype=np.int32, copy=True))
+    L = Hf.shape[0]
+    acc = np.zeros(L, dtype=np.uint8)
+    order = np.zeros(L, dtype=np.int32)
+    gap = ctypes.c_double()
+    k = lib().orc_accept_renoise(_ptr(Hf), _ptr(sm), _ptr(cv), _ptr(acc), L, V, float(b),
+                                 seed, row_base, step, _ptr(order), ctypes.byref(gap))
+    return dict(canvas=cv, accepted=acc, n_accepted=int(k), order=order, boundary_gap=gap.value)
+
+
+def stop(argmax: np.ndarray, prev_argmax: np.ndarray, H: np.ndarray, step: int,
+         threshold: float = 0.005) -> dict:
+    a = np.ascontiguousarray(np.asarray(argmax, dtype=np.int32))
+    p = np.ascontiguousarray(np.asarray(prev_argmax, dtype=np.int32))
+    Hf = np.ascontiguousarray(np.asarray(H, dtype=np.float32))
+    mean = ctypes.c_double()
+    s = lib().orc_stop(_ptr(a), _ptr(p), _ptr(Hf), a.shape[0], step, float(threshold),
+                       ctypes.byref(mean))
+    return dict(stop=int(s), mean_entropy=mean.value)
+
+
+# ---------------------------------------------------------------- attention
+def attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, rows) -> np.ndarray:
+    """fp64 attention for the listed flat query rows (b*L+i)*Hq+h; bf16 inputs as uint16."""
+    arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.uint16)) for a in (q, kp, vp, kc, vc)]
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((r.shape[0], D), dtype=np.float64)
+    lib().orc_attention_rows(*[_ptr(a) for a in arrs], B, L, P, Hq, Hkv, D, float(scale),
+                             _ptr(r), r.shape[0], _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- step / block
+def step(x_bits: np.ndarray, w_bits: np.ndarray, canvas: np.ndarray, prev_argmax: np.ndarray,
+         B: int, L: int, T: float, b: float, seed: int, k: int,
+         stop_threshold: float = 0.005) -> dict:
+    """One denoising step (LM head -> sampler -> accept/renoise -> stop) for B canvases."""
+    V = w_bits.shape[1]
+    lg = logits(x_bits, w_bits)
+    s = sampler(lg, T, seed, np.arange(B * L), k)
+    Hf = s["H"].astype(np.float32)
+    new_canvas = np.array(canvas, dtype=np.int32, copy=True).reshape(B, L)
+    accepted = np.zeros((B, L), np.uint8)
+    n_acc = np.zeros(B, np.int32)
+    stops = np.zeros(B, np.int32)
+    means = np.zeros(B)
+    gaps = np.zeros(B)
+    orders = np.zeros((B, L), np.int32)
+    for bb in range(B):
+        sl = slice(bb * L, (bb + 1) * L)
+        a = accept_renoise(Hf[sl], s["sample"][sl], new_canvas[bb], V, b, seed, bb * L, k)
+        new_canvas[bb] = a["canvas"]
+        accepted[bb] = a["accepted"]
+        n_acc[bb] = a["n_accepted"]
+        gaps[bb] = a["boundary_gap"]
+        orders[bb] = a["order"]
+        st = stop(s["argmax"][sl], np.asarray(prev_argmax).reshape(B, L)[bb], Hf[sl], k,
+                  stop_threshold)
+        stops[bb] = st["stop"]
+        means[bb] = st["mean_entropy"]
+    return dict(logits=lg, H=s["H"], H32=Hf, sample=s["sample"], argmax=s["argmax"],
+                gumbel_margin=s["gumbel_margin"], argmax_margin=s["argmax_margin"],
+                canvas=new_canvas.reshape(-1), accepted=accepted.reshape(-1),
+                n_accepted=n_acc, stop=stops, mean_entropy=means, boundary_gap=gaps,
+                order=orders)
+
+
+def block(hidden_bits_fn, w_bits: np.ndarray, B: int, L: int, b: float, seed: int,
+          max_steps: int = 48, t0: float = 0.8, t1: float = 0.4,
+          stop_threshold: float = 0.005) -> dict:
+    """The denoising loop of a batch of B independent canvases.
+
+    [Lab] items 1-5: uniform init, per-step sample/accept/renoise, linear
+    temperature, adaptive stop; the result is the argmax canvas of the step
+    at which a canvas stopped (or of the last step).  ``hidden_bits_fn(k)``
+    returns the bf16 hidden states [B*L, d] of step k (the decoder body is
+    outside this path).  Each canvas stops on its own: once its stop test
+    fires, its canvas, argmax and step count are frozen.
+    """
+    V = w_bits.shape[1]
+    canvas = init_canvas(B * L, V, seed).reshape(B, L)
+    prev = np.zeros((B, L), np.int32)
+    out_argmax = np.zeros((B, L), np.int32)
+    steps = np.zeros(B, np.int32)
+    done = np.zeros(B, bool)
+    history = []
+    for k in range(max_steps):
+        T = temperature(k, max_steps, t0, t1)
+        r = step(hidden_bits_fn(k), w_bits, canvas.reshape(-1), prev.reshape(-1), B, L, T, b,
+                 seed, k, stop_threshold)
+        am = r["argmax"].reshape(B, L)
+        cv = r["canvas"].reshape(B, L)
+        live = ~done
+        canvas[live] = cv[live]
+        out_argmax[live] = am[live]
+        steps[live] = k + 1
+        history.append(dict(T=T, live=live.copy(), n_accepted=r["n_accepted"].copy(),
+                            stop=r["stop"].copy(), mean_entropy=r["mean_entropy"].copy(),
+                            argmax=r["argmax"].copy(), canvas=r["canvas"].copy(),
+                            H32=r["H32"].copy(), sample=r["sample"].copy(),
+                            gumbel_margin=r["gumbel_margin"].copy(),
+                            argmax_margin=r["argmax_margin"].copy(),
+                            boundary_gap=r["boundary_gap"].copy(), order=r["order"].copy()))
+        done = done | (r["stop"] == 1)
+        prev = am.copy()
+        if bool(np.all(done)):
+            break
+    return dict(steps=steps, argmax=out_argmax.reshape(-1), canvas=canvas.reshape(-1),
+                history=history)
