@@ -1,0 +1,256 @@
+"""Python binding of libdg.so -- argument marshalling only.
+
+Every function here forwards to the C ABI declared in include/dg.h with
+ctypes: tensors are passed as device pointers (``tensor.data_ptr()``), the
+stream as the raw cudaStream_t of the current torch stream.  No step of the
+denoising path runs in Python or PyTorch; if the library is missing, the
+first call raises (there is no fallback).
+
+PyTorch is used only for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdg.so")
+
+DG_OK = 0
+STATUS_NAMES = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
+                3: "DG_ERR_ALIGNMENT", 4: "DG_ERR_WORKSPACE", 5: "DG_ERR_CUDA",
+                6: "DG_ERR_TIMEOUT", 7: "DG_ERR_DEVICE"}
+
+# Functions include/dg.h declares (checked by the CPU test-suite).
+EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
+            "dg_canvas_attn_workspace", "dg_canvas_attn",
+            "dg_denoise_step_workspace", "dg_denoise_step",
+            "dg_generate_block_workspace", "dg_generate_block",
+            "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
+            "dg_gumbel_fill", "dg_logf_eval"]
+
+
+class DgError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%s)" % (what, STATUS_NAMES.get(code, code),
+                                                 _lib().dg_status_string(code).decode()))
+
+
+class StepParams(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int), ("V", ctypes.c_int),
+                ("temperature", ctypes.c_double), ("entropy_bound", ctypes.c_float),
+                ("stop_threshold", ctypes.c_float), ("step", ctypes.c_int),
+                ("seed", ctypes.c_uint64)]
+
+
+class StepIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("canvas", "prev_argmax", "argmax", "sample", "entropy", "accepted",
+                 "n_accepted", "mean_entropy", "stop")]
+
+
+class BlockParams(ctypes.Structure):
+    _fields_ = [("max_steps", ctypes.c_int), ("t_start", ctypes.c_double),
+                ("t_end", ctypes.c_double), ("hidden_step_stride", ctypes.c_int64)]
+
+
+class BlockIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("canvas", "argmax", "steps_taken", "mean_entropy", "n_accepted_hist")]
+
+
+_L = None
+
+
+def _lib():
+    global _L
+    if _L is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdg.so is not built: run __graft_entry__.build() "
+                               "(block_diffusion_decoding_gb300/build.py)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, u32, u64, sz, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32,
+                                      ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float)
+        sp, si, bp, bi = (ctypes.POINTER(StepParams), ctypes.POINTER(StepIO),
+                          ctypes.POINTER(BlockParams), ctypes.POINTER(BlockIO))
+        sig = {
+            "dg_status_string": ([i32], ctypes.c_char_p),
+            "dg_version": ([], i32),
+            "dg_read_device_status": ([vp, ctypes.POINTER(ctypes.c_int), i32, vp], i32),
+            "dg_canvas_attn_workspace": ([i32] * 6, sz),
+            "dg_canvas_attn": ([vp] * 6 + [i32] * 6 + [f32, vp, sz, vp], i32),
+            "dg_denoise_step_workspace": ([sp], sz),
+            "dg_denoise_step": ([vp, vp, sp, si, vp, sz, vp], i32),
+            "dg_generate_block_workspace": ([sp, bp], sz),
+            "dg_generate_block": ([vp, vp, sp, bp, bi, vp, sz, vp], i32),
+            "dg_sampler_workspace": ([sp], sz),
+            "dg_sampler_from_logits": ([vp, sp, si, vp, sz, vp], i32),
+            "dg_accept_renoise": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
+            "dg_gumbel_fill": ([u64, u32, u32, u32, i32, vp, vp], i32),
+            "dg_logf_eval": ([vp, vp, i32, vp], i32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _L = L
+    return _L
+
+
+def lib():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _lib()
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != DG_OK:
+        raise DgError(rc, what)
+
+
+# ---------------------------------------------------------------- attention
+def canvas_attn_workspace(B, L, P, Hq, Hkv, D) -> int:
+    return int(_lib().dg_canvas_attn_workspace(B, L, P, Hq, Hkv, D))
+
+
+def canvas_attn(q, k_prefix, v_prefix, k_canvas, v_canvas, out, scale, workspace, stream=None):
+    """dg_canvas_attn on bf16 tensors q/out [B,L,Hq,D], k/v prefix [B,P,Hkv,D], canvas [B,L,Hkv,D]."""
+    B, L, Hq, D = q.shape
+    if k_prefix is not None and k_prefix.shape[1] > 0:
+        P = k_prefix.shape[1]
+    else:
+        P = 0
+    Hkv = k_canvas.shape[2]
+    rc = _lib().dg_canvas_attn(_p(q), _p(k_prefix) if P else None, _p(v_prefix) if P else None,
+                               _p(k_canvas), _p(v_canvas), _p(out), B, L, P, Hq, Hkv, D,
+                               float(scale), _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_canvas_attn")
+
+
+# ---------------------------------------------------------------- step
+def step_params(B, L, d, V, temperature, entropy_bound=0.1, stop_threshold=0.005, step=0,
+                seed=0) -> StepParams:
+    return StepParams(B, L, d, V, temperature, entropy_bound, stop_threshold, step, seed)
+
+
+class StepBuffers:
+    """Device outputs of one step (dg_step_io) for B canvases of length L."""
+
+    def __init__(self, B: int, L: int, device="cuda"):
+        M = B * L
+        i32 = dict(dtype=torch.int32, device=device)
+        self.canvas = torch.zeros(M, **i32)
+        self.prev_argmax = torch.full((M,), -1, **i32)
+        self.argmax = torch.zeros(M, **i32)
+        self.sample = torch.zeros(M, **i32)
+        self.entropy = torch.zeros(M, dtype=torch.float32, device=device)
+        self.accepted = torch.zeros(M, dtype=torch.uint8, device=device)
+        self.n_accepted = torch.zeros(B, **i32)
+        self.mean_entropy = torch.zeros(B, dtype=torch.float32, device=device)
+        self.stop = torch.zeros(B, **i32)
+
+    def io(self) -> StepIO:
+        return StepIO(*[ctypes.c_void_p(getattr(self, n).data_ptr()) for n, _ in StepIO._fields_])
+
+
+def denoise_step_workspace(p: StepParams) -> int:
+    return int(_lib().dg_denoise_step_workspace(ctypes.byref(p)))
+
+
+def denoise_step(hidden, w, p: StepParams, bufs: StepBuffers, workspace, stream=None):
+    io = bufs.io()
+    rc = _lib().dg_denoise_step(_p(hidden), _p(w), ctypes.byref(p), ctypes.byref(io),
+                                _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_denoise_step")
+
+
+def sampler_workspace(p: StepParams) -> int:
+    return int(_lib().dg_sampler_workspace(ctypes.byref(p)))
+
+
+def sampler_from_logits(logits, p: StepParams, bufs: StepBuffers, workspace, stream=None):
+    io = bufs.io()
+    rc = _lib().dg_sampler_from_logits(_p(logits), ctypes.byref(p), ctypes.byref(io),
+                                       _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_sampler_from_logits")
+
+
+def accept_renoise(entropy, sample, argmax, p: StepParams, bufs: StepBuffers, workspace,
+                   stream=None):
+    io = bufs.io()
+    rc = _lib().dg_accept_renoise(_p(entropy), _p(sample), _p(argmax), ctypes.byref(p),
+                                  ctypes.byref(io), _p(workspace), workspace.numel(),
+                                  _stream(stream))
+    _check(rc, "dg_accept_renoise")
+
+
+# ---------------------------------------------------------------- block loop
+class BlockBuffers:
+    def __init__(self, B: int, L: int, max_steps: int, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        self.canvas = torch.zeros(B * L, **i32)
+        self.argmax = torch.zeros(B * L, **i32)
+        self.steps_taken = torch.zeros(B, **i32)
+        self.mean_entropy = torch.zeros(B, dtype=torch.float32, device=device)
+        self.n_accepted_hist = torch.zeros(max_steps * B, **i32)
+
+    def io(self) -> BlockIO:
+        return BlockIO(*[ctypes.c_void_p(getattr(self, n).data_ptr()) for n, _ in BlockIO._fields_])
+
+
+def block_params(max_steps=48, t_start=0.8, t_end=0.4, hidden_step_stride=0) -> BlockParams:
+    return BlockParams(max_steps, t_start, t_end, hidden_step_stride)
+
+
+def generate_block_workspace(p: StepParams, bp: BlockParams) -> int:
+    return int(_lib().dg_generate_block_workspace(ctypes.byref(p), ctypes.byref(bp)))
+
+
+def generate_block(hidden_steps, w, p: StepParams, bp: BlockParams, bufs: BlockBuffers,
+                   workspace, stream=None):
+    io = bufs.io()
+    rc = _lib().dg_generate_block(_p(hidden_steps), _p(w), ctypes.byref(p), ctypes.byref(bp),
+                                  ctypes.byref(io), _p(workspace), workspace.numel(),
+                                  _stream(stream))
+    _check(rc, "dg_generate_block")
+
+
+# ---------------------------------------------------------------- checks / status
+def gumbel_fill(seed, row, step, v0, n, out, stream=None):
+    _check(_lib().dg_gumbel_fill(seed, row, step, v0, n, _p(out), _stream(stream)),
+           "dg_gumbel_fill")
+
+
+def logf_eval(x, y, stream=None):
+    _check(_lib().dg_logf_eval(_p(x), _p(y), x.numel(), _stream(stream)), "dg_logf_eval")
+
+
+def read_device_status(workspace, clear=False, stream=None) -> int:
+    v = ctypes.c_int(0)
+    _check(_lib().dg_read_device_status(_p(workspace), ctypes.byref(v), 1 if clear else 0,
+                                        _stream(stream)), "dg_read_device_status")
+    return v.value
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zeroed byte tensor usable as a workspace."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def bf16_from_bits(bits, device="cuda") -> torch.Tensor:
+    """A bf16 tensor holding the given uint16 bit patterns (numpy array)."""
+    import numpy as np
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device) if str(device) != "cpu" else t

@@ -1,0 +1,793 @@
+// dg_api.cu -- the C ABI of libdg.so (declared in include/dg.h): argument
+// validation, workspace layout, TMA tensor-map encoding, kernel launches and
+// the CUDA graph of the block loop.  Host code only; kernels live in the
+// other .cu files.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "dg_kernels.h"
+
+using namespace dg;
+
+namespace {
+
+// ---------------------------------------------------------------- small utilities
+constexpr int kMaxSlots = 256;       // upper bound on LM-head CTAs (>= SM count)
+constexpr int kAssumedMaxSMs = 256;  // workspace queries do not touch the GPU
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+inline uint64_t f2u(float f)
+{
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return u;
+}
+inline uint64_t d2u(double f)
+{
+    uint64_t u;
+    std::memcpy(&u, &f, 8);
+    return u;
+}
+
+#define DG_CUDA_TRY(expr)                                  \
+    do {                                                   \
+        cudaError_t e_ = (expr);                           \
+        if (e_ != cudaSuccess) {                           \
+            (void)cudaGetLastError();                      \
+            return DG_ERR_CUDA;                            \
+        }                                                  \
+    } while (0)
+
+struct DeviceInfo {
+    int sms = 0;
+    bool attrs_set = false;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+
+int current_device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    DG_CUDA_TRY(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (di.sms == 0) {
+        DG_CUDA_TRY(cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev));
+    }
+    if (!di.attrs_set) {
+        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kLmSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d128,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         attn_smem_bytes(128)));
+        DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d256,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         attn_smem_bytes(256)));
+        di.attrs_set = true;
+    }
+    *out = &di;
+    return DG_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle.  dims/strides innermost first;
+// strides[i] is the byte stride of dimension i+1.
+int make_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                  const uint64_t *strides_bytes, const uint32_t *box)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return DG_ERR_CUDA;
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                    const_cast<void *>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- LM-head plan
+struct LmPlan {
+    int M, V, d;
+    int BN, ntn, mblocks, total, n_slots;
+};
+
+// Pick the tile width: fewest columns on the busiest CTA, plus a per-tile
+// overhead (re-reading the hidden block, epilogue start-up).
+LmPlan plan_lm_head(int M, int d, int V, int sms)
+{
+    LmPlan p{};
+    p.M = M;
+    p.V = V;
+    p.d = d;
+    p.mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
+    const char *env = std::getenv("DG_LM_BN");
+    const int forced = env ? std::atoi(env) : 0;
+    long best = -1;
+    for (int bn = 128; bn >= 64; bn -= 16) {
+        if (forced && bn != forced) continue;
+        const int ntn = (V + bn - 1) / bn;
+        const int total = ntn * p.mblocks;
+        const int slots = std::min(std::min(total, sms), kMaxSlots);
+        const long per_cta = (total + slots - 1) / slots;
+        const long cost = per_cta * (bn + 40);
+        if (best < 0 || cost < best) {
+            best = cost;
+            p.BN = bn;
+            p.ntn = ntn;
+            p.total = total;
+            p.n_slots = slots;
+        }
+    }
+    return p;
+}
+
+// Upper bound on the slot count of any plan for these shapes (workspace
+// queries do not know the SM count; every plan uses at most this many).
+int slot_bound(int M, int V)
+{
+    const long mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
+    const long tiles = mblocks * ((V + 63) / 64);
+    return static_cast<int>(std::min<long>(tiles, kMaxSlots));
+}
+
+// Workspace layout of one step: header | partials (7 x n_slots x M x 4 B) |
+// counters (B ints).
+struct StepWs {
+    WsHeader *hdr;
+    Partials part;
+    int *counters;
+};
+
+size_t step_ws_bytes(int M, int B, int slots)
+{
+    size_t b = sizeof(WsHeader);
+    b += round_up(static_cast<size_t>(7) * slots * M * 4, 256);
+    b += round_up(static_cast<size_t>(B) * 4, 256);
+    return b;
+}
+
+StepWs carve_step_ws(void *ws, int M, int slots)
+{
+    StepWs w{};
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    w.hdr = reinterpret_cast<WsHeader *>(p);
+    p += sizeof(WsHeader);
+    const size_t n = static_cast<size_t>(slots) * M;
+    float *f = reinterpret_cast<float *>(p);
+    w.part.m = f;
+    w.part.S = f + n;
+    w.part.A = f + 2 * n;
+    w.part.gbest = f + 3 * n;
+    w.part.amax = f + 4 * n;
+    w.part.gidx = reinterpret_cast<int *>(f + 5 * n);
+    w.part.aidx = reinterpret_cast<int *>(f + 6 * n);
+    p += round_up(7 * n * 4, 256);
+    w.counters = reinterpret_cast<int *>(p);
+    return w;
+}
+
+int check_step_params(const dg_step_params *p)
+{
+    if (p == nullptr) return DG_ERR_INVALID_ARG;
+    if (p->B < 1 || p->L < 1 || p->V < 1 || p->d < 1) return DG_ERR_INVALID_ARG;
+    if (!(p->temperature > 0.0) || !std::isfinite(p->temperature)) return DG_ERR_INVALID_ARG;
+    if (!(p->entropy_bound >= 0.f) || !std::isfinite(p->entropy_bound)) return DG_ERR_INVALID_ARG;
+    if (!std::isfinite(p->stop_threshold)) return DG_ERR_INVALID_ARG;
+    if (p->step < 0) return DG_ERR_INVALID_ARG;
+    if (p->L > kMaxCanvas) return DG_ERR_UNSUPPORTED;
+    if (p->V % 8 != 0 || p->V < 64) return DG_ERR_UNSUPPORTED;
+    if (static_cast<long long>(p->B) * p->L > (1LL << 30)) return DG_ERR_UNSUPPORTED;
+    return DG_OK;
+}
+
+int check_io(const dg_step_io *io, bool need_outputs)
+{
+    if (io == nullptr) return DG_ERR_INVALID_ARG;
+    if (!io->canvas || !io->prev_argmax || !io->accepted || !io->n_accepted || !io->mean_entropy ||
+        !io->stop)
+        return DG_ERR_INVALID_ARG;
+    if (need_outputs && (!io->argmax || !io->sample || !io->entropy)) return DG_ERR_INVALID_ARG;
+    return DG_OK;
+}
+
+StepSource step_source(const dg_step_params *p)
+{
+    StepSource s{};
+    s.ctl = nullptr;
+    s.invT = static_cast<float>(1.0 / p->temperature);
+    s.c2 = s.invT * 1.44269502162933349609375f;   // fp32(log2 e)
+    s.step = p->step;
+    return s;
+}
+
+AcceptArgs accept_args(const dg_step_params *p, const dg_step_io *io)
+{
+    AcceptArgs a{};
+    a.B = p->B;
+    a.L = p->L;
+    a.V = p->V;
+    a.bound = p->entropy_bound;
+    a.threshold = p->stop_threshold;
+    a.seed = p->seed;
+    a.step = p->step;
+    a.canvas = io->canvas;
+    a.prev_argmax = io->prev_argmax;
+    a.accepted = io->accepted;
+    a.n_accepted = io->n_accepted;
+    a.mean_entropy = io->mean_entropy;
+    a.stop = io->stop;
+    return a;
+}
+
+// Enqueue LM head (or logits fold) + combine/accept for one step.
+int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, const float *logits,
+                 const uint16_t *w, const dg_step_params *p, const LmPlan &plan, StepWs &ws,
+                 const StepSource &src, float *H, int32_t *sample, int32_t *argmax,
+                 const AcceptArgs &acc, cudaStream_t st)
+{
+    const int M = p->B * p->L;
+    if (logits == nullptr) {
+        CUtensorMap mx, mw;
+        {
+            const uint64_t dims[3] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(M),
+                                      static_cast<uint64_t>(x_steps)};
+            const uint64_t strides[2] = {static_cast<uint64_t>(p->d) * 2,
+                                         static_cast<uint64_t>(hidden_stride) * 2};
+            const uint32_t box[3] = {64, 256, 1};
+            const int rank = x_steps > 1 ? 3 : 2;
+            int rc = make_map_bf16(&mx, hidden, rank, dims, strides, box);
+            if (rc != DG_OK) return rc;
+        }
+        {
+            const uint64_t dims[2] = {static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d)};
+            const uint64_t strides[1] = {static_cast<uint64_t>(p->V) * 2};
+            const uint32_t box[2] = {64, 64};
+            int rc = make_map_bf16(&mw, w, 2, dims, strides, box);
+            if (rc != DG_OK) return rc;
+        }
+        LmHeadArgs a{};
+        a.M = M;
+        a.d = p->d;
+        a.V = p->V;
+        a.BN = plan.BN;
+        a.ntn = plan.ntn;
+        a.total = plan.total;
+        a.kblocks = p->d / 64;
+        a.nbox_b = (plan.BN + 63) / 64;
+        a.x_3d = x_steps > 1 ? 1 : 0;
+        a.part = ws.part;
+        a.src = src;
+        a.seed = p->seed;
+        a.ws = ws.hdr;
+        a.counters = ws.counters;
+        a.ncounters = p->B;
+        lm_head_kernel<<<plan.n_slots, kLmThreads, kLmSmemBytes, st>>>(mx, mw, a);
+    } else {
+        FoldArgs f{};
+        f.M = M;
+        f.V = p->V;
+        f.BN = plan.BN;
+        f.ntn = plan.ntn;
+        f.total = plan.total;
+        f.n_slots = plan.n_slots;
+        f.part = ws.part;
+        f.src = src;
+        f.seed = p->seed;
+        f.counters = ws.counters;
+        f.ncounters = p->B;
+        logits_fold_kernel<<<plan.n_slots, 256, 0, st>>>(logits, f);
+    }
+    DG_CUDA_TRY(cudaGetLastError());
+    CombineArgs c{};
+    c.part = ws.part;
+    c.n_slots = plan.n_slots;
+    c.ntn = plan.ntn;
+    c.total = plan.total;
+    c.M = M;
+    c.H = H;
+    c.sample = sample;
+    c.argmax = argmax;
+    c.counters = ws.counters;
+    dim3 grid((p->L + 7) / 8, p->B);
+    combine_accept_kernel<<<grid, 256, 0, st>>>(c, acc);
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+// ---------------------------------------------------------------- attention plan
+struct AttnPlan {
+    int BKV, nkt_p, nkt_c, nkt, mtiles, blocks, nsplit, tps;
+};
+
+AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
+{
+    AttnPlan a{};
+    a.BKV = (D == 128) ? 128 : 64;
+    a.nkt_p = (P + a.BKV - 1) / a.BKV;
+    a.nkt_c = (L + a.BKV - 1) / a.BKV;
+    a.nkt = a.nkt_p + a.nkt_c;
+    const int G = Hq / Hkv;
+    a.mtiles = (L * G + 127) / 128;
+    a.blocks = a.mtiles * Hkv * B;
+    // splits: minimise (waves x tiles per split), preferring fewer splits
+    long best = -1;
+    const char *env = std::getenv("DG_ATTN_SPLITS");
+    const int forced = env ? std::atoi(env) : 0;
+    for (int ns = 1; ns <= a.nkt; ++ns) {
+        const int tps = (a.nkt + ns - 1) / ns;
+        const int real = (a.nkt + tps - 1) / tps;
+        if (real != ns) continue;
+        if (forced && ns != std::min(forced, a.nkt)) continue;
+        const long waves = (static_cast<long>(a.blocks) * ns + sms - 1) / sms;
+        const long cost = waves * (tps + 2) * 16 + ns;
+        if (best < 0 || cost < best) {
+            best = cost;
+            a.nsplit = ns;
+            a.tps = tps;
+        }
+    }
+    if (best < 0) {   // forced split count not realisable: no split
+        a.nsplit = 1;
+        a.tps = a.nkt;
+    }
+    return a;
+}
+
+size_t attn_ws_bytes(int B, int L, int Hq, int D, int nsplit)
+{
+    size_t b = sizeof(WsHeader);
+    if (nsplit > 1) {
+        const size_t nr = static_cast<size_t>(B) * L * Hq;
+        b += round_up(static_cast<size_t>(nsplit) * nr * D * 4, 256);
+        b += round_up(static_cast<size_t>(nsplit) * nr * 8, 256);
+    }
+    return b;
+}
+
+// ---------------------------------------------------------------- block-loop graph cache
+struct BlockGraph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+std::map<std::vector<uint64_t>, BlockGraph> g_block_graphs;
+
+size_t block_ws_layout(const dg_step_params *p, int slots, size_t *off_ctl, size_t *off_scratch)
+{
+    const int M = p->B * p->L;
+    size_t b = step_ws_bytes(M, p->B, slots);
+    b = round_up(b, 256);
+    *off_ctl = b;
+    b += round_up(sizeof(LoopCtl), 256);
+    *off_scratch = b;
+    // H (M f32), sample, argmax, prev_argmax (M i32), accepted (M u8),
+    // n_accepted, stop, done (B i32)
+    b += round_up(static_cast<size_t>(M) * 4, 256) * 4;
+    b += round_up(static_cast<size_t>(M), 256);
+    b += round_up(static_cast<size_t>(p->B) * 4, 256) * 3;
+    return b;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char *dg_status_string(int status)
+{
+    switch (status) {
+    case DG_OK: return "ok";
+    case DG_ERR_INVALID_ARG: return "invalid argument";
+    case DG_ERR_UNSUPPORTED: return "unsupported shape";
+    case DG_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+    case DG_ERR_WORKSPACE: return "workspace missing or too small";
+    case DG_ERR_CUDA: return "CUDA runtime error";
+    case DG_ERR_TIMEOUT: return "device wait timed out";
+    case DG_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+    }
+}
+
+int dg_version(void) { return 100; }
+
+int dg_read_device_status(const void *workspace, int *status_out, int clear, void *stream)
+{
+    if (workspace == nullptr || status_out == nullptr) return DG_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaStream_t st = as_stream(stream);
+    DG_CUDA_TRY(cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st));
+    DG_CUDA_TRY(cudaStreamSynchronize(st));
+    *status_out = v;
+    if (clear) {
+        DG_CUDA_TRY(cudaMemsetAsync(const_cast<void *>(workspace), 0, sizeof(WsHeader), st));
+        DG_CUDA_TRY(cudaStreamSynchronize(st));
+    }
+    return DG_OK;
+}
+
+// ---------------------------------------------------------------- attention
+size_t dg_canvas_attn_workspace(int B, int L, int P, int Hq, int Hkv, int D)
+{
+    if (B < 1 || L < 1 || P < 0 || Hq < 1 || Hkv < 1 || (D != 128 && D != 256) || Hq % Hkv)
+        return 0;
+    const int G = Hq / Hkv;
+    if (G > 16 || (G & (G - 1)) != 0) return 0;
+    // the split count depends on the SM count: take the largest over any GPU
+    size_t mx = 0;
+    for (int sms = 1; sms <= kAssumedMaxSMs; ++sms) {
+        const AttnPlan q = plan_attn(B, L, P, Hq, Hkv, D, sms);
+        mx = std::max(mx, attn_ws_bytes(B, L, Hq, D, q.nsplit));
+    }
+    return mx;
+}
+
+int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                   const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *out, int B, int L,
+                   int P, int Hq, int Hkv, int D, float scale, void *workspace,
+                   size_t workspace_bytes, void *stream)
+{
+    if (!q || !k_canvas || !v_canvas || !out) return DG_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || P < 0 || Hq < 1 || Hkv < 1) return DG_ERR_INVALID_ARG;
+    if (P > 0 && (!k_prefix || !v_prefix)) return DG_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return DG_ERR_INVALID_ARG;
+    if (D != 128 && D != 256) return DG_ERR_UNSUPPORTED;
+    if (Hq % Hkv != 0) return DG_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (G > 16 || (G & (G - 1)) != 0) return DG_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * L * Hq > (1LL << 30) || P > (1 << 30)) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_canvas) || !aligned16(v_canvas) || !aligned16(out) ||
+        (P > 0 && (!aligned16(k_prefix) || !aligned16(v_prefix))))
+        return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_canvas_attn_workspace(B, L, P, Hq, Hkv, D))
+        return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    int rc = current_device_info(&di);
+    if (rc != DG_OK) return rc;
+    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms);
+    cudaStream_t st = as_stream(stream);
+
+    CUtensorMap mq, mkp, mvp, mkc, mvc;
+    {
+        // Q [B, L, Hq, D] as {D, G, Hkv, L, B}
+        const uint64_t dims[5] = {static_cast<uint64_t>(D), static_cast<uint64_t>(G),
+                                  static_cast<uint64_t>(Hkv), static_cast<uint64_t>(L),
+                                  static_cast<uint64_t>(B)};
+        const uint64_t strides[4] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(G) * D * 2,
+                                     static_cast<uint64_t>(Hq) * D * 2,
+                                     static_cast<uint64_t>(L) * Hq * D * 2};
+        const uint32_t box[5] = {64, static_cast<uint32_t>(G), 1, static_cast<uint32_t>(128 / G), 1};
+        rc = make_map_bf16(&mq, q, 5, dims, strides, box);
+        if (rc != DG_OK) return rc;
+    }
+    auto kv_map = [&](CUtensorMap *m, const uint16_t *base, int rows) -> int {
+        // [B, rows, Hkv, D] as {D, Hkv, rows, B}
+        const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
+                                  static_cast<uint64_t>(rows), static_cast<uint64_t>(B)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2,
+                                     static_cast<uint64_t>(Hkv) * D * 2,
+                                     static_cast<uint64_t>(rows) * Hkv * D * 2};
+        const uint32_t box[4] = {64, 1, static_cast<uint32_t>(ap.BKV), 1};
+        return make_map_bf16(m, base, 4, dims, strides, box);
+    };
+    if ((rc = kv_map(&mkc, k_canvas, L)) != DG_OK) return rc;
+    if ((rc = kv_map(&mvc, v_canvas, L)) != DG_OK) return rc;
+    if (P > 0) {
+        if ((rc = kv_map(&mkp, k_prefix, P)) != DG_OK) return rc;
+        if ((rc = kv_map(&mvp, v_prefix, P)) != DG_OK) return rc;
+    } else {
+        mkp = mkc;
+        mvp = mvc;
+    }
+    AttnArgs a{};
+    a.B = B;
+    a.L = L;
+    a.P = P;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.G = G;
+    a.rows = L * G;
+    a.mtiles = ap.mtiles;
+    a.nsplit = ap.nsplit;
+    a.nkt_p = ap.nkt_p;
+    a.nkt_c = ap.nkt_c;
+    a.tiles_per_split = ap.tps;
+    a.scale_log2 = scale * 1.44269502162933349609375f;
+    a.out = out;
+    a.ws = static_cast<WsHeader *>(workspace);
+    if (ap.nsplit > 1) {
+        uint8_t *p = static_cast<uint8_t *>(workspace) + sizeof(WsHeader);
+        const size_t nr = static_cast<size_t>(B) * L * Hq;
+        a.part_o = reinterpret_cast<float *>(p);
+        a.part_ml = reinterpret_cast<float *>(
+            p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 4, 256));
+    }
+    dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);
+    if (D == 128)
+        attn_kernel_d128<<<grid, kAttnThreads, attn_smem_bytes(128), st>>>(mq, mkp, mvp, mkc, mvc, a);
+    else
+        attn_kernel_d256<<<grid, kAttnThreads, attn_smem_bytes(256), st>>>(mq, mkp, mvp, mkc, mvc, a);
+    DG_CUDA_TRY(cudaGetLastError());
+    if (ap.nsplit > 1) {
+        const size_t nr = static_cast<size_t>(B) * L * Hq;
+        attn_combine_kernel<<<static_cast<unsigned>((nr + 7) / 8), 256, 0, st>>>(a);
+        DG_CUDA_TRY(cudaGetLastError());
+    }
+    return DG_OK;
+}
+
+// ---------------------------------------------------------------- one step
+size_t dg_denoise_step_workspace(const dg_step_params *p)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    const int M = p->B * p->L;
+    return step_ws_bytes(M, p->B, slot_bound(M, p->V));
+}
+
+int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_params *p,
+                    const dg_step_io *io, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if ((rc = check_io(io, true)) != DG_OK) return rc;
+    if (!hidden || !w) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(w)) return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_denoise_step_workspace(p))
+        return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    const int M = p->B * p->L;
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    const StepSource src = step_source(p);
+    const AcceptArgs acc = accept_args(p, io);
+    return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
+                        io->argmax, acc, as_stream(stream));
+}
+
+// ---------------------------------------------------------------- sampler on given logits
+size_t dg_sampler_workspace(const dg_step_params *p)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    const int M = p->B * p->L;
+    return step_ws_bytes(M, p->B, slot_bound(M, p->V));
+}
+
+int dg_sampler_from_logits(const float *logits, const dg_step_params *p, const dg_step_io *io,
+                           void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if ((rc = check_io(io, true)) != DG_OK) return rc;
+    if (!logits) return DG_ERR_INVALID_ARG;
+    if (!aligned16(logits)) return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_sampler_workspace(p)) return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    const int M = p->B * p->L;
+    const LmPlan plan = plan_lm_head(M, 64, p->V, di->sms);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    const StepSource src = step_source(p);
+    const AcceptArgs acc = accept_args(p, io);
+    return enqueue_step(nullptr, 0, 1, logits, nullptr, p, plan, ws, src, io->entropy, io->sample,
+                        io->argmax, acc, as_stream(stream));
+}
+
+int dg_accept_renoise(const float *entropy, const int32_t *sample, const int32_t *argmax,
+                      const dg_step_params *p, const dg_step_io *io, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if ((rc = check_io(io, false)) != DG_OK) return rc;
+    if (!entropy || !sample || !argmax) return DG_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < sizeof(WsHeader)) return DG_ERR_WORKSPACE;
+    AcceptArgs acc = accept_args(p, io);
+    accept_only_kernel<<<p->B, 256, 0, as_stream(stream)>>>(entropy, sample, argmax, acc);
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+// ---------------------------------------------------------------- block loop
+size_t dg_generate_block_workspace(const dg_step_params *p, const dg_block_params *bp)
+{
+    if (check_step_params(p) != DG_OK || bp == nullptr) return 0;
+    const int M = p->B * p->L;
+    size_t oc, os;
+    return block_ws_layout(p, slot_bound(M, p->V), &oc, &os);
+}
+
+int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_step_params *p,
+                      const dg_block_params *bp, const dg_block_io *io, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if (bp == nullptr || io == nullptr) return DG_ERR_INVALID_ARG;
+    if (bp->max_steps < 1 || bp->max_steps > kMaxLoopSteps) return DG_ERR_UNSUPPORTED;
+    if (!(bp->t_start > 0.0) || !(bp->t_end > 0.0)) return DG_ERR_INVALID_ARG;
+    if (bp->hidden_step_stride < 0) return DG_ERR_INVALID_ARG;
+    if (!io->canvas || !io->argmax || !io->steps_taken || !io->mean_entropy)
+        return DG_ERR_INVALID_ARG;
+    if (!hidden_steps || !w) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden_steps) || !aligned16(w)) return DG_ERR_ALIGNMENT;
+    if ((bp->hidden_step_stride * 2) % 16 != 0) return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_generate_block_workspace(p, bp))
+        return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    const int M = p->B * p->L;
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
+    size_t off_ctl, off_scr;
+    block_ws_layout(p, slot_bound(M, p->V), &off_ctl, &off_scr);
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    LoopCtl *ctl = reinterpret_cast<LoopCtl *>(base + off_ctl);
+    uint8_t *sp = base + off_scr;
+    const size_t m4 = round_up(static_cast<size_t>(M) * 4, 256);
+    const size_t b4 = round_up(static_cast<size_t>(p->B) * 4, 256);
+    float *H = reinterpret_cast<float *>(sp);
+    int32_t *sample = reinterpret_cast<int32_t *>(sp + m4);
+    int32_t *argmax = reinterpret_cast<int32_t *>(sp + 2 * m4);
+    int32_t *prev = reinterpret_cast<int32_t *>(sp + 3 * m4);
+    uint8_t *accepted = sp + 4 * m4;
+    uint8_t *sp2 = sp + 4 * m4 + round_up(static_cast<size_t>(M), 256);
+    int32_t *n_acc = reinterpret_cast<int32_t *>(sp2);
+    int32_t *stop = reinterpret_cast<int32_t *>(sp2 + b4);
+    int32_t *done = reinterpret_cast<int32_t *>(sp2 + 2 * b4);
+
+    cudaStream_t st = as_stream(stream);
+    const int x_steps = bp->hidden_step_stride > 0 ? bp->max_steps : 1;
+
+    int dev = 0;
+    DG_CUDA_TRY(cudaGetDevice(&dev));
+    const std::vector<uint64_t> key = {
+        reinterpret_cast<uint64_t>(hidden_steps), reinterpret_cast<uint64_t>(w),
+        reinterpret_cast<uint64_t>(workspace), reinterpret_cast<uint64_t>(io->canvas),
+        reinterpret_cast<uint64_t>(io->argmax), reinterpret_cast<uint64_t>(io->steps_taken),
+        reinterpret_cast<uint64_t>(io->mean_entropy),
+        reinterpret_cast<uint64_t>(io->n_accepted_hist), static_cast<uint64_t>(p->B),
+        static_cast<uint64_t>(p->L), static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->V),
+        f2u(p->entropy_bound), f2u(p->stop_threshold), d2u(bp->t_start), d2u(bp->t_end), p->seed,
+        static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(bp->hidden_step_stride),
+        static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.n_slots),
+        static_cast<uint64_t>(dev)};
+
+    BlockGraph *bgp = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_block_graphs.find(key);
+        if (it != g_block_graphs.end()) bgp = &it->second;
+    }
+    if (bgp == nullptr) {
+        BlockGraph bg;
+        DG_CUDA_TRY(cudaGraphCreate(&bg.graph, 0));
+        cudaGraphConditionalHandle cond;
+        DG_CUDA_TRY(cudaGraphConditionalHandleCreate(&cond, bg.graph, 1, cudaGraphCondAssignDefault));
+        cudaGraphNodeParams np = {};
+        np.type = cudaGraphNodeTypeConditional;
+        np.conditional.handle = cond;
+        np.conditional.type = cudaGraphCondTypeWhile;
+        np.conditional.size = 1;
+        cudaGraphNode_t wnode;
+        DG_CUDA_TRY(cudaGraphAddNode(&wnode, bg.graph, nullptr, nullptr, 0, &np));
+        cudaGraph_t body = np.conditional.phGraph_out[0];
+        cudaStream_t cap;
+        DG_CUDA_TRY(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+        if (cudaStreamBeginCaptureToGraph(cap, body, nullptr, nullptr, 0,
+                                          cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaStreamDestroy(cap);
+            cudaGraphDestroy(bg.graph);
+            return DG_ERR_CUDA;
+        }
+        StepSource src{};
+        src.ctl = ctl;
+        AcceptArgs acc{};
+        acc.B = p->B;
+        acc.L = p->L;
+        acc.V = p->V;
+        acc.bound = p->entropy_bound;
+        acc.threshold = p->stop_threshold;
+        acc.seed = p->seed;
+        acc.canvas = io->canvas;
+        acc.prev_argmax = prev;
+        acc.accepted = accepted;
+        acc.n_accepted = n_acc;
+        acc.mean_entropy = io->mean_entropy;
+        acc.stop = stop;
+        acc.ctl = ctl;
+        acc.done = done;
+        acc.steps_taken = io->steps_taken;
+        acc.out_argmax = io->argmax;
+        acc.n_acc_hist = io->n_accepted_hist;
+        acc.cond = cond;
+        int erc = enqueue_step(hidden_steps, bp->hidden_step_stride, x_steps, nullptr, w, p, plan,
+                               ws, src, H, sample, argmax, acc, cap);
+        cudaGraph_t captured = nullptr;
+        cudaError_t ce = cudaStreamEndCapture(cap, &captured);
+        cudaStreamDestroy(cap);
+        if (erc != DG_OK || ce != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphDestroy(bg.graph);
+            return erc != DG_OK ? erc : DG_ERR_CUDA;
+        }
+        if (cudaGraphInstantiate(&bg.exec, bg.graph, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphDestroy(bg.graph);
+            return DG_ERR_CUDA;
+        }
+        std::lock_guard<std::mutex> lk(g_mu);
+        bgp = &(g_block_graphs[key] = bg);
+    }
+    loop_init_kernel<<<std::max(1, (M + 255) / 256), 256, 0, st>>>(
+        ctl, bp->max_steps, bp->t_start, bp->t_end, p->B, done, io->steps_taken, io->canvas, prev,
+        M, static_cast<uint32_t>(p->V), static_cast<uint32_t>(p->seed),
+        static_cast<uint32_t>(p->seed >> 32));
+    DG_CUDA_TRY(cudaGetLastError());
+    DG_CUDA_TRY(cudaGraphLaunch(bgp->exec, st));
+    return DG_OK;
+}
+
+// ---------------------------------------------------------------- check entries
+int dg_gumbel_fill(uint64_t seed, uint32_t row, uint32_t step, uint32_t v0, int n, float *out,
+                   void *stream)
+{
+    if (n < 0 || (n > 0 && out == nullptr)) return DG_ERR_INVALID_ARG;
+    if (n == 0) return DG_OK;
+    gumbel_fill_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(
+        static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), row, step, v0, n, out);
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+int dg_logf_eval(const float *x, float *y, int n, void *stream)
+{
+    if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return DG_ERR_INVALID_ARG;
+    if (n == 0) return DG_OK;
+    logf_eval_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(x, y, n);
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// dg_kernels.h -- argument blocks and kernel declarations shared by the
+// kernel files and the host-side entry points (dg_api.cu).
+#pragma once
+
+#include "dg_sampler.cuh"
+
+namespace dg {
+
+constexpr int kRowsPerBlock = 256;   // LM-head row block (two 128-row UMMAs)
+constexpr int kMaxCanvas = 1024;     // largest canvas the acceptance kernel sorts
+
+struct FoldArgs {
+    int M, V, BN, ntn, total, n_slots;
+    Partials part;
+    StepSource src;
+    uint64_t seed;
+    int *counters;
+    int ncounters;
+};
+
+struct CombineArgs {
+    Partials part;
+    int n_slots, ntn, total, M;
+    float *H;
+    int32_t *sample;
+    int32_t *argmax;
+    int *counters;      // [B] last-CTA counters, zeroed by the producer kernel
+};
+
+struct AcceptArgs {
+    int B, L, V;
+    float bound;        // entropy bound b
+    float threshold;    // stop threshold
+    uint64_t seed;
+    int step;           // single-step mode only
+    int32_t *canvas;
+    int32_t *prev_argmax;
+    uint8_t *accepted;
+    int32_t *n_accepted;
+    float *mean_entropy;
+    int32_t *stop;
+    // block loop only (ctl == nullptr otherwise)
+    LoopCtl *ctl;
+    int32_t *done;
+    int32_t *steps_taken;
+    int32_t *out_argmax;
+    int32_t *n_acc_hist;
+    unsigned long long cond;   // cudaGraphConditionalHandle
+};
+
+struct LmHeadArgs {
+    int M, d, V;
+    int BN;             // vocabulary columns per tile (multiple of 16, <= 128)
+    int ntn;            // vocabulary tiles per row block
+    int total;          // tiles = row blocks * ntn
+    int kblocks;        // d / 64
+    int nbox_b;         // 64-column TMA boxes per W stage
+    int x_3d;           // hidden states carry a step coordinate
+    Partials part;
+    StepSource src;
+    uint64_t seed;
+    WsHeader *ws;
+    int *counters;
+    int ncounters;
+};
+
+// LM-head kernel geometry
+constexpr int kLmStages = 4;
+constexpr int kLmBK = 64;
+constexpr int kLmABytes = kRowsPerBlock * kLmBK * 2;     // 32 KB
+constexpr int kLmBBoxBytes = 64 * kLmBK * 2;             // 8 KB
+constexpr int kLmBBytes = 2 * kLmBBoxBytes;              // 16 KB
+constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
+constexpr int kLmThreads = 384;
+constexpr int kLmSmemBytes = kLmStages * kLmStageBytes + 1024 + 256;
+
+__global__ void lm_head_kernel(const __grid_constant__ CUtensorMap map_x,
+                               const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+__global__ void logits_fold_kernel(const float *__restrict__ logits, FoldArgs a);
+__global__ void combine_accept_kernel(CombineArgs c, AcceptArgs a);
+__global__ void accept_only_kernel(const float *__restrict__ H, const int32_t *__restrict__ sample,
+                                   const int32_t *__restrict__ argmax, AcceptArgs a);
+__global__ void loop_init_kernel(LoopCtl *ctl, int max_steps, double t0, double t1, int B,
+                                 int32_t *done, int32_t *steps_taken, int32_t *canvas,
+                                 int32_t *prev_argmax, int n, uint32_t V, uint32_t k0,
+                                 uint32_t k1);
+__global__ void gumbel_fill_kernel(uint32_t k0, uint32_t k1, uint32_t row, uint32_t step,
+                                   uint32_t v0, int n, float *out);
+__global__ void logf_eval_kernel(const float *x, float *y, int n);
+
+// ---------------------------------------------------------------- attention
+struct AttnArgs {
+    int B, L, P, Hq, Hkv, D;
+    int G;              // Hq / Hkv
+    int rows;           // folded query rows per (b, g): L * G
+    int mtiles;         // ceil(rows / 128)
+    int nsplit;         // key splits
+    int nkt_p, nkt_c;   // key tiles in the prefix / canvas
+    int tiles_per_split;
+    float scale_log2;   // scale * log2(e)
+    uint16_t *out;      // [B, L, Hq, D] (nsplit == 1)
+    float *part_o;      // [nsplit][B*L*Hq][D] unnormalised (nsplit > 1)
+    float *part_ml;     // [nsplit][B*L*Hq][2] (row max in base 2, row sum)
+    WsHeader *ws;
+};
+
+constexpr int kAttnThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+
+__global__ void attn_kernel_d128(const __grid_constant__ CUtensorMap map_q,
+                                 const __grid_constant__ CUtensorMap map_kp,
+                                 const __grid_constant__ CUtensorMap map_vp,
+                                 const __grid_constant__ CUtensorMap map_kc,
+                                 const __grid_constant__ CUtensorMap map_vc, AttnArgs a);
+__global__ void attn_kernel_d256(const __grid_constant__ CUtensorMap map_q,
+                                 const __grid_constant__ CUtensorMap map_kp,
+                                 const __grid_constant__ CUtensorMap map_vp,
+                                 const __grid_constant__ CUtensorMap map_kc,
+                                 const __grid_constant__ CUtensorMap map_vc, AttnArgs a);
+__global__ void attn_combine_kernel(AttnArgs a);
+
+int attn_smem_bytes(int D);
+
+}  // namespace dg

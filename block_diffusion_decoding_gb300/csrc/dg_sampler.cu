@@ -1,0 +1,326 @@
+// dg_sampler.cu -- the sampler tail of a denoising step:
+//   * combine: merge per-slot partial states into per-position entropy,
+//     Gumbel-max sample and argmax;
+//   * accept: per canvas, sort positions by entropy, commit the largest
+//     prefix allowed by the entropy bound, renoise the rest, run the stop
+//     test (fused behind the combine: the last combine CTA of a canvas runs
+//     it, found with an atomic counter, no waiting);
+//   * the logits-from-memory fold, the block-loop init and the small kernels
+//     used to check Philox / log / Gumbel in isolation.
+//
+// "DiffusionGemma Lab", section 2: item 1 (uniform init), item 2 (sort by
+// entropy ascending, commit the largest prefix with cumsum(H) - max(H) <=
+// 0.1, at least one), item 3 (stop when the argmax canvas is unchanged and
+// mean entropy < 0.005), item 5 (commit the sample, output the argmax).
+// "Parallel Denoising From an Autoregressive Checkpoint", section "Finding",
+// bullet "Entropy-bounded acceptance": the remainder is renoised uniformly.
+#include "dg_kernels.h"
+
+namespace dg {
+
+// ---------------------------------------------------------------- fold of fp32 logits
+// One thread per row of a 256-row block; CTA c folds the tiles of slot c.
+__global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restrict__ logits,
+                                                          FoldArgs a)
+{
+    const int c = blockIdx.x;
+    if (c == 0) {
+        for (int i = threadIdx.x; i < a.ncounters; i += blockDim.x) a.counters[i] = 0;
+    }
+    const FoldConsts fc = fold_consts(a.src, a.seed);
+    const int t0 = tile_begin(c, a.total, a.n_slots), t1 = tile_begin(c + 1, a.total, a.n_slots);
+    RowState st;
+    row_state_init(st);
+    int cur_m = -1;
+    for (int t = t0; t < t1; ++t) {
+        const int m = t / a.ntn, n = t % a.ntn;
+        const int row = m * kRowsPerBlock + threadIdx.x;
+        if (m != cur_m) {
+            if (cur_m >= 0) {
+                const int prow = cur_m * kRowsPerBlock + threadIdx.x;
+                if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
+            }
+            row_state_init(st);
+            cur_m = m;
+        }
+        if (row >= a.M) continue;
+        const float *src = logits + static_cast<size_t>(row) * a.V;
+        for (int c0 = 0; c0 < a.BN; c0 += 16) {
+            const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
+            if (v0 >= static_cast<uint32_t>(a.V)) break;
+            float lg[16];
+            if (v0 + 16u <= static_cast<uint32_t>(a.V)) {
+                const float4 *p4 = reinterpret_cast<const float4 *>(src + v0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 f = __ldg(p4 + q);
+                    lg[4 * q] = f.x; lg[4 * q + 1] = f.y; lg[4 * q + 2] = f.z; lg[4 * q + 3] = f.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    lg[j] = (v0 + j < static_cast<uint32_t>(a.V)) ? __ldg(src + v0 + j) : 0.f;
+            }
+            fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc);
+        }
+    }
+    if (cur_m >= 0) {
+        const int prow = cur_m * kRowsPerBlock + threadIdx.x;
+        if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
+    }
+}
+
+// ---------------------------------------------------------------- accept (one canvas)
+__device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float *__restrict__ H,
+                              const int32_t *__restrict__ sample,
+                              const int32_t *__restrict__ argmax)
+{
+    __shared__ uint64_t keys[kMaxCanvas];
+    __shared__ double scan[2][kMaxCanvas];
+    __shared__ int s_kstar;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int L = a.L;
+    int Lp = 1;
+    while (Lp < L) Lp <<= 1;
+    const size_t base = static_cast<size_t>(b) * L;
+
+    // keys (H, position): H >= 0, so its bit pattern orders like the value
+    for (int i = tid; i < Lp; i += nt) {
+        if (i < L) {
+            const float h = __ldcg(H + base + i);
+            keys[i] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(i);
+        } else {
+            keys[i] = ~0ull;
+        }
+    }
+    if (tid == 0) s_kstar = 1;
+    __syncthreads();
+    // bitonic sort, ascending
+    for (int k = 2; k <= Lp; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < Lp; i += nt) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const uint64_t x = keys[i], y = keys[ixj];
+                    const bool up = (i & k) == 0;
+                    if (up ? (x > y) : (x < y)) { keys[i] = y; keys[ixj] = x; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // exclusive prefix sums of the sorted entropies, fp64, fixed tree order
+    for (int j = tid; j < Lp; j += nt) {
+        double v = 0.0;
+        if (j >= 1 && j - 1 < L)
+            v = static_cast<double>(__uint_as_float(static_cast<uint32_t>(keys[j - 1] >> 32)));
+        scan[0][j] = v;
+    }
+    __syncthreads();
+    int src = 0;
+    for (int off = 1; off < Lp; off <<= 1) {
+        for (int j = tid; j < Lp; j += nt)
+            scan[src ^ 1][j] = (j >= off) ? scan[src][j] + scan[src][j - off] : scan[src][j];
+        src ^= 1;
+        __syncthreads();
+    }
+    // k* = max { k in [1, L] : sum of the first k-1 sorted entropies <= b }
+    int local = 1;
+    for (int j = tid; j < L; j += nt)
+        if (scan[src][j] <= static_cast<double>(a.bound)) local = max(local, j + 1);
+    atomicMax(&s_kstar, local);
+    __syncthreads();
+    const int kstar = s_kstar;
+    const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
+    for (int j = tid; j < L; j += nt) {
+        const int pos = static_cast<int>(keys[j] & 0xFFFFFFFFu);
+        const size_t r = base + pos;
+        if (j < kstar) {
+            a.canvas[r] = __ldcg(sample + r);
+            a.accepted[r] = 1;
+        } else {
+            const uint4 x = philox4x32_10(make_uint4(0u, static_cast<uint32_t>(r),
+                                                     static_cast<uint32_t>(step), kStreamRenoise),
+                                          k0, k1);
+            a.canvas[r] = static_cast<int32_t>(token_from_word(x.x, static_cast<uint32_t>(a.V)));
+            a.accepted[r] = 0;
+        }
+    }
+    // stop test: unchanged argmax and mean entropy below the threshold
+    int same = 1;
+    for (int i = tid; i < L; i += nt) same &= (__ldcg(argmax + base + i) == a.prev_argmax[base + i]);
+    const int all_same = __syncthreads_and(same);
+    for (int i = tid; i < L; i += nt) a.prev_argmax[base + i] = __ldcg(argmax + base + i);
+    if (tid == 0) {
+        const double lastH =
+            static_cast<double>(__uint_as_float(static_cast<uint32_t>(keys[L - 1] >> 32)));
+        const double total = scan[src][L - 1] + lastH;
+        const double mean = total / static_cast<double>(L);
+        const int stop = (step >= 1 && all_same && mean < static_cast<double>(a.threshold)) ? 1 : 0;
+        a.n_accepted[b] = kstar;
+        a.mean_entropy[b] = static_cast<float>(mean);
+        a.stop[b] = stop;
+        if (a.ctl != nullptr) {   // block loop bookkeeping
+            if (a.n_acc_hist != nullptr) a.n_acc_hist[static_cast<size_t>(step) * a.B + b] = kstar;
+            a.steps_taken[b] = step + 1;
+            if (stop || step + 1 >= a.ctl->max_steps) a.done[b] = 1;
+        }
+    }
+    if (a.ctl != nullptr) {
+        // freeze the block output: the argmax canvas of the latest live step
+        for (int i = tid; i < L; i += nt) a.out_argmax[base + i] = __ldcg(argmax + base + i);
+    }
+}
+
+// Block loop: the last canvas to finish its acceptance advances the loop.
+__device__ void loop_advance(const AcceptArgs &a)
+{
+    __threadfence();
+    LoopCtl *ctl = a.ctl;
+    const int done_now = atomicAdd(&ctl->canvases_finished, 1) + 1;
+    if (done_now < ctl->n_live) return;
+    __threadfence();
+    int live = 0;
+    for (int b = 0; b < a.B; ++b) live += (__ldcg(a.done + b) == 0);
+    const int next = ctl->step + 1;
+    ctl->canvases_finished = 0;
+    ctl->n_live = live;
+    if (live == 0 || next >= ctl->max_steps) {
+        cudaGraphSetConditional(a.cond, 0u);
+    } else {
+        ctl->step = next;
+    }
+    __threadfence();
+}
+
+// ---------------------------------------------------------------- combine + accept
+// grid = (ceil(L / 8), B), 256 threads: warp w of CTA (x, b) merges the
+// partial states of canvas row b*L + 8x + w; the last CTA of canvas b runs
+// the acceptance for it.
+__global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, AcceptArgs a)
+{
+    const int b = blockIdx.y;
+    if (a.ctl != nullptr && __ldcg(a.done + b) != 0) return;   // canvas already stopped
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * 8 + warp;
+    if (i < a.L) {
+        const int r = b * a.L + i;
+        const int m = r / kRowsPerBlock;
+        const int lo = m * c.ntn, hi = lo + c.ntn;
+        RowState st;
+        row_state_init(st);
+        for (int s = lane; s < c.n_slots; s += 32) {
+            const int t0 = tile_begin(s, c.total, c.n_slots);
+            const int t1 = tile_begin(s + 1, c.total, c.n_slots);
+            if (t0 < hi && t1 > lo && t1 > t0) {
+                RowState p;
+                partial_load(c.part, static_cast<size_t>(s) * c.M + r, p);
+                row_state_merge(st, p);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            RowState o;
+            o.m = __shfl_xor_sync(0xFFFFFFFFu, st.m, off);
+            o.S = __shfl_xor_sync(0xFFFFFFFFu, st.S, off);
+            o.A = __shfl_xor_sync(0xFFFFFFFFu, st.A, off);
+            o.gbest = __shfl_xor_sync(0xFFFFFFFFu, st.gbest, off);
+            o.gidx = __shfl_xor_sync(0xFFFFFFFFu, st.gidx, off);
+            o.amax = __shfl_xor_sync(0xFFFFFFFFu, st.amax, off);
+            o.aidx = __shfl_xor_sync(0xFFFFFFFFu, st.aidx, off);
+            row_state_merge(st, o);
+        }
+        if (lane == 0) {
+            float h = 0.6931471805599453f * (log2f(st.S) - st.A / st.S);
+            h = fmaxf(h, 0.f);
+            c.H[r] = h;
+            c.sample[r] = st.gidx;
+            c.argmax[r] = st.aidx;
+        }
+    }
+    // last CTA of this canvas?
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&c.counters[b], 1);
+        s_last = (prev == static_cast<int>(gridDim.x) - 1);
+        if (s_last) c.counters[b] = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int step =
+        (a.ctl != nullptr) ? *reinterpret_cast<volatile int32_t *>(&a.ctl->step) : a.step;
+    accept_canvas(a, b, step, c.H, c.sample, c.argmax);
+    if (a.ctl != nullptr) {
+        __syncthreads();
+        if (threadIdx.x == 0) loop_advance(a);
+    }
+}
+
+// Acceptance alone on given entropy / sample / argmax (one CTA per canvas).
+__global__ void __launch_bounds__(256) accept_only_kernel(const float *__restrict__ H,
+                                                          const int32_t *__restrict__ sample,
+                                                          const int32_t *__restrict__ argmax,
+                                                          AcceptArgs a)
+{
+    accept_canvas(a, blockIdx.x, a.step, H, sample, argmax);
+}
+
+// ---------------------------------------------------------------- block-loop init
+__global__ void loop_init_kernel(LoopCtl *ctl, int max_steps, double t0, double t1, int B,
+                                 int32_t *done, int32_t *steps_taken, int32_t *canvas,
+                                 int32_t *prev_argmax, int n, uint32_t V, uint32_t k0,
+                                 uint32_t k1)
+{
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    const int stride = gridDim.x * blockDim.x;
+    if (tid == 0) {
+        ctl->step = 0;
+        ctl->max_steps = max_steps;
+        ctl->canvases_finished = 0;
+        ctl->n_live = B;
+    }
+    for (int k = tid; k < max_steps; k += stride) {
+        // T_k = t0 + (t1 - t0) k / (N - 1), in fp64
+        const double T = (max_steps <= 1) ? t0
+                                          : t0 + (t1 - t0) * static_cast<double>(k) /
+                                                     static_cast<double>(max_steps - 1);
+        const float invT = static_cast<float>(1.0 / T);
+        ctl->invT[k] = invT;
+        ctl->c2[k] = __fmul_rn(invT, __uint_as_float(0x3FB8AA3Bu));   // * log2(e)
+    }
+    for (int b = tid; b < B; b += stride) {
+        done[b] = 0;
+        steps_taken[b] = 0;
+    }
+    for (int r = tid; r < n; r += stride) {
+        // "DiffusionGemma Lab" section 2 item 1: uniform random init, not [MASK]
+        const uint4 x = philox4x32_10(make_uint4(0u, static_cast<uint32_t>(r), 0u, kStreamInit),
+                                      k0, k1);
+        canvas[r] = static_cast<int32_t>(token_from_word(x.x, V));
+        prev_argmax[r] = -1;
+    }
+}
+
+// ---------------------------------------------------------------- check kernels
+__global__ void gumbel_fill_kernel(uint32_t k0, uint32_t k1, uint32_t row, uint32_t step,
+                                   uint32_t v0, int n, float *out)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < n) {
+        const uint32_t v = v0 + static_cast<uint32_t>(t);
+        const uint4 r = philox4x32_10(make_uint4(v >> 2, row, step, kStreamGumbel), k0, k1);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        out[t] = gumbel_from_bits(w[v & 3u]);
+    }
+}
+
+__global__ void logf_eval_kernel(const float *x, float *y, int n)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < n) y[t] = sampler_logf(x[t]);
+}
+
+}  // namespace dg

@@ -1,0 +1,211 @@
+/*
+ * dg.h -- C ABI of the GB300 (sm_103a) block-diffusion denoising-step library
+ * (libdg.so).  One denoising step of DiffusionGemma-style block diffusion over
+ * a 256-token canvas: bidirectional canvas attention, the LM head with a fused
+ * entropy / Gumbel-max / argmax epilogue, entropy-bounded acceptance with
+ * uniform renoise, and the adaptive stop test; plus the block loop around it.
+ *
+ * Sources, by page title and section:
+ *   "DiffusionGemma Lab", section 2 "The generation algorithm, as written in
+ *     the code", items 1-7 (uniform canvas init, the acceptance rule
+ *     cumsum(H) - max(H) <= 0.1, the stop rule, the 0.8 -> 0.4 temperature
+ *     schedule, the argmax output, shared encoder/decoder weights, the full
+ *     256-token canvas).
+ *   "DiffusionGemma: Parallel Denoising From an Autoregressive Checkpoint",
+ *     section "Finding" (causal encoder KV cache + bidirectional canvas
+ *     decoder; the three sampler bullets; the H100 cost breakdown that names
+ *     full-vocabulary softmax and canvas attention as per-step costs).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is caller-owned memory.  Tensor arguments are
+ *     DEVICE pointers unless the name says host.  bf16 tensors are passed as
+ *     uint16_t bit patterns.  All tensors are dense row-major (last dimension
+ *     contiguous) and 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy stream).
+ *     Calls are asynchronous on that stream.  No call allocates device memory
+ *     in the hot path: scratch comes from the caller's workspace, sized by the
+ *     matching *_workspace() query (which touches no GPU).
+ *   - Return value: a dg_status.  It reports host-side validation (checked
+ *     before anything is launched) and launch errors.  Kernels that detect a
+ *     problem on the device (a bounded wait that ran out, a bounds check)
+ *     record it in the status word at the start of the workspace and return
+ *     early; read it with dg_read_device_status().
+ *   - Supported shapes are listed per call; anything else returns
+ *     DG_ERR_UNSUPPORTED without launching.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dg_status {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad value   */
+    DG_ERR_UNSUPPORTED = 2,   /* shape outside the supported set              */
+    DG_ERR_ALIGNMENT = 3,     /* a tensor pointer is not 16-byte aligned      */
+    DG_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required   */
+    DG_ERR_CUDA = 5,          /* a CUDA runtime call failed                   */
+    DG_ERR_TIMEOUT = 6,       /* device: a bounded wait ran out               */
+    DG_ERR_DEVICE = 7         /* device: a bounds/consistency check failed    */
+} dg_status;
+
+/* Static, never-NULL description of a status code. */
+const char *dg_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int dg_version(void);
+
+/* Device status word kept in the first bytes of every workspace: 0 when no
+ * kernel has reported a problem, else a DG_ERR_* code.  Reads it with a
+ * synchronous copy on `stream` into *status_out (host).  Clears it when
+ * `clear` is non-zero. */
+int dg_read_device_status(const void *workspace, int *status_out, int clear, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Canvas attention.                                                         */
+/* "DiffusionGemma Lab" section 2 item 6 and "Parallel Denoising ..." section */
+/* "Finding": the decoder attends bidirectionally across the canvas (no mask) */
+/* and to the causal encoder's KV cache.  For batch b, canvas position i and  */
+/* query head h, with kv head g = h / (Hq / Hkv):                             */
+/*   out[b,i,h,:] = softmax_j(scale * q[b,i,h,:] . K_j) V_j,                  */
+/* keys j running over the P cached rows k_prefix[b,:,g,:] followed by the L  */
+/* canvas rows k_canvas[b,:,g,:] (same for V).                                 */
+/* Layouts: q, out [B, L, Hq, D]; k_prefix, v_prefix [B, P, Hkv, D];          */
+/*          k_canvas, v_canvas [B, L, Hkv, D]; all bf16.                       */
+/* bf16 inputs, fp32 accumulation and softmax, bf16 output.                   */
+/* Supported: D in {128, 256}; Hq % Hkv == 0 and Hq/Hkv a power of two <= 16; */
+/* 1 <= L; 0 <= P; B >= 1.  P == 0 is allowed (k_prefix/v_prefix may be NULL).*/
+/* ------------------------------------------------------------------------ */
+size_t dg_canvas_attn_workspace(int B, int L, int P, int Hq, int Hkv, int D);
+int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                   const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *out,
+                   int B, int L, int P, int Hq, int Hkv, int D, float scale,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* One denoising step after the decoder body: LM head -> per-position        */
+/* entropy, Gumbel-max sample and argmax -> entropy-bounded acceptance and    */
+/* uniform renoise -> adaptive stop test.                                     */
+/*                                                                            */
+/* "DiffusionGemma Lab" section 2 items 2, 3 and 5; "Parallel Denoising ..."  */
+/* section "Finding", bullets "Entropy-bounded acceptance" and "Adaptive      */
+/* stopping".  Per canvas position (row r = b*L + i):                         */
+/*   logits = hidden[r,:] . w          (bf16 in, fp32 accumulate; never       */
+/*                                      written to memory)                    */
+/*   entropy[r] = H(softmax(logits / T)) in nats                              */
+/*   argmax[r]  = argmax logits (ties -> lowest vocabulary index)             */
+/*   sample[r]  = argmax_v fp32(fmaf(logit_v, fp32(1/T), G_v)), G_v the       */
+/*                standard Gumbel variate -ln(-ln u) of Philox4x32-10 word    */
+/*                (v & 3) of counter (v >> 2, r, step, 0), key = seed         */
+/*   per canvas: sort positions by (entropy, position) ascending; commit the  */
+/*   largest prefix whose entropies, minus its largest one, sum (fp64) to     */
+/*   <= entropy_bound (always >= 1): canvas[r] = sample[r], accepted[r] = 1;  */
+/*   every other position is redrawn: canvas[r] = (x * V) >> 32 with x word 0 */
+/*   of counter (0, r, step, 1).                                              */
+/*   stop[b] = step >= 1 && argmax == prev_argmax over the canvas &&          */
+/*             mean entropy < stop_threshold; then prev_argmax <- argmax.     */
+/* Layouts: hidden [B*L, d] bf16; w [d, V] bf16 (vocabulary contiguous).      */
+/* Supported: d % 64 == 0, 64 <= d <= 16384; V % 8 == 0, 64 <= V < 2^31;      */
+/* 1 <= L <= 1024; B >= 1.                                                    */
+/* ------------------------------------------------------------------------ */
+typedef struct dg_step_params {
+    int B;                  /* canvases in the batch                          */
+    int L;                  /* canvas length (256)                            */
+    int d;                  /* hidden size                                    */
+    int V;                  /* vocabulary size                                */
+    double temperature;     /* T of this step, > 0 (1/T is rounded to fp32)   */
+    float entropy_bound;    /* b (0.1)                                        */
+    float stop_threshold;   /* mean-entropy stop threshold (0.005)            */
+    int step;               /* step index k (Philox counter; k >= 1 arms stop)*/
+    uint64_t seed;          /* Philox key                                     */
+} dg_step_params;
+
+typedef struct dg_step_io {
+    int32_t *canvas;        /* [B*L] in/out: current canvas tokens            */
+    int32_t *prev_argmax;   /* [B*L] in/out: argmax of the previous step      */
+    int32_t *argmax;        /* [B*L] out                                      */
+    int32_t *sample;        /* [B*L] out                                      */
+    float *entropy;         /* [B*L] out, nats                                */
+    uint8_t *accepted;      /* [B*L] out, 1 = committed this step             */
+    int32_t *n_accepted;    /* [B]   out                                      */
+    float *mean_entropy;    /* [B]   out                                      */
+    int32_t *stop;          /* [B]   out, 1 = stop                            */
+} dg_step_io;
+
+size_t dg_denoise_step_workspace(const dg_step_params *p);
+int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_params *p,
+                    const dg_step_io *io, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* The denoising loop of one block (batch of B independent canvases).        */
+/* "DiffusionGemma Lab" section 2 items 1-5; "Parallel Denoising ..."         */
+/* section "Finding" (temperature annealing, adaptive stopping, N = 48).      */
+/* Initialises canvas[r] = (x * V) >> 32, x word 0 of Philox counter          */
+/* (0, r, 0, 2); then for k = 0 .. max_steps-1 runs dg_denoise_step with      */
+/* T_k = t_start + (t_end - t_start) * k / (max_steps - 1) (computed in fp64) */
+/* on hidden_steps + k * hidden_step_stride, until every canvas has stopped.  */
+/* A canvas that stops keeps its canvas and argmax from that step.  The loop  */
+/* runs on the device as one CUDA graph with a conditional while node; the    */
+/* host waits only at the end.                                                */
+/* hidden_steps: device bf16, hidden_step_stride elements apart per step (0 = */
+/* the same hidden states every step); the decoder body that would produce    */
+/* them is outside this library.                                              */
+/* ------------------------------------------------------------------------ */
+typedef struct dg_block_params {
+    int max_steps;              /* N (48)                                     */
+    double t_start;             /* 0.8                                        */
+    double t_end;               /* 0.4                                        */
+    int64_t hidden_step_stride; /* elements between consecutive steps         */
+} dg_block_params;
+
+typedef struct dg_block_io {
+    int32_t *canvas;            /* [B*L] out: final canvas tokens             */
+    int32_t *argmax;            /* [B*L] out: the block output                */
+    int32_t *steps_taken;       /* [B]   out                                  */
+    float *mean_entropy;        /* [B]   out: at the last step taken          */
+    int32_t *n_accepted_hist;   /* [max_steps*B] out, may be NULL             */
+} dg_block_io;
+
+size_t dg_generate_block_workspace(const dg_step_params *p, const dg_block_params *bp);
+int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w,
+                      const dg_step_params *p, const dg_block_params *bp,
+                      const dg_block_io *io, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Entry points that run one stage of the step on given inputs, through the  */
+/* same device code as dg_denoise_step (for checking each stage alone).      */
+/* ------------------------------------------------------------------------ */
+
+/* The step of dg_denoise_step with fp32 logits [B*L, V] read from memory in  */
+/* place of hidden . w.  Same params/io; p->d is ignored. */
+size_t dg_sampler_workspace(const dg_step_params *p);
+int dg_sampler_from_logits(const float *logits, const dg_step_params *p, const dg_step_io *io,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Acceptance, renoise and stop test alone on given entropy/sample/argmax     */
+/* [B*L] (device).  Writes canvas, accepted, n_accepted, stop, mean_entropy   */
+/* and prev_argmax of io; io->entropy/sample/argmax are not used. */
+int dg_accept_renoise(const float *entropy, const int32_t *sample, const int32_t *argmax,
+                      const dg_step_params *p, const dg_step_io *io, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Standard Gumbel variates of vocabulary entries v0 .. v0+n-1 for (row, step) */
+/* as the sampler draws them (device float[n]). */
+int dg_gumbel_fill(uint64_t seed, uint32_t row, uint32_t step, uint32_t v0, int n,
+                   float *out, void *stream);
+
+/* The sampler's fp32 natural logarithm applied to x[0..n) (device arrays).   */
+int dg_logf_eval(const float *x, float *y, int n, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

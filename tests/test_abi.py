@@ -1,0 +1,110 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/dg.h declares, answers workspace queries, and rejects bad arguments
+on the host before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_diffusion_decoding_gb300 as dg
+from block_diffusion_decoding_gb300 import build as dgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dgbuild.build()
+    return dg.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "dg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 14
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(dg.EXPORTED) == declared
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert isinstance(lib.dg_status_string(code), bytes)
+    assert lib.dg_status_string(99) == b"unknown status"
+    assert lib.dg_version() >= 100
+
+
+def test_struct_layouts_match_header(lib):
+    # int B, L, d, V; double T; float b, thr; int step; (pad) uint64 seed
+    assert ctypes.sizeof(dg.StepParams) == 48
+    assert dg.StepParams.seed.offset == 40
+    assert ctypes.sizeof(dg.StepIO) == 9 * 8
+    assert ctypes.sizeof(dg.BlockParams) == 32
+    assert ctypes.sizeof(dg.BlockIO) == 5 * 8
+
+
+def test_workspace_queries(lib):
+    p = dg.step_params(1, 256, 2816, 262144, 0.8)
+    ws = dg.denoise_step_workspace(p)
+    assert ws >= 256 + 7 * 4 * 256 * 152
+    assert dg.generate_block_workspace(p, dg.block_params()) > ws
+    assert dg.sampler_workspace(p) > 0
+    # a long cache needs split-KV scratch
+    assert dg.canvas_attn_workspace(1, 256, 32768, 4, 1, 128) > 1 << 20
+    assert dg.canvas_attn_workspace(1, 16, 0, 4, 1, 128) >= 256
+    # unsupported shapes answer 0
+    assert dg.canvas_attn_workspace(1, 256, 256, 4, 1, 64) == 0
+    assert dg.canvas_attn_workspace(1, 256, 256, 3, 2, 128) == 0
+    assert dg.denoise_step_workspace(dg.step_params(1, 256, 1024, 1001, 0.8)) == 0
+
+
+def _vp(x):
+    return ctypes.c_void_p(x)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    good = 1 << 20   # aligned fake addresses: never dereferenced, validation fails first
+    p = dg.step_params(1, 256, 1024, 16384, 0.8)
+    io = dg.StepIO(*[_vp(good + 64 * i) for i in range(9)])
+    ws_sz = dg.denoise_step_workspace(p)
+
+    def call(h, w, p_, io_, ws, n):
+        return lib.dg_denoise_step(h, w, ctypes.byref(p_), ctypes.byref(io_), ws, n, None)
+
+    assert call(None, _vp(good), p, io, _vp(good), ws_sz) == 1            # null hidden
+    assert call(_vp(good + 2), _vp(good), p, io, _vp(good), ws_sz) == 3   # misaligned
+    assert call(_vp(good), _vp(good), p, io, _vp(good), ws_sz - 1) == 4   # workspace too small
+    assert call(_vp(good), _vp(good), p, io, None, ws_sz) == 4            # no workspace
+    bad = dg.step_params(1, 256, 1000, 16384, 0.8)                         # d % 64 != 0
+    assert call(_vp(good), _vp(good), bad, io, _vp(good), 1 << 30) == 2
+    bad = dg.step_params(1, 256, 1024, 16384, -1.0)                        # T <= 0
+    assert call(_vp(good), _vp(good), bad, io, _vp(good), 1 << 30) == 1
+    bad = dg.step_params(1, 2048, 1024, 16384, 0.8)                        # L > 1024
+    assert call(_vp(good), _vp(good), bad, io, _vp(good), 1 << 30) == 2
+    io_missing = dg.StepIO(*([None] + [_vp(good)] * 8))
+    assert call(_vp(good), _vp(good), p, io_missing, _vp(good), ws_sz) == 1
+
+    def attn(D, Hq, Hkv, q=good, n=1 << 30):
+        return lib.dg_canvas_attn(_vp(q), _vp(good), _vp(good), _vp(good), _vp(good), _vp(good),
+                                  1, 256, 256, Hq, Hkv, D, 0.1, _vp(good), n, None)
+
+    assert attn(64, 4, 1) == 2          # head dim
+    assert attn(128, 6, 4) == 2         # Hq % Hkv
+    assert attn(128, 12, 4) == 2        # G = 3 not a power of two
+    assert attn(128, 4, 1, q=good + 8) == 3
+    assert attn(128, 4, 1, n=0) == 4
+    # block loop
+    bio = dg.BlockIO(*[_vp(good + 64 * i) for i in range(5)])
+    for bp, code in ((dg.block_params(max_steps=0), 2), (dg.block_params(t_start=0.0), 1),
+                     (dg.block_params(hidden_step_stride=-1), 1)):
+        assert lib.dg_generate_block(_vp(good), _vp(good), ctypes.byref(p), ctypes.byref(bp),
+                                     ctypes.byref(bio), _vp(good), 1 << 30, None) == code
+    # check entries
+    assert lib.dg_logf_eval(None, None, -1, None) == 1
+    assert lib.dg_gumbel_fill(0, 0, 0, 0, 0, None, None) == 0

@@ -1,0 +1,367 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bit-exact: the fp32 log, Gumbel noise, samples and argmax on identical fp32
+logits, the acceptance/renoise/stop stage on identical entropies.  Within
+tolerance: entropies (1e-4 absolute), attention outputs (2e-2 of the row's
+largest magnitude).  Tokens from the fused GEMM path are compared where the
+oracle's margins are above 1e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_diffusion_decoding_gb300 as dg
+import dg_synth
+import oracle
+from tests._helpers import (ATTN_TOL, DEV, H_TOL, MARGIN, acceptance_is_decided, np_f, np_i32,
+                            to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _status_ok(ws):
+    assert dg.read_device_status(ws) == 0
+
+
+# ------------------------------------------------------------------ primitives
+def test_logf_bit_exact():
+    rng = np.random.default_rng(0)
+    xs = np.concatenate([
+        rng.uniform(5.9e-8, 1.0, 6000), rng.uniform(1.0, 17.0, 6000),
+        np.exp(rng.uniform(-40, 40, 6000)),
+        np.array([1.0, 2.0, 0.5, 0.70710677, 0.70710683, 1.4142135, 1.4142137, 16.635532,
+                  5.9604645e-08, 0.99999994, 1.0000001]),
+    ]).astype(np.float32)
+    x = torch.from_numpy(xs).to(DEV)
+    y = torch.empty_like(x)
+    dg.logf_eval(x, y)
+    got = y.cpu().numpy()
+    ref = np.array([oracle.logf(float(v)) for v in xs], np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("seed,row,step,v0,n", [(0, 0, 0, 0, 4096),
+                                                (123456789012345, 77, 5, 13, 3001),
+                                                (2**64 - 1, 2**32 - 1, 47, 262144 - 1000, 1000)])
+def test_gumbel_bit_exact(seed, row, step, v0, n):
+    out = torch.empty(n, dtype=torch.float32, device=DEV)
+    dg.gumbel_fill(seed, row, step, v0, n, out)
+    ref = oracle.gumbel_fill(seed, row, step, v0, n)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------ acceptance / renoise / stop
+def _random_entropies(rng, L, kind):
+    if kind == "exp":
+        return rng.exponential(0.03, L)
+    if kind == "mixed":
+        h = rng.exponential(1.0, L) * rng.choice([1e-4, 1e-2, 1.0, 5.0], L)
+        h[rng.integers(0, L, 5)] = 0.0
+        return h
+    if kind == "ties":
+        return rng.choice([0.0, 0.01, 0.02, 0.5], L)
+    if kind == "flat":
+        return np.full(L, math.log(16384.0))
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("B,L,kind", [(1, 256, "exp"), (3, 256, "mixed"), (2, 100, "ties"),
+                                      (1, 1024, "exp"), (1, 1, "mixed"), (2, 256, "flat"),
+                                      (4, 37, "exp")])
+def test_accept_renoise_stop_bit_exact(B, L, kind):
+    rng = np.random.default_rng(L * 7 + B)
+    V, b, seed, step = 16384, 0.1, 99, 3
+    H = np.stack([_random_entropies(rng, L, kind) for _ in range(B)]).astype(np.float32)
+    if kind == "mixed":
+        H[0] = np.float32(1e-4)   # canvas 0: confident, low mean entropy
+    sample = rng.integers(0, V, (B, L)).astype(np.int32)
+    argmax = rng.integers(0, V, (B, L)).astype(np.int32)
+    prev = argmax.copy()
+    if B > 1:
+        prev[1, L // 2] += 1      # canvas 1: argmax changed -> no stop
+    canvas = rng.integers(0, V, (B, L)).astype(np.int32)
+
+    p = dg.step_params(B, L, 64, V, 0.8, b, 0.005, step=step, seed=seed)
+    bufs = dg.StepBuffers(B, L, DEV)
+    bufs.canvas.copy_(torch.from_numpy(canvas.reshape(-1)))
+    bufs.prev_argmax.copy_(torch.from_numpy(prev.reshape(-1)))
+    ws = dg.workspace(4096, DEV)
+    dg.accept_renoise(torch.from_numpy(H.reshape(-1)).to(DEV),
+                      torch.from_numpy(sample.reshape(-1)).to(DEV),
+                      torch.from_numpy(argmax.reshape(-1)).to(DEV), p, bufs, ws)
+    torch.cuda.synchronize()
+    for bb in range(B):
+        r = oracle.accept_renoise(H[bb], sample[bb], canvas[bb], V, b, seed, bb * L, step)
+        s = oracle.stop(argmax[bb], prev[bb], H[bb], step)
+        sl = slice(bb * L, (bb + 1) * L)
+        assert np.array_equal(np_i32(bufs.canvas)[sl], r["canvas"])
+        assert np.array_equal(bufs.accepted.cpu().numpy()[sl], r["accepted"])
+        assert int(bufs.n_accepted[bb]) == r["n_accepted"]
+        assert int(bufs.stop[bb]) == s["stop"]
+        assert abs(float(bufs.mean_entropy[bb]) - s["mean_entropy"]) <= 1e-6 * max(1, s["mean_entropy"])
+        assert np.array_equal(np_i32(bufs.prev_argmax)[sl], argmax[bb])
+    if kind == "mixed" and L > 1:
+        assert int(bufs.stop[0]) == 1 and int(bufs.n_accepted[0]) == L
+    _status_ok(ws)
+
+
+def test_accept_step0_never_stops():
+    L, V = 64, 1024
+    p = dg.step_params(1, L, 64, V, 0.8, 0.1, 0.005, step=0, seed=1)
+    bufs = dg.StepBuffers(1, L, DEV)
+    am = torch.arange(L, dtype=torch.int32, device=DEV)
+    bufs.prev_argmax.copy_(am)
+    ws = dg.workspace(4096, DEV)
+    dg.accept_renoise(torch.zeros(L, device=DEV), am, am, p, bufs, ws)
+    torch.cuda.synchronize()
+    assert int(bufs.stop[0]) == 0 and int(bufs.n_accepted[0]) == L
+
+
+# ------------------------------------------------------------------ sampler on identical fp32 logits
+def _check_step_against_oracle(bufs, ref, B, L, exact_tokens):
+    H = np_f(bufs.entropy)
+    assert np.abs(H - ref["H"]).max() < H_TOL, np.abs(H - ref["H"]).max()
+    am, sm = np_i32(bufs.argmax), np_i32(bufs.sample)
+    if exact_tokens:
+        assert np.array_equal(am, ref["argmax"])
+        assert np.array_equal(sm, ref["sample"])
+    else:
+        ok = ref["argmax_margin"] >= MARGIN
+        assert ok.mean() > 0.9
+        assert np.array_equal(am[ok], ref["argmax"][ok])
+        ok = ref["gumbel_margin"] >= MARGIN
+        assert ok.mean() > 0.9
+        assert np.array_equal(sm[ok], ref["sample"][ok])
+    canvas, acc = np_i32(bufs.canvas), bufs.accepted.cpu().numpy()
+    checked = 0
+    for bb in range(B):
+        sl = slice(bb * L, (bb + 1) * L)
+        if not acceptance_is_decided(ref["H"][sl], int(ref["n_accepted"][bb]),
+                                     float(ref["boundary_gap"][bb])):
+            continue
+        checked += 1
+        assert int(bufs.n_accepted[bb]) == int(ref["n_accepted"][bb])
+        assert np.array_equal(acc[sl], ref["accepted"][sl])
+        # accepted positions hold the sample; every other one the renoise token
+        acc_ref = ref["accepted"][sl] == 1
+        if exact_tokens or bool(np.all(ref["gumbel_margin"][sl][acc_ref] >= MARGIN)):
+            assert np.array_equal(canvas[sl], ref["canvas"][sl])
+        else:
+            assert np.array_equal(canvas[sl][~acc_ref], ref["canvas"][sl][~acc_ref])
+    return checked
+
+
+@pytest.mark.parametrize("B,L,V,scale", [(1, 256, 16384, 1.0), (2, 256, 4096, 4.0),
+                                         (1, 64, 1000, 2.0), (3, 100, 2048, 0.5)])
+def test_sampler_from_logits(B, L, V, scale):
+    rng = np.random.default_rng(V + L)
+    logits = (rng.standard_normal((B * L, V)) * scale
+              * rng.uniform(0.2, 3.0, (B * L, 1))).astype(np.float32)
+    logits[0, 5] = logits[0, 7] = logits[0].max() + 1.0       # tie -> lower index wins
+    T, b, seed, k = 0.8, 0.1, 2024, 1
+    canvas0 = rng.integers(0, V, B * L).astype(np.int32)
+    prev = rng.integers(0, V, B * L).astype(np.int32)
+    p = dg.step_params(B, L, 64, V, T, b, 0.005, step=k, seed=seed)
+    bufs = dg.StepBuffers(B, L, DEV)
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    bufs.prev_argmax.copy_(torch.from_numpy(prev))
+    ws = dg.workspace(dg.sampler_workspace(p), DEV)
+    dg.sampler_from_logits(torch.from_numpy(logits).to(DEV), p, bufs, ws)
+    torch.cuda.synchronize()
+    _status_ok(ws)
+    s = oracle.sampler(logits.astype(np.float64), T, seed, np.arange(B * L), k)
+    ref = dict(s)
+    ref["canvas"] = np.zeros(B * L, np.int32)
+    ref["accepted"] = np.zeros(B * L, np.uint8)
+    ref["n_accepted"] = np.zeros(B, np.int32)
+    ref["boundary_gap"] = np.zeros(B)
+    Hf = s["H"].astype(np.float32)
+    for bb in range(B):
+        sl = slice(bb * L, (bb + 1) * L)
+        a = oracle.accept_renoise(Hf[sl], s["sample"][sl], canvas0[sl], V, b, seed, bb * L, k)
+        ref["canvas"][sl], ref["accepted"][sl] = a["canvas"], a["accepted"]
+        ref["n_accepted"][bb], ref["boundary_gap"][bb] = a["n_accepted"], a["boundary_gap"]
+    assert int(np_i32(bufs.argmax)[0]) == 5
+    _check_step_against_oracle(bufs, ref, B, L, exact_tokens=True)
+
+
+# ------------------------------------------------------------------ fused LM head (tcgen05 GEMM + epilogue)
+@pytest.mark.parametrize("B,L,d,V,w_std,k", [(1, 256, 1024, 16384, 0.05, 0),   # the small step
+                                             (2, 256, 256, 4096, 0.08, 2),     # two row blocks
+                                             (1, 100, 128, 1000, 0.2, 1),      # ragged rows / vocab
+                                             (3, 64, 512, 8192, 0.05, 5)])
+def test_denoise_step_matches_oracle(B, L, d, V, w_std, k):
+    cfg = dg_synth.StepConfig("t", B=B, L=L, d=d, V=V, w_std=w_std, seed=11)
+    xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
+    T, b, seed = oracle.temperature(k, 48), 0.1, 5
+    rng = np.random.default_rng(1)
+    canvas0 = rng.integers(0, V, B * L).astype(np.int32)
+    prev = rng.integers(0, V, B * L).astype(np.int32)
+    p = dg.step_params(B, L, d, V, T, b, 0.005, step=k, seed=seed)
+    bufs = dg.StepBuffers(B, L, DEV)
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    bufs.prev_argmax.copy_(torch.from_numpy(prev))
+    ws = dg.workspace(dg.denoise_step_workspace(p), DEV)
+    x, w = to_dev(xb), to_dev(wb)
+    dg.denoise_step(x, w, p, bufs, ws)
+    torch.cuda.synchronize()
+    _status_ok(ws)
+    ref = oracle.step(xb, wb, canvas0, prev, B, L, T, b, seed, k)
+    _check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+    # repeat: same result (deterministic)
+    H1 = np_f(bufs.entropy).copy()
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    dg.denoise_step(x, w, p, bufs, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(np_f(bufs.entropy), H1)
+
+
+def test_denoise_step_uniform_and_one_hot_rows():
+    """Zero hidden rows give uniform logits (H = ln V, argmax 0); a row aligned
+    with one vocabulary column at large scale gives H ~ 0 at that column."""
+    L, d, V = 256, 128, 4096
+    x = np.zeros((L, d), np.float32)
+    w = np.zeros((d, V), np.float32)
+    for i in range(0, L, 2):          # odd rows stay zero -> uniform
+        x[i, i // 2] = 1.0
+        w[i // 2, (37 * i) % V] = 200.0
+    xb, wb = dg_synth.f32_to_bf16_bits(x), dg_synth.f32_to_bf16_bits(w)
+    p = dg.step_params(1, L, d, V, 0.8, 0.1, 0.005, step=0, seed=3)
+    bufs = dg.StepBuffers(1, L, DEV)
+    ws = dg.workspace(dg.denoise_step_workspace(p), DEV)
+    dg.denoise_step(to_dev(xb), to_dev(wb), p, bufs, ws)
+    torch.cuda.synchronize()
+    H, am = np_f(bufs.entropy), np_i32(bufs.argmax)
+    assert np.abs(H[1::2] - math.log(V)).max() < H_TOL
+    assert (am[1::2] == 0).all()
+    assert np.abs(H[0::2]).max() < H_TOL
+    assert np.array_equal(am[0::2], np.array([(37 * i) % V for i in range(0, L, 2)]))
+    assert np.array_equal(np_i32(bufs.sample)[0::2], am[0::2])
+
+
+# ------------------------------------------------------------------ canvas attention
+def _attn_case(B, L, P, Hq, Hkv, D, seed=0, row_stride=1):
+    cfg = dg_synth.StepConfig("a", B=B, L=L, P=P, Hq=Hq, Hkv=Hkv, D=D, seed=seed)
+    ai = dg_synth.attention_inputs(cfg)
+    t = {k: to_dev(v) for k, v in ai.items()}
+    out = torch.full_like(t["q"], float("nan"))
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    ws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    dg.canvas_attn(t["q"], t["kp"] if P else None, t["vp"] if P else None, t["kc"], t["vc"],
+                   out, scale, ws)
+    torch.cuda.synchronize()
+    _status_ok(ws)
+    rows = np.arange(0, B * L * Hq, row_stride)
+    ref = oracle.attention_rows(ai["q"], ai["kp"], ai["vp"], ai["kc"], ai["vc"], B, L, P, Hq, Hkv,
+                                D, scale, rows)
+    got = out.float().reshape(-1, D).cpu().numpy()[rows]
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max(axis=1) / np.abs(ref).max(axis=1)
+    assert err.max() < ATTN_TOL, (err.max(), int(rows[err.argmax()]))
+    return err.max()
+
+
+@pytest.mark.parametrize("B,L,P,Hq,Hkv,D,stride", [
+    (1, 256, 256, 4, 1, 128, 1),      # the small step's attention
+    (2, 100, 37, 4, 2, 128, 1),       # ragged canvas and prefix
+    (1, 64, 0, 2, 1, 128, 1),         # no cached prefix
+    (1, 48, 300, 16, 8, 256, 1),      # head dim 256, G = 2, ragged
+    (1, 256, 4096, 4, 1, 128, 5),     # many key tiles -> split-KV + combine
+    (2, 256, 1000, 16, 8, 256, 9),    # head dim 256 with splits
+    (1, 16, 5, 8, 1, 128, 1),         # G = 8, tiny
+])
+def test_canvas_attn_matches_oracle(B, L, P, Hq, Hkv, D, stride):
+    _attn_case(B, L, P, Hq, Hkv, D, seed=B + L + P, row_stride=stride)
+
+
+def test_canvas_attn_constant_values_and_zero_keys():
+    """Constant value rows -> every output equals that row; zero keys -> mean of values."""
+    B, L, P, Hq, Hkv, D = 1, 128, 200, 4, 1, 128
+    cfg = dg_synth.StepConfig("a", B=B, L=L, P=P, Hq=Hq, Hkv=Hkv, D=D, seed=4)
+    ai = dg_synth.attention_inputs(cfg)
+    row = dg_synth.f32_to_bf16_bits(np.linspace(-2, 2, D).astype(np.float32))
+    vp = np.broadcast_to(row, ai["vp"].shape).copy()
+    vc = np.broadcast_to(row, ai["vc"].shape).copy()
+    out = torch.empty(B, L, Hq, D, dtype=torch.bfloat16, device=DEV)
+    ws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    dg.canvas_attn(to_dev(ai["q"]), to_dev(ai["kp"]), to_dev(vp), to_dev(ai["kc"]), to_dev(vc),
+                   out, 0.1, ws)
+    torch.cuda.synchronize()
+    expect = torch.from_numpy(dg_synth.bf16_bits_to_f32(row))
+    assert (out.float().cpu().reshape(-1, D) - expect).abs().max() < 2e-2
+    zk = np.zeros_like(ai["kp"]), np.zeros_like(ai["kc"])
+    dg.canvas_attn(to_dev(ai["q"]), to_dev(zk[0]), to_dev(ai["vp"]), to_dev(zk[1]), to_dev(ai["vc"]),
+                   out, 0.1, ws)
+    torch.cuda.synchronize()
+    allv = np.concatenate([dg_synth.bf16_bits_to_f32(ai["vp"])[0, :, 0],
+                           dg_synth.bf16_bits_to_f32(ai["vc"])[0, :, 0]]).astype(np.float64).mean(0)
+    got = out.float().cpu().numpy().reshape(-1, D)
+    assert np.abs(got - allv[None]).max() < 2e-2 * np.abs(allv).max() + 2e-3
+
+
+# ------------------------------------------------------------------ the block loop
+def _run_block(hidden_bits_steps, wb, B, L, d, V, seed, max_steps=48, stride_steps=True):
+    hid = to_dev(hidden_bits_steps)
+    p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=0, seed=seed)
+    bp = dg.block_params(max_steps, 0.8, 0.4, B * L * d if stride_steps else 0)
+    bufs = dg.BlockBuffers(B, L, max_steps, DEV)
+    ws = dg.workspace(dg.generate_block_workspace(p, bp), DEV)
+    dg.generate_block(hid, to_dev(wb), p, bp, bufs, ws)
+    torch.cuda.synchronize()
+    _status_ok(ws)
+    return bufs
+
+
+def test_block_flat_logits_one_commit_per_step():
+    """Untrained-model behaviour: exactly one commit per step, 48 steps, no stop."""
+    B, L, d, V = 1, 256, 64, 4096
+    wb = dg_synth.lm_weight(dg_synth.StepConfig("w", d=d, V=V))
+    hid = np.zeros((L, d), np.uint16)
+    bufs = _run_block(hid, wb, B, L, d, V, seed=0, stride_steps=False)
+    assert int(bufs.steps_taken[0]) == 48
+    assert (np_i32(bufs.n_accepted_hist) == 1).all()
+    assert (np_i32(bufs.argmax) == 0).all()
+    assert abs(float(bufs.mean_entropy[0]) - math.log(V)) < H_TOL
+
+
+def test_block_one_hot_stops_after_two_steps_and_batches_independently():
+    L, d, V = 64, 64, 1024
+    w = np.zeros((d, V), np.float32)
+    w[np.arange(d), np.arange(d) * 3] = 300.0
+    x1 = np.zeros((L, d), np.float32)
+    x1[np.arange(L), np.arange(L) % d] = 1.0
+    hid = np.concatenate([dg_synth.f32_to_bf16_bits(x1), np.zeros((L, d), np.uint16)])
+    bufs = _run_block(hid, dg_synth.f32_to_bf16_bits(w), 2, L, d, V, seed=1, max_steps=10,
+                      stride_steps=False)
+    assert np_i32(bufs.steps_taken).tolist() == [2, 10]
+    assert np.array_equal(np_i32(bufs.argmax)[:L], (np.arange(L) % d) * 3)
+    assert np.array_equal(np_i32(bufs.canvas)[:L], (np.arange(L) % d) * 3)
+    hist = np_i32(bufs.n_accepted_hist).reshape(10, 2)
+    assert hist[0, 0] == L and hist[1, 0] == L and (hist[:, 1] == 1).all()
+
+
+def test_block_converging_matches_oracle():
+    """A small version of the converging block workload: per-position targets and
+    confidences, hidden states sharpen with the step; the loop must follow the
+    oracle step for step when every decision is clear of its margin."""
+    cfg = dg_synth.StepConfig("blk", L=64, d=256, V=2048, w_std=0.02, seed=3)
+    wb = dg_synth.lm_weight(cfg)
+    tg = dg_synth.block_targets(cfg)
+    N = 48
+    hs = np.stack([dg_synth.block_hidden(cfg, wb, tg, k) for k in range(N)])
+    ref = oracle.block(lambda k: hs[k], wb, 1, cfg.L, 0.1, 9, max_steps=N)
+    bufs = _run_block(hs, wb, 1, cfg.L, cfg.d, cfg.V, seed=9, max_steps=N)
+    steps = int(bufs.steps_taken[0])
+    assert 1 <= steps <= N
+    clear = all(
+        h["boundary_gap"][0] >= MARGIN and (h["gumbel_margin"] >= MARGIN).all()
+        and (h["argmax_margin"] >= MARGIN).all() for h in ref["history"])
+    if not clear:
+        pytest.skip("a decision of this trajectory is within its margin")
+    assert steps == int(ref["steps"][0])
+    hist = np_i32(bufs.n_accepted_hist)[:steps]
+    assert hist.tolist() == [int(h["n_accepted"][0]) for h in ref["history"]]
+    assert np.array_equal(np_i32(bufs.argmax), ref["argmax"])
+    assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
