@@ -1,0 +1,420 @@
+"""Benchmark of one denoising step of block diffusion on GB300.
+
+A step = canvas attention over [KV cache ; canvas] + LM head with the fused
+entropy / Gumbel-max / argmax epilogue + acceptance / renoise / stop test,
+all through the C ABI of libdg.so.  The default workload is the full-width
+single step (16 query / 8 kv heads, head dim 256, 4096 cached keys, LM head
+2816 x 262144, per-row logit scale U(0.5, 8), T = 0.8, b = 0.1).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own independent canvas (replicas,
+no data-path collective); value = total steps/s over all ranks.
+The reference arm (--impl reference) times the fp64 CPU oracle on a bounded
+sample of the same workload and scales it to the full step.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle runs single-threaded (BLAS included) so its core count is exact.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dg_synth  # noqa: E402
+
+DEFAULT_CONFIG = "step_full"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle sample
+def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0):
+    """Time the CPU oracle on a bounded sample of one step and scale it to the full step.
+
+    Sample: every canvas row of the LM head + sampler against the first v_sample
+    vocabulary columns (time scaled by V / v_sample), attention for attn_rows of
+    the B*L*Hq query rows (scaled by the row count), the acceptance + stop test on
+    the full canvas.  Returns (seconds per full step, description).
+    """
+    import oracle
+    xb, wb = inputs_host["x"], inputs_host["w"]
+    vs = min(v_sample, cfg.V)
+    w_s = np.ascontiguousarray(wb[:, :vs])
+    t0 = time.perf_counter()
+    lg = oracle.logits(xb, w_s)
+    s = oracle.sampler(lg, cfg.temperature, seed, np.arange(cfg.M), 1)
+    t_lm = time.perf_counter() - t0
+    rows = np.linspace(0, cfg.B * cfg.L * cfg.Hq - 1, attn_rows).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_rows(inputs_host["q"], inputs_host["kp"], inputs_host["vp"],
+                          inputs_host["kc"], inputs_host["vc"], cfg.B, cfg.L, cfg.P, cfg.Hq,
+                          cfg.Hkv, cfg.D, 1.0 / math.sqrt(cfg.D), rows)
+    t_at = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    Hf = s["H"].astype(np.float32)
+    for b in range(cfg.B):
+        sl = slice(b * cfg.L, (b + 1) * cfg.L)
+        oracle.accept_renoise(Hf[sl], s["sample"][sl], np.zeros(cfg.L, np.int32), cfg.V,
+                              cfg.entropy_bound, seed, b * cfg.L, 1)
+        oracle.stop(s["argmax"][sl], s["argmax"][sl], Hf[sl], 1)
+    t_acc = time.perf_counter() - t0
+    full = t_lm * (cfg.V / vs) + t_at * (cfg.B * cfg.L * cfg.Hq / len(rows)) + t_acc
+    desc = ("oracle (fp64 C + numpy fp64 matmul, 1 thread): all %d canvas rows x %d of %d vocab "
+            "columns (LM head + sampler, scaled x%.0f), %d of %d attention rows (scaled), "
+            "acceptance + stop on the full canvas" % (cfg.M, vs, cfg.V, cfg.V / vs, len(rows),
+                                                      cfg.B * cfg.L * cfg.Hq))
+    return full, desc, dict(t_lm=t_lm, t_attn=t_at, t_accept=t_acc)
+
+
+def host_inputs_small_sample(cfg, seed=0):
+    """Host (numpy, bf16 bits) inputs of the workload for the oracle sample; W is drawn
+    only for the sampled columns to keep the reference arm bounded."""
+    cfg_s = dg_synth.StepConfig(cfg.name + "_cols", B=cfg.B, L=cfg.L, Hq=cfg.Hq, Hkv=cfg.Hkv,
+                                D=cfg.D, P=cfg.P, d=cfg.d, V=min(cfg.V, 8192), w_std=cfg.w_std,
+                                row_scale=cfg.row_scale, seed=seed)
+    out = dict(dg_synth.attention_inputs(cfg_s))
+    out["x"] = dg_synth.lm_hidden(cfg_s)
+    out["w"] = dg_synth.lm_weight(cfg_s)
+    return out
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    host = host_inputs_small_sample(cfg, seed=cfg.seed)
+    times = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        t, desc, _ = oracle_step_estimate(cfg, host, v_sample=2048, attn_rows=16, seed=i)
+        if i >= args.warmup:
+            times.append(t)
+    per = sum(times) / len(times)
+    value = 1.0 / per
+    line = dict(impl="reference", metric="denoise steps/s (256-tok canvas, bs=1)",
+                value=value, unit="steps/s", n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=per * 1e3, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                config=_config_json(cfg, l2="n/a (CPU)"),
+                cpu_baseline=dict(value=value, unit="steps/s", cores=1, kind="oracle",
+                                  sample=desc),
+                e2e=dict(value=value, unit="steps/s", h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config_json(cfg, l2):
+    return {"workload": "%s: single denoising step, B=%d L=%d, attention Hq=%d Hkv=%d D=%d "
+                        "P=%d, LM head d=%d V=%d, T=%.1f b=%.1f" % (
+                            cfg.name, cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V,
+                            cfg.temperature, cfg.entropy_bound),
+            "global_batch": cfg.B, "seq_len": cfg.L, "parallelism": "replicas", "l2": l2}
+
+
+# ----------------------------------------------------------------------------- our arm
+def _traffic_record(kernel_sources):
+    """Per-launch DRAM bytes of the LM-head kernel from the committed ncu summary,
+    valid only while the kernel sources are unchanged."""
+    path = os.path.join(ROOT, "profiles", "lm_head_kernel_step_full.md")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in kernel_sources:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, cfg):
+    import torch
+    import block_diffusion_decoding_gb300 as dg
+    from block_diffusion_decoding_gb300 import build as dgbuild
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+    dgbuild.build()
+    dg.lib()
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+
+    # ---- synthetic inputs, resident in HBM (seeded per rank: independent canvases)
+    g = torch.Generator(device=dev).manual_seed(1000 + rank)
+    bf = torch.bfloat16
+    B, L, Hq, Hkv, D, P, d, V = cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V
+    M = B * L
+    q = torch.randn(B, L, Hq, D, device=dev, generator=g).to(bf)
+    kp = torch.randn(B, P, Hkv, D, device=dev, generator=g).to(bf)
+    vp = torch.randn(B, P, Hkv, D, device=dev, generator=g).to(bf)
+    kc = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+    vc = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+    attn_out = torch.empty_like(q)
+    x = torch.randn(M, d, device=dev, generator=g)
+    if cfg.row_scale is not None:
+        lo, hi = cfg.row_scale
+        x *= torch.rand(M, 1, device=dev, generator=g) * (hi - lo) + lo
+    x = x.to(bf)
+    w = torch.empty(d, V, device=dev, dtype=bf)
+    for r0 in range(0, d, 256):
+        r1 = min(d, r0 + 256)
+        w[r0:r1] = (torch.randn(r1 - r0, V, device=dev, generator=g) * cfg.w_std).to(bf)
+    scale = 1.0 / math.sqrt(D)
+    aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), dev)
+    bufs = dg.StepBuffers(B, L, dev)
+    bufs.canvas.copy_(torch.randint(0, V, (M,), device=dev, generator=g, dtype=torch.int32))
+    p0 = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 0,
+                        seed=rank)
+    sws = dg.workspace(dg.denoise_step_workspace(p0), dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k):
+        dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws)
+        p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold,
+                           k, seed=rank)
+        dg.denoise_step(x, w, p, bufs, sws)
+
+    def timed(fn, n, first):
+        """Per-iteration CUDA-event times (ms) with an L2 flush before each iteration."""
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn(first + i)
+            e.record(stream)
+            evs.append((s, e))
+        torch.cuda.synchronize(dev)
+        return [s.elapsed_time(e) for s, e in evs]
+
+    # ---- warmup, then the timed region (barrier + sync on both sides)
+    timed(step, args.warmup, 0)
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = dg.kernel_launches()
+    with ClockSampler(local) as clk:
+        ts = timed(step, args.steps, args.warmup)
+    launches = dg.kernel_launches() - n0
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    step_ms = sum(ts) / len(ts)
+    status = dg.read_device_status(sws) | dg.read_device_status(aws)
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    # ---- per-kernel timings (same flush discipline) for the roofline
+    lm_ms = statistics.mean(timed(lambda k: dg.lm_head_fold(x, w, p0, sws), args.steps, 0))
+    at_ms = statistics.mean(timed(lambda k: dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale,
+                                                           aws), args.steps, 0))
+    lm_bytes = d * V * 2 + M * d * 2
+    lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
+    lm_flops = 2.0 * M * d * V
+    at_flops = 4.0 * B * Hq * L * (P + L) * D
+    at_bytes = 2 * (B * L * Hq * D * 2) + 2 * (B * (P + L) * Hkv * D * 2)
+    srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
+            for f in ("dg_lm_head.cu", "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
+    traffic = _traffic_record(srcs)
+
+    # ---- end to end through the C ABI with host buffers (pinned), per-step H2D + D2H
+    h_x = x.cpu().pin_memory()
+    h_q, h_kc, h_vc = q.cpu().pin_memory(), kc.cpu().pin_memory(), vc.cpu().pin_memory()
+    h_canvas = torch.empty(M, dtype=torch.int32).pin_memory()
+    h_argmax = torch.empty(M, dtype=torch.int32).pin_memory()
+    h_stop = torch.empty(B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_q, h_kc, h_vc))
+    d2h = sum(t.numel() * t.element_size() for t in (h_canvas, h_argmax, h_stop))
+
+    def e2e_step(k):
+        x.copy_(h_x, non_blocking=True)
+        q.copy_(h_q, non_blocking=True)
+        kc.copy_(h_kc, non_blocking=True)
+        vc.copy_(h_vc, non_blocking=True)
+        step(k)
+        h_canvas.copy_(bufs.canvas, non_blocking=True)
+        h_argmax.copy_(bufs.argmax, non_blocking=True)
+        h_stop.copy_(bufs.stop, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        return int(h_stop[0])
+
+    for i in range(2):
+        e2e_step(i)
+    e2e_times = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e2e_step(args.warmup + i)
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_ms = 1e3 * sum(e2e_times) / len(e2e_times)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {"x": x.view(torch.int16).cpu().numpy().view(np.uint16),
+                "w": w[:, :16384].contiguous().view(torch.int16).cpu().numpy().view(np.uint16),
+                "q": q.view(torch.int16).cpu().numpy().view(np.uint16),
+                "kp": kp.view(torch.int16).cpu().numpy().view(np.uint16),
+                "vp": vp.view(torch.int16).cpu().numpy().view(np.uint16),
+                "kc": kc.view(torch.int16).cpu().numpy().view(np.uint16),
+                "vc": vc.view(torch.int16).cpu().numpy().view(np.uint16)}
+        est = [oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64)[0] for _ in range(2)]
+        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64)
+        cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle",
+                   sample=desc)
+    if world > 1:
+        tdist.destroy_process_group()
+    if rank != 0:
+        return 0
+    value = world * 1e3 / step_ms
+    line = dict(
+        metric="denoise steps/s (256-tok canvas, bs=1)", value=value, unit="steps/s",
+        n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=step_ms,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+        data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step"),
+        canvas_tokens_per_s=value * M,
+        roofline=dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
+                      frac=lm_gbs / hbm_peak, traffic=traffic, kernel="lm_head_kernel",
+                      peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
+                      algorithmic_bytes=lm_bytes),
+        kernels={"lm_head_kernel": {"ms": lm_ms, "GB_per_s": lm_gbs,
+                                    "TFLOP_per_s": lm_flops / (lm_ms * 1e-3) / 1e12},
+                 "canvas_attn": {"ms": at_ms, "TFLOP_per_s": at_flops / (at_ms * 1e-3) / 1e12,
+                                 "frac_of_bf16_peak": at_flops / (at_ms * 1e-3) / 1e12 / bf16_peak,
+                                 "GB_per_s": at_bytes / (at_ms * 1e-3) / 1e9}},
+        step_roofline_ms=(lm_bytes / (hbm_peak * 1e9) + at_flops / (bf16_peak * 1e12)) * 1e3,
+        cpu_baseline=cpu,
+        e2e=dict(value=world * 1e3 / e2e_ms, unit="steps/s", h2d_bytes_per_step=h2d,
+                 d2h_bytes_per_step=d2h),
+        clocks=clk.summary(), gpu_launches=launches, device_status=status)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(dg_synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    cfg = dg_synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

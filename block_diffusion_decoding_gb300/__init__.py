@@ -30,7 +30,7 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_denoise_step_workspace", "dg_denoise_step",
             "dg_generate_block_workspace", "dg_generate_block",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
-            "dg_gumbel_fill", "dg_logf_eval"]
+            "dg_lm_head_fold", "dg_kernel_launches", "dg_gumbel_fill", "dg_logf_eval"]
 
 
 class DgError(RuntimeError):
@@ -90,6 +90,8 @@ def _lib():
             "dg_sampler_workspace": ([sp], sz),
             "dg_sampler_from_logits": ([vp, sp, si, vp, sz, vp], i32),
             "dg_accept_renoise": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
+            "dg_lm_head_fold": ([vp, vp, sp, vp, sz, vp], i32),
+            "dg_kernel_launches": ([], u64),
             "dg_gumbel_fill": ([u64, u32, u32, u32, i32, vp, vp], i32),
             "dg_logf_eval": ([vp, vp, i32, vp], i32),
         }
@@ -174,6 +176,18 @@ def denoise_step(hidden, w, p: StepParams, bufs: StepBuffers, workspace, stream=
     rc = _lib().dg_denoise_step(_p(hidden), _p(w), ctypes.byref(p), ctypes.byref(io),
                                 _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "dg_denoise_step")
+
+
+def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):
+    """The LM-head kernel of the step alone (partial states into the workspace)."""
+    rc = _lib().dg_lm_head_fold(_p(hidden), _p(w), ctypes.byref(p), _p(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(rc, "dg_lm_head_fold")
+
+
+def kernel_launches() -> int:
+    """Kernels this library has launched (or enqueued into a capture) so far."""
+    return int(_lib().dg_kernel_launches())
 
 
 def sampler_workspace(p: StepParams) -> int:

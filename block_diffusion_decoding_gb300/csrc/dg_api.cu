@@ -3,6 +3,7 @@
 // the CUDA graph of the block loop.  Host code only; kernels live in the
 // other .cu files.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -53,6 +54,10 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_dev;
+std::atomic<uint64_t> g_launches{0};
+
+// Every kernel launch goes through here so the library can count them.
+#define DG_LAUNCHED() g_launches.fetch_add(1, std::memory_order_relaxed)
 
 int current_device_info(DeviceInfo **out)
 {
@@ -261,7 +266,7 @@ AcceptArgs accept_args(const dg_step_params *p, const dg_step_io *io)
 int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, const float *logits,
                  const uint16_t *w, const dg_step_params *p, const LmPlan &plan, StepWs &ws,
                  const StepSource &src, float *H, int32_t *sample, int32_t *argmax,
-                 const AcceptArgs &acc, cudaStream_t st)
+                 const AcceptArgs &acc, cudaStream_t st, bool lm_only = false)
 {
     const int M = p->B * p->L;
     if (logits == nullptr) {
@@ -300,6 +305,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.counters = ws.counters;
         a.ncounters = p->B;
         lm_head_kernel<<<plan.n_slots, kLmThreads, kLmSmemBytes, st>>>(mx, mw, a);
+        DG_LAUNCHED();
     } else {
         FoldArgs f{};
         f.M = M;
@@ -314,8 +320,10 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         f.counters = ws.counters;
         f.ncounters = p->B;
         logits_fold_kernel<<<plan.n_slots, 256, 0, st>>>(logits, f);
+        DG_LAUNCHED();
     }
     DG_CUDA_TRY(cudaGetLastError());
+    if (lm_only) return DG_OK;
     CombineArgs c{};
     c.part = ws.part;
     c.n_slots = plan.n_slots;
@@ -328,6 +336,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     c.counters = ws.counters;
     dim3 grid((p->L + 7) / 8, p->B);
     combine_accept_kernel<<<grid, 256, 0, st>>>(c, acc);
+    DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
 }
@@ -545,10 +554,12 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
         attn_kernel_d128<<<grid, kAttnThreads, attn_smem_bytes(128), st>>>(mq, mkp, mvp, mkc, mvc, a);
     else
         attn_kernel_d256<<<grid, kAttnThreads, attn_smem_bytes(256), st>>>(mq, mkp, mvp, mkc, mvc, a);
+    DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     if (ap.nsplit > 1) {
         const size_t nr = static_cast<size_t>(B) * L * Hq;
         attn_combine_kernel<<<static_cast<unsigned>((nr + 7) / 8), 256, 0, st>>>(a);
+        DG_LAUNCHED();
         DG_CUDA_TRY(cudaGetLastError());
     }
     return DG_OK;
@@ -583,6 +594,29 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
                         io->argmax, acc, as_stream(stream));
 }
+
+int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_params *p,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if (!hidden || !w) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(w)) return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_denoise_step_workspace(p))
+        return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    const int M = p->B * p->L;
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    const StepSource src = step_source(p);
+    AcceptArgs acc{};
+    return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, nullptr, nullptr, nullptr,
+                        acc, as_stream(stream), true);
+}
+
+uint64_t dg_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------- sampler on given logits
 size_t dg_sampler_workspace(const dg_step_params *p)
@@ -623,6 +657,7 @@ int dg_accept_renoise(const float *entropy, const int32_t *sample, const int32_t
     if (workspace == nullptr || workspace_bytes < sizeof(WsHeader)) return DG_ERR_WORKSPACE;
     AcceptArgs acc = accept_args(p, io);
     accept_only_kernel<<<p->B, 256, 0, as_stream(stream)>>>(entropy, sample, argmax, acc);
+    DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
 }
@@ -764,6 +799,7 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
         ctl, bp->max_steps, bp->t_start, bp->t_end, p->B, done, io->steps_taken, io->canvas, prev,
         M, static_cast<uint32_t>(p->V), static_cast<uint32_t>(p->seed),
         static_cast<uint32_t>(p->seed >> 32));
+    DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     DG_CUDA_TRY(cudaGraphLaunch(bgp->exec, st));
     return DG_OK;
@@ -777,6 +813,7 @@ int dg_gumbel_fill(uint64_t seed, uint32_t row, uint32_t step, uint32_t v0, int 
     if (n == 0) return DG_OK;
     gumbel_fill_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(
         static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), row, step, v0, n, out);
+    DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
 }
@@ -786,6 +823,7 @@ int dg_logf_eval(const float *x, float *y, int n, void *stream)
     if (n < 0 || (n > 0 && (x == nullptr || y == nullptr))) return DG_ERR_INVALID_ARG;
     if (n == 0) return DG_OK;
     logf_eval_kernel<<<(n + 255) / 256, 256, 0, as_stream(stream)>>>(x, y, n);
+    DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
 }

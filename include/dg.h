@@ -189,6 +189,17 @@ size_t dg_sampler_workspace(const dg_step_params *p);
 int dg_sampler_from_logits(const float *logits, const dg_step_params *p, const dg_step_io *io,
                            void *workspace, size_t workspace_bytes, void *stream);
 
+/* The first kernel of dg_denoise_step alone: the LM-head GEMM with its      */
+/* fused entropy / Gumbel-max / argmax epilogue, leaving the per-position     */
+/* partial states in the workspace (no combine, acceptance or stop).  Same    */
+/* arguments and workspace size as dg_denoise_step; io is not needed.         */
+int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_params *p,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Number of kernels this library has launched (or enqueued into a stream    */
+/* capture) in this process so far.                                           */
+uint64_t dg_kernel_launches(void);
+
 /* Acceptance, renoise and stop test alone on given entropy/sample/argmax     */
 /* [B*L] (device).  Writes canvas, accepted, n_accepted, stop, mean_entropy   */
 /* and prev_argmax of io; io->entropy/sample/argmax are not used. */
