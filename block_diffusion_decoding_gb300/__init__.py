@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
 # Functions include/dg.h declares (checked by the CPU test-suite).
 EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_canvas_attn_workspace", "dg_canvas_attn",
-            "dg_denoise_step_workspace", "dg_denoise_step",
+            "dg_denoise_step_workspace", "dg_denoise_step", "dg_denoise_step_noalloc",
             "dg_generate_block_workspace", "dg_generate_block",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
             "dg_lm_head_fold", "dg_kernel_launches", "dg_gumbel_fill", "dg_logf_eval"]
@@ -85,6 +85,7 @@ def _lib():
             "dg_canvas_attn": ([vp] * 6 + [i32] * 6 + [f32, vp, sz, vp], i32),
             "dg_denoise_step_workspace": ([sp], sz),
             "dg_denoise_step": ([vp, vp, sp, si, vp, sz, vp], i32),
+            "dg_denoise_step_noalloc": ([vp, vp, sp, si, vp], i32),
             "dg_generate_block_workspace": ([sp, bp], sz),
             "dg_generate_block": ([vp, vp, sp, bp, bi, vp, sz, vp], i32),
             "dg_sampler_workspace": ([sp], sz),

@@ -1,0 +1,247 @@
+// dg_noalloc.cu -- dg_denoise_step_noalloc: the denoising step for callers
+// that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at the point where they run a step: an
+// inference engine that hands out all device memory from its own pool, code
+// running inside a region where allocation is forbidden (a memory budget that
+// is already fully committed, a driver-level allocator that must not be
+// re-entered), or a host program that only receives device pointers for its
+// inputs and outputs.  They have no workspace to pass.  This entry point runs
+// the same two kernels as dg_denoise_step (LM head with the fused sampler
+// epilogue, then combine + acceptance + stop) and keeps their scratch -- the
+// per-CTA partial states, the per-canvas counters and the status header -- in
+// one fixed array in the library's own device memory, declared below.  The
+// array is part of the loaded module: every GPU that loads the library holds
+// it until the process exits.
+//
+// Capacity: kNoAllocScratchBytes = 4 MiB.  A step needs 256 bytes of header,
+// 7 x 4 bytes x (LM-head CTAs) x B*L of partial states and 4 bytes per canvas
+// (each rounded up to 256 bytes).  With one CTA per SM on a 152-SM GB300 that
+// is at most B*L = 985 canvas rows (three 256-token canvases); larger steps
+// are rejected with DG_ERR_UNSUPPORTED before anything is launched.
+//
+// Sharing: every call, from any thread or stream, uses the same array and
+// leaves the last call's contents in it.  The counters that must start at
+// zero are zeroed by the first kernel of each call; the status header is
+// cleared once, at set-up.  Calls whose kernels overlap on the GPU (two
+// streams, two threads without ordering) race on the array and give wrong
+// results: order them on one stream.
+//
+// Set-up: the first call on each device (with that device current) looks up
+// the device address of the array with cudaGetSymbolAddress, sets the LM-head
+// kernel's shared-memory limit and clears the status header (a synchronous
+// cudaMemset).  Make that first call before any stream capture.  Nothing here
+// calls cudaMalloc, cudaFree or any allocating library routine.  Kernels
+// launched by this entry point are not counted by dg_kernel_launches.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+
+#include "dg_kernels.h"
+
+using namespace dg;
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+
+// The scratch of dg_denoise_step_noalloc.  In host code this name is only a
+// stand-in for the symbol; kernels receive the device address obtained with
+// cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocDevice {
+    unsigned char *scratch = nullptr;   // device address of g_noalloc_scratch
+    int sms = 0;
+};
+
+std::mutex g_na_mu;
+std::map<int, NoAllocDevice> g_na_dev;
+
+inline size_t na_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool na_aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int na_setup(NoAllocDevice **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_na_mu);
+    NoAllocDevice &st = g_na_dev[dev];
+    if (st.scratch == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr ||
+            cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kLmSmemBytes) != cudaSuccess ||
+            cudaMemset(ptr, 0, sizeof(WsHeader)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return DG_ERR_CUDA;
+        }
+        st.scratch = static_cast<unsigned char *>(ptr);
+    }
+    *out = &st;
+    return DG_OK;
+}
+
+typedef CUresult (*NaEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                               const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                               const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int na_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+           uint32_t box_outer)
+{
+    static NaEncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<NaEncodeFn>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    if (fn == nullptr) return DG_ERR_CUDA;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t elem[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                    strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w,
+                                       const dg_step_params *p, const dg_step_io *io,
+                                       void *stream)
+{
+    // ---- the same argument checks as dg_denoise_step
+    if (p == nullptr || io == nullptr || hidden == nullptr || w == nullptr) return DG_ERR_INVALID_ARG;
+    if (p->B < 1 || p->L < 1 || p->V < 1 || p->d < 1) return DG_ERR_INVALID_ARG;
+    if (!(p->temperature > 0.0) || !std::isfinite(p->temperature)) return DG_ERR_INVALID_ARG;
+    if (!(p->entropy_bound >= 0.f) || !std::isfinite(p->entropy_bound)) return DG_ERR_INVALID_ARG;
+    if (!std::isfinite(p->stop_threshold) || p->step < 0) return DG_ERR_INVALID_ARG;
+    if (!io->canvas || !io->prev_argmax || !io->argmax || !io->sample || !io->entropy ||
+        !io->accepted || !io->n_accepted || !io->mean_entropy || !io->stop)
+        return DG_ERR_INVALID_ARG;
+    if (p->L > kMaxCanvas || p->V % 8 != 0 || p->V < 64) return DG_ERR_UNSUPPORTED;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (static_cast<long long>(p->B) * p->L > (1LL << 20)) return DG_ERR_UNSUPPORTED;
+    if (!na_aligned16(hidden) || !na_aligned16(w)) return DG_ERR_ALIGNMENT;
+
+    NoAllocDevice *st = nullptr;
+    int rc = na_setup(&st);
+    if (rc != DG_OK) return rc;
+
+    // ---- tile plan: the same choice as dg_denoise_step
+    const int M = p->B * p->L;
+    const int mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
+    const char *env = std::getenv("DG_LM_BN");
+    const int forced = env ? std::atoi(env) : 0;
+    int BN = 0, ntn = 0, total = 0, slots = 0;
+    long best = -1;
+    for (int bn = 128; bn >= 64; bn -= 16) {
+        if (forced && bn != forced) continue;
+        const int n = (p->V + bn - 1) / bn;
+        const int t = n * mblocks;
+        const int s = std::min(std::min(t, st->sms), 256);
+        const long cost = static_cast<long>((t + s - 1) / s) * (bn + 40);
+        if (best < 0 || cost < best) {
+            best = cost;
+            BN = bn;
+            ntn = n;
+            total = t;
+            slots = s;
+        }
+    }
+
+    // ---- scratch layout (as a workspace): header | partials | counters
+    const size_t npart = static_cast<size_t>(slots) * M;
+    const size_t need = sizeof(WsHeader) + na_round_up(7 * npart * 4, 256) +
+                        na_round_up(static_cast<size_t>(p->B) * 4, 256);
+    if (need > kNoAllocScratchBytes) return DG_ERR_UNSUPPORTED;
+    unsigned char *base = st->scratch;
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(base);
+    float *f = reinterpret_cast<float *>(base + sizeof(WsHeader));
+    Partials part;
+    part.m = f;
+    part.S = f + npart;
+    part.A = f + 2 * npart;
+    part.gbest = f + 3 * npart;
+    part.amax = f + 4 * npart;
+    part.gidx = reinterpret_cast<int *>(f + 5 * npart);
+    part.aidx = reinterpret_cast<int *>(f + 6 * npart);
+    int *counters = reinterpret_cast<int *>(base + sizeof(WsHeader) + na_round_up(7 * npart * 4, 256));
+
+    CUtensorMap mx, mw;
+    if ((rc = na_map(&mx, hidden, static_cast<uint64_t>(p->d), static_cast<uint64_t>(M), 64, 256)) != DG_OK)
+        return rc;
+    if ((rc = na_map(&mw, w, static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d), 64, 64)) != DG_OK)
+        return rc;
+
+    StepSource src{};
+    src.ctl = nullptr;
+    src.invT = static_cast<float>(1.0 / p->temperature);
+    src.c2 = src.invT * 1.44269502162933349609375f;
+    src.step = p->step;
+
+    LmHeadArgs a{};
+    a.M = M;
+    a.d = p->d;
+    a.V = p->V;
+    a.BN = BN;
+    a.ntn = ntn;
+    a.total = total;
+    a.kblocks = p->d / 64;
+    a.nbox_b = (BN + 63) / 64;
+    a.x_3d = 0;
+    a.part = part;
+    a.src = src;
+    a.seed = p->seed;
+    a.ws = hdr;
+    a.counters = counters;
+    a.ncounters = p->B;
+
+    CombineArgs c{};
+    c.part = part;
+    c.n_slots = slots;
+    c.ntn = ntn;
+    c.total = total;
+    c.M = M;
+    c.H = io->entropy;
+    c.sample = io->sample;
+    c.argmax = io->argmax;
+    c.counters = counters;
+
+    AcceptArgs acc{};
+    acc.B = p->B;
+    acc.L = p->L;
+    acc.V = p->V;
+    acc.bound = p->entropy_bound;
+    acc.threshold = p->stop_threshold;
+    acc.seed = p->seed;
+    acc.step = p->step;
+    acc.canvas = io->canvas;
+    acc.prev_argmax = io->prev_argmax;
+    acc.accepted = io->accepted;
+    acc.n_accepted = io->n_accepted;
+    acc.mean_entropy = io->mean_entropy;
+    acc.stop = io->stop;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    lm_head_kernel<<<slots, kLmThreads, kLmSmemBytes, s>>>(mx, mw, a);
+    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    combine_accept_kernel<<<dim3((p->L + 7) / 8, p->B), 256, 0, s>>>(c, acc);
+    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    return DG_OK;
+}
