@@ -83,7 +83,20 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def wait_first(self, timeout=3.0):
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout:
+            time.sleep(0.01)
+
+    def mark(self, t_start, t_end):
+        """The timed region; samples within 0.25 s of it are kept (nvidia-smi
+        samples every 200 ms, so a short region still gets its neighbours)."""
+        self.window = (t_start - 0.25, t_end + 0.25)
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 0.5 and not any(t > t_end for t, _ in self.lines):
+            time.sleep(0.01)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -96,7 +109,10 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lo, hi = getattr(self, "window", (-1e30, 1e30))
+        for t, ln in self.lines:
+            if not lo <= t <= hi:
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -290,14 +306,18 @@ def run_ours(args, cfg):
         return [s.elapsed_time(e) for s, e in evs]
 
     # ---- warmup, then the timed region (barrier + sync on both sides)
-    timed(step, args.warmup, 0)
-    if world > 1:
-        tdist.barrier()
-    torch.cuda.synchronize(dev)
-    n0 = dg.kernel_launches()
     with ClockSampler(local) as clk:
+        clk.wait_first()
+        timed(step, args.warmup, 0)
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+        n0 = dg.kernel_launches()
+        t_start = time.perf_counter()
         ts = timed(step, args.steps, args.warmup)
-    launches = dg.kernel_launches() - n0
+        t_end = time.perf_counter()
+        launches = dg.kernel_launches() - n0
+        clk.mark(t_start, t_end)
     if world > 1:
         tdist.barrier()
     torch.cuda.synchronize(dev)
@@ -403,8 +423,8 @@ def run_ours(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(dg_synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -175,12 +175,28 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             tc_fence_after();
             const int row = m * kRowsPerBlock + h * 128 + q * 32 + lane;
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * 256 + h * 128);
-            for (int c0 = 0; c0 < a.BN; c0 += 16) {
+            const bool live = row < a.M;
+            int c0 = 0;
+            for (; c0 + 32 <= a.BN; c0 += 32) {
+                uint32_t r32[32];
+                tmem_ld32_nowait(tb + static_cast<uint32_t>(c0), r32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float lg[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) lg[j] = __uint_as_float(r32[16 * hh + j]);
+                    const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0 + 16 * hh);
+                    if (v0 < static_cast<uint32_t>(a.V))
+                        fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+                }
+            }
+            if (c0 < a.BN) {    // a 16-column tail (BN = 16 mod 32)
                 float lg[16];
                 tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
                 const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
-                if (row < a.M && v0 < static_cast<uint32_t>(a.V))
-                    fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc);
+                if (v0 < static_cast<uint32_t>(a.V))
+                    fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
             }
             tc_fence_before();
             __syncwarp();

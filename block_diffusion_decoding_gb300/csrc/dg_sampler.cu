@@ -43,13 +43,16 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
             row_state_init(st);
             cur_m = m;
         }
-        if (row >= a.M) continue;
-        const float *src = logits + static_cast<size_t>(row) * a.V;
+        const bool live = row < a.M;
+        const float *src = logits + static_cast<size_t>(live ? row : 0) * a.V;
         for (int c0 = 0; c0 < a.BN; c0 += 16) {
             const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
             if (v0 >= static_cast<uint32_t>(a.V)) break;
             float lg[16];
-            if (v0 + 16u <= static_cast<uint32_t>(a.V)) {
+            if (!live) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) lg[j] = 0.f;
+            } else if (v0 + 16u <= static_cast<uint32_t>(a.V)) {
                 const float4 *p4 = reinterpret_cast<const float4 *>(src + v0);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -61,7 +64,7 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
                 for (int j = 0; j < 16; ++j)
                     lg[j] = (v0 + j < static_cast<uint32_t>(a.V)) ? __ldg(src + v0 + j) : 0.f;
             }
-            fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc);
+            fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
         }
     }
     if (cur_m >= 0) {

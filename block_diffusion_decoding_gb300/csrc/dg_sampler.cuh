@@ -58,64 +58,134 @@ struct FoldConsts {
     uint32_t step;   // Philox counter word 2
 };
 
+DG_DEVICE float fast_log2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Pruning of the Gumbel-max search.  A column v can only replace the running
+// best score B if its exact score fmaf(logit, invT, G_v) exceeds B, i.e. if
+// G_v > tau = B - logit * invT (up to the roundings of the score, a few ulp).
+// G_v = -ln(-ln u) never exceeds -ln(-ln(1 - 2^-24)) = 16.636, so columns
+// with tau > 16.7 are out without drawing their noise.  For the rest, G_v is
+// estimated with the hardware log2 (absolute error of a few 1e-7 in the log,
+// i.e. a relative error below 1e-3 in -ln u as long as u <= 0.999) and the
+// column is evaluated exactly whenever the estimate is within kGumbelSlack of
+// tau, or u > 0.999.  The slack is more than ten times any error of the
+// estimate, so every column that can win is evaluated with the exact fp32
+// sequence: the result is the one of evaluating every column exactly.
+constexpr float kGumbelMaxPlusSlack = 16.75f;
+constexpr float kGumbelSlack = 1.0e-2f;
+constexpr float kUExact = 0.999f;
+
 // Fold 16 consecutive logits lg[0..15] of vocabulary entries v0 .. v0+15
-// (v0 a multiple of 16) of canvas row `row` into the state.  Entries >= V
-// are ignored.
+// (v0 a multiple of 16, the same for every lane of the warp) of canvas row
+// `row` into the state.  Entries >= V are ignored; a lane with live == false
+// (a row past the end) leaves its state alone.  Must be called by all 32
+// lanes of the warp together (it votes across the warp).
 DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
-                      uint32_t row, const FoldConsts &fc)
+                      uint32_t row, const FoldConsts &fc, bool live)
 {
     const bool full = v0 + 16u <= V;
-    float t[16];
+    float x[16];
     float cmax = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const bool ok = full || (v0 + j < V);
-        t[j] = ok ? __fmul_rn(lg[j], fc.c2) : -INFINITY;
-        cmax = fmaxf(cmax, t[j]);
+        x[j] = (live && (full || (v0 + j < V))) ? lg[j] : -INFINITY;
+        cmax = fmaxf(cmax, x[j]);
     }
-    if (cmax > st.m) {
+    if (!__any_sync(0xFFFFFFFFu, live)) return;
+    // argmax: only a chunk whose maximum beats the running best can move it;
+    // the first column holding that maximum wins ties
+    if (cmax > st.amax) {
+        int jj = 15;
+#pragma unroll
+        for (int j = 15; j >= 0; --j)
+            if (x[j] == cmax) jj = j;
+        st.amax = cmax;
+        st.aidx = static_cast<int>(v0) + jj;
+    }
+    // softmax statistics in base 2 (c2 > 0, so the maximum maps through)
+    const float mt = cmax * fc.c2;
+    if (mt > st.m) {
         if (st.S > 0.f) {
-            const float f = fast_exp2(st.m - cmax);
-            st.A = f * fmaf(st.m - cmax, st.S, st.A);
+            const float f = fast_exp2(st.m - mt);
+            st.A = f * fmaf(st.m - mt, st.S, st.A);
             st.S = f * st.S;
         }
-        st.m = cmax;
+        st.m = mt;
     }
-    if (full) {
+    float es[16], as[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float dlt = t[j] - st.m;
-            const float e = fast_exp2(dlt);
-            st.S += e;
-            st.A = fmaf(e, dlt, st.A);
-            if (lg[j] > st.amax) { st.amax = lg[j]; st.aidx = static_cast<int>(v0 + j); }
-        }
-    } else {
+    for (int j = 0; j < 16; ++j) {
+        const float dlt = fmaf(x[j], fc.c2, -st.m);
+        const float e = fast_exp2(dlt);         // 0 for ignored entries
+        es[j] = (e > 0.f) ? e : 0.f;
+        as[j] = (e > 0.f) ? e * dlt : 0.f;
+    }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (v0 + j < V) {
-                const float dlt = t[j] - st.m;
-                const float e = fast_exp2(dlt);
-                st.S += e;
-                st.A = fmaf(e, dlt, st.A);
-                if (lg[j] > st.amax) { st.amax = lg[j]; st.aidx = static_cast<int>(v0 + j); }
-            }
+    for (int h = 8; h >= 1; h >>= 1) {
+#pragma unroll
+        for (int j = 0; j < h; ++j) {
+            es[j] += es[j + h];
+            as[j] += as[j + h];
         }
     }
-    // Gumbel-max: counter (v >> 2, row, step, 0), word v & 3.
+    if (live) {
+        st.S += es[0];
+        st.A += as[0];
+    }
+    // Gumbel-max over the columns that can still win: counter (v >> 2, row,
+    // step, 0), word v & 3.  Stage 1 (logit only) decides whether the warp
+    // draws the noise of this chunk at all.
+    const float lim = st.gbest - kGumbelMaxPlusSlack;
+    float lz[16];
+    uint32_t need = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        lz[j] = x[j] * fc.invT;
+        need |= (lz[j] > lim ? 1u : 0u) << j;
+    }
+    if (!__any_sync(0xFFFFFFFFu, need != 0)) return;
+    uint32_t w[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint4 r = philox4x32_10(make_uint4((v0 >> 2) + q, row, fc.step, kStreamGumbel),
                                       fc.k0, fc.k1);
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        w[4 * q] = r.x;
+        w[4 * q + 1] = r.y;
+        w[4 * q + 2] = r.z;
+        w[4 * q + 3] = r.w;
+    }
+    // Stage 2: approximate Gumbel noise against the running best (taken before
+    // this chunk; it only grows, so this can only admit more candidates).
+    const float best0 = st.gbest;
+    uint32_t cand = 0;
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int j = 4 * q + b;
-            if (full || (v0 + j < V)) {
-                const float g = gumbel_from_bits(w[b]);
-                const float sc = __fmaf_rn(lg[j], fc.invT, g);
-                if (sc > st.gbest) { st.gbest = sc; st.gidx = static_cast<int>(v0 + j); }
-            }
+    for (int j = 0; j < 16; ++j) {
+        const float u = __fmul_rn(__fadd_rn(static_cast<float>(w[j] >> 9), 0.5f),
+                                  __uint_as_float(0x34000000u));
+        const float e1 = -0.69314718f * fast_log2(u);
+        const float g = -0.69314718f * fast_log2(e1);
+        const bool c = (u > kUExact) || (g > (best0 - lz[j]) - kGumbelSlack);
+        cand |= ((need >> j) & 1u) & (c ? 1u : 0u) ? (1u << j) : 0u;
+    }
+    // Exact fp32 score for the candidates, in increasing column order; lanes
+    // with candidates work through theirs together.
+    while (__any_sync(0xFFFFFFFFu, cand != 0)) {
+        if (cand != 0) {
+            const int j = __ffs(cand) - 1;
+            cand &= cand - 1u;
+            uint32_t wj = w[0];
+            float xj = x[0];
+#pragma unroll
+            for (int t = 1; t < 16; ++t)
+                if (t == j) { wj = w[t]; xj = x[t]; }
+            const float g = gumbel_from_bits(wj);
+            const float sc = __fmaf_rn(xj, fc.invT, g);
+            if (sc > st.gbest) { st.gbest = sc; st.gidx = static_cast<int>(v0) + j; }
         }
     }
 }

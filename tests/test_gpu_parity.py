@@ -154,7 +154,8 @@ def _check_step_against_oracle(bufs, ref, B, L, exact_tokens):
 
 
 @pytest.mark.parametrize("B,L,V,scale", [(1, 256, 16384, 1.0), (2, 256, 4096, 4.0),
-                                         (1, 64, 1000, 2.0), (3, 100, 2048, 0.5)])
+                                         (1, 64, 1000, 2.0), (3, 100, 2048, 0.5),
+                                         (1, 48, 262144, 6.0), (1, 32, 262144, 0.05)])
 def test_sampler_from_logits(B, L, V, scale):
     rng = np.random.default_rng(V + L)
     logits = (rng.standard_normal((B * L, V)) * scale
@@ -344,8 +345,9 @@ def test_block_one_hot_stops_after_two_steps_and_batches_independently():
 
 def test_block_converging_matches_oracle():
     """A small version of the converging block workload: per-position targets and
-    confidences, hidden states sharpen with the step; the loop must follow the
-    oracle step for step when every decision is clear of its margin."""
+    confidences, hidden states sharpen with the step.  Every step whose decisions
+    are clear of their margins must commit what the oracle commits; if all are
+    clear the stop step, the final canvas and the argmax output must match too."""
     cfg = dg_synth.StepConfig("blk", L=64, d=256, V=2048, w_std=0.02, seed=3)
     wb = dg_synth.lm_weight(cfg)
     tg = dg_synth.block_targets(cfg)
@@ -355,13 +357,19 @@ def test_block_converging_matches_oracle():
     bufs = _run_block(hs, wb, 1, cfg.L, cfg.d, cfg.V, seed=9, max_steps=N)
     steps = int(bufs.steps_taken[0])
     assert 1 <= steps <= N
-    clear = all(
-        h["boundary_gap"][0] >= MARGIN and (h["gumbel_margin"] >= MARGIN).all()
-        and (h["argmax_margin"] >= MARGIN).all() for h in ref["history"])
-    if not clear:
-        pytest.skip("a decision of this trajectory is within its margin")
-    assert steps == int(ref["steps"][0])
-    hist = np_i32(bufs.n_accepted_hist)[:steps]
-    assert hist.tolist() == [int(h["n_accepted"][0]) for h in ref["history"]]
-    assert np.array_equal(np_i32(bufs.argmax), ref["argmax"])
-    assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
+    hist = np_i32(bufs.n_accepted_hist)
+    clear_steps = []
+    for k, h in enumerate(ref["history"][:steps]):
+        acc = np.zeros(cfg.L, bool)
+        acc[h["order"][0][: int(h["n_accepted"][0])]] = True
+        clear = (acceptance_is_decided(h["H32"], int(h["n_accepted"][0]), float(h["boundary_gap"][0]))
+                 and bool((h["gumbel_margin"][acc] >= MARGIN).all())
+                 and bool((h["argmax_margin"] >= MARGIN).all()))
+        if clear:
+            clear_steps.append(k)
+            assert hist[k] == int(h["n_accepted"][0]), k
+    assert len(clear_steps) >= len(ref["history"]) // 2
+    if len(clear_steps) == len(ref["history"]):
+        assert steps == int(ref["steps"][0])
+        assert np.array_equal(np_i32(bufs.argmax), ref["argmax"])
+        assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
