@@ -170,7 +170,7 @@ int slot_bound(int M, int V)
 {
     const long mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
     const long tiles = mblocks * ((V + 63) / 64);
-    return static_cast<int>(std::min<long>(tiles, kMaxSlots));
+    return static_cast<int>(std::min<long>(tiles, kMaxSlots)) * kLmColGroups;
 }
 
 // Workspace layout of one step: header | partials (7 x n_slots x M x 4 B) |
@@ -326,7 +326,10 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     if (lm_only) return DG_OK;
     CombineArgs c{};
     c.part = ws.part;
-    c.n_slots = plan.n_slots;
+    // the LM head writes one partial state per (CTA, column group); the
+    // logits fold one per CTA
+    c.spc = (logits == nullptr) ? kLmColGroups : 1;
+    c.n_slots = plan.n_slots * c.spc;
     c.ntn = plan.ntn;
     c.total = plan.total;
     c.M = M;
@@ -588,7 +591,7 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
@@ -609,7 +612,7 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
     const StepSource src = step_source(p);
     AcceptArgs acc{};
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, nullptr, nullptr, nullptr,
@@ -639,7 +642,7 @@ int dg_sampler_from_logits(const float *logits, const dg_step_params *p, const d
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, 64, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
     return enqueue_step(nullptr, 0, 1, logits, nullptr, p, plan, ws, src, io->entropy, io->sample,
@@ -696,7 +699,7 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
     size_t off_ctl, off_scr;
     block_ws_layout(p, slot_bound(M, p->V), &off_ctl, &off_scr);
     uint8_t *base = static_cast<uint8_t *>(workspace);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots);
+    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
     LoopCtl *ctl = reinterpret_cast<LoopCtl *>(base + off_ctl);
     uint8_t *sp = base + off_scr;
     const size_t m4 = round_up(static_cast<size_t>(M) * 4, 256);

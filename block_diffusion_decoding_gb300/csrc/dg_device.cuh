@@ -317,9 +317,10 @@ DG_DEVICE uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
 {
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        const uint32_t a = c.x, b = c.z;
-        const uint32_t lo0 = a * 0xD2511F53u, hi0 = __umulhi(a, 0xD2511F53u);
-        const uint32_t lo1 = b * 0xCD9E8D57u, hi1 = __umulhi(b, 0xCD9E8D57u);
+        const uint64_t p0 = static_cast<uint64_t>(c.x) * 0xD2511F53u;   // one wide multiply
+        const uint64_t p1 = static_cast<uint64_t>(c.z) * 0xCD9E8D57u;
+        const uint32_t lo0 = static_cast<uint32_t>(p0), hi0 = static_cast<uint32_t>(p0 >> 32);
+        const uint32_t lo1 = static_cast<uint32_t>(p1), hi1 = static_cast<uint32_t>(p1 >> 32);
         c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;

@@ -21,6 +21,7 @@ struct FoldArgs {
 struct CombineArgs {
     Partials part;
     int n_slots, ntn, total, M;
+    int spc;            // partial-state slots per producer CTA (slot s belongs to CTA s / spc)
     float *H;
     int32_t *sample;
     int32_t *argmax;
@@ -71,7 +72,9 @@ constexpr int kLmABytes = kRowsPerBlock * kLmBK * 2;     // 32 KB
 constexpr int kLmBBoxBytes = 64 * kLmBK * 2;             // 8 KB
 constexpr int kLmBBytes = 2 * kLmBBoxBytes;              // 16 KB
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
-constexpr int kLmThreads = 384;
+constexpr int kLmEpiWarps = 16;                          // 2 per (row half, TMEM quadrant)
+constexpr int kLmColGroups = kLmEpiWarps / 8;             // column groups per row
+constexpr int kLmThreads = 128 + 32 * kLmEpiWarps;        // 640
 constexpr int kLmSmemBytes = kLmStages * kLmStageBytes + 1024 + 256;
 
 __global__ void lm_head_kernel(const __grid_constant__ CUtensorMap map_x,

@@ -10,7 +10,7 @@
 // logits never reach HBM.  The vocabulary projection W [d, V] streams once
 // from HBM through TMA; it is the bandwidth roofline of the step.
 //
-// CTA layout (384 threads, one CTA per SM, persistent over a contiguous
+// CTA layout (640 threads, one CTA per SM, persistent over a contiguous
 // range of tiles):
 //   warp 0      TMA producer: per 64-deep k block, the hidden block
 //               X[256 rows, 64] (K-major, 128B swizzle) and BN/64 boxes of
@@ -20,10 +20,11 @@
 //               MMAs (one per 128-row half) per 16-deep k step into a
 //               double-buffered fp32 accumulator (2 buffers x 2 halves x 128
 //               columns = 512 TMEM columns);
-//   warps 4-11  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 of half
-//               (w - 4) / 4, one canvas row per thread, 16 columns at a time,
-//               and folds them (dg_sampler.cuh) while the MMA fills the other
-//               buffer.
+//   warps 4-19  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 of half
+//               ((w - 4) / 4) % 2, one canvas row per thread, every other
+//               16-column chunk (two warps share a row's columns), and folds
+//               them (dg_sampler.cuh) while the MMA fills the other buffer;
+//               each warp keeps its own partial state (slot 2 CTA + group).
 #include "dg_kernels.h"
 
 namespace dg {
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&acc_full[s], 1);
-            mbar_init(&acc_empty[s], 8);
+            mbar_init(&acc_empty[s], kLmEpiWarps);
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
@@ -113,6 +114,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = make_idesc_bf16(128, a.BN, 1);
+            // descriptors of stage 0; stage s and k step kk only move the start
+            // address field (bits 0-13, in 16-byte units)
+            const uint32_t sa0 = smem_u32(smem);
+            const uint64_t adesc0 = make_sdesc_sw128(sa0, 16, 1024);
+            const uint64_t bdesc0 = make_sdesc_sw128(sa0 + kLmABytes, kLmBBoxBytes, 1024);
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -125,19 +131,18 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&full[s], ph, a.ws, 104)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * kLmStageBytes);
-                    const uint32_t sb = sa + kLmABytes;
+                    const uint64_t soff = static_cast<uint64_t>((s * kLmStageBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kLmBK / 16; ++kk) {
                         // B: MN-major, 64-column blocks 8 KB apart (LBO), 8-row
                         // groups 1 KB apart (SBO); a 16-deep k step is 2 groups.
-                        const uint64_t bdesc = make_sdesc_sw128(sb + kk * 2048, kLmBBoxBytes, 1024);
+                        const uint64_t bdesc = bdesc0 + soff + static_cast<uint64_t>(kk * (2048 >> 4));
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             // A: K-major, 128-byte rows, 8-row groups 1 KB apart;
                             // a 16-deep k step advances 32 bytes inside the row.
-                            const uint64_t adesc =
-                                make_sdesc_sw128(sa + h * (kLmABytes / 2) + kk * 32, 16, 1024);
+                            const uint64_t adesc = adesc0 + soff +
+                                static_cast<uint64_t>((h * (kLmABytes / 2) + kk * 32) >> 4);
                             umma_bf16(d0 + h * 128, adesc, bdesc, idesc, (kb | kk) != 0);
                         }
                     }
@@ -152,7 +157,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
-        const int h = (warp - 4) >> 2, q = warp & 3;
+        const int e = warp - 4;
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int h = (e >> 2) & 1;             // 128-row half
+        const int cg = e >> 3;                  // column group: chunks cg, cg + G, ...
+        const size_t slot = static_cast<size_t>(c) * kLmColGroups + cg;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         RowState st;
         row_state_init(st);
@@ -165,7 +174,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             if (m != cur_m) {
                 if (cur_m >= 0) {
                     const int prow = cur_m * kRowsPerBlock + h * 128 + q * 32 + lane;
-                    if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
+                    row_state_finalize(st, fc);
+                    if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
                 }
                 row_state_init(st);
                 cur_m = m;
@@ -176,22 +186,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const int row = m * kRowsPerBlock + h * 128 + q * 32 + lane;
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * 256 + h * 128);
             const bool live = row < a.M;
-            int c0 = 0;
-            for (; c0 + 32 <= a.BN; c0 += 32) {
-                uint32_t r32[32];
-                tmem_ld32_nowait(tb + static_cast<uint32_t>(c0), r32);
-                tmem_wait_ld();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float lg[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) lg[j] = __uint_as_float(r32[16 * hh + j]);
-                    const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0 + 16 * hh);
-                    if (v0 < static_cast<uint32_t>(a.V))
-                        fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
-                }
-            }
-            if (c0 < a.BN) {    // a 16-column tail (BN = 16 mod 32)
+            // one call site of the (large) fold keeps the hot loop in the
+            // instruction cache
+#pragma unroll 1
+            for (int c0 = 16 * cg; c0 < a.BN; c0 += 16 * kLmColGroups) {
                 float lg[16];
                 tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
                 const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
@@ -204,7 +202,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
         if (cur_m >= 0) {
             const int prow = cur_m * kRowsPerBlock + h * 128 + q * 32 + lane;
-            if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
+            row_state_finalize(st, fc);
+            if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
         }
     }
     tc_fence_before();

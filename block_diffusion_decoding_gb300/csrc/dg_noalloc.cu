@@ -14,8 +14,8 @@
 // array is part of the loaded module: every GPU that loads the library holds
 // it until the process exits.
 //
-// Capacity: kNoAllocScratchBytes = 4 MiB.  A step needs 256 bytes of header,
-// 7 x 4 bytes x (LM-head CTAs) x B*L of partial states and 4 bytes per canvas
+// Capacity: kNoAllocScratchBytes = 8 MiB.  A step needs 256 bytes of header,
+// 7 x 4 bytes x 2 x (LM-head CTAs) x B*L of partial states and 4 bytes per canvas
 // (each rounded up to 256 bytes).  With one CTA per SM on a 152-SM GB300 that
 // is at most B*L = 985 canvas rows (three 256-token canvases); larger steps
 // are rejected with DG_ERR_UNSUPPORTED before anything is launched.
@@ -43,7 +43,7 @@
 
 using namespace dg;
 
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
 // The scratch of dg_denoise_step_noalloc.  In host code this name is only a
 // stand-in for the symbol; kernels receive the device address obtained with
@@ -166,7 +166,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     }
 
     // ---- scratch layout (as a workspace): header | partials | counters
-    const size_t npart = static_cast<size_t>(slots) * M;
+    const size_t npart = static_cast<size_t>(slots) * kLmColGroups * M;
     const size_t need = sizeof(WsHeader) + na_round_up(7 * npart * 4, 256) +
                         na_round_up(static_cast<size_t>(p->B) * 4, 256);
     if (need > kNoAllocScratchBytes) return DG_ERR_UNSUPPORTED;
@@ -214,7 +214,8 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
 
     CombineArgs c{};
     c.part = part;
-    c.n_slots = slots;
+    c.n_slots = slots * kLmColGroups;
+    c.spc = kLmColGroups;
     c.ntn = ntn;
     c.total = total;
     c.M = M;

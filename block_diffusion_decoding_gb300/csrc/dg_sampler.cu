@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
         if (m != cur_m) {
             if (cur_m >= 0) {
                 const int prow = cur_m * kRowsPerBlock + threadIdx.x;
+                row_state_finalize(st, fc);
                 if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
             }
             row_state_init(st);
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
     }
     if (cur_m >= 0) {
         const int prow = cur_m * kRowsPerBlock + threadIdx.x;
+        row_state_finalize(st, fc);
         if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
     }
 }
@@ -213,8 +215,9 @@ __global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, Acce
         RowState st;
         row_state_init(st);
         for (int s = lane; s < c.n_slots; s += 32) {
-            const int t0 = tile_begin(s, c.total, c.n_slots);
-            const int t1 = tile_begin(s + 1, c.total, c.n_slots);
+            const int cta = s / c.spc;
+            const int t0 = tile_begin(cta, c.total, c.n_slots / c.spc);
+            const int t1 = tile_begin(cta + 1, c.total, c.n_slots / c.spc);
             if (t0 < hi && t1 > lo && t1 > t0) {
                 RowState p;
                 partial_load(c.part, static_cast<size_t>(s) * c.M + r, p);

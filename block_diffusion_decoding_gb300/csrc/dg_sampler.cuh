@@ -26,10 +26,16 @@ struct RowState {
     float m;      // running max of t (base-2 scaled logits)
     float S;      // sum 2^(t - m)
     float A;      // sum 2^(t - m) (t - m)
-    float gbest;  // best Gumbel score
+    float gbest;  // best exact Gumbel score among the columns evaluated exactly
     int gidx;     // its vocabulary index
     float amax;   // best logit
     int aidx;     // its vocabulary index
+    // fold only (not part of the stored partial): best approximate Gumbel
+    // score seen, and the column holding it if it is still unevaluated
+    float apb;    // best approximate score (-inf: none yet)
+    float kx;     // kept column: logit
+    uint32_t kw;  // kept column: Philox word
+    int kj;       // kept column: vocabulary index, -1 = none
 };
 
 DG_DEVICE void row_state_init(RowState &s)
@@ -41,6 +47,10 @@ DG_DEVICE void row_state_init(RowState &s)
     s.gidx = 0x7FFFFFFF;
     s.amax = -INFINITY;
     s.aidx = 0x7FFFFFFF;
+    s.apb = -INFINITY;
+    s.kx = 0.f;
+    s.kw = 0u;
+    s.kj = -1;
 }
 
 DG_DEVICE float fast_exp2(float x)
@@ -65,20 +75,29 @@ DG_DEVICE float fast_log2(float x)
     return y;
 }
 
+// The exact fp32 score fmaf(logit, invT, G) of one column (rarely reached:
+// kept out of line so the hot fold stays small).
+static __device__ __noinline__ float exact_gumbel_score(float logit, float invT, uint32_t bits)
+{
+    return __fmaf_rn(logit, invT, gumbel_from_bits(bits));
+}
+
 // Pruning of the Gumbel-max search.  A column v can only replace the running
 // best score B if its exact score fmaf(logit, invT, G_v) exceeds B, i.e. if
-// G_v > tau = B - logit * invT (up to the roundings of the score, a few ulp).
+// G_v > B - logit * invT (up to the roundings of the score, a few ulp).
 // G_v = -ln(-ln u) never exceeds -ln(-ln(1 - 2^-24)) = 16.636, so columns
-// with tau > 16.7 are out without drawing their noise.  For the rest, G_v is
-// estimated with the hardware log2 (absolute error of a few 1e-7 in the log,
-// i.e. a relative error below 1e-3 in -ln u as long as u <= 0.999) and the
-// column is evaluated exactly whenever the estimate is within kGumbelSlack of
-// tau, or u > 0.999.  The slack is more than ten times any error of the
-// estimate, so every column that can win is evaluated with the exact fp32
-// sequence: the result is the one of evaluating every column exactly.
+// with B - logit * invT > 16.75 are out without drawing their noise (stage
+// 1).  For the rest, G_v is estimated (stage 2): -ln u by its series when
+// u > 0.99 (relative error < 3e-9) and by the hardware log2 otherwise
+// (-ln u >= 0.01 there, so an absolute log2 error of 2^-22 is a relative
+// error below 2e-5), then -ln of that by the hardware log2: the estimate is
+// within 1e-4 of G_v.  Only columns whose estimated score is within
+// 2 kGumbelSlack (= 20x that error) of the larger of B and the chunk's best
+// estimate can be the chunk's exact best, so only those are evaluated with
+// the exact fp32 sequence, in increasing column order with strict
+// improvement: the result is the one of evaluating every column exactly.
 constexpr float kGumbelMaxPlusSlack = 16.75f;
-constexpr float kGumbelSlack = 1.0e-2f;
-constexpr float kUExact = 0.999f;
+constexpr float kGumbelSlack = 1.0e-3f;
 
 // Fold 16 consecutive logits lg[0..15] of vocabulary entries v0 .. v0+15
 // (v0 a multiple of 16, the same for every lane of the warp) of canvas row
@@ -140,7 +159,8 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     // Gumbel-max over the columns that can still win: counter (v >> 2, row,
     // step, 0), word v & 3.  Stage 1 (logit only) decides whether the warp
     // draws the noise of this chunk at all.
-    const float lim = st.gbest - kGumbelMaxPlusSlack;
+    // the exact best is at least max(gbest, apb - slack)
+    const float lim = fmaxf(st.gbest, st.apb - 2.0f * kGumbelSlack) - kGumbelMaxPlusSlack;
     float lz[16];
     uint32_t need = 0;
 #pragma unroll
@@ -159,34 +179,83 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         w[4 * q + 2] = r.z;
         w[4 * q + 3] = r.w;
     }
-    // Stage 2: approximate Gumbel noise against the running best (taken before
-    // this chunk; it only grows, so this can only admit more candidates).
-    const float best0 = st.gbest;
-    uint32_t cand = 0;
+    // Stage 2: approximate scores lz + G~.  A column can end up as the chunk's
+    // exact best only if its approximate score is within twice the estimate's
+    // error of the chunk's best approximate score, and above the running best.
+    float ap[16];
+    float amax = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const float u = __fmul_rn(__fadd_rn(static_cast<float>(w[j] >> 9), 0.5f),
-                                  __uint_as_float(0x34000000u));
-        const float e1 = -0.69314718f * fast_log2(u);
+        // u = ((x >> 9) + 1/2) 2^-23 = (1 + (x >> 9) 2^-23) - (1 - 2^-24), exact
+        const float u = __fadd_rn(__uint_as_float(0x3F800000u | (w[j] >> 9)), -0.99999994f);
+        const float om = 1.0f - u;   // exact
+        // -ln u: series near u = 1 (relative error < 3e-9), hardware log2 below
+        const float e1 = (u > 0.99f) ? fmaf(om * om, 0.5f + om * (1.0f / 3.0f), om)
+                                     : -0.69314718f * fast_log2(u);
         const float g = -0.69314718f * fast_log2(e1);
-        const bool c = (u > kUExact) || (g > (best0 - lz[j]) - kGumbelSlack);
-        cand |= ((need >> j) & 1u) & (c ? 1u : 0u) ? (1u << j) : 0u;
+        ap[j] = ((need >> j) & 1u) ? lz[j] + g : -INFINITY;
+        amax = fmaxf(amax, ap[j]);
     }
-    // Exact fp32 score for the candidates, in increasing column order; lanes
-    // with candidates work through theirs together.
-    while (__any_sync(0xFFFFFFFFu, cand != 0)) {
+    // Deferred exact evaluation.  Invariant: the exact best of the columns
+    // seen so far is either among those evaluated exactly (gbest, gidx) or is
+    // the kept column (kj).  Every column whose estimate is more than
+    // 2 kGumbelSlack below the best estimate seen (apb) is more than
+    // kGumbelSlack below the exact score of the column holding apb, so it
+    // cannot be the exact best and is dropped.
+    const float apb_new = fmaxf(st.apb, amax);
+    const float thr = apb_new - 2.0f * kGumbelSlack;
+    uint32_t cand = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) cand |= (ap[j] > thr ? 1u : 0u) << j;
+    const bool keep_alive = st.kj >= 0 && st.apb > thr;   // the kept column still contends
+    if (!keep_alive) st.kj = -1;
+    st.apb = apb_new;
+    const bool fast = (__popc(cand) <= 1) && !(keep_alive && cand != 0);
+    if (fast) {
+        // at most one contender in this chunk and none left over: keep it
         if (cand != 0) {
             const int j = __ffs(cand) - 1;
-            cand &= cand - 1u;
             uint32_t wj = w[0];
             float xj = x[0];
 #pragma unroll
             for (int t = 1; t < 16; ++t)
                 if (t == j) { wj = w[t]; xj = x[t]; }
-            const float g = gumbel_from_bits(wj);
-            const float sc = __fmaf_rn(xj, fc.invT, g);
-            if (sc > st.gbest) { st.gbest = sc; st.gidx = static_cast<int>(v0) + j; }
+            st.kj = static_cast<int>(v0) + j;
+            st.kw = wj;
+            st.kx = xj;
         }
+    }
+    // near ties (rare): evaluate every contender exactly, then nothing is kept
+    uint32_t slow = fast ? 0u : cand;
+    const bool flush_kept = !fast && st.kj >= 0;
+    if (flush_kept) {
+        const float sc = exact_gumbel_score(st.kx, fc.invT, st.kw);
+        if (sc > st.gbest || (sc == st.gbest && st.kj < st.gidx)) { st.gbest = sc; st.gidx = st.kj; }
+        st.kj = -1;
+    }
+    while (__any_sync(0xFFFFFFFFu, slow != 0)) {
+        if (slow != 0) {
+            const int j = __ffs(slow) - 1;
+            slow &= slow - 1u;
+            uint32_t wj = w[0];
+            float xj = x[0];
+#pragma unroll
+            for (int t = 1; t < 16; ++t)
+                if (t == j) { wj = w[t]; xj = x[t]; }
+            const float sc = exact_gumbel_score(xj, fc.invT, wj);
+            const int idx = static_cast<int>(v0) + j;
+            if (sc > st.gbest || (sc == st.gbest && idx < st.gidx)) { st.gbest = sc; st.gidx = idx; }
+        }
+    }
+}
+
+// Resolve the kept column (evaluate it exactly) before the state is stored.
+DG_DEVICE void row_state_finalize(RowState &st, const FoldConsts &fc)
+{
+    if (st.kj >= 0) {
+        const float sc = exact_gumbel_score(st.kx, fc.invT, st.kw);
+        if (sc > st.gbest || (sc == st.gbest && st.kj < st.gidx)) { st.gbest = sc; st.gidx = st.kj; }
+        st.kj = -1;
     }
 }
 

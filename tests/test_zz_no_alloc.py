@@ -55,7 +55,7 @@ def test_noalloc_step_matches_workspace_step_on_two_consecutive_calls():
 
 def test_noalloc_rejects_steps_beyond_its_scratch():
     lib = dg.lib()
-    # 16 canvases of 1024 positions need far more than the 4 MiB scratch
+    # 16 canvases of 1024 positions need far more than the 8 MiB scratch
     p = dg.step_params(16, 1024, 1024, 16384, 0.8)
     bufs = dg.StepBuffers(1, 8, DEV)          # never touched: the call is rejected first
     x = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
