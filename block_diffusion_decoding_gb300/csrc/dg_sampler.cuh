@@ -112,7 +112,9 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     float cmax = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        x[j] = (live && (full || (v0 + j < V))) ? lg[j] : -INFINITY;
+        // ignored entries get a finite sentinel: their exponentials underflow
+        // to exactly 0 and no -inf * 0 can appear below
+        x[j] = (live && (full || (v0 + j < V))) ? lg[j] : -1.0e30f;
         cmax = fmaxf(cmax, x[j]);
     }
     if (!__any_sync(0xFFFFFFFFu, live)) return;
@@ -141,8 +143,8 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     for (int j = 0; j < 16; ++j) {
         const float dlt = fmaf(x[j], fc.c2, -st.m);
         const float e = fast_exp2(dlt);         // 0 for ignored entries
-        es[j] = (e > 0.f) ? e : 0.f;
-        as[j] = (e > 0.f) ? e * dlt : 0.f;
+        es[j] = e;
+        as[j] = e * dlt;
     }
 #pragma unroll
     for (int h = 8; h >= 1; h >>= 1) {
@@ -162,13 +164,13 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     // the exact best is at least max(gbest, apb - slack)
     const float lim = fmaxf(st.gbest, st.apb - 2.0f * kGumbelSlack) - kGumbelMaxPlusSlack;
     float lz[16];
-    uint32_t need = 0;
+    bool need = false;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         lz[j] = x[j] * fc.invT;
-        need |= (lz[j] > lim ? 1u : 0u) << j;
+        need |= lz[j] > lim;
     }
-    if (!__any_sync(0xFFFFFFFFu, need != 0)) return;
+    if (!__any_sync(0xFFFFFFFFu, need)) return;
     uint32_t w[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -193,7 +195,7 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         const float e1 = (u > 0.99f) ? fmaf(om * om, 0.5f + om * (1.0f / 3.0f), om)
                                      : -0.69314718f * fast_log2(u);
         const float g = -0.69314718f * fast_log2(e1);
-        ap[j] = ((need >> j) & 1u) ? lz[j] + g : -INFINITY;
+        ap[j] = lz[j] + g;   // columns stage 1 ruled out cannot win anyway
         amax = fmaxf(amax, ap[j]);
     }
     // Deferred exact evaluation.  Invariant: the exact best of the columns
@@ -205,8 +207,10 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     const float apb_new = fmaxf(st.apb, amax);
     const float thr = apb_new - 2.0f * kGumbelSlack;
     uint32_t cand = 0;
+    if (amax > thr) {   // only a chunk that reaches the contending range has candidates
 #pragma unroll
-    for (int j = 0; j < 16; ++j) cand |= (ap[j] > thr ? 1u : 0u) << j;
+        for (int j = 0; j < 16; ++j) cand |= (ap[j] > thr ? 1u : 0u) << j;
+    }
     const bool keep_alive = st.kj >= 0 && st.apb > thr;   // the kept column still contends
     if (!keep_alive) st.kj = -1;
     st.apb = apb_new;
