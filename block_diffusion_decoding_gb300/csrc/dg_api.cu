@@ -13,13 +13,13 @@
 #include <vector>
 
 #include "dg_kernels.h"
+#include "dg_plan.h"
 
 using namespace dg;
 
 namespace {
 
 // ---------------------------------------------------------------- small utilities
-constexpr int kMaxSlots = 256;       // upper bound on LM-head CTAs (>= SM count)
 constexpr int kAssumedMaxSMs = 256;  // workspace queries do not touch the GPU
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -71,6 +71,9 @@ int current_device_info(DeviceInfo **out)
     if (!di.attrs_set) {
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kLmSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPairSmemBytes));
         DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d128,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          attn_smem_bytes(128)));
@@ -126,51 +129,6 @@ int make_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
-}
-
-// ---------------------------------------------------------------- LM-head plan
-struct LmPlan {
-    int M, V, d;
-    int BN, ntn, mblocks, total, n_slots;
-};
-
-// Pick the tile width: fewest columns on the busiest CTA, plus a per-tile
-// overhead (re-reading the hidden block, epilogue start-up).
-LmPlan plan_lm_head(int M, int d, int V, int sms)
-{
-    LmPlan p{};
-    p.M = M;
-    p.V = V;
-    p.d = d;
-    p.mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
-    const char *env = std::getenv("DG_LM_BN");
-    const int forced = env ? std::atoi(env) : 0;
-    long best = -1;
-    for (int bn = 128; bn >= 64; bn -= 16) {
-        if (forced && bn != forced) continue;
-        const int ntn = (V + bn - 1) / bn;
-        const int total = ntn * p.mblocks;
-        const int slots = std::min(std::min(total, sms), kMaxSlots);
-        const long per_cta = (total + slots - 1) / slots;
-        const long cost = per_cta * (bn + 40);
-        if (best < 0 || cost < best) {
-            best = cost;
-            p.BN = bn;
-            p.ntn = ntn;
-            p.total = total;
-            p.n_slots = slots;
-        }
-    }
-    return p;
-}
-
-// Upper bound on the slot count of any plan for these shapes (workspace
-// queries do not know the SM count; every plan uses at most this many).
-int slot_bound(int M, int V)
-{
-    const long mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
-    const long tiles = mblocks * ((V + 63) / 64);
-    return static_cast<int>(std::min<long>(tiles, kMaxSlots)) * kLmColGroups;
 }
 
 // Workspace layout of one step: header | partials (7 x n_slots x M x 4 B) |
@@ -276,7 +234,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
                                       static_cast<uint64_t>(x_steps)};
             const uint64_t strides[2] = {static_cast<uint64_t>(p->d) * 2,
                                          static_cast<uint64_t>(hidden_stride) * 2};
-            const uint32_t box[3] = {64, 256, 1};
+            const uint32_t box[3] = {64, plan.pair ? 128u : 256u, 1};
             const int rank = x_steps > 1 ? 3 : 2;
             int rc = make_map_bf16(&mx, hidden, rank, dims, strides, box);
             if (rc != DG_OK) return rc;
@@ -304,7 +262,10 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.ws = ws.hdr;
         a.counters = ws.counters;
         a.ncounters = p->B;
-        lm_head_kernel<<<plan.n_slots, kLmThreads, kLmSmemBytes, st>>>(mx, mw, a);
+        if (plan.pair)
+            lm_head_pair_kernel<<<plan.grid, kLmThreads, kPairSmemBytes, st>>>(mx, mw, a);
+        else
+            lm_head_kernel<<<plan.grid, kLmThreads, kLmSmemBytes, st>>>(mx, mw, a);
         DG_LAUNCHED();
     } else {
         FoldArgs f{};
@@ -313,13 +274,13 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         f.BN = plan.BN;
         f.ntn = plan.ntn;
         f.total = plan.total;
-        f.n_slots = plan.n_slots;
+        f.n_slots = plan.units;
         f.part = ws.part;
         f.src = src;
         f.seed = p->seed;
         f.counters = ws.counters;
         f.ncounters = p->B;
-        logits_fold_kernel<<<plan.n_slots, 256, 0, st>>>(logits, f);
+        logits_fold_kernel<<<plan.units, 256, 0, st>>>(logits, f);
         DG_LAUNCHED();
     }
     DG_CUDA_TRY(cudaGetLastError());
@@ -328,8 +289,8 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     c.part = ws.part;
     // the LM head writes one partial state per (CTA, column group); the
     // logits fold one per CTA
-    c.spc = (logits == nullptr) ? kLmColGroups : 1;
-    c.n_slots = plan.n_slots * c.spc;
+    c.spc = (logits == nullptr) ? plan.spc : 1;
+    c.n_slots = plan.units * c.spc;
     c.ntn = plan.ntn;
     c.total = plan.total;
     c.M = M;
@@ -591,7 +552,7 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
+    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
@@ -612,7 +573,7 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
+    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
     const StepSource src = step_source(p);
     AcceptArgs acc{};
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, nullptr, nullptr, nullptr,
@@ -642,7 +603,7 @@ int dg_sampler_from_logits(const float *logits, const dg_step_params *p, const d
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, 64, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
+    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
     return enqueue_step(nullptr, 0, 1, logits, nullptr, p, plan, ws, src, io->entropy, io->sample,
@@ -699,7 +660,7 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
     size_t off_ctl, off_scr;
     block_ws_layout(p, slot_bound(M, p->V), &off_ctl, &off_scr);
     uint8_t *base = static_cast<uint8_t *>(workspace);
-    StepWs ws = carve_step_ws(workspace, M, plan.n_slots * kLmColGroups);
+    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
     LoopCtl *ctl = reinterpret_cast<LoopCtl *>(base + off_ctl);
     uint8_t *sp = base + off_scr;
     const size_t m4 = round_up(static_cast<size_t>(M) * 4, 256);
@@ -728,7 +689,7 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
         static_cast<uint64_t>(p->L), static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->V),
         f2u(p->entropy_bound), f2u(p->stop_threshold), d2u(bp->t_start), d2u(bp->t_end), p->seed,
         static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(bp->hidden_step_stride),
-        static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.n_slots),
+        static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.grid * 2 + (plan.pair ? 1 : 0)),
         static_cast<uint64_t>(dev)};
 
     BlockGraph *bgp = nullptr;

@@ -79,6 +79,17 @@ constexpr int kLmSmemBytes = kLmStages * kLmStageBytes + 1024 + 256;
 
 __global__ void lm_head_kernel(const __grid_constant__ CUtensorMap map_x,
                                const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+
+// 2-CTA cluster variant: CTA rank r of a cluster owns rows [128 r, 128 r + 128)
+// of each 256-row block and all BN (128 or 256) columns of the cluster's
+// tiles; the W tile is multicast to both CTAs, each loading half of it.
+constexpr int kPairABytes = 128 * kLmBK * 2;             // 16 KB: X rows of this CTA
+constexpr int kPairStageBytes = kPairABytes + 4 * kLmBBoxBytes;   // + up to 256 W columns
+constexpr int kPairStages = 4;
+constexpr int kPairColGroups = 4;                        // epilogue warps per TMEM quadrant
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024 + 256;
+__global__ void lm_head_pair_kernel(const __grid_constant__ CUtensorMap map_x,
+                                    const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 __global__ void logits_fold_kernel(const float *__restrict__ logits, FoldArgs a);
 __global__ void combine_accept_kernel(CombineArgs c, AcceptArgs a);
 __global__ void accept_only_kernel(const float *__restrict__ H, const int32_t *__restrict__ sample,

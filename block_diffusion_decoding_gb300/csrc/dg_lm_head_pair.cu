@@ -1,0 +1,210 @@
+// dg_lm_head_pair.cu -- the LM head of the denoising step on clusters of two
+// CTAs, for large vocabularies (the full-vocabulary softmax the "Parallel
+// Denoising From an Autoregressive Checkpoint" page, section "Finding",
+// names as a per-step cost).
+//
+// The two CTAs of a cluster work in lockstep on the same tiles (256 canvas
+// rows x BN vocabulary columns, BN = 128 or 256).  CTA rank r owns rows
+// [128 r, 128 r + 128) of the row block: it streams its own half of the
+// hidden block (X, K-major) and half of the W tile, which it multicasts into
+// the shared memory of both CTAs, so every W byte leaves L2 once for two SMs.
+// Each CTA then issues one 128 x BN x 16 UMMA per 16-deep k step into its own
+// double-buffered TMEM accumulator (2 x BN <= 512 columns) and folds the
+// finished accumulator exactly like the single-CTA kernel (dg_lm_head.cu).
+//
+//   warp 0      TMA producer: X[128 rows, 64] locally, W[64, BN/2] multicast;
+//               a stage is free once both CTAs' UMMAs have read it (the
+//               empty barrier takes one multicast commit from each CTA);
+//   warp 1      TMEM allocator + UMMA issuer;
+//   warps 4-19  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, every
+//               4th 16-column chunk starting at chunk (w - 4) / 4, and keeps
+//               its own partial state (slot 4 cluster + (w - 4) / 4).
+#include "dg_kernels.h"
+
+namespace dg {
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+    lm_head_pair_kernel(const __grid_constant__ CUtensorMap map_x,
+                        const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kPairStages * kPairStageBytes);
+    uint64_t *empty = full + kPairStages;
+    uint64_t *acc_full = empty + kPairStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = static_cast<int>(cluster_ctarank());          // row half
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(num_clusters_x());
+    const int t0 = tile_begin(cid, a.total, ncl), t1 = tile_begin(cid + 1, a.total, ncl);
+    const int ntiles = t1 - t0;
+    const int half_boxes = a.BN / 128;                           // W boxes this CTA loads
+
+    if (cid == 0 && r == 0 && warp == 2) {
+        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
+    }
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 2);          // one commit from each CTA of the pair
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], kLmEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&map_x);
+        tma_prefetch_desc(&map_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // both CTAs' barriers exist before either multicasts into the other
+    cluster_sync_all();
+    const uint32_t tmem_base = *tmem_slot;
+    const FoldConsts fc = fold_consts(a.src, a.seed);
+    const int xstep = a.x_3d ? static_cast<int>(fc.step) : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            const uint32_t tx = static_cast<uint32_t>(kPairABytes + 2 * half_boxes * kLmBBoxBytes);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int t = t0; t < t1 && ok; ++t) {
+                const int m = t / a.ntn, n = t % a.ntn;
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, a.ws, 301)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], tx);
+                    uint8_t *sa = smem + s * kPairStageBytes;
+                    uint8_t *sb = sa + kPairABytes;
+                    // the block loop passes hidden states with a step coordinate (3-D map)
+                    if (a.x_3d)
+                        tma_load_3d(sa, &map_x, &full[s], kb * kLmBK, m * kRowsPerBlock + r * 128,
+                                    xstep, pol_x);
+                    else
+                        tma_load_2d(sa, &map_x, &full[s], kb * kLmBK, m * kRowsPerBlock + r * 128,
+                                    pol_x);
+                    for (int j = 0; j < half_boxes; ++j) {
+                        const int jb = r * half_boxes + j;
+                        tma_load_2d_multicast(sb + jb * kLmBBoxBytes, &map_w, &full[s],
+                                              n * a.BN + jb * 64, kb * kLmBK, 0x3, pol_w);
+                    }
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == kPairStages) { s = 0; ph ^= 1u; }
+                }
+            }
+            // everything addressed to this CTA (own and peer copies) has landed
+            for (int q = 0; q < kPairStages; ++q)
+                if (armed >> q & 1u) mbar_wait(&full[q], armed_par >> q & 1u, a.ws, 302);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc_bf16(128, a.BN, 1);
+            const uint32_t sa0 = smem_u32(smem);
+            const uint64_t adesc0 = make_sdesc_sw128(sa0, 16, 1024);
+            const uint64_t bdesc0 = make_sdesc_sw128(sa0 + kPairABytes, kLmBBoxBytes, 1024);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int acc = i & 1;
+                const uint32_t use = static_cast<uint32_t>(i >> 1);
+                if (!mbar_wait(&acc_empty[acc], (use & 1u) ^ 1u, a.ws, 303)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * a.BN);
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&full[s], ph, a.ws, 304)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t soff = static_cast<uint64_t>((s * kPairStageBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kLmBK / 16; ++kk) {
+                        // A: K-major 128-byte rows, 8-row groups 1 KB apart, +32 B per k step;
+                        // B: MN-major, 64-column blocks 8 KB apart, 8-row groups 1 KB apart
+                        const uint64_t adesc = adesc0 + soff + static_cast<uint64_t>(kk * 2);
+                        const uint64_t bdesc = bdesc0 + soff + static_cast<uint64_t>(kk * (2048 >> 4));
+                        umma_bf16(d, adesc, bdesc, idesc, (kb | kk) != 0);
+                    }
+                    umma_commit_multicast(&empty[s], 0x3);
+                    if (++s == kPairStages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[acc]);
+            }
+            umma_commit(mma_done);
+            mbar_wait(mma_done, 0, a.ws, 305);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int cg = (warp - 4) >> 2;          // column group
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const size_t slot = static_cast<size_t>(cid) * kPairColGroups + cg;
+        RowState st;
+        row_state_init(st);
+        int cur_m = -1;
+        for (int i = 0; i < ntiles; ++i) {
+            const int t = t0 + i;
+            const int m = t / a.ntn, n = t % a.ntn;
+            const int acc = i & 1;
+            const uint32_t use = static_cast<uint32_t>(i >> 1);
+            if (m != cur_m) {
+                if (cur_m >= 0) {
+                    const int prow = cur_m * kRowsPerBlock + r * 128 + q * 32 + lane;
+                    row_state_finalize(st, fc);
+                    if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
+                }
+                row_state_init(st);
+                cur_m = m;
+            }
+            const bool ok = mbar_wait(&acc_full[acc], use & 1u, a.ws, 306);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            const int row = m * kRowsPerBlock + r * 128 + q * 32 + lane;
+            const bool live = row < a.M;
+            const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * a.BN);
+#pragma unroll 1
+            for (int c0 = 16 * cg; c0 < a.BN; c0 += 16 * kPairColGroups) {
+                float lg[16];
+                tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
+                const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
+                if (v0 < static_cast<uint32_t>(a.V))
+                    fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+        if (cur_m >= 0) {
+            const int prow = cur_m * kRowsPerBlock + r * 128 + q * 32 + lane;
+            row_state_finalize(st, fc);
+            if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+    // neither CTA leaves while the other may still write into it
+    cluster_sync_all();
+}
+
+}  // namespace dg

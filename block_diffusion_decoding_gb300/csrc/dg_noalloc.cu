@@ -40,6 +40,7 @@
 #include <mutex>
 
 #include "dg_kernels.h"
+#include "dg_plan.h"
 
 using namespace dg;
 
@@ -78,6 +79,8 @@ int na_setup(NoAllocDevice **out)
             cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kLmSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(lm_head_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) != cudaSuccess ||
             cudaMemset(ptr, 0, sizeof(WsHeader)) != cudaSuccess) {
             (void)cudaGetLastError();
             return DG_ERR_CUDA;
@@ -143,30 +146,13 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     int rc = na_setup(&st);
     if (rc != DG_OK) return rc;
 
-    // ---- tile plan: the same choice as dg_denoise_step
+    // ---- kernel and tile plan: the same choice as dg_denoise_step
     const int M = p->B * p->L;
-    const int mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
-    const char *env = std::getenv("DG_LM_BN");
-    const int forced = env ? std::atoi(env) : 0;
-    int BN = 0, ntn = 0, total = 0, slots = 0;
-    long best = -1;
-    for (int bn = 128; bn >= 64; bn -= 16) {
-        if (forced && bn != forced) continue;
-        const int n = (p->V + bn - 1) / bn;
-        const int t = n * mblocks;
-        const int s = std::min(std::min(t, st->sms), 256);
-        const long cost = static_cast<long>((t + s - 1) / s) * (bn + 40);
-        if (best < 0 || cost < best) {
-            best = cost;
-            BN = bn;
-            ntn = n;
-            total = t;
-            slots = s;
-        }
-    }
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, st->sms);
+    const int BN = plan.BN, ntn = plan.ntn, total = plan.total;
 
     // ---- scratch layout (as a workspace): header | partials | counters
-    const size_t npart = static_cast<size_t>(slots) * kLmColGroups * M;
+    const size_t npart = static_cast<size_t>(plan.part_slots()) * M;
     const size_t need = sizeof(WsHeader) + na_round_up(7 * npart * 4, 256) +
                         na_round_up(static_cast<size_t>(p->B) * 4, 256);
     if (need > kNoAllocScratchBytes) return DG_ERR_UNSUPPORTED;
@@ -184,7 +170,8 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     int *counters = reinterpret_cast<int *>(base + sizeof(WsHeader) + na_round_up(7 * npart * 4, 256));
 
     CUtensorMap mx, mw;
-    if ((rc = na_map(&mx, hidden, static_cast<uint64_t>(p->d), static_cast<uint64_t>(M), 64, 256)) != DG_OK)
+    if ((rc = na_map(&mx, hidden, static_cast<uint64_t>(p->d), static_cast<uint64_t>(M), 64,
+                     plan.pair ? 128u : 256u)) != DG_OK)
         return rc;
     if ((rc = na_map(&mw, w, static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d), 64, 64)) != DG_OK)
         return rc;
@@ -214,8 +201,8 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
 
     CombineArgs c{};
     c.part = part;
-    c.n_slots = slots * kLmColGroups;
-    c.spc = kLmColGroups;
+    c.n_slots = plan.part_slots();
+    c.spc = plan.spc;
     c.ntn = ntn;
     c.total = total;
     c.M = M;
@@ -240,7 +227,10 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     acc.stop = io->stop;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    lm_head_kernel<<<slots, kLmThreads, kLmSmemBytes, s>>>(mx, mw, a);
+    if (plan.pair)
+        lm_head_pair_kernel<<<plan.grid, kLmThreads, kPairSmemBytes, s>>>(mx, mw, a);
+    else
+        lm_head_kernel<<<plan.grid, kLmThreads, kLmSmemBytes, s>>>(mx, mw, a);
     if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
     combine_accept_kernel<<<dim3((p->L + 7) / 8, p->B), 256, 0, s>>>(c, acc);
     if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
