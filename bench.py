@@ -216,9 +216,9 @@ def _config_json(cfg, l2):
 
 
 # ----------------------------------------------------------------------------- our arm
-def _traffic_record(kernel_sources):
+def _traffic_record(kernel_sources, kernel):
     """Per-launch DRAM bytes of the LM-head kernel from the committed ncu summary,
-    valid only while the kernel sources are unchanged."""
+    valid only while the kernel sources are unchanged and for the same kernel."""
     path = os.path.join(ROOT, "profiles", "lm_head_kernel_step_full.md")
     if not os.path.exists(path):
         return None
@@ -233,7 +233,7 @@ def _traffic_record(kernel_sources):
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
                 rec[k.strip()] = v.strip()
-    if rec.get("source_sha256_16") != digest:
+    if rec.get("source_sha256_16") != digest or rec.get("kernel") != kernel:
         return None
     try:
         return float(rec["dram_bytes_per_launch"])
@@ -337,9 +337,11 @@ def run_ours(args, cfg):
     lm_flops = 2.0 * M * d * V
     at_flops = 4.0 * B * Hq * L * (P + L) * D
     at_bytes = 2 * (B * L * Hq * D * 2) + 2 * (B * (P + L) * Hkv * D * 2)
+    lm_plan = dg.lm_head_plan(M, d, V)
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
-            for f in ("dg_lm_head.cu", "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
-    traffic = _traffic_record(srcs)
+            for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_plan.h", "dg_sampler.cuh",
+                      "dg_device.cuh", "dg_kernels.h")]
+    traffic = _traffic_record(srcs, lm_plan["kernel"])
 
     # ---- end to end through the C ABI with host buffers (pinned), per-step H2D + D2H
     h_x = x.cpu().pin_memory()
@@ -403,11 +405,12 @@ def run_ours(args, cfg):
         data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step"),
         canvas_tokens_per_s=value * M,
         roofline=dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
-                      frac=lm_gbs / hbm_peak, traffic=traffic, kernel="lm_head_kernel",
+                      frac=lm_gbs / hbm_peak, traffic=traffic, kernel=lm_plan["kernel"],
                       peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
                       algorithmic_bytes=lm_bytes),
-        kernels={"lm_head_kernel": {"ms": lm_ms, "GB_per_s": lm_gbs,
-                                    "TFLOP_per_s": lm_flops / (lm_ms * 1e-3) / 1e12},
+        kernels={lm_plan["kernel"]: {"ms": lm_ms, "GB_per_s": lm_gbs,
+                                     "TFLOP_per_s": lm_flops / (lm_ms * 1e-3) / 1e12,
+                                     "BN": lm_plan["BN"], "ctas": lm_plan["ctas"]},
                  "canvas_attn": {"ms": at_ms, "TFLOP_per_s": at_flops / (at_ms * 1e-3) / 1e12,
                                  "frac_of_bf16_peak": at_flops / (at_ms * 1e-3) / 1e12 / bf16_peak,
                                  "GB_per_s": at_bytes / (at_ms * 1e-3) / 1e9}},

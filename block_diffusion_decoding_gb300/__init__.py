@@ -30,7 +30,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_denoise_step_workspace", "dg_denoise_step", "dg_denoise_step_noalloc",
             "dg_generate_block_workspace", "dg_generate_block",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
-            "dg_lm_head_fold", "dg_kernel_launches", "dg_gumbel_fill", "dg_logf_eval"]
+            "dg_lm_head_fold", "dg_kernel_launches", "dg_lm_head_plan", "dg_gumbel_fill",
+            "dg_logf_eval"]
 
 
 class DgError(RuntimeError):
@@ -77,6 +78,7 @@ def _lib():
                                       ctypes.c_uint64, ctypes.c_size_t, ctypes.c_float)
         sp, si, bp, bi = (ctypes.POINTER(StepParams), ctypes.POINTER(StepIO),
                           ctypes.POINTER(BlockParams), ctypes.POINTER(BlockIO))
+        ip = ctypes.POINTER(ctypes.c_int)
         sig = {
             "dg_status_string": ([i32], ctypes.c_char_p),
             "dg_version": ([], i32),
@@ -93,6 +95,7 @@ def _lib():
             "dg_accept_renoise": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
             "dg_lm_head_fold": ([vp, vp, sp, vp, sz, vp], i32),
             "dg_kernel_launches": ([], u64),
+            "dg_lm_head_plan": ([i32, i32, i32, ip, ip, ip], i32),
             "dg_gumbel_fill": ([u64, u32, u32, u32, i32, vp, vp], i32),
             "dg_logf_eval": ([vp, vp, i32, vp], i32),
         }
@@ -184,6 +187,15 @@ def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):
     rc = _lib().dg_lm_head_fold(_p(hidden), _p(w), ctypes.byref(p), _p(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "dg_lm_head_fold")
+
+
+def lm_head_plan(rows: int, d: int, V: int) -> dict:
+    """The LM-head launch the step would make on the current device."""
+    cl, bn, ctas = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = _lib().dg_lm_head_plan(rows, d, V, ctypes.byref(cl), ctypes.byref(bn), ctypes.byref(ctas))
+    _check(rc, "dg_lm_head_plan")
+    return {"kernel": "lm_head_pair_kernel" if cl.value == 2 else "lm_head_kernel",
+            "cluster_ctas": cl.value, "BN": bn.value, "ctas": ctas.value}
 
 
 def kernel_launches() -> int:

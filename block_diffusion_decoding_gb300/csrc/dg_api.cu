@@ -310,6 +310,15 @@ struct AttnPlan {
     int BKV, nkt_p, nkt_c, nkt, mtiles, blocks, nsplit, tps;
 };
 
+// Largest split count any plan may take: enough CTAs for two waves on a GPU
+// with kAssumedMaxSMs SMs, and at most one KV tile per split.  The workspace
+// query sizes the split partials with it.
+int attn_split_cap(int blocks, int nkt)
+{
+    const int cap = (2 * kAssumedMaxSMs + blocks - 1) / blocks;
+    return std::max(1, std::min(cap, nkt));
+}
+
 AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
 {
     AttnPlan a{};
@@ -320,11 +329,13 @@ AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
     const int G = Hq / Hkv;
     a.mtiles = (L * G + 127) / 128;
     a.blocks = a.mtiles * Hkv * B;
-    // splits: minimise (waves x tiles per split), preferring fewer splits
+    // splits: minimise (waves x tiles per split), preferring fewer splits;
+    // never more than two waves' worth of CTAs on the largest GPU
     long best = -1;
     const char *env = std::getenv("DG_ATTN_SPLITS");
     const int forced = env ? std::atoi(env) : 0;
-    for (int ns = 1; ns <= a.nkt; ++ns) {
+    const int cap = attn_split_cap(a.blocks, a.nkt);
+    for (int ns = 1; ns <= cap; ++ns) {
         const int tps = (a.nkt + ns - 1) / ns;
         const int real = (a.nkt + tps - 1) / tps;
         if (real != ns) continue;
@@ -423,13 +434,12 @@ size_t dg_canvas_attn_workspace(int B, int L, int P, int Hq, int Hkv, int D)
         return 0;
     const int G = Hq / Hkv;
     if (G > 16 || (G & (G - 1)) != 0) return 0;
-    // the split count depends on the SM count: take the largest over any GPU
-    size_t mx = 0;
-    for (int sms = 1; sms <= kAssumedMaxSMs; ++sms) {
-        const AttnPlan q = plan_attn(B, L, P, Hq, Hkv, D, sms);
-        mx = std::max(mx, attn_ws_bytes(B, L, Hq, D, q.nsplit));
-    }
-    return mx;
+    // the split count depends on the SM count: size for the largest allowed
+    const int BKV = (D == 128) ? 128 : 64;
+    const int nkt = (P + BKV - 1) / BKV + (L + BKV - 1) / BKV;
+    const long blocks = static_cast<long>((L * G + 127) / 128) * Hkv * B;
+    const int cap = attn_split_cap(static_cast<int>(std::min<long>(blocks, 1 << 30)), nkt);
+    return attn_ws_bytes(B, L, Hq, D, cap);
 }
 
 int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
@@ -581,6 +591,21 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 }
 
 uint64_t dg_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int dg_lm_head_plan(int rows, int d, int V, int *cluster_ctas, int *bn, int *ctas)
+{
+    if (rows < 1 || d < 1 || V < 1) return DG_ERR_INVALID_ARG;
+    if (rows > (1 << 20) || V % 8 != 0 || V < 64) return DG_ERR_UNSUPPORTED;
+    if (d % 64 != 0 || d > 16384) return DG_ERR_UNSUPPORTED;
+    DeviceInfo *di = nullptr;
+    const int rc = current_device_info(&di);
+    if (rc != DG_OK) return rc;
+    const LmPlan plan = plan_lm_head(rows, d, V, di->sms);
+    if (cluster_ctas) *cluster_ctas = plan.pair ? 2 : 1;
+    if (bn) *bn = plan.BN;
+    if (ctas) *ctas = plan.grid;
+    return DG_OK;
+}
 
 // ---------------------------------------------------------------- sampler on given logits
 size_t dg_sampler_workspace(const dg_step_params *p)

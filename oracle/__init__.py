@@ -182,15 +182,29 @@ def sampler_row(logits_row: np.ndarray, T: float, seed: int, row: int, step: int
                 gumbel_margin=gm.value, argmax_margin=amm.value)
 
 
-def sampler(logits_rows: np.ndarray, T: float, seed: int, rows: Sequence[int], step: int) -> dict:
-    """Run sampler_row over a block of logits; rows[i] is the global row id of logits_rows[i]."""
+def sampler(logits_rows: np.ndarray, T: float, seed: int, rows: Sequence[int], step: int,
+            workers: int = 1) -> dict:
+    """Run sampler_row over a block of logits; rows[i] is the global row id of logits_rows[i].
+
+    Rows are independent; ``workers`` > 1 runs them on that many threads (the
+    C routine runs without the interpreter lock), with identical results.
+    """
     n = logits_rows.shape[0]
     res = dict(H=np.zeros(n), sample=np.zeros(n, np.int32), argmax=np.zeros(n, np.int32),
                gumbel_margin=np.zeros(n), argmax_margin=np.zeros(n))
-    for t in range(n):
+
+    def one(t):
         r = sampler_row(logits_rows[t], T, seed, int(rows[t]), step)
         for k in res:
             res[k][t] = r[k]
+
+    if workers > 1 and n > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(n)))
+    else:
+        for t in range(n):
+            one(t)
     return res
 
 
@@ -234,11 +248,11 @@ def attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, rows) -> np.nd
 # ---------------------------------------------------------------- step / block
 def step(x_bits: np.ndarray, w_bits: np.ndarray, canvas: np.ndarray, prev_argmax: np.ndarray,
          B: int, L: int, T: float, b: float, seed: int, k: int,
-         stop_threshold: float = 0.005) -> dict:
+         stop_threshold: float = 0.005, workers: int = 1) -> dict:
     """One denoising step (LM head -> sampler -> accept/renoise -> stop) for B canvases."""
     V = w_bits.shape[1]
     lg = logits(x_bits, w_bits)
-    s = sampler(lg, T, seed, np.arange(B * L), k)
+    s = sampler(lg, T, seed, np.arange(B * L), k, workers=workers)
     Hf = s["H"].astype(np.float32)
     new_canvas = np.array(canvas, dtype=np.int32, copy=True).reshape(B, L)
     accepted = np.zeros((B, L), np.uint8)
@@ -268,7 +282,7 @@ def step(x_bits: np.ndarray, w_bits: np.ndarray, canvas: np.ndarray, prev_argmax
 
 def block(hidden_bits_fn, w_bits: np.ndarray, B: int, L: int, b: float, seed: int,
           max_steps: int = 48, t0: float = 0.8, t1: float = 0.4,
-          stop_threshold: float = 0.005) -> dict:
+          stop_threshold: float = 0.005, workers: int = 1) -> dict:
     """The denoising loop of a batch of B independent canvases.
 
     [Lab] items 1-5: uniform init, per-step sample/accept/renoise, linear
@@ -288,7 +302,7 @@ def block(hidden_bits_fn, w_bits: np.ndarray, B: int, L: int, b: float, seed: in
     for k in range(max_steps):
         T = temperature(k, max_steps, t0, t1)
         r = step(hidden_bits_fn(k), w_bits, canvas.reshape(-1), prev.reshape(-1), B, L, T, b,
-                 seed, k, stop_threshold)
+                 seed, k, stop_threshold, workers=workers)
         am = r["argmax"].reshape(B, L)
         cv = r["canvas"].reshape(B, L)
         live = ~done

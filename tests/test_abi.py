@@ -108,3 +108,7 @@ def test_host_validation_rejects_before_launch(lib):
     # check entries
     assert lib.dg_logf_eval(None, None, -1, None) == 1
     assert lib.dg_gumbel_fill(0, 0, 0, 0, 0, None, None) == 0
+    # LM-head plan query: shapes the step rejects are rejected before any device call
+    assert lib.dg_lm_head_plan(0, 1024, 16384, None, None, None) == 1
+    assert lib.dg_lm_head_plan(256, 1000, 16384, None, None, None) == 2
+    assert lib.dg_lm_head_plan(256, 1024, 16380, None, None, None) == 2

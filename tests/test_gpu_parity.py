@@ -15,14 +15,10 @@ import torch
 import block_diffusion_decoding_gb300 as dg
 import dg_synth
 import oracle
-from tests._helpers import (ATTN_TOL, DEV, H_TOL, MARGIN, acceptance_is_decided, np_f, np_i32,
-                            to_dev)
+from tests._helpers import (ATTN_TOL, DEV, H_TOL, MARGIN, acceptance_is_decided,
+                            check_step_against_oracle, np_f, np_i32, status_ok, to_dev)
 
 pytestmark = pytest.mark.gpu
-
-
-def _status_ok(ws):
-    assert dg.read_device_status(ws) == 0
 
 
 # ------------------------------------------------------------------ primitives
@@ -104,7 +100,7 @@ def test_accept_renoise_stop_bit_exact(B, L, kind):
         assert np.array_equal(np_i32(bufs.prev_argmax)[sl], argmax[bb])
     if kind == "mixed" and L > 1:
         assert int(bufs.stop[0]) == 1 and int(bufs.n_accepted[0]) == L
-    _status_ok(ws)
+    status_ok(ws)
 
 
 def test_accept_step0_never_stops():
@@ -120,37 +116,6 @@ def test_accept_step0_never_stops():
 
 
 # ------------------------------------------------------------------ sampler on identical fp32 logits
-def _check_step_against_oracle(bufs, ref, B, L, exact_tokens):
-    H = np_f(bufs.entropy)
-    assert np.abs(H - ref["H"]).max() < H_TOL, np.abs(H - ref["H"]).max()
-    am, sm = np_i32(bufs.argmax), np_i32(bufs.sample)
-    if exact_tokens:
-        assert np.array_equal(am, ref["argmax"])
-        assert np.array_equal(sm, ref["sample"])
-    else:
-        ok = ref["argmax_margin"] >= MARGIN
-        assert ok.mean() > 0.9
-        assert np.array_equal(am[ok], ref["argmax"][ok])
-        ok = ref["gumbel_margin"] >= MARGIN
-        assert ok.mean() > 0.9
-        assert np.array_equal(sm[ok], ref["sample"][ok])
-    canvas, acc = np_i32(bufs.canvas), bufs.accepted.cpu().numpy()
-    checked = 0
-    for bb in range(B):
-        sl = slice(bb * L, (bb + 1) * L)
-        if not acceptance_is_decided(ref["H"][sl], int(ref["n_accepted"][bb]),
-                                     float(ref["boundary_gap"][bb])):
-            continue
-        checked += 1
-        assert int(bufs.n_accepted[bb]) == int(ref["n_accepted"][bb])
-        assert np.array_equal(acc[sl], ref["accepted"][sl])
-        # accepted positions hold the sample; every other one the renoise token
-        acc_ref = ref["accepted"][sl] == 1
-        if exact_tokens or bool(np.all(ref["gumbel_margin"][sl][acc_ref] >= MARGIN)):
-            assert np.array_equal(canvas[sl], ref["canvas"][sl])
-        else:
-            assert np.array_equal(canvas[sl][~acc_ref], ref["canvas"][sl][~acc_ref])
-    return checked
 
 
 @pytest.mark.parametrize("B,L,V,scale", [(1, 256, 16384, 1.0), (2, 256, 4096, 4.0),
@@ -171,7 +136,7 @@ def test_sampler_from_logits(B, L, V, scale):
     ws = dg.workspace(dg.sampler_workspace(p), DEV)
     dg.sampler_from_logits(torch.from_numpy(logits).to(DEV), p, bufs, ws)
     torch.cuda.synchronize()
-    _status_ok(ws)
+    status_ok(ws)
     s = oracle.sampler(logits.astype(np.float64), T, seed, np.arange(B * L), k)
     ref = dict(s)
     ref["canvas"] = np.zeros(B * L, np.int32)
@@ -185,7 +150,7 @@ def test_sampler_from_logits(B, L, V, scale):
         ref["canvas"][sl], ref["accepted"][sl] = a["canvas"], a["accepted"]
         ref["n_accepted"][bb], ref["boundary_gap"][bb] = a["n_accepted"], a["boundary_gap"]
     assert int(np_i32(bufs.argmax)[0]) == 5
-    _check_step_against_oracle(bufs, ref, B, L, exact_tokens=True)
+    check_step_against_oracle(bufs, ref, B, L, exact_tokens=True)
 
 
 # ------------------------------------------------------------------ fused LM head (tcgen05 GEMM + epilogue)
@@ -208,9 +173,9 @@ def test_denoise_step_matches_oracle(B, L, d, V, w_std, k):
     x, w = to_dev(xb), to_dev(wb)
     dg.denoise_step(x, w, p, bufs, ws)
     torch.cuda.synchronize()
-    _status_ok(ws)
+    status_ok(ws)
     ref = oracle.step(xb, wb, canvas0, prev, B, L, T, b, seed, k)
-    _check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+    check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
     # repeat: same result (deterministic)
     H1 = np_f(bufs.entropy).copy()
     bufs.canvas.copy_(torch.from_numpy(canvas0))
@@ -253,7 +218,7 @@ def _attn_case(B, L, P, Hq, Hkv, D, seed=0, row_stride=1):
     dg.canvas_attn(t["q"], t["kp"] if P else None, t["vp"] if P else None, t["kc"], t["vc"],
                    out, scale, ws)
     torch.cuda.synchronize()
-    _status_ok(ws)
+    status_ok(ws)
     rows = np.arange(0, B * L * Hq, row_stride)
     ref = oracle.attention_rows(ai["q"], ai["kp"], ai["vp"], ai["kc"], ai["vc"], B, L, P, Hq, Hkv,
                                 D, scale, rows)
@@ -311,7 +276,7 @@ def _run_block(hidden_bits_steps, wb, B, L, d, V, seed, max_steps=48, stride_ste
     ws = dg.workspace(dg.generate_block_workspace(p, bp), DEV)
     dg.generate_block(hid, to_dev(wb), p, bp, bufs, ws)
     torch.cuda.synchronize()
-    _status_ok(ws)
+    status_ok(ws)
     return bufs
 
 
