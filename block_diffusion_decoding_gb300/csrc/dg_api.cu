@@ -287,10 +287,8 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     if (lm_only) return DG_OK;
     CombineArgs c{};
     c.part = ws.part;
-    // the LM head writes one partial state per (CTA, column group); the
-    // logits fold one per CTA
-    c.spc = (logits == nullptr) ? plan.spc : 1;
-    c.n_slots = plan.units * c.spc;
+    // one partial state per (row, producer unit)
+    c.n_slots = plan.units;
     c.ntn = plan.ntn;
     c.total = plan.total;
     c.M = M;
@@ -329,8 +327,10 @@ AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
     const int G = Hq / Hkv;
     a.mtiles = (L * G + 127) / 128;
     a.blocks = a.mtiles * Hkv * B;
-    // splits: minimise (waves x tiles per split), preferring fewer splits;
-    // never more than two waves' worth of CTAs on the largest GPU
+    // splits: minimise the estimated time in key-tile units -- waves x (tiles
+    // per split + a fixed cost of about 3 tiles per CTA) + about 4 tiles for
+    // the split combine -- preferring fewer splits; never more than two
+    // waves' worth of CTAs on the largest GPU
     long best = -1;
     const char *env = std::getenv("DG_ATTN_SPLITS");
     const int forced = env ? std::atoi(env) : 0;
@@ -341,7 +341,7 @@ AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
         if (real != ns) continue;
         if (forced && ns != std::min(forced, a.nkt)) continue;
         const long waves = (static_cast<long>(a.blocks) * ns + sms - 1) / sms;
-        const long cost = waves * (tps + 2) * 16 + ns;
+        const long cost = (waves * (tps + 3) + (ns > 1 ? 4 : 0)) * 16 + ns;
         if (best < 0 || cost < best) {
             best = cost;
             a.nsplit = ns;
@@ -467,19 +467,7 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms);
     cudaStream_t st = as_stream(stream);
 
-    CUtensorMap mq, mkp, mvp, mkc, mvc;
-    {
-        // Q [B, L, Hq, D] as {D, G, Hkv, L, B}
-        const uint64_t dims[5] = {static_cast<uint64_t>(D), static_cast<uint64_t>(G),
-                                  static_cast<uint64_t>(Hkv), static_cast<uint64_t>(L),
-                                  static_cast<uint64_t>(B)};
-        const uint64_t strides[4] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(G) * D * 2,
-                                     static_cast<uint64_t>(Hq) * D * 2,
-                                     static_cast<uint64_t>(L) * Hq * D * 2};
-        const uint32_t box[5] = {64, static_cast<uint32_t>(G), 1, static_cast<uint32_t>(128 / G), 1};
-        rc = make_map_bf16(&mq, q, 5, dims, strides, box);
-        if (rc != DG_OK) return rc;
-    }
+    CUtensorMap mkp, mvp, mkc, mvc;
     auto kv_map = [&](CUtensorMap *m, const uint16_t *base, int rows) -> int {
         // [B, rows, Hkv, D] as {D, Hkv, rows, B}
         const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
@@ -514,6 +502,7 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     a.nkt_c = ap.nkt_c;
     a.tiles_per_split = ap.tps;
     a.scale_log2 = scale * 1.44269502162933349609375f;
+    a.q = q;
     a.out = out;
     a.ws = static_cast<WsHeader *>(workspace);
     if (ap.nsplit > 1) {
@@ -525,9 +514,9 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     }
     dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);
     if (D == 128)
-        attn_kernel_d128<<<grid, kAttnThreads, attn_smem_bytes(128), st>>>(mq, mkp, mvp, mkc, mvc, a);
+        attn_kernel_d128<<<grid, kAttnThreads, attn_smem_bytes(128), st>>>(mkp, mvp, mkc, mvc, a);
     else
-        attn_kernel_d256<<<grid, kAttnThreads, attn_smem_bytes(256), st>>>(mq, mkp, mvp, mkc, mvc, a);
+        attn_kernel_d256<<<grid, kAttnThreads, attn_smem_bytes(256), st>>>(mkp, mvp, mkc, mvc, a);
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     if (ap.nsplit > 1) {

@@ -8,22 +8,28 @@
 //
 // GQA folding: the G = Hq / Hkv query heads that share kv head g are folded
 // into the row dimension, so one 128-row tile holds 128 / G canvas positions
-// x G heads and every K/V tile is used by all of them.  The 5-D TMA map of
-// Q does the folding (box = 64 dims x G heads x 1 group x 128/G positions).
+// x G heads (row = position * G + head in group) and every K/V tile is used
+// by all of them.
 //
-// CTA (192 threads) = one 128-row query tile x one kv head x one batch
-// entry x one split of the key tiles:
-//   warp 0     TMA: Q once, then K and V tiles (prefix tiles, then canvas
-//              tiles) into a 2-stage ring, 128-byte swizzle;
-//   warp 1     TMEM allocator + UMMA issuer: S = Q K^T (K-major B) into one
-//              of two S buffers, and O += P V (V as MN-major B) into the O
-//              accumulator, software-pipelined so that S of tile j+1 is
-//              computed while the softmax works on tile j;
-//   warps 2-5  softmax, one query row per thread: reads S from TMEM, keeps
-//              a reference max that only moves when a tile's max exceeds it
-//              by more than 2^8 (then O is rescaled in TMEM), writes P as
-//              bf16 into shared memory in the UMMA A layout, and at the end
-//              normalises O (or writes unnormalised O, max, sum per split).
+// CTA (224 threads) = one 128-row query tile x one kv head x one batch
+// entry x one split of the key tiles.  Operands that the tensor core reads
+// from the A side live in tensor memory, so shared memory holds only the
+// K/V rings (7 tiles of 32 KB) and the UMMAs read one operand from it:
+//   TMEM        O [128 x D] fp32 | S0, S1 [128 x BKV] fp32 | Q [128 x D] bf16
+//               (the bf16 P of a tile overwrites the first BKV/2 columns of
+//               the S buffer it was computed from);
+//   warp 0      TMA: K tiles (prefix tiles, then canvas tiles) into a
+//               4-stage ring, released as soon as S = Q K^T has read them;
+//   warp 6      TMA: V tiles into a 3-stage ring, released after O += P V;
+//   warp 1      TMEM allocator + UMMA issuer, order S(0), S(1), PV(0), S(2),
+//               PV(1), ...: S of tile j+1 is computed while the softmax
+//               works on tile j, PV of tile j follows as soon as P(j) is in;
+//   warps 2-5   load the Q rows into TMEM, then softmax, one query row per
+//               thread: read S, keep a reference max that only moves when a
+//               tile's max exceeds it by more than 2^8 (then O is rescaled in
+//               TMEM, after the PV of the previous tile), write P as bf16
+//               pairs into TMEM, and at the end normalise O (or write
+//               unnormalised O, max and sum per split).
 #include "dg_kernels.h"
 
 namespace dg {
@@ -32,18 +38,19 @@ template <int D>
 struct AttnGeom {
     static constexpr int BKV = (D == 128) ? 128 : 64;      // keys per tile
     static constexpr int NA = D / 64;                      // 64-dim atoms
-    static constexpr int QBytes = 128 * D * 2;
-    static constexpr int KVBytes = BKV * D * 2;
+    static constexpr int KVBytes = BKV * D * 2;            // 32 KB
     static constexpr int KVAtomBytes = BKV * 128;          // one 64-dim atom
-    static constexpr int PBytes = 128 * BKV * 2;
-    static constexpr int OffQ = 0;
-    static constexpr int OffK = OffQ + QBytes;
-    static constexpr int OffV = OffK + 2 * KVBytes;
-    static constexpr int OffP = OffV + 2 * KVBytes;
-    static constexpr int OffBar = OffP + PBytes;
+    static constexpr int NK = 4;                           // K ring stages
+    static constexpr int NV = 3;                           // V ring stages
+    static constexpr int OffK = 0;
+    static constexpr int OffV = OffK + NK * KVBytes;
+    static constexpr int OffBar = OffV + NV * KVBytes;
     static constexpr int Smem = OffBar + 256 + 1024;
-    static constexpr int ColS = 0;                         // S buffers: [0, 2 BKV)
-    static constexpr int ColO = 2 * BKV;                   // O: [2 BKV, 2 BKV + D)
+    static constexpr int ColO = 0;                         // O: [0, D)
+    static constexpr int ColS = D;                         // S buffers: [D, D + 2 BKV)
+    static constexpr int ColQ = D + 2 * BKV;               // Q: D / 2 columns
+    static_assert(ColQ + D / 2 <= 512, "TMEM columns");
+    static_assert(Smem <= 232448, "shared memory");
 };
 
 int attn_smem_bytes(int D)
@@ -51,27 +58,58 @@ int attn_smem_bytes(int D)
     return D == 128 ? AttnGeom<128>::Smem : AttnGeom<256>::Smem;
 }
 
+// Loads kv tiles [j0, j1) of one ring (K or V) with TMA.  Returns after every
+// copy it started has landed.
+template <int D, int NS>
+__device__ __forceinline__ void attn_ring_producer(uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                                   const CUtensorMap *map_p,
+                                                   const CUtensorMap *map_c, const AttnArgs &a,
+                                                   int j0, int nt, int g, int b, int where)
+{
+    using Gm = AttnGeom<D>;
+    const uint64_t pol = policy_evict_first();
+    uint32_t armed = 0, armed_par = 0;
+    for (int it = 0; it < nt; ++it) {
+        const int s = it % NS;
+        const uint32_t use = static_cast<uint32_t>(it / NS);
+        if (!mbar_wait(&empty[s], (use & 1u) ^ 1u, a.ws, where)) break;
+        const int j = j0 + it;
+        const bool pre = j < a.nkt_p;
+        const CUtensorMap *m = pre ? map_p : map_c;
+        const int row0 = (pre ? j : j - a.nkt_p) * Gm::BKV;
+        mbar_arrive_expect_tx(&full[s], Gm::KVBytes);
+        for (int at = 0; at < Gm::NA; ++at)
+            tma_load_4d(ring + s * Gm::KVBytes + at * Gm::KVAtomBytes, m, &full[s], at * 64, g,
+                        row0, b, pol);
+        armed |= 1u << s;
+        armed_par = (armed_par & ~(1u << s)) | ((use & 1u) << s);
+    }
+    for (int s = 0; s < NS; ++s)
+        if (armed >> s & 1u) mbar_wait(&full[s], armed_par >> s & 1u, a.ws, where + 1);
+}
+
 template <int D>
-__device__ __forceinline__ void attn_body(const CUtensorMap *map_q, const CUtensorMap *map_kp,
-                                          const CUtensorMap *map_vp, const CUtensorMap *map_kc,
-                                          const CUtensorMap *map_vc, const AttnArgs &a)
+__device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUtensorMap *map_vp,
+                                          const CUtensorMap *map_kc, const CUtensorMap *map_vc,
+                                          const AttnArgs &a)
 {
     using Gm = AttnGeom<D>;
     constexpr int BKV = Gm::BKV;
+    constexpr int NK = Gm::NK, NV = Gm::NV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Gm::OffBar);
-    uint64_t *bar_q = bars + 0;
-    uint64_t *k_full = bars + 1;     // [2]
-    uint64_t *v_full = bars + 3;     // [2]
-    uint64_t *kv_empty = bars + 5;   // [2]
-    uint64_t *s_full = bars + 7;     // [2]
-    uint64_t *s_empty = bars + 9;    // [2]
-    uint64_t *p_full = bars + 11;
-    uint64_t *pv_done = bars + 12;
-    uint64_t *o_full = bars + 13;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    uint64_t *k_full = bars;                 // [NK]
+    uint64_t *k_empty = k_full + NK;         // [NK]
+    uint64_t *v_full = k_empty + NK;         // [NV]
+    uint64_t *v_empty = v_full + NV;         // [NV]
+    uint64_t *s_full = v_empty + NV;         // [2]
+    uint64_t *pv_done = s_full + 2;          // [2]
+    uint64_t *p_full = pv_done + 2;          // [2]
+    uint64_t *q_ready = p_full + 2;
+    uint64_t *o_full = q_ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_full + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x;
@@ -83,20 +121,39 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_q, const CUtens
     const int j1 = min(nkt, j0 + a.tiles_per_split);
     const int nt = j1 - j0;
 
+    // softmax warps (2-5): thread = one query row of the tile; its Q row is
+    // fetched now so that the loads overlap the set-up below
+    const int q = warp & 3;                  // TMEM lane quadrant of the warp
+    const int r = q * 32 + lane;             // row within the 128-row tile
+    const int frow = mt * 128 + r;           // folded row = position * G + head
+    const int i = frow / a.G, hj = frow % a.G;
+    const bool live = i < a.L;
+    const size_t flat =
+        (static_cast<size_t>(b) * a.L + i) * a.Hq + static_cast<size_t>(g) * a.G + hj;
+    uint4 qv[D / 8];
+    if (warp >= 2 && warp < 6) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + flat * D);
+#pragma unroll
+        for (int k = 0; k < D / 8; ++k) qv[k] = live ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+    }
+
     if (warp == 0 && lane == 0) {
-        mbar_init(bar_q, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NK; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-            mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], 4);
+            mbar_init(&k_empty[s], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&pv_done[s], 1);
+            mbar_init(&p_full[s], 4);
+        }
+        mbar_init(q_ready, 4);
         mbar_init(o_full, 1);
         fence_barrier_init();
-        tma_prefetch_desc(map_q);
         tma_prefetch_desc(map_kc);
         tma_prefetch_desc(map_vc);
         if (a.P > 0) {
@@ -114,117 +171,105 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_q, const CUtens
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // -------------------------------------------------------------- TMA
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            mbar_arrive_expect_tx(bar_q, Gm::QBytes);
-            const int pos0 = mt * (128 / a.G);
-            for (int at = 0; at < Gm::NA; ++at)   // Q map: {dim, head-in-group, group, pos, batch}
-                tma_load_5d(smem + Gm::OffQ + at * 128 * 128, map_q, bar_q, at * 64, 0, g, pos0, b,
-                            pol);
-            uint32_t armed = 0, armed_par = 0;
-            for (int it = 0; it < nt; ++it) {
-                const int s = it & 1;
-                const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (!mbar_wait(&kv_empty[s], (use & 1u) ^ 1u, a.ws, 201)) break;
-                const int j = j0 + it;
-                const bool pre = j < a.nkt_p;
-                const CUtensorMap *mk = pre ? map_kp : map_kc;
-                const CUtensorMap *mv = pre ? map_vp : map_vc;
-                const int row0 = (pre ? j : j - a.nkt_p) * BKV;
-                mbar_arrive_expect_tx(&k_full[s], Gm::KVBytes);
-                for (int at = 0; at < Gm::NA; ++at)
-                    tma_load_4d(smem + Gm::OffK + s * Gm::KVBytes + at * Gm::KVAtomBytes, mk,
-                                &k_full[s], at * 64, g, row0, b, pol);
-                mbar_arrive_expect_tx(&v_full[s], Gm::KVBytes);
-                for (int at = 0; at < Gm::NA; ++at)
-                    tma_load_4d(smem + Gm::OffV + s * Gm::KVBytes + at * Gm::KVAtomBytes, mv,
-                                &v_full[s], at * 64, g, row0, b, pol);
-                armed |= 1u << s;
-                armed_par = (armed_par & ~(1u << s)) | ((use & 1u) << s);
-            }
-            // every copy this thread started has landed before the CTA can exit
-            mbar_wait(bar_q, 0, a.ws, 202);
-            for (int s = 0; s < 2; ++s) {
-                if (armed >> s & 1u) {
-                    mbar_wait(&k_full[s], armed_par >> s & 1u, a.ws, 203);
-                    mbar_wait(&v_full[s], armed_par >> s & 1u, a.ws, 204);
-                }
-            }
-        }
+        // -------------------------------------------------------------- K loads
+        if (lane == 0)
+            attn_ring_producer<D, NK>(smem + Gm::OffK, k_full, k_empty, map_kp, map_kc, a, j0, nt,
+                                      g, b, 201);
+    } else if (warp == 6) {
+        // -------------------------------------------------------------- V loads
+        if (lane == 0)
+            attn_ring_producer<D, NV>(smem + Gm::OffV, v_full, v_empty, map_vp, map_vc, a, j0, nt,
+                                      g, b, 203);
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t idesc_s = make_idesc_bf16(128, BKV, 0);
             const uint32_t idesc_o = make_idesc_bf16(128, D, 1);
-            const uint32_t sq = smem_u32(smem + Gm::OffQ);
-            const uint32_t sp = smem_u32(smem + Gm::OffP);
-            bool ok = mbar_wait(bar_q, 0, a.ws, 211);
-            auto issue_pv = [&](int jt) -> bool {
-                const int s = jt & 1;
-                if (!mbar_wait(p_full, static_cast<uint32_t>(jt & 1), a.ws, 212)) return false;
-                if (!mbar_wait(&v_full[s], static_cast<uint32_t>((jt >> 1) & 1), a.ws, 213))
+            const uint32_t sk0 = smem_u32(smem + Gm::OffK);
+            const uint32_t sv0 = smem_u32(smem + Gm::OffV);
+            bool ok = mbar_wait(q_ready, 0, a.ws, 211);
+            tc_fence_after();
+            auto issue_s = [&](int it) -> bool {
+                const int s = it % NK;
+                if (!mbar_wait(&k_full[s], static_cast<uint32_t>((it / NK) & 1), a.ws, 212))
                     return false;
                 tc_fence_after();
-                const uint32_t sv = smem_u32(smem + Gm::OffV + s * Gm::KVBytes);
-#pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk) {
-                    // A = P: K-major, 64-key atoms of 128 rows x 128 B
-                    const uint64_t adesc =
-                        make_sdesc_sw128(sp + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-                    // B = V: MN-major, 64-dim atoms KVAtomBytes apart, 8-key groups 1 KB apart
-                    const uint64_t bdesc = make_sdesc_sw128(sv + kk * 2048, Gm::KVAtomBytes, 1024);
-                    umma_bf16(tmem + Gm::ColO, adesc, bdesc, idesc_o, (jt | kk) != 0);
-                }
-                umma_commit(&kv_empty[s]);
-                umma_commit(pv_done);
-                return true;
-            };
-            for (int it = 0; it < nt && ok; ++it) {
-                const int s = it & 1;
-                const uint32_t use = static_cast<uint32_t>(it >> 1);
-                if (!mbar_wait(&k_full[s], use & 1u, a.ws, 214)) { ok = false; break; }
-                if (!mbar_wait(&s_empty[s], (use & 1u) ^ 1u, a.ws, 215)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t sk = smem_u32(smem + Gm::OffK + s * Gm::KVBytes);
+                const uint32_t sk = sk0 + s * Gm::KVBytes;
+                const uint32_t d = tmem + Gm::ColS + (it & 1) * BKV;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t adesc =
-                        make_sdesc_sw128(sq + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+                    // B = K: K-major, 64-dim atoms KVAtomBytes apart, +32 B per 16 dims
                     const uint64_t bdesc =
                         make_sdesc_sw128(sk + (kk >> 2) * Gm::KVAtomBytes + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem + Gm::ColS + s * BKV, adesc, bdesc, idesc_s, kk != 0);
+                    umma_bf16_ts(d, tmem + Gm::ColQ + kk * 8, bdesc, idesc_s, kk != 0);
                 }
-                umma_commit(&s_full[s]);
-                if (it >= 1 && !issue_pv(it - 1)) { ok = false; break; }
+                umma_commit(&k_empty[s]);
+                umma_commit(&s_full[it & 1]);
+                return true;
+            };
+            auto issue_pv = [&](int jt) -> bool {
+                const int s = jt % NV;
+                // one barrier per S buffer: the softmax cannot run two tiles ahead of a wait
+                if (!mbar_wait(&p_full[jt & 1], static_cast<uint32_t>((jt >> 1) & 1), a.ws, 213))
+                    return false;
+                if (!mbar_wait(&v_full[s], static_cast<uint32_t>((jt / NV) & 1), a.ws, 214))
+                    return false;
+                tc_fence_after();
+                const uint32_t sv = sv0 + s * Gm::KVBytes;
+                const uint32_t pa = tmem + Gm::ColS + (jt & 1) * BKV;
+#pragma unroll
+                for (int kk = 0; kk < BKV / 16; ++kk) {
+                    // B = V: MN-major, 64-dim atoms KVAtomBytes apart, 8-key groups 1 KB apart
+                    const uint64_t bdesc = make_sdesc_sw128(sv + kk * 2048, Gm::KVAtomBytes, 1024);
+                    umma_bf16_ts(tmem + Gm::ColO, pa + kk * 8, bdesc, idesc_o, (jt | kk) != 0);
+                }
+                umma_commit(&v_empty[s]);
+                umma_commit(&pv_done[jt & 1]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int it = 1; it < nt && ok; ++it) {
+                // S(it) overwrites the buffer of P(it - 2), whose PV was issued before
+                ok = issue_s(it) && issue_pv(it - 1);
             }
-            if (ok && nt >= 1) ok = issue_pv(nt - 1);
+            if (ok) ok = issue_pv(nt - 1);
             umma_commit(o_full);
-            mbar_wait(o_full, 0, a.ws, 216);
+            mbar_wait(o_full, 0, a.ws, 215);
         }
     } else {
         // -------------------------------------------------------------- softmax
-        const int q = warp & 3;                  // TMEM lane quadrant of this warp
-        const int r = q * 32 + lane;             // row within the 128-row tile
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        // ---- Q row into TMEM (rows past the canvas are zero)
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+            uint32_t w[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 v = qv[(c0 >> 2) + k];
+                w[4 * k] = v.x;
+                w[4 * k + 1] = v.y;
+                w[4 * k + 2] = v.z;
+                w[4 * k + 3] = v.w;
+            }
+            tmem_st32(tmem + lane_off + Gm::ColQ + c0, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        uint8_t *sP = smem + Gm::OffP;
         for (int it = 0; it < nt; ++it) {
-            const int s = it & 1;
-            const uint32_t use = static_cast<uint32_t>(it >> 1);
-            ok = mbar_wait(&s_full[s], use & 1u, a.ws, 221);
+            const int sb = it & 1;
+            ok = mbar_wait(&s_full[sb], static_cast<uint32_t>((it >> 1) & 1), a.ws, 221);
             if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
             tc_fence_after();
+            const uint32_t ts = tmem + lane_off + Gm::ColS + sb * BKV;
             uint32_t sr[BKV];
 #pragma unroll
             for (int c0 = 0; c0 < BKV; c0 += 32)
-                tmem_ld32_nowait(tmem + lane_off + Gm::ColS + s * BKV + c0,
-                                 *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
+                tmem_ld32_nowait(ts + c0, *reinterpret_cast<uint32_t(*)[32]>(&sr[c0]));
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[s]);
 
             const int j = j0 + it;
             const bool pre = j < a.nkt_p;
@@ -259,51 +304,38 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_q, const CUtens
                 pk[c >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
             }
             l += psum;
-            if (it >= 1) {
-                ok = mbar_wait(pv_done, static_cast<uint32_t>((it - 1) & 1), a.ws, 222);
+            if (__any_sync(0xFFFFFFFFu, rescale)) {
+                // O holds the PVs up to tile it - 1: wait for the last one (the
+                // completed S(it) already implies every earlier PV is done)
+                ok = mbar_wait(&pv_done[(it - 1) & 1], static_cast<uint32_t>(((it - 1) >> 1) & 1),
+                               a.ws, 222);
                 if (!__all_sync(0xFFFFFFFFu, ok)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        const uint32_t ta = tmem + lane_off + Gm::ColO + c0;
-                        tmem_ld32_nowait(ta, o);
-                        tmem_wait_ld();
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    const uint32_t ta = tmem + lane_off + Gm::ColO + c0;
+                    tmem_ld32_nowait(ta, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * factor);
-                        tmem_st32(ta, o);
-                    }
-                    tmem_wait_st();
+                    for (int k = 0; k < 32; ++k)
+                        o[k] = __float_as_uint(__uint_as_float(o[k]) * factor);
+                    tmem_st32(ta, o);
                 }
             }
-            // P row r, K-major 128B-swizzled: 64-key atoms of 128 rows x 128 B
+            // P(it) as bf16 pairs over the first BKV / 2 columns of its S buffer
 #pragma unroll
-            for (int at = 0; at < BKV / 64; ++at) {
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t off = static_cast<uint32_t>(at * 128 * 128 + r * 128 +
-                                                               ((ch ^ (r & 7)) << 4));
-                    const int w0 = at * 32 + ch * 4;
-                    *reinterpret_cast<uint4 *>(sP + off) =
-                        make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
-                }
-            }
-            fence_proxy_async_smem();
+            for (int c0 = 0; c0 < BKV / 2; c0 += 32)
+                tmem_st32(ts + c0, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c0]));
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[sb]);
         }
         // -------------------------------------------------------------- epilogue
         if (ok) ok = mbar_wait(o_full, 0, a.ws, 223);
         if (__all_sync(0xFFFFFFFFu, ok)) {
             tc_fence_after();
-            const int frow = mt * 128 + r;           // folded row = position * G + head
-            const int i = frow / a.G, hj = frow % a.G;
-            const bool live = i < a.L;
-            const size_t flat =
-                (static_cast<size_t>(b) * a.L + i) * a.Hq + static_cast<size_t>(g) * a.G + hj;
             const float inv_l = 1.f / l;
             const size_t nrows = static_cast<size_t>(a.B) * a.L * a.Hq;
 #pragma unroll 1
@@ -351,23 +383,21 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_q, const CUtens
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_kernel_d128(const __grid_constant__ CUtensorMap map_q,
-                     const __grid_constant__ CUtensorMap map_kp,
+    attn_kernel_d128(const __grid_constant__ CUtensorMap map_kp,
                      const __grid_constant__ CUtensorMap map_vp,
                      const __grid_constant__ CUtensorMap map_kc,
                      const __grid_constant__ CUtensorMap map_vc, AttnArgs a)
 {
-    attn_body<128>(&map_q, &map_kp, &map_vp, &map_kc, &map_vc, a);
+    attn_body<128>(&map_kp, &map_vp, &map_kc, &map_vc, a);
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_kernel_d256(const __grid_constant__ CUtensorMap map_q,
-                     const __grid_constant__ CUtensorMap map_kp,
+    attn_kernel_d256(const __grid_constant__ CUtensorMap map_kp,
                      const __grid_constant__ CUtensorMap map_vp,
                      const __grid_constant__ CUtensorMap map_kc,
                      const __grid_constant__ CUtensorMap map_vc, AttnArgs a)
 {
-    attn_body<256>(&map_q, &map_kp, &map_vp, &map_kc, &map_vc, a);
+    attn_body<256>(&map_kp, &map_vp, &map_kc, &map_vc, a);
 }
 
 // Merge the key splits: one warp per query row, lanes over the head dim.

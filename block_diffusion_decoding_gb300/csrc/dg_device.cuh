@@ -218,6 +218,20 @@ DG_DEVICE void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16.  A (M = 128 rows) sits in the
+// 128 TMEM lanes, row i in lane i, two bf16 K-elements per 32-bit column
+// (the lower K index in the low half); a_tmem is its first column.
+DG_DEVICE void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on *bar once every tcgen05.mma issued so far by this thread is done.
 DG_DEVICE void umma_commit(uint64_t *bar)
 {

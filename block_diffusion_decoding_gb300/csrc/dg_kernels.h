@@ -20,8 +20,7 @@ struct FoldArgs {
 
 struct CombineArgs {
     Partials part;
-    int n_slots, ntn, total, M;
-    int spc;            // partial-state slots per producer CTA (slot s belongs to CTA s / spc)
+    int n_slots, ntn, total, M;   // slot s of a row = producer unit s (tile range tile_begin(s))
     float *H;
     int32_t *sample;
     int32_t *argmax;
@@ -75,7 +74,8 @@ constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
 constexpr int kLmEpiWarps = 16;                          // 2 per (row half, TMEM quadrant)
 constexpr int kLmColGroups = kLmEpiWarps / 8;             // column groups per row
 constexpr int kLmThreads = 128 + 32 * kLmEpiWarps;        // 640
-constexpr int kLmSmemBytes = kLmStages * kLmStageBytes + 1024 + 256;
+constexpr int kLmMergeBytes = (kLmColGroups - 1) * 7 * kRowsPerBlock * 4;   // 7 KB
+constexpr int kLmSmemBytes = kLmStages * kLmStageBytes + 1024 + 256 + kLmMergeBytes;
 
 __global__ void lm_head_kernel(const __grid_constant__ CUtensorMap map_x,
                                const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
@@ -87,7 +87,8 @@ constexpr int kPairABytes = 128 * kLmBK * 2;             // 16 KB: X rows of thi
 constexpr int kPairStageBytes = kPairABytes + 4 * kLmBBoxBytes;   // + up to 256 W columns
 constexpr int kPairStages = 4;
 constexpr int kPairColGroups = 4;                        // epilogue warps per TMEM quadrant
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024 + 256;
+constexpr int kPairMergeBytes = (kPairColGroups - 1) * 7 * 128 * 4;     // 10.5 KB
+constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024 + 256 + kPairMergeBytes;
 __global__ void lm_head_pair_kernel(const __grid_constant__ CUtensorMap map_x,
                                     const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 __global__ void logits_fold_kernel(const float *__restrict__ logits, FoldArgs a);
@@ -112,21 +113,20 @@ struct AttnArgs {
     int nkt_p, nkt_c;   // key tiles in the prefix / canvas
     int tiles_per_split;
     float scale_log2;   // scale * log2(e)
+    const uint16_t *q;  // [B, L, Hq, D]
     uint16_t *out;      // [B, L, Hq, D] (nsplit == 1)
     float *part_o;      // [nsplit][B*L*Hq][D] unnormalised (nsplit > 1)
     float *part_ml;     // [nsplit][B*L*Hq][2] (row max in base 2, row sum)
     WsHeader *ws;
 };
 
-constexpr int kAttnThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kAttnThreads = 224;    // warp 0 K loads, 1 MMA, 2-5 softmax, 6 V loads
 
-__global__ void attn_kernel_d128(const __grid_constant__ CUtensorMap map_q,
-                                 const __grid_constant__ CUtensorMap map_kp,
+__global__ void attn_kernel_d128(const __grid_constant__ CUtensorMap map_kp,
                                  const __grid_constant__ CUtensorMap map_vp,
                                  const __grid_constant__ CUtensorMap map_kc,
                                  const __grid_constant__ CUtensorMap map_vc, AttnArgs a);
-__global__ void attn_kernel_d256(const __grid_constant__ CUtensorMap map_q,
-                                 const __grid_constant__ CUtensorMap map_kp,
+__global__ void attn_kernel_d256(const __grid_constant__ CUtensorMap map_kp,
                                  const __grid_constant__ CUtensorMap map_vp,
                                  const __grid_constant__ CUtensorMap map_kc,
                                  const __grid_constant__ CUtensorMap map_vc, AttnArgs a);

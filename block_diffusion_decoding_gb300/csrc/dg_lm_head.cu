@@ -24,7 +24,9 @@
 //               ((w - 4) / 4) % 2, one canvas row per thread, every other
 //               16-column chunk (two warps share a row's columns), and folds
 //               them (dg_sampler.cuh) while the MMA fills the other buffer;
-//               each warp keeps its own partial state (slot 2 CTA + group).
+//               at each row-block boundary the two column groups merge
+//               their states in shared memory and one partial state per
+//               (row, CTA) goes to global memory (slot = CTA index).
 #include "dg_kernels.h"
 
 namespace dg {
@@ -41,7 +43,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     uint64_t *acc_full = empty + kLmStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *mrg_ready = mma_done + 1;
+    uint64_t *mrg_done = mrg_ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mrg_done + 1);
+    const GroupMerge gm{reinterpret_cast<float *>(smem + kLmStages * kLmStageBytes + 256),
+                        mrg_ready, mrg_done, kLmColGroups, kRowsPerBlock};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x, n_slots = gridDim.x;
@@ -61,6 +67,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             mbar_init(&acc_empty[s], kLmEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(mrg_ready, kLmEpiWarps - kLmEpiWarps / kLmColGroups);
+        mbar_init(mrg_done, kLmEpiWarps / kLmColGroups);
         fence_barrier_init();
         tma_prefetch_desc(&map_x);
         tma_prefetch_desc(&map_w);
@@ -161,7 +169,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int h = (e >> 2) & 1;             // 128-row half
         const int cg = e >> 3;                  // column group: chunks cg, cg + G, ...
-        const size_t slot = static_cast<size_t>(c) * kLmColGroups + cg;
+        const int rix = h * 128 + q * 32 + lane;  // row within the 256-row block
+        uint32_t merges = 0;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         RowState st;
         row_state_init(st);
@@ -173,9 +182,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const uint32_t use = static_cast<uint32_t>(i >> 1);
             if (m != cur_m) {
                 if (cur_m >= 0) {
-                    const int prow = cur_m * kRowsPerBlock + h * 128 + q * 32 + lane;
+                    const int prow = cur_m * kRowsPerBlock + rix;
                     row_state_finalize(st, fc);
-                    if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
+                    group_merge_store(st, cg, rix, merges++, gm, a.part,
+                                      static_cast<size_t>(prow) * n_slots + c, prow < a.M, a.ws);
                 }
                 row_state_init(st);
                 cur_m = m;
@@ -201,9 +211,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
         if (cur_m >= 0) {
-            const int prow = cur_m * kRowsPerBlock + h * 128 + q * 32 + lane;
+            const int prow = cur_m * kRowsPerBlock + rix;
             row_state_finalize(st, fc);
-            if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
+            group_merge_store(st, cg, rix, merges, gm, a.part,
+                              static_cast<size_t>(prow) * n_slots + c, prow < a.M, a.ws);
         }
     }
     tc_fence_before();

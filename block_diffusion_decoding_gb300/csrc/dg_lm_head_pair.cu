@@ -17,8 +17,10 @@
 //               empty barrier takes one multicast commit from each CTA);
 //   warp 1      TMEM allocator + UMMA issuer;
 //   warps 4-19  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, every
-//               4th 16-column chunk starting at chunk (w - 4) / 4, and keeps
-//               its own partial state (slot 4 cluster + (w - 4) / 4).
+//               4th 16-column chunk starting at chunk (w - 4) / 4; the four
+//               column groups merge their states in shared memory at each
+//               row-block boundary and store one partial state per (row,
+//               cluster) (slot = cluster index).
 #include "dg_kernels.h"
 
 namespace dg {
@@ -35,7 +37,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     uint64_t *acc_full = empty + kPairStages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *mrg_ready = mma_done + 1;
+    uint64_t *mrg_done = mrg_ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mrg_done + 1);
+    const GroupMerge gm{reinterpret_cast<float *>(smem + kPairStages * kPairStageBytes + 256),
+                        mrg_ready, mrg_done, kPairColGroups, 128};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = static_cast<int>(cluster_ctarank());          // row half
@@ -58,6 +64,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             mbar_init(&acc_empty[s], kLmEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(mrg_ready, kLmEpiWarps - kLmEpiWarps / kPairColGroups);
+        mbar_init(mrg_done, kLmEpiWarps / kPairColGroups);
         fence_barrier_init();
         tma_prefetch_desc(&map_x);
         tma_prefetch_desc(&map_w);
@@ -155,7 +163,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
         const int q = warp & 3;                  // TMEM lane quadrant of this warp
         const int cg = (warp - 4) >> 2;          // column group
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const size_t slot = static_cast<size_t>(cid) * kPairColGroups + cg;
+        const int rix = q * 32 + lane;             // row within this CTA's 128 rows
+        uint32_t merges = 0;
         RowState st;
         row_state_init(st);
         int cur_m = -1;
@@ -166,9 +175,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             const uint32_t use = static_cast<uint32_t>(i >> 1);
             if (m != cur_m) {
                 if (cur_m >= 0) {
-                    const int prow = cur_m * kRowsPerBlock + r * 128 + q * 32 + lane;
+                    const int prow = cur_m * kRowsPerBlock + r * 128 + rix;
                     row_state_finalize(st, fc);
-                    if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
+                    group_merge_store(st, cg, rix, merges++, gm, a.part,
+                                      static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws);
                 }
                 row_state_init(st);
                 cur_m = m;
@@ -192,9 +202,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
         if (cur_m >= 0) {
-            const int prow = cur_m * kRowsPerBlock + r * 128 + q * 32 + lane;
+            const int prow = cur_m * kRowsPerBlock + r * 128 + rix;
             row_state_finalize(st, fc);
-            if (prow < a.M) partial_store(a.part, slot * a.M + prow, st);
+            group_merge_store(st, cg, rix, merges, gm, a.part,
+                              static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws);
         }
     }
     tc_fence_before();

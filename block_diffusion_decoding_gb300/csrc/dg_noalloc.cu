@@ -15,10 +15,10 @@
 // it until the process exits.
 //
 // Capacity: kNoAllocScratchBytes = 8 MiB.  A step needs 256 bytes of header,
-// 7 x 4 bytes x 2 x (LM-head CTAs) x B*L of partial states and 4 bytes per canvas
-// (each rounded up to 256 bytes).  With one CTA per SM on a 152-SM GB300 that
-// is at most B*L = 985 canvas rows (three 256-token canvases); larger steps
-// are rejected with DG_ERR_UNSUPPORTED before anything is launched.
+// 7 x 4 bytes x (LM-head units) x B*L of partial states and 4 bytes per canvas
+// (each rounded up to 256 bytes).  With one unit per SM on a 152-SM GB300
+// that is at most B*L = 1970 canvas rows (seven 256-token canvases); larger
+// steps are rejected with DG_ERR_UNSUPPORTED before anything is launched.
 //
 // Sharing: every call, from any thread or stream, uses the same array and
 // leaves the last call's contents in it.  The counters that must start at
@@ -202,7 +202,6 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     CombineArgs c{};
     c.part = part;
     c.n_slots = plan.part_slots();
-    c.spc = plan.spc;
     c.ntn = ntn;
     c.total = total;
     c.M = M;

@@ -19,10 +19,10 @@ struct LmPlan {
     int ntn;          // vocabulary tiles per 256-row block
     int mblocks;      // 256-row blocks
     int total;        // tiles
-    int units;        // CTAs (single) or clusters (pair) -- the tile schedule's slots
-    int spc;          // partial-state slots per unit
+    int units;        // CTAs (single) or clusters (pair): the tile schedule's
+                      // slots, one partial state per (row, unit)
     int grid;         // CTAs launched
-    int part_slots() const { return units * spc; }
+    int part_slots() const { return units; }
 };
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
@@ -59,7 +59,6 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms)
             best.ntn = ntn;
             best.total = total;
             best.units = units;
-            best.spc = pair ? kPairColGroups : kLmColGroups;
             best.grid = pair ? 2 * units : units;
         }
     };
@@ -75,9 +74,7 @@ inline int slot_bound(int M, int V)
 {
     const long mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
     const long tiles = mblocks * ((V + 63) / 64);
-    const long single = std::min<long>(tiles, kMaxSlots) * kLmColGroups;
-    const long pair = std::min<long>(tiles, kMaxSlots / 2) * kPairColGroups;
-    return static_cast<int>(std::max(single, pair));
+    return static_cast<int>(std::min<long>(tiles, kMaxSlots));
 }
 
 }  // namespace dg

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
             if (cur_m >= 0) {
                 const int prow = cur_m * kRowsPerBlock + threadIdx.x;
                 row_state_finalize(st, fc);
-                if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
+                if (prow < a.M) partial_store(a.part, static_cast<size_t>(prow) * a.n_slots + c, st);
             }
             row_state_init(st);
             cur_m = m;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
     if (cur_m >= 0) {
         const int prow = cur_m * kRowsPerBlock + threadIdx.x;
         row_state_finalize(st, fc);
-        if (prow < a.M) partial_store(a.part, static_cast<size_t>(c) * a.M + prow, st);
+        if (prow < a.M) partial_store(a.part, static_cast<size_t>(prow) * a.n_slots + c, st);
     }
 }
 
@@ -211,18 +211,20 @@ __global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, Acce
     if (i < a.L) {
         const int r = b * a.L + i;
         const int m = r / kRowsPerBlock;
-        const int lo = m * c.ntn, hi = lo + c.ntn;
+        // the producer units whose tile ranges meet row block m are contiguous
+        const int u0 = tile_slot(m * c.ntn, c.total, c.n_slots);
+        const int u1 = tile_slot(m * c.ntn + c.ntn - 1, c.total, c.n_slots);
         RowState st;
         row_state_init(st);
-        for (int s = lane; s < c.n_slots; s += 32) {
-            const int cta = s / c.spc;
-            const int t0 = tile_begin(cta, c.total, c.n_slots / c.spc);
-            const int t1 = tile_begin(cta + 1, c.total, c.n_slots / c.spc);
-            if (t0 < hi && t1 > lo && t1 > t0) {
-                RowState p;
-                partial_load(c.part, static_cast<size_t>(s) * c.M + r, p);
-                row_state_merge(st, p);
-            }
+        const size_t base = static_cast<size_t>(r) * c.n_slots;
+        for (int s = u0 + lane; s <= u1; s += 64) {
+            // two slots per lane per pass: all fourteen loads are in flight together
+            RowState p0, p1;
+            partial_load(c.part, base + s, p0);
+            const bool two = s + 32 <= u1;
+            if (two) partial_load(c.part, base + s + 32, p1);
+            row_state_merge(st, p0);
+            if (two) row_state_merge(st, p1);
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {

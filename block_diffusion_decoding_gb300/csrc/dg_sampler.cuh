@@ -290,8 +290,9 @@ DG_DEVICE void row_state_merge(RowState &a, const RowState &b)
     }
 }
 
-// Partial states in global memory: structure of arrays, slot-major
-// ([n_slots][M]), so consecutive rows of one slot are contiguous.
+// Partial states in global memory: structure of arrays, row-major
+// ([M][n_slots]), so the slots of one row are contiguous (the combine reads
+// them with one lane per slot).
 struct Partials {
     float *m, *S, *A, *gbest, *amax;
     int *gidx, *aidx;
@@ -327,6 +328,72 @@ __host__ __device__ inline int tile_begin(int c, int total, int n_slots)
 {
     const int q = total / n_slots, rem = total % n_slots;
     return c * q + (c < rem ? c : rem);
+}
+
+// The slot whose range holds tile t (0 <= t < total): the first `rem` slots
+// own q + 1 tiles each, the others q.
+__host__ __device__ inline int tile_slot(int t, int total, int n_slots)
+{
+    const int q = total / n_slots, rem = total % n_slots;
+    const int big = rem * (q + 1);
+    return t < big ? t / (q + 1) : rem + (t - big) / q;
+}
+
+// Merge of the column groups' states inside one LM-head CTA before the
+// single store per (row, CTA).  The epilogue warps of group g > 0 put their
+// finalized states into shared memory ([g - 1][field][row]) and arrive on
+// `ready`; the group-0 warps wait, merge them into their own state, store,
+// and arrive on `done`, which group g > 0 waits for before it writes the
+// buffer again at the next row-block boundary.  `k` counts the merges of
+// this CTA (the phase of both barriers).  All waits are bounded.
+struct GroupMerge {
+    float *buf;          // shared: (G - 1) x 7 x rows words
+    uint64_t *ready;     // count: warps of groups 1 .. G-1
+    uint64_t *done;      // count: warps of group 0
+    int G;               // column groups
+    int rows;            // rows of the CTA
+};
+
+DG_DEVICE void group_merge_store(RowState &st, int cg, int rix, uint32_t k,
+                                 const GroupMerge &gm, const Partials &p, size_t idx, bool store,
+                                 WsHeader *ws)
+{
+    const int lane = threadIdx.x & 31;
+    if (cg != 0) {
+        bool ok = true;
+        if (k > 0) ok = mbar_wait(gm.done, (k - 1) & 1u, ws, 120);
+        if (ok) {
+            float *f = gm.buf + static_cast<size_t>(cg - 1) * 7 * gm.rows + rix;
+            f[0 * gm.rows] = st.m;
+            f[1 * gm.rows] = st.S;
+            f[2 * gm.rows] = st.A;
+            f[3 * gm.rows] = st.gbest;
+            f[4 * gm.rows] = __int_as_float(st.gidx);
+            f[5 * gm.rows] = st.amax;
+            f[6 * gm.rows] = __int_as_float(st.aidx);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(gm.ready);
+        return;
+    }
+    const bool ok = mbar_wait(gm.ready, k & 1u, ws, 121);
+    if (ok) {
+        for (int g = 1; g < gm.G; ++g) {
+            const float *f = gm.buf + static_cast<size_t>(g - 1) * 7 * gm.rows + rix;
+            RowState o;
+            o.m = f[0 * gm.rows];
+            o.S = f[1 * gm.rows];
+            o.A = f[2 * gm.rows];
+            o.gbest = f[3 * gm.rows];
+            o.gidx = __float_as_int(f[4 * gm.rows]);
+            o.amax = f[5 * gm.rows];
+            o.aidx = __float_as_int(f[6 * gm.rows]);
+            row_state_merge(st, o);
+        }
+        if (store) partial_store(p, idx, st);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(gm.done);
 }
 
 // Device-resident control block of the block loop (in the workspace).  The

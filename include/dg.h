@@ -148,8 +148,8 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 /* this is a deployment convenience.  Same kernels, same results; their       */
 /* scratch lives in one 8 MiB array inside the library's device memory,      */
 /* held by every GPU that loads the library until the process exits.         */
-/* Limit: steps needing more than 8 MiB of scratch (7 x 4 B x 2 x CTAs x B*L  */
-/* + 512 B; B*L <= 985 on a 152-SM GB300) return DG_ERR_UNSUPPORTED.  The     */
+/* Limit: steps needing more than 8 MiB of scratch (7 x 4 B x CTAs x B*L     */
+/* + 512 B; B*L <= 1970 on a 152-SM GB300) return DG_ERR_UNSUPPORTED.  The    */
 /* first call on a device sets up the array's address (cudaGetSymbolAddress) and */
 /* clears its status header: make it before any stream capture.  All calls    */
 /* share the array; calls that overlap on the GPU race -- order them on one   */
