@@ -339,8 +339,8 @@ def run_ours(args, cfg):
     at_bytes = 2 * (B * L * Hq * D * 2) + 2 * (B * (P + L) * Hkv * D * 2)
     lm_plan = dg.lm_head_plan(M, d, V)
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
-            for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_plan.h", "dg_sampler.cuh",
-                      "dg_device.cuh", "dg_kernels.h")]
+            for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
+                      "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
     traffic = _traffic_record(srcs, lm_plan["kernel"])
 
     # ---- end to end through the C ABI with host buffers (pinned), per-step H2D + D2H

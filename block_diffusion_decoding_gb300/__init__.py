@@ -191,11 +191,11 @@ def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):
 
 def lm_head_plan(rows: int, d: int, V: int) -> dict:
     """The LM-head launch the step would make on the current device."""
-    cl, bn, ctas = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    rc = _lib().dg_lm_head_plan(rows, d, V, ctypes.byref(cl), ctypes.byref(bn), ctypes.byref(ctas))
+    kind, bn, ctas = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = _lib().dg_lm_head_plan(rows, d, V, ctypes.byref(kind), ctypes.byref(bn), ctypes.byref(ctas))
     _check(rc, "dg_lm_head_plan")
-    return {"kernel": "lm_head_pair_kernel" if cl.value == 2 else "lm_head_kernel",
-            "cluster_ctas": cl.value, "BN": bn.value, "ctas": ctas.value}
+    names = ("lm_head_kernel", "lm_head_pair_kernel", "lm_head_duo_kernel")
+    return {"kernel": names[kind.value], "kind": kind.value, "BN": bn.value, "ctas": ctas.value}
 
 
 def kernel_launches() -> int:

@@ -74,6 +74,9 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_pair_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPairSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDuoSmemBytes));
         DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d128,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          attn_smem_bytes(128)));
@@ -234,7 +237,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
                                       static_cast<uint64_t>(x_steps)};
             const uint64_t strides[2] = {static_cast<uint64_t>(p->d) * 2,
                                          static_cast<uint64_t>(hidden_stride) * 2};
-            const uint32_t box[3] = {64, plan.pair ? 128u : 256u, 1};
+            const uint32_t box[3] = {64, plan.cluster() ? 128u : 256u, 1};
             const int rank = x_steps > 1 ? 3 : 2;
             int rc = make_map_bf16(&mx, hidden, rank, dims, strides, box);
             if (rc != DG_OK) return rc;
@@ -262,10 +265,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.ws = ws.hdr;
         a.counters = ws.counters;
         a.ncounters = p->B;
-        if (plan.pair)
-            lm_head_pair_kernel<<<plan.grid, kLmThreads, kPairSmemBytes, st>>>(mx, mw, a);
-        else
-            lm_head_kernel<<<plan.grid, kLmThreads, kLmSmemBytes, st>>>(mx, mw, a);
+        DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st));
         DG_LAUNCHED();
     } else {
         FoldArgs f{};
@@ -581,7 +581,7 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 
 uint64_t dg_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int dg_lm_head_plan(int rows, int d, int V, int *cluster_ctas, int *bn, int *ctas)
+int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas)
 {
     if (rows < 1 || d < 1 || V < 1) return DG_ERR_INVALID_ARG;
     if (rows > (1 << 20) || V % 8 != 0 || V < 64) return DG_ERR_UNSUPPORTED;
@@ -590,7 +590,7 @@ int dg_lm_head_plan(int rows, int d, int V, int *cluster_ctas, int *bn, int *cta
     const int rc = current_device_info(&di);
     if (rc != DG_OK) return rc;
     const LmPlan plan = plan_lm_head(rows, d, V, di->sms);
-    if (cluster_ctas) *cluster_ctas = plan.pair ? 2 : 1;
+    if (kind) *kind = plan.kind;
     if (bn) *bn = plan.BN;
     if (ctas) *ctas = plan.grid;
     return DG_OK;
@@ -703,7 +703,7 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
         static_cast<uint64_t>(p->L), static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->V),
         f2u(p->entropy_bound), f2u(p->stop_threshold), d2u(bp->t_start), d2u(bp->t_end), p->seed,
         static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(bp->hidden_step_stride),
-        static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.grid * 2 + (plan.pair ? 1 : 0)),
+        static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.grid * 4 + plan.kind),
         static_cast<uint64_t>(dev)};
 
     BlockGraph *bgp = nullptr;

@@ -119,6 +119,30 @@ DG_DEVICE void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int
         : "memory");
 }
 
+// TMA loads of a 2-SM UMMA pair: the data lands in this CTA's shared memory,
+// the completion (complete_tx) goes to the mbarrier at cluster address
+// bar_cluster, which may be the even CTA's.
+DG_DEVICE void tma_load_2d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
+                                int y, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+DG_DEVICE void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int x,
+                                int y, int z, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z),
+        "l"(policy)
+        : "memory");
+}
+
 DG_DEVICE void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z,
                            uint64_t policy)
 {
@@ -252,9 +276,98 @@ DG_DEVICE void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
         : "memory");
 }
 
+// ---- 2-SM UMMA (cta_group::2): the CTA pair of a 2-CTA cluster acts as one
+// MMA unit.  One warp of each CTA allocates (collectively) the same TMEM
+// columns in both; the even CTA issues the MMAs; A (M = 256) is rows 0-127
+// from the even CTA's shared memory and 128-255 from the odd one's at the
+// same offset, B's N columns are split in halves the same way, and D rows
+// 0-127 / 128-255 land in the even / odd CTA's TMEM at the same address.
+DG_DEVICE void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+DG_DEVICE void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+DG_DEVICE void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+DG_DEVICE void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrival on the mbarrier at this shared offset in every CTA of cta_mask once
+// the pair MMAs issued so far by this thread are done.
+DG_DEVICE void umma_commit_pair(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // ------------------------------------------------------------------------
 // Thread-block clusters
 // ------------------------------------------------------------------------
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+DG_DEVICE uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address.
+DG_DEVICE void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// Bounded wait that acquires at cluster scope (for barriers that other CTAs
+// of the cluster arrive on).
+DG_DEVICE bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+DG_DEVICE bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, WsHeader *ws, int where)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+            report_error(ws, DG_ERR_TIMEOUT, where);
+            return false;
+        }
+    }
+}
 DG_DEVICE uint32_t cluster_ctarank()
 {
     uint32_t r;

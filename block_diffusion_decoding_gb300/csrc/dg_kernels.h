@@ -91,6 +91,15 @@ constexpr int kPairMergeBytes = (kPairColGroups - 1) * 7 * 128 * 4;     // 10.5 
 constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024 + 256 + kPairMergeBytes;
 __global__ void lm_head_pair_kernel(const __grid_constant__ CUtensorMap map_x,
                                     const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+
+// 2-SM UMMA variant (tcgen05 cta_group::2): each CTA of the pair loads its
+// own 128 rows of X and 128 of the 256 W columns of a tile; the even CTA
+// issues 256 x 256 x 16 UMMAs over both CTAs' shared memory.
+constexpr int kDuoStages = 6;
+constexpr int kDuoStageBytes = kPairABytes + 2 * kLmBBoxBytes;      // 32 KB
+constexpr int kDuoSmemBytes = kDuoStages * kDuoStageBytes + 1024 + 256 + kPairMergeBytes;
+__global__ void lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
+                                   const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 __global__ void logits_fold_kernel(const float *__restrict__ logits, FoldArgs a);
 __global__ void combine_accept_kernel(CombineArgs c, AcceptArgs a);
 __global__ void accept_only_kernel(const float *__restrict__ H, const int32_t *__restrict__ sample,

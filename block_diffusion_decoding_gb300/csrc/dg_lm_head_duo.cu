@@ -1,0 +1,230 @@
+// dg_lm_head_duo.cu -- the LM head of the denoising step on 2-CTA clusters
+// that issue 2-SM UMMAs (tcgen05 cta_group::2), for large vocabularies (the
+// full-vocabulary softmax the "Parallel Denoising From an Autoregressive
+// Checkpoint" page, section "Finding", names as a per-step cost).
+//
+// A tile is 256 canvas rows x 256 vocabulary columns.  CTA rank r of the
+// pair streams rows [128 r, 128 r + 128) of the hidden block and columns
+// [128 r, 128 r + 128) of the W tile into its own shared memory; the even
+// CTA issues one 256 x 256 x 16 UMMA per 16-deep k step that reads both
+// CTAs' halves, and each CTA receives its 128 rows x 256 columns of the
+// product in its own TMEM (double-buffered, 2 x 256 columns).  Compared with
+// a W tile multicast to both CTAs, every CTA writes and the tensor core reads
+// a third less shared memory per k block, which is what bounds the single-CTA
+// MMA at this shape.
+//
+//   warp 0      TMA producer (both CTAs): X[128 rows, 64] and W[64, 128] of
+//               its own halves into a 6-stage ring; both CTAs' copies
+//               complete on the even CTA's full barrier (the even CTA expects
+//               the bytes of both halves); a stage is free once the pair MMAs
+//               that read it are done (the commit is multicast to both CTAs'
+//               empty barriers);
+//   warp 1      TMEM allocator (both CTAs, collectively); UMMA issuer (even
+//               CTA); the accumulator is free once the epilogues of both
+//               CTAs have read it (the odd CTA's warps arrive remotely);
+//   warps 4-19  epilogue, as in dg_lm_head_pair.cu: warp w reads TMEM lanes
+//               32 (w % 4) .. +31, every 4th 16-column chunk starting at
+//               chunk (w - 4) / 4; the column groups merge in shared memory
+//               and one partial state per (row, cluster) is stored.
+#include "dg_kernels.h"
+
+namespace dg {
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+    lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
+                       const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDuoStages * kDuoStageBytes);
+    uint64_t *empty = full + kDuoStages;
+    uint64_t *acc_full = empty + kDuoStages;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
+    uint64_t *mrg_ready = mma_done + 1;
+    uint64_t *mrg_done = mrg_ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mrg_done + 1);
+    const GroupMerge gm{reinterpret_cast<float *>(smem + kDuoStages * kDuoStageBytes + 256),
+                        mrg_ready, mrg_done, kPairColGroups, 128};
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = static_cast<int>(cluster_ctarank());          // row / column half
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(num_clusters_x());
+    const int t0 = tile_begin(cid, a.total, ncl), t1 = tile_begin(cid + 1, a.total, ncl);
+    const int ntiles = t1 - t0;
+
+    if (cid == 0 && r == 0 && warp == 2) {
+        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
+    }
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kDuoStages; ++s) {
+            mbar_init(&full[s], 1);          // used in the even CTA only
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], 2 * kLmEpiWarps);   // used in the even CTA only
+        }
+        mbar_init(mma_done, 1);
+        mbar_init(mrg_ready, kLmEpiWarps - kLmEpiWarps / kPairColGroups);
+        mbar_init(mrg_done, kLmEpiWarps / kPairColGroups);
+        fence_barrier_init();
+        tma_prefetch_desc(&map_x);
+        tma_prefetch_desc(&map_w);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // both CTAs' barriers exist before either signals the other
+    cluster_sync_all();
+    const uint32_t tmem_base = *tmem_slot;
+    const FoldConsts fc = fold_consts(a.src, a.seed);
+    const int xstep = a.x_3d ? static_cast<int>(fc.step) : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            const uint32_t lead_full = mapa_shared(smem_u32(full), 0);
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t armed = 0, armed_par = 0;
+            bool ok = true;
+            for (int t = t0; t < t1 && ok; ++t) {
+                const int m = t / a.ntn, n = t % a.ntn;
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, a.ws, 401)) { ok = false; break; }
+                    if (r == 0) mbar_arrive_expect_tx(&full[s], 2 * kDuoStageBytes);
+                    const uint32_t fb = lead_full + static_cast<uint32_t>(s * 8);
+                    uint8_t *sa = smem + s * kDuoStageBytes;
+                    uint8_t *sb = sa + kPairABytes;
+                    // the block loop passes hidden states with a step coordinate (3-D map)
+                    if (a.x_3d)
+                        tma_load_3d_pair(sa, &map_x, fb, kb * kLmBK, m * kRowsPerBlock + r * 128,
+                                         xstep, pol_x);
+                    else
+                        tma_load_2d_pair(sa, &map_x, fb, kb * kLmBK, m * kRowsPerBlock + r * 128,
+                                         pol_x);
+                    for (int j = 0; j < 2; ++j)
+                        tma_load_2d_pair(sb + j * kLmBBoxBytes, &map_w, fb,
+                                         n * a.BN + r * 128 + j * 64, kb * kLmBK, pol_w);
+                    armed |= 1u << s;
+                    armed_par = (armed_par & ~(1u << s)) | (ph << s);
+                    if (++s == kDuoStages) { s = 0; ph ^= 1u; }
+                }
+            }
+            // the even CTA: every copy of both CTAs has landed before the
+            // closing cluster barrier lets either CTA leave
+            if (r == 0)
+                for (int q = 0; q < kDuoStages; ++q)
+                    if (armed >> q & 1u) mbar_wait(&full[q], armed_par >> q & 1u, a.ws, 402);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && r == 0) {
+            const uint32_t idesc = make_idesc_bf16(256, a.BN, 1);
+            const uint32_t sa0 = smem_u32(smem);
+            const uint64_t adesc0 = make_sdesc_sw128(sa0, 16, 1024);
+            const uint64_t bdesc0 = make_sdesc_sw128(sa0 + kPairABytes, kLmBBoxBytes, 1024);
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int acc = i & 1;
+                const uint32_t use = static_cast<uint32_t>(i >> 1);
+                if (!mbar_wait_cluster(&acc_empty[acc], (use & 1u) ^ 1u, a.ws, 404)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * a.BN);
+                for (int kb = 0; kb < a.kblocks; ++kb) {
+                    if (!mbar_wait(&full[s], ph, a.ws, 405)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t soff = static_cast<uint64_t>((s * kDuoStageBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kLmBK / 16; ++kk) {
+                        // A: K-major 128-byte rows, 8-row groups 1 KB apart, +32 B per k step;
+                        // B: MN-major, 64-column blocks 8 KB apart, 8-row groups 1 KB apart
+                        const uint64_t adesc = adesc0 + soff + static_cast<uint64_t>(kk * 2);
+                        const uint64_t bdesc = bdesc0 + soff + static_cast<uint64_t>(kk * (2048 >> 4));
+                        umma_bf16_pair(d, adesc, bdesc, idesc, (kb | kk) != 0);
+                    }
+                    umma_commit_pair(&empty[s], 0x3);
+                    if (++s == kDuoStages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair(&acc_full[acc], 0x3);
+            }
+            umma_commit_pair(mma_done, 0x1);
+            mbar_wait(mma_done, 0, a.ws, 406);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int cg = (warp - 4) >> 2;          // column group
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const int rix = q * 32 + lane;           // row within this CTA's 128 rows
+        const uint32_t lead_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
+        uint32_t merges = 0;
+        RowState st;
+        row_state_init(st);
+        int cur_m = -1;
+        for (int i = 0; i < ntiles; ++i) {
+            const int t = t0 + i;
+            const int m = t / a.ntn, n = t % a.ntn;
+            const int acc = i & 1;
+            const uint32_t use = static_cast<uint32_t>(i >> 1);
+            if (m != cur_m) {
+                if (cur_m >= 0) {
+                    const int prow = cur_m * kRowsPerBlock + r * 128 + rix;
+                    row_state_finalize(st, fc);
+                    group_merge_store(st, cg, rix, merges++, gm, a.part,
+                                      static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws);
+                }
+                row_state_init(st);
+                cur_m = m;
+            }
+            const bool ok = mbar_wait_cluster(&acc_full[acc], use & 1u, a.ws, 407);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            const int row = m * kRowsPerBlock + r * 128 + rix;
+            const bool live = row < a.M;
+            const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * a.BN);
+#pragma unroll 1
+            for (int c0 = 16 * cg; c0 < a.BN; c0 += 16 * kPairColGroups) {
+                float lg[16];
+                tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
+                const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
+                if (v0 < static_cast<uint32_t>(a.V))
+                    fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+            }
+            tc_fence_before();
+            __syncwarp();
+            // the even CTA's MMA may overwrite this accumulator once both
+            // CTAs' epilogues have read it
+            if (lane == 0) mbar_arrive_cluster(lead_acc_empty + static_cast<uint32_t>(acc * 8));
+        }
+        if (cur_m >= 0) {
+            const int prow = cur_m * kRowsPerBlock + r * 128 + rix;
+            row_state_finalize(st, fc);
+            group_merge_store(st, cg, rix, merges, gm, a.part,
+                              static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // no CTA releases its TMEM or leaves while the pair's MMAs, commits or
+    // remote arrivals may still reach it
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
+    }
+}
+
+}  // namespace dg

@@ -29,7 +29,7 @@
 //
 // Set-up: the first call on each device (with that device current) looks up
 // the device address of the array with cudaGetSymbolAddress, sets the LM-head
-// kernel's shared-memory limit and clears the status header (a synchronous
+// kernels' shared-memory limits and clears the status header (a synchronous
 // cudaMemset).  Make that first call before any stream capture.  Nothing here
 // calls cudaMalloc, cudaFree or any allocating library routine.  Kernels
 // launched by this entry point are not counted by dg_kernel_launches.
@@ -81,6 +81,8 @@ int na_setup(NoAllocDevice **out)
                                  kLmSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(lm_head_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(lm_head_duo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kDuoSmemBytes) != cudaSuccess ||
             cudaMemset(ptr, 0, sizeof(WsHeader)) != cudaSuccess) {
             (void)cudaGetLastError();
             return DG_ERR_CUDA;
@@ -171,7 +173,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
 
     CUtensorMap mx, mw;
     if ((rc = na_map(&mx, hidden, static_cast<uint64_t>(p->d), static_cast<uint64_t>(M), 64,
-                     plan.pair ? 128u : 256u)) != DG_OK)
+                     plan.cluster() ? 128u : 256u)) != DG_OK)
         return rc;
     if ((rc = na_map(&mw, w, static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d), 64, 64)) != DG_OK)
         return rc;
@@ -226,11 +228,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     acc.stop = io->stop;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (plan.pair)
-        lm_head_pair_kernel<<<plan.grid, kLmThreads, kPairSmemBytes, s>>>(mx, mw, a);
-    else
-        lm_head_kernel<<<plan.grid, kLmThreads, kLmSmemBytes, s>>>(mx, mw, a);
-    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    if (launch_lm_head(plan, mx, mw, a, s) != cudaSuccess) return DG_ERR_CUDA;
     combine_accept_kernel<<<dim3((p->L + 7) / 8, p->B), 256, 0, s>>>(c, acc);
     if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
     return DG_OK;

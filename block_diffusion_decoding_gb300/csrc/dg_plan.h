@@ -12,9 +12,16 @@ namespace dg {
 
 constexpr int kMaxSlots = 256;       // upper bound on LM-head CTAs (>= SM count)
 
+// LM-head kernels
+enum LmKind : int {
+    kLmSingle = 0,    // lm_head_kernel: one CTA per tile, 256 rows x BN columns
+    kLmPair = 1,      // lm_head_pair_kernel: 2-CTA cluster, W tile multicast
+    kLmDuo = 2,       // lm_head_duo_kernel: 2-CTA cluster, 2-SM UMMA
+};
+
 struct LmPlan {
     int M, V, d;
-    bool pair;        // 2-CTA cluster kernel (lm_head_pair_kernel) or single-CTA kernel
+    int kind;         // LmKind
     int BN;           // vocabulary columns per tile
     int ntn;          // vocabulary tiles per 256-row block
     int mblocks;      // 256-row blocks
@@ -23,10 +30,11 @@ struct LmPlan {
                       // slots, one partial state per (row, unit)
     int grid;         // CTAs launched
     int part_slots() const { return units; }
+    bool cluster() const { return kind != kLmSingle; }
 };
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
-// CTA, plus a per-tile overhead.  DG_LM_KERNEL=single|pair and DG_LM_BN
+// CTA, plus a per-tile overhead.  DG_LM_KERNEL=single|pair|duo and DG_LM_BN
 // force a choice.
 inline LmPlan plan_lm_head(int M, int d, int V, int sms)
 {
@@ -38,23 +46,30 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms)
     const char *env_bn = std::getenv("DG_LM_BN");
     const int forced_bn = env_bn ? std::atoi(env_bn) : 0;
     const char *env_k = std::getenv("DG_LM_KERNEL");
-    const bool only_single = env_k && std::strcmp(env_k, "single") == 0;
-    const bool only_pair = env_k && std::strcmp(env_k, "pair") == 0;
+    const int only = !env_k ? -1
+                     : std::strcmp(env_k, "single") == 0 ? kLmSingle
+                     : std::strcmp(env_k, "pair") == 0   ? kLmPair
+                     : std::strcmp(env_k, "duo") == 0    ? kLmDuo
+                                                         : -1;
     long best_cost = -1;
-    auto consider = [&](bool pair, int bn) {
+    auto consider = [&](int kind, int bn) {
         if (forced_bn && bn != forced_bn) return;
-        if ((pair && only_single) || (!pair && only_pair)) return;
+        if (only >= 0 && kind != only) return;
+        const bool pair = kind != kLmSingle;
         const int ntn = (V + bn - 1) / bn;
         const int total = ntn * best.mblocks;
         const int cap = pair ? std::max(1, sms / 2) : sms;
         const int units = std::min(std::min(total, cap), kMaxSlots / (pair ? 2 : 1));
         const long per_unit = (total + units - 1) / units;
-        // per-SM columns of a tile: bn (single, 256 rows) or bn / 2 (pair, 128
-        // rows each, and half the hidden-block traffic per tile)
-        const long cost = per_unit * (pair ? bn / 2 + 30 : bn + 40);
+        // per-SM columns of a tile: bn (single, 256 rows) or bn / 2 (clusters,
+        // 128 rows each, and half the hidden-block traffic per tile), plus a
+        // per-tile overhead (the 2-SM UMMA kernel moves a third less shared
+        // memory per k block than the multicast one)
+        const long over = kind == kLmSingle ? 40 : kind == kLmPair ? 30 : 25;
+        const long cost = per_unit * ((pair ? bn / 2 : bn) + over);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            best.pair = pair;
+            best.kind = kind;
             best.BN = bn;
             best.ntn = ntn;
             best.total = total;
@@ -62,10 +77,31 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms)
             best.grid = pair ? 2 * units : units;
         }
     };
-    for (int bn = 128; bn >= 64; bn -= 16) consider(false, bn);
-    consider(true, 256);
-    consider(true, 128);
+    for (int bn = 128; bn >= 64; bn -= 16) consider(kLmSingle, bn);
+    consider(kLmPair, 256);
+    consider(kLmPair, 128);
+    consider(kLmDuo, 256);
     return best;
+}
+
+inline int lm_smem_bytes(int kind)
+{
+    return kind == kLmSingle ? kLmSmemBytes : kind == kLmPair ? kPairSmemBytes : kDuoSmemBytes;
+}
+
+// Launch the planned LM-head kernel (maps: X box {64, 128} for the cluster
+// kernels, {64, 256} otherwise; W box {64, 64}).
+inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, const CUtensorMap &mw,
+                                  const LmHeadArgs &a, cudaStream_t st)
+{
+    const int smem = lm_smem_bytes(plan.kind);
+    if (plan.kind == kLmSingle)
+        lm_head_kernel<<<plan.grid, kLmThreads, smem, st>>>(mx, mw, a);
+    else if (plan.kind == kLmPair)
+        lm_head_pair_kernel<<<plan.grid, kLmThreads, smem, st>>>(mx, mw, a);
+    else
+        lm_head_duo_kernel<<<plan.grid, kLmThreads, smem, st>>>(mx, mw, a);
+    return cudaGetLastError();
 }
 
 // Upper bound on the partial-state slots of any plan for these shapes

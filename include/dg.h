@@ -218,11 +218,12 @@ uint64_t dg_kernel_launches(void);
 
 /* The LM-head launch dg_denoise_step would make on the current device for    */
 /* rows = B*L canvas positions, hidden size d and vocabulary V (no launch).   */
-/* *cluster_ctas: 1 = single-CTA kernel, 2 = 2-CTA cluster kernel; *bn:       */
-/* vocabulary columns per tile; *ctas: CTAs launched.  Any output pointer may */
-/* be NULL.  Returns DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED for shapes the   */
-/* step rejects, DG_ERR_CUDA without a device. */
-int dg_lm_head_plan(int rows, int d, int V, int *cluster_ctas, int *bn, int *ctas);
+/* *kind: 0 = single-CTA kernel, 1 = 2-CTA cluster with the W tile multicast */
+/* to both CTAs, 2 = 2-CTA cluster issuing 2-SM UMMAs; *bn: vocabulary        */
+/* columns per tile; *ctas: CTAs launched.  Any output pointer may be NULL.   */
+/* Returns DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED for shapes the step        */
+/* rejects, DG_ERR_CUDA without a device. */
+int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas);
 
 /* Acceptance, renoise and stop test alone on given entropy/sample/argmax     */
 /* [B*L] (device).  Writes canvas, accepted, n_accepted, stop, mean_entropy   */
