@@ -230,6 +230,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
                  const AcceptArgs &acc, cudaStream_t st, bool lm_only = false)
 {
     const int M = p->B * p->L;
+    const bool pdl = use_pdl(st);
     if (logits == nullptr) {
         CUtensorMap mx, mw;
         {
@@ -265,7 +266,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.ws = ws.hdr;
         a.counters = ws.counters;
         a.ncounters = p->B;
-        DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st));
+        DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl));
         DG_LAUNCHED();
     } else {
         FoldArgs f{};
@@ -296,8 +297,8 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     c.sample = sample;
     c.argmax = argmax;
     c.counters = ws.counters;
-    dim3 grid((p->L + 7) / 8, p->B);
-    combine_accept_kernel<<<grid, 256, 0, st>>>(c, acc);
+    DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + 7) / 8, p->B), dim3(256), 0, st,
+                              pdl, c, acc));
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
@@ -512,18 +513,16 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
         a.part_ml = reinterpret_cast<float *>(
             p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 4, 256));
     }
-    dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);
-    if (D == 128)
-        attn_kernel_d128<<<grid, kAttnThreads, attn_smem_bytes(128), st>>>(mkp, mvp, mkc, mvc, a);
-    else
-        attn_kernel_d256<<<grid, kAttnThreads, attn_smem_bytes(256), st>>>(mkp, mvp, mkc, mvc, a);
+    const bool pdl = use_pdl(st);
+    DG_CUDA_TRY(launch_kernel(D == 128 ? attn_kernel_d128 : attn_kernel_d256,
+                              dim3(ap.mtiles, Hkv * B, ap.nsplit), dim3(kAttnThreads),
+                              attn_smem_bytes(D), st, pdl, mkp, mvp, mkc, mvc, a));
     DG_LAUNCHED();
-    DG_CUDA_TRY(cudaGetLastError());
     if (ap.nsplit > 1) {
         const size_t nr = static_cast<size_t>(B) * L * Hq;
-        attn_combine_kernel<<<static_cast<unsigned>((nr + 7) / 8), 256, 0, st>>>(a);
+        DG_CUDA_TRY(launch_kernel(attn_combine_kernel, dim3(static_cast<unsigned>((nr + 7) / 8)),
+                                  dim3(256), 0, st, pdl, a));
         DG_LAUNCHED();
-        DG_CUDA_TRY(cudaGetLastError());
     }
     return DG_OK;
 }

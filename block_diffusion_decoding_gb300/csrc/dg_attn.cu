@@ -111,6 +111,9 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
     uint64_t *o_full = q_ready + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_full + 1);
 
+    // inputs may come from the previous kernel of the stream
+    griddep_wait();
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x;
     const int bg = blockIdx.y;
@@ -403,6 +406,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // Merge the key splits: one warp per query row, lanes over the head dim.
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const size_t nrows = static_cast<size_t>(a.B) * a.L * a.Hq;
     const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;

@@ -45,6 +45,24 @@ DG_DEVICE uint64_t globaltimer_ns()
 }
 
 // ------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream runs; it
+// waits here before touching memory that kernel reads or writes.  Without
+// the launch attribute both are no-ops.
+// ------------------------------------------------------------------------
+DG_DEVICE void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel of the stream launch (once every CTA of this grid has
+// called this or exited).
+DG_DEVICE void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------
 DG_DEVICE void mbar_init(uint64_t *bar, uint32_t count)

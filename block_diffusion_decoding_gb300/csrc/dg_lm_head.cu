@@ -54,9 +54,6 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int t0 = tile_begin(c, a.total, n_slots), t1 = tile_begin(c + 1, a.total, n_slots);
     const int ntiles = t1 - t0;
 
-    if (c == 0 && warp == 2) {
-        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
-    }
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kLmStages; ++s) {
             mbar_init(&full[s], 1);
@@ -81,6 +78,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel of the stream; from here on
+    // its outputs are visible and the memory it reads may be overwritten
+    griddep_wait();
+    griddep_launch_dependents();
+    if (c == 0 && warp == 2) {
+        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
+    }
     const FoldConsts fc = fold_consts(a.src, a.seed);
     const int xstep = a.x_3d ? static_cast<int>(fc.step) : 0;
 

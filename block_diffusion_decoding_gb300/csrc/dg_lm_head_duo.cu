@@ -3,17 +3,17 @@
 // full-vocabulary softmax the "Parallel Denoising From an Autoregressive
 // Checkpoint" page, section "Finding", names as a per-step cost).
 //
-// A tile is 256 canvas rows x 256 vocabulary columns.  CTA rank r of the
-// pair streams rows [128 r, 128 r + 128) of the hidden block and columns
-// [128 r, 128 r + 128) of the W tile into its own shared memory; the even
-// CTA issues one 256 x 256 x 16 UMMA per 16-deep k step that reads both
-// CTAs' halves, and each CTA receives its 128 rows x 256 columns of the
-// product in its own TMEM (double-buffered, 2 x 256 columns).  Compared with
+// A tile is 256 canvas rows x BN (256 or 128) vocabulary columns.  CTA rank
+// r of the pair streams rows [128 r, 128 r + 128) of the hidden block and
+// columns [r BN/2, (r + 1) BN/2) of the W tile into its own shared memory;
+// the even CTA issues one 256 x BN x 16 UMMA per 16-deep k step that reads
+// both CTAs' halves, and each CTA receives its 128 rows x BN columns of the
+// product in its own TMEM (double-buffered, 2 x BN columns).  Compared with
 // a W tile multicast to both CTAs, every CTA writes and the tensor core reads
 // a third less shared memory per k block, which is what bounds the single-CTA
 // MMA at this shape.
 //
-//   warp 0      TMA producer (both CTAs): X[128 rows, 64] and W[64, 128] of
+//   warp 0      TMA producer (both CTAs): X[128 rows, 64] and W[64, BN/2] of
 //               its own halves into a 6-stage ring; both CTAs' copies
 //               complete on the even CTA's full barrier (the even CTA expects
 //               the bytes of both halves); a stage is free once the pair MMAs
@@ -54,10 +54,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     const int ncl = static_cast<int>(num_clusters_x());
     const int t0 = tile_begin(cid, a.total, ncl), t1 = tile_begin(cid + 1, a.total, ncl);
     const int ntiles = t1 - t0;
+    const int half_boxes = a.BN / 128;                           // W boxes this CTA loads
+    const uint32_t stage_tx = static_cast<uint32_t>(kPairABytes + half_boxes * kLmBBoxBytes);
 
-    if (cid == 0 && r == 0 && warp == 2) {
-        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
-    }
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kDuoStages; ++s) {
             mbar_init(&full[s], 1);          // used in the even CTA only
@@ -84,6 +83,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     // both CTAs' barriers exist before either signals the other
     cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel of the stream; from here on
+    // its outputs are visible and the memory it reads may be overwritten
+    griddep_wait();
+    griddep_launch_dependents();
+    if (cid == 0 && r == 0 && warp == 2) {
+        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
+    }
     const FoldConsts fc = fold_consts(a.src, a.seed);
     const int xstep = a.x_3d ? static_cast<int>(fc.step) : 0;
 
@@ -101,7 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
                 const int m = t / a.ntn, n = t % a.ntn;
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.ws, 401)) { ok = false; break; }
-                    if (r == 0) mbar_arrive_expect_tx(&full[s], 2 * kDuoStageBytes);
+                    if (r == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_tx);
                     const uint32_t fb = lead_full + static_cast<uint32_t>(s * 8);
                     uint8_t *sa = smem + s * kDuoStageBytes;
                     uint8_t *sb = sa + kPairABytes;
@@ -112,9 +118,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
                     else
                         tma_load_2d_pair(sa, &map_x, fb, kb * kLmBK, m * kRowsPerBlock + r * 128,
                                          pol_x);
-                    for (int j = 0; j < 2; ++j)
+                    for (int j = 0; j < half_boxes; ++j)
                         tma_load_2d_pair(sb + j * kLmBBoxBytes, &map_w, fb,
-                                         n * a.BN + r * 128 + j * 64, kb * kLmBK, pol_w);
+                                         n * a.BN + r * (a.BN / 2) + j * 64, kb * kLmBK, pol_w);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == kDuoStages) { s = 0; ph ^= 1u; }

@@ -51,9 +51,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     const int ntiles = t1 - t0;
     const int half_boxes = a.BN / 128;                           // W boxes this CTA loads
 
-    if (cid == 0 && r == 0 && warp == 2) {
-        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
-    }
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kPairStages; ++s) {
             mbar_init(&full[s], 1);
@@ -80,6 +77,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     // both CTAs' barriers exist before either multicasts into the other
     cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
+    // set-up above overlaps the previous kernel of the stream; from here on
+    // its outputs are visible and the memory it reads may be overwritten
+    griddep_wait();
+    griddep_launch_dependents();
+    if (cid == 0 && r == 0 && warp == 2) {
+        for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
+    }
     const FoldConsts fc = fold_consts(a.src, a.seed);
     const int xstep = a.x_3d ? static_cast<int>(fc.step) : 0;
 

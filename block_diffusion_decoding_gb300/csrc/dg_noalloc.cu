@@ -228,8 +228,10 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     acc.stop = io->stop;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_lm_head(plan, mx, mw, a, s) != cudaSuccess) return DG_ERR_CUDA;
-    combine_accept_kernel<<<dim3((p->L + 7) / 8, p->B), 256, 0, s>>>(c, acc);
-    if (cudaGetLastError() != cudaSuccess) return DG_ERR_CUDA;
+    const bool pdl = use_pdl(s);
+    if (launch_lm_head(plan, mx, mw, a, s, pdl) != cudaSuccess) return DG_ERR_CUDA;
+    if (launch_kernel(combine_accept_kernel, dim3((p->L + 7) / 8, p->B), dim3(256), 0, s, pdl, c,
+                      acc) != cudaSuccess)
+        return DG_ERR_CUDA;
     return DG_OK;
 }

@@ -81,6 +81,7 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms)
     consider(kLmPair, 256);
     consider(kLmPair, 128);
     consider(kLmDuo, 256);
+    consider(kLmDuo, 128);
     return best;
 }
 
@@ -89,19 +90,47 @@ inline int lm_smem_bytes(int kind)
     return kind == kLmSingle ? kLmSmemBytes : kind == kLmPair ? kPairSmemBytes : kDuoSmemBytes;
 }
 
+// Launch with programmatic stream serialization when `pdl` is set: the kernel
+// may start while the previous kernel of the stream is still running (every
+// kernel of the step waits, griddep_wait, before it touches memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool pdl, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Programmatic launches are used outside stream capture only.
+inline bool use_pdl(cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return cs == cudaStreamCaptureStatusNone;
+}
+
 // Launch the planned LM-head kernel (maps: X box {64, 128} for the cluster
 // kernels, {64, 256} otherwise; W box {64, 64}).
 inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, const CUtensorMap &mw,
-                                  const LmHeadArgs &a, cudaStream_t st)
+                                  const LmHeadArgs &a, cudaStream_t st, bool pdl)
 {
     const int smem = lm_smem_bytes(plan.kind);
-    if (plan.kind == kLmSingle)
-        lm_head_kernel<<<plan.grid, kLmThreads, smem, st>>>(mx, mw, a);
-    else if (plan.kind == kLmPair)
-        lm_head_pair_kernel<<<plan.grid, kLmThreads, smem, st>>>(mx, mw, a);
-    else
-        lm_head_duo_kernel<<<plan.grid, kLmThreads, smem, st>>>(mx, mw, a);
-    return cudaGetLastError();
+    auto kern = plan.kind == kLmSingle ? lm_head_kernel
+                : plan.kind == kLmPair ? lm_head_pair_kernel
+                                       : lm_head_duo_kernel;
+    return launch_kernel(kern, dim3(plan.grid), dim3(kLmThreads), smem, st, pdl, mx, mw, a);
 }
 
 // Upper bound on the partial-state slots of any plan for these shapes

@@ -76,69 +76,77 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
 }
 
 // ---------------------------------------------------------------- accept (one canvas)
+// Rank of every key among the L keys (H, position) gives the ascending order
+// without a sorting network; the exclusive prefix sums of the sorted
+// entropies (fp64) then count the accepted prefix: they never decrease, so
+// k* = #{j : sum of the first j sorted entropies <= b} (and k* >= 1).
 __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float *__restrict__ H,
                               const int32_t *__restrict__ sample,
                               const int32_t *__restrict__ argmax)
 {
     __shared__ uint64_t keys[kMaxCanvas];
-    __shared__ double scan[2][kMaxCanvas];
+    __shared__ uint64_t sorted[kMaxCanvas];
+    __shared__ double wsum[32];
     __shared__ int s_kstar;
     const int tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
     const int L = a.L;
-    int Lp = 1;
-    while (Lp < L) Lp <<= 1;
     const size_t base = static_cast<size_t>(b) * L;
 
     // keys (H, position): H >= 0, so its bit pattern orders like the value
-    for (int i = tid; i < Lp; i += nt) {
-        if (i < L) {
-            const float h = __ldcg(H + base + i);
-            keys[i] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(i);
-        } else {
-            keys[i] = ~0ull;
+    for (int i = tid; i < L; i += nt) {
+        const float h = __ldcg(H + base + i);
+        keys[i] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(i);
+    }
+    if (tid == 0) s_kstar = 0;
+    __syncthreads();
+    for (int i = tid; i < L; i += nt) {
+        const uint64_t k = keys[i];
+        int rank = 0;
+#pragma unroll 8
+        for (int j = 0; j < L; ++j) rank += (keys[j] < k) ? 1 : 0;
+        sorted[rank] = k;
+    }
+    __syncthreads();
+    // sorted positions [j0, j1) of this thread; block exclusive scan in fp64
+    const int per = (L + nt - 1) / nt;
+    const int j0 = min(L, tid * per), j1 = min(L, j0 + per);
+    auto hval = [&](int j) {
+        return static_cast<double>(__uint_as_float(static_cast<uint32_t>(sorted[j] >> 32)));
+    };
+    double loc = 0.0;
+    for (int j = j0; j < j1; ++j) loc += hval(j);
+    double incl = loc;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const double o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        double w = (lane < nw) ? wsum[lane] : 0.0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double o = __shfl_up_sync(0xFFFFFFFFu, w, off);
+            if (lane >= off) w += o;
         }
-    }
-    if (tid == 0) s_kstar = 1;
-    __syncthreads();
-    // bitonic sort, ascending
-    for (int k = 2; k <= Lp; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < Lp; i += nt) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const uint64_t x = keys[i], y = keys[ixj];
-                    const bool up = (i & k) == 0;
-                    if (up ? (x > y) : (x < y)) { keys[i] = y; keys[ixj] = x; }
-                }
-            }
-            __syncthreads();
-        }
-    }
-    // exclusive prefix sums of the sorted entropies, fp64, fixed tree order
-    for (int j = tid; j < Lp; j += nt) {
-        double v = 0.0;
-        if (j >= 1 && j - 1 < L)
-            v = static_cast<double>(__uint_as_float(static_cast<uint32_t>(keys[j - 1] >> 32)));
-        scan[0][j] = v;
+        if (lane < nw) wsum[lane] = w;      // inclusive warp totals
     }
     __syncthreads();
-    int src = 0;
-    for (int off = 1; off < Lp; off <<= 1) {
-        for (int j = tid; j < Lp; j += nt)
-            scan[src ^ 1][j] = (j >= off) ? scan[src][j] + scan[src][j - off] : scan[src][j];
-        src ^= 1;
-        __syncthreads();
+    double run = incl - loc + (wid > 0 ? wsum[wid - 1] : 0.0);
+    int cnt = 0;
+    for (int j = j0; j < j1; ++j) {
+        cnt += (run <= static_cast<double>(a.bound)) ? 1 : 0;
+        run += hval(j);
     }
-    // k* = max { k in [1, L] : sum of the first k-1 sorted entropies <= b }
-    int local = 1;
-    for (int j = tid; j < L; j += nt)
-        if (scan[src][j] <= static_cast<double>(a.bound)) local = max(local, j + 1);
-    atomicMax(&s_kstar, local);
+    if (cnt) atomicAdd(&s_kstar, cnt);
     __syncthreads();
-    const int kstar = s_kstar;
+    const int kstar = max(1, s_kstar);
+    const double total = wsum[nw - 1];
     const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
     for (int j = tid; j < L; j += nt) {
-        const int pos = static_cast<int>(keys[j] & 0xFFFFFFFFu);
+        const int pos = static_cast<int>(sorted[j] & 0xFFFFFFFFu);
         const size_t r = base + pos;
         if (j < kstar) {
             a.canvas[r] = __ldcg(sample + r);
@@ -157,9 +165,6 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
     const int all_same = __syncthreads_and(same);
     for (int i = tid; i < L; i += nt) a.prev_argmax[base + i] = __ldcg(argmax + base + i);
     if (tid == 0) {
-        const double lastH =
-            static_cast<double>(__uint_as_float(static_cast<uint32_t>(keys[L - 1] >> 32)));
-        const double total = scan[src][L - 1] + lastH;
         const double mean = total / static_cast<double>(L);
         const int stop = (step >= 1 && all_same && mean < static_cast<double>(a.threshold)) ? 1 : 0;
         a.n_accepted[b] = kstar;
@@ -204,6 +209,8 @@ __device__ void loop_advance(const AcceptArgs &a)
 // the acceptance for it.
 __global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, AcceptArgs a)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int b = blockIdx.y;
     if (a.ctl != nullptr && __ldcg(a.done + b) != 0) return;   // canvas already stopped
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
