@@ -261,17 +261,33 @@ def run_ours(args, cfg):
     bf = torch.bfloat16
     B, L, Hq, Hkv, D, P, d, V = cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V
     M = B * L
-    q = torch.randn(B, L, Hq, D, device=dev, generator=g).to(bf)
+    # the per-step inputs (canvas hidden states, canvas queries, canvas keys
+    # and values) live in one device block, so the end-to-end run moves them
+    # from one pinned host block with a single copy
+    shapes = {"x": (M, d), "q": (B, L, Hq, D), "kc": (B, L, Hkv, D), "vc": (B, L, Hkv, D)}
+    offs, tot = {}, 0
+    for k, shp in shapes.items():
+        offs[k] = tot
+        tot += (math.prod(shp) * 2 + 255) // 256 * 256
+    step_in = torch.empty(tot, dtype=torch.uint8, device=dev)
+
+    def view(k):
+        n = math.prod(shapes[k]) * 2
+        return step_in[offs[k]:offs[k] + n].view(bf).view(shapes[k])
+
+    q, kc, vc, x = view("q"), view("kc"), view("vc"), view("x")
+    q.copy_(torch.randn(B, L, Hq, D, device=dev, generator=g))
     kp = torch.randn(B, P, Hkv, D, device=dev, generator=g).to(bf)
     vp = torch.randn(B, P, Hkv, D, device=dev, generator=g).to(bf)
-    kc = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
-    vc = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+    kc.copy_(torch.randn(B, L, Hkv, D, device=dev, generator=g))
+    vc.copy_(torch.randn(B, L, Hkv, D, device=dev, generator=g))
     attn_out = torch.empty_like(q)
-    x = torch.randn(M, d, device=dev, generator=g)
+    xf = torch.randn(M, d, device=dev, generator=g)
     if cfg.row_scale is not None:
         lo, hi = cfg.row_scale
-        x *= torch.rand(M, 1, device=dev, generator=g) * (hi - lo) + lo
-    x = x.to(bf)
+        xf *= torch.rand(M, 1, device=dev, generator=g) * (hi - lo) + lo
+    x.copy_(xf)
+    del xf
     w = torch.empty(d, V, device=dev, dtype=bf)
     for r0 in range(0, d, 256):
         r1 = min(d, r0 + 256)
@@ -343,26 +359,20 @@ def run_ours(args, cfg):
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
     traffic = _traffic_record(srcs, lm_plan["kernel"])
 
-    # ---- end to end through the C ABI with host buffers (pinned), per-step H2D + D2H
-    h_x = x.cpu().pin_memory()
-    h_q, h_kc, h_vc = q.cpu().pin_memory(), kc.cpu().pin_memory(), vc.cpu().pin_memory()
-    h_canvas = torch.empty(M, dtype=torch.int32).pin_memory()
-    h_argmax = torch.empty(M, dtype=torch.int32).pin_memory()
-    h_stop = torch.empty(B, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_q, h_kc, h_vc))
-    d2h = sum(t.numel() * t.element_size() for t in (h_canvas, h_argmax, h_stop))
+    # ---- end to end through the C ABI with host buffers (pinned): per step,
+    # one H2D copy of the step's inputs (hidden states, canvas Q/K/V) and one
+    # D2H copy of the result (canvas, argmax, stop)
+    h_in = step_in.cpu().pin_memory()
+    h_out = torch.empty_like(bufs.readback, device="cpu").pin_memory()
+    h2d = step_in.numel()
+    d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step(k):
-        x.copy_(h_x, non_blocking=True)
-        q.copy_(h_q, non_blocking=True)
-        kc.copy_(h_kc, non_blocking=True)
-        vc.copy_(h_vc, non_blocking=True)
+        step_in.copy_(h_in, non_blocking=True)
         step(k)
-        h_canvas.copy_(bufs.canvas, non_blocking=True)
-        h_argmax.copy_(bufs.argmax, non_blocking=True)
-        h_stop.copy_(bufs.stop, non_blocking=True)
+        h_out.copy_(bufs.readback, non_blocking=True)
         torch.cuda.synchronize(dev)
-        return int(h_stop[0])
+        return int(h_out[-1])
 
     for i in range(2):
         e2e_step(i)
@@ -398,29 +408,235 @@ def run_ours(args, cfg):
     if rank != 0:
         return 0
     value = world * 1e3 / step_ms
+    # each kernel's roofline: the slower of its algorithmic bytes at the
+    # measured copy bandwidth and its FLOPs at the measured bf16 peak
+    lm_roof_ms = max(lm_bytes / (hbm_peak * 1e9), lm_flops / (bf16_peak * 1e12)) * 1e3
+    at_roof_ms = max(at_bytes / (hbm_peak * 1e9), at_flops / (bf16_peak * 1e12)) * 1e3
+    lm_tensor = lm_flops / (bf16_peak * 1e12) > lm_bytes / (hbm_peak * 1e9)
+    lm_tflops = lm_flops / (lm_ms * 1e-3) / 1e12
+    if lm_tensor:
+        roof = dict(bound="tensor", achieved=lm_tflops, peak=bf16_peak, unit="TFLOP/s",
+                    frac=lm_tflops / bf16_peak, traffic=traffic, kernel=lm_plan["kernel"],
+                    peak_source=peak_kind + " (MEASURED_PEAKS.json bf16_tflops, burst)",
+                    algorithmic_flops=lm_flops)
+    else:
+        roof = dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
+                    frac=lm_gbs / hbm_peak, traffic=traffic, kernel=lm_plan["kernel"],
+                    peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
+                    algorithmic_bytes=lm_bytes)
     line = dict(
         metric="denoise steps/s (256-tok canvas, bs=1)", value=value, unit="steps/s",
         n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=step_ms,
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
         data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step"),
         canvas_tokens_per_s=value * M,
-        roofline=dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
-                      frac=lm_gbs / hbm_peak, traffic=traffic, kernel=lm_plan["kernel"],
-                      peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
-                      algorithmic_bytes=lm_bytes),
-        kernels={lm_plan["kernel"]: {"ms": lm_ms, "GB_per_s": lm_gbs,
-                                     "TFLOP_per_s": lm_flops / (lm_ms * 1e-3) / 1e12,
+        roofline=roof,
+        kernels={lm_plan["kernel"]: {"ms": lm_ms, "GB_per_s": lm_gbs, "TFLOP_per_s": lm_tflops,
+                                     "roofline_ms": lm_roof_ms, "frac_of_roofline": lm_roof_ms / lm_ms,
                                      "BN": lm_plan["BN"], "ctas": lm_plan["ctas"]},
                  "canvas_attn": {"ms": at_ms, "TFLOP_per_s": at_flops / (at_ms * 1e-3) / 1e12,
-                                 "frac_of_bf16_peak": at_flops / (at_ms * 1e-3) / 1e12 / bf16_peak,
-                                 "GB_per_s": at_bytes / (at_ms * 1e-3) / 1e9}},
-        step_roofline_ms=(lm_bytes / (hbm_peak * 1e9) + at_flops / (bf16_peak * 1e12)) * 1e3,
+                                 "GB_per_s": at_bytes / (at_ms * 1e-3) / 1e9,
+                                 "roofline_ms": at_roof_ms, "frac_of_roofline": at_roof_ms / at_ms}},
+        step_roofline_ms=lm_roof_ms + at_roof_ms,
+        step_frac_of_roofline=(lm_roof_ms + at_roof_ms) / step_ms,
         cpu_baseline=cpu,
         e2e=dict(value=world * 1e3 / e2e_ms, unit="steps/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h),
         clocks=clk.summary(), gpu_launches=launches, device_status=status)
     print(json.dumps(line), flush=True)
     return 0
+
+# ----------------------------------------------------------------------------- block loop
+def run_block(args, cfg):
+    """The block loop (dg_generate_block, one CUDA graph per block) on the
+    converging workload: hidden(k) = g_k(c) W[:,t]/|W[:,t]| + N(0, 1/d) for
+    per-position targets t ~ U(V) and confidences c ~ U(0, 1); a block runs
+    until every canvas stops (argmax unchanged and mean entropy < 0.005) or
+    48 steps.  K timed blocks, L2 flushed before each; value = denoise steps
+    per second inside the loop (steps taken / block time)."""
+    import torch
+    import block_diffusion_decoding_gb300 as dg
+    from block_diffusion_decoding_gb300 import build as dgbuild
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+    dgbuild.build()
+    dg.lib()
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    g = torch.Generator(device=dev).manual_seed(2000 + rank)
+    bf = torch.bfloat16
+    B, L, d, V, N = cfg.B, cfg.L, cfg.d, cfg.V, cfg.max_steps
+    M = B * L
+    w = torch.empty(d, V, device=dev, dtype=bf)
+    for r0 in range(0, d, 256):
+        r1 = min(d, r0 + 256)
+        w[r0:r1] = (torch.randn(r1 - r0, V, device=dev, generator=g) * cfg.w_std).to(bf)
+    t = torch.randint(0, V, (M,), device=dev, generator=g)
+    c = torch.rand(M, device=dev, generator=g, dtype=torch.float64)
+    cols = w[:, t].double().T
+    cols /= cols.norm(dim=1, keepdim=True)
+    hid = torch.empty(N, M, d, device=dev, dtype=bf)
+    for k in range(N):
+        gk = (2.0 + 6.0 * c) * (1.0 + k / 4.0)
+        noise = torch.randn(M, d, device=dev, generator=g, dtype=torch.float64) / math.sqrt(d)
+        hid[k] = (gk[:, None] * cols + noise).to(bf)
+    del cols
+    p = dg.step_params(B, L, d, V, cfg.t_start, cfg.entropy_bound, cfg.stop_threshold, 0,
+                       seed=rank)
+    bp = dg.block_params(N, cfg.t_start, cfg.t_end, M * d)
+    bufs = dg.BlockBuffers(B, L, N, dev)
+    bws = dg.workspace(dg.generate_block_workspace(p, bp), dev)
+    sws = dg.workspace(dg.denoise_step_workspace(p), dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, n):
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record(stream)
+            fn()
+            e_.record(stream)
+            evs.append((s_, e_))
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b_) for a, b_ in evs]
+
+    def block():
+        dg.generate_block(hid, w, p, bp, bufs, bws)
+
+    with ClockSampler(local) as clk:
+        clk.wait_first()
+        timed(block, args.warmup)
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = time.perf_counter()
+        ts = timed(block, args.steps)
+        t_end = time.perf_counter()
+        clk.mark(t_start, t_end)
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    status = dg.read_device_status(bws)
+    steps = int(bufs.steps_taken.max().item())
+    hist = bufs.n_accepted_hist.view(N, B)[:steps].float()
+    block_ms = sum(ts) / len(ts)
+    if world > 1:
+        tt = torch.tensor([block_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        block_ms = float(tt.item())
+    step_ms = block_ms / steps
+
+    # flat logits (hidden = 0): exactly one commit per step, 48 steps
+    flat = torch.zeros(M, d, device=dev, dtype=bf)
+    fbp = dg.block_params(N, cfg.t_start, cfg.t_end, 0)
+    fbufs = dg.BlockBuffers(B, L, N, dev)
+    dg.generate_block(flat, w, p, fbp, fbufs, bws)
+    torch.cuda.synchronize(dev)
+    flat_ok = (int(fbufs.steps_taken.min().item()) == N and
+               bool((fbufs.n_accepted_hist == 1).all().item()))
+
+    # the LM-head kernel alone on the first step's hidden states (roofline)
+    lm_ms = statistics.mean(timed(lambda: dg.lm_head_fold(hid[0], w, p, sws), args.steps))
+    lm_bytes = d * V * 2 + M * d * 2
+    lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
+    lm_plan = dg.lm_head_plan(M, d, V)
+    srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
+            for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
+                      "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
+    traffic = _traffic_record(srcs, lm_plan["kernel"])
+
+    # end to end: the block's hidden states go up from pinned host memory,
+    # the result (canvas, argmax, steps taken) comes back
+    h_hid = hid.cpu().pin_memory()
+    h_out = [torch.empty_like(tns, device="cpu").pin_memory()
+             for tns in (bufs.canvas, bufs.argmax, bufs.steps_taken)]
+    e2e_times = []
+    for i in range(args.steps + 1):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        hid.copy_(h_hid, non_blocking=True)
+        block()
+        for h, dsrc in zip(h_out, (bufs.canvas, bufs.argmax, bufs.steps_taken)):
+            h.copy_(dsrc, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if i > 0:
+            e2e_times.append(time.perf_counter() - t0)
+    e2e_ms = 1e3 * sum(e2e_times) / len(e2e_times)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {"x": hid[0].view(torch.int16).cpu().numpy().view(np.uint16),
+                "w": w[:, :16384].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)}
+        est = [oracle_block_step_estimate(cfg, host)[0] for _ in range(2)]
+        _, desc = oracle_block_step_estimate(cfg, host)
+        cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle",
+                   sample=desc)
+    if world > 1:
+        tdist.destroy_process_group()
+    if rank != 0:
+        return 0
+    value = world * 1e3 / step_ms
+    line = dict(
+        metric="denoise steps/s (256-tok canvas, bs=1)", value=value, unit="steps/s",
+        n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=step_ms,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+        data="synthetic",
+        config={"workload": "%s: block loop (CUDA graph, conditional while), B=%d L=%d, LM head "
+                            "d=%d V=%d, T %.1f->%.1f over %d steps, b=%.1f, stop mean H < %.3f; "
+                            "timed unit = one block" % (cfg.name, B, L, d, V, cfg.t_start,
+                                                        cfg.t_end, N, cfg.entropy_bound,
+                                                        cfg.stop_threshold),
+                "global_batch": B, "seq_len": L, "parallelism": "replicas",
+                "l2": "flushed (256 MiB write) before every block"},
+        block_ms=block_ms, steps_to_stop=steps,
+        commits_per_step=float(hist.mean().item()),
+        canvas_tokens_per_s=world * M / (block_ms * 1e-3),
+        flat_case_one_commit_per_step_48_steps=flat_ok,
+        roofline=dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
+                      frac=lm_gbs / hbm_peak, traffic=traffic, kernel=lm_plan["kernel"],
+                      peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
+                      algorithmic_bytes=lm_bytes),
+        step_roofline_ms=lm_bytes / (hbm_peak * 1e9) * 1e3,
+        step_frac_of_roofline=lm_bytes / (hbm_peak * 1e9) * 1e3 / step_ms,
+        cpu_baseline=cpu,
+        e2e=dict(value=world * steps * 1e3 / e2e_ms, unit="steps/s",
+                 h2d_bytes_per_step=hid.numel() * 2 // steps,
+                 d2h_bytes_per_step=sum(h.numel() * h.element_size() for h in h_out) // steps),
+        clocks=clk.summary(),
+        gpu_launches=args.steps * (1 + 2 * steps), gpu_launches_note="graph replays: loop init "
+        "+ 2 kernels per step (LM head, combine/accept) per block",
+        device_status=status)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def oracle_block_step_estimate(cfg, host, v_sample=16384):
+    """One step of the block loop on the CPU oracle, column-sampled: every canvas
+    row against the first v_sample vocabulary columns (LM head + sampler, time
+    scaled by V / v_sample), then the acceptance and stop test."""
+    import oracle
+    vs = min(v_sample, cfg.V)
+    t0 = time.perf_counter()
+    lg = oracle.logits(host["x"], np.ascontiguousarray(host["w"][:, :vs]))
+    s = oracle.sampler(lg, cfg.t_start, 0, np.arange(cfg.M), 0)
+    t_lm = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    Hf = s["H"].astype(np.float32)
+    oracle.accept_renoise(Hf, s["sample"], np.zeros(cfg.M, np.int32), cfg.V, cfg.entropy_bound,
+                          0, 0, 0)
+    oracle.stop(s["argmax"], s["argmax"], Hf, 0)
+    t_acc = time.perf_counter() - t0
+    desc = ("oracle (fp64 C + numpy fp64 matmul, 1 thread): one loop step, all %d canvas rows x "
+            "%d of %d vocab columns (scaled x%.0f), acceptance + stop" % (cfg.M, vs, cfg.V,
+                                                                         cfg.V / vs))
+    return t_lm * cfg.V / vs + t_acc, desc
 
 
 def main():
@@ -436,6 +652,8 @@ def main():
     cfg = dg_synth.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if cfg.name == "block_full":
+        return run_block(args, cfg)
     return run_ours(args, cfg)
 
 

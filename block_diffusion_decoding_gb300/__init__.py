@@ -157,15 +157,18 @@ class StepBuffers:
     def __init__(self, B: int, L: int, device="cuda"):
         M = B * L
         i32 = dict(dtype=torch.int32, device=device)
-        self.canvas = torch.zeros(M, **i32)
+        # what a caller reads back after a step -- canvas, argmax, stop -- is
+        # one contiguous int32 block (`readback`), so one copy fetches it
+        self.readback = torch.zeros(2 * M + B, **i32)
+        self.canvas = self.readback[:M]
+        self.argmax = self.readback[M:2 * M]
+        self.stop = self.readback[2 * M:]
         self.prev_argmax = torch.full((M,), -1, **i32)
-        self.argmax = torch.zeros(M, **i32)
         self.sample = torch.zeros(M, **i32)
         self.entropy = torch.zeros(M, dtype=torch.float32, device=device)
         self.accepted = torch.zeros(M, dtype=torch.uint8, device=device)
         self.n_accepted = torch.zeros(B, **i32)
         self.mean_entropy = torch.zeros(B, dtype=torch.float32, device=device)
-        self.stop = torch.zeros(B, **i32)
 
     def io(self) -> StepIO:
         return StepIO(*[ctypes.c_void_p(getattr(self, n).data_ptr()) for n, _ in StepIO._fields_])
