@@ -450,10 +450,10 @@ DG_DEVICE uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// 32 lanes x 32 bit, 16 consecutive columns per thread.
-DG_DEVICE void tmem_ld16(uint32_t taddr, float (&v)[16])
+// 32 lanes x 32 bit, 16 consecutive columns per thread, issued without
+// waiting: the registers are valid only after tmem_wait_ld16 on them.
+DG_DEVICE void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16])
 {
-    uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -461,7 +461,25 @@ DG_DEVICE void tmem_ld16(uint32_t taddr, float (&v)[16])
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Waits for this thread's TMEM loads; the registers pass through the wait so
+// that no use of them can be scheduled before it.
+DG_DEVICE void tmem_wait_ld16(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+DG_DEVICE void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    tmem_ld16_issue(taddr, r);
+    tmem_wait_ld16(r);
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }

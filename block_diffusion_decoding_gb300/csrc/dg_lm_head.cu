@@ -200,16 +200,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const int row = m * kRowsPerBlock + h * 128 + q * 32 + lane;
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * 256 + h * 128);
             const bool live = row < a.M;
-            // one call site of the (large) fold keeps the hot loop in the
-            // instruction cache
-#pragma unroll 1
-            for (int c0 = 16 * cg; c0 < a.BN; c0 += 16 * kLmColGroups) {
-                float lg[16];
-                tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
-                const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
-                if (v0 < static_cast<uint32_t>(a.V))
-                    fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
-            }
+            fold_tile(st, tb, 16 * cg, 16 * kLmColGroups, a.BN, static_cast<uint32_t>(n * a.BN),
+                      static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);

@@ -201,14 +201,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             const int row = m * kRowsPerBlock + r * 128 + rix;
             const bool live = row < a.M;
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * a.BN);
-#pragma unroll 1
-            for (int c0 = 16 * cg; c0 < a.BN; c0 += 16 * kPairColGroups) {
-                float lg[16];
-                tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
-                const uint32_t v0 = static_cast<uint32_t>(n * a.BN + c0);
-                if (v0 < static_cast<uint32_t>(a.V))
-                    fold16(st, lg, v0, static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
-            }
+            fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, a.BN, static_cast<uint32_t>(n * a.BN),
+                      static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
             tc_fence_before();
             __syncwarp();
             // the even CTA's MMA may overwrite this accumulator once both

@@ -110,12 +110,20 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     const bool full = v0 + 16u <= V;
     float x[16];
     float cmax = -INFINITY;
+    if (live && full) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        // ignored entries get a finite sentinel: their exponentials underflow
-        // to exactly 0 and no -inf * 0 can appear below
-        x[j] = (live && (full || (v0 + j < V))) ? lg[j] : -1.0e30f;
-        cmax = fmaxf(cmax, x[j]);
+        for (int j = 0; j < 16; ++j) {
+            x[j] = lg[j];
+            cmax = fmaxf(cmax, x[j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            // ignored entries get a finite sentinel: their exponentials
+            // underflow to exactly 0 and no -inf * 0 can appear below
+            x[j] = (live && (full || (v0 + j < V))) ? lg[j] : -1.0e30f;
+            cmax = fmaxf(cmax, x[j]);
+        }
     }
     if (!__any_sync(0xFFFFFFFFu, live)) return;
     // argmax: only a chunk whose maximum beats the running best can move it;
@@ -163,14 +171,11 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     // draws the noise of this chunk at all.
     // the exact best is at least max(gbest, apb - slack)
     const float lim = fmaxf(st.gbest, st.apb - 2.0f * kGumbelSlack) - kGumbelMaxPlusSlack;
+    // rounding is monotone, so the chunk's largest scaled logit is cmax * invT
+    if (!__any_sync(0xFFFFFFFFu, cmax * fc.invT > lim)) return;
     float lz[16];
-    bool need = false;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        lz[j] = x[j] * fc.invT;
-        need |= lz[j] > lim;
-    }
-    if (!__any_sync(0xFFFFFFFFu, need)) return;
+    for (int j = 0; j < 16; ++j) lz[j] = x[j] * fc.invT;
     uint32_t w[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -287,6 +292,25 @@ DG_DEVICE void row_state_merge(RowState &a, const RowState &b)
     if (b.amax > a.amax || (b.amax == a.amax && b.aidx < a.aidx)) {
         a.amax = b.amax;
         a.aidx = b.aidx;
+    }
+}
+
+// Fold one accumulator tile into a row's state: the 16-column chunks
+// first, first + stride, ... < BN at TMEM address tb (this warp's lane
+// quadrant, the buffer's first column) of vocabulary entries vbase + c.  All
+// 32 lanes of the warp call it together.  (Loading the next chunk while one
+// is folded needs 16 more live registers than the 96 a thread has here and
+// spills; it measured slower.)
+DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int BN, uint32_t vbase,
+                         uint32_t V, uint32_t row, const FoldConsts &fc, bool live)
+{
+#pragma unroll 1
+    for (int c0 = first; c0 < BN; c0 += stride) {
+        float lg[16];
+        tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
+        const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
+        // one call site of the (large) fold keeps the loop in the instruction cache
+        if (v0 < V) fold16(st, lg, v0, V, row, fc, live);
     }
 }
 
