@@ -277,13 +277,17 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
             const int j = j0 + it;
             const bool pre = j < a.nkt_p;
             const int valid = pre ? min(BKV, a.P - j * BKV) : min(BKV, a.L - (j - a.nkt_p) * BKV);
-            float tmax = -INFINITY;
+            if (valid < BKV) {   // ragged tile: keys past the end weigh nothing
 #pragma unroll
-            for (int c = 0; c < BKV; ++c) {
-                const float v = (c < valid) ? __uint_as_float(sr[c]) * a.scale_log2 : -INFINITY;
-                sr[c] = __float_as_uint(v);
-                tmax = fmaxf(tmax, v);
+                for (int c = 0; c < BKV; ++c)
+                    if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
             }
+            // the scale is positive, so the scaled maximum is the maximum scaled
+            float rmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BKV; c += 2)
+                rmax = max3(rmax, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            const float tmax = rmax * a.scale_log2;
             float factor = 1.f;
             bool rescale = false;
             if (m_ref == -INFINITY) {
@@ -294,19 +298,22 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
                 m_ref = tmax;
                 rescale = true;
             }
-            float psum = 0.f;
+            // p = 2^(s scale - m), two columns per paired instruction; the row
+            // sum is kept in fp32 (the MMA sees p rounded to bf16)
+            const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 acc = make_float2(0.f, 0.f);
             uint32_t pk[BKV / 2];
 #pragma unroll
             for (int c = 0; c < BKV; c += 2) {
-                const float p0 = fast_exp2(__uint_as_float(sr[c]) - m_ref);
-                const float p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_ref);
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                // the row sum uses the bf16-rounded weights the MMA sees
-                const float2 back = __bfloat1622float2(h2);
-                psum += back.x + back.y;
+                const float2 d2 = fma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])),
+                                       sc2, nm2);
+                const float2 p2 = make_float2(fast_exp2(d2.x), fast_exp2(d2.y));
+                acc = add2(acc, p2);
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p2.x, p2.y);
                 pk[c >> 1] = *reinterpret_cast<const uint32_t *>(&h2);
             }
-            l += psum;
+            l += acc.x + acc.y;
             if (__any_sync(0xFFFFFFFFu, rescale)) {
                 // O holds the PVs up to tile it - 1: wait for the last one (the
                 // completed S(it) already implies every earlier PV is done)

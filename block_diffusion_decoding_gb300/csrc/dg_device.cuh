@@ -342,6 +342,36 @@ DG_DEVICE void umma_commit_pair(uint64_t *bar, uint16_t cta_mask)
 }
 
 // ------------------------------------------------------------------------
+// Paired fp32 arithmetic (two lanes of a 64-bit register pair per
+// instruction) and a three-input maximum.
+// ------------------------------------------------------------------------
+DG_DEVICE float2 fma2(float2 a, float2 b, float2 c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)),
+          "l"(*reinterpret_cast<const uint64_t *>(&c)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
+DG_DEVICE float2 add2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
+DG_DEVICE float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// ------------------------------------------------------------------------
 // Thread-block clusters
 // ------------------------------------------------------------------------
 // Address of the same shared-memory location in CTA `rank` of the cluster.
