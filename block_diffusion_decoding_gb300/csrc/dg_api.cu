@@ -83,6 +83,12 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d256,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          attn_smem_bytes(256)));
+        DG_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel_d128,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         attn_pair_smem_bytes(128)));
+        DG_CUDA_TRY(cudaFuncSetAttribute(attn_pair_kernel_d256,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         attn_pair_smem_bytes(256)));
         di.attrs_set = true;
     }
     *out = &di;
@@ -306,6 +312,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
 
 // ---------------------------------------------------------------- attention plan
 struct AttnPlan {
+    bool pair;   // 2-CTA clusters issuing 2-SM UMMAs (attn_pair_kernel_*)
     int BKV, nkt_p, nkt_c, nkt, mtiles, blocks, nsplit, tps;
 };
 
@@ -321,12 +328,19 @@ int attn_split_cap(int blocks, int nkt)
 AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
 {
     AttnPlan a{};
-    a.BKV = (D == 128) ? 128 : 64;
+    // head dim 256: the 2-SM pair kernel (its 128-key S UMMAs replace 64-key
+    // ones; measured 35.5 vs 39.6 us at 16/8 heads, 4096 cached keys); head
+    // dim 128: one CTA per query tile (the pair measured 2 us slower there).
+    // DG_ATTN_KERNEL=single|pair forces a choice.
+    const char *envk = std::getenv("DG_ATTN_KERNEL");
+    a.pair = envk ? std::strcmp(envk, "pair") == 0 : D == 256;
+    a.BKV = (a.pair || D == 128) ? 128 : 64;
     a.nkt_p = (P + a.BKV - 1) / a.BKV;
     a.nkt_c = (L + a.BKV - 1) / a.BKV;
     a.nkt = a.nkt_p + a.nkt_c;
     const int G = Hq / Hkv;
     a.mtiles = (L * G + 127) / 128;
+    if (a.pair) a.mtiles += a.mtiles & 1;   // query tiles in pairs
     a.blocks = a.mtiles * Hkv * B;
     // splits: minimise the estimated time in key-tile units -- waves x (tiles
     // per split + a fixed cost of about 3 tiles per CTA) + about 4 tiles for
@@ -468,22 +482,37 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms);
     cudaStream_t st = as_stream(stream);
 
-    CUtensorMap mkp, mvp, mkc, mvc;
-    auto kv_map = [&](CUtensorMap *m, const uint16_t *base, int rows) -> int {
-        // [B, rows, Hkv, D] as {D, Hkv, rows, B}
+    CUtensorMap mq, mkp, mvp, mkc, mvc;
+    {
+        // Q [B, L, Hq, D] as {D, G, Hkv, L, B}: a box is 64 dims x the G heads
+        // of one kv head x 128 / G positions (one folded 128-row tile)
+        const uint64_t dims[5] = {static_cast<uint64_t>(D), static_cast<uint64_t>(G),
+                                  static_cast<uint64_t>(Hkv), static_cast<uint64_t>(L),
+                                  static_cast<uint64_t>(B)};
+        const uint64_t strides[4] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(G) * D * 2,
+                                     static_cast<uint64_t>(Hq) * D * 2,
+                                     static_cast<uint64_t>(L) * Hq * D * 2};
+        const uint32_t box[5] = {64, static_cast<uint32_t>(G), 1, static_cast<uint32_t>(128 / G), 1};
+        if ((rc = make_map_bf16(&mq, q, 5, dims, strides, box)) != DG_OK) return rc;
+    }
+    // K / V [B, rows, Hkv, D] as {D, Hkv, rows, B}; the pair kernel stages
+    // half a key tile of K and a full key tile of half the dims of V per CTA
+    const uint32_t k_rows = static_cast<uint32_t>(ap.pair ? ap.BKV / 2 : ap.BKV);
+    const uint32_t v_rows = static_cast<uint32_t>(ap.BKV);
+    auto kv_map = [&](CUtensorMap *m, const uint16_t *base, int rows, uint32_t box_rows) -> int {
         const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
                                   static_cast<uint64_t>(rows), static_cast<uint64_t>(B)};
         const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2,
                                      static_cast<uint64_t>(Hkv) * D * 2,
                                      static_cast<uint64_t>(rows) * Hkv * D * 2};
-        const uint32_t box[4] = {64, 1, static_cast<uint32_t>(ap.BKV), 1};
+        const uint32_t box[4] = {64, 1, box_rows, 1};
         return make_map_bf16(m, base, 4, dims, strides, box);
     };
-    if ((rc = kv_map(&mkc, k_canvas, L)) != DG_OK) return rc;
-    if ((rc = kv_map(&mvc, v_canvas, L)) != DG_OK) return rc;
+    if ((rc = kv_map(&mkc, k_canvas, L, k_rows)) != DG_OK) return rc;
+    if ((rc = kv_map(&mvc, v_canvas, L, v_rows)) != DG_OK) return rc;
     if (P > 0) {
-        if ((rc = kv_map(&mkp, k_prefix, P)) != DG_OK) return rc;
-        if ((rc = kv_map(&mvp, v_prefix, P)) != DG_OK) return rc;
+        if ((rc = kv_map(&mkp, k_prefix, P, k_rows)) != DG_OK) return rc;
+        if ((rc = kv_map(&mvp, v_prefix, P, v_rows)) != DG_OK) return rc;
     } else {
         mkp = mkc;
         mvp = mvc;
@@ -514,9 +543,15 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
             p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 4, 256));
     }
     const bool pdl = use_pdl(st);
-    DG_CUDA_TRY(launch_kernel(D == 128 ? attn_kernel_d128 : attn_kernel_d256,
-                              dim3(ap.mtiles, Hkv * B, ap.nsplit), dim3(kAttnThreads),
-                              attn_smem_bytes(D), st, pdl, mkp, mvp, mkc, mvc, a));
+    const dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);
+    if (ap.pair)
+        DG_CUDA_TRY(launch_kernel(D == 128 ? attn_pair_kernel_d128 : attn_pair_kernel_d256, grid,
+                                  dim3(kAttnThreads), attn_pair_smem_bytes(D), st, pdl, mq, mkp,
+                                  mvp, mkc, mvc, a));
+    else
+        DG_CUDA_TRY(launch_kernel(D == 128 ? attn_kernel_d128 : attn_kernel_d256, grid,
+                                  dim3(kAttnThreads), attn_smem_bytes(D), st, pdl, mkp, mvp, mkc,
+                                  mvc, a));
     DG_LAUNCHED();
     if (ap.nsplit > 1) {
         const size_t nr = static_cast<size_t>(B) * L * Hq;

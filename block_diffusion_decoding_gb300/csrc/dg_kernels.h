@@ -140,6 +140,19 @@ __global__ void attn_kernel_d256(const __grid_constant__ CUtensorMap map_kp,
                                  const __grid_constant__ CUtensorMap map_kc,
                                  const __grid_constant__ CUtensorMap map_vc, AttnArgs a);
 __global__ void attn_combine_kernel(AttnArgs a);
+// 2-CTA clusters issuing 2-SM UMMAs: two consecutive query tiles share every
+// 128-key tile (dg_attn_pair.cu)
+__global__ void attn_pair_kernel_d128(const __grid_constant__ CUtensorMap map_q,
+                                      const __grid_constant__ CUtensorMap map_kp,
+                                      const __grid_constant__ CUtensorMap map_vp,
+                                      const __grid_constant__ CUtensorMap map_kc,
+                                      const __grid_constant__ CUtensorMap map_vc, AttnArgs a);
+__global__ void attn_pair_kernel_d256(const __grid_constant__ CUtensorMap map_q,
+                                      const __grid_constant__ CUtensorMap map_kp,
+                                      const __grid_constant__ CUtensorMap map_vp,
+                                      const __grid_constant__ CUtensorMap map_kc,
+                                      const __grid_constant__ CUtensorMap map_vc, AttnArgs a);
+int attn_pair_smem_bytes(int D);
 
 int attn_smem_bytes(int D);
 

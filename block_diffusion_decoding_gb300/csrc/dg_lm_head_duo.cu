@@ -207,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             __syncwarp();
             // the even CTA's MMA may overwrite this accumulator once both
             // CTAs' epilogues have read it
-            if (lane == 0) mbar_arrive_cluster(lead_acc_empty + static_cast<uint32_t>(acc * 8));
+            if (lane == 0) mbar_arrive_cluster_relaxed(lead_acc_empty + static_cast<uint32_t>(acc * 8));
         }
         if (cur_m >= 0) {
             const int prow = cur_m * kRowsPerBlock + r * 128 + rix;

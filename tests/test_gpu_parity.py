@@ -242,6 +242,20 @@ def test_canvas_attn_matches_oracle(B, L, P, Hq, Hkv, D, stride):
     _attn_case(B, L, P, Hq, Hkv, D, seed=B + L + P, row_stride=stride)
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("B,L,P,Hq,Hkv,D,stride", [
+    (1, 256, 256, 4, 1, 128, 1),      # head dim 128
+    (2, 100, 37, 4, 2, 128, 1),       # ragged canvas and prefix, odd query-tile count
+    (1, 48, 300, 16, 8, 256, 1),      # head dim 256, one query tile per kv head
+    (2, 256, 1000, 16, 8, 256, 9),    # head dim 256 with splits
+])
+def test_canvas_attn_both_kernels(kernel, B, L, P, Hq, Hkv, D, stride, monkeypatch):
+    """One CTA per query tile and 2-CTA clusters with 2-SM UMMAs, whichever the
+    planner picks by default for the head dim."""
+    monkeypatch.setenv("DG_ATTN_KERNEL", kernel)
+    _attn_case(B, L, P, Hq, Hkv, D, seed=7 + B + L, row_stride=stride)
+
+
 def test_canvas_attn_constant_values_and_zero_keys():
     """Constant value rows -> every output equals that row; zero keys -> mean of values."""
     B, L, P, Hq, Hkv, D = 1, 128, 200, 4, 1, 128
