@@ -639,6 +639,53 @@ def oracle_block_step_estimate(cfg, host, v_sample=16384):
     return t_lm * cfg.V / vs + t_acc, desc
 
 
+def run_kernel_only(args, cfg):
+    """One kernel of the step alone on the workload's shapes (for profilers:
+    only that kernel's inputs are allocated).  Prints per-launch CUDA-event
+    times; not the benchmark line."""
+    import torch
+    import block_diffusion_decoding_gb300 as dg
+    from block_diffusion_decoding_gb300 import build as dgbuild
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dgbuild.build()
+    g = torch.Generator(device=dev).manual_seed(1000)
+    bf = torch.bfloat16
+    B, L, Hq, Hkv, D, P, d, V = cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V
+    M = B * L
+    if args.kernel == "attention":
+        q = torch.randn(B, L, Hq, D, device=dev, generator=g).to(bf)
+        kp = torch.randn(B, P, Hkv, D, device=dev, generator=g).to(bf)
+        vp = torch.randn(B, P, Hkv, D, device=dev, generator=g).to(bf)
+        kc = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+        vc = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+        out = torch.empty_like(q)
+        ws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), dev)
+        fn = lambda: dg.canvas_attn(q, kp, vp, kc, vc, out, 1.0 / math.sqrt(D), ws)
+    else:
+        x = torch.randn(M, d, device=dev, generator=g).to(bf)
+        w = torch.empty(d, V, device=dev, dtype=bf)
+        for r0 in range(0, d, 256):
+            r1 = min(d, r0 + 256)
+            w[r0:r1] = (torch.randn(r1 - r0, V, device=dev, generator=g) * cfg.w_std).to(bf)
+        p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 1)
+        ws = dg.workspace(dg.denoise_step_workspace(p), dev)
+        fn = lambda: dg.lm_head_fold(x, w, p, ws)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        fn()
+        e_.record()
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            ts.append(s_.elapsed_time(e_))
+    print(json.dumps({"kernel_only": args.kernel, "config": cfg.name,
+                      "us_mean": 1e3 * sum(ts) / len(ts), "launches": args.steps,
+                      "device_status": dg.read_device_status(ws)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,11 +694,15 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(dg_synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["attention", "lm_head"],
+                    help="run one kernel of the step alone (for profilers), not the benchmark")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     cfg = dg_synth.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.kernel:
+        return run_kernel_only(args, cfg)
     if cfg.name == "block_full":
         return run_block(args, cfg)
     return run_ours(args, cfg)
