@@ -184,6 +184,34 @@ def test_denoise_step_matches_oracle(B, L, d, V, w_std, k):
     assert np.array_equal(np_f(bufs.entropy), H1)
 
 
+@pytest.mark.parametrize("kernel", [None, "single", "pair", "duo"])
+@pytest.mark.parametrize("B,L,d,V", [(1, 1024, 64, 64),      # largest canvas, one k block, tiny V
+                                     (2, 1, 128, 2048),      # one position per canvas
+                                     (5, 200, 192, 1104)])   # canvases straddling row blocks
+def test_denoise_step_edge_shapes(kernel, B, L, d, V, monkeypatch):
+    """Edge shapes through every LM-head kernel (None = the planner's choice)."""
+    if kernel is None:
+        monkeypatch.delenv("DG_LM_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("DG_LM_KERNEL", kernel)
+    cfg = dg_synth.StepConfig("e", B=B, L=L, d=d, V=V, w_std=0.1, seed=23)
+    xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
+    T, b, seed, k = oracle.temperature(7, 48), 0.1, 17, 7
+    rng = np.random.default_rng(B + L)
+    canvas0 = rng.integers(0, V, B * L).astype(np.int32)
+    prev = rng.integers(0, V, B * L).astype(np.int32)
+    p = dg.step_params(B, L, d, V, T, b, 0.005, step=k, seed=seed)
+    bufs = dg.StepBuffers(B, L, DEV)
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    bufs.prev_argmax.copy_(torch.from_numpy(prev))
+    ws = dg.workspace(dg.denoise_step_workspace(p), DEV)
+    dg.denoise_step(to_dev(xb), to_dev(wb), p, bufs, ws)
+    torch.cuda.synchronize()
+    status_ok(ws)
+    ref = oracle.step(xb, wb, canvas0, prev, B, L, T, b, seed, k)
+    check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+
+
 def test_denoise_step_uniform_and_one_hot_rows():
     """Zero hidden rows give uniform logits (H = ln V, argmax 0); a row aligned
     with one vocabulary column at large scale gives H ~ 0 at that column."""
@@ -254,6 +282,15 @@ def test_canvas_attn_both_kernels(kernel, B, L, P, Hq, Hkv, D, stride, monkeypat
     planner picks by default for the head dim."""
     monkeypatch.setenv("DG_ATTN_KERNEL", kernel)
     _attn_case(B, L, P, Hq, Hkv, D, seed=7 + B + L, row_stride=stride)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("B,L,P,Hq,Hkv,D", [(1, 1, 5, 16, 1, 128),    # one position, G = 16
+                                          (1, 1, 0, 2, 2, 256),      # no prefix, G = 1
+                                          (3, 7, 129, 8, 4, 256)])   # ragged everything
+def test_canvas_attn_edge_shapes(kernel, B, L, P, Hq, Hkv, D, monkeypatch):
+    monkeypatch.setenv("DG_ATTN_KERNEL", kernel)
+    _attn_case(B, L, P, Hq, Hkv, D, seed=3 + P, row_stride=1)
 
 
 def test_canvas_attn_constant_values_and_zero_keys():
