@@ -375,7 +375,7 @@ size_t attn_ws_bytes(int B, int L, int Hq, int D, int nsplit)
     size_t b = sizeof(WsHeader);
     if (nsplit > 1) {
         const size_t nr = static_cast<size_t>(B) * L * Hq;
-        b += round_up(static_cast<size_t>(nsplit) * nr * D * 4, 256);
+        b += round_up(static_cast<size_t>(nsplit) * nr * D * 2, 256);
         b += round_up(static_cast<size_t>(nsplit) * nr * 8, 256);
     }
     return b;
@@ -538,9 +538,9 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     if (ap.nsplit > 1) {
         uint8_t *p = static_cast<uint8_t *>(workspace) + sizeof(WsHeader);
         const size_t nr = static_cast<size_t>(B) * L * Hq;
-        a.part_o = reinterpret_cast<float *>(p);
+        a.part_o = reinterpret_cast<uint16_t *>(p);
         a.part_ml = reinterpret_cast<float *>(
-            p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 4, 256));
+            p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 2, 256));
     }
     const bool pdl = use_pdl(st);
     const dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);

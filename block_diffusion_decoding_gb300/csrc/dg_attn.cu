@@ -354,28 +354,23 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
                 tmem_ld32_nowait(tmem + lane_off + Gm::ColO + c0, o);
                 tmem_wait_ld();
                 if (!live) continue;
-                if (a.nsplit == 1) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.out + flat * D + c0);
+                // the output row, or (several key splits) this split's
+                // normalised partial row, as bf16
+                uint16_t *row_out = (a.nsplit == 1)
+                                        ? a.out + flat * D
+                                        : a.part_o + (static_cast<size_t>(split) * nrows + flat) * D;
+                uint4 *dst = reinterpret_cast<uint4 *>(row_out + c0);
 #pragma unroll
-                    for (int k = 0; k < 32; k += 8) {
-                        uint32_t w4[4];
+                for (int k = 0; k < 32; k += 8) {
+                    uint32_t w4[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                                __uint_as_float(o[k + 2 * e]) * inv_l,
-                                __uint_as_float(o[k + 2 * e + 1]) * inv_l);
-                            w4[e] = *reinterpret_cast<const uint32_t *>(&h2);
-                        }
-                        dst[k >> 3] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                            __uint_as_float(o[k + 2 * e]) * inv_l,
+                            __uint_as_float(o[k + 2 * e + 1]) * inv_l);
+                        w4[e] = *reinterpret_cast<const uint32_t *>(&h2);
                     }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        a.part_o + (static_cast<size_t>(split) * nrows + flat) * D + c0);
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        dst[k >> 2] = make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]),
-                                                  __uint_as_float(o[k + 2]),
-                                                  __uint_as_float(o[k + 3]));
+                    dst[k >> 3] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
             if (live && a.nsplit > 1) {
@@ -411,6 +406,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // Merge the key splits: one warp per query row, lanes over the head dim.
+// Split z left its row normalised by its own sum l_z, with its reference max
+// m_z (base 2); the row is sum_z 2^(m_z - M) l_z O_z / sum_z 2^(m_z - M) l_z.
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
 {
     griddep_wait();
@@ -429,12 +426,25 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
     const int per = a.D / 32;   // 4 or 8 consecutive dims per lane
     for (int z = 0; z < a.nsplit; ++z) {
         const float2 v = ml[z * nrows + row];
-        const float w = fast_exp2(v.x - mx);
-        den = fmaf(w, v.y, den);
-        const float *po = a.part_o + (z * nrows + row) * a.D + lane * per;
+        const float wz = fast_exp2(v.x - mx) * v.y;
+        den += wz;
+        const uint16_t *po = a.part_o + (z * nrows + row) * a.D + lane * per;
+        uint32_t pw[4];
+        if (per == 8) {
+            const uint4 q4 = *reinterpret_cast<const uint4 *>(po);
+            pw[0] = q4.x; pw[1] = q4.y; pw[2] = q4.z; pw[3] = q4.w;
+        } else {
+            const uint2 q2 = *reinterpret_cast<const uint2 *>(po);
+            pw[0] = q2.x; pw[1] = q2.y; pw[2] = 0u; pw[3] = 0u;
+        }
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (e < per) acc[e] = fmaf(w, po[e], acc[e]);
+        for (int e = 0; e < 4; ++e) {
+            if (2 * e < per) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[e]));
+                acc[2 * e] = fmaf(wz, f.x, acc[2 * e]);
+                acc[2 * e + 1] = fmaf(wz, f.y, acc[2 * e + 1]);
+            }
+        }
     }
     const float inv = 1.f / den;
     uint16_t *dst = a.out + row * a.D + lane * per;

@@ -398,28 +398,23 @@ __device__ __forceinline__ void attn_pair_body(const CUtensorMap *map_q, const C
                 tmem_ld32_nowait(tmem + lane_off + Gm::ColO + c0, o);
                 tmem_wait_ld();
                 if (!live) continue;
-                if (a.nsplit == 1) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.out + flat * D + c0);
+                // the output row, or (several key splits) this split's
+                // normalised partial row, as bf16
+                uint16_t *row_out = (a.nsplit == 1)
+                                        ? a.out + flat * D
+                                        : a.part_o + (static_cast<size_t>(split) * nrows + flat) * D;
+                uint4 *dst = reinterpret_cast<uint4 *>(row_out + c0);
 #pragma unroll
-                    for (int k = 0; k < 32; k += 8) {
-                        uint32_t w4[4];
+                for (int k = 0; k < 32; k += 8) {
+                    uint32_t w4[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                                __uint_as_float(o[k + 2 * e]) * inv_l,
-                                __uint_as_float(o[k + 2 * e + 1]) * inv_l);
-                            w4[e] = *reinterpret_cast<const uint32_t *>(&h2);
-                        }
-                        dst[k >> 3] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                            __uint_as_float(o[k + 2 * e]) * inv_l,
+                            __uint_as_float(o[k + 2 * e + 1]) * inv_l);
+                        w4[e] = *reinterpret_cast<const uint32_t *>(&h2);
                     }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        a.part_o + (static_cast<size_t>(split) * nrows + flat) * D + c0);
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        dst[k >> 2] = make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]),
-                                                  __uint_as_float(o[k + 2]),
-                                                  __uint_as_float(o[k + 3]));
+                    dst[k >> 3] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
             if (live && a.nsplit > 1) {

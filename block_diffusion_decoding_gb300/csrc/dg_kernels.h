@@ -124,7 +124,7 @@ struct AttnArgs {
     float scale_log2;   // scale * log2(e)
     const uint16_t *q;  // [B, L, Hq, D]
     uint16_t *out;      // [B, L, Hq, D] (nsplit == 1)
-    float *part_o;      // [nsplit][B*L*Hq][D] unnormalised (nsplit > 1)
+    uint16_t *part_o;   // [nsplit][B*L*Hq][D] bf16, each split's rows normalised by its sum (nsplit > 1)
     float *part_ml;     // [nsplit][B*L*Hq][2] (row max in base 2, row sum)
     WsHeader *ws;
 };
