@@ -88,6 +88,10 @@ def lib():
                                          _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                          _c_dbl, _vp, _c_i64, _vp]
         L.orc_attention_rows.restype = None
+        L.orc_attention_rows_ex.argtypes = [_vp, _vp, _vp, _vp, _vp,
+                                            _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                            _c_dbl, _c_i32, _vp, _c_i64, _vp]
+        L.orc_attention_rows_ex.restype = None
         L.orc_gumbel_fill.argtypes = [_c_u64, _c_u32, _c_u32, _c_u32, _c_i32, _vp]
         L.orc_gumbel_fill.restype = None
         _lib = L
@@ -235,13 +239,18 @@ def stop(argmax: np.ndarray, prev_argmax: np.ndarray, H: np.ndarray, step: int,
 
 
 # ---------------------------------------------------------------- attention
-def attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, rows) -> np.ndarray:
-    """fp64 attention for the listed flat query rows (b*L+i)*Hq+h; bf16 inputs as uint16."""
+def attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, rows,
+                   causal: bool = False) -> np.ndarray:
+    """fp64 attention for the listed flat query rows (b*L+i)*Hq+h; bf16 inputs as uint16.
+
+    causal: the encoder's cache-append forward -- the query at canvas
+    position i sees the P cached keys and the canvas keys 0 .. i.
+    """
     arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.uint16)) for a in (q, kp, vp, kc, vc)]
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     out = np.zeros((r.shape[0], D), dtype=np.float64)
-    lib().orc_attention_rows(*[_ptr(a) for a in arrs], B, L, P, Hq, Hkv, D, float(scale),
-                             _ptr(r), r.shape[0], _ptr(out))
+    lib().orc_attention_rows_ex(*[_ptr(a) for a in arrs], B, L, P, Hq, Hkv, D, float(scale),
+                                1 if causal else 0, _ptr(r), r.shape[0], _ptr(out))
     return out
 
 

@@ -317,21 +317,28 @@ static double orc_bf16(uint16_t h)
     return (double)orc_bits_to_float(b);
 }
 
-void orc_attention_rows(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
-                        const uint16_t *kc, const uint16_t *vc,
-                        int32_t B, int32_t L, int32_t P, int32_t Hq, int32_t Hkv, int32_t D,
-                        double scale, const int64_t *rows, int64_t nrows, double *out)
+/* With causal != 0 (the encoder's cache-append forward, "Parallel Denoising
+   From an Autoregressive Checkpoint", section "Finding": the causal encoder
+   extends the append-only cache with the committed block), the query at
+   canvas position i sees the P cached keys and the canvas keys 0 .. i only. */
+void orc_attention_rows_ex(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
+                           const uint16_t *kc, const uint16_t *vc,
+                           int32_t B, int32_t L, int32_t P, int32_t Hq, int32_t Hkv, int32_t D,
+                           double scale, int32_t causal, const int64_t *rows, int64_t nrows,
+                           double *out)
 {
     int32_t group = Hq / Hkv;
-    int64_t nk = (int64_t)P + L;
-    double *s = (double *)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    int64_t nk_all = (int64_t)P + L;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(nk_all > 0 ? nk_all : 1));
     (void)B;
     for (int64_t t = 0; t < nrows; ++t) {
         int64_t flat = rows[t];
         int64_t h = flat % Hq;
         int64_t bi = flat / Hq;            /* b*L + i */
         int64_t b = bi / L;
+        int64_t i = bi % L;
         int64_t g = h / group;
+        int64_t nk = causal ? (int64_t)P + i + 1 : nk_all;
         const uint16_t *qr = q + flat * D;
         double smax = -INFINITY;
         for (int64_t j = 0; j < nk; ++j) {
@@ -354,6 +361,14 @@ void orc_attention_rows(const uint16_t *q, const uint16_t *kp, const uint16_t *v
         }
     }
     free(s);
+}
+
+void orc_attention_rows(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
+                        const uint16_t *kc, const uint16_t *vc,
+                        int32_t B, int32_t L, int32_t P, int32_t Hq, int32_t Hkv, int32_t D,
+                        double scale, const int64_t *rows, int64_t nrows, double *out)
+{
+    orc_attention_rows_ex(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, 0, rows, nrows, out);
 }
 
 /* Gumbel variates of vocabulary entries v0 .. v0+n-1 of one (row, step). */

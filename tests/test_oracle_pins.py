@@ -332,6 +332,35 @@ def test_attention_special_cases():
     assert np.abs(out - oracle.bf16_bits_to_f64(vc)[0, 0, 0][None]).max() == 0.0
 
 
+def test_causal_attention_matches_torch_sdpa_with_mask():
+    """Cache-append forward: canvas position i sees all P cached keys and the
+    canvas keys 0 .. i (an explicit boolean mask in torch's SDPA, float64)."""
+    B, L, P, Hq, Hkv, D = 2, 11, 6, 4, 2, 16
+    q, kp, vp, kc, vc = _attn_inputs(B, L, P, Hq, Hkv, D, seed=5)
+    scale = 1.0 / math.sqrt(D)
+    rows = np.arange(B * L * Hq)
+    got = oracle.attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, rows, causal=True)
+    f = lambda a: torch.from_numpy(oracle.bf16_bits_to_f64(a))
+    Q = f(q).permute(0, 2, 1, 3)
+    K = torch.cat([f(kp), f(kc)], 1).permute(0, 2, 1, 3).repeat_interleave(Hq // Hkv, dim=1)
+    Vv = torch.cat([f(vp), f(vc)], 1).permute(0, 2, 1, 3).repeat_interleave(Hq // Hkv, dim=1)
+    keyj = torch.arange(P + L)[None, :]
+    posi = torch.arange(L)[:, None]
+    mask = (keyj < P) | (keyj - P <= posi)                       # [L, P + L]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, Vv, attn_mask=mask, scale=scale)
+    ref = ref.permute(0, 2, 1, 3).reshape(-1, D).numpy()
+    assert np.abs(got - ref).max() < 1e-12
+    # without a cache the first canvas position sees only itself
+    got0 = oracle.attention_rows(q, kp[:, :0], vp[:, :0], kc, vc, B, L, 0, Hq, Hkv, D, scale,
+                                 np.arange(Hq), causal=True)
+    assert np.abs(got0 - oracle.bf16_bits_to_f64(vc)[0, 0].repeat(Hq // Hkv, 0)).max() == 0.0
+    # the last position sees every key: the same as the unmasked attention
+    last = np.array([((b * L) + L - 1) * Hq + h for b in range(B) for h in range(Hq)])
+    a = oracle.attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, last, causal=True)
+    u = oracle.attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, last)
+    assert np.array_equal(a, u)
+
+
 # ------------------------------------------------------------------ LM-head GEMM
 def test_logits_exact_on_small_integers():
     rng = np.random.default_rng(6)
