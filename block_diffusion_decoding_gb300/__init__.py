@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
 # Functions include/dg.h declares (checked by the CPU test-suite).
 EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_canvas_attn_workspace", "dg_canvas_attn",
+            "dg_encoder_append_workspace", "dg_encoder_append",
             "dg_denoise_step_workspace", "dg_denoise_step", "dg_denoise_step_noalloc",
             "dg_generate_block_workspace", "dg_generate_block",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
@@ -85,6 +86,9 @@ def _lib():
             "dg_read_device_status": ([vp, ctypes.POINTER(ctypes.c_int), i32, vp], i32),
             "dg_canvas_attn_workspace": ([i32] * 6, sz),
             "dg_canvas_attn": ([vp] * 6 + [i32] * 6 + [f32, vp, sz, vp], i32),
+            "dg_encoder_append_workspace": ([i32] * 6, sz),
+            "dg_encoder_append": ([vp, vp, vp, i32, i32, vp, vp, vp] + [i32] * 5
+                                  + [f32, vp, sz, vp], i32),
             "dg_denoise_step_workspace": ([sp], sz),
             "dg_denoise_step": ([vp, vp, sp, si, vp, sz, vp], i32),
             "dg_denoise_step_noalloc": ([vp, vp, sp, si, vp], i32),
@@ -143,6 +147,21 @@ def canvas_attn(q, k_prefix, v_prefix, k_canvas, v_canvas, out, scale, workspace
                                _p(k_canvas), _p(v_canvas), _p(out), B, L, P, Hq, Hkv, D,
                                float(scale), _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "dg_canvas_attn")
+
+
+def encoder_append_workspace(B, L, P, Hq, Hkv, D) -> int:
+    return int(_lib().dg_encoder_append_workspace(B, L, P, Hq, Hkv, D))
+
+
+def encoder_append(q, k_cache, v_cache, P, k_new, v_new, out, scale, workspace, stream=None):
+    """dg_encoder_append: the caches [B, P_max, Hkv, D] hold P tokens; the block's
+    k_new/v_new [B, L, Hkv, D] are appended and q [B, L, Hq, D] attends causally."""
+    B, L, Hq, D = q.shape
+    P_max, Hkv = k_cache.shape[1], k_cache.shape[2]
+    rc = _lib().dg_encoder_append(_p(q), _p(k_cache), _p(v_cache), int(P), int(P_max),
+                                  _p(k_new), _p(v_new), _p(out), B, L, Hq, Hkv, D, float(scale),
+                                  _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_encoder_append")
 
 
 # ---------------------------------------------------------------- step

@@ -408,6 +408,116 @@ size_t block_ws_layout(const dg_step_params *p, int slots, size_t *off_ctl, size
 }  // namespace
 
 // ====================================================================== C ABI
+// Canvas attention over [prefix rows 0 .. P-1 ; canvas rows]; the prefix
+// tensors hold prefix_alloc >= P rows per batch entry (a cache with room to
+// grow); causal masks canvas keys after each query's position.
+static int attn_run(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+             const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *out, int B, int L, int P,
+             int prefix_alloc, int Hq, int Hkv, int D, float scale, int causal, void *workspace,
+             size_t workspace_bytes, void *stream)
+{
+    if (!q || !k_canvas || !v_canvas || !out) return DG_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || P < 0 || Hq < 1 || Hkv < 1) return DG_ERR_INVALID_ARG;
+    if (P > 0 && (!k_prefix || !v_prefix)) return DG_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return DG_ERR_INVALID_ARG;
+    if (D != 128 && D != 256) return DG_ERR_UNSUPPORTED;
+    if (Hq % Hkv != 0) return DG_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (G > 16 || (G & (G - 1)) != 0) return DG_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * L * Hq > (1LL << 30) || P > (1 << 30)) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_canvas) || !aligned16(v_canvas) || !aligned16(out) ||
+        (P > 0 && (!aligned16(k_prefix) || !aligned16(v_prefix))))
+        return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_canvas_attn_workspace(B, L, P, Hq, Hkv, D))
+        return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    int rc = current_device_info(&di);
+    if (rc != DG_OK) return rc;
+    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms);
+    cudaStream_t st = as_stream(stream);
+
+    CUtensorMap mq, mkp, mvp, mkc, mvc;
+    {
+        // Q [B, L, Hq, D] as {D, G, Hkv, L, B}: a box is 64 dims x the G heads
+        // of one kv head x 128 / G positions (one folded 128-row tile)
+        const uint64_t dims[5] = {static_cast<uint64_t>(D), static_cast<uint64_t>(G),
+                                  static_cast<uint64_t>(Hkv), static_cast<uint64_t>(L),
+                                  static_cast<uint64_t>(B)};
+        const uint64_t strides[4] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(G) * D * 2,
+                                     static_cast<uint64_t>(Hq) * D * 2,
+                                     static_cast<uint64_t>(L) * Hq * D * 2};
+        const uint32_t box[5] = {64, static_cast<uint32_t>(G), 1, static_cast<uint32_t>(128 / G), 1};
+        if ((rc = make_map_bf16(&mq, q, 5, dims, strides, box)) != DG_OK) return rc;
+    }
+    // K / V [B, rows, Hkv, D] as {D, Hkv, rows, B}; the pair kernel stages
+    // half a key tile of K and a full key tile of half the dims of V per CTA
+    const uint32_t k_rows = static_cast<uint32_t>(ap.pair ? ap.BKV / 2 : ap.BKV);
+    const uint32_t v_rows = static_cast<uint32_t>(ap.BKV);
+    auto kv_map = [&](CUtensorMap *m, const uint16_t *base, int rows, int rows_alloc,
+                      uint32_t box_rows) -> int {
+        const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
+                                  static_cast<uint64_t>(rows), static_cast<uint64_t>(B)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2,
+                                     static_cast<uint64_t>(Hkv) * D * 2,
+                                     static_cast<uint64_t>(rows_alloc) * Hkv * D * 2};
+        const uint32_t box[4] = {64, 1, box_rows, 1};
+        return make_map_bf16(m, base, 4, dims, strides, box);
+    };
+    if ((rc = kv_map(&mkc, k_canvas, L, L, k_rows)) != DG_OK) return rc;
+    if ((rc = kv_map(&mvc, v_canvas, L, L, v_rows)) != DG_OK) return rc;
+    if (P > 0) {
+        if ((rc = kv_map(&mkp, k_prefix, P, prefix_alloc, k_rows)) != DG_OK) return rc;
+        if ((rc = kv_map(&mvp, v_prefix, P, prefix_alloc, v_rows)) != DG_OK) return rc;
+    } else {
+        mkp = mkc;
+        mvp = mvc;
+    }
+    AttnArgs a{};
+    a.B = B;
+    a.L = L;
+    a.P = P;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.G = G;
+    a.rows = L * G;
+    a.mtiles = ap.mtiles;
+    a.nsplit = ap.nsplit;
+    a.nkt_p = ap.nkt_p;
+    a.nkt_c = ap.nkt_c;
+    a.tiles_per_split = ap.tps;
+    a.scale_log2 = scale * 1.44269502162933349609375f;
+    a.causal = causal;
+    a.q = q;
+    a.out = out;
+    a.ws = static_cast<WsHeader *>(workspace);
+    if (ap.nsplit > 1) {
+        uint8_t *p = static_cast<uint8_t *>(workspace) + sizeof(WsHeader);
+        const size_t nr = static_cast<size_t>(B) * L * Hq;
+        a.part_o = reinterpret_cast<uint16_t *>(p);
+        a.part_ml = reinterpret_cast<float *>(
+            p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 2, 256));
+    }
+    const bool pdl = use_pdl(st);
+    const dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);
+    if (ap.pair)
+        DG_CUDA_TRY(launch_kernel(D == 128 ? attn_pair_kernel_d128 : attn_pair_kernel_d256, grid,
+                                  dim3(kAttnThreads), attn_pair_smem_bytes(D), st, pdl, mq, mkp,
+                                  mvp, mkc, mvc, a));
+    else
+        DG_CUDA_TRY(launch_kernel(D == 128 ? attn_kernel_d128 : attn_kernel_d256, grid,
+                                  dim3(kAttnThreads), attn_smem_bytes(D), st, pdl, mkp, mvp, mkc,
+                                  mvc, a));
+    DG_LAUNCHED();
+    if (ap.nsplit > 1) {
+        const size_t nr = static_cast<size_t>(B) * L * Hq;
+        DG_CUDA_TRY(launch_kernel(attn_combine_kernel, dim3(static_cast<unsigned>((nr + 7) / 8)),
+                                  dim3(256), 0, st, pdl, a));
+        DG_LAUNCHED();
+    }
+    return DG_OK;
+}
+
 extern "C" {
 
 const char *dg_status_string(int status)
@@ -462,104 +572,42 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
                    int P, int Hq, int Hkv, int D, float scale, void *workspace,
                    size_t workspace_bytes, void *stream)
 {
-    if (!q || !k_canvas || !v_canvas || !out) return DG_ERR_INVALID_ARG;
-    if (B < 1 || L < 1 || P < 0 || Hq < 1 || Hkv < 1) return DG_ERR_INVALID_ARG;
-    if (P > 0 && (!k_prefix || !v_prefix)) return DG_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return DG_ERR_INVALID_ARG;
-    if (D != 128 && D != 256) return DG_ERR_UNSUPPORTED;
-    if (Hq % Hkv != 0) return DG_ERR_UNSUPPORTED;
-    const int G = Hq / Hkv;
-    if (G > 16 || (G & (G - 1)) != 0) return DG_ERR_UNSUPPORTED;
-    if (static_cast<long long>(B) * L * Hq > (1LL << 30) || P > (1 << 30)) return DG_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_canvas) || !aligned16(v_canvas) || !aligned16(out) ||
-        (P > 0 && (!aligned16(k_prefix) || !aligned16(v_prefix))))
-        return DG_ERR_ALIGNMENT;
-    if (workspace == nullptr || workspace_bytes < dg_canvas_attn_workspace(B, L, P, Hq, Hkv, D))
-        return DG_ERR_WORKSPACE;
-    DeviceInfo *di = nullptr;
-    int rc = current_device_info(&di);
-    if (rc != DG_OK) return rc;
-    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms);
-    cudaStream_t st = as_stream(stream);
+    return attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, out, B, L, P, P, Hq, Hkv, D, scale,
+                    0, workspace, workspace_bytes, stream);
+}
 
-    CUtensorMap mq, mkp, mvp, mkc, mvc;
-    {
-        // Q [B, L, Hq, D] as {D, G, Hkv, L, B}: a box is 64 dims x the G heads
-        // of one kv head x 128 / G positions (one folded 128-row tile)
-        const uint64_t dims[5] = {static_cast<uint64_t>(D), static_cast<uint64_t>(G),
-                                  static_cast<uint64_t>(Hkv), static_cast<uint64_t>(L),
-                                  static_cast<uint64_t>(B)};
-        const uint64_t strides[4] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(G) * D * 2,
-                                     static_cast<uint64_t>(Hq) * D * 2,
-                                     static_cast<uint64_t>(L) * Hq * D * 2};
-        const uint32_t box[5] = {64, static_cast<uint32_t>(G), 1, static_cast<uint32_t>(128 / G), 1};
-        if ((rc = make_map_bf16(&mq, q, 5, dims, strides, box)) != DG_OK) return rc;
-    }
-    // K / V [B, rows, Hkv, D] as {D, Hkv, rows, B}; the pair kernel stages
-    // half a key tile of K and a full key tile of half the dims of V per CTA
-    const uint32_t k_rows = static_cast<uint32_t>(ap.pair ? ap.BKV / 2 : ap.BKV);
-    const uint32_t v_rows = static_cast<uint32_t>(ap.BKV);
-    auto kv_map = [&](CUtensorMap *m, const uint16_t *base, int rows, uint32_t box_rows) -> int {
-        const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Hkv),
-                                  static_cast<uint64_t>(rows), static_cast<uint64_t>(B)};
-        const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2,
-                                     static_cast<uint64_t>(Hkv) * D * 2,
-                                     static_cast<uint64_t>(rows) * Hkv * D * 2};
-        const uint32_t box[4] = {64, 1, box_rows, 1};
-        return make_map_bf16(m, base, 4, dims, strides, box);
-    };
-    if ((rc = kv_map(&mkc, k_canvas, L, k_rows)) != DG_OK) return rc;
-    if ((rc = kv_map(&mvc, v_canvas, L, v_rows)) != DG_OK) return rc;
-    if (P > 0) {
-        if ((rc = kv_map(&mkp, k_prefix, P, k_rows)) != DG_OK) return rc;
-        if ((rc = kv_map(&mvp, v_prefix, P, v_rows)) != DG_OK) return rc;
-    } else {
-        mkp = mkc;
-        mvp = mvc;
-    }
-    AttnArgs a{};
-    a.B = B;
-    a.L = L;
-    a.P = P;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.D = D;
-    a.G = G;
-    a.rows = L * G;
-    a.mtiles = ap.mtiles;
-    a.nsplit = ap.nsplit;
-    a.nkt_p = ap.nkt_p;
-    a.nkt_c = ap.nkt_c;
-    a.tiles_per_split = ap.tps;
-    a.scale_log2 = scale * 1.44269502162933349609375f;
-    a.q = q;
-    a.out = out;
-    a.ws = static_cast<WsHeader *>(workspace);
-    if (ap.nsplit > 1) {
-        uint8_t *p = static_cast<uint8_t *>(workspace) + sizeof(WsHeader);
-        const size_t nr = static_cast<size_t>(B) * L * Hq;
-        a.part_o = reinterpret_cast<uint16_t *>(p);
-        a.part_ml = reinterpret_cast<float *>(
-            p + round_up(static_cast<size_t>(ap.nsplit) * nr * D * 2, 256));
-    }
-    const bool pdl = use_pdl(st);
-    const dim3 grid(ap.mtiles, Hkv * B, ap.nsplit);
-    if (ap.pair)
-        DG_CUDA_TRY(launch_kernel(D == 128 ? attn_pair_kernel_d128 : attn_pair_kernel_d256, grid,
-                                  dim3(kAttnThreads), attn_pair_smem_bytes(D), st, pdl, mq, mkp,
-                                  mvp, mkc, mvc, a));
-    else
-        DG_CUDA_TRY(launch_kernel(D == 128 ? attn_kernel_d128 : attn_kernel_d256, grid,
-                                  dim3(kAttnThreads), attn_smem_bytes(D), st, pdl, mkp, mvp, mkc,
-                                  mvc, a));
-    DG_LAUNCHED();
-    if (ap.nsplit > 1) {
-        const size_t nr = static_cast<size_t>(B) * L * Hq;
-        DG_CUDA_TRY(launch_kernel(attn_combine_kernel, dim3(static_cast<unsigned>((nr + 7) / 8)),
-                                  dim3(256), 0, st, pdl, a));
-        DG_LAUNCHED();
-    }
-    return DG_OK;
+size_t dg_encoder_append_workspace(int B, int L, int P, int Hq, int Hkv, int D)
+{
+    return dg_canvas_attn_workspace(B, L, P, Hq, Hkv, D);
+}
+
+int dg_encoder_append(const uint16_t *q, uint16_t *k_cache, uint16_t *v_cache, int P, int P_max,
+                      const uint16_t *k_new, const uint16_t *v_new, uint16_t *out, int B, int L,
+                      int Hq, int Hkv, int D, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    if (!k_cache || !v_cache || !k_new || !v_new) return DG_ERR_INVALID_ARG;
+    if (P < 0 || L < 1 || B < 1 || Hkv < 1 || P_max < P + L) return DG_ERR_INVALID_ARG;
+    if (D != 128 && D != 256) return DG_ERR_UNSUPPORTED;
+    if (static_cast<long long>(P_max) * Hkv * D > (1LL << 31)) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return DG_ERR_ALIGNMENT;
+    if (workspace == nullptr || workspace_bytes < dg_encoder_append_workspace(B, L, P, Hq, Hkv, D))
+        return DG_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    // append: cache rows [P, P + L) of every batch entry <- the block's K / V
+    const size_t row_bytes = static_cast<size_t>(Hkv) * D * 2;
+    const size_t off = static_cast<size_t>(P) * Hkv * D;
+    DG_CUDA_TRY(cudaMemcpy2DAsync(k_cache + off, static_cast<size_t>(P_max) * row_bytes, k_new,
+                                  static_cast<size_t>(L) * row_bytes,
+                                  static_cast<size_t>(L) * row_bytes, static_cast<size_t>(B),
+                                  cudaMemcpyDeviceToDevice, st));
+    DG_CUDA_TRY(cudaMemcpy2DAsync(v_cache + off, static_cast<size_t>(P_max) * row_bytes, v_new,
+                                  static_cast<size_t>(L) * row_bytes,
+                                  static_cast<size_t>(L) * row_bytes, static_cast<size_t>(B),
+                                  cudaMemcpyDeviceToDevice, st));
+    // the block attends causally to [cache rows 0 .. P-1 ; its own rows]
+    return attn_run(q, k_cache, v_cache, k_new, v_new, out, B, L, P, P_max, Hq, Hkv, D, scale, 1,
+                    workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- one step

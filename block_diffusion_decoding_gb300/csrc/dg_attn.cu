@@ -282,6 +282,16 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
                 for (int c = 0; c < BKV; ++c)
                     if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
             }
+            if (a.causal && !pre) {
+                // cache-append forward: canvas keys after this row's position
+                // weigh nothing (column c is canvas key (j - nkt_p) BKV + c)
+                const int last = i - (j - a.nkt_p) * BKV;   // last visible column
+                if (__any_sync(0xFFFFFFFFu, last < BKV - 1)) {
+#pragma unroll
+                    for (int c = 0; c < BKV; ++c)
+                        if (c > last) sr[c] = __float_as_uint(-INFINITY);
+                }
+            }
             // the scale is positive, so the scaled maximum is the maximum scaled
             float rmax = -INFINITY;
 #pragma unroll
@@ -301,7 +311,10 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
             // p = 2^(s scale - m), two columns per paired instruction; the row
             // sum is kept in fp32 (the MMA sees p rounded to bf16)
             const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            // a row with no visible key yet (causal, later key split) keeps
+            // m_ref = -inf and weighs every column 0
+            const float mexp = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float2 nm2 = make_float2(-mexp, -mexp);
             float2 acc = make_float2(0.f, 0.f);
             uint32_t pk[BKV / 2];
 #pragma unroll
@@ -346,7 +359,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
         if (ok) ok = mbar_wait(o_full, 0, a.ws, 223);
         if (__all_sync(0xFFFFFFFFu, ok)) {
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;   // no visible key: zero row
             const size_t nrows = static_cast<size_t>(a.B) * a.L * a.Hq;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -426,7 +439,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
     const int per = a.D / 32;   // 4 or 8 consecutive dims per lane
     for (int z = 0; z < a.nsplit; ++z) {
         const float2 v = ml[z * nrows + row];
-        const float wz = fast_exp2(v.x - mx) * v.y;
+        // a split with no visible key for this row has l = 0 (and a zero row)
+        const float wz = (v.y > 0.f) ? fast_exp2(v.x - mx) * v.y : 0.f;
         den += wz;
         const uint16_t *po = a.part_o + (z * nrows + row) * a.D + lane * per;
         uint32_t pw[4];

@@ -329,6 +329,16 @@ __device__ __forceinline__ void attn_pair_body(const CUtensorMap *map_q, const C
                 for (int c = 0; c < BKV; ++c)
                     if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
             }
+            if (a.causal && !pre) {
+                // cache-append forward: canvas keys after this row's position
+                // weigh nothing (column c is canvas key (j - nkt_p) BKV + c)
+                const int last = i - (j - a.nkt_p) * BKV;   // last visible column
+                if (__any_sync(0xFFFFFFFFu, last < BKV - 1)) {
+#pragma unroll
+                    for (int c = 0; c < BKV; ++c)
+                        if (c > last) sr[c] = __float_as_uint(-INFINITY);
+                }
+            }
             // the scale is positive, so the scaled maximum is the maximum scaled
             float rmax = -INFINITY;
 #pragma unroll
@@ -346,7 +356,10 @@ __device__ __forceinline__ void attn_pair_body(const CUtensorMap *map_q, const C
                 rescale = true;
             }
             const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            // a row with no visible key yet (causal, later key split) keeps
+            // m_ref = -inf and weighs every column 0
+            const float mexp = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const float2 nm2 = make_float2(-mexp, -mexp);
             float2 acc = make_float2(0.f, 0.f);
             uint32_t pk[BKV / 2];
 #pragma unroll
@@ -390,7 +403,7 @@ __device__ __forceinline__ void attn_pair_body(const CUtensorMap *map_q, const C
         if (ok) ok = mbar_wait(o_full, 0, a.ws, 253);
         if (__all_sync(0xFFFFFFFFu, ok)) {
             tc_fence_after();
-            const float inv_l = 1.f / l;
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;   // no visible key: zero row
             const size_t nrows = static_cast<size_t>(a.B) * a.L * a.Hq;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {

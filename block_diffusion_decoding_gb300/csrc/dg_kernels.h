@@ -122,6 +122,7 @@ struct AttnArgs {
     int nkt_p, nkt_c;   // key tiles in the prefix / canvas
     int tiles_per_split;
     float scale_log2;   // scale * log2(e)
+    int causal;         // canvas keys after a query's position are masked (cache append)
     const uint16_t *q;  // [B, L, Hq, D]
     uint16_t *out;      // [B, L, Hq, D] (nsplit == 1)
     uint16_t *part_o;   // [nsplit][B*L*Hq][D] bf16, each split's rows normalised by its sum (nsplit > 1)

@@ -88,6 +88,27 @@ int dg_canvas_attn(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
                    void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Encoder cache append.                                                     */
+/* "Parallel Denoising From an Autoregressive Checkpoint", section           */
+/* "Finding": after a block is committed, the causal encoder runs once more  */
+/* over it and extends its append-only KV cache, which the next block's      */
+/* canvas then attends to.  This call (1) copies the block's keys / values   */
+/* k_new, v_new [B, L, Hkv, D] into rows P .. P+L-1 of the caches k_cache,   */
+/* v_cache [B, P_max, Hkv, D] (rows 0 .. P-1 hold the earlier tokens) and    */
+/* (2) computes the block's causal attention: for canvas position i,         */
+/*   out[b,i,h,:] = softmax_j(scale * q[b,i,h,:] . K_j) V_j over the P cached */
+/* rows and the block's rows 0 .. i.  q, out [B, L, Hq, D]; all bf16;         */
+/* P_max >= P + L.  After the call the caches hold P + L tokens.  Same        */
+/* kernels, supported shapes and workspace rules as dg_canvas_attn; the       */
+/* caches are written in stream order before the attention reads them.       */
+/* ------------------------------------------------------------------------ */
+size_t dg_encoder_append_workspace(int B, int L, int P, int Hq, int Hkv, int D);
+int dg_encoder_append(const uint16_t *q, uint16_t *k_cache, uint16_t *v_cache, int P, int P_max,
+                      const uint16_t *k_new, const uint16_t *v_new, uint16_t *out, int B, int L,
+                      int Hq, int Hkv, int D, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* One denoising step after the decoder body: LM head -> per-position        */
 /* entropy, Gumbel-max sample and argmax -> entropy-bounded acceptance and    */
 /* uniform renoise -> adaptive stop test.                                     */

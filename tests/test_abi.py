@@ -108,6 +108,14 @@ def test_host_validation_rejects_before_launch(lib):
     # check entries
     assert lib.dg_logf_eval(None, None, -1, None) == 1
     assert lib.dg_gumbel_fill(0, 0, 0, 0, 0, None, None) == 0
+    # encoder cache append: the cache must have room for the block
+    def enc(P, P_max, D=128, kc=good):
+        return lib.dg_encoder_append(_vp(good), _vp(kc), _vp(good), P, P_max, _vp(good), _vp(good),
+                                     _vp(good), 1, 256, 4, 1, D, 0.1, _vp(good), 1 << 30, None)
+
+    assert enc(100, 300) == 1           # P + L > P_max
+    assert enc(0, 256, D=64) == 2       # head dim
+    assert enc(0, 256, kc=good + 4) == 3
     # LM-head plan query: shapes the step rejects are rejected before any device call
     assert lib.dg_lm_head_plan(0, 1024, 16384, None, None, None) == 1
     assert lib.dg_lm_head_plan(256, 1000, 16384, None, None, None) == 2
