@@ -617,6 +617,90 @@ def run_block(args, cfg):
     return 0
 
 
+# ----------------------------------------------------------------------------- encoder append
+def run_encoder(args, cfg):
+    """The encoder cache append (dg_encoder_append): the committed block's K/V
+    appended to a cache holding P tokens and the block's causal attention over
+    [cache ; block].  Timed per call with the L2 flushed before each; the cache
+    is reset to P tokens before every call (outside the timed region)."""
+    import torch
+    import block_diffusion_decoding_gb300 as dg
+    from block_diffusion_decoding_gb300 import build as dgbuild
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+    dgbuild.build()
+    dg.lib()
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    g = torch.Generator(device=dev).manual_seed(3000 + rank)
+    bf = torch.bfloat16
+    B, L, Hq, Hkv, D, P = cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P
+    P_max = P + L
+    q = torch.randn(B, L, Hq, D, device=dev, generator=g).to(bf)
+    kcache = torch.randn(B, P_max, Hkv, D, device=dev, generator=g).to(bf)
+    vcache = torch.randn(B, P_max, Hkv, D, device=dev, generator=g).to(bf)
+    knew = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+    vnew = torch.randn(B, L, Hkv, D, device=dev, generator=g).to(bf)
+    out = torch.empty_like(q)
+    ws = dg.workspace(dg.encoder_append_workspace(B, L, P, Hq, Hkv, D), dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = 1.0 / math.sqrt(D)
+    ts = []
+    with ClockSampler(local) as clk:
+        clk.wait_first()
+        t_start = None
+        for i in range(args.warmup + args.steps):
+            if i == args.warmup:
+                if world > 1:
+                    tdist.barrier()
+                torch.cuda.synchronize(dev)
+                t_start = time.perf_counter()
+            flush.fill_(i & 0xFF)
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record(stream)
+            dg.encoder_append(q, kcache, vcache, P, knew, vnew, out, scale, ws)
+            e_.record(stream)
+            if i >= args.warmup:
+                ts.append((s_, e_))
+        torch.cuda.synchronize(dev)
+        clk.mark(t_start, time.perf_counter())
+    ms = sum(a.elapsed_time(b_) for a, b_ in ts) / len(ts)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        ms = float(tt.item())
+        tdist.destroy_process_group()
+    status = dg.read_device_status(ws)
+    if rank != 0:
+        return 0
+    # causal: the block's position i sees P + i + 1 keys
+    flops = 4.0 * B * Hq * D * (L * P + L * (L + 1) / 2)
+    nbytes = 2 * (2 * B * L * Hq * D) + 2 * (2 * B * (P + L) * Hkv * D) + 2 * (2 * B * L * Hkv * D)
+    roof_ms = max(flops / (bf16_peak * 1e12), nbytes / (hbm_peak * 1e9)) * 1e3
+    tflops = flops / (ms * 1e-3) / 1e12
+    line = dict(
+        metric="encoder cache appends/s (256-token block)", value=world * 1e3 / ms,
+        unit="appends/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=ms,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
+        config={"workload": "%s: encoder cache append, B=%d block L=%d, cache P=%d, Hq=%d Hkv=%d "
+                            "D=%d, causal over [cache ; block]" % (cfg.name, B, L, P, Hq, Hkv, D),
+                "global_batch": B, "seq_len": L, "parallelism": "replicas",
+                "l2": "flushed (256 MiB write) before every call"},
+        roofline=dict(bound="tensor", achieved=tflops, peak=bf16_peak, unit="TFLOP/s",
+                      frac=tflops / bf16_peak, traffic=None, kernel="attention (causal)",
+                      peak_source=peak_kind + " (MEASURED_PEAKS.json bf16_tflops, burst)",
+                      algorithmic_flops=flops),
+        step_roofline_ms=roof_ms, step_frac_of_roofline=roof_ms / ms,
+        clocks=clk.summary(), device_status=status)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def oracle_block_step_estimate(cfg, host, v_sample=16384):
     """One step of the block loop on the CPU oracle, column-sampled: every canvas
     row against the first v_sample vocabulary columns (LM head + sampler, time
@@ -705,6 +789,8 @@ def main():
         return run_kernel_only(args, cfg)
     if cfg.name == "block_full":
         return run_block(args, cfg)
+    if cfg.name.startswith("encoder"):
+        return run_encoder(args, cfg)
     return run_ours(args, cfg)
 
 

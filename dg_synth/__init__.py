@@ -65,6 +65,9 @@ CONFIGS = {
     "long_context": StepConfig("long_context", P=32768),
     # full block loop (hidden states built per step, see block_hidden)
     "block_full": StepConfig("block_full", d=2816, V=262144, w_std=0.02, P=0, Hq=4, Hkv=1),
+    # encoder cache append after a committed block (causal attention over
+    # [cache ; block]) at the full-width step's attention shapes
+    "encoder_full": StepConfig("encoder_full", Hq=16, Hkv=8, D=256, P=4096),
 }
 
 
