@@ -92,6 +92,12 @@ def lib():
                                             _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                             _c_dbl, _c_i32, _vp, _c_i64, _vp]
         L.orc_attention_rows_ex.restype = None
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_decode.restype = _c_dbl
+        L.orc_e4m3_encode.argtypes = [_c_flt]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_quantize_rows_e4m3.argtypes = [_vp, _c_i64, _c_i64, _vp, _vp]
+        L.orc_quantize_rows_e4m3.restype = None
         L.orc_gumbel_fill.argtypes = [_c_u64, _c_u32, _c_u32, _c_u32, _c_i32, _vp]
         L.orc_gumbel_fill.restype = None
         _lib = L
@@ -254,13 +260,61 @@ def attention_rows(q, kp, vp, kc, vc, B, L, P, Hq, Hkv, D, scale, rows,
     return out
 
 
+# ---------------------------------------------------------------- FP8 (E4M3) LM head
+def e4m3_decode(code: int) -> float:
+    return float(lib().orc_e4m3_decode(int(code)))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().orc_e4m3_encode(float(x)))
+
+
+def e4m3_table() -> np.ndarray:
+    """Values of all 256 codes (NaN for 0x7F, 0xFF)."""
+    return np.array([e4m3_decode(c) for c in range(256)])
+
+
+def quantize_rows_e4m3(x_bits: np.ndarray):
+    """Per-row E4M3 quantisation of bf16 rows [n, c] -> (codes uint8 [n, c], scale fp32 [n])."""
+    x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
+    n, c = x.shape
+    q = np.zeros((n, c), np.uint8)
+    sc = np.zeros(n, np.float32)
+    lib().orc_quantize_rows_e4m3(_ptr(x), n, c, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def quantize_weight_e4m3(w_bits: np.ndarray):
+    """W [d, V] (bf16 bits) -> (W8t [V, d] codes, scale [V]): each vocabulary
+    column quantised as one row."""
+    return quantize_rows_e4m3(np.ascontiguousarray(np.asarray(w_bits, dtype=np.uint16).T))
+
+
+def logits_fp8(x8: np.ndarray, sx: np.ndarray, w8t: np.ndarray, sw: np.ndarray,
+               col_chunk: int = 32768) -> np.ndarray:
+    """fp64 logits of the quantised operands: (dec(x8) sx) (dec(w8t) sw)^T."""
+    tab = e4m3_table()
+    X = tab[np.asarray(x8)] * np.asarray(sx, np.float64)[:, None]
+    V = w8t.shape[0]
+    out = np.empty((X.shape[0], V))
+    for c0 in range(0, V, col_chunk):
+        c1 = min(V, c0 + col_chunk)
+        Wc = tab[np.asarray(w8t[c0:c1])] * np.asarray(sw[c0:c1], np.float64)[:, None]
+        out[:, c0:c1] = X @ Wc.T
+    return out
+
+
 # ---------------------------------------------------------------- step / block
 def step(x_bits: np.ndarray, w_bits: np.ndarray, canvas: np.ndarray, prev_argmax: np.ndarray,
          B: int, L: int, T: float, b: float, seed: int, k: int,
-         stop_threshold: float = 0.005, workers: int = 1) -> dict:
-    """One denoising step (LM head -> sampler -> accept/renoise -> stop) for B canvases."""
-    V = w_bits.shape[1]
-    lg = logits(x_bits, w_bits)
+         stop_threshold: float = 0.005, workers: int = 1, lg: Optional[np.ndarray] = None) -> dict:
+    """One denoising step (LM head -> sampler -> accept/renoise -> stop) for B canvases.
+
+    lg: precomputed fp64 logits (e.g. of the FP8 operands); x_bits/w_bits are
+    then used only for the vocabulary size."""
+    V = w_bits.shape[1] if lg is None else lg.shape[1]
+    if lg is None:
+        lg = logits(x_bits, w_bits)
     s = sampler(lg, T, seed, np.arange(B * L), k, workers=workers)
     Hf = s["H"].astype(np.float32)
     new_canvas = np.array(canvas, dtype=np.int32, copy=True).reshape(B, L)

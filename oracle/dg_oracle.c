@@ -377,3 +377,67 @@ void orc_gumbel_fill(uint64_t seed, uint32_t row, uint32_t step, uint32_t v0, in
     for (int32_t t = 0; t < n; ++t)
         out[t] = orc_gumbel_from_bits(orc_gumbel_bits(seed, row, step, v0 + (uint32_t)t));
 }
+
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) weight and hidden-state streams for the LM head.  The pages
+ * quote their H100 throughput for an FP8 model ("DiffusionGemma Lab",
+ * section 1; "Parallel Denoising From an Autoregressive Checkpoint", section
+ * "Finding"); the format is OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3
+ * mantissa bits, no infinities, 0x7F / 0xFF NaN, largest finite 448.
+ * Quantisation of a row of n values x (bf16): amax = max |x|; if amax == 0
+ * every code is 0 and the scale 1, else inv = fp32(448 / amax), scale =
+ * fp32(amax / 448), code_j = E4M3 nearest-even of fp32(x_j * inv), saturated
+ * to +-448.  The row then stands for decode(code_j) * scale.
+ * ------------------------------------------------------------------------- */
+double orc_e4m3_decode(uint8_t c)
+{
+    const int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    double v;
+    if (e == 0xF && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);                 /* subnormal: m/8 * 2^-6 */
+    else v = ldexp(8.0 + m, e - 10);                     /* (1 + m/8) * 2^(e-7) */
+    return s ? -v : v;
+}
+
+uint8_t orc_e4m3_encode(float x)
+{
+    /* nearest of the 127 non-negative finite codes to |x| (ties: even code),
+       saturating at 448; a plain search over the code table */
+    const uint8_t sign = (signbit(x) ? 0x80 : 0x00);
+    double a = fabs((double)x);
+    if (isnan(x)) return 0x7F;
+    if (a > 448.0) a = 448.0;
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        const double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            bd = d;
+            best = (uint8_t)c;
+        }
+    }
+    return (uint8_t)(best | sign);
+}
+
+void orc_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int64_t cols, uint8_t *q, float *scale)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * cols;
+        float amax = 0.0f;
+        for (int64_t j = 0; j < cols; ++j) {
+            const float v = fabsf((float)orc_bf16(xr[j]));
+            if (v > amax) amax = v;
+        }
+        if (amax == 0.0f) {
+            scale[r] = 1.0f;
+            for (int64_t j = 0; j < cols; ++j) q[r * cols + j] = 0;
+            continue;
+        }
+        const float inv = 448.0f / amax;
+        scale[r] = amax / 448.0f;
+        for (int64_t j = 0; j < cols; ++j) {
+            const float v = (float)orc_bf16(xr[j]) * inv;
+            q[r * cols + j] = orc_e4m3_encode(v);
+        }
+    }
+}

@@ -419,3 +419,65 @@ def test_loop_batched_canvases_stop_independently():
     hid = np.concatenate([confident, flat])      # canvas 0 confident, canvas 1 flat
     res = oracle.block(lambda k: hid, w, 2, L, 0.1, 3, max_steps=6)
     assert res["steps"].tolist() == [2, 6]
+
+
+# ------------------------------------------------------------------ FP8 (E4M3) LM-head operands
+def test_e4m3_decode_matches_torch_and_published_values():
+    tab = oracle.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(tab), nan) and nan.sum() == 2       # 0x7F, 0xFF
+    assert np.array_equal(tab[~nan], ref[~nan])
+    # published landmarks of the format: largest finite, smallest normal and
+    # subnormal, one, minus two
+    assert tab[0x7E] == 448.0 and tab[0x08] == 2.0 ** -6 and tab[0x01] == 2.0 ** -9
+    assert tab[0x38] == 1.0 and tab[0xC0] == -2.0 and tab[0x00] == 0.0
+
+
+def test_e4m3_encode_nearest_even_and_saturating():
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.standard_normal(3000) * 50, rng.uniform(-448, 448, 3000),
+                        rng.standard_normal(1000) * 1e-3]).astype(np.float32)
+    codes = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
+    # torch's conversion (round to nearest even) agrees on the finite range
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    # brute force: the decoded code is a nearest finite value
+    tab = oracle.e4m3_table()
+    fin = tab[np.isfinite(tab)]
+    dist = np.abs(tab[codes] - x.astype(np.float64))
+    best = np.abs(fin[None, :] - x.astype(np.float64)[:, None]).min(axis=1)
+    assert np.array_equal(dist, best)
+    # saturation instead of NaN beyond the largest finite value
+    assert oracle.e4m3_encode(1e6) == 0x7E and oracle.e4m3_encode(-500.0) == 0xFE
+
+
+def test_row_quantisation_scale_and_error_bound():
+    rng = np.random.default_rng(9)
+    x = _bf16_bits(rng.standard_normal((6, 300)) * rng.uniform(0.01, 100, (6, 1)))
+    x[3] = 0   # an all-zero row: codes 0, scale 1
+    q, sc = oracle.quantize_rows_e4m3(x)
+    xf = oracle.bf16_bits_to_f64(x)
+    tab = oracle.e4m3_table()
+    assert (q[3] == 0).all() and sc[3] == 1.0
+    for r in (0, 1, 2, 4, 5):
+        amax = np.abs(xf[r]).max()
+        assert sc[r] == np.float32(np.float32(amax) / np.float32(448.0))
+        assert np.abs(tab[q[r]]).max() == 448.0          # the largest entry maps to 448
+        # E4M3 keeps 3 mantissa bits: error <= 2^-4 of the value (normals) or
+        # half the smallest subnormal step (2^-10) in code units
+        err = np.abs(tab[q[r]] * sc[r] - xf[r])
+        bound = np.maximum(np.abs(xf[r]) * 2.0 ** -4, 2.0 ** -10 * sc[r]) * 1.0001
+        assert (err <= bound).all()
+
+
+def test_fp8_logits_exact_on_small_integers():
+    """Codes of small integers are exact: the FP8 logits equal the integer product."""
+    rng = np.random.default_rng(10)
+    X = rng.integers(-8, 9, size=(5, 64)).astype(np.float32)
+    W = rng.integers(-8, 9, size=(64, 40)).astype(np.float32)
+    x8 = np.array([[oracle.e4m3_encode(v) for v in row] for row in X], np.uint8)
+    w8t = np.array([[oracle.e4m3_encode(v) for v in row] for row in W.T], np.uint8)
+    got = oracle.logits_fp8(x8, np.ones(5, np.float32), w8t, np.ones(40, np.float32), col_chunk=7)
+    assert np.array_equal(got, X.astype(np.float64) @ W.astype(np.float64))
+
