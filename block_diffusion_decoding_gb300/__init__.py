@@ -32,7 +32,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_generate_block_workspace", "dg_generate_block",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
             "dg_lm_head_fold", "dg_kernel_launches", "dg_lm_head_plan", "dg_gumbel_fill",
-            "dg_logf_eval"]
+            "dg_logf_eval", "dg_quantize_rows_e4m3", "dg_quantize_weight_e4m3",
+            "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8"]
 
 
 class DgError(RuntimeError):
@@ -102,6 +103,11 @@ def _lib():
             "dg_lm_head_plan": ([i32, i32, i32, ip, ip, ip], i32),
             "dg_gumbel_fill": ([u64, u32, u32, u32, i32, vp, vp], i32),
             "dg_logf_eval": ([vp, vp, i32, vp], i32),
+            "dg_quantize_rows_e4m3": ([vp, ctypes.c_int64, i32, vp, vp, vp], i32),
+            "dg_quantize_weight_e4m3": ([vp, i32, i32, vp, vp, vp], i32),
+            "dg_denoise_step_fp8_workspace": ([sp], sz),
+            "dg_denoise_step_fp8": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
+            "dg_lm_head_fold_fp8": ([vp, vp, vp, sp, vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -218,6 +224,41 @@ def lm_head_plan(rows: int, d: int, V: int) -> dict:
     _check(rc, "dg_lm_head_plan")
     names = ("lm_head_kernel", "lm_head_pair_kernel", "lm_head_duo_kernel")
     return {"kernel": names[kind.value], "kind": kind.value, "BN": bn.value, "ctas": ctas.value}
+
+
+# ---------------------------------------------------------------- FP8 LM head
+def quantize_rows_e4m3(x, codes, scale, stream=None):
+    """x [rows, cols] bf16 -> E4M3 codes (uint8, same shape) and fp32 row scales."""
+    rows, cols = x.shape
+    rc = _lib().dg_quantize_rows_e4m3(_p(x), rows, cols, _p(codes), _p(scale), _stream(stream))
+    _check(rc, "dg_quantize_rows_e4m3")
+
+
+def quantize_weight_e4m3(w, w8t, scale, stream=None):
+    """W [d, V] bf16 -> W8t [V, d] E4M3 codes and fp32 column scales [V]."""
+    d, V = w.shape
+    rc = _lib().dg_quantize_weight_e4m3(_p(w), d, V, _p(w8t), _p(scale), _stream(stream))
+    _check(rc, "dg_quantize_weight_e4m3")
+
+
+def denoise_step_fp8_workspace(p: StepParams) -> int:
+    return int(_lib().dg_denoise_step_fp8_workspace(ctypes.byref(p)))
+
+
+def denoise_step_fp8(hidden, w8t, w_scale, p: StepParams, bufs: StepBuffers, workspace,
+                     stream=None):
+    io = bufs.io()
+    rc = _lib().dg_denoise_step_fp8(_p(hidden), _p(w8t), _p(w_scale), ctypes.byref(p),
+                                    ctypes.byref(io), _p(workspace), workspace.numel(),
+                                    _stream(stream))
+    _check(rc, "dg_denoise_step_fp8")
+
+
+def lm_head_fold_fp8(hidden, w8t, w_scale, p: StepParams, workspace, stream=None):
+    """Row quantisation + the FP8 LM-head kernel of the step alone."""
+    rc = _lib().dg_lm_head_fold_fp8(_p(hidden), _p(w8t), _p(w_scale), ctypes.byref(p),
+                                    _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_lm_head_fold_fp8")
 
 
 def kernel_launches() -> int:

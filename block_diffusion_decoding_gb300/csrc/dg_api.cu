@@ -77,6 +77,9 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_fp8_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDuoSmemBytes));
         DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d128,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          attn_smem_bytes(128)));
@@ -118,10 +121,10 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle.  dims/strides innermost first;
+// Tensor map with 128-byte swizzle.  dims/strides innermost first;
 // strides[i] is the byte stride of dimension i+1.
-int make_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                  const uint64_t *strides_bytes, const uint32_t *box)
+int make_map_sw128(CUtensorMap *map, CUtensorMapDataType dt, const void *base, int rank,
+                   const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return DG_ERR_CUDA;
@@ -133,11 +136,25 @@ int make_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *
         e[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+    CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank),
                     const_cast<void *>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
+}
+
+int make_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                  const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return make_map_sw128(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes,
+                          box);
+}
+
+// E4M3 codes are moved as bytes.
+int make_map_u8(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return make_map_sw128(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides_bytes, box);
 }
 
 // Workspace layout of one step: header | partials (7 x n_slots x M x 4 B) |
@@ -229,15 +246,61 @@ AcceptArgs accept_args(const dg_step_params *p, const dg_step_io *io)
     return a;
 }
 
+// E4M3 operands of the LM head: X8 [M, d] with row scales, W8t [V, d] with
+// column scales.
+struct Fp8Operands {
+    const uint8_t *x8;
+    const float *sx;
+    const uint8_t *w8t;
+    const float *sw;
+};
+
 // Enqueue LM head (or logits fold) + combine/accept for one step.
 int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, const float *logits,
                  const uint16_t *w, const dg_step_params *p, const LmPlan &plan, StepWs &ws,
                  const StepSource &src, float *H, int32_t *sample, int32_t *argmax,
-                 const AcceptArgs &acc, cudaStream_t st, bool lm_only = false)
+                 const AcceptArgs &acc, cudaStream_t st, bool lm_only = false,
+                 const Fp8Operands *f8 = nullptr)
 {
     const int M = p->B * p->L;
     const bool pdl = use_pdl(st);
-    if (logits == nullptr) {
+    if (f8 != nullptr) {
+        CUtensorMap mx, mw;
+        {
+            const uint64_t dims[2] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(M)};
+            const uint64_t strides[1] = {static_cast<uint64_t>(p->d)};
+            const uint32_t box[2] = {128, 128};
+            int rc = make_map_u8(&mx, f8->x8, 2, dims, strides, box);
+            if (rc != DG_OK) return rc;
+        }
+        {
+            const uint64_t dims[2] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->V)};
+            const uint64_t strides[1] = {static_cast<uint64_t>(p->d)};
+            const uint32_t box[2] = {128, static_cast<uint32_t>(plan.BN / 2)};
+            int rc = make_map_u8(&mw, f8->w8t, 2, dims, strides, box);
+            if (rc != DG_OK) return rc;
+        }
+        LmHeadArgs a{};
+        a.M = M;
+        a.d = p->d;
+        a.V = p->V;
+        a.BN = plan.BN;
+        a.ntn = plan.ntn;
+        a.total = plan.total;
+        a.kblocks = p->d / 128;
+        a.nbox_b = 1;
+        a.x_3d = 0;
+        a.row_scale = f8->sx;
+        a.col_scale = f8->sw;
+        a.part = ws.part;
+        a.src = src;
+        a.seed = p->seed;
+        a.ws = ws.hdr;
+        a.counters = ws.counters;
+        a.ncounters = p->B;
+        DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl, true));
+        DG_LAUNCHED();
+    } else if (logits == nullptr) {
         CUtensorMap mx, mw;
         {
             const uint64_t dims[3] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(M),
@@ -518,6 +581,87 @@ static int attn_run(const uint16_t *q, const uint16_t *k_prefix, const uint16_t 
     return DG_OK;
 }
 
+namespace {
+
+int check_fp8_step(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
+                   const dg_step_params *p)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if (!hidden || !w8t || !w_scale) return DG_ERR_INVALID_ARG;
+    if (p->d % 128 != 0 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(w8t) || !aligned16(w_scale)) return DG_ERR_ALIGNMENT;
+    return DG_OK;
+}
+
+// Row quantisation: the register-resident vector kernel where the shapes and
+// alignments allow it, else one warp per row.
+cudaError_t launch_quantize_rows(const uint16_t *x, int64_t rows, int cols, uint8_t *q, float *scale,
+                                 cudaStream_t st, bool pdl)
+{
+    const bool vec = cols % 8 == 0 && cols <= 128 * 8 * kQuantVecs && aligned16(x) &&
+                     (reinterpret_cast<uintptr_t>(q) & 7u) == 0 && rows <= 0x7FFFFFFF;
+    cudaError_t e;
+    if (vec)
+        e = launch_kernel(quantize_rows_e4m3_vec_kernel, dim3(static_cast<unsigned>(rows)),
+                          dim3(128), 0, st, pdl, x, cols, q, scale);
+    else
+        e = launch_kernel(quantize_rows_e4m3_kernel, dim3(static_cast<unsigned>((rows + 7) / 8)),
+                          dim3(256), 0, st, pdl, x, rows, cols, q, scale);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e;
+}
+
+// Workspace of the FP8 step: the step's | X8 [M, d] | row scales [M].
+size_t fp8_ws_bytes(const dg_step_params *p, size_t *off_x8, size_t *off_sx)
+{
+    const size_t M = static_cast<size_t>(p->B) * p->L;
+    size_t off = round_up(step_ws_bytes(static_cast<int>(M), p->B, slot_bound(static_cast<int>(M), p->V)), 256);
+    if (off_x8) *off_x8 = off;
+    off += round_up(M * p->d, 256);
+    if (off_sx) *off_sx = off;
+    return off + round_up(M * 4, 256);
+}
+
+int fp8_step(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
+             const dg_step_params *p, const dg_step_io *io, void *workspace,
+             size_t workspace_bytes, void *stream, bool lm_only)
+{
+    int rc = check_fp8_step(hidden, w8t, w_scale, p);
+    if (rc != DG_OK) return rc;
+    if (!lm_only && (rc = check_io(io, true)) != DG_OK) return rc;
+    size_t off_x8 = 0, off_sx = 0;
+    const size_t need = fp8_ws_bytes(p, &off_x8, &off_sx);
+    if (workspace == nullptr || workspace_bytes < need) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    const int M = p->B * p->L;
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, true);
+    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
+    Fp8Operands f8{};
+    f8.x8 = static_cast<uint8_t *>(workspace) + off_x8;
+    f8.sx = reinterpret_cast<const float *>(static_cast<uint8_t *>(workspace) + off_sx);
+    f8.w8t = w8t;
+    f8.sw = w_scale;
+    cudaStream_t st = as_stream(stream);
+    // the hidden states of this step are quantised per canvas row first
+    DG_CUDA_TRY(launch_quantize_rows(hidden, M, p->d, const_cast<uint8_t *>(f8.x8),
+                                     const_cast<float *>(f8.sx), st, use_pdl(st)));
+    DG_LAUNCHED();
+    const StepSource src = step_source(p);
+    if (lm_only) {
+        AcceptArgs acc{};
+        return enqueue_step(nullptr, 0, 1, nullptr, nullptr, p, plan, ws, src, nullptr, nullptr,
+                            nullptr, acc, st, true, &f8);
+    }
+    const AcceptArgs acc = accept_args(p, io);
+    return enqueue_step(nullptr, 0, 1, nullptr, nullptr, p, plan, ws, src, io->entropy, io->sample,
+                        io->argmax, acc, st, false, &f8);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char *dg_status_string(int status)
@@ -662,6 +806,54 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 }
 
 uint64_t dg_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------- FP8 LM head
+int dg_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int cols, uint8_t *codes, float *scale,
+                          void *stream)
+{
+    if (!x || !codes || !scale || rows < 1 || cols < 1) return DG_ERR_INVALID_ARG;
+    if (rows > (1LL << 31) * 8 - 8) return DG_ERR_UNSUPPORTED;
+    DG_CUDA_TRY(launch_quantize_rows(x, rows, cols, codes, scale, as_stream(stream), false));
+    DG_LAUNCHED();
+    return DG_OK;
+}
+
+int dg_quantize_weight_e4m3(const uint16_t *w, int d, int V, uint8_t *w8t, float *scale,
+                            void *stream)
+{
+    if (!w || !w8t || !scale || d < 1 || V < 1) return DG_ERR_INVALID_ARG;
+    if (d > 65535 * 32) return DG_ERR_UNSUPPORTED;
+    cudaStream_t st = as_stream(stream);
+    column_amax_kernel<<<(V + 255) / 256, 256, 0, st>>>(w, d, V, scale);
+    DG_LAUNCHED();
+    quantize_cols_e4m3_kernel<<<dim3((V + 31) / 32, (d + 31) / 32), 256, 0, st>>>(w, d, V, scale,
+                                                                                 w8t);
+    DG_LAUNCHED();
+    scale_from_amax_kernel<<<(V + 255) / 256, 256, 0, st>>>(scale, V);
+    DG_LAUNCHED();
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+size_t dg_denoise_step_fp8_workspace(const dg_step_params *p)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    return fp8_ws_bytes(p, nullptr, nullptr);
+}
+
+int dg_denoise_step_fp8(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
+                        const dg_step_params *p, const dg_step_io *io, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    return fp8_step(hidden, w8t, w_scale, p, io, workspace, workspace_bytes, stream, false);
+}
+
+int dg_lm_head_fold_fp8(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
+                        const dg_step_params *p, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    return fp8_step(hidden, w8t, w_scale, p, nullptr, workspace, workspace_bytes, stream, true);
+}
 
 int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas)
 {

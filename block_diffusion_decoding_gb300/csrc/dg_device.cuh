@@ -352,6 +352,19 @@ DG_DEVICE void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
         : "memory");
 }
 
+// 2-SM UMMA of E4M3 operands (kind::f8f6f4: K = 32 per instruction, fp32
+// accumulator), both from shared memory.
+DG_DEVICE void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                              uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 DG_DEVICE void umma_bf16_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                  uint32_t accumulate)
 {
@@ -554,6 +567,17 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int b_mn_ma
            | (1u << 10)                                // B format: bf16
            | (0u << 15)                                // A major: K
            | (static_cast<uint32_t>(b_mn_major) << 16) // B major
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0),
+// both K-major, fp32 accumulator.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N)
+{
+    return (1u << 4)                                   // D format: f32
+           | (0u << 7)                                 // A format: E4M3
+           | (0u << 10)                                // B format: E4M3
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

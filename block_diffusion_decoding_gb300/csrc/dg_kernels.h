@@ -50,12 +50,16 @@ struct AcceptArgs {
 
 struct LmHeadArgs {
     int M, d, V;
-    int BN;             // vocabulary columns per tile (multiple of 16, <= 128)
+    int BN;             // vocabulary columns per tile (multiple of 16)
     int ntn;            // vocabulary tiles per row block
     int total;          // tiles = row blocks * ntn
-    int kblocks;        // d / 64
+    int kblocks;        // k blocks of 128 bytes per row: d / 64 (bf16), d / 128 (FP8)
     int nbox_b;         // 64-column TMA boxes per W stage
     int x_3d;           // hidden states carry a step coordinate
+    // FP8 operands (E4M3 codes): logit = acc * row_scale[row] * col_scale[v];
+    // both null for bf16 operands
+    const float *row_scale;
+    const float *col_scale;
     Partials part;
     StepSource src;
     uint64_t seed;
@@ -100,6 +104,23 @@ constexpr int kDuoStageBytes = kPairABytes + 2 * kLmBBoxBytes;      // 32 KB
 constexpr int kDuoSmemBytes = kDuoStages * kDuoStageBytes + 1024 + 256 + kPairMergeBytes;
 __global__ void lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
                                    const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+// FP8 (E4M3) operands of the 2-SM kernel: X8 [M, d] and W8t [V, d] (both
+// K-major, 128-byte k blocks = 128 codes); same tiles, 256 x 256 x 32 UMMAs.
+__global__ void lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,
+                                       const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+// Per-row E4M3 quantisation of bf16 rows [rows, cols] (one warp per row) and of
+// the columns of W [d, V] into W8t [V, d] (column maxima, then 32 x 32 tiles).
+__global__ void quantize_rows_e4m3_kernel(const uint16_t *__restrict__ x, int64_t rows, int cols,
+                                          uint8_t *__restrict__ q, float *__restrict__ scale);
+constexpr int kQuantVecs = 16;   // 16-byte vectors per thread of the vector row kernel
+__global__ void quantize_rows_e4m3_vec_kernel(const uint16_t *__restrict__ x, int cols,
+                                              uint8_t *__restrict__ q, float *__restrict__ scale);
+__global__ void column_amax_kernel(const uint16_t *__restrict__ w, int d, int V,
+                                   float *__restrict__ amax);
+__global__ void quantize_cols_e4m3_kernel(const uint16_t *__restrict__ w, int d, int V,
+                                          const float *__restrict__ amax,
+                                          uint8_t *__restrict__ w8t);
+__global__ void scale_from_amax_kernel(float *__restrict__ s, int n);
 __global__ void logits_fold_kernel(const float *__restrict__ logits, FoldArgs a);
 __global__ void combine_accept_kernel(CombineArgs c, AcceptArgs a);
 __global__ void accept_only_kernel(const float *__restrict__ H, const int32_t *__restrict__ sample,

@@ -26,13 +26,22 @@
 //               32 (w % 4) .. +31, every 4th 16-column chunk starting at
 //               chunk (w - 4) / 4; the column groups merge in shared memory
 //               and one partial state per (row, cluster) is stored.
+//
+// The FP8 instance (lm_head_duo_fp8_kernel) takes E4M3 codes of the hidden
+// block X8 [M, d] and of the transposed weight W8t [V, d], both K-major: a
+// k block is 128 codes (the same 128 bytes per row as 64 bf16 values), the
+// W half tile is one box of BN/2 rows x 128 bytes, and the UMMA is
+// kind::f8f6f4 with K = 32.  The epilogue applies the row and column scales
+// before the fold.  Half the weight bytes per vocabulary column.
 #include "dg_kernels.h"
 
 namespace dg {
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
-    lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
-                       const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+namespace {
+
+template <bool kFp8>
+DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map_w,
+                                const LmHeadArgs &a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -112,15 +121,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
                     uint8_t *sa = smem + s * kDuoStageBytes;
                     uint8_t *sb = sa + kPairABytes;
                     // the block loop passes hidden states with a step coordinate (3-D map)
+                    // 128 bytes of each row: 64 bf16 values or 128 codes
+                    const int kx = kb * (kFp8 ? 128 : kLmBK);
                     if (a.x_3d)
-                        tma_load_3d_pair(sa, &map_x, fb, kb * kLmBK, m * kRowsPerBlock + r * 128,
-                                         xstep, pol_x);
-                    else
-                        tma_load_2d_pair(sa, &map_x, fb, kb * kLmBK, m * kRowsPerBlock + r * 128,
+                        tma_load_3d_pair(sa, &map_x, fb, kx, m * kRowsPerBlock + r * 128, xstep,
                                          pol_x);
-                    for (int j = 0; j < half_boxes; ++j)
-                        tma_load_2d_pair(sb + j * kLmBBoxBytes, &map_w, fb,
-                                         n * a.BN + r * (a.BN / 2) + j * 64, kb * kLmBK, pol_w);
+                    else
+                        tma_load_2d_pair(sa, &map_x, fb, kx, m * kRowsPerBlock + r * 128, pol_x);
+                    if constexpr (kFp8) {
+                        // W8t rows n BN + r BN/2 .., 128 codes of k block kb
+                        tma_load_2d_pair(sb, &map_w, fb, kb * 128, n * a.BN + r * (a.BN / 2),
+                                         pol_w);
+                    } else {
+                        for (int j = 0; j < half_boxes; ++j)
+                            tma_load_2d_pair(sb + j * kLmBBoxBytes, &map_w, fb,
+                                             n * a.BN + r * (a.BN / 2) + j * 64, kb * kLmBK, pol_w);
+                    }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == kDuoStages) { s = 0; ph ^= 1u; }
@@ -135,10 +151,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && r == 0) {
-            const uint32_t idesc = make_idesc_bf16(256, a.BN, 1);
+            const uint32_t idesc = kFp8 ? make_idesc_e4m3(256, a.BN) : make_idesc_bf16(256, a.BN, 1);
             const uint32_t sa0 = smem_u32(smem);
             const uint64_t adesc0 = make_sdesc_sw128(sa0, 16, 1024);
-            const uint64_t bdesc0 = make_sdesc_sw128(sa0 + kPairABytes, kLmBBoxBytes, 1024);
+            // B: K-major 128-byte rows (FP8) or MN-major 64-column blocks (bf16)
+            const uint64_t bdesc0 = kFp8 ? make_sdesc_sw128(sa0 + kPairABytes, 16, 1024)
+                                         : make_sdesc_sw128(sa0 + kPairABytes, kLmBBoxBytes, 1024);
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -153,12 +171,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
                     tc_fence_after();
                     const uint64_t soff = static_cast<uint64_t>((s * kDuoStageBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kLmBK / 16; ++kk) {
-                        // A: K-major 128-byte rows, 8-row groups 1 KB apart, +32 B per k step;
-                        // B: MN-major, 64-column blocks 8 KB apart, 8-row groups 1 KB apart
+                    for (int kk = 0; kk < 4; ++kk) {
+                        // A: K-major 128-byte rows, 8-row groups 1 KB apart, +32 B per k step
+                        // (16 bf16 or 32 codes)
                         const uint64_t adesc = adesc0 + soff + static_cast<uint64_t>(kk * 2);
-                        const uint64_t bdesc = bdesc0 + soff + static_cast<uint64_t>(kk * (2048 >> 4));
-                        umma_bf16_pair(d, adesc, bdesc, idesc, (kb | kk) != 0);
+                        if constexpr (kFp8) {
+                            // B: K-major like A
+                            const uint64_t bdesc = bdesc0 + soff + static_cast<uint64_t>(kk * 2);
+                            umma_e4m3_pair(d, adesc, bdesc, idesc, (kb | kk) != 0);
+                        } else {
+                            // B: MN-major, 64-column blocks 8 KB apart, 8-row groups 1 KB
+                            // apart, +16 rows (2 KB) per k step
+                            const uint64_t bdesc =
+                                bdesc0 + soff + static_cast<uint64_t>(kk * (2048 >> 4));
+                            umma_bf16_pair(d, adesc, bdesc, idesc, (kb | kk) != 0);
+                        }
                     }
                     umma_commit_pair(&empty[s], 0x3);
                     if (++s == kDuoStages) { s = 0; ph ^= 1u; }
@@ -201,8 +228,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
             const int row = m * kRowsPerBlock + r * 128 + rix;
             const bool live = row < a.M;
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * a.BN);
-            fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, a.BN, static_cast<uint32_t>(n * a.BN),
-                      static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+            if constexpr (kFp8) {
+                const float rs = live ? __ldg(a.row_scale + row) : 0.f;
+                fold_tile_scaled(st, tb, 16 * cg, 16 * kPairColGroups, a.BN,
+                                 static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
+                                 static_cast<uint32_t>(row), fc, live, rs, a.col_scale);
+            } else {
+                fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, a.BN,
+                          static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
+                          static_cast<uint32_t>(row), fc, live);
+            }
             tc_fence_before();
             __syncwarp();
             // the even CTA's MMA may overwrite this accumulator once both
@@ -225,6 +260,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, 512);
     }
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+    lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
+                       const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+{
+    lm_head_duo_body<false>(map_x, map_w, a);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+    lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,
+                           const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+{
+    lm_head_duo_body<true>(map_x, map_w, a);
 }
 
 }  // namespace dg

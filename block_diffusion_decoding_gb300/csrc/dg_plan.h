@@ -35,8 +35,8 @@ struct LmPlan {
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
 // CTA, plus a per-tile overhead.  DG_LM_KERNEL=single|pair|duo and DG_LM_BN
-// force a choice.
-inline LmPlan plan_lm_head(int M, int d, int V, int sms)
+// force a choice.  FP8 operands have the 2-SM UMMA kernel only.
+inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
 {
     LmPlan best{};
     best.M = M;
@@ -44,9 +44,10 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms)
     best.d = d;
     best.mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
     const char *env_bn = std::getenv("DG_LM_BN");
-    const int forced_bn = env_bn ? std::atoi(env_bn) : 0;
+    int forced_bn = env_bn ? std::atoi(env_bn) : 0;
     const char *env_k = std::getenv("DG_LM_KERNEL");
-    const int only = !env_k ? -1
+    const int only = fp8    ? kLmDuo
+                     : !env_k ? -1
                      : std::strcmp(env_k, "single") == 0 ? kLmSingle
                      : std::strcmp(env_k, "pair") == 0   ? kLmPair
                      : std::strcmp(env_k, "duo") == 0    ? kLmDuo
@@ -77,11 +78,15 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms)
             best.grid = pair ? 2 * units : units;
         }
     };
-    for (int bn = 128; bn >= 64; bn -= 16) consider(kLmSingle, bn);
-    consider(kLmPair, 256);
-    consider(kLmPair, 128);
-    consider(kLmDuo, 256);
-    consider(kLmDuo, 128);
+    for (int pass = 0; pass < 2 && best_cost < 0; ++pass) {
+        // a forced width no candidate of the kernel has is ignored
+        if (pass == 1) forced_bn = 0;
+        for (int bn = 128; bn >= 64; bn -= 16) consider(kLmSingle, bn);
+        consider(kLmPair, 256);
+        consider(kLmPair, 128);
+        consider(kLmDuo, 256);
+        consider(kLmDuo, 128);
+    }
     return best;
 }
 
@@ -122,14 +127,16 @@ inline bool use_pdl(cudaStream_t st)
 }
 
 // Launch the planned LM-head kernel (maps: X box {64, 128} for the cluster
-// kernels, {64, 256} otherwise; W box {64, 64}).
+// kernels, {64, 256} otherwise; W box {64, 64}; FP8: X8 box {128, 128}, W8t
+// box {128, BN / 2}).
 inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, const CUtensorMap &mw,
-                                  const LmHeadArgs &a, cudaStream_t st, bool pdl)
+                                  const LmHeadArgs &a, cudaStream_t st, bool pdl, bool fp8 = false)
 {
     const int smem = lm_smem_bytes(plan.kind);
-    auto kern = plan.kind == kLmSingle ? lm_head_kernel
-                : plan.kind == kLmPair ? lm_head_pair_kernel
-                                       : lm_head_duo_kernel;
+    auto kern = fp8                    ? lm_head_duo_fp8_kernel
+                : plan.kind == kLmSingle ? lm_head_kernel
+                : plan.kind == kLmPair   ? lm_head_pair_kernel
+                                         : lm_head_duo_kernel;
     return launch_kernel(kern, dim3(plan.grid), dim3(kLmThreads), smem, st, pdl, mx, mw, a);
 }
 

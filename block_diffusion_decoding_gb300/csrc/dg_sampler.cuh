@@ -314,6 +314,39 @@ DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int B
     }
 }
 
+// fold_tile for FP8 operands: the accumulator holds sum_k dec(x8) dec(w8);
+// logit = (acc * rs) * cs[v] with the row's scale rs and the column scales
+// cs (fp32 [V], 16-byte aligned).
+DG_DEVICE void fold_tile_scaled(RowState &st, uint32_t tb, int first, int stride, int BN,
+                                uint32_t vbase, uint32_t V, uint32_t row, const FoldConsts &fc,
+                                bool live, float rs, const float *__restrict__ cs)
+{
+#pragma unroll 1
+    for (int c0 = first; c0 < BN; c0 += stride) {
+        float lg[16];
+        tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
+        const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
+        if (v0 < V) {
+            if (v0 + 16u <= V) {
+                const float4 *c4 = reinterpret_cast<const float4 *>(cs + v0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 c = __ldg(c4 + j);
+                    lg[4 * j + 0] = __fmul_rn(__fmul_rn(lg[4 * j + 0], rs), c.x);
+                    lg[4 * j + 1] = __fmul_rn(__fmul_rn(lg[4 * j + 1], rs), c.y);
+                    lg[4 * j + 2] = __fmul_rn(__fmul_rn(lg[4 * j + 2], rs), c.z);
+                    lg[4 * j + 3] = __fmul_rn(__fmul_rn(lg[4 * j + 3], rs), c.w);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    lg[j] = (v0 + j < V) ? __fmul_rn(__fmul_rn(lg[j], rs), __ldg(cs + v0 + j)) : 0.f;
+            }
+            fold16(st, lg, v0, V, row, fc, live);
+        }
+    }
+}
+
 // Partial states in global memory: structure of arrays, row-major
 // ([M][n_slots]), so the slots of one row are contiguous (the combine reads
 // them with one lane per slot).

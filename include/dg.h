@@ -246,6 +246,52 @@ uint64_t dg_kernel_launches(void);
 /* rejects, DG_ERR_CUDA without a device. */
 int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas);
 
+/* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) LM head.  The pages quote their throughput for an FP8 model     */
+/* ("DiffusionGemma Lab" section 1; "Parallel Denoising From an              */
+/* Autoregressive Checkpoint", section "Finding"); E4M3 is the OCP FP8       */
+/* format (bias 7, no infinities, largest finite 448).  The pages do not fix */
+/* the scaling granularity; this library takes one fp32 scale per canvas row  */
+/* of the hidden states and one per vocabulary column of W.                   */
+/* Quantising a row x[0..n): amax = max |x_j|; amax == 0: codes 0, scale 1;   */
+/* else inv = fp32(448 / amax), scale = fp32(amax / 448) and code_j = the    */
+/* E4M3 value nearest fp32(x_j * inv) (ties to even, saturated at +-448).    */
+/* The row stands for decode(code_j) * scale.                                 */
+/* ------------------------------------------------------------------------ */
+
+/* x [rows, cols] bf16 (device) -> codes [rows, cols] u8 and scale [rows] f32 */
+/* (device, caller-owned).  Any alignment.  Errors: DG_ERR_INVALID_ARG for    */
+/* null pointers or sizes < 1; DG_ERR_CUDA if the launch fails.               */
+int dg_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int cols, uint8_t *codes,
+                          float *scale, void *stream);
+
+/* W [d, V] bf16 (vocabulary contiguous, device) -> w8t [V, d] u8 (the       */
+/* transposed codes, each vocabulary column quantised as one row) and        */
+/* scale [V] f32 (device, caller-owned).  A load-time conversion of the      */
+/* model's weight (3 launches).  Errors as dg_quantize_rows_e4m3.            */
+int dg_quantize_weight_e4m3(const uint16_t *w, int d, int V, uint8_t *w8t, float *scale,
+                            void *stream);
+
+/* dg_denoise_step with the LM head on E4M3 operands: the hidden states are  */
+/* quantised per row inside the step (into the workspace), the weight comes  */
+/* quantised by dg_quantize_weight_e4m3, and                                  */
+/*   logit[r, v] = (sum_k dec(x8[r,k]) dec(w8t[v,k])) * sx[r] * w_scale[v]   */
+/* (fp32 accumulation on the tensor cores, then two fp32 products); the      */
+/* sampler, acceptance and stop test are dg_denoise_step's.  Layouts: hidden */
+/* [B*L, d] bf16; w8t [V, d] u8; w_scale [V] f32; all 16-byte aligned.        */
+/* Supported: d % 128 == 0, 128 <= d <= 16384; V, L, B as dg_denoise_step.   */
+/* Errors as dg_denoise_step.                                                 */
+size_t dg_denoise_step_fp8_workspace(const dg_step_params *p);
+int dg_denoise_step_fp8(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
+                        const dg_step_params *p, const dg_step_io *io, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* The quantisation of the hidden states and the FP8 LM-head kernel of       */
+/* dg_denoise_step_fp8 alone (partial states left in the workspace).         */
+int dg_lm_head_fold_fp8(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
+                        const dg_step_params *p, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
 /* Acceptance, renoise and stop test alone on given entropy/sample/argmax     */
 /* [B*L] (device).  Writes canvas, accepted, n_accepted, stop, mean_entropy   */
 /* and prev_argmax of io; io->entropy/sample/argmax are not used. */

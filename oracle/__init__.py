@@ -274,20 +274,37 @@ def e4m3_table() -> np.ndarray:
     return np.array([e4m3_decode(c) for c in range(256)])
 
 
-def quantize_rows_e4m3(x_bits: np.ndarray):
-    """Per-row E4M3 quantisation of bf16 rows [n, c] -> (codes uint8 [n, c], scale fp32 [n])."""
+def quantize_rows_e4m3(x_bits: np.ndarray, workers: int = 1):
+    """Per-row E4M3 quantisation of bf16 rows [n, c] -> (codes uint8 [n, c], scale fp32 [n]).
+
+    Rows are independent; ``workers`` > 1 runs blocks of rows on that many
+    threads (the C routine runs without the interpreter lock), with identical
+    results."""
     x = np.ascontiguousarray(np.asarray(x_bits, dtype=np.uint16))
     n, c = x.shape
     q = np.zeros((n, c), np.uint8)
     sc = np.zeros(n, np.float32)
-    lib().orc_quantize_rows_e4m3(_ptr(x), n, c, _ptr(q), _ptr(sc))
+    L = lib()
+    L.orc_e4m3_encode(0.0)          # fills the encoder's code table before any thread runs
+
+    def block(r0, r1):
+        L.orc_quantize_rows_e4m3(_ptr(x[r0:r1]), r1 - r0, c, _ptr(q[r0:r1]), _ptr(sc[r0:r1]))
+
+    if workers > 1 and n > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        step = -(-n // (4 * workers))
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(lambda r0: block(r0, min(n, r0 + step)), range(0, n, step)))
+    else:
+        block(0, n)
     return q, sc
 
 
-def quantize_weight_e4m3(w_bits: np.ndarray):
+def quantize_weight_e4m3(w_bits: np.ndarray, workers: int = 1):
     """W [d, V] (bf16 bits) -> (W8t [V, d] codes, scale [V]): each vocabulary
     column quantised as one row."""
-    return quantize_rows_e4m3(np.ascontiguousarray(np.asarray(w_bits, dtype=np.uint16).T))
+    return quantize_rows_e4m3(np.ascontiguousarray(np.asarray(w_bits, dtype=np.uint16).T),
+                              workers=workers)
 
 
 def logits_fp8(x8: np.ndarray, sx: np.ndarray, w8t: np.ndarray, sw: np.ndarray,

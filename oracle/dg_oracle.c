@@ -407,10 +407,16 @@ uint8_t orc_e4m3_encode(float x)
     double a = fabs((double)x);
     if (isnan(x)) return 0x7F;
     if (a > 448.0) a = 448.0;
+    static double table[0x7F];           /* decoded non-negative codes, filled once */
+    static int have_table = 0;
+    if (!have_table) {
+        for (int c = 0; c <= 0x7E; ++c) table[c] = orc_e4m3_decode((uint8_t)c);
+        have_table = 1;
+    }
     uint8_t best = 0;
     double bd = INFINITY;
     for (int c = 0; c <= 0x7E; ++c) {
-        const double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+        const double d = fabs(table[c] - a);
         if (d < bd || (d == bd && (c & 1) == 0)) {
             bd = d;
             best = (uint8_t)c;

@@ -120,3 +120,29 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.dg_lm_head_plan(0, 1024, 16384, None, None, None) == 1
     assert lib.dg_lm_head_plan(256, 1000, 16384, None, None, None) == 2
     assert lib.dg_lm_head_plan(256, 1024, 16380, None, None, None) == 2
+
+
+def test_fp8_entry_points_validate_before_launch(lib):
+    good = 1 << 20
+    p = dg.step_params(1, 256, 1024, 16384, 0.8)
+    io = dg.StepIO(*[_vp(good + 64 * i) for i in range(9)])
+    ws_sz = dg.denoise_step_fp8_workspace(p)
+    # the step's workspace plus the quantised hidden block and its row scales
+    assert ws_sz >= dg.denoise_step_workspace(p) + 256 * 1024 + 256 * 4
+
+    def step(h=good, w8=good, sw=good, p_=p, n=ws_sz, io_=io):
+        return lib.dg_denoise_step_fp8(_vp(h) if h else None, _vp(w8) if w8 else None,
+                                       _vp(sw) if sw else None, ctypes.byref(p_),
+                                       ctypes.byref(io_), _vp(good), n, None)
+
+    assert step(sw=0) == 1                                               # null scales
+    assert step(w8=good + 8) == 3                                        # misaligned codes
+    assert step(n=ws_sz - 1) == 4                                        # workspace too small
+    assert step(p_=dg.step_params(1, 256, 1088, 16384, 0.8), n=1 << 30) == 2   # d % 128 != 0
+    assert step(io_=dg.StepIO(*([None] + [_vp(good)] * 8))) == 1
+    assert lib.dg_lm_head_fold_fp8(_vp(good), None, _vp(good), ctypes.byref(p), _vp(good),
+                                   ws_sz, None) == 1
+    assert dg.denoise_step_fp8_workspace(dg.step_params(1, 256, 1024, 1001, 0.8)) == 0
+    assert lib.dg_quantize_rows_e4m3(None, 4, 4, _vp(good), _vp(good), None) == 1
+    assert lib.dg_quantize_rows_e4m3(_vp(good), 0, 4, _vp(good), _vp(good), None) == 1
+    assert lib.dg_quantize_weight_e4m3(_vp(good), 0, 64, _vp(good), _vp(good), None) == 1
