@@ -131,20 +131,27 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle sample
-def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0):
+def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0, fp8=False):
     """Time the CPU oracle on a bounded sample of one step and scale it to the full step.
 
     Sample: every canvas row of the LM head + sampler against the first v_sample
     vocabulary columns (time scaled by V / v_sample), attention for attn_rows of
     the B*L*Hq query rows (scaled by the row count), the acceptance + stop test on
-    the full canvas.  Returns (seconds per full step, description).
+    the full canvas.  fp8: the LM head on E4M3 operands (the oracle quantises
+    the hidden rows and the sampled W columns, then forms the fp64 logits of the
+    quantised operands).  Returns (seconds per full step, description).
     """
     import oracle
     xb, wb = inputs_host["x"], inputs_host["w"]
     vs = min(v_sample, cfg.V)
     w_s = np.ascontiguousarray(wb[:, :vs])
     t0 = time.perf_counter()
-    lg = oracle.logits(xb, w_s)
+    if fp8:
+        x8, sx = oracle.quantize_rows_e4m3(xb)
+        w8t, sw = oracle.quantize_weight_e4m3(w_s)
+        lg = oracle.logits_fp8(x8, sx, w8t, sw)
+    else:
+        lg = oracle.logits(xb, w_s)
     s = oracle.sampler(lg, cfg.temperature, seed, np.arange(cfg.M), 1)
     t_lm = time.perf_counter() - t0
     rows = np.linspace(0, cfg.B * cfg.L * cfg.Hq - 1, attn_rows).astype(np.int64)
@@ -163,8 +170,10 @@ def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0):
     t_acc = time.perf_counter() - t0
     full = t_lm * (cfg.V / vs) + t_at * (cfg.B * cfg.L * cfg.Hq / len(rows)) + t_acc
     desc = ("oracle (fp64 C + numpy fp64 matmul, 1 thread): all %d canvas rows x %d of %d vocab "
-            "columns (LM head + sampler, scaled x%.0f), %d of %d attention rows (scaled), "
-            "acceptance + stop on the full canvas" % (cfg.M, vs, cfg.V, cfg.V / vs, len(rows),
+            "columns (%sLM head + sampler, scaled x%.0f), %d of %d attention rows (scaled), "
+            "acceptance + stop on the full canvas" % (cfg.M, vs, cfg.V,
+                                                      "E4M3 quantisation + " if fp8 else "",
+                                                      cfg.V / vs, len(rows),
                                                       cfg.B * cfg.L * cfg.Hq))
     return full, desc, dict(t_lm=t_lm, t_attn=t_at, t_accept=t_acc)
 
@@ -207,10 +216,12 @@ def run_reference(args, cfg):
     return 0
 
 
-def _config_json(cfg, l2):
+def _config_json(cfg, l2, lm_dtype="bf16"):
     return {"workload": "%s: single denoising step, B=%d L=%d, attention Hq=%d Hkv=%d D=%d "
-                        "P=%d, LM head d=%d V=%d, T=%.1f b=%.1f" % (
+                        "P=%d, LM head d=%d V=%d%s, T=%.1f b=%.1f" % (
                             cfg.name, cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V,
+                            " (E4M3 operands, per-row / per-column scales)"
+                            if lm_dtype == "fp8" else "",
                             cfg.temperature, cfg.entropy_bound),
             "global_batch": cfg.B, "seq_len": cfg.L, "parallelism": "replicas", "l2": l2}
 
@@ -298,15 +309,36 @@ def run_ours(args, cfg):
     bufs.canvas.copy_(torch.randint(0, V, (M,), device=dev, generator=g, dtype=torch.int32))
     p0 = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 0,
                         seed=rank)
-    sws = dg.workspace(dg.denoise_step_workspace(p0), dev)
+    fp8 = args.lm_dtype == "fp8"
+    if fp8:
+        # load-time conversion of W to E4M3 codes [V, d] + column scales (not timed);
+        # the hidden states are quantised inside every step
+        w8 = torch.empty(V, d, dtype=torch.uint8, device=dev)
+        w_scale = torch.empty(V, dtype=torch.float32, device=dev)
+        dg.quantize_weight_e4m3(w, w8, w_scale)
+        sws = dg.workspace(dg.denoise_step_fp8_workspace(p0), dev)
+    else:
+        sws = dg.workspace(dg.denoise_step_workspace(p0), dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     stream = torch.cuda.current_stream(dev)
+
+    def lm_step(p):
+        if fp8:
+            dg.denoise_step_fp8(x, w8, w_scale, p, bufs, sws)
+        else:
+            dg.denoise_step(x, w, p, bufs, sws)
+
+    def lm_fold():
+        if fp8:
+            dg.lm_head_fold_fp8(x, w8, w_scale, p0, sws)
+        else:
+            dg.lm_head_fold(x, w, p0, sws)
 
     def step(k):
         dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws)
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold,
                            k, seed=rank)
-        dg.denoise_step(x, w, p, bufs, sws)
+        lm_step(p)
 
     def timed(fn, n, first):
         """Per-iteration CUDA-event times (ms) with an L2 flush before each iteration."""
@@ -345,19 +377,24 @@ def run_ours(args, cfg):
         step_ms = float(t.item())
 
     # ---- per-kernel timings (same flush discipline) for the roofline
-    lm_ms = statistics.mean(timed(lambda k: dg.lm_head_fold(x, w, p0, sws), args.steps, 0))
+    lm_ms = statistics.mean(timed(lambda k: lm_fold(), args.steps, 0))
     at_ms = statistics.mean(timed(lambda k: dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale,
                                                            aws), args.steps, 0))
-    lm_bytes = d * V * 2 + M * d * 2
+    # FP8: W codes + column scales, and the bf16 hidden states read by the row quantisation
+    lm_bytes = (d * V + 4 * V if fp8 else d * V * 2) + M * d * 2
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
     lm_flops = 2.0 * M * d * V
+    # E4M3 runs at twice the bf16 rate (nominal dense ratio 4.5 / 2.25 PFLOP/s)
+    lm_peak = bf16_peak * (2.0 if fp8 else 1.0)
     at_flops = 4.0 * B * Hq * L * (P + L) * D
     at_bytes = 2 * (B * L * Hq * D * 2) + 2 * (B * (P + L) * Hkv * D * 2)
     lm_plan = dg.lm_head_plan(M, d, V)
+    if fp8:
+        lm_plan = dict(lm_plan, kernel="lm_head_duo_fp8_kernel")
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
             for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
-    traffic = _traffic_record(srcs, lm_plan["kernel"])
+    traffic = None if fp8 else _traffic_record(srcs, lm_plan["kernel"])
 
     # ---- end to end through the C ABI with host buffers (pinned): per step,
     # one H2D copy of the step's inputs (hidden states, canvas Q/K/V) and one
@@ -399,8 +436,9 @@ def run_ours(args, cfg):
                 "vp": vp.view(torch.int16).cpu().numpy().view(np.uint16),
                 "kc": kc.view(torch.int16).cpu().numpy().view(np.uint16),
                 "vc": vc.view(torch.int16).cpu().numpy().view(np.uint16)}
-        est = [oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64)[0] for _ in range(2)]
-        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64)
+        est = [oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8)[0]
+               for _ in range(2)]
+        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8)
         cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle",
                    sample=desc)
     if world > 1:
@@ -410,14 +448,16 @@ def run_ours(args, cfg):
     value = world * 1e3 / step_ms
     # each kernel's roofline: the slower of its algorithmic bytes at the
     # measured copy bandwidth and its FLOPs at the measured bf16 peak
-    lm_roof_ms = max(lm_bytes / (hbm_peak * 1e9), lm_flops / (bf16_peak * 1e12)) * 1e3
+    lm_roof_ms = max(lm_bytes / (hbm_peak * 1e9), lm_flops / (lm_peak * 1e12)) * 1e3
     at_roof_ms = max(at_bytes / (hbm_peak * 1e9), at_flops / (bf16_peak * 1e12)) * 1e3
-    lm_tensor = lm_flops / (bf16_peak * 1e12) > lm_bytes / (hbm_peak * 1e9)
+    lm_tensor = lm_flops / (lm_peak * 1e12) > lm_bytes / (hbm_peak * 1e9)
     lm_tflops = lm_flops / (lm_ms * 1e-3) / 1e12
     if lm_tensor:
-        roof = dict(bound="tensor", achieved=lm_tflops, peak=bf16_peak, unit="TFLOP/s",
-                    frac=lm_tflops / bf16_peak, traffic=traffic, kernel=lm_plan["kernel"],
-                    peak_source=peak_kind + " (MEASURED_PEAKS.json bf16_tflops, burst)",
+        roof = dict(bound="tensor", achieved=lm_tflops, peak=lm_peak, unit="TFLOP/s",
+                    frac=lm_tflops / lm_peak, traffic=traffic, kernel=lm_plan["kernel"],
+                    peak_source=peak_kind + (" (MEASURED_PEAKS.json bf16_tflops, burst, x2 for "
+                                             "E4M3 by the nominal dense ratio)" if fp8 else
+                                             " (MEASURED_PEAKS.json bf16_tflops, burst)"),
                     algorithmic_flops=lm_flops)
     else:
         roof = dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
@@ -427,8 +467,10 @@ def run_ours(args, cfg):
     line = dict(
         metric="denoise steps/s (256-tok canvas, bs=1)", value=value, unit="steps/s",
         n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=step_ms,
-        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
-        data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step"),
+        higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="e4m3 LM head (fp32 accumulate), bf16 attention" if fp8 else "bf16",
+        data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step",
+                                              lm_dtype=args.lm_dtype),
         canvas_tokens_per_s=value * M,
         roofline=roof,
         kernels={lm_plan["kernel"]: {"ms": lm_ms, "GB_per_s": lm_gbs, "TFLOP_per_s": lm_tflops,
@@ -753,8 +795,16 @@ def run_kernel_only(args, cfg):
             r1 = min(d, r0 + 256)
             w[r0:r1] = (torch.randn(r1 - r0, V, device=dev, generator=g) * cfg.w_std).to(bf)
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 1)
-        ws = dg.workspace(dg.denoise_step_workspace(p), dev)
-        fn = lambda: dg.lm_head_fold(x, w, p, ws)
+        if args.lm_dtype == "fp8":
+            w8 = torch.empty(V, d, dtype=torch.uint8, device=dev)
+            w_scale = torch.empty(V, dtype=torch.float32, device=dev)
+            dg.quantize_weight_e4m3(w, w8, w_scale)
+            del w
+            ws = dg.workspace(dg.denoise_step_fp8_workspace(p), dev)
+            fn = lambda: dg.lm_head_fold_fp8(x, w8, w_scale, p, ws)
+        else:
+            ws = dg.workspace(dg.denoise_step_workspace(p), dev)
+            fn = lambda: dg.lm_head_fold(x, w, p, ws)
     ts = []
     for i in range(args.warmup + args.steps):
         s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -778,6 +828,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(dg_synth.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lm-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="LM-head operands: bf16, or E4M3 codes with per-row / per-column scales")
     ap.add_argument("--kernel", choices=["attention", "lm_head"],
                     help="run one kernel of the step alone (for profilers), not the benchmark")
     args = ap.parse_args()
