@@ -158,11 +158,13 @@ int make_map_u8(CUtensorMap *map, const void *base, int rank, const uint64_t *di
 }
 
 // Workspace layout of one step: header | partials (7 x n_slots x M x 4 B) |
-// counters (B ints).
+// counters (B ints) | row keys (M u32: the Gumbel lower bounds the LM-head
+// units share within a launch).
 struct StepWs {
     WsHeader *hdr;
     Partials part;
     int *counters;
+    uint32_t *rowkey;
 };
 
 size_t step_ws_bytes(int M, int B, int slots)
@@ -170,10 +172,11 @@ size_t step_ws_bytes(int M, int B, int slots)
     size_t b = sizeof(WsHeader);
     b += round_up(static_cast<size_t>(7) * slots * M * 4, 256);
     b += round_up(static_cast<size_t>(B) * 4, 256);
+    b += round_up(static_cast<size_t>(M) * 4, 256);
     return b;
 }
 
-StepWs carve_step_ws(void *ws, int M, int slots)
+StepWs carve_step_ws(void *ws, int M, int B, int slots)
 {
     StepWs w{};
     uint8_t *p = static_cast<uint8_t *>(ws);
@@ -190,6 +193,8 @@ StepWs carve_step_ws(void *ws, int M, int slots)
     w.part.aidx = reinterpret_cast<int *>(f + 6 * n);
     p += round_up(7 * n * 4, 256);
     w.counters = reinterpret_cast<int *>(p);
+    p += round_up(static_cast<size_t>(B) * 4, 256);
+    w.rowkey = reinterpret_cast<uint32_t *>(p);
     return w;
 }
 
@@ -298,6 +303,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.ws = ws.hdr;
         a.counters = ws.counters;
         a.ncounters = p->B;
+        a.rowkey = ws.rowkey;
         DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl, true));
         DG_LAUNCHED();
     } else if (logits == nullptr) {
@@ -335,6 +341,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.ws = ws.hdr;
         a.counters = ws.counters;
         a.ncounters = p->B;
+        a.rowkey = ws.rowkey;
         DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl));
         DG_LAUNCHED();
     } else {
@@ -638,7 +645,7 @@ int fp8_step(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, true);
-    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
+    StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     Fp8Operands f8{};
     f8.x8 = static_cast<uint8_t *>(workspace) + off_x8;
     f8.sx = reinterpret_cast<const float *>(static_cast<uint8_t *>(workspace) + off_sx);
@@ -777,7 +784,7 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
+    StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
@@ -798,7 +805,7 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
+    StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     const StepSource src = step_source(p);
     AcceptArgs acc{};
     return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, nullptr, nullptr, nullptr,
@@ -891,7 +898,7 @@ int dg_sampler_from_logits(const float *logits, const dg_step_params *p, const d
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
     const LmPlan plan = plan_lm_head(M, 64, p->V, di->sms);
-    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
+    StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
     return enqueue_step(nullptr, 0, 1, logits, nullptr, p, plan, ws, src, io->entropy, io->sample,
@@ -948,7 +955,7 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
     size_t off_ctl, off_scr;
     block_ws_layout(p, slot_bound(M, p->V), &off_ctl, &off_scr);
     uint8_t *base = static_cast<uint8_t *>(workspace);
-    StepWs ws = carve_step_ws(workspace, M, plan.part_slots());
+    StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     LoopCtl *ctl = reinterpret_cast<LoopCtl *>(base + off_ctl);
     uint8_t *sp = base + off_scr;
     const size_t m4 = round_up(static_cast<size_t>(M) * 4, 256);

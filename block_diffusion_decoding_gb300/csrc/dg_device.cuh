@@ -20,9 +20,48 @@ namespace dg {
 struct WsHeader {
     int32_t status;          // 0 or a DG_ERR_* code (first error wins)
     int32_t where;           // kernel-specific location of the first error
-    int32_t pad[62];
+    // Row-bound sharing of the LM-head units (see LmHeadArgs::rowkey): the
+    // launch count, the count + 1 once the running launch cleared the row
+    // keys, and the units finished in the running launch (0 between launches)
+    uint32_t lm_epoch;
+    uint32_t lm_ready;
+    uint32_t lm_done;
+    int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+DG_DEVICE uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+DG_DEVICE uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+DG_DEVICE void st_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Order-preserving map of fp32 scores to u32 keys (larger score, larger key;
+// -inf > key 0, which stands for "no bound").
+DG_DEVICE uint32_t score_key(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+DG_DEVICE float key_score(uint32_t k)
+{
+    if (k == 0u) return -INFINITY;
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 DG_DEVICE void report_error(WsHeader *ws, int code, int where)
 {

@@ -66,6 +66,10 @@ struct LmHeadArgs {
     WsHeader *ws;
     int *counters;
     int ncounters;
+    // per-row lower bounds on the best Gumbel score, shared by the units of
+    // one launch ([M] order-preserving keys, 0 = none; all 0 between
+    // launches); null: not shared
+    uint32_t *rowkey;
 };
 
 // LM-head kernel geometry

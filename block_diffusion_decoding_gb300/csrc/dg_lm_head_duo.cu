@@ -99,6 +99,18 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     if (cid == 0 && r == 0 && warp == 2) {
         for (int i = lane; i < a.ncounters; i += 32) a.counters[i] = 0;
     }
+    // Row-bound sharing (a.rowkey): the launch's tag is the epoch in the
+    // workspace header.  Unit 0 clears the row keys, then publishes
+    // ready = epoch + 1; a unit reads or raises keys only after it has seen
+    // that.  The last unit to finish advances the epoch.
+    const bool share = a.rowkey != nullptr;
+    const uint32_t epoch = share ? ld_relaxed_gpu(&a.ws->lm_epoch) : 0u;
+    if (share && cid == 0 && r == 0 && warp == 3) {
+        for (int i = lane; i < a.M; i += 32) a.rowkey[i] = 0u;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(&a.ws->lm_ready, epoch + 1u);
+    }
     const FoldConsts fc = fold_consts(a.src, a.seed);
     const int xstep = a.x_3d ? static_cast<int>(fc.step) : 0;
 
@@ -222,11 +234,20 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                 row_state_init(st);
                 cur_m = m;
             }
+            const int row = m * kRowsPerBlock + r * 128 + rix;
+            const bool live = row < a.M;
+            // the best scores other units have published for this row (read
+            // before the wait for the accumulator, used after it)
+            bool shared_ok = false;
+            uint32_t key = 0u;
+            if (share) {
+                shared_ok = ld_acquire_gpu(&a.ws->lm_ready) == epoch + 1u;
+                if (shared_ok && live) key = ld_relaxed_gpu(a.rowkey + row);
+            }
             const bool ok = mbar_wait_cluster(&acc_full[acc], use & 1u, a.ws, 407);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
-            const int row = m * kRowsPerBlock + r * 128 + rix;
-            const bool live = row < a.M;
+            st.glb = fmaxf(st.glb, key_score(key));
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * a.BN);
             if constexpr (kFp8) {
                 const float rs = live ? __ldg(a.row_scale + row) : 0.f;
@@ -237,6 +258,14 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                 fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, a.BN,
                           static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
                           static_cast<uint32_t>(row), fc, live);
+            }
+            if (shared_ok && live) {
+                // publish this unit's bound when it beats what is known
+                const float lbv = fmaxf(st.gbest, st.apb - 2.0f * kGumbelSlack);
+                if (lbv > st.glb) {
+                    atomicMax(a.rowkey + row, score_key(lbv));
+                    st.glb = lbv;
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -259,6 +288,18 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, 512);
+    }
+    if (share) {
+        // every key access of this unit is done before it is counted
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint32_t prev = atomicAdd(&a.ws->lm_done, 1u);
+            if (prev == gridDim.x - 1u) {
+                a.ws->lm_done = 0u;
+                a.ws->lm_epoch = epoch + 1u;
+            }
+        }
     }
 }
 

@@ -32,6 +32,8 @@ struct RowState {
     int aidx;     // its vocabulary index
     // fold only (not part of the stored partial): best approximate Gumbel
     // score seen, and the column holding it if it is still unevaluated
+    float glb;    // a lower bound on the row's best exact score over the whole
+                  // vocabulary, from other units of the same launch (-inf: none)
     float apb;    // best approximate score (-inf: none yet)
     float kx;     // kept column: logit
     uint32_t kw;  // kept column: Philox word
@@ -47,6 +49,7 @@ DG_DEVICE void row_state_init(RowState &s)
     s.gidx = 0x7FFFFFFF;
     s.amax = -INFINITY;
     s.aidx = 0x7FFFFFFF;
+    s.glb = -INFINITY;
     s.apb = -INFINITY;
     s.kx = 0.f;
     s.kw = 0u;
@@ -98,6 +101,22 @@ static __device__ __noinline__ float exact_gumbel_score(float logit, float invT,
 // improvement: the result is the one of evaluating every column exactly.
 constexpr float kGumbelMaxPlusSlack = 16.75f;
 constexpr float kGumbelSlack = 1.0e-3f;
+
+// Word threshold of stage 1b.  For a Philox word x the fold uses
+// u = ((x >> 9) + 1/2) 2^-23, so 1 - u = ((~x >> 9) + 1/2) 2^-23 exactly.
+// G = -ln(-ln u) <= t holds whenever -ln u >= e^-t, and -ln u >= 1 - u, so
+// every word with (~x >> 9) >= K = ceil(e^-t 2^23) gives G <= t; in terms of
+// x, only words x >= (2^23 - K) << 9 can give G > t.  The caller subtracts
+// kGumbelSlack from t, which covers the error of the hardware exp2 here
+// (relative 2^-22) and the roundings of the exact score many times over.
+// Returns 0 (every word stays) for t = -inf or NaN and for K >= 2^23.
+DG_DEVICE uint32_t gumbel_word_threshold(float t)
+{
+    const float ys = fast_exp2(fmaf(-t, 1.44269504f, 23.0f));   // e^-t 2^23
+    if (!(ys < 8388608.0f)) return 0u;
+    const uint32_t K = static_cast<uint32_t>(ceilf(ys));          // 0 .. 2^23
+    return K == 0u ? 0xFFFFFFFFu : (8388608u - K) << 9;
+}
 
 // Fold 16 consecutive logits lg[0..15] of vocabulary entries v0 .. v0+15
 // (v0 a multiple of 16, the same for every lane of the warp) of canvas row
@@ -167,12 +186,15 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         st.A += as[0];
     }
     // Gumbel-max over the columns that can still win: counter (v >> 2, row,
-    // step, 0), word v & 3.  Stage 1 (logit only) decides whether the warp
-    // draws the noise of this chunk at all.
-    // the exact best is at least max(gbest, apb - slack)
-    const float lim = fmaxf(st.gbest, st.apb - 2.0f * kGumbelSlack) - kGumbelMaxPlusSlack;
+    // step, 0), word v & 3.  lb is a lower bound on the exact best score of
+    // the row: the best exact score found here, the best estimate less twice
+    // its error margin, or the bound other units of the launch published.
+    // Stage 1 (logits only) decides whether the warp draws the noise of this
+    // chunk at all.
+    const float lb = fmaxf(fmaxf(st.gbest, st.apb - 2.0f * kGumbelSlack), st.glb);
     // rounding is monotone, so the chunk's largest scaled logit is cmax * invT
-    if (!__any_sync(0xFFFFFFFFu, cmax * fc.invT > lim)) return;
+    const float cz = cmax * fc.invT;
+    if (!__any_sync(0xFFFFFFFFu, cz > lb - kGumbelMaxPlusSlack)) return;
     float lz[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) lz[j] = x[j] * fc.invT;
@@ -186,6 +208,16 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         w[4 * q + 2] = r.z;
         w[4 * q + 3] = r.w;
     }
+    // Stage 1b (noise words only): a column of this chunk can reach lb only
+    // if its Gumbel value exceeds lb - cz; the columns whose word is below the
+    // threshold of gumbel_word_threshold cannot, and need no logarithm.
+    const uint32_t wthr = gumbel_word_threshold(lb - cz - kGumbelSlack);
+    uint32_t in = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) in |= (w[j] >= wthr ? 1u : 0u) << j;
+    if (!live) in = 0;
+    // no column of the warp can win: stage 2 would change nothing
+    if (!__any_sync(0xFFFFFFFFu, in != 0)) return;
     // Stage 2: approximate scores lz + G~.  A column can end up as the chunk's
     // exact best only if its approximate score is within twice the estimate's
     // error of the chunk's best approximate score, and above the running best.
@@ -200,7 +232,8 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         const float e1 = (u > 0.99f) ? fmaf(om * om, 0.5f + om * (1.0f / 3.0f), om)
                                      : -0.69314718f * fast_log2(u);
         const float g = -0.69314718f * fast_log2(e1);
-        ap[j] = lz[j] + g;   // columns stage 1 ruled out cannot win anyway
+        // columns stage 1 or 1b ruled out score below lb: they cannot be the best
+        ap[j] = ((in >> j) & 1u) ? lz[j] + g : -INFINITY;
         amax = fmaxf(amax, ap[j]);
     }
     // Deferred exact evaluation.  Invariant: the exact best of the columns

@@ -7,6 +7,7 @@ largest magnitude).  Tokens from the fused GEMM path are compared where the
 oracle's margins are above 1e-3.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -210,6 +211,50 @@ def test_denoise_step_edge_shapes(kernel, B, L, d, V, monkeypatch):
     status_ok(ws)
     ref = oracle.step(xb, wb, canvas0, prev, B, L, T, b, seed, k)
     check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+
+
+@pytest.mark.parametrize("kernel", ["duo", "pair"])
+def test_shared_row_bounds_across_launches(kernel, monkeypatch):
+    """The 2-SM LM head lets its units share per-row lower bounds on the best
+    Gumbel score within a launch (to skip noise that cannot win).  Several
+    steps on one workspace, with a status clear between them, must each match
+    the oracle, and a repeated step must reproduce its outputs bit for bit
+    (the shared bounds change which columns are skipped, never the result).
+    Two row blocks, mixed per-row logit scales as in the full-width step."""
+    monkeypatch.setenv("DG_LM_KERNEL", kernel)
+    B, L, d, V = 2, 256, 256, 65536
+    cfg = dg_synth.StepConfig("rb", B=B, L=L, d=d, V=V, w_std=0.06, row_scale=(0.5, 8.0),
+                              seed=31)
+    xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
+    x, w = to_dev(xb), to_dev(wb)
+    rng = np.random.default_rng(7)
+    canvas0 = rng.integers(0, V, B * L).astype(np.int32)
+    prev = rng.integers(0, V, B * L).astype(np.int32)
+    p0 = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=0, seed=3)
+    ws = dg.workspace(dg.denoise_step_workspace(p0), DEV)
+    lg = oracle.logits(xb, wb)
+    first = {}
+    for rep in range(2):
+        for k in (0, 1, 5):
+            T = oracle.temperature(k, 48)
+            p = dg.step_params(B, L, d, V, T, 0.1, 0.005, step=k, seed=3)
+            bufs = dg.StepBuffers(B, L, DEV)
+            bufs.canvas.copy_(torch.from_numpy(canvas0))
+            bufs.prev_argmax.copy_(torch.from_numpy(prev))
+            dg.denoise_step(x, w, p, bufs, ws)
+            torch.cuda.synchronize()
+            status_ok(ws)
+            out = (np_f(bufs.entropy), np_i32(bufs.sample), np_i32(bufs.argmax),
+                   np_i32(bufs.canvas))
+            if rep == 0:
+                ref = oracle.step(xb, wb, canvas0, prev, B, L, T, 0.1, 3, k,
+                                  workers=os.cpu_count() or 1, lg=lg)
+                check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+                first[k] = out
+            else:
+                for a_, b_ in zip(out, first[k]):
+                    assert np.array_equal(a_, b_)
+        dg.read_device_status(ws, clear=True)
 
 
 def test_denoise_step_uniform_and_one_hot_rows():
