@@ -222,8 +222,10 @@ def lm_head_plan(rows: int, d: int, V: int) -> dict:
     kind, bn, ctas = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     rc = _lib().dg_lm_head_plan(rows, d, V, ctypes.byref(kind), ctypes.byref(bn), ctypes.byref(ctas))
     _check(rc, "dg_lm_head_plan")
-    names = ("lm_head_kernel", "lm_head_pair_kernel", "lm_head_duo_kernel")
-    return {"kernel": names[kind.value], "kind": kind.value, "BN": bn.value, "ctas": ctas.value}
+    names = ("lm_head_kernel", "lm_head_pair_kernel", "lm_head_duo_kernel", "lm_head_duo_kernel")
+    # kind 3: the 2-SM kernel with adjacent BN-column schedule tiles fused
+    return {"kernel": names[kind.value], "kind": kind.value, "BN": bn.value, "ctas": ctas.value,
+            "fused": kind.value == 3}
 
 
 # ---------------------------------------------------------------- FP8 LM head

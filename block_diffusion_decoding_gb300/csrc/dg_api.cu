@@ -304,6 +304,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.counters = ws.counters;
         a.ncounters = p->B;
         a.rowkey = ws.rowkey;
+        a.fuse2 = plan.kind == kLmDuoFused ? 1 : 0;
         DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl, true));
         DG_LAUNCHED();
     } else if (logits == nullptr) {
@@ -342,6 +343,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.counters = ws.counters;
         a.ncounters = p->B;
         a.rowkey = ws.rowkey;
+        a.fuse2 = plan.kind == kLmDuoFused ? 1 : 0;
         DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl));
         DG_LAUNCHED();
     } else {

@@ -56,6 +56,8 @@ struct LmHeadArgs {
     int kblocks;        // k blocks of 128 bytes per row: d / 64 (bf16), d / 128 (FP8)
     int nbox_b;         // 64-column TMA boxes per W stage
     int x_3d;           // hidden states carry a step coordinate
+    int fuse2;          // 2-SM UMMA kernel only: two adjacent tiles of a unit's
+                        // range in one row block run as one tile of 2 BN columns
     // FP8 operands (E4M3 codes): logit = acc * row_scale[row] * col_scale[v];
     // both null for bf16 operands
     const float *row_scale;

@@ -3,7 +3,11 @@
 // full-vocabulary softmax the "Parallel Denoising From an Autoregressive
 // Checkpoint" page, section "Finding", names as a per-step cost).
 //
-// A tile is 256 canvas rows x BN (256 or 128) vocabulary columns.  CTA rank
+// A tile is 256 canvas rows x BN (256 or 128) vocabulary columns; with
+// a.fuse2 (BN = 128) each pair of adjacent tiles of a cluster's range that
+// lie in one row block runs as one 256-column tile, so the ranges balance to
+// 128 columns while nearly every tile still has 256 (a range of odd length
+// ends on a 128-column tile, whose epilogue is also the shorter tail).  CTA rank
 // r of the pair streams rows [128 r, 128 r + 128) of the hidden block and
 // columns [r BN/2, (r + 1) BN/2) of the W tile into its own shared memory;
 // the even CTA issues one 256 x BN x 16 UMMA per 16-deep k step that reads
@@ -39,6 +43,17 @@ namespace dg {
 
 namespace {
 
+// Tiles (of a.BN columns) that the tile starting at schedule tile t of a
+// unit's range [t, t1) covers: 2 when a.fuse2 is set and tile t + 1 is in the
+// range and in the same row block, else 1.
+DG_DEVICE int duo_tile_span(const LmHeadArgs &a, int t, int t1)
+{
+    return (a.fuse2 && t + 1 < t1 && (t + 1) % a.ntn != 0) ? 2 : 1;
+}
+
+// TMEM columns between the two accumulator buffers (the widest tile)
+constexpr int kDuoAccCols = 256;
+
 template <bool kFp8>
 DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map_w,
                                 const LmHeadArgs &a)
@@ -62,9 +77,9 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(num_clusters_x());
     const int t0 = tile_begin(cid, a.total, ncl), t1 = tile_begin(cid + 1, a.total, ncl);
-    const int ntiles = t1 - t0;
-    const int half_boxes = a.BN / 128;                           // W boxes this CTA loads
-    const uint32_t stage_tx = static_cast<uint32_t>(kPairABytes + half_boxes * kLmBBoxBytes);
+    // bytes of W one CTA stages per k block: BN / 2 columns (bf16, in boxes of
+    // 64 columns) or BN / 2 rows of 128 codes (FP8, one box), per spanned tile
+    const int w_half_bytes = a.BN * 64;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kDuoStages; ++s) {
@@ -124,8 +139,12 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;
             bool ok = true;
-            for (int t = t0; t < t1 && ok; ++t) {
+            for (int t = t0, span = 1; t < t1 && ok; t += span) {
+                span = duo_tile_span(a, t, t1);
                 const int m = t / a.ntn, n = t % a.ntn;
+                const int bn = span * a.BN;                     // columns of this tile
+                const uint32_t stage_tx =
+                    static_cast<uint32_t>(kPairABytes + span * w_half_bytes);
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.ws, 401)) { ok = false; break; }
                     if (r == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_tx);
@@ -141,13 +160,15 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                     else
                         tma_load_2d_pair(sa, &map_x, fb, kx, m * kRowsPerBlock + r * 128, pol_x);
                     if constexpr (kFp8) {
-                        // W8t rows n BN + r BN/2 .., 128 codes of k block kb
-                        tma_load_2d_pair(sb, &map_w, fb, kb * 128, n * a.BN + r * (a.BN / 2),
-                                         pol_w);
+                        // W8t rows n BN + r bn/2 .., 128 codes of k block kb, in boxes
+                        // of BN/2 rows (K-major: the boxes stack into one operand)
+                        for (int j = 0; j < span; ++j)
+                            tma_load_2d_pair(sb + j * w_half_bytes, &map_w, fb, kb * 128,
+                                             n * a.BN + r * (bn / 2) + j * (a.BN / 2), pol_w);
                     } else {
-                        for (int j = 0; j < half_boxes; ++j)
+                        for (int j = 0; j < bn / 128; ++j)
                             tma_load_2d_pair(sb + j * kLmBBoxBytes, &map_w, fb,
-                                             n * a.BN + r * (a.BN / 2) + j * 64, kb * kLmBK, pol_w);
+                                             n * a.BN + r * (bn / 2) + j * 64, kb * kLmBK, pol_w);
                     }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
@@ -163,7 +184,9 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && r == 0) {
-            const uint32_t idesc = kFp8 ? make_idesc_e4m3(256, a.BN) : make_idesc_bf16(256, a.BN, 1);
+            const uint32_t idesc1 = kFp8 ? make_idesc_e4m3(256, a.BN) : make_idesc_bf16(256, a.BN, 1);
+            const uint32_t idesc2 =
+                kFp8 ? make_idesc_e4m3(256, 2 * a.BN) : make_idesc_bf16(256, 2 * a.BN, 1);
             const uint32_t sa0 = smem_u32(smem);
             const uint64_t adesc0 = make_sdesc_sw128(sa0, 16, 1024);
             // B: K-major 128-byte rows (FP8) or MN-major 64-column blocks (bf16)
@@ -172,12 +195,15 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int i = 0; i < ntiles && ok; ++i) {
+            int i = 0;
+            for (int t = t0, span = 1; t < t1 && ok; t += span, ++i) {
+                span = duo_tile_span(a, t, t1);
+                const uint32_t idesc = span == 2 ? idesc2 : idesc1;
                 const int acc = i & 1;
                 const uint32_t use = static_cast<uint32_t>(i >> 1);
                 if (!mbar_wait_cluster(&acc_empty[acc], (use & 1u) ^ 1u, a.ws, 404)) break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * a.BN);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kDuoAccCols);
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&full[s], ph, a.ws, 405)) { ok = false; break; }
                     tc_fence_after();
@@ -219,8 +245,10 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
         RowState st;
         row_state_init(st);
         int cur_m = -1;
-        for (int i = 0; i < ntiles; ++i) {
-            const int t = t0 + i;
+        int i = 0;
+        for (int t = t0, span = 1; t < t1; t += span, ++i) {
+            span = duo_tile_span(a, t, t1);
+            const int bn = span * a.BN;
             const int m = t / a.ntn, n = t % a.ntn;
             const int acc = i & 1;
             const uint32_t use = static_cast<uint32_t>(i >> 1);
@@ -248,14 +276,14 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             st.glb = fmaxf(st.glb, key_score(key));
-            const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * a.BN);
+            const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * kDuoAccCols);
             if constexpr (kFp8) {
                 const float rs = live ? __ldg(a.row_scale + row) : 0.f;
-                fold_tile_scaled(st, tb, 16 * cg, 16 * kPairColGroups, a.BN,
+                fold_tile_scaled(st, tb, 16 * cg, 16 * kPairColGroups, bn,
                                  static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
                                  static_cast<uint32_t>(row), fc, live, rs, a.col_scale);
             } else {
-                fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, a.BN,
+                fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, bn,
                           static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
                           static_cast<uint32_t>(row), fc, live);
             }

@@ -194,6 +194,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     a.kblocks = p->d / 64;
     a.nbox_b = (BN + 63) / 64;
     a.x_3d = 0;
+    a.fuse2 = plan.kind == kLmDuoFused ? 1 : 0;
     a.part = part;
     a.src = src;
     a.seed = p->seed;

@@ -17,6 +17,10 @@ enum LmKind : int {
     kLmSingle = 0,    // lm_head_kernel: one CTA per tile, 256 rows x BN columns
     kLmPair = 1,      // lm_head_pair_kernel: 2-CTA cluster, W tile multicast
     kLmDuo = 2,       // lm_head_duo_kernel: 2-CTA cluster, 2-SM UMMA
+    kLmDuoFused = 3,  // lm_head_duo_kernel on 128-column schedule tiles, each
+                      // adjacent pair in a cluster's range (same row block)
+                      // run as one 256-column tile: a 256-column kernel whose
+                      // tile count per cluster is balanced to half a tile
 };
 
 struct LmPlan {
@@ -31,11 +35,12 @@ struct LmPlan {
     int grid;         // CTAs launched
     int part_slots() const { return units; }
     bool cluster() const { return kind != kLmSingle; }
+    bool duo() const { return kind == kLmDuo || kind == kLmDuoFused; }
 };
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
-// CTA, plus a per-tile overhead.  DG_LM_KERNEL=single|pair|duo and DG_LM_BN
-// force a choice.  FP8 operands have the 2-SM UMMA kernel only.
+// CTA, plus a per-tile overhead.  DG_LM_KERNEL=single|pair|duo|fused and
+// DG_LM_BN force a choice.  FP8 operands have the 2-SM UMMA kernel only.
 inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
 {
     LmPlan best{};
@@ -46,16 +51,19 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
     const char *env_bn = std::getenv("DG_LM_BN");
     int forced_bn = env_bn ? std::atoi(env_bn) : 0;
     const char *env_k = std::getenv("DG_LM_KERNEL");
-    const int only = fp8    ? kLmDuo
-                     : !env_k ? -1
+    const int only_env = !env_k ? -1
                      : std::strcmp(env_k, "single") == 0 ? kLmSingle
                      : std::strcmp(env_k, "pair") == 0   ? kLmPair
                      : std::strcmp(env_k, "duo") == 0    ? kLmDuo
+                     : std::strcmp(env_k, "fused") == 0  ? kLmDuoFused
                                                          : -1;
+    // a forced kernel FP8 operands do not have is ignored
+    const int only = fp8 && only_env != kLmDuo && only_env != kLmDuoFused ? -1 : only_env;
     long best_cost = -1;
     auto consider = [&](int kind, int bn) {
         if (forced_bn && bn != forced_bn) return;
         if (only >= 0 && kind != only) return;
+        if (fp8 && kind != kLmDuo && kind != kLmDuoFused) return;
         const bool pair = kind != kLmSingle;
         const int ntn = (V + bn - 1) / bn;
         const int total = ntn * best.mblocks;
@@ -67,7 +75,10 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
         // per-tile overhead (the 2-SM UMMA kernel moves a third less shared
         // memory per k block than the multicast one)
         const long over = kind == kLmSingle ? 40 : kind == kLmPair ? 30 : 25;
-        const long cost = per_unit * ((pair ? bn / 2 : bn) + over);
+        // fused: the per-tile overhead is paid once per 256-column tile
+        const long cost = kind == kLmDuoFused
+                              ? per_unit * (bn / 2) + (per_unit + 1) / 2 * over
+                              : per_unit * ((pair ? bn / 2 : bn) + over);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best.kind = kind;
@@ -86,6 +97,7 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
         consider(kLmPair, 128);
         consider(kLmDuo, 256);
         consider(kLmDuo, 128);
+        consider(kLmDuoFused, 128);
     }
     return best;
 }
@@ -128,7 +140,7 @@ inline bool use_pdl(cudaStream_t st)
 
 // Launch the planned LM-head kernel (maps: X box {64, 128} for the cluster
 // kernels, {64, 256} otherwise; W box {64, 64}; FP8: X8 box {128, 128}, W8t
-// box {128, BN / 2}).
+// box {128, BN / 2}).  a.fuse2 must be set for kLmDuoFused.
 inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, const CUtensorMap &mw,
                                   const LmHeadArgs &a, cudaStream_t st, bool pdl, bool fp8 = false)
 {
@@ -136,7 +148,7 @@ inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, con
     auto kern = fp8                    ? lm_head_duo_fp8_kernel
                 : plan.kind == kLmSingle ? lm_head_kernel
                 : plan.kind == kLmPair   ? lm_head_pair_kernel
-                                         : lm_head_duo_kernel;
+                                         : lm_head_duo_kernel;   // kLmDuo, kLmDuoFused
     return launch_kernel(kern, dim3(plan.grid), dim3(kLmThreads), smem, st, pdl, mx, mw, a);
 }
 

@@ -240,8 +240,10 @@ uint64_t dg_kernel_launches(void);
 /* The LM-head launch dg_denoise_step would make on the current device for    */
 /* rows = B*L canvas positions, hidden size d and vocabulary V (no launch).   */
 /* *kind: 0 = single-CTA kernel, 1 = 2-CTA cluster with the W tile multicast */
-/* to both CTAs, 2 = 2-CTA cluster issuing 2-SM UMMAs; *bn: vocabulary        */
-/* columns per tile; *ctas: CTAs launched.  Any output pointer may be NULL.   */
+/* to both CTAs, 2 = 2-CTA cluster issuing 2-SM UMMAs, 3 = the kind-2 kernel */
+/* on a schedule of bn-column tiles whose adjacent pairs run as one tile of  */
+/* 2 bn columns; *bn: vocabulary columns per (schedule) tile; *ctas: CTAs    */
+/* launched.  Any output pointer may be NULL.                                 */
 /* Returns DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED for shapes the step        */
 /* rejects, DG_ERR_CUDA without a device. */
 int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas);

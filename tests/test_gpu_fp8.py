@@ -98,7 +98,10 @@ def _fp8_step(cfg, xb, wb, k, seed, canvas0, prev, workers=1):
                                              (1, 100, 128, 1000, 0.2, 1),      # ragged rows / vocab
                                              (5, 200, 384, 1104, 0.1, 7),      # canvases straddle blocks
                                              (1, 1024, 128, 64, 0.1, 3)])      # largest canvas, tiny V
-def test_fp8_step_matches_oracle(B, L, d, V, w_std, k):
+@pytest.mark.parametrize("kernel", ["duo", "fused"])
+def test_fp8_step_matches_oracle(B, L, d, V, w_std, k, kernel, monkeypatch):
+    """Plain and fused tile schedules of the 2-SM FP8 LM head."""
+    monkeypatch.setenv("DG_LM_KERNEL", kernel)
     cfg = dg_synth.StepConfig("f8", B=B, L=L, d=d, V=V, w_std=w_std, seed=13)
     xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
     rng = np.random.default_rng(B * L + V)
@@ -115,18 +118,28 @@ def test_fp8_step_matches_oracle(B, L, d, V, w_std, k):
     assert np.array_equal(np_f(bufs.entropy), H1)
 
 
-def test_fp8_step_full_width_every_row():
+def test_fp8_step_full_width_every_row(monkeypatch):
     """The full-width LM head (2816 x 262144, per-row logit scale U(0.5, 8)) on
-    FP8 operands, every row against the oracle."""
+    FP8 operands, every row against the oracle: the planned tile schedule,
+    then the plain 256-column one on the same inputs."""
     cfg = dg_synth.CONFIGS["step_full"]
     xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
     rng = np.random.default_rng(3)
     canvas0 = rng.integers(0, cfg.V, cfg.M).astype(np.int32)
     prev = rng.integers(0, cfg.V, cfg.M).astype(np.int32)
-    ref, bufs, _ = _fp8_step(cfg, xb, wb, 4, 21, canvas0, prev, workers=WORKERS)
+    monkeypatch.delenv("DG_LM_KERNEL", raising=False)
+    ref, bufs, (x, w8d, swd, p, ws) = _fp8_step(cfg, xb, wb, 4, 21, canvas0, prev,
+                                                workers=WORKERS)
     decided = check_step_against_oracle(bufs, ref, cfg.B, cfg.L, exact_tokens=False)
     assert np.abs(np_f(bufs.mean_entropy) - ref["mean_entropy"]).max() < H_TOL
     assert decided == 1
+    monkeypatch.setenv("DG_LM_KERNEL", "duo")
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    bufs.prev_argmax.copy_(torch.from_numpy(prev))
+    dg.denoise_step_fp8(x, w8d, swd, p, bufs, ws)
+    torch.cuda.synchronize()
+    status_ok(ws)
+    assert check_step_against_oracle(bufs, ref, cfg.B, cfg.L, exact_tokens=False) == 1
 
 
 def test_fp8_step_constant_rows():

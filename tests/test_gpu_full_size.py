@@ -79,10 +79,11 @@ def _step_case(cfg, k, seed, kernel_env, monkeypatch):
 
 
 def test_full_width_step_every_row(monkeypatch):
-    """2816 x 262144 LM head: the planned kernel (2-SM UMMA pair) and the other
-    two LM-head kernels against the same oracle step."""
+    """2816 x 262144 LM head: the planned kernel (2-SM UMMA pair on fused
+    128-column schedule tiles), the same kernel on plain 256-column tiles and
+    the other two LM-head kernels against the same oracle step."""
     cfg = dg_synth.CONFIGS["step_full"]
-    ref, res = _step_case(cfg, k=3, seed=0, kernel_env=[None, "single", "pair"],
+    ref, res = _step_case(cfg, k=3, seed=0, kernel_env=[None, "duo", "single", "pair"],
                           monkeypatch=monkeypatch)
     assert all(dec == 1 for dec, _ in res)
     # the per-row entropies span confident to uncertain rows
