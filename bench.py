@@ -789,7 +789,12 @@ def run_kernel_only(args, cfg):
         ws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), dev)
         fn = lambda: dg.canvas_attn(q, kp, vp, kc, vc, out, 1.0 / math.sqrt(D), ws)
     else:
-        x = torch.randn(M, d, device=dev, generator=g).to(bf)
+        xf = torch.randn(M, d, device=dev, generator=g)
+        if cfg.row_scale is not None:
+            lo, hi = cfg.row_scale
+            xf *= torch.rand(M, 1, device=dev, generator=g) * (hi - lo) + lo
+        x = xf.to(bf)
+        del xf
         w = torch.empty(d, V, device=dev, dtype=bf)
         for r0 in range(0, d, 256):
             r1 = min(d, r0 + 256)

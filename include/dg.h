@@ -24,7 +24,11 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy stream).
  *     Calls are asynchronous on that stream.  No call allocates device memory
  *     in the hot path: scratch comes from the caller's workspace, sized by the
- *     matching *_workspace() query (which touches no GPU).
+ *     matching *_workspace() query (which touches no GPU).  A workspace is
+ *     zero-filled by the caller before its first use, and again after a
+ *     device-side error was reported in it; between calls the library leaves
+ *     it in a state the next call expects.  Calls that share a workspace are
+ *     ordered on one stream.
  *   - Return value: a dg_status.  It reports host-side validation (checked
  *     before anything is launched) and launch errors.  Kernels that detect a
  *     problem on the device (a bounded wait that ran out, a bounds check)
