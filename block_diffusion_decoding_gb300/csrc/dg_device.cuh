@@ -449,6 +449,15 @@ DG_DEVICE float2 add2(float2 a, float2 b)
     return *reinterpret_cast<const float2 *>(&d);
 }
 
+DG_DEVICE float2 mul2(float2 a, float2 b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const uint64_t *>(&a)), "l"(*reinterpret_cast<const uint64_t *>(&b)));
+    return *reinterpret_cast<const float2 *>(&d);
+}
+
 DG_DEVICE float max3(float a, float b, float c)
 {
     float d;

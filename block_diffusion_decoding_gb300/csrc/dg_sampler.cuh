@@ -131,19 +131,17 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     float cmax = -INFINITY;
     if (live && full) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            x[j] = lg[j];
-            cmax = fmaxf(cmax, x[j]);
-        }
+        for (int j = 0; j < 16; ++j) x[j] = lg[j];
     } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             // ignored entries get a finite sentinel: their exponentials
             // underflow to exactly 0 and no -inf * 0 can appear below
             x[j] = (live && (full || (v0 + j < V))) ? lg[j] : -1.0e30f;
-            cmax = fmaxf(cmax, x[j]);
         }
     }
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) cmax = max3(cmax, x[j], x[j + 1]);
     if (!__any_sync(0xFFFFFFFFu, live)) return;
     // argmax: only a chunk whose maximum beats the running best can move it;
     // the first column holding that maximum wins ties
@@ -165,25 +163,29 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         }
         st.m = mt;
     }
-    float es[16], as[16];
+    // on pairs of columns (packed fp32: the same roundings as one column at
+    // a time); the sums run as a fixed tree, column j with j + 8, then + 4,
+    // + 2, + 1
+    float2 es[8], as[8];
+    const float2 c2v = make_float2(fc.c2, fc.c2), nm = make_float2(-st.m, -st.m);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const float dlt = fmaf(x[j], fc.c2, -st.m);
-        const float e = fast_exp2(dlt);         // 0 for ignored entries
-        es[j] = e;
-        as[j] = e * dlt;
+    for (int q = 0; q < 8; ++q) {
+        const float2 dlt = fma2(make_float2(x[2 * q], x[2 * q + 1]), c2v, nm);
+        const float2 e = make_float2(fast_exp2(dlt.x), fast_exp2(dlt.y));   // 0 for ignored entries
+        es[q] = e;
+        as[q] = mul2(e, dlt);
     }
 #pragma unroll
-    for (int h = 8; h >= 1; h >>= 1) {
+    for (int h = 4; h >= 1; h >>= 1) {
 #pragma unroll
-        for (int j = 0; j < h; ++j) {
-            es[j] += es[j + h];
-            as[j] += as[j + h];
+        for (int q = 0; q < h; ++q) {
+            es[q] = add2(es[q], es[q + h]);
+            as[q] = add2(as[q], as[q + h]);
         }
     }
     if (live) {
-        st.S += es[0];
-        st.A += as[0];
+        st.S += es[0].x + es[0].y;
+        st.A += as[0].x + as[0].y;
     }
     // Gumbel-max over the columns that can still win: counter (v >> 2, row,
     // step, 0), word v & 3.  lb is a lower bound on the exact best score of
@@ -196,8 +198,13 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     const float cz = cmax * fc.invT;
     if (!__any_sync(0xFFFFFFFFu, cz > lb - kGumbelMaxPlusSlack)) return;
     float lz[16];
+    const float2 iv = make_float2(fc.invT, fc.invT);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) lz[j] = x[j] * fc.invT;
+    for (int q = 0; q < 8; ++q) {
+        const float2 z = mul2(make_float2(x[2 * q], x[2 * q + 1]), iv);
+        lz[2 * q] = z.x;
+        lz[2 * q + 1] = z.y;
+    }
     uint32_t w[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
