@@ -230,7 +230,7 @@ def _config_json(cfg, l2, lm_dtype="bf16"):
 def _traffic_record(kernel_sources, kernel):
     """Per-launch DRAM bytes of the LM-head kernel from the committed ncu summary,
     valid only while the kernel sources are unchanged and for the same kernel."""
-    path = os.path.join(ROOT, "profiles", "lm_head_kernel_step_full.md")
+    path = os.path.join(ROOT, "profiles", "lm_head_duo_kernel_step_full.md")
     if not os.path.exists(path):
         return None
     h = hashlib.sha256()
