@@ -375,7 +375,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     c.sample = sample;
     c.argmax = argmax;
     c.counters = ws.counters;
-    DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + 7) / 8, p->B), dim3(256), 0, st,
+    DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + kCombineRows - 1) / kCombineRows, p->B), dim3(kAcceptThreads), 0, st,
                               pdl, c, acc));
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
@@ -917,7 +917,7 @@ int dg_accept_renoise(const float *entropy, const int32_t *sample, const int32_t
     if (!entropy || !sample || !argmax) return DG_ERR_INVALID_ARG;
     if (workspace == nullptr || workspace_bytes < sizeof(WsHeader)) return DG_ERR_WORKSPACE;
     AcceptArgs acc = accept_args(p, io);
-    accept_only_kernel<<<p->B, 256, 0, as_stream(stream)>>>(entropy, sample, argmax, acc);
+    accept_only_kernel<<<p->B, kAcceptThreads, 0, as_stream(stream)>>>(entropy, sample, argmax, acc);
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;

@@ -231,7 +231,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool pdl = use_pdl(s);
     if (launch_lm_head(plan, mx, mw, a, s, pdl) != cudaSuccess) return DG_ERR_CUDA;
-    if (launch_kernel(combine_accept_kernel, dim3((p->L + 7) / 8, p->B), dim3(256), 0, s, pdl, c,
+    if (launch_kernel(combine_accept_kernel, dim3((p->L + kCombineRows - 1) / kCombineRows, p->B), dim3(kAcceptThreads), 0, s, pdl, c,
                       acc) != cudaSuccess)
         return DG_ERR_CUDA;
     return DG_OK;

@@ -76,80 +76,102 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
 }
 
 // ---------------------------------------------------------------- accept (one canvas)
-// Rank of every key among the L keys (H, position) gives the ascending order
-// without a sorting network; the exclusive prefix sums of the sorted
-// entropies (fp64) then count the accepted prefix: they never decrease, so
-// k* = #{j : sum of the first j sorted entropies <= b} (and k* >= 1).
+// Run by one CTA of kAcceptThreads threads (>= L).  The rank of every key
+// (H, position) among the L keys gives the ascending order without a sorting
+// network: each key is counted against up to kRankSplit slices of the keys
+// by separate threads, and the slice counts are summed.  The exclusive
+// prefix sums of the sorted entropies (fp64) never decrease, so k* = #{j :
+// sum of the first j sorted entropies <= b} (and k* >= 1); one warp scans
+// them 32 at a time and stops at the first chunk that passes b.  Position i
+// is accepted iff its rank is below k*.
+constexpr int kRankSplit = 4;
+
 __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float *__restrict__ H,
                               const int32_t *__restrict__ sample,
                               const int32_t *__restrict__ argmax)
 {
     __shared__ uint64_t keys[kMaxCanvas];
-    __shared__ uint64_t sorted[kMaxCanvas];
+    __shared__ float hsorted[kMaxCanvas];
+    __shared__ int prank[kRankSplit * kMaxCanvas];
     __shared__ double wsum[32];
     __shared__ int s_kstar;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
     const int L = a.L;
     const size_t base = static_cast<size_t>(b) * L;
+    const bool own = tid < L;    // this thread's position i = tid (nt >= L)
 
-    // keys (H, position): H >= 0, so its bit pattern orders like the value
-    for (int i = tid; i < L; i += nt) {
-        const float h = __ldcg(H + base + i);
-        keys[i] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(i);
+    // keys (H, position): H >= 0, so its bit pattern orders like the value;
+    // the stop-test operands and the sample are fetched now, with the keys
+    float h = 0.f;
+    int32_t am = 0, pa = 0, smp = 0;
+    if (own) {
+        h = __ldcg(H + base + tid);
+        am = __ldcg(argmax + base + tid);
+        pa = a.prev_argmax[base + tid];
+        smp = __ldcg(sample + base + tid);
+        keys[tid] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(tid);
     }
-    if (tid == 0) s_kstar = 0;
     __syncthreads();
-    for (int i = tid; i < L; i += nt) {
+    // partial ranks: thread t counts key t % L against slice t / L
+    const int nq = max(1, min(kRankSplit, nt / L));
+    if (tid < nq * L) {
+        const int i = tid % L, q = tid / L;
+        const int j0 = q * L / nq, j1 = (q + 1) * L / nq;
         const uint64_t k = keys[i];
-        int rank = 0;
+        int cnt = 0;
 #pragma unroll 8
-        for (int j = 0; j < L; ++j) rank += (keys[j] < k) ? 1 : 0;
-        sorted[rank] = k;
+        for (int j = j0; j < j1; ++j) cnt += (keys[j] < k) ? 1 : 0;
+        prank[q * L + i] = cnt;
     }
-    __syncthreads();
-    // sorted positions [j0, j1) of this thread; block exclusive scan in fp64
-    const int per = (L + nt - 1) / nt;
-    const int j0 = min(L, tid * per), j1 = min(L, j0 + per);
-    auto hval = [&](int j) {
-        return static_cast<double>(__uint_as_float(static_cast<uint32_t>(sorted[j] >> 32)));
-    };
-    double loc = 0.0;
-    for (int j = j0; j < j1; ++j) loc += hval(j);
-    double incl = loc;
+    // fp64 total of the entropies (mean for the stop test), a fixed tree
+    double tot = own ? static_cast<double>(h) : 0.0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const double o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) wsum[wid] = incl;
+    for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, off);
+    if (lane == 0) wsum[wid] = tot;
     __syncthreads();
+    int rank = 0;
+    if (own) {
+        for (int q = 0; q < nq; ++q) rank += prank[q * L + tid];
+        hsorted[rank] = h;
+    }
+    __syncthreads();
+    // k*: warp 0 scans the sorted entropies in chunks of 32 (exclusive sums)
     if (wid == 0) {
-        double w = (lane < nw) ? wsum[lane] : 0.0;
+        double carry = 0.0;
+        int kcount = 0;
+        for (int c0 = 0; c0 < L; c0 += 32) {
+            const int j = c0 + lane;
+            const double hv = (j < L) ? static_cast<double>(hsorted[j]) : 0.0;
+            double incl = hv;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const double o = __shfl_up_sync(0xFFFFFFFFu, w, off);
-            if (lane >= off) w += o;
+            for (int off = 1; off < 32; off <<= 1) {
+                const double o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const double prev = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+            const double excl = carry + (lane == 0 ? 0.0 : prev);
+            kcount += __popc(__ballot_sync(0xFFFFFFFFu, j < L && excl <= static_cast<double>(a.bound)));
+            const double last = __shfl_sync(0xFFFFFFFFu, excl, 31);
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            if (last > static_cast<double>(a.bound)) break;   // the sums only grow
         }
-        if (lane < nw) wsum[lane] = w;      // inclusive warp totals
+        double t = (lane < nw) ? wsum[lane] : 0.0;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+        if (lane == 0) {
+            s_kstar = max(1, kcount);
+            wsum[0] = t;
+        }
     }
     __syncthreads();
-    double run = incl - loc + (wid > 0 ? wsum[wid - 1] : 0.0);
-    int cnt = 0;
-    for (int j = j0; j < j1; ++j) {
-        cnt += (run <= static_cast<double>(a.bound)) ? 1 : 0;
-        run += hval(j);
-    }
-    if (cnt) atomicAdd(&s_kstar, cnt);
-    __syncthreads();
-    const int kstar = max(1, s_kstar);
-    const double total = wsum[nw - 1];
+    const int kstar = s_kstar;
+    const double total = wsum[0];
     const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
-    for (int j = tid; j < L; j += nt) {
-        const int pos = static_cast<int>(sorted[j] & 0xFFFFFFFFu);
-        const size_t r = base + pos;
-        if (j < kstar) {
-            a.canvas[r] = __ldcg(sample + r);
+    if (own) {
+        const size_t r = base + tid;
+        if (rank < kstar) {
+            a.canvas[r] = smp;
             a.accepted[r] = 1;
         } else {
             const uint4 x = philox4x32_10(make_uint4(0u, static_cast<uint32_t>(r),
@@ -160,10 +182,12 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
         }
     }
     // stop test: unchanged argmax and mean entropy below the threshold
-    int same = 1;
-    for (int i = tid; i < L; i += nt) same &= (__ldcg(argmax + base + i) == a.prev_argmax[base + i]);
-    const int all_same = __syncthreads_and(same);
-    for (int i = tid; i < L; i += nt) a.prev_argmax[base + i] = __ldcg(argmax + base + i);
+    const int all_same = __syncthreads_and(own ? (am == pa) : 1);
+    if (own) {
+        a.prev_argmax[base + tid] = am;
+        // freeze the block output: the argmax canvas of the latest live step
+        if (a.ctl != nullptr) a.out_argmax[base + tid] = am;
+    }
     if (tid == 0) {
         const double mean = total / static_cast<double>(L);
         const int stop = (step >= 1 && all_same && mean < static_cast<double>(a.threshold)) ? 1 : 0;
@@ -175,10 +199,6 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
             a.steps_taken[b] = step + 1;
             if (stop || step + 1 >= a.ctl->max_steps) a.done[b] = 1;
         }
-    }
-    if (a.ctl != nullptr) {
-        // freeze the block output: the argmax canvas of the latest live step
-        for (int i = tid; i < L; i += nt) a.out_argmax[base + i] = __ldcg(argmax + base + i);
     }
 }
 
@@ -204,17 +224,17 @@ __device__ void loop_advance(const AcceptArgs &a)
 }
 
 // ---------------------------------------------------------------- combine + accept
-// grid = (ceil(L / 8), B), 256 threads: warp w of CTA (x, b) merges the
-// partial states of canvas row b*L + 8x + w; the last CTA of canvas b runs
-// the acceptance for it.
-__global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, AcceptArgs a)
+// grid = (ceil(L / kCombineRows), B), kAcceptThreads threads: warp w of CTA
+// (x, b) merges the partial states of canvas row b*L + kCombineRows x + w;
+// the last CTA of canvas b runs the acceptance for it.
+__global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineArgs c, AcceptArgs a)
 {
     griddep_wait();
     griddep_launch_dependents();
     const int b = blockIdx.y;
     if (a.ctl != nullptr && __ldcg(a.done + b) != 0) return;   // canvas already stopped
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x * 8 + warp;
+    const int i = blockIdx.x * kCombineRows + warp;
     if (i < a.L) {
         const int r = b * a.L + i;
         const int m = r / kRowsPerBlock;
@@ -224,14 +244,16 @@ __global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, Acce
         RowState st;
         row_state_init(st);
         const size_t base = static_cast<size_t>(r) * c.n_slots;
-        for (int s = u0 + lane; s <= u1; s += 64) {
-            // two slots per lane per pass: all fourteen loads are in flight together
-            RowState p0, p1;
-            partial_load(c.part, base + s, p0);
-            const bool two = s + 32 <= u1;
-            if (two) partial_load(c.part, base + s + 32, p1);
-            row_state_merge(st, p0);
-            if (two) row_state_merge(st, p1);
+        for (int s = u0 + lane; s <= u1; s += 4 * 32) {
+            // four slots per lane per pass, all loads in flight together
+            RowState p[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (s + 32 * k <= u1) partial_load(c.part, base + s + 32 * k, p[k]);
+                else row_state_init(p[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) row_state_merge(st, p[k]);
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
@@ -275,7 +297,7 @@ __global__ void __launch_bounds__(256) combine_accept_kernel(CombineArgs c, Acce
 }
 
 // Acceptance alone on given entropy / sample / argmax (one CTA per canvas).
-__global__ void __launch_bounds__(256) accept_only_kernel(const float *__restrict__ H,
+__global__ void __launch_bounds__(kAcceptThreads) accept_only_kernel(const float *__restrict__ H,
                                                           const int32_t *__restrict__ sample,
                                                           const int32_t *__restrict__ argmax,
                                                           AcceptArgs a)
