@@ -44,6 +44,16 @@ DG_DEVICE uint32_t ld_relaxed_gpu(const uint32_t *p)
     return v;
 }
 
+// Atomic add with acquire-release semantics at GPU scope: the caller's earlier
+// writes are visible to whoever observes the new value, and the writes that
+// preceded the values it observes are visible to the caller afterwards.
+DG_DEVICE int atomic_add_acq_rel_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 DG_DEVICE void st_release_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -603,6 +613,18 @@ DG_DEVICE void tma_load_2d_multicast(void *dst, const CUtensorMap *map, uint64_t
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask),
         "l"(policy)
+        : "memory");
+}
+
+DG_DEVICE void tma_load_3d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
+                                     int z, uint16_t cta_mask, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
+        "h"(cta_mask), "l"(policy)
         : "memory");
 }
 

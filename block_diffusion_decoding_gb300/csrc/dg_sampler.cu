@@ -90,13 +90,13 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
                               const int32_t *__restrict__ sample,
                               const int32_t *__restrict__ argmax)
 {
-    __shared__ uint64_t keys[kMaxCanvas];
+    __shared__ __align__(16) uint64_t keys[kMaxCanvas];
     __shared__ float hsorted[kMaxCanvas];
     __shared__ int prank[kRankSplit * kMaxCanvas];
-    __shared__ double wsum[32];
+    __shared__ double wsum[1];
     __shared__ int s_kstar;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
+    const int lane = tid & 31, wid = tid >> 5;
     const int L = a.L;
     const size_t base = static_cast<size_t>(b) * L;
     const bool own = tid < L;    // this thread's position i = tid (nt >= L)
@@ -113,22 +113,23 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
         keys[tid] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(tid);
     }
     __syncthreads();
-    // partial ranks: thread t counts key t % L against slice t / L
+    // partial ranks: thread t counts key t % L against slice t / L (slices
+    // start on even keys, two keys per 16-byte shared load)
     const int nq = max(1, min(kRankSplit, nt / L));
     if (tid < nq * L) {
         const int i = tid % L, q = tid / L;
-        const int j0 = q * L / nq, j1 = (q + 1) * L / nq;
+        const int j0 = (q * L / nq) & ~1, j1 = (q + 1 == nq) ? L : ((q + 1) * L / nq) & ~1;
         const uint64_t k = keys[i];
         int cnt = 0;
-#pragma unroll 8
-        for (int j = j0; j < j1; ++j) cnt += (keys[j] < k) ? 1 : 0;
+        int j = j0;
+#pragma unroll 4
+        for (; j + 1 < j1; j += 2) {
+            const ulonglong2 kk = *reinterpret_cast<const ulonglong2 *>(&keys[j]);
+            cnt += (kk.x < k ? 1 : 0) + (kk.y < k ? 1 : 0);
+        }
+        if (j < j1) cnt += (keys[j] < k) ? 1 : 0;
         prank[q * L + i] = cnt;
     }
-    // fp64 total of the entropies (mean for the stop test), a fixed tree
-    double tot = own ? static_cast<double>(h) : 0.0;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, off);
-    if (lane == 0) wsum[wid] = tot;
     __syncthreads();
     int rank = 0;
     if (own) {
@@ -156,7 +157,11 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
             carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
             if (last > static_cast<double>(a.bound)) break;   // the sums only grow
         }
-        double t = (lane < nw) ? wsum[lane] : 0.0;
+        // fp64 total of the entropies (mean for the stop test): lane l sums
+        // sorted entries l, l + 32, ... in order, then a fixed butterfly (fp64
+        // is slow here: one warp does it)
+        double t = 0.0;
+        for (int j = lane; j < L; j += 32) t += static_cast<double>(hsorted[j]);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
         if (lane == 0) {
@@ -279,14 +284,13 @@ __global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineA
     __shared__ int s_last;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const int prev = atomicAdd(&c.counters[b], 1);
+        // release this CTA's rows, acquire every other CTA's (acq_rel add)
+        const int prev = atomic_add_acq_rel_gpu(&c.counters[b], 1);
         s_last = (prev == static_cast<int>(gridDim.x) - 1);
         if (s_last) c.counters[b] = 0;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     const int step =
         (a.ctl != nullptr) ? *reinterpret_cast<volatile int32_t *>(&a.ctl->step) : a.step;
     accept_canvas(a, b, step, c.H, c.sample, c.argmax);
