@@ -616,18 +616,6 @@ DG_DEVICE void tma_load_2d_multicast(void *dst, const CUtensorMap *map, uint64_t
         : "memory");
 }
 
-DG_DEVICE void tma_load_3d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
-                                     int z, uint16_t cta_mask, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
-        "h"(cta_mask), "l"(policy)
-        : "memory");
-}
-
 // Instruction descriptor, kind::f16: D fp32, A/B bf16, A K-major,
 // B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int b_mn_major)
