@@ -36,6 +36,13 @@
  *     early; read it with dg_read_device_status().
  *   - Supported shapes are listed per call; anything else returns
  *     DG_ERR_UNSUPPORTED without launching.
+ *   - Kernel choice: the library picks the LM-head and attention kernels and
+ *     their tilings from the shapes and the SM count (dg_lm_head_plan reports
+ *     the LM-head choice).  For testing and tuning, the environment variables
+ *     DG_LM_KERNEL (single | pair | duo | fused), DG_LM_BN (tile width),
+ *     DG_ATTN_KERNEL (single | pair) and DG_ATTN_SPLITS (key splits) force a
+ *     choice; a choice the shapes do not allow is ignored.  Results do not
+ *     depend on the choice beyond floating-point summation order.
  */
 #ifndef DG_H
 #define DG_H
