@@ -9,7 +9,10 @@ namespace dg {
 constexpr int kRowsPerBlock = 256;   // LM-head row block (two 128-row UMMAs)
 constexpr int kMaxCanvas = 1024;     // largest canvas the acceptance kernel sorts
 constexpr int kAcceptThreads = 1024; // threads of the combine / acceptance CTAs (>= kMaxCanvas)
-constexpr int kCombineRows = kAcceptThreads / 32;   // canvas rows merged per combine CTA (a warp each)
+// canvas rows merged per combine CTA, a warp each (the other warps of the
+// CTA only take part in the acceptance): few merging warps per SM keep the
+// merges' issue slots free
+constexpr int kCombineRows = 8;
 
 struct FoldArgs {
     int M, V, BN, ntn, total, n_slots;

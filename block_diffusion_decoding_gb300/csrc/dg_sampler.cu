@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineA
     if (a.ctl != nullptr && __ldcg(a.done + b) != 0) return;   // canvas already stopped
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i = blockIdx.x * kCombineRows + warp;
-    if (i < a.L) {
+    if (warp < kCombineRows && i < a.L) {
         const int r = b * a.L + i;
         const int m = r / kRowsPerBlock;
         // the producer units whose tile ranges meet row block m are contiguous
