@@ -375,7 +375,8 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     c.sample = sample;
     c.argmax = argmax;
     c.counters = ws.counters;
-    DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + kCombineRows - 1) / kCombineRows, p->B), dim3(kAcceptThreads), 0, st,
+    c.rows_per_cta = combine_rows_per_cta(p->B, p->L, plan.sms);
+    DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + c.rows_per_cta - 1) / c.rows_per_cta, p->B), dim3(kAcceptThreads), 0, st,
                               pdl, c, acc));
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());

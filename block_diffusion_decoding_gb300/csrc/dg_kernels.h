@@ -11,8 +11,14 @@ constexpr int kMaxCanvas = 1024;     // largest canvas the acceptance kernel sor
 constexpr int kAcceptThreads = 1024; // threads of the combine / acceptance CTAs (>= kMaxCanvas)
 // canvas rows merged per combine CTA, a warp each (the other warps of the
 // CTA only take part in the acceptance): few merging warps per SM keep the
-// merges' issue slots free
-constexpr int kCombineRows = 8;
+// merges' issue slots free, so a CTA merges kCombineRowsMin rows unless the
+// B canvases then need more CTAs than the GPU has SMs
+constexpr int kCombineRowsMin = 8;
+inline int combine_rows_per_cta(int B, int L, int sms)
+{
+    const long need = (static_cast<long>(B) * L + sms - 1) / sms;
+    return static_cast<int>(need < kCombineRowsMin ? kCombineRowsMin : need > 32 ? 32 : need);
+}
 
 struct FoldArgs {
     int M, V, BN, ntn, total, n_slots;
@@ -30,6 +36,7 @@ struct CombineArgs {
     int32_t *sample;
     int32_t *argmax;
     int *counters;      // [B] last-CTA counters, zeroed by the producer kernel
+    int rows_per_cta;   // canvas rows merged per combine CTA (<= 32)
 };
 
 struct AcceptArgs {

@@ -212,6 +212,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     c.sample = io->sample;
     c.argmax = io->argmax;
     c.counters = counters;
+    c.rows_per_cta = combine_rows_per_cta(p->B, p->L, plan.sms);
 
     AcceptArgs acc{};
     acc.B = p->B;
@@ -231,7 +232,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool pdl = use_pdl(s);
     if (launch_lm_head(plan, mx, mw, a, s, pdl) != cudaSuccess) return DG_ERR_CUDA;
-    if (launch_kernel(combine_accept_kernel, dim3((p->L + kCombineRows - 1) / kCombineRows, p->B), dim3(kAcceptThreads), 0, s, pdl, c,
+    if (launch_kernel(combine_accept_kernel, dim3((p->L + c.rows_per_cta - 1) / c.rows_per_cta, p->B), dim3(kAcceptThreads), 0, s, pdl, c,
                       acc) != cudaSuccess)
         return DG_ERR_CUDA;
     return DG_OK;

@@ -33,6 +33,7 @@ struct LmPlan {
     int units;        // CTAs (single) or clusters (pair): the tile schedule's
                       // slots, one partial state per (row, unit)
     int grid;         // CTAs launched
+    int sms;          // SMs of the device the plan was made for
     int part_slots() const { return units; }
     bool cluster() const { return kind != kLmSingle; }
     bool duo() const { return kind == kLmDuo || kind == kLmDuoFused; }
@@ -48,6 +49,7 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
     best.V = V;
     best.d = d;
     best.mblocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
+    best.sms = sms;
     const char *env_bn = std::getenv("DG_LM_BN");
     int forced_bn = env_bn ? std::atoi(env_bn) : 0;
     const char *env_k = std::getenv("DG_LM_KERNEL");

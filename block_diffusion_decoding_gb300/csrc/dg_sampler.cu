@@ -229,9 +229,9 @@ __device__ void loop_advance(const AcceptArgs &a)
 }
 
 // ---------------------------------------------------------------- combine + accept
-// grid = (ceil(L / kCombineRows), B), kAcceptThreads threads: warp w of CTA
-// (x, b) merges the partial states of canvas row b*L + kCombineRows x + w;
-// the last CTA of canvas b runs the acceptance for it.
+// grid = (ceil(L / R), B) with R = c.rows_per_cta, kAcceptThreads threads:
+// warp w < R of CTA (x, b) merges the partial states of canvas row
+// b*L + R x + w; the last CTA of canvas b runs the acceptance for it.
 __global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineArgs c, AcceptArgs a)
 {
     griddep_wait();
@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineA
     const int b = blockIdx.y;
     if (a.ctl != nullptr && __ldcg(a.done + b) != 0) return;   // canvas already stopped
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x * kCombineRows + warp;
-    if (warp < kCombineRows && i < a.L) {
+    const int i = blockIdx.x * c.rows_per_cta + warp;
+    if (warp < c.rows_per_cta && i < a.L) {
         const int r = b * a.L + i;
         const int m = r / kRowsPerBlock;
         // the producer units whose tile ranges meet row block m are contiguous
