@@ -420,7 +420,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // Merge the key splits: one warp per query row, lanes over the head dim.
 // Split z left its row normalised by its own sum l_z, with its reference max
-// m_z (base 2); the row is sum_z 2^(m_z - M) l_z O_z / sum_z 2^(m_z - M) l_z.
+// m_z (base 2); the row is sum_z 2^(m_z - M) l_z O_z / sum_z 2^(m_z - M) l_z,
+// merged online four splits at a time (all their loads in flight together;
+// the running sums are rescaled when a later split raises the maximum).
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
 {
     griddep_wait();
@@ -430,33 +432,54 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
     const int lane = threadIdx.x & 31;
     if (row >= nrows) return;
     const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml);
-    float mx = -INFINITY;
-    for (int z = 0; z < a.nsplit; ++z) mx = fmaxf(mx, ml[z * nrows + row].x);
-    float den = 0.f;
+    const int per = a.D / 32;   // 4 or 8 consecutive dims per lane
+    float M = -INFINITY, den = 0.f;
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    const int per = a.D / 32;   // 4 or 8 consecutive dims per lane
-    for (int z = 0; z < a.nsplit; ++z) {
-        const float2 v = ml[z * nrows + row];
-        // a split with no visible key for this row has l = 0 (and a zero row)
-        const float wz = (v.y > 0.f) ? fast_exp2(v.x - mx) * v.y : 0.f;
-        den += wz;
-        const uint16_t *po = a.part_o + (z * nrows + row) * a.D + lane * per;
-        uint32_t pw[4];
-        if (per == 8) {
-            const uint4 q4 = *reinterpret_cast<const uint4 *>(po);
-            pw[0] = q4.x; pw[1] = q4.y; pw[2] = q4.z; pw[3] = q4.w;
-        } else {
-            const uint2 q2 = *reinterpret_cast<const uint2 *>(po);
-            pw[0] = q2.x; pw[1] = q2.y; pw[2] = 0u; pw[3] = 0u;
+    for (int z0 = 0; z0 < a.nsplit; z0 += 4) {
+        float2 v[4];
+        uint32_t pw[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int z = z0 + k;
+            if (z < a.nsplit) {
+                v[k] = ml[z * nrows + row];
+                const uint16_t *po = a.part_o + (z * nrows + row) * a.D + lane * per;
+                if (per == 8) {
+                    const uint4 q4 = *reinterpret_cast<const uint4 *>(po);
+                    pw[k][0] = q4.x; pw[k][1] = q4.y; pw[k][2] = q4.z; pw[k][3] = q4.w;
+                } else {
+                    const uint2 q2 = *reinterpret_cast<const uint2 *>(po);
+                    pw[k][0] = q2.x; pw[k][1] = q2.y; pw[k][2] = 0u; pw[k][3] = 0u;
+                }
+            } else {
+                v[k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pw[k][e] = 0u;
+            }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (2 * e < per) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[e]));
-                acc[2 * e] = fmaf(wz, f.x, acc[2 * e]);
-                acc[2 * e + 1] = fmaf(wz, f.y, acc[2 * e + 1]);
+        for (int k = 0; k < 4; ++k) {
+            // a split with no visible key for this row has l = 0 (and a zero row)
+            if (!(v[k].y > 0.f)) continue;
+            if (v[k].x > M) {
+                const float f = fast_exp2(M - v[k].x);   // 0 while M = -inf
+                den *= f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] *= f;
+                M = v[k].x;
+            }
+            const float wz = fast_exp2(v[k].x - M) * v[k].y;
+            den += wz;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (2 * e < per) {
+                    const float2 f2 =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pw[k][e]));
+                    acc[2 * e] = fmaf(wz, f2.x, acc[2 * e]);
+                    acc[2 * e + 1] = fmaf(wz, f2.y, acc[2 * e + 1]);
+                }
             }
         }
     }
