@@ -361,6 +361,7 @@ DG_DEVICE void fold_tile_scaled(RowState &st, uint32_t tb, int first, int stride
                                 uint32_t vbase, uint32_t V, uint32_t row, const FoldConsts &fc,
                                 bool live, float rs, const float *__restrict__ cs)
 {
+    const float2 rs2 = make_float2(rs, rs);
 #pragma unroll 1
     for (int c0 = first; c0 < BN; c0 += stride) {
         float lg[16];
@@ -368,14 +369,19 @@ DG_DEVICE void fold_tile_scaled(RowState &st, uint32_t tb, int first, int stride
         const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
         if (v0 < V) {
             if (v0 + 16u <= V) {
+                // (acc * rs) * cs on column pairs, the same roundings as one at a time
                 const float4 *c4 = reinterpret_cast<const float4 *>(cs + v0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float4 c = __ldg(c4 + j);
-                    lg[4 * j + 0] = __fmul_rn(__fmul_rn(lg[4 * j + 0], rs), c.x);
-                    lg[4 * j + 1] = __fmul_rn(__fmul_rn(lg[4 * j + 1], rs), c.y);
-                    lg[4 * j + 2] = __fmul_rn(__fmul_rn(lg[4 * j + 2], rs), c.z);
-                    lg[4 * j + 3] = __fmul_rn(__fmul_rn(lg[4 * j + 3], rs), c.w);
+                    const float2 p0 = mul2(mul2(make_float2(lg[4 * j], lg[4 * j + 1]), rs2),
+                                           make_float2(c.x, c.y));
+                    const float2 p1 = mul2(mul2(make_float2(lg[4 * j + 2], lg[4 * j + 3]), rs2),
+                                           make_float2(c.z, c.w));
+                    lg[4 * j + 0] = p0.x;
+                    lg[4 * j + 1] = p0.y;
+                    lg[4 * j + 2] = p1.x;
+                    lg[4 * j + 3] = p1.y;
                 }
             } else {
 #pragma unroll
