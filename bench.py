@@ -57,6 +57,24 @@ def _dist():
     return ws, rank, local
 
 
+def _reduce_max(value, device):
+    """The largest of `value` over the ranks of the initialised process group
+    (the slowest replica's time), or `value` itself without one."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _replica_value(world, ms):
+    """Whole-job rate of `world` independent replicas whose slowest rank took
+    `ms` per unit (steps/s, appends/s)."""
+    return world * 1e3 / ms
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling during the timed region."""
@@ -371,10 +389,7 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     step_ms = sum(ts) / len(ts)
     status = dg.read_device_status(sws) | dg.read_device_status(aws)
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = _reduce_max(step_ms, dev)
 
     # ---- per-kernel timings (same flush discipline) for the roofline
     lm_ms = statistics.mean(timed(lambda k: lm_fold(), args.steps, 0))
@@ -421,10 +436,7 @@ def run_ours(args, cfg):
         e2e_step(args.warmup + i)
         e2e_times.append(time.perf_counter() - t0)
     e2e_ms = 1e3 * sum(e2e_times) / len(e2e_times)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _reduce_max(e2e_ms, dev)
 
     # ---- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
@@ -445,7 +457,7 @@ def run_ours(args, cfg):
         tdist.destroy_process_group()
     if rank != 0:
         return 0
-    value = world * 1e3 / step_ms
+    value = _replica_value(world, step_ms)
     # each kernel's roofline: the slower of its algorithmic bytes at the
     # measured copy bandwidth and its FLOPs at the measured bf16 peak
     lm_roof_ms = max(lm_bytes / (hbm_peak * 1e9), lm_flops / (lm_peak * 1e12)) * 1e3
@@ -482,7 +494,7 @@ def run_ours(args, cfg):
         step_roofline_ms=lm_roof_ms + at_roof_ms,
         step_frac_of_roofline=(lm_roof_ms + at_roof_ms) / step_ms,
         cpu_baseline=cpu,
-        e2e=dict(value=world * 1e3 / e2e_ms, unit="steps/s", h2d_bytes_per_step=h2d,
+        e2e=dict(value=_replica_value(world, e2e_ms), unit="steps/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h),
         clocks=clk.summary(), gpu_launches=launches, device_status=status)
     print(json.dumps(line), flush=True)
@@ -568,10 +580,7 @@ def run_block(args, cfg):
     steps = int(bufs.steps_taken.max().item())
     hist = bufs.n_accepted_hist.view(N, B)[:steps].float()
     block_ms = sum(ts) / len(ts)
-    if world > 1:
-        tt = torch.tensor([block_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        block_ms = float(tt.item())
+    block_ms = _reduce_max(block_ms, dev)
     step_ms = block_ms / steps
 
     # flat logits (hidden = 0): exactly one commit per step, 48 steps
@@ -624,7 +633,7 @@ def run_block(args, cfg):
         tdist.destroy_process_group()
     if rank != 0:
         return 0
-    value = world * 1e3 / step_ms
+    value = _replica_value(world, step_ms)
     line = dict(
         metric="denoise steps/s (256-tok canvas, bs=1)", value=value, unit="steps/s",
         n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=step_ms,
@@ -712,10 +721,8 @@ def run_encoder(args, cfg):
         torch.cuda.synchronize(dev)
         clk.mark(t_start, time.perf_counter())
     ms = sum(a.elapsed_time(b_) for a, b_ in ts) / len(ts)
+    ms = _reduce_max(ms, dev)
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        ms = float(tt.item())
         tdist.destroy_process_group()
     status = dg.read_device_status(ws)
     if rank != 0:
@@ -726,7 +733,7 @@ def run_encoder(args, cfg):
     roof_ms = max(flops / (bf16_peak * 1e12), nbytes / (hbm_peak * 1e9)) * 1e3
     tflops = flops / (ms * 1e-3) / 1e12
     line = dict(
-        metric="encoder cache appends/s (256-token block)", value=world * 1e3 / ms,
+        metric="encoder cache appends/s (256-token block)", value=_replica_value(world, ms),
         unit="appends/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=ms,
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
         config={"workload": "%s: encoder cache append, B=%d block L=%d, cache P=%d, Hq=%d Hkv=%d "
