@@ -100,7 +100,7 @@ def _lib():
             "dg_accept_renoise": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
             "dg_lm_head_fold": ([vp, vp, sp, vp, sz, vp], i32),
             "dg_kernel_launches": ([], u64),
-            "dg_lm_head_plan": ([i32, i32, i32, ip, ip, ip], i32),
+            "dg_lm_head_plan": ([i32, i32, i32, ip, ip, ip, ip], i32),
             "dg_gumbel_fill": ([u64, u32, u32, u32, i32, vp, vp], i32),
             "dg_logf_eval": ([vp, vp, i32, vp], i32),
             "dg_quantize_rows_e4m3": ([vp, ctypes.c_int64, i32, vp, vp, vp], i32),
@@ -219,13 +219,18 @@ def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):
 
 def lm_head_plan(rows: int, d: int, V: int) -> dict:
     """The LM-head launch the step would make on the current device."""
-    kind, bn, ctas = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    rc = _lib().dg_lm_head_plan(rows, d, V, ctypes.byref(kind), ctypes.byref(bn), ctypes.byref(ctas))
+    kind, bn, ctas, epi = (ctypes.c_int(0) for _ in range(4))
+    rc = _lib().dg_lm_head_plan(rows, d, V, ctypes.byref(kind), ctypes.byref(bn),
+                                ctypes.byref(ctas), ctypes.byref(epi))
     _check(rc, "dg_lm_head_plan")
-    names = ("lm_head_kernel", "lm_head_pair_kernel", "lm_head_duo_kernel", "lm_head_duo_kernel")
-    # kind 3: the 2-SM kernel with adjacent BN-column schedule tiles fused
-    return {"kernel": names[kind.value], "kind": kind.value, "BN": bn.value, "ctas": ctas.value,
-            "fused": kind.value == 3}
+    # kinds 2 and 3: the 2-SM kernel (3: adjacent BN-column schedule tiles
+    # fused), with 8 epilogue warps or, in lm_head_duo_wide_kernel, 16
+    if kind.value >= 2:
+        name = "lm_head_duo_wide_kernel" if epi.value == 16 else "lm_head_duo_kernel"
+    else:
+        name = ("lm_head_kernel", "lm_head_pair_kernel")[kind.value]
+    return {"kernel": name, "kind": kind.value, "BN": bn.value, "ctas": ctas.value,
+            "fused": kind.value == 3, "epilogue_warps": epi.value}
 
 
 # ---------------------------------------------------------------- FP8 LM head

@@ -77,6 +77,9 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_wide_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDuoSmemBytes));
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_fp8_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
@@ -865,7 +868,7 @@ int dg_lm_head_fold_fp8(const uint16_t *hidden, const uint8_t *w8t, const float 
     return fp8_step(hidden, w8t, w_scale, p, nullptr, workspace, workspace_bytes, stream, true);
 }
 
-int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas)
+int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas, int *epilogue_warps)
 {
     if (rows < 1 || d < 1 || V < 1) return DG_ERR_INVALID_ARG;
     if (rows > (1 << 20) || V % 8 != 0 || V < 64) return DG_ERR_UNSUPPORTED;
@@ -877,6 +880,7 @@ int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas)
     if (kind) *kind = plan.kind;
     if (bn) *bn = plan.BN;
     if (ctas) *ctas = plan.grid;
+    if (epilogue_warps) *epilogue_warps = plan.epi_warps;
     return DG_OK;
 }
 

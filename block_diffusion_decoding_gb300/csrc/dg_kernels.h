@@ -118,10 +118,28 @@ __global__ void lm_head_pair_kernel(const __grid_constant__ CUtensorMap map_x,
 // own 128 rows of X and 128 of the 256 W columns of a tile; the even CTA
 // issues 256 x 256 x 16 UMMAs over both CTAs' shared memory.
 constexpr int kDuoStages = 6;
+// Epilogue of the 2-SM kernel: 4 x CG warps (CG column groups per TMEM lane
+// quadrant).  With one 256-row block every tile brings new W columns from
+// HBM, the stream sets the tile rate and the fold hides under it: 8 warps
+// (CG = 2) suffice and leave the producer and MMA warps more issue slots.
+// With several row blocks the W tiles come from L2, the tiles arrive at the
+// MMA rate and the fold's latency shows: 16 warps (CG = 4).  FP8 tiles carry
+// half the bytes and take 16 too.
+constexpr int kDuoCGNarrow = 2;
+constexpr int kDuoCGWide = 4;
+template <int kCG>
+struct DuoEpilogue {
+    static constexpr int CG = kCG;
+    static constexpr int Warps = 4 * kCG;
+    static constexpr int Threads = 128 + 32 * Warps;
+};
 constexpr int kDuoStageBytes = kPairABytes + 2 * kLmBBoxBytes;      // 32 KB
 constexpr int kDuoSmemBytes = kDuoStages * kDuoStageBytes + 1024 + 256 + kPairMergeBytes;
 __global__ void lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
                                    const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+// the same kernel with 16 epilogue warps (several row blocks)
+__global__ void lm_head_duo_wide_kernel(const __grid_constant__ CUtensorMap map_x,
+                                        const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 // FP8 (E4M3) operands of the 2-SM kernel: X8 [M, d] and W8t [V, d] (both
 // K-major, 128-byte k blocks = 128 codes); same tiles, 256 x 256 x 32 UMMAs.
 __global__ void lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,

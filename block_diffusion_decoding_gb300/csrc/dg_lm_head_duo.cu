@@ -26,10 +26,12 @@
 //   warp 1      TMEM allocator (both CTAs, collectively); UMMA issuer (even
 //               CTA); the accumulator is free once the epilogues of both
 //               CTAs have read it (the odd CTA's warps arrive remotely);
-//   warps 4-19  epilogue, as in dg_lm_head_pair.cu: warp w reads TMEM lanes
-//               32 (w % 4) .. +31, every 4th 16-column chunk starting at
-//               chunk (w - 4) / 4; the column groups merge in shared memory
-//               and one partial state per (row, cluster) is stored.
+//   warps 4..   epilogue (4 x CG warps: CG = 2 in lm_head_duo_kernel, 4 in
+//               lm_head_duo_wide_kernel and the FP8 instance): warp w
+//               reads TMEM lanes 32 (w % 4) .. +31, every CG-th 16-column
+//               chunk starting at chunk (w - 4) / 4; the column groups merge
+//               in shared memory and one partial state per (row, cluster)
+//               is stored.
 //
 // The FP8 instance (lm_head_duo_fp8_kernel) takes E4M3 codes of the hidden
 // block X8 [M, d] and of the transposed weight W8t [V, d], both K-major: a
@@ -54,7 +56,7 @@ DG_DEVICE int duo_tile_span(const LmHeadArgs &a, int t, int t1)
 // TMEM columns between the two accumulator buffers (the widest tile)
 constexpr int kDuoAccCols = 256;
 
-template <bool kFp8>
+template <bool kFp8, int kCG>
 DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map_w,
                                 const LmHeadArgs &a)
 {
@@ -69,8 +71,10 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     uint64_t *mrg_ready = mma_done + 1;
     uint64_t *mrg_done = mrg_ready + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mrg_done + 1);
+    constexpr int CG = DuoEpilogue<kCG>::CG;            // epilogue column groups
+    constexpr int EpiWarps = DuoEpilogue<kCG>::Warps;
     const GroupMerge gm{reinterpret_cast<float *>(smem + kDuoStages * kDuoStageBytes + 256),
-                        mrg_ready, mrg_done, kPairColGroups, 128};
+                        mrg_ready, mrg_done, CG, 128};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = static_cast<int>(cluster_ctarank());          // row / column half
@@ -88,11 +92,11 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&acc_full[s], 1);
-            mbar_init(&acc_empty[s], 2 * kLmEpiWarps);   // used in the even CTA only
+            mbar_init(&acc_empty[s], 2 * EpiWarps);   // used in the even CTA only
         }
         mbar_init(mma_done, 1);
-        mbar_init(mrg_ready, kLmEpiWarps - kLmEpiWarps / kPairColGroups);
-        mbar_init(mrg_done, kLmEpiWarps / kPairColGroups);
+        mbar_init(mrg_ready, EpiWarps - EpiWarps / CG);
+        mbar_init(mrg_done, EpiWarps / CG);
         fence_barrier_init();
         tma_prefetch_desc(&map_x);
         tma_prefetch_desc(&map_w);
@@ -279,11 +283,11 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * kDuoAccCols);
             if constexpr (kFp8) {
                 const float rs = live ? __ldg(a.row_scale + row) : 0.f;
-                fold_tile_scaled(st, tb, 16 * cg, 16 * kPairColGroups, bn,
+                fold_tile_scaled(st, tb, 16 * cg, 16 * CG, bn,
                                  static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
                                  static_cast<uint32_t>(row), fc, live, rs, a.col_scale);
             } else {
-                fold_tile(st, tb, 16 * cg, 16 * kPairColGroups, bn,
+                fold_tile(st, tb, 16 * cg, 16 * CG, bn,
                           static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
                           static_cast<uint32_t>(row), fc, live);
             }
@@ -333,18 +337,25 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
 
 }  // namespace
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGNarrow>::Threads, 1)
     lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
                        const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
 {
-    lm_head_duo_body<false>(map_x, map_w, a);
+    lm_head_duo_body<false, kDuoCGNarrow>(map_x, map_w, a);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWide>::Threads, 1)
+    lm_head_duo_wide_kernel(const __grid_constant__ CUtensorMap map_x,
+                            const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+{
+    lm_head_duo_body<false, kDuoCGWide>(map_x, map_w, a);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWide>::Threads, 1)
     lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,
                            const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
 {
-    lm_head_duo_body<true>(map_x, map_w, a);
+    lm_head_duo_body<true, kDuoCGWide>(map_x, map_w, a);
 }
 
 }  // namespace dg

@@ -83,6 +83,9 @@ int na_setup(NoAllocDevice **out)
                                  kPairSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(lm_head_duo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kDuoSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(lm_head_duo_wide_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kDuoSmemBytes) != cudaSuccess ||
             cudaMemset(ptr, 0, sizeof(WsHeader)) != cudaSuccess) {
             (void)cudaGetLastError();
             return DG_ERR_CUDA;

@@ -34,14 +34,17 @@ struct LmPlan {
                       // slots, one partial state per (row, unit)
     int grid;         // CTAs launched
     int sms;          // SMs of the device the plan was made for
+    int epi_warps;    // epilogue warps of the 2-SM kernel (8 or 16; 0 otherwise)
     int part_slots() const { return units; }
     bool cluster() const { return kind != kLmSingle; }
     bool duo() const { return kind == kLmDuo || kind == kLmDuoFused; }
 };
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
-// CTA, plus a per-tile overhead.  DG_LM_KERNEL=single|pair|duo|fused and
-// DG_LM_BN force a choice.  FP8 operands have the 2-SM UMMA kernel only.
+// CTA, plus a per-tile overhead; the 2-SM kernel runs 8 epilogue warps on a
+// single 256-row block of bf16 operands, else 16.  DG_LM_KERNEL=single|pair|
+// duo|fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
+// have the 2-SM UMMA kernel only.
 inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
 {
     LmPlan best{};
@@ -101,6 +104,14 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
         consider(kLmDuo, 128);
         consider(kLmDuoFused, 128);
     }
+    if (best.duo()) {
+        const char *env_e = std::getenv("DG_LM_EPI");
+        const int forced_e = env_e ? std::atoi(env_e) : 0;
+        best.epi_warps = fp8 ? 4 * kDuoCGWide
+                         : forced_e == 8 || forced_e == 16 ? forced_e
+                         : best.mblocks == 1             ? 4 * kDuoCGNarrow
+                                                         : 4 * kDuoCGWide;
+    }
     return best;
 }
 
@@ -147,11 +158,16 @@ inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, con
                                   const LmHeadArgs &a, cudaStream_t st, bool pdl, bool fp8 = false)
 {
     const int smem = lm_smem_bytes(plan.kind);
+    const bool wide = plan.epi_warps == 4 * kDuoCGWide;
     auto kern = fp8                    ? lm_head_duo_fp8_kernel
                 : plan.kind == kLmSingle ? lm_head_kernel
                 : plan.kind == kLmPair   ? lm_head_pair_kernel
-                                         : lm_head_duo_kernel;   // kLmDuo, kLmDuoFused
-    return launch_kernel(kern, dim3(plan.grid), dim3(kLmThreads), smem, st, pdl, mx, mw, a);
+                : wide                   ? lm_head_duo_wide_kernel   // kLmDuo, kLmDuoFused
+                                         : lm_head_duo_kernel;
+    const int threads = !plan.duo() ? kLmThreads
+                        : wide      ? DuoEpilogue<kDuoCGWide>::Threads
+                                    : DuoEpilogue<kDuoCGNarrow>::Threads;
+    return launch_kernel(kern, dim3(plan.grid), dim3(threads), smem, st, pdl, mx, mw, a);
 }
 
 // Upper bound on the partial-state slots of any plan for these shapes

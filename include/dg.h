@@ -40,6 +40,7 @@
  *     their tilings from the shapes and the SM count (dg_lm_head_plan reports
  *     the LM-head choice).  For testing and tuning, the environment variables
  *     DG_LM_KERNEL (single | pair | duo | fused), DG_LM_BN (tile width),
+ *     DG_LM_EPI (8 | 16: epilogue warps of the 2-SM kernel, bf16 operands),
  *     DG_ATTN_KERNEL (single | pair) and DG_ATTN_SPLITS (key splits) force a
  *     choice; a choice the shapes do not allow is ignored.  Results do not
  *     depend on the choice beyond floating-point summation order.
@@ -254,10 +255,12 @@ uint64_t dg_kernel_launches(void);
 /* to both CTAs, 2 = 2-CTA cluster issuing 2-SM UMMAs, 3 = the kind-2 kernel */
 /* on a schedule of bn-column tiles whose adjacent pairs run as one tile of  */
 /* 2 bn columns; *bn: vocabulary columns per (schedule) tile; *ctas: CTAs    */
-/* launched.  Any output pointer may be NULL.                                 */
+/* launched; *epilogue_warps: the kind-2/3 kernel's epilogue warps (8 for a  */
+/* single 256-row block, else 16; 0 for kinds 0 and 1).  Any output pointer  */
+/* may be NULL.                                                               */
 /* Returns DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED for shapes the step        */
 /* rejects, DG_ERR_CUDA without a device. */
-int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas);
+int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas, int *epilogue_warps);
 
 /* ------------------------------------------------------------------------ */
 /* FP8 (E4M3) LM head.  The pages quote their throughput for an FP8 model     */

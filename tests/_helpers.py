@@ -76,3 +76,17 @@ def check_step_against_oracle(bufs, ref, B, L, exact_tokens):
         else:
             assert np.array_equal(canvas[sl][~acc_ref], ref["canvas"][sl][~acc_ref])
     return checked
+
+
+def force_lm_kernel(monkeypatch, spec):
+    """Force the LM-head choice: None = the planner's; "kind" or "kind/epi"
+    (kind single | pair | duo | fused; epi 8 | 16 epilogue warps of the
+    2-SM kernel)."""
+    monkeypatch.delenv("DG_LM_KERNEL", raising=False)
+    monkeypatch.delenv("DG_LM_EPI", raising=False)
+    if spec is None:
+        return
+    kind, _, epi = spec.partition("/")
+    monkeypatch.setenv("DG_LM_KERNEL", kind)
+    if epi:
+        monkeypatch.setenv("DG_LM_EPI", epi)

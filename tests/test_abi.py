@@ -117,9 +117,9 @@ def test_host_validation_rejects_before_launch(lib):
     assert enc(0, 256, D=64) == 2       # head dim
     assert enc(0, 256, kc=good + 4) == 3
     # LM-head plan query: shapes the step rejects are rejected before any device call
-    assert lib.dg_lm_head_plan(0, 1024, 16384, None, None, None) == 1
-    assert lib.dg_lm_head_plan(256, 1000, 16384, None, None, None) == 2
-    assert lib.dg_lm_head_plan(256, 1024, 16380, None, None, None) == 2
+    assert lib.dg_lm_head_plan(0, 1024, 16384, None, None, None, None) == 1
+    assert lib.dg_lm_head_plan(256, 1000, 16384, None, None, None, None) == 2
+    assert lib.dg_lm_head_plan(256, 1024, 16380, None, None, None, None) == 2
 
 
 def test_fp8_entry_points_validate_before_launch(lib):

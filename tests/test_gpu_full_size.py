@@ -26,7 +26,8 @@ import block_diffusion_decoding_gb300 as dg
 import dg_synth
 import oracle
 from tests._helpers import (ATTN_TOL, DEV, H_TOL, MARGIN, acceptance_is_decided,
-                            check_step_against_oracle, np_f, np_i32, status_ok, to_dev)
+                            check_step_against_oracle, force_lm_kernel, np_f, np_i32, status_ok,
+                            to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -60,10 +61,7 @@ def _step_case(cfg, k, seed, kernel_env, monkeypatch):
     ws = dg.workspace(dg.denoise_step_workspace(p), DEV)
     results = []
     for env in kernel_env:
-        if env is None:
-            monkeypatch.delenv("DG_LM_KERNEL", raising=False)
-        else:
-            monkeypatch.setenv("DG_LM_KERNEL", env)
+        force_lm_kernel(monkeypatch, env)
         bufs = dg.StepBuffers(B, L, DEV)
         bufs.canvas.copy_(torch.from_numpy(canvas0))
         bufs.prev_argmax.copy_(torch.from_numpy(prev))
@@ -74,16 +72,17 @@ def _step_case(cfg, k, seed, kernel_env, monkeypatch):
         assert np.array_equal(np_i32(bufs.stop), ref["stop"])
         assert np.abs(np_f(bufs.mean_entropy) - ref["mean_entropy"]).max() < H_TOL
         results.append((decided, np_f(bufs.entropy).copy()))
-    monkeypatch.delenv("DG_LM_KERNEL", raising=False)
+    force_lm_kernel(monkeypatch, None)
     return ref, results
 
 
 def test_full_width_step_every_row(monkeypatch):
     """2816 x 262144 LM head: the planned kernel (2-SM UMMA pair on fused
-    128-column schedule tiles), the same kernel on plain 256-column tiles and
-    the other two LM-head kernels against the same oracle step."""
+    128-column schedule tiles, 8 epilogue warps), the same kernel on plain
+    256-column tiles, with 16 epilogue warps, and the other two LM-head
+    kernels against the same oracle step."""
     cfg = dg_synth.CONFIGS["step_full"]
-    ref, res = _step_case(cfg, k=3, seed=0, kernel_env=[None, "duo", "single", "pair"],
+    ref, res = _step_case(cfg, k=3, seed=0, kernel_env=[None, "duo", "fused/16", "single", "pair"],
                           monkeypatch=monkeypatch)
     assert all(dec == 1 for dec, _ in res)
     # the per-row entropies span confident to uncertain rows

@@ -17,7 +17,8 @@ import block_diffusion_decoding_gb300 as dg
 import dg_synth
 import oracle
 from tests._helpers import (ATTN_TOL, DEV, H_TOL, MARGIN, acceptance_is_decided,
-                            check_step_against_oracle, np_f, np_i32, status_ok, to_dev)
+                            check_step_against_oracle, force_lm_kernel, np_f, np_i32, status_ok,
+                            to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -185,16 +186,15 @@ def test_denoise_step_matches_oracle(B, L, d, V, w_std, k):
     assert np.array_equal(np_f(bufs.entropy), H1)
 
 
-@pytest.mark.parametrize("kernel", [None, "single", "pair", "duo", "fused"])
+@pytest.mark.parametrize("kernel", [None, "single", "pair", "duo", "fused", "duo/8", "fused/16"])
 @pytest.mark.parametrize("B,L,d,V", [(1, 1024, 64, 64),      # largest canvas, one k block, tiny V
                                      (2, 1, 128, 2048),      # one position per canvas
                                      (5, 200, 192, 1104)])   # canvases straddling row blocks
 def test_denoise_step_edge_shapes(kernel, B, L, d, V, monkeypatch):
-    """Edge shapes through every LM-head kernel (None = the planner's choice)."""
-    if kernel is None:
-        monkeypatch.delenv("DG_LM_KERNEL", raising=False)
-    else:
-        monkeypatch.setenv("DG_LM_KERNEL", kernel)
+    """Edge shapes through every LM-head kernel (None = the planner's choice;
+    "/8", "/16": the 2-SM kernel's epilogue width forced against the
+    planner's, which takes 8 warps for one row block and 16 for several)."""
+    force_lm_kernel(monkeypatch, kernel)
     cfg = dg_synth.StepConfig("e", B=B, L=L, d=d, V=V, w_std=0.1, seed=23)
     xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
     T, b, seed, k = oracle.temperature(7, 48), 0.1, 17, 7
@@ -213,7 +213,7 @@ def test_denoise_step_edge_shapes(kernel, B, L, d, V, monkeypatch):
     check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
 
 
-@pytest.mark.parametrize("kernel", ["duo", "fused", "pair"])
+@pytest.mark.parametrize("kernel", ["duo", "fused", "pair", "fused/8"])
 def test_shared_row_bounds_across_launches(kernel, monkeypatch):
     """The 2-SM LM head lets its units share per-row lower bounds on the best
     Gumbel score within a launch (to skip noise that cannot win).  Several
@@ -221,7 +221,7 @@ def test_shared_row_bounds_across_launches(kernel, monkeypatch):
     the oracle, and a repeated step must reproduce its outputs bit for bit
     (the shared bounds change which columns are skipped, never the result).
     Two row blocks, mixed per-row logit scales as in the full-width step."""
-    monkeypatch.setenv("DG_LM_KERNEL", kernel)
+    force_lm_kernel(monkeypatch, kernel)
     B, L, d, V = 2, 256, 256, 65536
     cfg = dg_synth.StepConfig("rb", B=B, L=L, d=d, V=V, w_std=0.06, row_scale=(0.5, 8.0),
                               seed=31)
@@ -255,6 +255,24 @@ def test_shared_row_bounds_across_launches(kernel, monkeypatch):
                 for a_, b_ in zip(out, first[k]):
                     assert np.array_equal(a_, b_)
         dg.read_device_status(ws, clear=True)
+
+
+def test_lm_head_plan_epilogue_width(monkeypatch):
+    """The 2-SM kernel runs 8 epilogue warps on one 256-row block and 16 on
+    several; DG_LM_EPI forces either; the other kernels report 0."""
+    force_lm_kernel(monkeypatch, None)
+    one = dg.lm_head_plan(256, 2816, 262144)
+    assert one["kind"] in (2, 3) and one["epilogue_warps"] == 8
+    assert one["kernel"] == "lm_head_duo_kernel"
+    many = dg.lm_head_plan(4096, 2816, 262144)
+    assert many["kind"] in (2, 3) and many["epilogue_warps"] == 16
+    assert many["kernel"] == "lm_head_duo_wide_kernel"
+    force_lm_kernel(monkeypatch, "fused/16")
+    assert dg.lm_head_plan(256, 2816, 262144)["epilogue_warps"] == 16
+    force_lm_kernel(monkeypatch, "duo/8")
+    assert dg.lm_head_plan(4096, 2816, 262144)["epilogue_warps"] == 8
+    force_lm_kernel(monkeypatch, "single")
+    assert dg.lm_head_plan(256, 2816, 262144)["epilogue_warps"] == 0
 
 
 def test_denoise_step_uniform_and_one_hot_rows():

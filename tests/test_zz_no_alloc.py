@@ -25,9 +25,10 @@ def _state(bufs):
     return {n: getattr(bufs, n).detach().cpu().numpy().copy() for n, _ in dg.StepIO._fields_}
 
 
-def test_noalloc_step_matches_workspace_step_on_two_consecutive_calls():
+@pytest.mark.parametrize("B", [1, 2])   # one row block / two (the LM head's two epilogue widths)
+def test_noalloc_step_matches_workspace_step_on_two_consecutive_calls(B):
     lib = dg.lib()
-    cfg = dg_synth.StepConfig("noalloc", B=1, L=256, d=1024, V=16384, w_std=0.05, seed=21)
+    cfg = dg_synth.StepConfig("noalloc", B=B, L=256, d=1024, V=16384, w_std=0.05, seed=21)
     x, w = to_dev(dg_synth.lm_hidden(cfg)), to_dev(dg_synth.lm_weight(cfg))
     rng = np.random.default_rng(5)
     canvas0 = torch.from_numpy(rng.integers(0, cfg.V, cfg.M).astype(np.int32))
