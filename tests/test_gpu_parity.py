@@ -356,6 +356,37 @@ def test_canvas_attn_edge_shapes(kernel, B, L, P, Hq, Hkv, D, monkeypatch):
     _attn_case(B, L, P, Hq, Hkv, D, seed=3 + P, row_stride=1)
 
 
+def test_canvas_attn_pair_split_counts_on_one_workspace(monkeypatch):
+    """The 2-SM kernel with 2, 3 and 4 key splits, launched in turn on one
+    workspace: every launch must match the oracle, and a repeated launch with
+    the same split count must reproduce its output bit for bit (nothing a
+    launch leaves in the workspace changes the next one)."""
+    monkeypatch.setenv("DG_ATTN_KERNEL", "pair")
+    B, L, P, Hq, Hkv, D = 2, 256, 1000, 16, 8, 256
+    cfg = dg_synth.StepConfig("a", B=B, L=L, P=P, Hq=Hq, Hkv=Hkv, D=D, seed=13)
+    ai = dg_synth.attention_inputs(cfg)
+    t = {k: to_dev(v) for k, v in ai.items()}
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    ws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    rows = np.arange(0, B * L * Hq, 7)
+    ref = oracle.attention_rows(ai["q"], ai["kp"], ai["vp"], ai["kc"], ai["vc"], B, L, P, Hq, Hkv,
+                                D, scale, rows)
+    first = {}
+    for splits in (4, 2, 3, 4, 2):
+        monkeypatch.setenv("DG_ATTN_SPLITS", str(splits))
+        out = torch.full_like(t["q"], float("nan"))
+        dg.canvas_attn(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], out, scale, ws)
+        torch.cuda.synchronize()
+        status_ok(ws)
+        got = out.float().reshape(-1, D).cpu().numpy()
+        assert np.isfinite(got).all()
+        err = np.abs(got[rows] - ref).max(axis=1) / np.abs(ref).max(axis=1)
+        assert err.max() < ATTN_TOL, (splits, err.max())
+        if splits in first:
+            assert np.array_equal(got, first[splits])
+        first[splits] = got
+
+
 def test_canvas_attn_constant_values_and_zero_keys():
     """Constant value rows -> every output equals that row; zero keys -> mean of values."""
     B, L, P, Hq, Hkv, D = 1, 128, 200, 4, 1, 128
