@@ -245,10 +245,11 @@ def _config_json(cfg, l2, lm_dtype="bf16"):
 
 
 # ----------------------------------------------------------------------------- our arm
-def _traffic_record(kernel_sources, kernel):
-    """Per-launch DRAM bytes of the LM-head kernel from the committed ncu summary,
-    valid only while the kernel sources are unchanged and for the same kernel."""
-    path = os.path.join(ROOT, "profiles", "lm_head_duo_kernel_step_full.md")
+def _traffic_record(kernel_sources, kernel, shape):
+    """Per-launch DRAM bytes of the LM-head kernel from its committed ncu summary
+    (profiles/<kernel>_step_full.md), valid only while the kernel sources are
+    unchanged and for the same kernel and GEMM shape (rows, d, V)."""
+    path = os.path.join(ROOT, "profiles", "%s_step_full.md" % kernel)
     if not os.path.exists(path):
         return None
     h = hashlib.sha256()
@@ -263,6 +264,8 @@ def _traffic_record(kernel_sources, kernel):
                 k, v = line.strip()[2:].split(":", 1)
                 rec[k.strip()] = v.strip()
     if rec.get("source_sha256_16") != digest or rec.get("kernel") != kernel:
+        return None
+    if rec.get("shape") != "x".join(str(v) for v in shape):
         return None
     try:
         return float(rec["dram_bytes_per_launch"])
@@ -409,7 +412,7 @@ def run_ours(args, cfg):
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
             for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
-    traffic = None if fp8 else _traffic_record(srcs, lm_plan["kernel"])
+    traffic = _traffic_record(srcs, lm_plan["kernel"], (M, d, V))
 
     # ---- end to end through the C ABI with host buffers (pinned): per step,
     # one H2D copy of the step's inputs (hidden states, canvas Q/K/V) and one
@@ -600,7 +603,7 @@ def run_block(args, cfg):
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
             for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
-    traffic = _traffic_record(srcs, lm_plan["kernel"])
+    traffic = _traffic_record(srcs, lm_plan["kernel"], (M, d, V))
 
     # end to end: the block's hidden states go up from pinned host memory,
     # the result (canvas, argmax, steps taken) comes back
