@@ -746,6 +746,26 @@ DG_DEVICE uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
     return c;
 }
 
+// Four Philox4x32-10 blocks under one key, advanced round by round: the
+// same words as four philox4x32_10 calls, with one key-schedule update per
+// round for all four and four independent multiply chains in flight.
+DG_DEVICE void philox4x32_10_x4(uint4 (&c)[4], uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint64_t p0 = static_cast<uint64_t>(c[q].x) * 0xD2511F53u;
+            const uint64_t p1 = static_cast<uint64_t>(c[q].z) * 0xCD9E8D57u;
+            const uint32_t lo0 = static_cast<uint32_t>(p0), hi0 = static_cast<uint32_t>(p0 >> 32);
+            const uint32_t lo1 = static_cast<uint32_t>(p1), hi1 = static_cast<uint32_t>(p1 >> 32);
+            c[q] = make_uint4(hi1 ^ c[q].y ^ k0, lo1, hi0 ^ c[q].w ^ k1, lo0);
+        }
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
+
 // Philox streams of the sampler: counter (lane, row, step, stream).
 enum : uint32_t { kStreamGumbel = 0u, kStreamRenoise = 1u, kStreamInit = 2u };
 

@@ -206,14 +206,18 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         lz[2 * q + 1] = z.y;
     }
     uint32_t w[16];
+    {
+        uint4 r[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 r = philox4x32_10(make_uint4((v0 >> 2) + q, row, fc.step, kStreamGumbel),
-                                      fc.k0, fc.k1);
-        w[4 * q] = r.x;
-        w[4 * q + 1] = r.y;
-        w[4 * q + 2] = r.z;
-        w[4 * q + 3] = r.w;
+        for (int q = 0; q < 4; ++q) r[q] = make_uint4((v0 >> 2) + q, row, fc.step, kStreamGumbel);
+        philox4x32_10_x4(r, fc.k0, fc.k1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[4 * q] = r[q].x;
+            w[4 * q + 1] = r[q].y;
+            w[4 * q + 2] = r[q].z;
+            w[4 * q + 3] = r[q].w;
+        }
     }
     // Stage 1b (noise words only): a column of this chunk can reach lb only
     // if its Gumbel value exceeds lb - cz; the columns whose word is below the
