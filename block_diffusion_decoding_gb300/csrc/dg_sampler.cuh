@@ -223,12 +223,17 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     // if its Gumbel value exceeds lb - cz; the columns whose word is below the
     // threshold of gumbel_word_threshold cannot, and need no logarithm.
     const uint32_t wthr = gumbel_word_threshold(lb - cz - kGumbelSlack);
+    // no column of the warp can win: stage 2 would change nothing (tested on
+    // the chunk's largest word first; the per-column mask is built only for
+    // a chunk that goes on)
+    uint32_t wmax = w[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) wmax = max(wmax, w[j]);
+    if (!__any_sync(0xFFFFFFFFu, live && wmax >= wthr)) return;
     uint32_t in = 0;
 #pragma unroll
     for (int j = 0; j < 16; ++j) in |= (w[j] >= wthr ? 1u : 0u) << j;
     if (!live) in = 0;
-    // no column of the warp can win: stage 2 would change nothing
-    if (!__any_sync(0xFFFFFFFFu, in != 0)) return;
     // Stage 2: approximate scores lz + G~.  A column can end up as the chunk's
     // exact best only if its approximate score is within twice the estimate's
     // error of the chunk's best approximate score, and above the running best.
