@@ -197,14 +197,6 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     // rounding is monotone, so the chunk's largest scaled logit is cmax * invT
     const float cz = cmax * fc.invT;
     if (!__any_sync(0xFFFFFFFFu, cz > lb - kGumbelMaxPlusSlack)) return;
-    float lz[16];
-    const float2 iv = make_float2(fc.invT, fc.invT);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float2 z = mul2(make_float2(x[2 * q], x[2 * q + 1]), iv);
-        lz[2 * q] = z.x;
-        lz[2 * q + 1] = z.y;
-    }
     uint32_t w[16];
     {
         uint4 r[4];
@@ -234,6 +226,14 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
 #pragma unroll
     for (int j = 0; j < 16; ++j) in |= (w[j] >= wthr ? 1u : 0u) << j;
     if (!live) in = 0;
+    float lz[16];
+    const float2 iv = make_float2(fc.invT, fc.invT);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float2 z = mul2(make_float2(x[2 * q], x[2 * q + 1]), iv);
+        lz[2 * q] = z.x;
+        lz[2 * q + 1] = z.y;
+    }
     // Stage 2: approximate scores lz + G~.  A column can end up as the chunk's
     // exact best only if its approximate score is within twice the estimate's
     // error of the chunk's best approximate score, and above the running best.
