@@ -410,7 +410,7 @@ def run_ours(args, cfg):
     if fp8:
         lm_plan = dict(lm_plan, kernel="lm_head_duo_fp8_kernel")
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
-            for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
+            for f in ("dg_lm_head.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
     traffic = _traffic_record(srcs, lm_plan["kernel"], (M, d, V))
 
@@ -601,7 +601,7 @@ def run_block(args, cfg):
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
     lm_plan = dg.lm_head_plan(M, d, V)
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
-            for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
+            for f in ("dg_lm_head.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
     traffic = _traffic_record(srcs, lm_plan["kernel"], (M, d, V))
 

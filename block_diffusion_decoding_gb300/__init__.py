@@ -228,7 +228,7 @@ def lm_head_plan(rows: int, d: int, V: int) -> dict:
     if kind.value >= 2:
         name = "lm_head_duo_wide_kernel" if epi.value == 16 else "lm_head_duo_kernel"
     else:
-        name = ("lm_head_kernel", "lm_head_pair_kernel")[kind.value]
+        name = "lm_head_kernel"
     return {"kernel": name, "kind": kind.value, "BN": bn.value, "ctas": ctas.value,
             "fused": kind.value == 3, "epilogue_warps": epi.value}
 

@@ -71,9 +71,6 @@ int current_device_info(DeviceInfo **out)
     if (!di.attrs_set) {
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kLmSmemBytes));
-        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_pair_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kPairSmemBytes));
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));

@@ -354,17 +354,6 @@ DG_DEVICE void umma_commit(uint64_t *bar)
         : "memory");
 }
 
-// As umma_commit, but the arrival goes to the mbarrier at the same shared
-// offset in every CTA of the cluster named in cta_mask.
-DG_DEVICE void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // ---- 2-SM UMMA (cta_group::2): the CTA pair of a 2-CTA cluster acts as one
 // MMA unit.  One warp of each CTA allocates (collectively) the same TMEM
 // columns in both; the even CTA issues the MMAs; A (M = 256) is rows 0-127
@@ -600,20 +589,6 @@ DG_DEVICE void cluster_sync_all()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// TMA 2-D load delivered to the same shared offset (data and complete_tx) in
-// every CTA of cta_mask.  The tensor lives in this GPU's own memory.
-DG_DEVICE void tma_load_2d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
-                                     uint16_t cta_mask, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask),
-        "l"(policy)
-        : "memory");
 }
 
 // Instruction descriptor, kind::f16: D fp32, A/B bf16, A K-major,

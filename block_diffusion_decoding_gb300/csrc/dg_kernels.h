@@ -102,17 +102,12 @@ constexpr int kLmSmemBytes = kLmStages * kLmStageBytes + 1024 + 256 + kLmMergeBy
 __global__ void lm_head_kernel(const __grid_constant__ CUtensorMap map_x,
                                const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 
-// 2-CTA cluster variant: CTA rank r of a cluster owns rows [128 r, 128 r + 128)
-// of each 256-row block and all BN (128 or 256) columns of the cluster's
-// tiles; the W tile is multicast to both CTAs, each loading half of it.
+// Shared-memory geometry of the 2-CTA cluster kernels: each CTA of the pair
+// stages its own 128 X rows per k block; the epilogue's column groups merge
+// through up to (4 - 1) x 7 x 128 floats.
 constexpr int kPairABytes = 128 * kLmBK * 2;             // 16 KB: X rows of this CTA
-constexpr int kPairStageBytes = kPairABytes + 4 * kLmBBoxBytes;   // + up to 256 W columns
-constexpr int kPairStages = 4;
-constexpr int kPairColGroups = 4;                        // epilogue warps per TMEM quadrant
+constexpr int kPairColGroups = 4;                        // largest epilogue column-group count
 constexpr int kPairMergeBytes = (kPairColGroups - 1) * 7 * 128 * 4;     // 10.5 KB
-constexpr int kPairSmemBytes = kPairStages * kPairStageBytes + 1024 + 256 + kPairMergeBytes;
-__global__ void lm_head_pair_kernel(const __grid_constant__ CUtensorMap map_x,
-                                    const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 
 // 2-SM UMMA variant (tcgen05 cta_group::2): each CTA of the pair loads its
 // own 128 rows of X and 128 of the 256 W columns of a tile; the even CTA

@@ -79,8 +79,6 @@ int na_setup(NoAllocDevice **out)
             cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaFuncSetAttribute(lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kLmSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(lm_head_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(lm_head_duo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kDuoSmemBytes) != cudaSuccess ||
             cudaFuncSetAttribute(lm_head_duo_wide_kernel,

@@ -15,7 +15,7 @@ constexpr int kMaxSlots = 256;       // upper bound on LM-head CTAs (>= SM count
 // LM-head kernels
 enum LmKind : int {
     kLmSingle = 0,    // lm_head_kernel: one CTA per tile, 256 rows x BN columns
-    kLmPair = 1,      // lm_head_pair_kernel: 2-CTA cluster, W tile multicast
+                      // (kind 1 is not used)
     kLmDuo = 2,       // lm_head_duo_kernel: 2-CTA cluster, 2-SM UMMA
     kLmDuoFused = 3,  // lm_head_duo_kernel on 128-column schedule tiles, each
                       // adjacent pair in a cluster's range (same row block)
@@ -42,8 +42,8 @@ struct LmPlan {
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
 // CTA, plus a per-tile overhead; the 2-SM kernel runs 8 epilogue warps on a
-// single 256-row block of bf16 operands, else 16.  DG_LM_KERNEL=single|pair|
-// duo|fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
+// single 256-row block of bf16 operands, else 16.  DG_LM_KERNEL=single|duo|
+// fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
 // have the 2-SM UMMA kernel only.
 inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
 {
@@ -58,7 +58,6 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
     const char *env_k = std::getenv("DG_LM_KERNEL");
     const int only_env = !env_k ? -1
                      : std::strcmp(env_k, "single") == 0 ? kLmSingle
-                     : std::strcmp(env_k, "pair") == 0   ? kLmPair
                      : std::strcmp(env_k, "duo") == 0    ? kLmDuo
                      : std::strcmp(env_k, "fused") == 0  ? kLmDuoFused
                                                          : -1;
@@ -77,9 +76,8 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
         const long per_unit = (total + units - 1) / units;
         // per-SM columns of a tile: bn (single, 256 rows) or bn / 2 (clusters,
         // 128 rows each, and half the hidden-block traffic per tile), plus a
-        // per-tile overhead (the 2-SM UMMA kernel moves a third less shared
-        // memory per k block than the multicast one)
-        const long over = kind == kLmSingle ? 40 : kind == kLmPair ? 30 : 25;
+        // per-tile overhead
+        const long over = kind == kLmSingle ? 40 : 25;
         // fused: the per-tile overhead is paid once per 256-column tile
         const long cost = kind == kLmDuoFused
                               ? per_unit * (bn / 2) + (per_unit + 1) / 2 * over
@@ -98,8 +96,6 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
         // a forced width no candidate of the kernel has is ignored
         if (pass == 1) forced_bn = 0;
         for (int bn = 128; bn >= 64; bn -= 16) consider(kLmSingle, bn);
-        consider(kLmPair, 256);
-        consider(kLmPair, 128);
         consider(kLmDuo, 256);
         consider(kLmDuo, 128);
         consider(kLmDuoFused, 128);
@@ -117,7 +113,7 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
 
 inline int lm_smem_bytes(int kind)
 {
-    return kind == kLmSingle ? kLmSmemBytes : kind == kLmPair ? kPairSmemBytes : kDuoSmemBytes;
+    return kind == kLmSingle ? kLmSmemBytes : kDuoSmemBytes;
 }
 
 // Launch with programmatic stream serialization when `pdl` is set: the kernel
@@ -161,7 +157,6 @@ inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, con
     const bool wide = plan.epi_warps == 4 * kDuoCGWide;
     auto kern = fp8                    ? lm_head_duo_fp8_kernel
                 : plan.kind == kLmSingle ? lm_head_kernel
-                : plan.kind == kLmPair   ? lm_head_pair_kernel
                 : wide                   ? lm_head_duo_wide_kernel   // kLmDuo, kLmDuoFused
                                          : lm_head_duo_kernel;
     const int threads = !plan.duo() ? kLmThreads

@@ -39,7 +39,7 @@
  *   - Kernel choice: the library picks the LM-head and attention kernels and
  *     their tilings from the shapes and the SM count (dg_lm_head_plan reports
  *     the LM-head choice).  For testing and tuning, the environment variables
- *     DG_LM_KERNEL (single | pair | duo | fused), DG_LM_BN (tile width),
+ *     DG_LM_KERNEL (single | duo | fused), DG_LM_BN (tile width),
  *     DG_LM_EPI (8 | 16: epilogue warps of the 2-SM kernel, bf16 operands),
  *     DG_ATTN_KERNEL (single | pair) and DG_ATTN_SPLITS (key splits) force a
  *     choice; a choice the shapes do not allow is ignored.  Results do not
@@ -251,12 +251,12 @@ uint64_t dg_kernel_launches(void);
 
 /* The LM-head launch dg_denoise_step would make on the current device for    */
 /* rows = B*L canvas positions, hidden size d and vocabulary V (no launch).   */
-/* *kind: 0 = single-CTA kernel, 1 = 2-CTA cluster with the W tile multicast */
-/* to both CTAs, 2 = 2-CTA cluster issuing 2-SM UMMAs, 3 = the kind-2 kernel */
-/* on a schedule of bn-column tiles whose adjacent pairs run as one tile of  */
-/* 2 bn columns; *bn: vocabulary columns per (schedule) tile; *ctas: CTAs    */
-/* launched; *epilogue_warps: the kind-2/3 kernel's epilogue warps (8 for a  */
-/* single 256-row block, else 16; 0 for kinds 0 and 1).  Any output pointer  */
+/* *kind: 0 = single-CTA kernel, 2 = 2-CTA cluster issuing 2-SM UMMAs,      */
+/* 3 = the kind-2 kernel on a schedule of bn-column tiles whose adjacent     */
+/* pairs run as one tile of 2 bn columns (kind 1 is not used); *bn:          */
+/* vocabulary columns per (schedule) tile; *ctas: CTAs launched;             */
+/* *epilogue_warps: the kind-2/3 kernel's epilogue warps (8 for a single     */
+/* 256-row block, else 16; 0 for kind 0).  Any output pointer                */
 /* may be NULL.                                                               */
 /* Returns DG_ERR_INVALID_ARG / DG_ERR_UNSUPPORTED for shapes the step        */
 /* rejects, DG_ERR_CUDA without a device. */

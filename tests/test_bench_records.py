@@ -13,7 +13,7 @@ sys.path.insert(0, ROOT)
 import bench  # noqa: E402
 
 SRCS = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
-        for f in ("dg_lm_head.cu", "dg_lm_head_pair.cu", "dg_lm_head_duo.cu", "dg_plan.h",
+        for f in ("dg_lm_head.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                   "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
 FULL = (256, 2816, 262144)
 

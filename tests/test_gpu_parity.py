@@ -186,7 +186,7 @@ def test_denoise_step_matches_oracle(B, L, d, V, w_std, k):
     assert np.array_equal(np_f(bufs.entropy), H1)
 
 
-@pytest.mark.parametrize("kernel", [None, "single", "pair", "duo", "fused", "duo/8", "fused/16"])
+@pytest.mark.parametrize("kernel", [None, "single", "duo", "fused", "duo/8", "fused/16"])
 @pytest.mark.parametrize("B,L,d,V", [(1, 1024, 64, 64),      # largest canvas, one k block, tiny V
                                      (2, 1, 128, 2048),      # one position per canvas
                                      (5, 200, 192, 1104)])   # canvases straddling row blocks
@@ -213,7 +213,7 @@ def test_denoise_step_edge_shapes(kernel, B, L, d, V, monkeypatch):
     check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
 
 
-@pytest.mark.parametrize("kernel", ["duo", "fused", "pair", "fused/8"])
+@pytest.mark.parametrize("kernel", ["duo", "fused", "fused/8"])
 def test_shared_row_bounds_across_launches(kernel, monkeypatch):
     """The 2-SM LM head lets its units share per-row lower bounds on the best
     Gumbel score within a launch (to skip noise that cannot win).  Several
