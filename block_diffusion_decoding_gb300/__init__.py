@@ -29,6 +29,7 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_canvas_attn_workspace", "dg_canvas_attn",
             "dg_encoder_append_workspace", "dg_encoder_append",
             "dg_denoise_step_workspace", "dg_denoise_step", "dg_denoise_step_noalloc",
+            "dg_noalloc_read_device_status",
             "dg_generate_block_workspace", "dg_generate_block",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
             "dg_lm_head_fold", "dg_kernel_launches", "dg_lm_head_plan", "dg_gumbel_fill",
@@ -93,6 +94,7 @@ def _lib():
             "dg_denoise_step_workspace": ([sp], sz),
             "dg_denoise_step": ([vp, vp, sp, si, vp, sz, vp], i32),
             "dg_denoise_step_noalloc": ([vp, vp, sp, si, vp], i32),
+            "dg_noalloc_read_device_status": ([ctypes.POINTER(ctypes.c_int), i32, vp], i32),
             "dg_generate_block_workspace": ([sp, bp], sz),
             "dg_generate_block": ([vp, vp, sp, bp, bi, vp, sz, vp], i32),
             "dg_sampler_workspace": ([sp], sz),

@@ -15,15 +15,21 @@
 // it until the process exits.
 //
 // Capacity: kNoAllocScratchBytes = 8 MiB.  A step needs 256 bytes of header,
-// 7 x 4 bytes x (LM-head units) x B*L of partial states and 4 bytes per canvas
-// (each rounded up to 256 bytes).  With one unit per SM on a 152-SM GB300
-// that is at most B*L = 1970 canvas rows (seven 256-token canvases); larger
-// steps are rejected with DG_ERR_UNSUPPORTED before anything is launched.
+// 7 x 4 bytes x (LM-head units) x B*L of partial states, 4 bytes per canvas
+// and 4 bytes per canvas row (the per-row Gumbel bounds the 2-SM LM-head
+// units share), each rounded up to 256 bytes.  With one unit per SM on a
+// 152-SM GB300 (the most any plan uses) every step of up to B*L = 1968
+// canvas rows fits (seven 256-token canvases); steps that need more are
+// rejected with DG_ERR_UNSUPPORTED before anything is launched.
 //
 // Sharing: every call, from any thread or stream, uses the same array and
 // leaves the last call's contents in it.  The counters that must start at
-// zero are zeroed by the first kernel of each call; the status header is
-// cleared once, at set-up.  Calls whose kernels overlap on the GPU (two
+// zero are zeroed by the first kernel of each call (the row bounds by the
+// LM head itself, under an epoch kept in the header); the status header is
+// cleared at set-up and by dg_noalloc_read_device_status(clear != 0).  A
+// kernel that meets a problem on the device (a bounded wait that ran out)
+// records it in the header and returns early; the step's outputs are then
+// not valid, and dg_noalloc_read_device_status reports it.  Calls whose kernels overlap on the GPU (two
 // streams, two threads without ordering) race on the array and give wrong
 // results: order them on one stream.
 //
@@ -154,10 +160,11 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     const LmPlan plan = plan_lm_head(M, p->d, p->V, st->sms);
     const int BN = plan.BN, ntn = plan.ntn, total = plan.total;
 
-    // ---- scratch layout (as a workspace): header | partials | counters
+    // ---- scratch layout (as a workspace): header | partials | counters | row keys
     const size_t npart = static_cast<size_t>(plan.part_slots()) * M;
     const size_t need = sizeof(WsHeader) + na_round_up(7 * npart * 4, 256) +
-                        na_round_up(static_cast<size_t>(p->B) * 4, 256);
+                        na_round_up(static_cast<size_t>(p->B) * 4, 256) +
+                        na_round_up(static_cast<size_t>(M) * 4, 256);
     if (need > kNoAllocScratchBytes) return DG_ERR_UNSUPPORTED;
     unsigned char *base = st->scratch;
     WsHeader *hdr = reinterpret_cast<WsHeader *>(base);
@@ -171,6 +178,8 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     part.gidx = reinterpret_cast<int *>(f + 5 * npart);
     part.aidx = reinterpret_cast<int *>(f + 6 * npart);
     int *counters = reinterpret_cast<int *>(base + sizeof(WsHeader) + na_round_up(7 * npart * 4, 256));
+    uint32_t *rowkey = reinterpret_cast<uint32_t *>(
+        reinterpret_cast<unsigned char *>(counters) + na_round_up(static_cast<size_t>(p->B) * 4, 256));
 
     CUtensorMap mx, mw;
     if ((rc = na_map(&mx, hidden, static_cast<uint64_t>(p->d), static_cast<uint64_t>(M), 64,
@@ -202,6 +211,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     a.ws = hdr;
     a.counters = counters;
     a.ncounters = p->B;
+    a.rowkey = rowkey;
 
     CombineArgs c{};
     c.part = part;
@@ -236,5 +246,31 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     if (launch_kernel(combine_accept_kernel, dim3((p->L + c.rows_per_cta - 1) / c.rows_per_cta, p->B), dim3(kAcceptThreads), 0, s, pdl, c,
                       acc) != cudaSuccess)
         return DG_ERR_CUDA;
+    return DG_OK;
+}
+
+// The status header of the scratch array: 0, or the DG_ERR_* code a kernel of
+// dg_denoise_step_noalloc recorded on the device.  Synchronous on `stream`;
+// clear != 0 resets the header afterwards (also on the stream).  Allocates
+// nothing; the first call on a device may do the array's set-up.
+extern "C" int dg_noalloc_read_device_status(int *status_out, int clear, void *stream)
+{
+    if (status_out == nullptr) return DG_ERR_INVALID_ARG;
+    NoAllocDevice *st = nullptr;
+    int rc = na_setup(&st);
+    if (rc != DG_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, st->scratch, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    *status_out = v;
+    if (clear && (cudaMemsetAsync(st->scratch, 0, sizeof(WsHeader), s) != cudaSuccess ||
+                  cudaStreamSynchronize(s) != cudaSuccess)) {
+        (void)cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
     return DG_OK;
 }

@@ -181,15 +181,23 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 /* this is a deployment convenience.  Same kernels, same results; their       */
 /* scratch lives in one 8 MiB array inside the library's device memory,      */
 /* held by every GPU that loads the library until the process exits.         */
-/* Limit: steps needing more than 8 MiB of scratch (7 x 4 B x CTAs x B*L     */
-/* + 512 B; B*L <= 1970 on a 152-SM GB300) return DG_ERR_UNSUPPORTED.  The    */
-/* first call on a device sets up the array's address (cudaGetSymbolAddress) and */
-/* clears its status header: make it before any stream capture.  All calls    */
-/* share the array; calls that overlap on the GPU race -- order them on one   */
-/* stream.  Calls no cudaMalloc/cudaFree.  Device-side errors of this path    */
-/* are not readable with dg_read_device_status.                               */
+/* Limit: steps needing more than 8 MiB of scratch (256 B + 7 x 4 B x units  */
+/* x B*L + 4 B x B + 4 B x B*L, each term but the first rounded up to 256 B; */
+/* units = the LM-head plan's CTAs, or clusters for kinds 2/3; every step    */
+/* with B*L <= 1968 fits on a 152-SM GB300) return DG_ERR_UNSUPPORTED.  The first call on a device */
+/* sets up the array's address (cudaGetSymbolAddress) and clears its status  */
+/* header: make it before any stream capture.  All calls share the array;    */
+/* calls that overlap on the GPU race -- order them on one stream.  Calls no */
+/* cudaMalloc/cudaFree.  Device-side errors of this path are read with       */
+/* dg_noalloc_read_device_status, not dg_read_device_status.                 */
 int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w, const dg_step_params *p,
                             const dg_step_io *io, void *stream);
+
+/* The device status word of dg_denoise_step_noalloc's scratch array (0 or a  */
+/* DG_ERR_* code recorded by its kernels), read with a synchronous copy on    */
+/* `stream` into *status_out (host); clear != 0 resets it.  Allocates        */
+/* nothing.  Errors: DG_ERR_INVALID_ARG (null status_out), DG_ERR_CUDA.      */
+int dg_noalloc_read_device_status(int *status_out, int clear, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* The denoising loop of one block (batch of B independent canvases).        */
