@@ -34,7 +34,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_sampler_workspace", "dg_sampler_from_logits", "dg_accept_renoise",
             "dg_lm_head_fold", "dg_kernel_launches", "dg_lm_head_plan", "dg_gumbel_fill",
             "dg_logf_eval", "dg_quantize_rows_e4m3", "dg_quantize_weight_e4m3",
-            "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8"]
+            "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8",
+            "dg_wait_timeout_probe"]
 
 
 class DgError(RuntimeError):
@@ -110,6 +111,7 @@ def _lib():
             "dg_denoise_step_fp8_workspace": ([sp], sz),
             "dg_denoise_step_fp8": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
             "dg_lm_head_fold_fp8": ([vp, vp, vp, sp, vp, sz, vp], i32),
+            "dg_wait_timeout_probe": ([vp, sz, u64, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -334,6 +336,12 @@ def gumbel_fill(seed, row, step, v0, n, out, stream=None):
 
 def logf_eval(x, y, stream=None):
     _check(_lib().dg_logf_eval(_p(x), _p(y), x.numel(), _stream(stream)), "dg_logf_eval")
+
+
+def wait_timeout_probe(workspace, limit_ns: int, stream=None):
+    """dg_wait_timeout_probe: a bounded wait that nothing completes, on purpose."""
+    _check(_lib().dg_wait_timeout_probe(_p(workspace), workspace.numel(), int(limit_ns),
+                                        _stream(stream)), "dg_wait_timeout_probe")
 
 
 def read_device_status(workspace, clear=False, stream=None) -> int:

@@ -1091,4 +1091,15 @@ int dg_logf_eval(const float *x, float *y, int n, void *stream)
     return DG_OK;
 }
 
+int dg_wait_timeout_probe(void *workspace, size_t workspace_bytes, uint64_t limit_ns, void *stream)
+{
+    if (workspace == nullptr || workspace_bytes < sizeof(WsHeader)) return DG_ERR_WORKSPACE;
+    if (limit_ns < 1000 || limit_ns > kWaitLimitNs) return DG_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    wait_probe_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<WsHeader *>(workspace), limit_ns);
+    DG_LAUNCHED();
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
 }  // extern "C"

@@ -155,17 +155,23 @@ DG_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // caller winds down without touching the resource it waited for.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-DG_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, WsHeader *ws, int where)
+DG_DEVICE bool mbar_wait_limit(uint64_t *bar, uint32_t parity, WsHeader *ws, int where,
+                               uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) {
             report_error(ws, DG_ERR_TIMEOUT, where);
             return false;
         }
     }
+}
+
+DG_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity, WsHeader *ws, int where)
+{
+    return mbar_wait_limit(bar, parity, ws, where, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------------

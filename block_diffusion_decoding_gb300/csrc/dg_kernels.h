@@ -163,6 +163,7 @@ __global__ void loop_init_kernel(LoopCtl *ctl, int max_steps, double t0, double 
 __global__ void gumbel_fill_kernel(uint32_t k0, uint32_t k1, uint32_t row, uint32_t step,
                                    uint32_t v0, int n, float *out);
 __global__ void logf_eval_kernel(const float *x, float *y, int n);
+__global__ void wait_probe_kernel(WsHeader *ws, uint64_t limit_ns);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {

@@ -358,6 +358,34 @@ __global__ void gumbel_fill_kernel(uint32_t k0, uint32_t k1, uint32_t row, uint3
     }
 }
 
+// The failure path of a bounded wait, on its own: one warp allocates TMEM,
+// waits on an mbarrier that nothing arrives on, gives up after limit_ns
+// (DG_ERR_TIMEOUT in the workspace header), frees its TMEM and returns.  A
+// wait that completed would be a bug and is reported as DG_ERR_DEVICE.
+__global__ void __launch_bounds__(32) wait_probe_kernel(WsHeader *ws, uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tslot;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    tmem_alloc(&tslot, 32);
+    tmem_relinquish();
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    const uint32_t taddr = tslot;
+    if (threadIdx.x == 0) {
+        // phase 0 of a fresh barrier completes only after one arrival
+        if (mbar_wait_limit(&bar, 0u, ws, 901, limit_ns)) report_error(ws, DG_ERR_DEVICE, 902);
+    }
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(taddr, 32);
+}
+
 __global__ void logf_eval_kernel(const float *x, float *y, int n)
 {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;

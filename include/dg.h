@@ -331,6 +331,17 @@ int dg_gumbel_fill(uint64_t seed, uint32_t row, uint32_t step, uint32_t v0, int 
 /* The sampler's fp32 natural logarithm applied to x[0..n) (device arrays).   */
 int dg_logf_eval(const float *x, float *y, int n, void *stream);
 
+/* The failure path of the library's bounded device waits, on its own (the   */
+/* pages describe no failure handling; this is a check of the library).  One */
+/* warp allocates 32 TMEM columns, waits on an mbarrier that nothing ever     */
+/* arrives on, gives up after limit_ns nanoseconds of global time, records  */
+/* DG_ERR_TIMEOUT in the workspace's status word, frees its TMEM and         */
+/* returns -- the way every kernel of the library winds down when a wait     */
+/* runs out.  The context stays usable.  limit_ns in [1000, 1e9].  Errors:   */
+/* DG_ERR_WORKSPACE (workspace missing or < 256 B), DG_ERR_INVALID_ARG,      */
+/* DG_ERR_ALIGNMENT, DG_ERR_CUDA.                                            */
+int dg_wait_timeout_probe(void *workspace, size_t workspace_bytes, uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -146,3 +146,13 @@ def test_fp8_entry_points_validate_before_launch(lib):
     assert lib.dg_quantize_rows_e4m3(None, 4, 4, _vp(good), _vp(good), None) == 1
     assert lib.dg_quantize_rows_e4m3(_vp(good), 0, 4, _vp(good), _vp(good), None) == 1
     assert lib.dg_quantize_weight_e4m3(_vp(good), 0, 64, _vp(good), _vp(good), None) == 1
+
+
+def test_wait_probe_rejects_bad_arguments_before_launch(lib):
+    buf = ctypes.create_string_buffer(512)
+    addr = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.dg_wait_timeout_probe(None, 256, 1000000, None) == 4          # no workspace
+    assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr), 128, 1000000, None) == 4
+    assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr), 256, 10, None) == 1
+    assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr), 256, 2 * 10**9, None) == 1
+    assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr + 4), 256, 1000000, None) == 3

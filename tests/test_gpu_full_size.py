@@ -190,7 +190,8 @@ def test_block_full_converging_final_steps_match_oracle():
     cap (entropies fall with the step); at the step it stopped on, the oracle's
     step on the same hidden states and temperature gives the reported mean
     entropy and argmax, its stop test fires, and the argmax equals the
-    oracle's argmax of the step before."""
+    oracle's argmax of the step before; at the step before that, the oracle's
+    stop test does not fire (so the loop stopped neither early nor late)."""
     cfg = dg_synth.CONFIGS["block_full"]
     wb = _weight("block_full")
     N = cfg.max_steps
@@ -218,3 +219,15 @@ def test_block_full_converging_final_steps_match_oracle():
     r_prev = oracle_sampler(last - 1)
     ok &= r_prev["argmax_margin"] >= MARGIN
     assert np.array_equal(am[ok], r_prev["argmax"][ok])
+    # the loop did not stop one step early: the oracle's stop test at step
+    # last - 1 (against the argmax of step last - 2) does not fire, and the
+    # decision is clear of the entropy tolerance
+    if last >= 2:
+        r_pp = oracle_sampler(last - 2)
+        H32p = r_prev["H"].astype(np.float32)
+        st = oracle.stop(r_prev["argmax"], r_pp["argmax"], H32p, last - 1, cfg.stop_threshold)
+        assert st["stop"] == 0
+        argmax_moved_clearly = bool(np.any((r_prev["argmax"] != r_pp["argmax"])
+                                           & (r_prev["argmax_margin"] >= MARGIN)
+                                           & (r_pp["argmax_margin"] >= MARGIN)))
+        assert argmax_moved_clearly or st["mean_entropy"] >= cfg.stop_threshold + 2 * H_TOL

@@ -455,31 +455,32 @@ def test_block_one_hot_stops_after_two_steps_and_batches_independently():
 
 def test_block_converging_matches_oracle():
     """A small version of the converging block workload: per-position targets and
-    confidences, hidden states sharpen with the step.  Every step whose decisions
-    are clear of their margins must commit what the oracle commits; if all are
-    clear the stop step, the final canvas and the argmax output must match too."""
-    cfg = dg_synth.StepConfig("blk", L=64, d=256, V=2048, w_std=0.02, seed=3)
+    confidences, hidden states sharpen with the step.  The data seed is one on
+    which every decision of the oracle's run is clear of its margin at every
+    step (asserted below on the oracle alone), so the loop must reproduce the
+    oracle's run exactly: commits per step, the stop step, the final canvas
+    and the argmax output."""
+    cfg = dg_synth.StepConfig("blk", L=64, d=256, V=2048, w_std=0.02, seed=18)
     wb = dg_synth.lm_weight(cfg)
     tg = dg_synth.block_targets(cfg)
     N = 48
     hs = np.stack([dg_synth.block_hidden(cfg, wb, tg, k) for k in range(N)])
     ref = oracle.block(lambda k: hs[k], wb, 1, cfg.L, 0.1, 9, max_steps=N)
-    bufs = _run_block(hs, wb, 1, cfg.L, cfg.d, cfg.V, seed=9, max_steps=N)
-    steps = int(bufs.steps_taken[0])
-    assert 1 <= steps <= N
-    hist = np_i32(bufs.n_accepted_hist)
-    clear_steps = []
-    for k, h in enumerate(ref["history"][:steps]):
+    n_ref = int(ref["steps"][0])
+    assert 2 <= n_ref < N
+    for k, h in enumerate(ref["history"]):
         acc = np.zeros(cfg.L, bool)
         acc[h["order"][0][: int(h["n_accepted"][0])]] = True
-        clear = (acceptance_is_decided(h["H32"], int(h["n_accepted"][0]), float(h["boundary_gap"][0]))
-                 and bool((h["gumbel_margin"][acc] >= MARGIN).all())
-                 and bool((h["argmax_margin"] >= MARGIN).all()))
-        if clear:
-            clear_steps.append(k)
-            assert hist[k] == int(h["n_accepted"][0]), k
-    assert len(clear_steps) >= len(ref["history"]) // 2
-    if len(clear_steps) == len(ref["history"]):
-        assert steps == int(ref["steps"][0])
-        assert np.array_equal(np_i32(bufs.argmax), ref["argmax"])
-        assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
+        assert acceptance_is_decided(h["H32"], int(h["n_accepted"][0]),
+                                     float(h["boundary_gap"][0])), k
+        assert (h["gumbel_margin"][acc] >= MARGIN).all(), k
+        assert (h["argmax_margin"] >= MARGIN).all(), k
+        assert abs(float(h["mean_entropy"][0]) - 0.005) >= 2 * H_TOL, k
+    bufs = _run_block(hs, wb, 1, cfg.L, cfg.d, cfg.V, seed=9, max_steps=N)
+    assert int(bufs.steps_taken[0]) == n_ref
+    hist = np_i32(bufs.n_accepted_hist)
+    assert hist[:n_ref].tolist() == [int(h["n_accepted"][0]) for h in ref["history"]]
+    assert np.array_equal(np_i32(bufs.argmax), ref["argmax"])
+    assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
+    last = ref["history"][-1]
+    assert abs(float(bufs.mean_entropy[0]) - float(last["mean_entropy"][0])) < H_TOL

@@ -178,6 +178,84 @@ def test_gumbel_score_definition():
     assert s["sample"] == int(np.argmax(score))
 
 
+def _brute_top_two(scores):
+    """Largest score, its lowest index, and the gap to the runner-up (a tie
+    for the top gives 0), by sorting a copy."""
+    sc = np.asarray(scores, np.float64)
+    top = float(sc.max())
+    first = int(np.nonzero(sc == top)[0][0])
+    srt = np.sort(sc)
+    return first, float(srt[-1] - srt[-2]) if sc.shape[0] > 1 else math.inf
+
+
+def test_gumbel_margin_brute_force():
+    """The Gumbel-max margin is the gap between the two largest fp32 scores.  At
+    T = 1 (fp32(1/T) = 1) the score fmaf(logit, 1, G) is one fp32 addition, which
+    numpy computes exactly the same way; the top two come from a sort."""
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        V = int(rng.integers(2, 300))
+        seed, row, step = int(rng.integers(0, 2**40)), int(rng.integers(0, 4096)), int(rng.integers(0, 48))
+        x = (rng.standard_normal(V) * rng.uniform(0.1, 6.0)).astype(np.float32)
+        G = oracle.gumbel_fill(seed, row, step, 0, V)
+        score = x + G                               # fp32 + fp32, rounded once
+        if trial % 4 == 0:
+            # plant a tie for the top: a later column reaches the same score
+            a = int(np.argmax(score))
+            b = (a + 1 + int(rng.integers(0, V - 1))) % V
+            xb = np.float32(score[a] - G[b])
+            if np.float32(xb + G[b]) == score[a]:
+                x[b] = xb
+                score = x + G
+        s = oracle.sampler_row(x.astype(np.float64), 1.0, seed, row, step)
+        first, gap = _brute_top_two(score)
+        assert s["sample"] == first
+        assert s["gumbel_margin"] == gap
+        if trial % 4 == 0 and (score == score.max()).sum() > 1:
+            assert s["gumbel_margin"] == 0.0
+
+
+def test_gumbel_margin_at_other_temperatures():
+    """At T != 1 the brute force forms the score in float64 (the fp32 product
+    is exact there) and rounds it to fp32: within one fp32 rounding of the
+    oracle's fused score, so margins agree to a few ulps of the scores."""
+    rng = np.random.default_rng(12)
+    for T in (0.8, 0.5, 0.4123):
+        V = 257
+        x = (rng.standard_normal(V) * 3.0).astype(np.float32)
+        G = oracle.gumbel_fill(5, 3, 2, 0, V)
+        invT = np.float64(np.float32(1.0 / T))
+        score = (x.astype(np.float64) * invT + G.astype(np.float64)).astype(np.float32)
+        s = oracle.sampler_row(x.astype(np.float64), T, 5, 3, 2)
+        _, gap = _brute_top_two(score)
+        tol = 4 * float(np.spacing(np.float32(np.abs(score).max())))
+        assert abs(s["gumbel_margin"] - gap) <= tol
+
+
+def _brute_boundary_gap(H, b):
+    """min over prefix lengths 1 .. L-1 of the (H, position)-sorted order of
+    |exact sum of the prefix - b| (math.fsum: correctly rounded)."""
+    order = sorted(range(len(H)), key=lambda i: (float(np.float32(H[i])), i))
+    vals = [float(np.float32(H[i])) for i in order]
+    return min((abs(math.fsum(vals[:j]) - b) for j in range(1, len(vals))), default=math.inf)
+
+
+def test_boundary_gap_brute_force():
+    rng = np.random.default_rng(13)
+    for trial in range(50):
+        L = int(rng.integers(2, 80))
+        H = rng.exponential(rng.uniform(0.005, 0.2), L).astype(np.float32)
+        b = float(rng.choice([0.0, 0.05, 0.1, 0.3]))
+        r = _accept(H, b=b)
+        assert abs(r["boundary_gap"] - _brute_boundary_gap(H, b)) < 1e-12
+    # a prefix that sums to b exactly (dyadic entropies): the gap is 0 and the
+    # prefix is accepted (the rule is <= b)
+    H = np.array([0.25, 0.125, 0.5, 0.0625, 2.0], np.float32)
+    r = _accept(H, b=0.4375)       # 0.0625 + 0.125 + 0.25 = 0.4375
+    assert r["boundary_gap"] == 0.0
+    assert r["n_accepted"] == 4    # the sum before the 4th sorted entry is exactly b
+
+
 # ------------------------------------------------------------------ acceptance
 def _accept(H, b=0.1, L=None, V=1 << 14, seed=0, step=0):
     H = np.asarray(H, np.float32)
