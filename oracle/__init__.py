@@ -100,6 +100,8 @@ def lib():
         L.orc_quantize_rows_e4m3.restype = None
         L.orc_gumbel_fill.argtypes = [_c_u64, _c_u32, _c_u32, _c_u32, _c_i32, _vp]
         L.orc_gumbel_fill.restype = None
+        L.orc_self_cond_row.argtypes = [_vp, _c_i32, _c_dbl, _vp, _c_i32, _vp]
+        L.orc_self_cond_row.restype = None
         _lib = L
     return _lib
 
@@ -242,6 +244,32 @@ def stop(argmax: np.ndarray, prev_argmax: np.ndarray, H: np.ndarray, step: int,
     s = lib().orc_stop(_ptr(a), _ptr(p), _ptr(Hf), a.shape[0], step, float(threshold),
                        ctypes.byref(mean))
     return dict(stop=int(s), mean_entropy=mean.value)
+
+
+def self_cond(logits_rows: np.ndarray, T: float, E: np.ndarray, workers: int = 1) -> np.ndarray:
+    """Self-conditioning read-out sc[i] = sum_v softmax(logits_i / T)_v E[v, :] (fp64)
+    for every row of a block of fp64 logits; E is the fp32 table [V, R].
+
+    Rows are independent; ``workers`` > 1 runs them on that many threads
+    (identical results)."""
+    lg = np.ascontiguousarray(np.asarray(logits_rows, dtype=np.float64))
+    Et = np.ascontiguousarray(np.asarray(E, dtype=np.float32))
+    n, V = lg.shape
+    R = Et.shape[1]
+    assert Et.shape[0] == V
+    out = np.zeros((n, R), dtype=np.float64)
+
+    def one(t):
+        lib().orc_self_cond_row(_ptr(lg[t]), V, float(T), _ptr(Et), R, _ptr(out[t]))
+
+    if workers > 1 and n > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, range(n)))
+    else:
+        for t in range(n):
+            one(t)
+    return out
 
 
 # ---------------------------------------------------------------- attention

@@ -447,3 +447,34 @@ void orc_quantize_rows_e4m3(const uint16_t *x, int64_t rows, int64_t cols, uint8
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Self-conditioning read-out of one canvas row.                        */
+/* [PD] "Finding", architecture paragraph: a small self-conditioning    */
+/* block (7.8M parameters) feeds the previous step's prediction back    */
+/* into the model; the hardware paragraph places its matmul, in full    */
+/* precision, in the sampling stage next to the full-vocabulary softmax.*/
+/* Reading: the fed-back prediction is the expected embedding under the */
+/* step's sampling distribution,                                        */
+/*   sc[j] = sum_v softmax(logits / T)_v E[v, j],   j < R,              */
+/* with a table E [V, R] (V R = 262144 x 30 = 7.86M at the full vocab-  */
+/* ulary).  fp64 throughout: the softmax weights exp(z_v - zmax) / S    */
+/* with z = logits / T, then the weighted sum over v in order.          */
+/* ------------------------------------------------------------------ */
+void orc_self_cond_row(const double *logits, int32_t V, double T, const float *E, int32_t R,
+                       double *sc_out)
+{
+    double zmax = -INFINITY;
+    for (int32_t v = 0; v < V; ++v) {
+        double z = logits[v] / T;
+        if (z > zmax) zmax = z;
+    }
+    double S = 0.0;
+    for (int32_t j = 0; j < R; ++j) sc_out[j] = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+        double e = exp(logits[v] / T - zmax);
+        S += e;
+        for (int32_t j = 0; j < R; ++j) sc_out[j] += e * (double)E[(int64_t)v * R + j];
+    }
+    for (int32_t j = 0; j < R; ++j) sc_out[j] /= S;
+}

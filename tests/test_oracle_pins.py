@@ -559,3 +559,44 @@ def test_fp8_logits_exact_on_small_integers():
     got = oracle.logits_fp8(x8, np.ones(5, np.float32), w8t, np.ones(40, np.float32), col_chunk=7)
     assert np.array_equal(got, X.astype(np.float64) @ W.astype(np.float64))
 
+
+
+# ------------------------------------------------------------------ self-conditioning read-out
+def test_self_cond_uniform_logits_give_the_mean_row():
+    """Equal logits: every token has weight 1/V, so the read-out is the mean of E's rows."""
+    rng = np.random.default_rng(21)
+    V, R = 1000, 30
+    E = rng.standard_normal((V, R)).astype(np.float32)
+    sc = oracle.self_cond(np.full((3, V), 2.5), 0.8, E)
+    ref = E.astype(np.float64).mean(axis=0)
+    assert np.abs(sc - ref).max() < 1e-12
+
+
+def test_self_cond_one_hot_picks_the_row():
+    """One logit 1e4 above the rest: every other weight underflows to 0 in fp64,
+    so the read-out is that token's row of E, exactly."""
+    rng = np.random.default_rng(22)
+    V, R = 777, 32
+    E = rng.standard_normal((V, R)).astype(np.float32)
+    lg = rng.standard_normal((4, V))
+    hot = [0, 5, 776, 300]
+    for i, v in enumerate(hot):
+        lg[i, v] = 1e4
+    sc = oracle.self_cond(lg, 0.4, E)
+    assert np.array_equal(sc, E[hot].astype(np.float64))
+
+
+def test_self_cond_matches_torch_softmax_matmul():
+    """Against torch in float64: softmax(logits / T) @ E (a library routine)."""
+    rng = np.random.default_rng(23)
+    V, R, T = 4096, 30, 0.8
+    E = rng.standard_normal((V, R)).astype(np.float32)
+    lg = rng.standard_normal((5, V)) * np.array([0.1, 1.0, 5.0, 20.0, 60.0])[:, None]
+    sc = oracle.self_cond(lg, T, E)
+    ref = (torch.softmax(torch.from_numpy(lg) / T, dim=1)
+           @ torch.from_numpy(E.astype(np.float64))).numpy()
+    assert np.abs(sc - ref).max() < 1e-12 * max(1.0, np.abs(ref).max())
+    # the weights sum to one: a constant column of E reads out as that constant
+    E2 = np.ones((V, 2), np.float32)
+    E2[:, 1] = 3.0
+    assert np.abs(oracle.self_cond(lg, T, E2) - np.array([1.0, 3.0])).max() < 1e-12
