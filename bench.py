@@ -149,7 +149,8 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- oracle sample
-def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0, fp8=False):
+def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0, fp8=False,
+                         sc_table=None):
     """Time the CPU oracle on a bounded sample of one step and scale it to the full step.
 
     Sample: every canvas row of the LM head + sampler against the first v_sample
@@ -171,6 +172,8 @@ def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0, 
     else:
         lg = oracle.logits(xb, w_s)
     s = oracle.sampler(lg, cfg.temperature, seed, np.arange(cfg.M), 1)
+    if sc_table is not None:
+        oracle.self_cond(lg, cfg.temperature, np.ascontiguousarray(sc_table[:vs]))
     t_lm = time.perf_counter() - t0
     rows = np.linspace(0, cfg.B * cfg.L * cfg.Hq - 1, attn_rows).astype(np.int64)
     t0 = time.perf_counter()
@@ -188,9 +191,11 @@ def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0, 
     t_acc = time.perf_counter() - t0
     full = t_lm * (cfg.V / vs) + t_at * (cfg.B * cfg.L * cfg.Hq / len(rows)) + t_acc
     desc = ("oracle (fp64 C + numpy fp64 matmul, 1 thread): all %d canvas rows x %d of %d vocab "
-            "columns (%sLM head + sampler, scaled x%.0f), %d of %d attention rows (scaled), "
+            "columns (%sLM head + sampler%s, scaled x%.0f), %d of %d attention rows (scaled), "
             "acceptance + stop on the full canvas" % (cfg.M, vs, cfg.V,
                                                       "E4M3 quantisation + " if fp8 else "",
+                                                      " + self-conditioning read-out"
+                                                      if sc_table is not None else "",
                                                       cfg.V / vs, len(rows),
                                                       cfg.B * cfg.L * cfg.Hq))
     return full, desc, dict(t_lm=t_lm, t_attn=t_at, t_accept=t_acc)
@@ -234,12 +239,14 @@ def run_reference(args, cfg):
     return 0
 
 
-def _config_json(cfg, l2, lm_dtype="bf16"):
+def _config_json(cfg, l2, lm_dtype="bf16", self_cond=False):
     return {"workload": "%s: single denoising step, B=%d L=%d, attention Hq=%d Hkv=%d D=%d "
-                        "P=%d, LM head d=%d V=%d%s, T=%.1f b=%.1f" % (
+                        "P=%d, LM head d=%d V=%d%s%s, T=%.1f b=%.1f" % (
                             cfg.name, cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V,
                             " (E4M3 operands, per-row / per-column scales)"
                             if lm_dtype == "fp8" else "",
+                            " + self-conditioning read-out (fp32 table [V, 32])"
+                            if self_cond else "",
                             cfg.temperature, cfg.entropy_bound),
             "global_batch": cfg.B, "seq_len": cfg.L, "parallelism": "replicas", "l2": l2}
 
@@ -331,6 +338,13 @@ def run_ours(args, cfg):
     p0 = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 0,
                         seed=rank)
     fp8 = args.lm_dtype == "fp8"
+    sc = args.self_cond
+    if sc:
+        # the self-conditioning table E [V, 32] fp32 (30 meaningful columns,
+        # V x 30 = 7.86M parameters at V = 262144) and the read-out [M, 32]
+        sc_table = torch.randn(V, 32, device=dev, generator=g) / math.sqrt(d)
+        sc_table[:, 30:] = 0
+        sc_out = torch.empty(M, 32, device=dev)
     if fp8:
         # load-time conversion of W to E4M3 codes [V, d] + column scales (not timed);
         # the hidden states are quantised inside every step
@@ -338,6 +352,8 @@ def run_ours(args, cfg):
         w_scale = torch.empty(V, dtype=torch.float32, device=dev)
         dg.quantize_weight_e4m3(w, w8, w_scale)
         sws = dg.workspace(dg.denoise_step_fp8_workspace(p0), dev)
+    elif sc:
+        sws = dg.workspace(dg.denoise_step_sc_workspace(p0), dev)
     else:
         sws = dg.workspace(dg.denoise_step_workspace(p0), dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
@@ -346,12 +362,16 @@ def run_ours(args, cfg):
     def lm_step(p):
         if fp8:
             dg.denoise_step_fp8(x, w8, w_scale, p, bufs, sws)
+        elif sc:
+            dg.denoise_step_sc(x, w, sc_table, p, bufs, sc_out, sws)
         else:
             dg.denoise_step(x, w, p, bufs, sws)
 
     def lm_fold():
         if fp8:
             dg.lm_head_fold_fp8(x, w8, w_scale, p0, sws)
+        elif sc:
+            dg.lm_head_fold_sc(x, w, sc_table, p0, sws)
         else:
             dg.lm_head_fold(x, w, p0, sws)
 
@@ -398,8 +418,9 @@ def run_ours(args, cfg):
     lm_ms = statistics.mean(timed(lambda k: lm_fold(), args.steps, 0))
     at_ms = statistics.mean(timed(lambda k: dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale,
                                                            aws), args.steps, 0))
-    # FP8: W codes + column scales, and the bf16 hidden states read by the row quantisation
-    lm_bytes = (d * V + 4 * V if fp8 else d * V * 2) + M * d * 2
+    # FP8: W codes + column scales, and the bf16 hidden states read by the row quantisation;
+    # self-conditioning: + the fp32 table E [V, 32]
+    lm_bytes = (d * V + 4 * V if fp8 else d * V * 2) + M * d * 2 + (V * 32 * 4 if sc else 0)
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
     lm_flops = 2.0 * M * d * V
     # E4M3 runs at twice the bf16 rate (nominal dense ratio 4.5 / 2.25 PFLOP/s)
@@ -409,6 +430,8 @@ def run_ours(args, cfg):
     lm_plan = dg.lm_head_plan(M, d, V)
     if fp8:
         lm_plan = dict(lm_plan, kernel="lm_head_duo_fp8_kernel")
+    if sc:
+        lm_plan = dict(lm_plan, kernel="lm_head_duo_sc_kernel")
     srcs = [os.path.join(ROOT, "block_diffusion_decoding_gb300", "csrc", f)
             for f in ("dg_lm_head.cu", "dg_lm_head_duo.cu", "dg_plan.h",
                       "dg_sampler.cuh", "dg_device.cuh", "dg_kernels.h")]
@@ -451,9 +474,11 @@ def run_ours(args, cfg):
                 "vp": vp.view(torch.int16).cpu().numpy().view(np.uint16),
                 "kc": kc.view(torch.int16).cpu().numpy().view(np.uint16),
                 "vc": vc.view(torch.int16).cpu().numpy().view(np.uint16)}
-        est = [oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8)[0]
-               for _ in range(2)]
-        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8)
+        sc_host = sc_table[:16384].cpu().numpy() if sc else None
+        est = [oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8,
+                                    sc_table=sc_host)[0] for _ in range(2)]
+        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8,
+                                          sc_table=sc_host)
         cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle",
                    sample=desc)
     if world > 1:
@@ -485,7 +510,7 @@ def run_ours(args, cfg):
         higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="e4m3 LM head (fp32 accumulate), bf16 attention" if fp8 else "bf16",
         data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step",
-                                              lm_dtype=args.lm_dtype),
+                                              lm_dtype=args.lm_dtype, self_cond=sc),
         canvas_tokens_per_s=value * M,
         roofline=roof,
         kernels={lm_plan["kernel"]: {"ms": lm_ms, "GB_per_s": lm_gbs, "TFLOP_per_s": lm_tflops,
@@ -845,6 +870,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="LM-head operands: bf16, or E4M3 codes with per-row / per-column scales")
+    ap.add_argument("--self-cond", action="store_true",
+                    help="the step with the self-conditioning read-out folded into the LM head")
     ap.add_argument("--kernel", choices=["attention", "lm_head"],
                     help="run one kernel of the step alone (for profilers), not the benchmark")
     args = ap.parse_args()

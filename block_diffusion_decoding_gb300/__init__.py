@@ -35,7 +35,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_lm_head_fold", "dg_kernel_launches", "dg_lm_head_plan", "dg_gumbel_fill",
             "dg_logf_eval", "dg_quantize_rows_e4m3", "dg_quantize_weight_e4m3",
             "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8",
-            "dg_wait_timeout_probe"]
+            "dg_wait_timeout_probe", "dg_denoise_step_sc_workspace", "dg_denoise_step_sc",
+            "dg_lm_head_fold_sc"]
 
 
 class DgError(RuntimeError):
@@ -112,6 +113,9 @@ def _lib():
             "dg_denoise_step_fp8": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
             "dg_lm_head_fold_fp8": ([vp, vp, vp, sp, vp, sz, vp], i32),
             "dg_wait_timeout_probe": ([vp, sz, u64, vp], i32),
+            "dg_denoise_step_sc_workspace": ([sp], sz),
+            "dg_denoise_step_sc": ([vp, vp, vp, sp, si, vp, vp, sz, vp], i32),
+            "dg_lm_head_fold_sc": ([vp, vp, vp, sp, vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -235,6 +239,30 @@ def lm_head_plan(rows: int, d: int, V: int) -> dict:
         name = "lm_head_kernel"
     return {"kernel": name, "kind": kind.value, "BN": bn.value, "ctas": ctas.value,
             "fused": kind.value == 3, "epilogue_warps": epi.value}
+
+
+# ---------------------------------------------------------------- self-conditioning step
+SC_DIM = 32
+
+
+def denoise_step_sc_workspace(p: StepParams) -> int:
+    return int(_lib().dg_denoise_step_sc_workspace(ctypes.byref(p)))
+
+
+def denoise_step_sc(hidden, w, sc_table, p: StepParams, bufs: StepBuffers, sc_out, workspace,
+                    stream=None):
+    """dg_denoise_step_sc: sc_table [V, 32] fp32, sc_out [B*L, 32] fp32."""
+    io = bufs.io()
+    rc = _lib().dg_denoise_step_sc(_p(hidden), _p(w), _p(sc_table), ctypes.byref(p),
+                                   ctypes.byref(io), _p(sc_out), _p(workspace), workspace.numel(),
+                                   _stream(stream))
+    _check(rc, "dg_denoise_step_sc")
+
+
+def lm_head_fold_sc(hidden, w, sc_table, p: StepParams, workspace, stream=None):
+    rc = _lib().dg_lm_head_fold_sc(_p(hidden), _p(w), _p(sc_table), ctypes.byref(p),
+                                   _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_lm_head_fold_sc")
 
 
 # ---------------------------------------------------------------- FP8 LM head

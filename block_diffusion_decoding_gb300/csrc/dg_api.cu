@@ -77,6 +77,9 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_wide_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_sc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDuoScSmemBytes));
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_fp8_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
@@ -260,12 +263,20 @@ struct Fp8Operands {
     const float *sw;
 };
 
+// Self-conditioning read-out of the step: the table E [V, kScDim], the
+// per-(row, unit) parts in the workspace and the read-out [M, kScDim].
+struct ScOperands {
+    const float *table;
+    float *part;
+    float *out;
+};
+
 // Enqueue LM head (or logits fold) + combine/accept for one step.
 int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, const float *logits,
                  const uint16_t *w, const dg_step_params *p, const LmPlan &plan, StepWs &ws,
                  const StepSource &src, float *H, int32_t *sample, int32_t *argmax,
                  const AcceptArgs &acc, cudaStream_t st, bool lm_only = false,
-                 const Fp8Operands *f8 = nullptr)
+                 const Fp8Operands *f8 = nullptr, const ScOperands *sco = nullptr)
 {
     const int M = p->B * p->L;
     const bool pdl = use_pdl(st);
@@ -344,6 +355,10 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         a.ncounters = p->B;
         a.rowkey = ws.rowkey;
         a.fuse2 = plan.kind == kLmDuoFused ? 1 : 0;
+        if (sco != nullptr) {
+            a.sc_table = sco->table;
+            a.sc_part = sco->part;
+        }
         DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl));
         DG_LAUNCHED();
     } else {
@@ -376,6 +391,10 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
     c.argmax = argmax;
     c.counters = ws.counters;
     c.rows_per_cta = combine_rows_per_cta(p->B, p->L, plan.sms);
+    if (sco != nullptr) {
+        c.sc_part = sco->part;
+        c.sc_out = sco->out;
+    }
     DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + c.rows_per_cta - 1) / c.rows_per_cta, p->B), dim3(kAcceptThreads), 0, st,
                               pdl, c, acc));
     DG_LAUNCHED();
@@ -670,6 +689,51 @@ int fp8_step(const uint16_t *hidden, const uint8_t *w8t, const float *w_scale,
                         io->argmax, acc, st, false, &f8);
 }
 
+// Workspace of the self-conditioning step: the step's | SC parts
+// [M][slots][kScDim] fp32.
+size_t sc_ws_bytes(const dg_step_params *p, size_t *off_sc)
+{
+    const size_t M = static_cast<size_t>(p->B) * p->L;
+    const int slots = slot_bound(static_cast<int>(M), p->V);
+    const size_t off = round_up(step_ws_bytes(static_cast<int>(M), p->B, slots), 256);
+    if (off_sc) *off_sc = off;
+    return off + round_up(static_cast<size_t>(slots) * M * kScDim * 4, 256);
+}
+
+int sc_step(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+            const dg_step_params *p, const dg_step_io *io, float *sc_out, void *workspace,
+            size_t workspace_bytes, void *stream, bool lm_only)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if (!lm_only && (rc = check_io(io, true)) != DG_OK) return rc;
+    if (!hidden || !w || !sc_table || (!lm_only && !sc_out)) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(w) || !aligned16(sc_table) ||
+        (!lm_only && !aligned16(sc_out)))
+        return DG_ERR_ALIGNMENT;
+    size_t off_sc = 0;
+    const size_t need = sc_ws_bytes(p, &off_sc);
+    if (workspace == nullptr || workspace_bytes < need) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    const int M = p->B * p->L;
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, false, true);
+    StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
+    ScOperands sco{sc_table, reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + off_sc),
+                   sc_out};
+    const StepSource src = step_source(p);
+    if (lm_only) {
+        AcceptArgs acc{};
+        return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, nullptr, nullptr, nullptr,
+                            acc, as_stream(stream), true, nullptr, &sco);
+    }
+    const AcceptArgs acc = accept_args(p, io);
+    return enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
+                        io->argmax, acc, as_stream(stream), false, nullptr, &sco);
+}
+
 }  // namespace
 
 extern "C" {
@@ -879,6 +943,28 @@ int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas, int *
     if (ctas) *ctas = plan.grid;
     if (epilogue_warps) *epilogue_warps = plan.epi_warps;
     return DG_OK;
+}
+
+// ---------------------------------------------------------------- self-conditioning step
+size_t dg_denoise_step_sc_workspace(const dg_step_params *p)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    return sc_ws_bytes(p, nullptr);
+}
+
+int dg_denoise_step_sc(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+                       const dg_step_params *p, const dg_step_io *io, float *sc_out,
+                       void *workspace, size_t workspace_bytes, void *stream)
+{
+    return sc_step(hidden, w, sc_table, p, io, sc_out, workspace, workspace_bytes, stream, false);
+}
+
+int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+                       const dg_step_params *p, void *workspace, size_t workspace_bytes,
+                       void *stream)
+{
+    return sc_step(hidden, w, sc_table, p, nullptr, nullptr, workspace, workspace_bytes, stream,
+                   true);
 }
 
 // ---------------------------------------------------------------- sampler on given logits

@@ -37,6 +37,10 @@ struct CombineArgs {
     int32_t *argmax;
     int *counters;      // [B] last-CTA counters, zeroed by the producer kernel
     int rows_per_cta;   // canvas rows merged per combine CTA (<= 32)
+    // self-conditioning: per-(row, unit) parts [M][n_slots][kScDim] in, the
+    // read-out sc [M][kScDim] out; both null without it
+    const float *sc_part;
+    float *sc_out;
 };
 
 struct AcceptArgs {
@@ -84,6 +88,10 @@ struct LmHeadArgs {
     // one launch ([M] order-preserving keys, 0 = none; all 0 between
     // launches); null: not shared
     uint32_t *rowkey;
+    // self-conditioning read-out (lm_head_duo_sc_kernel only): table E
+    // [V, kScDim] fp32 and the per-(row, unit) parts [M][units][kScDim]
+    const float *sc_table;
+    float *sc_part;
 };
 
 // LM-head kernel geometry
@@ -135,6 +143,11 @@ __global__ void lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
 // the same kernel with 16 epilogue warps (several row blocks)
 __global__ void lm_head_duo_wide_kernel(const __grid_constant__ CUtensorMap map_x,
                                         const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+// The 8-epilogue-warp kernel with the self-conditioning read-out folded in
+// (its column groups merge kScDim more words per row through shared memory).
+constexpr int kDuoScSmemBytes = kDuoSmemBytes + (kDuoCGNarrow - 1) * kScDim * 128 * 4;
+__global__ void lm_head_duo_sc_kernel(const __grid_constant__ CUtensorMap map_x,
+                                      const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
 // FP8 (E4M3) operands of the 2-SM kernel: X8 [M, d] and W8t [V, d] (both
 // K-major, 128-byte k blocks = 128 codes); same tiles, 256 x 256 x 32 UMMAs.
 __global__ void lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,

@@ -33,6 +33,11 @@
 //               in shared memory and one partial state per (row, cluster)
 //               is stored.
 //
+// The self-conditioning instance (lm_head_duo_sc_kernel, 8 epilogue warps)
+// folds sc = sum_v softmax(logits / T)_v E[v, :] along with the softmax
+// statistics (dg_sampler.cuh) and stores one unnormalised part per (row,
+// cluster) next to the partial state.
+//
 // The FP8 instance (lm_head_duo_fp8_kernel) takes E4M3 codes of the hidden
 // block X8 [M, d] and of the transposed weight W8t [V, d], both K-major: a
 // k block is 128 codes (the same 128 bytes per row as 64 bf16 values), the
@@ -56,7 +61,7 @@ DG_DEVICE int duo_tile_span(const LmHeadArgs &a, int t, int t1)
 // TMEM columns between the two accumulator buffers (the widest tile)
 constexpr int kDuoAccCols = 256;
 
-template <bool kFp8, int kCG>
+template <bool kFp8, int kCG, bool kSC = false>
 DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map_w,
                                 const LmHeadArgs &a)
 {
@@ -75,6 +80,9 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     constexpr int EpiWarps = DuoEpilogue<kCG>::Warps;
     const GroupMerge gm{reinterpret_cast<float *>(smem + kDuoStages * kDuoStageBytes + 256),
                         mrg_ready, mrg_done, CG, 128};
+    const ScMerge sm{reinterpret_cast<float *>(smem + kDuoStages * kDuoStageBytes + 256 +
+                                               kPairMergeBytes),
+                     a.sc_part};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = static_cast<int>(cluster_ctarank());          // row / column half
@@ -248,6 +256,8 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
         uint32_t merges = 0;
         RowState st;
         row_state_init(st);
+        ScAcc sc;
+        if constexpr (kSC) sc_init(sc);
         int cur_m = -1;
         int i = 0;
         for (int t = t0, span = 1; t < t1; t += span, ++i) {
@@ -260,10 +270,12 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                 if (cur_m >= 0) {
                     const int prow = cur_m * kRowsPerBlock + r * 128 + rix;
                     row_state_finalize(st, fc);
-                    group_merge_store(st, cg, rix, merges++, gm, a.part,
-                                      static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws);
+                    group_merge_store_t<kSC>(st, cg, rix, merges++, gm, a.part,
+                                             static_cast<size_t>(prow) * ncl + cid, prow < a.M,
+                                             a.ws, &sc, sm);
                 }
                 row_state_init(st);
+                if constexpr (kSC) sc_init(sc);
                 cur_m = m;
             }
             const int row = m * kRowsPerBlock + r * 128 + rix;
@@ -281,7 +293,11 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             tc_fence_after();
             st.glb = fmaxf(st.glb, key_score(key));
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * kDuoAccCols);
-            if constexpr (kFp8) {
+            if constexpr (kSC) {
+                fold_tile_sc(st, sc, a.sc_table, tb, 16 * cg, 16 * CG, bn,
+                             static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
+                             static_cast<uint32_t>(row), fc, live);
+            } else if constexpr (kFp8) {
                 const float rs = live ? __ldg(a.row_scale + row) : 0.f;
                 fold_tile_scaled(st, tb, 16 * cg, 16 * CG, bn,
                                  static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
@@ -308,8 +324,9 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
         if (cur_m >= 0) {
             const int prow = cur_m * kRowsPerBlock + r * 128 + rix;
             row_state_finalize(st, fc);
-            group_merge_store(st, cg, rix, merges, gm, a.part,
-                              static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws);
+            group_merge_store_t<kSC>(st, cg, rix, merges, gm, a.part,
+                                     static_cast<size_t>(prow) * ncl + cid, prow < a.M, a.ws,
+                                     &sc, sm);
         }
     }
     tc_fence_before();
@@ -349,6 +366,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWi
                             const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
 {
     lm_head_duo_body<false, kDuoCGWide>(map_x, map_w, a);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGNarrow>::Threads, 1)
+    lm_head_duo_sc_kernel(const __grid_constant__ CUtensorMap map_x,
+                          const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+{
+    lm_head_duo_body<false, kDuoCGNarrow, true>(map_x, map_w, a);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWide>::Threads, 1)

@@ -35,6 +35,7 @@ struct LmPlan {
     int grid;         // CTAs launched
     int sms;          // SMs of the device the plan was made for
     int epi_warps;    // epilogue warps of the 2-SM kernel (8 or 16; 0 otherwise)
+    bool sc;          // the self-conditioning instance (lm_head_duo_sc_kernel)
     int part_slots() const { return units; }
     bool cluster() const { return kind != kLmSingle; }
     bool duo() const { return kind == kLmDuo || kind == kLmDuoFused; }
@@ -45,7 +46,7 @@ struct LmPlan {
 // single 256-row block of bf16 operands, else 16.  DG_LM_KERNEL=single|duo|
 // fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
 // have the 2-SM UMMA kernel only.
-inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
+inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool sc = false)
 {
     LmPlan best{};
     best.M = M;
@@ -61,13 +62,14 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
                      : std::strcmp(env_k, "duo") == 0    ? kLmDuo
                      : std::strcmp(env_k, "fused") == 0  ? kLmDuoFused
                                                          : -1;
-    // a forced kernel FP8 operands do not have is ignored
-    const int only = fp8 && only_env != kLmDuo && only_env != kLmDuoFused ? -1 : only_env;
+    // a forced kernel FP8 operands or the self-conditioning read-out do not
+    // have is ignored
+    const int only = (fp8 || sc) && only_env != kLmDuo && only_env != kLmDuoFused ? -1 : only_env;
     long best_cost = -1;
     auto consider = [&](int kind, int bn) {
         if (forced_bn && bn != forced_bn) return;
         if (only >= 0 && kind != only) return;
-        if (fp8 && kind != kLmDuo && kind != kLmDuoFused) return;
+        if ((fp8 || sc) && kind != kLmDuo && kind != kLmDuoFused) return;
         const bool pair = kind != kLmSingle;
         const int ntn = (V + bn - 1) / bn;
         const int total = ntn * best.mblocks;
@@ -100,10 +102,12 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false)
         consider(kLmDuo, 128);
         consider(kLmDuoFused, 128);
     }
+    best.sc = sc;
     if (best.duo()) {
         const char *env_e = std::getenv("DG_LM_EPI");
         const int forced_e = env_e ? std::atoi(env_e) : 0;
         best.epi_warps = fp8 ? 4 * kDuoCGWide
+                         : sc ? 4 * kDuoCGNarrow
                          : forced_e == 8 || forced_e == 16 ? forced_e
                          : best.mblocks == 1             ? 4 * kDuoCGNarrow
                                                          : 4 * kDuoCGWide;
@@ -153,9 +157,10 @@ inline bool use_pdl(cudaStream_t st)
 inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, const CUtensorMap &mw,
                                   const LmHeadArgs &a, cudaStream_t st, bool pdl, bool fp8 = false)
 {
-    const int smem = lm_smem_bytes(plan.kind);
+    const int smem = plan.sc ? kDuoScSmemBytes : lm_smem_bytes(plan.kind);
     const bool wide = plan.epi_warps == 4 * kDuoCGWide;
     auto kern = fp8                    ? lm_head_duo_fp8_kernel
+                : plan.sc                ? lm_head_duo_sc_kernel
                 : plan.kind == kLmSingle ? lm_head_kernel
                 : wide                   ? lm_head_duo_wide_kernel   // kLmDuo, kLmDuoFused
                                          : lm_head_duo_kernel;

@@ -279,6 +279,20 @@ __global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineA
             c.sample[r] = st.gidx;
             c.argmax[r] = st.aidx;
         }
+        if (c.sc_out != nullptr) {
+            // self-conditioning read-out: lane k sums component k of the
+            // units' parts in unit order, each weighed by 2^(m_unit - m), then
+            // divides by S (every lane holds the same merged m and S)
+            float o = 0.f;
+            for (int s = u0; s <= u1; ++s) {
+                const size_t i = base + s;
+                const float Ss = __ldcg(c.part.S + i);
+                if (Ss > 0.f)
+                    o = fmaf(fast_exp2(__ldcg(c.part.m + i) - st.m),
+                             __ldcg(c.sc_part + i * kScDim + lane), o);
+            }
+            c.sc_out[static_cast<size_t>(r) * kScDim + lane] = o / st.S;
+        }
     }
     // last CTA of this canvas?
     __shared__ int s_last;

@@ -56,11 +56,68 @@ DG_DEVICE void row_state_init(RowState &s)
     s.kj = -1;
 }
 
+// Self-conditioning read-out ("Parallel Denoising From an Autoregressive
+// Checkpoint", section "Finding": a 7.8M-parameter block feeds the previous
+// prediction back; its matmul runs in full precision in the sampling stage).
+// Per canvas row, sc = sum_v softmax(logits / T)_v E[v, :] over a table
+// E [V, kScDim] (fp32).  The fold keeps o = sum_v 2^(t_v - m) E[v, :] next to
+// S, rescaled with it whenever the running maximum m moves; a merge weighs
+// each part by 2^(m_part - m); the read-out is o / S.
+constexpr int kScDim = 32;
+
+struct ScAcc {
+    float2 o[kScDim / 2];
+};
+
+DG_DEVICE void sc_init(ScAcc &a)
+{
+#pragma unroll
+    for (int k = 0; k < kScDim / 2; ++k) a.o[k] = make_float2(0.f, 0.f);
+}
+
 DG_DEVICE float fast_exp2(float x)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+DG_DEVICE void sc_scale(ScAcc &a, float f)
+{
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int k = 0; k < kScDim / 2; ++k) a.o[k] = mul2(a.o[k], f2);
+}
+
+// o += e E[v, :] for one vocabulary row erow (kScDim fp32, 16-byte aligned;
+// every lane of a warp reads the same row, a broadcast).
+DG_DEVICE void sc_add_row(ScAcc &a, float e, const float *__restrict__ erow)
+{
+    const float4 *e4 = reinterpret_cast<const float4 *>(erow);
+    const float2 ev = make_float2(e, e);
+#pragma unroll
+    for (int q = 0; q < kScDim / 4; ++q) {
+        const float4 r = __ldg(e4 + q);
+        a.o[2 * q] = fma2(ev, make_float2(r.x, r.y), a.o[2 * q]);
+        a.o[2 * q + 1] = fma2(ev, make_float2(r.z, r.w), a.o[2 * q + 1]);
+    }
+}
+
+// Before the softmax states sa and sb merge (row_state_merge(sa, sb)), the
+// read-out parts follow them: a <- 2^(ma - m) a + 2^(mb - m) b with
+// m = max(ma, mb); a part whose S is 0 holds nothing.
+DG_DEVICE void sc_merge(ScAcc &a, const RowState &sa, const ScAcc &b, const RowState &sb)
+{
+    if (!(sb.S > 0.f)) return;
+    if (!(sa.S > 0.f)) {
+        a = b;
+        return;
+    }
+    const float m = fmaxf(sa.m, sb.m);
+    const float2 fa = make_float2(fast_exp2(sa.m - m), fast_exp2(sa.m - m));
+    const float2 fb = make_float2(fast_exp2(sb.m - m), fast_exp2(sb.m - m));
+#pragma unroll
+    for (int k = 0; k < kScDim / 2; ++k) a.o[k] = fma2(fa, a.o[k], mul2(fb, b.o[k]));
 }
 
 // Per-step constants of the fold.
@@ -123,8 +180,12 @@ DG_DEVICE uint32_t gumbel_word_threshold(float t)
 // `row` into the state.  Entries >= V are ignored; a lane with live == false
 // (a row past the end) leaves its state alone.  Must be called by all 32
 // lanes of the warp together (it votes across the warp).
-DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
-                      uint32_t row, const FoldConsts &fc, bool live)
+// With kSC, the self-conditioning part sc (table E [V, kScDim]) is folded
+// along with S.
+template <bool kSC>
+DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
+                        uint32_t row, const FoldConsts &fc, bool live, ScAcc *sc,
+                        const float *__restrict__ E)
 {
     const bool full = v0 + 16u <= V;
     float x[16];
@@ -160,6 +221,7 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
             const float f = fast_exp2(st.m - mt);
             st.A = f * fmaf(st.m - mt, st.S, st.A);
             st.S = f * st.S;
+            if constexpr (kSC) sc_scale(*sc, f);
         }
         st.m = mt;
     }
@@ -174,6 +236,18 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
         const float2 e = make_float2(fast_exp2(dlt.x), fast_exp2(dlt.y));   // 0 for ignored entries
         es[q] = e;
         as[q] = mul2(e, dlt);
+    }
+    if constexpr (kSC) {
+        // columns in order, each weighted by its 2^(t - m) (0 past V: not read)
+        if (live) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (full || v0 + 2 * q < V)
+                    sc_add_row(*sc, es[q].x, E + static_cast<size_t>(v0 + 2 * q) * kScDim);
+                if (full || v0 + 2 * q + 1 < V)
+                    sc_add_row(*sc, es[q].y, E + static_cast<size_t>(v0 + 2 * q + 1) * kScDim);
+            }
+        }
     }
 #pragma unroll
     for (int h = 4; h >= 1; h >>= 1) {
@@ -307,6 +381,12 @@ DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t
     }
 }
 
+DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
+                      uint32_t row, const FoldConsts &fc, bool live)
+{
+    fold16_t<false>(st, lg, v0, V, row, fc, live, nullptr, nullptr);
+}
+
 // Resolve the kept column (evaluate it exactly) before the state is stored.
 DG_DEVICE void row_state_finalize(RowState &st, const FoldConsts &fc)
 {
@@ -360,6 +440,20 @@ DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int B
         const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
         // one call site of the (large) fold keeps the loop in the instruction cache
         if (v0 < V) fold16(st, lg, v0, V, row, fc, live);
+    }
+}
+
+// fold_tile with the self-conditioning part (table E [V, kScDim]).
+DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const float *__restrict__ E, uint32_t tb,
+                            int first, int stride, int BN, uint32_t vbase, uint32_t V,
+                            uint32_t row, const FoldConsts &fc, bool live)
+{
+#pragma unroll 1
+    for (int c0 = first; c0 < BN; c0 += stride) {
+        float lg[16];
+        tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
+        const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
+        if (v0 < V) fold16_t<true>(st, lg, v0, V, row, fc, live, &sc, E);
     }
 }
 
@@ -466,9 +560,19 @@ struct GroupMerge {
     int rows;            // rows of the CTA
 };
 
-DG_DEVICE void group_merge_store(RowState &st, int cg, int rix, uint32_t k,
-                                 const GroupMerge &gm, const Partials &p, size_t idx, bool store,
-                                 WsHeader *ws)
+// Self-conditioning parts of the column groups (kSC): (G - 1) x kScDim x
+// rows words of shared memory after the states, and the per-(row, unit)
+// parts in global memory ([M][n_slots][kScDim], unnormalised, relative to
+// the stored state's m).
+struct ScMerge {
+    float *buf;          // shared
+    float *part;         // global
+};
+
+template <bool kSC>
+DG_DEVICE void group_merge_store_t(RowState &st, int cg, int rix, uint32_t k,
+                                   const GroupMerge &gm, const Partials &p, size_t idx,
+                                   bool store, WsHeader *ws, ScAcc *sc, const ScMerge &sm)
 {
     const int lane = threadIdx.x & 31;
     if (cg != 0) {
@@ -483,6 +587,14 @@ DG_DEVICE void group_merge_store(RowState &st, int cg, int rix, uint32_t k,
             f[4 * gm.rows] = __int_as_float(st.gidx);
             f[5 * gm.rows] = st.amax;
             f[6 * gm.rows] = __int_as_float(st.aidx);
+            if constexpr (kSC) {
+                float *o = sm.buf + static_cast<size_t>(cg - 1) * kScDim * gm.rows + rix;
+#pragma unroll
+                for (int j = 0; j < kScDim / 2; ++j) {
+                    o[(2 * j) * gm.rows] = sc->o[j].x;
+                    o[(2 * j + 1) * gm.rows] = sc->o[j].y;
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(gm.ready);
@@ -500,12 +612,36 @@ DG_DEVICE void group_merge_store(RowState &st, int cg, int rix, uint32_t k,
             o.gidx = __float_as_int(f[4 * gm.rows]);
             o.amax = f[5 * gm.rows];
             o.aidx = __float_as_int(f[6 * gm.rows]);
+            if constexpr (kSC) {
+                const float *ob = sm.buf + static_cast<size_t>(g - 1) * kScDim * gm.rows + rix;
+                ScAcc b;
+#pragma unroll
+                for (int j = 0; j < kScDim / 2; ++j)
+                    b.o[j] = make_float2(ob[(2 * j) * gm.rows], ob[(2 * j + 1) * gm.rows]);
+                sc_merge(*sc, st, b, o);
+            }
             row_state_merge(st, o);
         }
-        if (store) partial_store(p, idx, st);
+        if (store) {
+            partial_store(p, idx, st);
+            if constexpr (kSC) {
+                float4 *dst = reinterpret_cast<float4 *>(sm.part + idx * kScDim);
+#pragma unroll
+                for (int j = 0; j < kScDim / 4; ++j)
+                    dst[j] = make_float4(sc->o[2 * j].x, sc->o[2 * j].y, sc->o[2 * j + 1].x,
+                                         sc->o[2 * j + 1].y);
+            }
+        }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(gm.done);
+}
+
+DG_DEVICE void group_merge_store(RowState &st, int cg, int rix, uint32_t k,
+                                 const GroupMerge &gm, const Partials &p, size_t idx, bool store,
+                                 WsHeader *ws)
+{
+    group_merge_store_t<false>(st, cg, rix, k, gm, p, idx, store, ws, nullptr, ScMerge{});
 }
 
 // Device-resident control block of the block loop (in the workspace).  The
