@@ -102,6 +102,8 @@ def lib():
         L.orc_gumbel_fill.restype = None
         L.orc_self_cond_row.argtypes = [_vp, _c_i32, _c_dbl, _vp, _c_i32, _vp]
         L.orc_self_cond_row.restype = None
+        L.orc_round_bf16.argtypes = [_c_dbl]
+        L.orc_round_bf16.restype = ctypes.c_uint16
         _lib = L
     return _lib
 
@@ -430,3 +432,87 @@ def block(hidden_bits_fn, w_bits: np.ndarray, B: int, L: int, b: float, seed: in
             break
     return dict(steps=steps, argmax=out_argmax.reshape(-1), canvas=canvas.reshape(-1),
                 history=history)
+
+
+# ---------------------------------------------------------------- MoE FFN (decoder body)
+def round_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 (ties to even) of each float64, as raw bits (dg_oracle.c)."""
+    a = np.asarray(x, dtype=np.float64).ravel()
+    L = lib()
+    out = np.fromiter((L.orc_round_bf16(float(v)) for v in a), dtype=np.uint16, count=a.shape[0])
+    return out.reshape(np.shape(x))
+
+
+def gelu_tanh(x: np.ndarray) -> np.ndarray:
+    """GELU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))."""
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x ** 3)))
+
+
+def topk_lowest_index(row: np.ndarray, k: int):
+    """The k largest entries of a row, largest first, ties to the lower index:
+    k rounds of 'take the first maximum of what is left'."""
+    left = [float(v) for v in row]
+    chosen = []
+    for _ in range(k):
+        best = None
+        for e, v in enumerate(left):
+            if v is None:
+                continue
+            if best is None or v > left[best]:
+                best = e
+        chosen.append(best)
+        left[best] = None
+    return chosen
+
+
+def moe_ffn(x_bits: np.ndarray, wr_bits: np.ndarray, wg_bits: np.ndarray, wu_bits: np.ndarray,
+            wd_bits: np.ndarray, top_k: int) -> dict:
+    """A mixture-of-experts FFN over the canvas hidden states, fp64.
+
+    "DiffusionGemma: When the LLM Stops Writing Left to Right", section "What
+    DiffusionGemma Actually Is" (128 experts, top-8 routing plus one shared
+    expert) and "Parallel Denoising From an Autoregressive Checkpoint",
+    section "Finding" (the MoE layer of a canvas forward touches ~84 distinct
+    experts).  Readings (the pages give no formulas): router logits
+    l = X Wr^T; each token takes its top_k experts by logit (ties to the
+    lower index) with gates softmax(l_selected); every expert, and the
+    shared one (index E of the weight stacks, gate 1), is a gated GELU FFN
+    (gelu_tanh(x Wg^T) * (x Wu^T)) Wd^T whose intermediate activation is
+    stored as bf16; out = shared(x) + sum_j gate_j expert_j(x).
+    Weights as raw bf16 bits: wr [E, d], wg / wu [E + 1, f, d], wd [E + 1, d, f].
+    The matmuls are numpy float64 (library steps).
+    """
+    X = bf16_bits_to_f64(x_bits)
+    Wr = bf16_bits_to_f64(wr_bits)
+    M, d = X.shape
+    E = Wr.shape[0]
+    lg = X @ Wr.T
+    experts = np.zeros((M, top_k), np.int32)
+    gates = np.zeros((M, top_k))
+    margin = np.full(M, np.inf)
+    for t in range(M):
+        sel = topk_lowest_index(lg[t], top_k)
+        experts[t] = sel
+        z = lg[t, sel]
+        g = np.exp(z - z.max())
+        gates[t] = g / g.sum()
+        if top_k < E:
+            rest = np.delete(lg[t], sel)
+            margin[t] = lg[t, sel[-1]] - rest.max()
+
+    def ffn(e, Xe):
+        Wg = bf16_bits_to_f64(wg_bits[e])
+        Wu = bf16_bits_to_f64(wu_bits[e])
+        Wd = bf16_bits_to_f64(wd_bits[e])
+        h = gelu_tanh(Xe @ Wg.T) * (Xe @ Wu.T)
+        hb = bf16_bits_to_f64(round_bf16_bits(h))
+        return hb @ Wd.T
+
+    out = ffn(E, X)                      # the shared expert, every token
+    for e in range(E):
+        rows, slots = np.nonzero(experts == e)
+        if rows.shape[0] == 0:
+            continue
+        out[rows] += gates[rows, slots][:, None] * ffn(e, X[rows])
+    return dict(out=out, experts=experts, gates=gates, router_logits=lg, margin=margin,
+                distinct=int(np.unique(experts).shape[0]))

@@ -478,3 +478,29 @@ void orc_self_cond_row(const double *logits, int32_t V, double T, const float *E
     }
     for (int32_t j = 0; j < R; ++j) sc_out[j] /= S;
 }
+
+/* ------------------------------------------------------------------ */
+/* Round to the nearest bf16 (8 significant bits), ties to even: the   */
+/* bf16 value a model stores for an activation computed in higher     */
+/* precision.  Returns the bit pattern.  Finite normal inputs within   */
+/* the bf16 range (the activations here); +-0 maps to +-0.             */
+/* ------------------------------------------------------------------ */
+uint16_t orc_round_bf16(double x)
+{
+    if (x == 0.0) return signbit(x) ? 0x8000u : 0u;
+    const int neg = x < 0.0;
+    double a = fabs(x);
+    int e;
+    (void)frexp(a, &e);                 /* a = f 2^e, f in [0.5, 1) */
+    /* 8 significant bits: the unit in the last place is 2^(e - 8) */
+    double q = ldexp(a, 8 - e);         /* in [128, 256) */
+    double fl = floor(q);
+    double rem = q - fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double r = ldexp(fl, e - 8);
+    float rf = (float)r;                /* exact: 8 significant bits */
+    uint32_t b = orc_float_to_bits(rf);
+    uint16_t h = (uint16_t)(b >> 16);
+    if (neg) h |= 0x8000u;
+    return h;
+}

@@ -600,3 +600,89 @@ def test_self_cond_matches_torch_softmax_matmul():
     E2 = np.ones((V, 2), np.float32)
     E2[:, 1] = 3.0
     assert np.abs(oracle.self_cond(lg, T, E2) - np.array([1.0, 3.0])).max() < 1e-12
+
+
+# ------------------------------------------------------------------ MoE FFN (decoder body)
+def test_round_bf16_matches_torch_on_fp32_values_and_ties():
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    # exact halfway cases: 8 significant bits + a half ulp, both parities
+    halves = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(2.0 + 2.0 ** -7), 0.5 + 2.0 ** -9],
+                      np.float32)
+    x = np.concatenate([x, halves])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_bf16_bits(x.astype(np.float64)), ref)
+
+
+def test_topk_lowest_index_against_stable_sort():
+    rng = np.random.default_rng(32)
+    for _ in range(200):
+        E = int(rng.integers(8, 130))
+        k = int(rng.integers(1, min(8, E) + 1))
+        row = rng.choice(np.linspace(-2, 2, 17), E)          # many ties
+        ref = np.argsort(-row, kind="stable")[:k].tolist()
+        assert oracle.topk_lowest_index(row, k) == ref
+
+
+def test_gelu_tanh_matches_torch():
+    x = np.linspace(-12, 12, 4001)
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    assert np.abs(oracle.gelu_tanh(x) - ref).max() < 1e-14
+
+
+def _moe_inputs(M, d, f, E, seed):
+    rng = np.random.default_rng(seed)
+    b = lambda a: _bf16_bits(a)
+    return dict(x=b(rng.standard_normal((M, d))), wr=b(rng.standard_normal((E, d)) * 0.5),
+                wg=b(rng.standard_normal((E + 1, f, d)) / np.sqrt(d)),
+                wu=b(rng.standard_normal((E + 1, f, d)) / np.sqrt(d)),
+                wd=b(rng.standard_normal((E + 1, d, f)) / np.sqrt(f)))
+
+
+def test_moe_matches_dense_torch_evaluation():
+    """Every expert on every token in torch float64, then weighted by a gate
+    matrix built from torch.topk and torch.softmax: the routed sum."""
+    M, d, f, E, k = 24, 64, 32, 16, 4
+    a = _moe_inputs(M, d, f, E, 33)
+    r = oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], k)
+    tb = lambda bits: torch.from_numpy(oracle.bf16_bits_to_f64(bits))
+    X, Wr = tb(a["x"]), tb(a["wr"])
+    lg = X @ Wr.T
+    val, idx = torch.topk(lg, k, dim=1)
+    G = torch.zeros(M, E, dtype=torch.float64)
+    G.scatter_(1, idx, torch.softmax(val, dim=1))
+    assert np.array_equal(np.sort(idx.numpy(), 1), np.sort(r["experts"], 1))
+
+    def ffn(e):
+        h = torch.nn.functional.gelu(X @ tb(a["wg"][e]).T, approximate="tanh") * (X @ tb(a["wu"][e]).T)
+        h = torch.from_numpy(oracle.bf16_bits_to_f64(
+            h.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)))
+        return h @ tb(a["wd"][e]).T
+
+    ref = ffn(E) + sum(G[:, e:e + 1] * ffn(e) for e in range(E))
+    err = np.abs(r["out"] - ref.numpy()).max() / np.abs(ref.numpy()).max()
+    assert err < 5e-3, err     # the two round the activation to bf16 by different paths
+    assert np.abs(r["gates"].sum(axis=1) - 1).max() < 1e-12
+
+
+def test_moe_top1_and_shared_only_cases():
+    M, d, f, E = 8, 32, 16, 8
+    a = _moe_inputs(M, d, f, E, 34)
+    X = oracle.bf16_bits_to_f64(a["x"])
+    tb = oracle.bf16_bits_to_f64
+
+    def ffn(e, Xe):
+        h = oracle.gelu_tanh(Xe @ tb(a["wg"][e]).T) * (Xe @ tb(a["wu"][e]).T)
+        return tb(oracle.round_bf16_bits(h)) @ tb(a["wd"][e]).T
+
+    # top-1: gate 1 on the best expert
+    r = oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], 1)
+    assert np.array_equal(r["experts"][:, 0], np.argmax(X @ tb(a["wr"]).T, axis=1))
+    assert (r["gates"] == 1.0).all()
+    ref = ffn(E, X) + np.stack([ffn(int(e), X[t:t + 1])[0] for t, e in enumerate(r["experts"][:, 0])])
+    assert np.abs(r["out"] - ref).max() < 1e-12 * np.abs(ref).max()
+    # zero routed experts' down projections: only the shared expert is left
+    wd = a["wd"].copy()
+    wd[:E] = 0
+    r = oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], wd, 3)
+    assert np.abs(r["out"] - ffn(E, X)).max() < 1e-12 * np.abs(r["out"]).max()
