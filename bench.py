@@ -239,6 +239,44 @@ def run_reference(args, cfg):
     return 0
 
 
+def run_reference_moe(args, mcfg):
+    """The oracle on the MoE workload (host cores, one thread), on a bounded
+    sample: the first 64 canvas rows of the layer (their routing and
+    experts), scaled to the 256-row layer by rows."""
+    ws_, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    sub = dg_synth.MoeConfig(mcfg.name + "_rows", M=64, d=mcfg.d, f=mcfg.f, E=mcfg.E,
+                             top_k=mcfg.top_k, alpha=mcfg.alpha, seed=mcfg.seed)
+    a = dg_synth.moe_inputs(sub)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], sub.top_k)
+        if i >= args.warmup:
+            times.append((time.perf_counter() - t0) * mcfg.M / sub.M)
+    per = sum(times) / len(times)
+    value = 1.0 / per
+    desc = ("oracle (numpy fp64 matmuls + plain routing, 1 thread): the first %d of %d canvas "
+            "rows, scaled by rows" % (sub.M, mcfg.M))
+    line = dict(impl="reference", metric="MoE FFN layers/s (256-token canvas)", value=value,
+                unit="layers/s", n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
+                ms_per_step=per * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic",
+                config={"workload": "%s: MoE FFN over the canvas, M=%d, d=%d, %d experts of f=%d, "
+                                    "top-%d + 1 shared" % (mcfg.name, mcfg.M, mcfg.d, mcfg.E,
+                                                           mcfg.f, mcfg.top_k),
+                        "global_batch": 1, "seq_len": mcfg.M, "parallelism": "replicas",
+                        "l2": "n/a (CPU)"},
+                cpu_baseline=dict(value=value, unit="layers/s", cores=1, kind="oracle",
+                                  sample=desc),
+                e2e=dict(value=value, unit="layers/s", h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def _config_json(cfg, l2, lm_dtype="bf16", self_cond=False):
     return {"workload": "%s: single denoising step, B=%d L=%d, attention Hq=%d Hkv=%d D=%d "
                         "P=%d, LM head d=%d V=%d%s%s, T=%.1f b=%.1f" % (
@@ -778,6 +816,146 @@ def run_encoder(args, cfg):
     return 0
 
 
+# ----------------------------------------------------------------------------- MoE FFN
+def run_moe(args, mcfg):
+    """One MoE FFN layer over the canvas (dg_moe_ffn): router, top-8 of 128
+    experts plus the shared one, gated GELU experts, weighted sum.  K timed
+    layers, L2 flushed before each; value = layers per second.  Roofline:
+    the weights of the experts the canvas touches (+ the shared expert and the
+    router) at the measured HBM bandwidth, against the layer's FLOPs at the
+    measured bf16 peak."""
+    import torch
+    import block_diffusion_decoding_gb300 as dg
+    from block_diffusion_decoding_gb300 import build as dgbuild
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+    dgbuild.build()
+    dg.lib()
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    g = torch.Generator(device=dev).manual_seed(4000 + rank)
+    bf = torch.bfloat16
+    M, d, f, E, K = mcfg.M, mcfg.d, mcfg.f, mcfg.E, mcfg.top_k
+    c = torch.randn(d, device=dev, generator=g)
+    x = ((mcfg.alpha * c[None, :] + torch.randn(M, d, device=dev, generator=g))
+         / math.sqrt(1 + mcfg.alpha ** 2)).to(bf)
+    wr = (torch.randn(E, d, device=dev, generator=g) / math.sqrt(d)).to(bf)
+    wg = torch.empty(E + 1, f, d, device=dev, dtype=bf)
+    wu = torch.empty_like(wg)
+    wd = torch.empty(E + 1, d, f, device=dev, dtype=bf)
+    for e in range(E + 1):
+        wg[e] = (torch.randn(f, d, device=dev, generator=g) / math.sqrt(d)).to(bf)
+        wu[e] = (torch.randn(f, d, device=dev, generator=g) / math.sqrt(d)).to(bf)
+        wd[e] = (torch.randn(d, f, device=dev, generator=g) / math.sqrt(f)).to(bf)
+    out = torch.empty(M, d, device=dev)
+    experts = torch.empty(M, K, dtype=torch.int32, device=dev)
+    gates = torch.empty(M, K, device=dev)
+    p = dg.moe_params(M, d, f, E, K)
+    ws = dg.workspace(dg.moe_ffn_workspace(p), dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def layer():
+        dg.moe_ffn(x, wr, wg, wu, wd, out, p, ws, experts, gates)
+
+    def timed(n):
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record(stream)
+            layer()
+            e_.record(stream)
+            evs.append((s_, e_))
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b_) for a, b_ in evs]
+
+    with ClockSampler(local) as clk:
+        clk.wait_first()
+        timed(args.warmup)
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+        n0 = dg.kernel_launches()
+        t_start = time.perf_counter()
+        ts = timed(args.steps)
+        t_end = time.perf_counter()
+        launches = dg.kernel_launches() - n0
+        clk.mark(t_start, t_end)
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize(dev)
+    ms = _reduce_max(sum(ts) / len(ts), dev)
+    status = dg.read_device_status(ws)
+    distinct = int(torch.unique(experts).numel())
+    # algorithmic traffic: the touched experts' and the shared expert's three
+    # matrices, the router, the hidden rows in and the fp32 output rows out
+    w_bytes = (distinct + 1) * 3 * f * d * 2 + E * d * 2
+    nbytes = w_bytes + M * d * 2 + M * d * 4
+    flops = 2.0 * M * d * E + (M * K + M) * 3 * 2.0 * d * f
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    roof_ms = max(nbytes / (hbm_peak * 1e9), flops / (bf16_peak * 1e12)) * 1e3
+
+    # end to end: the hidden rows up from pinned host memory, the output down
+    h_x = x.cpu().pin_memory()
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    e2e = []
+    for i in range(args.steps + 1):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        x.copy_(h_x, non_blocking=True)
+        layer()
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if i > 0:
+            e2e.append(time.perf_counter() - t0)
+    e2e_ms = _reduce_max(1e3 * sum(e2e) / len(e2e), dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        host = {k: v.view(torch.int16).cpu().numpy().view(np.uint16)
+                for k, v in dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd).items()}
+        t0 = time.perf_counter()
+        oracle.moe_ffn(host["x"], host["wr"], host["wg"], host["wu"], host["wd"], K)
+        t_or = time.perf_counter() - t0
+        cpu = dict(value=1.0 / t_or, unit="layers/s", cores=1, kind="oracle",
+                   sample="oracle (numpy fp64 matmuls + plain routing, 1 thread): the whole "
+                          "layer, all %d rows" % M)
+    if world > 1:
+        tdist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = dict(
+        metric="MoE FFN layers/s (256-token canvas)", value=_replica_value(world, ms),
+        unit="layers/s", n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=ms,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
+        config={"workload": "%s: MoE FFN over the canvas, M=%d rows, d=%d, %d experts of f=%d, "
+                            "top-%d + 1 shared, gated GELU; hidden rows share a canvas-wide "
+                            "component (alpha %.1f)" % (mcfg.name, M, d, E, f, K, mcfg.alpha),
+                "global_batch": 1, "seq_len": M, "parallelism": "replicas",
+                "l2": "flushed (256 MiB write) before every layer"},
+        distinct_experts=distinct,
+        roofline=dict(bound="hbm" if nbytes / hbm_peak > flops / (bf16_peak * 1e3) else "tensor",
+                      achieved=gbs, peak=hbm_peak, unit="GB/s", frac=gbs / hbm_peak,
+                      traffic=None, kernel="moe_ffn_kernel (+ router, route, gather, combine)",
+                      peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
+                      algorithmic_bytes=nbytes),
+        step_roofline_ms=roof_ms, step_frac_of_roofline=roof_ms / ms,
+        TFLOP_per_s=flops / (ms * 1e-3) / 1e12,
+        cpu_baseline=cpu,
+        e2e=dict(value=_replica_value(world, e2e_ms), unit="layers/s",
+                 h2d_bytes_per_step=M * d * 2, d2h_bytes_per_step=M * d * 4),
+        clocks=clk.summary(), gpu_launches=launches, device_status=status)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def oracle_block_step_estimate(cfg, host, v_sample=16384):
     """One step of the block loop on the CPU oracle, column-sampled: every canvas
     row against the first v_sample vocabulary columns (LM head + sampler, time
@@ -865,7 +1043,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(dg_synth.CONFIGS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    choices=sorted(dg_synth.CONFIGS) + sorted(dg_synth.MOE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-dtype", default="bf16", choices=["bf16", "fp8"],
@@ -876,6 +1055,10 @@ def main():
                     help="run one kernel of the step alone (for profilers), not the benchmark")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.config in dg_synth.MOE_CONFIGS:
+        if args.impl == "reference":
+            return run_reference_moe(args, dg_synth.MOE_CONFIGS[args.config])
+        return run_moe(args, dg_synth.MOE_CONFIGS[args.config])
     cfg = dg_synth.CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)

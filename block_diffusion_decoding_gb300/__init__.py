@@ -36,7 +36,7 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_logf_eval", "dg_quantize_rows_e4m3", "dg_quantize_weight_e4m3",
             "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8",
             "dg_wait_timeout_probe", "dg_denoise_step_sc_workspace", "dg_denoise_step_sc",
-            "dg_lm_head_fold_sc"]
+            "dg_lm_head_fold_sc", "dg_moe_ffn_workspace", "dg_moe_ffn"]
 
 
 class DgError(RuntimeError):
@@ -57,6 +57,11 @@ class StepIO(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("canvas", "prev_argmax", "argmax", "sample", "entropy", "accepted",
                  "n_accepted", "mean_entropy", "stop")]
+
+
+class MoeParams(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int), ("d", ctypes.c_int), ("f", ctypes.c_int),
+                ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int)]
 
 
 class BlockParams(ctypes.Structure):
@@ -116,6 +121,8 @@ def _lib():
             "dg_denoise_step_sc_workspace": ([sp], sz),
             "dg_denoise_step_sc": ([vp, vp, vp, sp, si, vp, vp, sz, vp], i32),
             "dg_lm_head_fold_sc": ([vp, vp, vp, sp, vp, sz, vp], i32),
+            "dg_moe_ffn_workspace": ([ctypes.POINTER(MoeParams)], sz),
+            "dg_moe_ffn": ([vp] * 8 + [ctypes.POINTER(MoeParams), vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -263,6 +270,25 @@ def lm_head_fold_sc(hidden, w, sc_table, p: StepParams, workspace, stream=None):
     rc = _lib().dg_lm_head_fold_sc(_p(hidden), _p(w), _p(sc_table), ctypes.byref(p),
                                    _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "dg_lm_head_fold_sc")
+
+
+# ---------------------------------------------------------------- MoE FFN
+def moe_params(M, d, f, n_experts, top_k) -> MoeParams:
+    return MoeParams(M, d, f, n_experts, top_k)
+
+
+def moe_ffn_workspace(p: MoeParams) -> int:
+    return int(_lib().dg_moe_ffn_workspace(ctypes.byref(p)))
+
+
+def moe_ffn(x, w_router, w_gate, w_up, w_down, out, p: MoeParams, workspace, experts=None,
+            gates=None, stream=None):
+    """dg_moe_ffn: x [M, d] bf16, w_router [E, d], w_gate / w_up [E+1, f, d],
+    w_down [E+1, d, f] bf16 -> out [M, d] fp32 (+ routing when given)."""
+    rc = _lib().dg_moe_ffn(_p(x), _p(w_router), _p(w_gate), _p(w_up), _p(w_down), _p(out),
+                           _p(experts), _p(gates), ctypes.byref(p), _p(workspace),
+                           workspace.numel(), _stream(stream))
+    _check(rc, "dg_moe_ffn")
 
 
 # ---------------------------------------------------------------- FP8 LM head

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdg.so")
 SOURCES = ["dg_api.cu", "dg_lm_head.cu", "dg_lm_head_duo.cu", "dg_attn.cu",
-           "dg_attn_pair.cu", "dg_sampler.cu", "dg_noalloc.cu", "dg_fp8.cu"]
+           "dg_attn_pair.cu", "dg_sampler.cu", "dg_noalloc.cu", "dg_fp8.cu", "dg_moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

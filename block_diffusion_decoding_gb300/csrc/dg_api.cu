@@ -83,6 +83,9 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_fp8_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(moe_ffn_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         moe_ffn_smem_bytes()));
         DG_CUDA_TRY(cudaFuncSetAttribute(attn_kernel_d128,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          attn_smem_bytes(128)));
@@ -734,6 +737,59 @@ int sc_step(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
                         io->argmax, acc, as_stream(stream), false, nullptr, &sco);
 }
 
+// ---------------------------------------------------------------- MoE FFN
+int moe_chunks_cap(int M, int E, int K)
+{
+    return E + 1 + (M * (K + 1) + kMoeChunk - 1) / kMoeChunk;
+}
+
+struct MoeWs {
+    size_t logits, sel_e, sel_g, pos_of, tok, gate, items, counts, next, ready, xs, hs, ys, total;
+};
+
+MoeWs moe_ws_layout(const dg_moe_params *p)
+{
+    const size_t M = p->M, K = p->top_k, E = p->n_experts, d = p->d, f = p->f;
+    const size_t R = M * (K + 1);
+    const size_t items = static_cast<size_t>(moe_chunks_cap(p->M, p->n_experts, p->top_k)) *
+                         (f / 128 + d / 128);
+    MoeWs w{};
+    size_t o = sizeof(WsHeader);
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += round_up(bytes, 256);
+        return at;
+    };
+    w.logits = take(M * E * 4);
+    w.sel_e = take(M * K * 4);
+    w.sel_g = take(M * K * 4);
+    w.pos_of = take(M * K * 4);
+    w.tok = take(R * 4);
+    w.gate = take(R * 4);
+    w.items = take(items * 16);
+    w.counts = take(16);
+    w.next = take(4);
+    w.ready = take(static_cast<size_t>(kMoeMaxChunks) * 4);
+    w.xs = take(R * d * 2);
+    w.hs = take(R * f * 2);
+    w.ys = take(R * d * 4);
+    w.total = o;
+    return w;
+}
+
+int check_moe_params(const dg_moe_params *p)
+{
+    if (p == nullptr) return DG_ERR_INVALID_ARG;
+    if (p->M < 1 || p->d < 1 || p->f < 1 || p->n_experts < 1 || p->top_k < 1)
+        return DG_ERR_INVALID_ARG;
+    if (p->top_k > p->n_experts) return DG_ERR_INVALID_ARG;
+    if (p->M > kMoeMaxTokens || p->n_experts > kMoeMaxExperts || p->top_k > kMoeMaxTopK)
+        return DG_ERR_UNSUPPORTED;
+    if (p->d % 128 != 0 || p->d > 16384 || p->f % 128 != 0 || p->f > 16384)
+        return DG_ERR_UNSUPPORTED;
+    return DG_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -965,6 +1021,108 @@ int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const float *s
 {
     return sc_step(hidden, w, sc_table, p, nullptr, nullptr, workspace, workspace_bytes, stream,
                    true);
+}
+
+// ---------------------------------------------------------------- MoE FFN
+size_t dg_moe_ffn_workspace(const dg_moe_params *p)
+{
+    if (check_moe_params(p) != DG_OK) return 0;
+    return moe_ws_layout(p).total;
+}
+
+int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_gate,
+               const uint16_t *w_up, const uint16_t *w_down, float *out, int32_t *experts_out,
+               float *gates_out, const dg_moe_params *p, void *workspace, size_t workspace_bytes,
+               void *stream)
+{
+    int rc = check_moe_params(p);
+    if (rc != DG_OK) return rc;
+    if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return DG_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_up) ||
+        !aligned16(w_down) || !aligned16(out))
+        return DG_ERR_ALIGNMENT;
+    const MoeWs L = moe_ws_layout(p);
+    if (workspace == nullptr || workspace_bytes < L.total) return DG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    uint8_t *base = static_cast<uint8_t *>(workspace);
+    const int M = p->M, K = p->top_k, E = p->n_experts, d = p->d, f = p->f;
+    const uint64_t R = static_cast<uint64_t>(M) * (K + 1);
+    MoeArgs a{};
+    a.M = M;
+    a.d = d;
+    a.f = f;
+    a.E = E;
+    a.top_k = K;
+    a.x = x;
+    a.logits = reinterpret_cast<float *>(base + L.logits);
+    a.sel_expert = experts_out ? experts_out : reinterpret_cast<int32_t *>(base + L.sel_e);
+    a.sel_gate = gates_out ? gates_out : reinterpret_cast<float *>(base + L.sel_g);
+    a.pos_of = reinterpret_cast<int32_t *>(base + L.pos_of);
+    a.tok_of_pos = reinterpret_cast<int32_t *>(base + L.tok);
+    a.gate_of_pos = reinterpret_cast<float *>(base + L.gate);
+    a.items = reinterpret_cast<int4 *>(base + L.items);
+    a.counts = reinterpret_cast<int32_t *>(base + L.counts);
+    a.next_item = reinterpret_cast<int32_t *>(base + L.next);
+    a.ready = reinterpret_cast<uint32_t *>(base + L.ready);
+    a.x_sorted = reinterpret_cast<uint16_t *>(base + L.xs);
+    a.h_sorted = reinterpret_cast<uint16_t *>(base + L.hs);
+    a.y_sorted = reinterpret_cast<float *>(base + L.ys);
+    a.out = out;
+    a.ws = static_cast<WsHeader *>(workspace);
+
+    CUtensorMap mwg, mwu, mwd, mxs, mhs;
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(f),
+                                  static_cast<uint64_t>(E + 1)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(f) * d * 2};
+        const uint32_t box[3] = {64, 128, 1};
+        if ((rc = make_map_bf16(&mwg, w_gate, 3, dims, strides, box)) != DG_OK) return rc;
+        if ((rc = make_map_bf16(&mwu, w_up, 3, dims, strides, box)) != DG_OK) return rc;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(f), static_cast<uint64_t>(d),
+                                  static_cast<uint64_t>(E + 1)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(f) * 2, static_cast<uint64_t>(d) * f * 2};
+        const uint32_t box[3] = {64, 128, 1};
+        if ((rc = make_map_bf16(&mwd, w_down, 3, dims, strides, box)) != DG_OK) return rc;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(d), R};
+        const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
+        const uint32_t box[2] = {64, kMoeChunk};
+        if ((rc = make_map_bf16(&mxs, a.x_sorted, 2, dims, strides, box)) != DG_OK) return rc;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(f), R};
+        const uint64_t strides[1] = {static_cast<uint64_t>(f) * 2};
+        const uint32_t box[2] = {64, kMoeChunk};
+        if ((rc = make_map_bf16(&mhs, a.h_sorted, 2, dims, strides, box)) != DG_OK) return rc;
+    }
+    cudaStream_t st = as_stream(stream);
+    const bool pdl = use_pdl(st);
+    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3((M + 15) / 16, (E + 15) / 16), dim3(256), 0,
+                              st, pdl, x, w_router, M, d, E,
+                              reinterpret_cast<float *>(base + L.logits)));
+    DG_LAUNCHED();
+    DG_CUDA_TRY(launch_kernel(moe_route_kernel, dim3(1), dim3(kMoeRouteThreads), 0, st, pdl, a));
+    DG_LAUNCHED();
+    const unsigned fill = static_cast<unsigned>(std::max(1, di->sms * 8));
+    const uint64_t gvec = R * static_cast<uint64_t>(d / 8);
+    DG_CUDA_TRY(launch_kernel(moe_gather_kernel,
+                              dim3(static_cast<unsigned>(std::min<uint64_t>((gvec + 255) / 256, fill))),
+                              dim3(256), 0, st, pdl, a));
+    DG_LAUNCHED();
+    DG_CUDA_TRY(launch_kernel(moe_ffn_kernel, dim3(di->sms), dim3(192), moe_ffn_smem_bytes(), st,
+                              pdl, mwg, mwu, mwd, mxs, mhs, a));
+    DG_LAUNCHED();
+    const uint64_t cvec = static_cast<uint64_t>(M) * (d / 4);
+    DG_CUDA_TRY(launch_kernel(moe_combine_kernel,
+                              dim3(static_cast<unsigned>(std::min<uint64_t>((cvec + 255) / 256, fill))),
+                              dim3(256), 0, st, pdl, a));
+    DG_LAUNCHED();
+    return DG_OK;
 }
 
 // ---------------------------------------------------------------- sampler on given logits

@@ -223,4 +223,49 @@ int attn_pair_smem_bytes(int D);
 
 int attn_smem_bytes(int D);
 
+// ---------------------------------------------------------------- MoE FFN
+constexpr int kMoeMaxExperts = 128;    // routed experts (plus one shared)
+constexpr int kMoeMaxTopK = 8;
+constexpr int kMoeMaxTokens = 2048;    // canvas rows per call
+constexpr int kMoeChunk = 128;         // tokens per token tile of the expert GEMMs
+constexpr int kMoeRouteThreads = 1024;
+// token chunks of one call: every expert's tokens in chunks of kMoeChunk
+constexpr int kMoeMaxChunks =
+    kMoeMaxExperts + 1 + (kMoeMaxTokens * (kMoeMaxTopK + 1) + kMoeChunk - 1) / kMoeChunk;
+
+struct MoeArgs {
+    int M, d, f, E, top_k;
+    const uint16_t *x;          // [M, d] bf16
+    const float *logits;        // [M, E] router logits
+    int32_t *sel_expert;        // [M, top_k] chosen experts, best first
+    float *sel_gate;            // [M, top_k] their gates
+    int32_t *pos_of;            // [M, top_k] row of each assignment in the sorted order
+    int32_t *tok_of_pos;        // [M (top_k + 1)] token of each sorted row
+    float *gate_of_pos;         // [M (top_k + 1)] gate of each sorted row (1: shared)
+    int4 *items;                // work list (expert, tile | chunk << 8, first row, tokens)
+    int32_t *counts;            // [4]: gate/up items, all items, sorted rows
+    int32_t *next_item;         // work-list counter of the FFN kernel
+    uint32_t *ready;            // [kMoeMaxChunks] H parts stored per chunk
+    uint16_t *x_sorted;         // [M (top_k + 1), d] bf16
+    uint16_t *h_sorted;         // [M (top_k + 1), f] bf16
+    float *y_sorted;            // [M (top_k + 1), d] fp32, gate applied
+    float *out;                 // [M, d] fp32
+    WsHeader *ws;
+};
+
+__global__ void moe_router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
+                                  int M, int d, int E, float *__restrict__ logits);
+__global__ void moe_route_kernel(MoeArgs a);
+__global__ void moe_gather_kernel(MoeArgs a);
+__global__ void moe_combine_kernel(MoeArgs a);
+// maps: gate / up weights [E+1, f, d] as {d, f, E+1}, box {64, 128, 1}; down
+// weights [E+1, d, f] as {f, d, E+1}, box {64, 128, 1}; X_sorted / H_sorted
+// as {d or f, rows}, box {64, 128}
+__global__ void moe_ffn_kernel(const __grid_constant__ CUtensorMap map_wg,
+                               const __grid_constant__ CUtensorMap map_wu,
+                               const __grid_constant__ CUtensorMap map_wd,
+                               const __grid_constant__ CUtensorMap map_xs,
+                               const __grid_constant__ CUtensorMap map_hs, MoeArgs a);
+int moe_ffn_smem_bytes();
+
 }  // namespace dg

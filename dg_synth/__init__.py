@@ -164,3 +164,44 @@ def block_hidden(cfg: StepConfig, w_bits: np.ndarray, targets: dict, k: int,
     g = np.random.Generator(np.random.PCG64(_ss(s, 100 + k)))
     noise = g.standard_normal((cfg.M, cfg.d)) / np.sqrt(cfg.d)
     return f32_to_bf16_bits((gk[:, None] * cols + noise).astype(np.float32))
+
+
+@dataclasses.dataclass(frozen=True)
+class MoeConfig:
+    """Shapes and value distributions of one synthetic MoE FFN layer over a canvas."""
+    name: str
+    M: int = 256               # canvas rows (B * L)
+    d: int = 2816              # hidden size
+    f: int = 768               # FFN width of every expert
+    E: int = 128               # routed experts (plus one shared)
+    top_k: int = 8
+    alpha: float = 1.2         # weight of the canvas-wide component of the hidden rows
+    seed: int = 0
+
+
+# The MoE workload: 128 experts, top-8 plus one shared expert (the pages'
+# routing); d as the full-width step; f = 768 per expert (the pages give no
+# expert shapes).  The hidden rows share a canvas-wide component, which makes
+# the router's choices overlap: about 84 distinct experts per canvas, the
+# count the pages report for a canvas forward.
+MOE_CONFIGS = {
+    "moe_full": MoeConfig("moe_full"),
+}
+
+
+def moe_inputs(cfg: MoeConfig, seed: Optional[int] = None) -> dict:
+    """x [M, d] = (alpha c + n) / sqrt(1 + alpha^2) with one canvas vector c and
+    per-row noise n (both N(0, 1)); router wr [E, d] ~ N(0, 1/d); gate / up
+    [E+1, f, d] ~ N(0, 1/d); down [E+1, d, f] ~ N(0, 1/f); all bf16 bits."""
+    s = cfg.seed if seed is None else seed
+    g = np.random.Generator(np.random.PCG64(_ss(s, 200)))
+    c = g.standard_normal(cfg.d)
+    n = g.standard_normal((cfg.M, cfg.d))
+    x = (cfg.alpha * c[None, :] + n) / np.sqrt(1.0 + cfg.alpha ** 2)
+    return dict(
+        x=f32_to_bf16_bits(x.astype(np.float32)),
+        wr=_normal_bf16(_ss(s, 201), (cfg.E, cfg.d), std=cfg.d ** -0.5),
+        wg=_normal_bf16(_ss(s, 202), (cfg.E + 1, cfg.f, cfg.d), std=cfg.d ** -0.5, chunk_rows=4),
+        wu=_normal_bf16(_ss(s, 203), (cfg.E + 1, cfg.f, cfg.d), std=cfg.d ** -0.5, chunk_rows=4),
+        wd=_normal_bf16(_ss(s, 204), (cfg.E + 1, cfg.d, cfg.f), std=cfg.f ** -0.5, chunk_rows=4),
+    )

@@ -227,6 +227,42 @@ int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const float *s
                        void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Mixture-of-experts FFN over the canvas hidden states (the decoder body's  */
+/* largest per-step cost).  "DiffusionGemma: When the LLM Stops Writing Left  */
+/* to Right", section "What DiffusionGemma Actually Is": 128 experts, top-8  */
+/* routing and one shared expert; "Parallel Denoising From an Autoregressive */
+/* Checkpoint", section "Finding": a canvas forward touches about 84 distinct */
+/* experts per layer.  The pages give no formulas; this library computes,    */
+/* per row t of x:                                                           */
+/*   l = x_t . w_router^T (fp32);  S_t = the top_k experts by l (ties to the */
+/*   lower index), gates g = softmax(l[S_t]);                                */
+/*   FFN_e(x) = (gelu_tanh(x . w_gate[e]^T) * (x . w_up[e]^T)) . w_down[e]^T,  */
+/*   the product of the first two rounded to bf16 before the last matmul;    */
+/*   out_t = FFN_E(x_t) + sum_j g_j FFN_{S_t[j]}(x_t)  (expert E = shared).   */
+/* bf16 operands, fp32 accumulation (tensor cores), fp32 output.  Layouts    */
+/* (bf16, K-major "weights as rows"): x [M, d]; w_router [E, d]; w_gate,      */
+/* w_up [E + 1, f, d]; w_down [E + 1, d, f] (index E = the shared expert);   */
+/* out [M, d] fp32.  experts_out [M, top_k] int32 and gates_out [M, top_k]   */
+/* fp32 receive the routing when not NULL.  Only the experts some row picks */
+/* are read.  Supported: 1 <= M <= 2048; d, f multiples of 128, <= 16384;     */
+/* 1 <= top_k <= min(8, E), E <= 128.  16-byte aligned pointers.  Errors as  */
+/* dg_denoise_step; device-side waits report through the workspace status.  */
+/* ------------------------------------------------------------------------ */
+typedef struct dg_moe_params {
+    int M;          /* canvas rows (B * L)                                    */
+    int d;          /* hidden size                                            */
+    int f;          /* FFN width of every expert                              */
+    int n_experts;  /* routed experts E (the shared one is extra)             */
+    int top_k;      /* experts per row                                        */
+} dg_moe_params;
+
+size_t dg_moe_ffn_workspace(const dg_moe_params *p);
+int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_gate,
+               const uint16_t *w_up, const uint16_t *w_down, float *out, int32_t *experts_out,
+               float *gates_out, const dg_moe_params *p, void *workspace, size_t workspace_bytes,
+               void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* The denoising loop of one block (batch of B independent canvases).        */
 /* "DiffusionGemma Lab" section 2 items 1-5; "Parallel Denoising ..."         */
 /* section "Finding" (temperature annealing, adaptive stopping, N = 48).      */

@@ -156,3 +156,16 @@ def test_wait_probe_rejects_bad_arguments_before_launch(lib):
     assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr), 256, 10, None) == 1
     assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr), 256, 2 * 10**9, None) == 1
     assert lib.dg_wait_timeout_probe(ctypes.c_void_p(addr + 4), 256, 1000000, None) == 3
+
+
+def test_moe_rejects_bad_arguments_before_launch(lib):
+    p = dg.moe_params(256, 2816, 768, 128, 8)
+    assert dg.moe_ffn_workspace(p) > 256 * 9 * 2816 * 4
+    assert dg.moe_ffn_workspace(dg.moe_params(256, 2816, 700, 128, 8)) == 0    # f % 128
+    assert dg.moe_ffn_workspace(dg.moe_params(4096, 2816, 768, 128, 8)) == 0   # M > 2048
+    assert dg.moe_ffn_workspace(dg.moe_params(256, 2816, 768, 4, 8)) == 0      # top_k > E
+    bad = dg.moe_params(256, 2816, 768, 256, 8)                                 # E > 128
+    rc = lib.dg_moe_ffn(*([None] * 8), ctypes.byref(bad), None, 0, None)
+    assert rc == 2
+    rc = lib.dg_moe_ffn(*([None] * 8), ctypes.byref(p), None, 0, None)
+    assert rc == 1
