@@ -36,7 +36,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_logf_eval", "dg_quantize_rows_e4m3", "dg_quantize_weight_e4m3",
             "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8",
             "dg_wait_timeout_probe", "dg_denoise_step_sc_workspace", "dg_denoise_step_sc",
-            "dg_lm_head_fold_sc", "dg_moe_ffn_workspace", "dg_moe_ffn"]
+            "dg_lm_head_fold_sc", "dg_moe_ffn_workspace", "dg_moe_ffn",
+            "dg_generate_block_fn", "dg_hidden_from_steps", "dg_hidden_embed_add"]
 
 
 class DgError(RuntimeError):
@@ -123,6 +124,9 @@ def _lib():
             "dg_lm_head_fold_sc": ([vp, vp, vp, sp, vp, sz, vp], i32),
             "dg_moe_ffn_workspace": ([ctypes.POINTER(MoeParams)], sz),
             "dg_moe_ffn": ([vp] * 8 + [ctypes.POINTER(MoeParams), vp, sz, vp], i32),
+            "dg_generate_block_fn": ([vp, vp, vp, vp, sp, bp, bi, vp, sz, vp], i32),
+            "dg_hidden_from_steps": ([vp] * 5, i32),
+            "dg_hidden_embed_add": ([vp] * 5, i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -363,6 +367,46 @@ class BlockBuffers:
 
     def io(self) -> BlockIO:
         return BlockIO(*[ctypes.c_void_p(getattr(self, n).data_ptr()) for n, _ in BlockIO._fields_])
+
+
+class HiddenSteps(ctypes.Structure):
+    """dg_hidden_steps: the user data of dg_hidden_from_steps."""
+    _fields_ = [("hidden_steps", ctypes.c_void_p), ("step_stride", ctypes.c_int64),
+                ("n", ctypes.c_int64)]
+
+
+class HiddenEmbed(ctypes.Structure):
+    """dg_hidden_embed: the user data of dg_hidden_embed_add."""
+    _fields_ = [("base", ctypes.c_void_p), ("base_step_stride", ctypes.c_int64),
+                ("table", ctypes.c_void_p), ("rows", ctypes.c_int), ("d", ctypes.c_int),
+                ("V", ctypes.c_int)]
+
+
+# A producer written in Python: f(step_ptr, canvas_ptr, hidden_out_ptr, stream_ptr, user_ptr) -> int
+HIDDEN_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                             ctypes.c_void_p, ctypes.c_void_p)
+
+
+def hidden_producer(name: str) -> ctypes.c_void_p:
+    """Address of a built-in producer: "from_steps" or "embed_add"."""
+    fn = {"from_steps": _lib().dg_hidden_from_steps,
+          "embed_add": _lib().dg_hidden_embed_add}[name]
+    return ctypes.cast(fn, ctypes.c_void_p)
+
+
+def generate_block_fn(producer, user, hidden_buf, w, p: StepParams, bp: BlockParams,
+                      bufs: "BlockBuffers", workspace, stream=None):
+    """dg_generate_block_fn: producer is hidden_producer(name) or a HIDDEN_FN
+    object; user a ctypes structure (kept alive by the caller while the loop's
+    graph may be rebuilt for the same arguments)."""
+    io = bufs.io()
+    fn = producer if isinstance(producer, ctypes.c_void_p) else ctypes.cast(producer,
+                                                                             ctypes.c_void_p)
+    rc = _lib().dg_generate_block_fn(fn, ctypes.cast(ctypes.byref(user), ctypes.c_void_p),
+                                     _p(hidden_buf), _p(w), ctypes.byref(p), ctypes.byref(bp),
+                                     ctypes.byref(io), _p(workspace), workspace.numel(),
+                                     _stream(stream))
+    _check(rc, "dg_generate_block_fn")
 
 
 def block_params(max_steps=48, t_start=0.8, t_end=0.4, hidden_step_stride=0) -> BlockParams:

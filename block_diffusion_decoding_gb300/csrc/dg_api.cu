@@ -1178,9 +1178,11 @@ size_t dg_generate_block_workspace(const dg_step_params *p, const dg_block_param
     return block_ws_layout(p, slot_bound(M, p->V), &oc, &os);
 }
 
-int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_step_params *p,
-                      const dg_block_params *bp, const dg_block_io *io, void *workspace,
-                      size_t workspace_bytes, void *stream)
+// The block loop; hidden states either from hidden_steps (+ k * stride) or,
+// with fn != null, from the caller's producer writing hidden_buf each step.
+static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, uint16_t *hidden_buf,
+                     const uint16_t *w, const dg_step_params *p, const dg_block_params *bp,
+                     const dg_block_io *io, void *workspace, size_t workspace_bytes, void *stream)
 {
     int rc = check_step_params(p);
     if (rc != DG_OK) return rc;
@@ -1190,10 +1192,11 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
     if (bp->hidden_step_stride < 0) return DG_ERR_INVALID_ARG;
     if (!io->canvas || !io->argmax || !io->steps_taken || !io->mean_entropy)
         return DG_ERR_INVALID_ARG;
-    if (!hidden_steps || !w) return DG_ERR_INVALID_ARG;
+    const uint16_t *hidden = fn != nullptr ? hidden_buf : hidden_steps;
+    if (!hidden || !w) return DG_ERR_INVALID_ARG;
     if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
-    if (!aligned16(hidden_steps) || !aligned16(w)) return DG_ERR_ALIGNMENT;
-    if ((bp->hidden_step_stride * 2) % 16 != 0) return DG_ERR_ALIGNMENT;
+    if (!aligned16(hidden) || !aligned16(w)) return DG_ERR_ALIGNMENT;
+    if (fn == nullptr && (bp->hidden_step_stride * 2) % 16 != 0) return DG_ERR_ALIGNMENT;
     if (workspace == nullptr || workspace_bytes < dg_generate_block_workspace(p, bp))
         return DG_ERR_WORKSPACE;
     DeviceInfo *di = nullptr;
@@ -1219,21 +1222,23 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
     int32_t *done = reinterpret_cast<int32_t *>(sp2 + 2 * b4);
 
     cudaStream_t st = as_stream(stream);
-    const int x_steps = bp->hidden_step_stride > 0 ? bp->max_steps : 1;
+    const int x_steps = (fn == nullptr && bp->hidden_step_stride > 0) ? bp->max_steps : 1;
+    const int64_t stride = fn == nullptr ? bp->hidden_step_stride : 0;
 
     int dev = 0;
     DG_CUDA_TRY(cudaGetDevice(&dev));
     const std::vector<uint64_t> key = {
-        reinterpret_cast<uint64_t>(hidden_steps), reinterpret_cast<uint64_t>(w),
+        reinterpret_cast<uint64_t>(hidden), reinterpret_cast<uint64_t>(w),
         reinterpret_cast<uint64_t>(workspace), reinterpret_cast<uint64_t>(io->canvas),
         reinterpret_cast<uint64_t>(io->argmax), reinterpret_cast<uint64_t>(io->steps_taken),
         reinterpret_cast<uint64_t>(io->mean_entropy),
         reinterpret_cast<uint64_t>(io->n_accepted_hist), static_cast<uint64_t>(p->B),
         static_cast<uint64_t>(p->L), static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->V),
         f2u(p->entropy_bound), f2u(p->stop_threshold), d2u(bp->t_start), d2u(bp->t_end), p->seed,
-        static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(bp->hidden_step_stride),
+        static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(stride),
         static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.grid * 4 + plan.kind),
-        static_cast<uint64_t>(dev)};
+        static_cast<uint64_t>(dev), reinterpret_cast<uint64_t>(fn),
+        reinterpret_cast<uint64_t>(user)};
 
     BlockGraph *bgp = nullptr;
     {
@@ -1284,8 +1289,12 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
         acc.out_argmax = io->argmax;
         acc.n_acc_hist = io->n_accepted_hist;
         acc.cond = cond;
-        int erc = enqueue_step(hidden_steps, bp->hidden_step_stride, x_steps, nullptr, w, p, plan,
-                               ws, src, H, sample, argmax, acc, cap);
+        // the producer's work for step k (it reads k from the control block on
+        // the device), then the step itself
+        int erc = fn != nullptr ? fn(&ctl->step, io->canvas, hidden_buf, cap, user) : DG_OK;
+        if (erc == DG_OK)
+            erc = enqueue_step(hidden, stride, x_steps, nullptr, w, p, plan, ws, src, H, sample,
+                               argmax, acc, cap);
         cudaGraph_t captured = nullptr;
         cudaError_t ce = cudaStreamEndCapture(cap, &captured);
         cudaStreamDestroy(cap);
@@ -1309,6 +1318,59 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     DG_CUDA_TRY(cudaGraphLaunch(bgp->exec, st));
+    return DG_OK;
+}
+
+int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w, const dg_step_params *p,
+                      const dg_block_params *bp, const dg_block_io *io, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    return block_run(hidden_steps, nullptr, nullptr, nullptr, w, p, bp, io, workspace,
+                     workspace_bytes, stream);
+}
+
+int dg_generate_block_fn(dg_hidden_fn produce_hidden, void *user, uint16_t *hidden_buf,
+                         const uint16_t *w, const dg_step_params *p, const dg_block_params *bp,
+                         const dg_block_io *io, void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    if (produce_hidden == nullptr) return DG_ERR_INVALID_ARG;
+    return block_run(nullptr, produce_hidden, user, hidden_buf, w, p, bp, io, workspace,
+                     workspace_bytes, stream);
+}
+
+int dg_hidden_from_steps(const int32_t *step, const int32_t *canvas, uint16_t *hidden_out,
+                         void *stream, void *user)
+{
+    (void)canvas;
+    const dg_hidden_steps *u = static_cast<const dg_hidden_steps *>(user);
+    if (u == nullptr || step == nullptr || hidden_out == nullptr || u->hidden_steps == nullptr)
+        return DG_ERR_INVALID_ARG;
+    if (u->n < 1 || u->step_stride < 0) return DG_ERR_INVALID_ARG;
+    const int64_t n = u->n;
+    hidden_from_steps_kernel<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 65535)),
+                               256, 0, as_stream(stream)>>>(step, u->hidden_steps, u->step_stride,
+                                                            n, hidden_out);
+    DG_LAUNCHED();
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+int dg_hidden_embed_add(const int32_t *step, const int32_t *canvas, uint16_t *hidden_out,
+                        void *stream, void *user)
+{
+    const dg_hidden_embed *u = static_cast<const dg_hidden_embed *>(user);
+    if (u == nullptr || step == nullptr || canvas == nullptr || hidden_out == nullptr ||
+        u->base == nullptr || u->table == nullptr)
+        return DG_ERR_INVALID_ARG;
+    if (u->rows < 1 || u->d < 1 || u->V < 1 || u->base_step_stride < 0) return DG_ERR_INVALID_ARG;
+    const int64_t n = static_cast<int64_t>(u->rows) * u->d;
+    hidden_embed_add_kernel<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 65535)),
+                              256, 0, as_stream(stream)>>>(step, canvas, u->base,
+                                                           u->base_step_stride, u->table, u->rows,
+                                                           u->d, u->V, hidden_out);
+    DG_LAUNCHED();
+    DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
 }
 

@@ -177,6 +177,12 @@ __global__ void gumbel_fill_kernel(uint32_t k0, uint32_t k1, uint32_t row, uint3
                                    uint32_t v0, int n, float *out);
 __global__ void logf_eval_kernel(const float *x, float *y, int n);
 __global__ void wait_probe_kernel(WsHeader *ws, uint64_t limit_ns);
+__global__ void hidden_from_steps_kernel(const int32_t *step, const uint16_t *__restrict__ src,
+                                         int64_t step_stride, int64_t n, uint16_t *__restrict__ out);
+__global__ void hidden_embed_add_kernel(const int32_t *step, const int32_t *__restrict__ canvas,
+                                        const uint16_t *__restrict__ base, int64_t base_step_stride,
+                                        const uint16_t *__restrict__ table, int rows, int d, int V,
+                                        uint16_t *__restrict__ out);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {

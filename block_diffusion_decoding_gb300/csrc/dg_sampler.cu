@@ -359,6 +359,39 @@ __global__ void loop_init_kernel(LoopCtl *ctl, int max_steps, double t0, double 
     }
 }
 
+// ---------------------------------------------------------------- hidden-state producers
+// Slice k (= *step, read on the device) of precomputed hidden states.
+__global__ void hidden_from_steps_kernel(const int32_t *step, const uint16_t *__restrict__ src,
+                                         int64_t step_stride, int64_t n, uint16_t *__restrict__ out)
+{
+    const int64_t k = *reinterpret_cast<const volatile int32_t *>(step);
+    const uint16_t *s = src + k * step_stride;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[i] = s[i];
+}
+
+// hidden[r, j] = bf16(base_k[r, j] + table[canvas[r], j]) (fp32 sum, nearest even).
+__global__ void hidden_embed_add_kernel(const int32_t *step, const int32_t *__restrict__ canvas,
+                                        const uint16_t *__restrict__ base, int64_t base_step_stride,
+                                        const uint16_t *__restrict__ table, int rows, int d, int V,
+                                        uint16_t *__restrict__ out)
+{
+    const int64_t k = *reinterpret_cast<const volatile int32_t *>(step);
+    const uint16_t *b = base + k * base_step_stride;
+    const int64_t n = static_cast<int64_t>(rows) * d;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / d, j = i % d;
+        int tok = canvas[r];
+        tok = tok < 0 ? 0 : (tok >= V ? V - 1 : tok);
+        const float v = __uint_as_float(static_cast<uint32_t>(b[i]) << 16) +
+                        __uint_as_float(static_cast<uint32_t>(table[static_cast<int64_t>(tok) * d + j]) << 16);
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        out[i] = *reinterpret_cast<const uint16_t *>(&h);
+    }
+}
+
 // ---------------------------------------------------------------- check kernels
 __global__ void gumbel_fill_kernel(uint32_t k0, uint32_t k1, uint32_t row, uint32_t step,
                                    uint32_t v0, int n, float *out)

@@ -298,6 +298,51 @@ int dg_generate_block(const uint16_t *hidden_steps, const uint16_t *w,
                       const dg_block_io *io, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* The block loop with the decoder body inside it.  "DiffusionGemma Lab",     */
+/* section 2 items 1-5: every step re-runs the decoder on the current canvas  */
+/* and samples from its logits.  produce_hidden enqueues, on `stream`, the    */
+/* work that writes the hidden states [B*L, d] (bf16) of the step into        */
+/* hidden_buf; the loop then runs dg_denoise_step on them.  The loop is one   */
+/* CUDA graph whose body is captured once per (shapes, pointers, callback,    */
+/* user) and replayed for every step on the device, so the callback is        */
+/* invoked while `stream` is being captured (once per distinct key, not once  */
+/* per step): it must enqueue only capturable work (kernel launches, async    */
+/* copies; no allocation, no synchronisation) and read the step index k from */
+/* *step (device int32, valid when its work runs) and the current canvas      */
+/* from canvas (device [B*L] int32, the tokens the step starts from).  It     */
+/* returns DG_OK or an error, which the call returns.  Everything else as     */
+/* dg_generate_block (hidden_step_stride is ignored).                        */
+typedef int (*dg_hidden_fn)(const int32_t *step, const int32_t *canvas, uint16_t *hidden_out,
+                            void *stream, void *user);
+int dg_generate_block_fn(dg_hidden_fn produce_hidden, void *user, uint16_t *hidden_buf,
+                         const uint16_t *w, const dg_step_params *p, const dg_block_params *bp,
+                         const dg_block_io *io, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Producers for dg_generate_block_fn (user points to the struct named).     */
+/* dg_hidden_from_steps: hidden_out = hidden_steps + k * step_stride, n       */
+/* elements (the hidden states of every step computed ahead, the same loop as */
+/* dg_generate_block).                                                        */
+typedef struct dg_hidden_steps {
+    const uint16_t *hidden_steps;   /* device bf16                            */
+    int64_t step_stride;            /* elements between steps                 */
+    int64_t n;                      /* elements per step (B * L * d)          */
+} dg_hidden_steps;
+int dg_hidden_from_steps(const int32_t *step, const int32_t *canvas, uint16_t *hidden_out,
+                         void *stream, void *user);
+/* dg_hidden_embed_add: hidden_out[r, j] = bf16(base_k[r, j] + table[canvas[r], */
+/* j]) with base_k = base + k * base_step_stride (fp32 sum, nearest even): a  */
+/* stand-in decoder whose output depends on the canvas being denoised (token  */
+/* ids are clamped to [0, V)).                                                */
+typedef struct dg_hidden_embed {
+    const uint16_t *base;           /* device bf16 [rows, d] per step         */
+    int64_t base_step_stride;       /* elements between steps (0: one base)   */
+    const uint16_t *table;          /* device bf16 [V, d]                     */
+    int rows, d, V;
+} dg_hidden_embed;
+int dg_hidden_embed_add(const int32_t *step, const int32_t *canvas, uint16_t *hidden_out,
+                        void *stream, void *user);
+
 /* ------------------------------------------------------------------------ */
 /* Entry points that run one stage of the step on given inputs, through the  */
 /* same device code as dg_denoise_step (for checking each stage alone).      */

@@ -399,9 +399,13 @@ def block(hidden_bits_fn, w_bits: np.ndarray, B: int, L: int, b: float, seed: in
     temperature, adaptive stop; the result is the argmax canvas of the step
     at which a canvas stopped (or of the last step).  ``hidden_bits_fn(k)``
     returns the bf16 hidden states [B*L, d] of step k (the decoder body is
-    outside this path).  Each canvas stops on its own: once its stop test
-    fires, its canvas, argmax and step count are frozen.
+    outside this path); a function of two arguments is called as
+    ``hidden_bits_fn(k, canvas)`` with the canvas [B*L] the step starts from
+    (a decoder that reads the canvas).  Each canvas stops on its own: once its
+    stop test fires, its canvas, argmax and step count are frozen.
     """
+    import inspect
+    two = len(inspect.signature(hidden_bits_fn).parameters) >= 2
     V = w_bits.shape[1]
     canvas = init_canvas(B * L, V, seed).reshape(B, L)
     prev = np.zeros((B, L), np.int32)
@@ -411,7 +415,8 @@ def block(hidden_bits_fn, w_bits: np.ndarray, B: int, L: int, b: float, seed: in
     history = []
     for k in range(max_steps):
         T = temperature(k, max_steps, t0, t1)
-        r = step(hidden_bits_fn(k), w_bits, canvas.reshape(-1), prev.reshape(-1), B, L, T, b,
+        hk = hidden_bits_fn(k, canvas.reshape(-1).copy()) if two else hidden_bits_fn(k)
+        r = step(hk, w_bits, canvas.reshape(-1), prev.reshape(-1), B, L, T, b,
                  seed, k, stop_threshold, workers=workers)
         am = r["argmax"].reshape(B, L)
         cv = r["canvas"].reshape(B, L)
