@@ -149,6 +149,22 @@ int make_map_sw128(CUtensorMap *map, CUtensorMapDataType dt, const void *base, i
     return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
 }
 
+// fp32 rows without swizzle (the self-conditioning table's tiles).
+int make_map_f32_plain(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                       uint32_t box_inner, uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return DG_ERR_CUDA;
+    const cuuint64_t d[2] = {inner, outer};
+    const cuuint64_t st[1] = {inner * 4};
+    const cuuint32_t b[2] = {box_inner, box_outer};
+    const cuuint32_t e[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), d, st, b, e,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
+}
+
 int make_map_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                   const uint64_t *strides_bytes, const uint32_t *box)
 {
@@ -361,8 +377,16 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         if (sco != nullptr) {
             a.sc_table = sco->table;
             a.sc_part = sco->part;
+            CUtensorMap me;
+            int rc = make_map_f32_plain(&me, sco->table, kScDim, static_cast<uint64_t>(p->V),
+                                        kScDim, kDuoScETileRows / 2);
+            if (rc != DG_OK) return rc;
+            DG_CUDA_TRY(launch_kernel(lm_head_duo_sc_kernel, dim3(plan.grid),
+                                      dim3(DuoEpilogue<kDuoCGNarrow>::Threads), kDuoScSmemBytes,
+                                      st, pdl, mx, mw, me, a));
+        } else {
+            DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl));
         }
-        DG_CUDA_TRY(launch_lm_head(plan, mx, mw, a, st, pdl));
         DG_LAUNCHED();
     } else {
         FoldArgs f{};

@@ -143,11 +143,20 @@ __global__ void lm_head_duo_kernel(const __grid_constant__ CUtensorMap map_x,
 // the same kernel with 16 epilogue warps (several row blocks)
 __global__ void lm_head_duo_wide_kernel(const __grid_constant__ CUtensorMap map_x,
                                         const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
-// The 8-epilogue-warp kernel with the self-conditioning read-out folded in
-// (its column groups merge kScDim more words per row through shared memory).
-constexpr int kDuoScSmemBytes = kDuoSmemBytes + (kDuoCGNarrow - 1) * kScDim * 128 * 4;
+// The 8-epilogue-warp kernel with the self-conditioning read-out folded in:
+// its column groups merge kScDim more words per row through shared memory,
+// and the TMA producer stages the table rows of each tile's columns (one
+// box of kDuoScETileRows / 2 rows x kScDim fp32 per 128 columns) into one
+// of two buffers, so the fold reads them from shared memory; the ring has
+// kDuoScStages stages to make room.
+constexpr int kDuoScStages = 4;
+constexpr int kDuoScETileRows = 256;
+constexpr int kDuoScSmemBytes = kDuoScStages * kDuoStageBytes + 1024 + 256 + kPairMergeBytes +
+                                (kDuoCGNarrow - 1) * kScDim * 128 * 4 +
+                                2 * kDuoScETileRows * kScDim * 4;
 __global__ void lm_head_duo_sc_kernel(const __grid_constant__ CUtensorMap map_x,
-                                      const __grid_constant__ CUtensorMap map_w, LmHeadArgs a);
+                                      const __grid_constant__ CUtensorMap map_w,
+                                      const __grid_constant__ CUtensorMap map_e, LmHeadArgs a);
 // FP8 (E4M3) operands of the 2-SM kernel: X8 [M, d] and W8t [V, d] (both
 // K-major, 128-byte k blocks = 128 codes); same tiles, 256 x 256 x 32 UMMAs.
 __global__ void lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,

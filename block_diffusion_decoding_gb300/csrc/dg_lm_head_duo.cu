@@ -63,26 +63,34 @@ constexpr int kDuoAccCols = 256;
 
 template <bool kFp8, int kCG, bool kSC = false>
 DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map_w,
-                                const LmHeadArgs &a)
+                                const LmHeadArgs &a, const CUtensorMap *map_e = nullptr)
 {
+    // the self-conditioning instance gives two stages of the ring to two
+    // buffers of the table E for the tiles in the accumulators
+    constexpr int Stages = kSC ? kDuoScStages : kDuoStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDuoStages * kDuoStageBytes);
-    uint64_t *empty = full + kDuoStages;
-    uint64_t *acc_full = empty + kDuoStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Stages * kDuoStageBytes);
+    uint64_t *empty = full + Stages;
+    uint64_t *acc_full = empty + Stages;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *mma_done = acc_empty + 2;
     uint64_t *mrg_ready = mma_done + 1;
     uint64_t *mrg_done = mrg_ready + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mrg_done + 1);
+    uint64_t *e_full = mrg_done + 1;      // kSC: E buffer b holds the table rows of
+    uint64_t *e_empty = e_full + 2;       // the tile in accumulator buffer b
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(e_empty + 2);
     constexpr int CG = DuoEpilogue<kCG>::CG;            // epilogue column groups
     constexpr int EpiWarps = DuoEpilogue<kCG>::Warps;
-    const GroupMerge gm{reinterpret_cast<float *>(smem + kDuoStages * kDuoStageBytes + 256),
+    const GroupMerge gm{reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256),
                         mrg_ready, mrg_done, CG, 128};
-    const ScMerge sm{reinterpret_cast<float *>(smem + kDuoStages * kDuoStageBytes + 256 +
+    const ScMerge sm{reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256 +
                                                kPairMergeBytes),
                      a.sc_part};
+    // kSC: two E buffers of kDuoScETileRows x kScDim fp32 each
+    float *ebuf = reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256 + kPairMergeBytes +
+                                            (kCG - 1) * kScDim * 128 * 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = static_cast<int>(cluster_ctarank());          // row / column half
@@ -94,7 +102,7 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     const int w_half_bytes = a.BN * 64;
 
     if (warp == 0 && lane == 0) {
-        for (int s = 0; s < kDuoStages; ++s) {
+        for (int s = 0; s < Stages; ++s) {
             mbar_init(&full[s], 1);          // used in the even CTA only
             mbar_init(&empty[s], 1);
         }
@@ -105,9 +113,16 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
         mbar_init(mma_done, 1);
         mbar_init(mrg_ready, EpiWarps - EpiWarps / CG);
         mbar_init(mrg_done, EpiWarps / CG);
+        if constexpr (kSC) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&e_full[b], 1);
+                mbar_init(&e_empty[b], EpiWarps);
+            }
+        }
         fence_barrier_init();
         tma_prefetch_desc(&map_x);
         tma_prefetch_desc(&map_w);
+        if constexpr (kSC) tma_prefetch_desc(map_e);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, 512);
@@ -150,13 +165,30 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             int s = 0;
             uint32_t ph = 0;
             uint32_t armed = 0, armed_par = 0;
+            uint32_t earmed = 0, earmed_par = 0;
             bool ok = true;
-            for (int t = t0, span = 1; t < t1 && ok; t += span) {
+            int ti = 0;
+            for (int t = t0, span = 1; t < t1 && ok; t += span, ++ti) {
                 span = duo_tile_span(a, t, t1);
                 const int m = t / a.ntn, n = t % a.ntn;
                 const int bn = span * a.BN;                     // columns of this tile
                 const uint32_t stage_tx =
                     static_cast<uint32_t>(kPairABytes + span * w_half_bytes);
+                if constexpr (kSC) {
+                    // this CTA's copy of the table rows of the tile's columns
+                    const int b = ti & 1;
+                    const uint32_t eu = static_cast<uint32_t>(ti >> 1);
+                    if (!mbar_wait(&e_empty[b], (eu & 1u) ^ 1u, a.ws, 408)) { ok = false; break; }
+                    const int nbox = (bn + kDuoScETileRows / 2 - 1) / (kDuoScETileRows / 2);
+                    mbar_arrive_expect_tx(&e_full[b],
+                                          static_cast<uint32_t>(nbox * (kDuoScETileRows / 2) * kScDim * 4));
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(ebuf + (static_cast<size_t>(b) * kDuoScETileRows +
+                                            j * (kDuoScETileRows / 2)) * kScDim,
+                                    map_e, &e_full[b], 0, n * a.BN + j * (kDuoScETileRows / 2), pol_x);
+                    earmed |= 1u << b;
+                    earmed_par = (earmed_par & ~(1u << b)) | ((eu & 1u) << b);
+                }
                 for (int kb = 0; kb < a.kblocks; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.ws, 401)) { ok = false; break; }
                     if (r == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_tx);
@@ -184,14 +216,17 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                     }
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
-                    if (++s == kDuoStages) { s = 0; ph ^= 1u; }
+                    if (++s == Stages) { s = 0; ph ^= 1u; }
                 }
             }
             // the even CTA: every copy of both CTAs has landed before the
             // closing cluster barrier lets either CTA leave
             if (r == 0)
-                for (int q = 0; q < kDuoStages; ++q)
+                for (int q = 0; q < Stages; ++q)
                     if (armed >> q & 1u) mbar_wait(&full[q], armed_par >> q & 1u, a.ws, 402);
+            if constexpr (kSC)
+                for (int b = 0; b < 2; ++b)
+                    if (earmed >> b & 1u) mbar_wait(&e_full[b], earmed_par >> b & 1u, a.ws, 409);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
@@ -238,7 +273,7 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                         }
                     }
                     umma_commit_pair(&empty[s], 0x3);
-                    if (++s == kDuoStages) { s = 0; ph ^= 1u; }
+                    if (++s == Stages) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit_pair(&acc_full[acc], 0x3);
@@ -294,9 +329,14 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
             st.glb = fmaxf(st.glb, key_score(key));
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * kDuoAccCols);
             if constexpr (kSC) {
-                fold_tile_sc(st, sc, a.sc_table, tb, 16 * cg, 16 * CG, bn,
-                             static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
-                             static_cast<uint32_t>(row), fc, live);
+                const int b = i & 1;
+                const bool eok = mbar_wait(&e_full[b], (use & 1u), a.ws, 410);
+                if (!__all_sync(0xFFFFFFFFu, eok)) break;
+                fold_tile_sc(st, sc, ebuf + static_cast<size_t>(b) * kDuoScETileRows * kScDim, tb,
+                             16 * cg, 16 * CG, bn, static_cast<uint32_t>(n * a.BN),
+                             static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&e_empty[b]);
             } else if constexpr (kFp8) {
                 const float rs = live ? __ldg(a.row_scale + row) : 0.f;
                 fold_tile_scaled(st, tb, 16 * cg, 16 * CG, bn,
@@ -370,9 +410,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWi
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGNarrow>::Threads, 1)
     lm_head_duo_sc_kernel(const __grid_constant__ CUtensorMap map_x,
-                          const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
+                          const __grid_constant__ CUtensorMap map_w,
+                          const __grid_constant__ CUtensorMap map_e, LmHeadArgs a)
 {
-    lm_head_duo_body<false, kDuoCGNarrow, true>(map_x, map_w, a);
+    lm_head_duo_body<false, kDuoCGNarrow, true>(map_x, map_w, a, &map_e);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWide>::Threads, 1)

@@ -151,16 +151,16 @@ inline bool use_pdl(cudaStream_t st)
     return cs == cudaStreamCaptureStatusNone;
 }
 
-// Launch the planned LM-head kernel (maps: X box {64, 128} for the cluster
+// Launch the planned LM-head kernel, not the self-conditioning instance,
+// which takes a third map (maps: X box {64, 128} for the cluster
 // kernels, {64, 256} otherwise; W box {64, 64}; FP8: X8 box {128, 128}, W8t
 // box {128, BN / 2}).  a.fuse2 must be set for kLmDuoFused.
 inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, const CUtensorMap &mw,
                                   const LmHeadArgs &a, cudaStream_t st, bool pdl, bool fp8 = false)
 {
-    const int smem = plan.sc ? kDuoScSmemBytes : lm_smem_bytes(plan.kind);
+    const int smem = lm_smem_bytes(plan.kind);
     const bool wide = plan.epi_warps == 4 * kDuoCGWide;
     auto kern = fp8                    ? lm_head_duo_fp8_kernel
-                : plan.sc                ? lm_head_duo_sc_kernel
                 : plan.kind == kLmSingle ? lm_head_kernel
                 : wide                   ? lm_head_duo_wide_kernel   // kLmDuo, kLmDuoFused
                                          : lm_head_duo_kernel;

@@ -89,15 +89,15 @@ DG_DEVICE void sc_scale(ScAcc &a, float f)
     for (int k = 0; k < kScDim / 2; ++k) a.o[k] = mul2(a.o[k], f2);
 }
 
-// o += e E[v, :] for one vocabulary row erow (kScDim fp32, 16-byte aligned;
-// every lane of a warp reads the same row, a broadcast).
+// o += e E[v, :] for one vocabulary row erow (kScDim fp32 in shared memory,
+// 16-byte aligned; every lane of a warp reads the same row, a broadcast).
 DG_DEVICE void sc_add_row(ScAcc &a, float e, const float *__restrict__ erow)
 {
     const float4 *e4 = reinterpret_cast<const float4 *>(erow);
     const float2 ev = make_float2(e, e);
 #pragma unroll
     for (int q = 0; q < kScDim / 4; ++q) {
-        const float4 r = __ldg(e4 + q);
+        const float4 r = e4[q];
         a.o[2 * q] = fma2(ev, make_float2(r.x, r.y), a.o[2 * q]);
         a.o[2 * q + 1] = fma2(ev, make_float2(r.z, r.w), a.o[2 * q + 1]);
     }
@@ -180,8 +180,8 @@ DG_DEVICE uint32_t gumbel_word_threshold(float t)
 // `row` into the state.  Entries >= V are ignored; a lane with live == false
 // (a row past the end) leaves its state alone.  Must be called by all 32
 // lanes of the warp together (it votes across the warp).
-// With kSC, the self-conditioning part sc (table E [V, kScDim]) is folded
-// along with S.
+// With kSC, the self-conditioning part sc is folded along with S; E points
+// at the table row of vocabulary entry v0 (rows kScDim floats apart).
 template <bool kSC>
 DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
                         uint32_t row, const FoldConsts &fc, bool live, ScAcc *sc,
@@ -242,10 +242,9 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
         if (live) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                if (full || v0 + 2 * q < V)
-                    sc_add_row(*sc, es[q].x, E + static_cast<size_t>(v0 + 2 * q) * kScDim);
+                if (full || v0 + 2 * q < V) sc_add_row(*sc, es[q].x, E + (2 * q) * kScDim);
                 if (full || v0 + 2 * q + 1 < V)
-                    sc_add_row(*sc, es[q].y, E + static_cast<size_t>(v0 + 2 * q + 1) * kScDim);
+                    sc_add_row(*sc, es[q].y, E + (2 * q + 1) * kScDim);
             }
         }
     }
@@ -443,8 +442,9 @@ DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int B
     }
 }
 
-// fold_tile with the self-conditioning part (table E [V, kScDim]).
-DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const float *__restrict__ E, uint32_t tb,
+// fold_tile with the self-conditioning part: Et holds the table rows of the
+// tile's columns vbase, vbase + 1, ... (kScDim floats each, shared memory).
+DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const float *__restrict__ Et, uint32_t tb,
                             int first, int stride, int BN, uint32_t vbase, uint32_t V,
                             uint32_t row, const FoldConsts &fc, bool live)
 {
@@ -453,7 +453,7 @@ DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const float *__restrict__ E
         float lg[16];
         tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
         const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
-        if (v0 < V) fold16_t<true>(st, lg, v0, V, row, fc, live, &sc, E);
+        if (v0 < V) fold16_t<true>(st, lg, v0, V, row, fc, live, &sc, Et + c0 * kScDim);
     }
 }
 
