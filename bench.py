@@ -318,7 +318,7 @@ def _traffic_record(kernel_sources, kernel, shape):
         return None
 
 
-def run_ours(args, cfg):
+def run_ours(args, cfg, emit=True):
     import torch
     import block_diffusion_decoding_gb300 as dg
     from block_diffusion_decoding_gb300 import build as dgbuild
@@ -563,11 +563,13 @@ def run_ours(args, cfg):
         e2e=dict(value=_replica_value(world, e2e_ms), unit="steps/s", h2d_bytes_per_step=h2d,
                  d2h_bytes_per_step=d2h),
         clocks=clk.summary(), gpu_launches=launches, device_status=status)
+    if not emit:
+        return line
     print(json.dumps(line), flush=True)
     return 0
 
 # ----------------------------------------------------------------------------- block loop
-def run_block(args, cfg):
+def run_block(args, cfg, emit=True):
     """The block loop (dg_generate_block, one CUDA graph per block) on the
     converging workload: hidden(k) = g_k(c) W[:,t]/|W[:,t]| + N(0, 1/d) for
     per-position targets t ~ U(V) and confidences c ~ U(0, 1); a block runs
@@ -730,12 +732,14 @@ def run_block(args, cfg):
         gpu_launches=args.steps * (1 + 2 * steps), gpu_launches_note="graph replays: loop init "
         "+ 2 kernels per step (LM head, combine/accept) per block",
         device_status=status)
+    if not emit:
+        return line
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ----------------------------------------------------------------------------- encoder append
-def run_encoder(args, cfg):
+def run_encoder(args, cfg, emit=True):
     """The encoder cache append (dg_encoder_append): the committed block's K/V
     appended to a cache holding P tokens and the block's causal attention over
     [cache ; block].  Timed per call with the L2 flushed before each; the cache
@@ -812,12 +816,14 @@ def run_encoder(args, cfg):
                       algorithmic_flops=flops),
         step_roofline_ms=roof_ms, step_frac_of_roofline=roof_ms / ms,
         clocks=clk.summary(), device_status=status)
+    if not emit:
+        return line
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ----------------------------------------------------------------------------- MoE FFN
-def run_moe(args, mcfg):
+def run_moe(args, mcfg, emit=True):
     """One MoE FFN layer over the canvas (dg_moe_ffn): router, top-8 of 128
     experts plus the shared one, gated GELU experts, weighted sum.  K timed
     layers, L2 flushed before each; value = layers per second.  Roofline:
@@ -952,6 +958,8 @@ def run_moe(args, mcfg):
         e2e=dict(value=_replica_value(world, e2e_ms), unit="layers/s",
                  h2d_bytes_per_step=M * d * 2, d2h_bytes_per_step=M * d * 4),
         clocks=clk.summary(), gpu_launches=launches, device_status=status)
+    if not emit:
+        return line
     print(json.dumps(line), flush=True)
     return 0
 
@@ -1038,6 +1046,74 @@ def run_kernel_only(args, cfg):
     return 0
 
 
+# ----------------------------------------------------------------------------- workload sweep
+SWEEP = [
+    # (name in the line, config, options): every configuration of the step, the
+    # block loop, the encoder append and the widened rows, each in its own
+    # timed region of at least 200 steps (10 blocks for the loop)
+    ("step_small", "step_small", {}),
+    ("batch1", "batch1", {}),
+    ("batch4", "batch4", {}),
+    ("batch16", "batch16", {}),
+    ("long_context", "long_context", {}),
+    ("block_full", "block_full", {"steps": 10}),
+    ("step_full_fp8", "step_full", {"lm_dtype": "fp8"}),
+    ("step_full_self_cond", "step_full", {"self_cond": True}),
+    ("encoder_full", "encoder_full", {}),
+    ("moe_full", "moe_full", {}),
+]
+
+
+def _compact(line):
+    """The numbers of a sub-run kept in the headline's workloads object."""
+    keep = ("metric", "value", "unit", "ms_per_step", "steps", "canvas_tokens_per_s",
+            "step_roofline_ms", "step_frac_of_roofline", "steps_to_stop", "commits_per_step",
+            "flat_case_one_commit_per_step_48_steps", "distinct_experts", "block_ms",
+            "TFLOP_per_s", "device_status", "gpu_launches")
+    out = {k: line[k] for k in keep if k in line}
+    out["workload"] = line["config"]["workload"]
+    if line.get("roofline"):
+        r = line["roofline"]
+        out["roofline"] = {k: r.get(k) for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                  "kernel")}
+    if line.get("kernels"):
+        out["kernels"] = {k: {kk: v.get(kk) for kk in ("ms", "frac_of_roofline", "roofline_ms")}
+                          for k, v in line["kernels"].items()}
+    if line.get("e2e"):
+        out["e2e"] = line["e2e"]["value"]
+    if line.get("clocks"):
+        out["clocks"] = line["clocks"]
+    return out
+
+
+def run_sweep(args):
+    """Every other workload, measured in the same process after the headline."""
+    import copy
+    res = {}
+    for name, cname, opt in SWEEP:
+        a = copy.copy(args)
+        a.steps = max(200, args.steps) if "steps" not in opt else opt["steps"]
+        a.warmup = max(5, args.warmup)
+        a.no_cpu_baseline = True
+        a.lm_dtype = opt.get("lm_dtype", "bf16")
+        a.self_cond = opt.get("self_cond", False)
+        try:
+            if cname in dg_synth.MOE_CONFIGS:
+                line = run_moe(a, dg_synth.MOE_CONFIGS[cname], emit=False)
+            else:
+                cfg = dg_synth.CONFIGS[cname]
+                if cfg.name == "block_full":
+                    line = run_block(a, cfg, emit=False)
+                elif cfg.name.startswith("encoder"):
+                    line = run_encoder(a, cfg, emit=False)
+                else:
+                    line = run_ours(a, cfg, emit=False)
+            res[name] = _compact(line)
+        except Exception as e:      # a workload that fails is reported, not hidden
+            res[name] = {"error": "%s: %s" % (type(e).__name__, e)}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1049,6 +1125,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lm-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="LM-head operands: bf16, or E4M3 codes with per-row / per-column scales")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the sweep of the other workloads after the headline step")
     ap.add_argument("--self-cond", action="store_true",
                     help="the step with the self-conditioning read-out folded into the LM head")
     ap.add_argument("--kernel", choices=["attention", "lm_head"],
@@ -1068,7 +1146,16 @@ def main():
         return run_block(args, cfg)
     if cfg.name.startswith("encoder"):
         return run_encoder(args, cfg)
-    return run_ours(args, cfg)
+    world = _dist()[0]
+    sweep = (cfg.name == DEFAULT_CONFIG and world == 1 and not args.no_workloads
+             and args.lm_dtype == "bf16" and not args.self_cond)
+    line = run_ours(args, cfg, emit=False)
+    if line == 0:        # ranks other than 0
+        return 0
+    if sweep:
+        line["workloads"] = run_sweep(args)
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 if __name__ == "__main__":

@@ -1096,33 +1096,36 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     a.out = out;
     a.ws = static_cast<WsHeader *>(workspace);
 
-    CUtensorMap mwg, mwu, mwd, mxs, mhs;
+    MoeMaps maps;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(f),
                                   static_cast<uint64_t>(E + 1)};
         const uint64_t strides[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(f) * d * 2};
         const uint32_t box[3] = {64, 128, 1};
-        if ((rc = make_map_bf16(&mwg, w_gate, 3, dims, strides, box)) != DG_OK) return rc;
-        if ((rc = make_map_bf16(&mwu, w_up, 3, dims, strides, box)) != DG_OK) return rc;
+        if ((rc = make_map_bf16(&maps.wg, w_gate, 3, dims, strides, box)) != DG_OK) return rc;
+        if ((rc = make_map_bf16(&maps.wu, w_up, 3, dims, strides, box)) != DG_OK) return rc;
     }
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(f), static_cast<uint64_t>(d),
                                   static_cast<uint64_t>(E + 1)};
         const uint64_t strides[2] = {static_cast<uint64_t>(f) * 2, static_cast<uint64_t>(d) * f * 2};
         const uint32_t box[3] = {64, 128, 1};
-        if ((rc = make_map_bf16(&mwd, w_down, 3, dims, strides, box)) != DG_OK) return rc;
+        if ((rc = make_map_bf16(&maps.wd, w_down, 3, dims, strides, box)) != DG_OK) return rc;
     }
-    {
-        const uint64_t dims[2] = {static_cast<uint64_t>(d), R};
-        const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
-        const uint32_t box[2] = {64, kMoeChunk};
-        if ((rc = make_map_bf16(&mxs, a.x_sorted, 2, dims, strides, box)) != DG_OK) return rc;
-    }
-    {
-        const uint64_t dims[2] = {static_cast<uint64_t>(f), R};
-        const uint64_t strides[1] = {static_cast<uint64_t>(f) * 2};
-        const uint32_t box[2] = {64, kMoeChunk};
-        if ((rc = make_map_bf16(&mhs, a.h_sorted, 2, dims, strides, box)) != DG_OK) return rc;
+    for (int i = 0; i < kMoeBoxes; ++i) {
+        const uint32_t rows = 16u << i;
+        {
+            const uint64_t dims[2] = {static_cast<uint64_t>(d), R};
+            const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
+            const uint32_t box[2] = {64, rows};
+            if ((rc = make_map_bf16(&maps.xs[i], a.x_sorted, 2, dims, strides, box)) != DG_OK) return rc;
+        }
+        {
+            const uint64_t dims[2] = {static_cast<uint64_t>(f), R};
+            const uint64_t strides[1] = {static_cast<uint64_t>(f) * 2};
+            const uint32_t box[2] = {64, rows};
+            if ((rc = make_map_bf16(&maps.hs[i], a.h_sorted, 2, dims, strides, box)) != DG_OK) return rc;
+        }
     }
     cudaStream_t st = as_stream(stream);
     const bool pdl = use_pdl(st);
@@ -1139,7 +1142,7 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
                               dim3(256), 0, st, pdl, a));
     DG_LAUNCHED();
     DG_CUDA_TRY(launch_kernel(moe_ffn_kernel, dim3(di->sms), dim3(192), moe_ffn_smem_bytes(), st,
-                              pdl, mwg, mwu, mwd, mxs, mhs, a));
+                              pdl, maps, a));
     DG_LAUNCHED();
     const uint64_t cvec = static_cast<uint64_t>(M) * (d / 4);
     DG_CUDA_TRY(launch_kernel(moe_combine_kernel,

@@ -273,14 +273,17 @@ __global__ void moe_router_kernel(const uint16_t *__restrict__ x, const uint16_t
 __global__ void moe_route_kernel(MoeArgs a);
 __global__ void moe_gather_kernel(MoeArgs a);
 __global__ void moe_combine_kernel(MoeArgs a);
-// maps: gate / up weights [E+1, f, d] as {d, f, E+1}, box {64, 128, 1}; down
-// weights [E+1, d, f] as {f, d, E+1}, box {64, 128, 1}; X_sorted / H_sorted
-// as {d or f, rows}, box {64, 128}
-__global__ void moe_ffn_kernel(const __grid_constant__ CUtensorMap map_wg,
-                               const __grid_constant__ CUtensorMap map_wu,
-                               const __grid_constant__ CUtensorMap map_wd,
-                               const __grid_constant__ CUtensorMap map_xs,
-                               const __grid_constant__ CUtensorMap map_hs, MoeArgs a);
+// Tensor maps of the expert GEMMs: gate / up weights [E+1, f, d] as
+// {d, f, E+1}, box {64, 128, 1}; down weights [E+1, d, f] as {f, d, E+1},
+// box {64, 128, 1}; X_sorted / H_sorted as {d or f, rows} with boxes of
+// {64, 16 << i} rows (a token chunk loads the smallest box that holds it).
+constexpr int kMoeBoxes = 4;
+struct MoeMaps {
+    CUtensorMap wg, wu, wd;
+    CUtensorMap xs[kMoeBoxes];
+    CUtensorMap hs[kMoeBoxes];
+};
+__global__ void moe_ffn_kernel(const __grid_constant__ MoeMaps maps, MoeArgs a);
 int moe_ffn_smem_bytes();
 
 }  // namespace dg

@@ -286,10 +286,7 @@ int moe_ffn_smem_bytes() { return kMoeStages * kMoeStageBytes + 1024 + 512; }
 // from warp 0 to warps 1-5 through a small queue in shared memory.  A down
 // item of expert e, chunk c waits (bounded) until every gate/up item of that
 // (e, c) has stored its part of H_sorted.
-__global__ void __launch_bounds__(192, 1)
-    moe_ffn_kernel(const __grid_constant__ CUtensorMap map_wg, const __grid_constant__ CUtensorMap map_wu,
-                   const __grid_constant__ CUtensorMap map_wd, const __grid_constant__ CUtensorMap map_xs,
-                   const __grid_constant__ CUtensorMap map_hs, MoeArgs a)
+__global__ void __launch_bounds__(192, 1) moe_ffn_kernel(const __grid_constant__ MoeMaps maps, MoeArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -320,11 +317,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
-        tma_prefetch_desc(&map_wg);
-        tma_prefetch_desc(&map_wu);
-        tma_prefetch_desc(&map_wd);
-        tma_prefetch_desc(&map_xs);
-        tma_prefetch_desc(&map_hs);
+        tma_prefetch_desc(&maps.wg);
+        tma_prefetch_desc(&maps.wu);
+        tma_prefetch_desc(&maps.wd);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -375,21 +370,23 @@ __global__ void __launch_bounds__(192, 1)
                     fence_proxy_async_global();
                 }
                 const int kblocks = (up ? a.d : a.f) / 64;
-                const uint32_t tx = static_cast<uint32_t>((up ? 2 : 1) * kMoeATile + kMoeBTile);
+                // the smallest token box that holds the chunk: 16, 32, 64 or 128 rows
+                const int bx = w.w <= 16 ? 0 : w.w <= 32 ? 1 : w.w <= 64 ? 2 : 3;
+                const CUtensorMap *mb = up ? &maps.xs[bx] : &maps.hs[bx];
+                const uint32_t tx = static_cast<uint32_t>((up ? 2 : 1) * kMoeATile + (16 << bx) * 128);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, a.ws, 703)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], tx);
                     uint8_t *sa = smem + s * kMoeStageBytes;
                     uint8_t *sb = sa + 2 * kMoeATile;
                     if (up) {
-                        tma_load_3d(sa, &map_wg, &full[s], kb * 64, (w.y & 255) * 128, w.x, pol_w);
-                        tma_load_3d(sa + kMoeATile, &map_wu, &full[s], kb * 64, (w.y & 255) * 128,
+                        tma_load_3d(sa, &maps.wg, &full[s], kb * 64, (w.y & 255) * 128, w.x, pol_w);
+                        tma_load_3d(sa + kMoeATile, &maps.wu, &full[s], kb * 64, (w.y & 255) * 128,
                                     w.x, pol_w);
-                        tma_load_2d(sb, &map_xs, &full[s], kb * 64, w.z, pol_x);
                     } else {
-                        tma_load_3d(sa, &map_wd, &full[s], kb * 64, (w.y & 255) * 128, w.x, pol_w);
-                        tma_load_2d(sb, &map_hs, &full[s], kb * 64, w.z, pol_x);
+                        tma_load_3d(sa, &maps.wd, &full[s], kb * 64, (w.y & 255) * 128, w.x, pol_w);
                     }
+                    tma_load_2d(sb, mb, &full[s], kb * 64, w.z, pol_x);
                     armed |= 1u << s;
                     armed_par = (armed_par & ~(1u << s)) | (ph << s);
                     if (++s == kMoeStages) { s = 0; ph ^= 1u; }
