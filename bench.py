@@ -413,11 +413,22 @@ def run_ours(args, cfg, emit=True):
         else:
             dg.lm_head_fold(x, w, p0, sws)
 
+    # The canvas attention and the LM head read different inputs in this step
+    # (the hidden states are given), so the attention runs on a second stream
+    # forked from and joined back into the step's stream: the step ends when
+    # both have.
+    side = torch.cuda.Stream(dev)
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+
     def step(k):
-        dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws)
+        fork.record(stream)
+        side.wait_event(fork)
+        dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws, stream=side)
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold,
                            k, seed=rank)
         lm_step(p)
+        join.record(side)
+        stream.wait_event(join)
 
     def timed(fn, n, first):
         """Per-iteration CUDA-event times (ms) with an L2 flush before each iteration."""

@@ -131,12 +131,20 @@ def test_python_producer_runs_once_per_graph():
     user = dg.HiddenSteps(0, 0, 0)            # unused by this producer; a distinct key
     buf = torch.empty(cfg.L, cfg.d, dtype=torch.bfloat16, device=DEV)
     w = to_dev(wb)
-    a = _run_fn(fn, user, buf, w, 1, cfg.L, cfg.d, cfg.V, 6)
-    b = _run_fn(fn, user, buf, w, 1, cfg.L, cfg.d, cfg.V, 6)   # same key: the graph is reused
+    p = dg.step_params(1, cfg.L, cfg.d, cfg.V, 0.8, 0.1, 0.005, step=0, seed=6)
+    bp = dg.block_params(N, 0.8, 0.4, 0)
+    bufs = dg.BlockBuffers(1, cfg.L, N, DEV)
+    ws = dg.workspace(dg.generate_block_workspace(p, bp), DEV)
+    results = []
+    for _ in range(3):              # the same arguments: the captured graph is replayed
+        dg.generate_block_fn(fn, user, buf, w, p, bp, bufs, ws)
+        torch.cuda.synchronize()
+        status_ok(ws)
+        results.append((np_i32(bufs.argmax).copy(), int(bufs.steps_taken[0])))
     assert len(calls) == 1
-    assert np.array_equal(np_i32(a.argmax), np_i32(b.argmax))
+    assert all(np.array_equal(r[0], results[0][0]) and r[1] == results[0][1] for r in results)
     ref = oracle.block(lambda k: hs[k], wb, 1, cfg.L, 0.1, 6, max_steps=N)
-    assert int(a.steps_taken[0]) == int(ref["steps"][0])
+    assert results[0][1] == int(ref["steps"][0])
 
 
 def test_three_canvases_through_cache_append():
