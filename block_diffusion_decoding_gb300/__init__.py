@@ -262,7 +262,7 @@ def denoise_step_sc_workspace(p: StepParams) -> int:
 
 def denoise_step_sc(hidden, w, sc_table, p: StepParams, bufs: StepBuffers, sc_out, workspace,
                     stream=None):
-    """dg_denoise_step_sc: sc_table [V, 32] fp32, sc_out [B*L, 32] fp32."""
+    """dg_denoise_step_sc: sc_table [V, 32] bf16, sc_out [B*L, 32] fp32."""
     io = bufs.io()
     rc = _lib().dg_denoise_step_sc(_p(hidden), _p(w), _p(sc_table), ctypes.byref(p),
                                    ctypes.byref(io), _p(sc_out), _p(workspace), workspace.numel(),

@@ -149,17 +149,17 @@ int make_map_sw128(CUtensorMap *map, CUtensorMapDataType dt, const void *base, i
     return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
 }
 
-// fp32 rows without swizzle (the self-conditioning table's tiles).
-int make_map_f32_plain(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
-                       uint32_t box_inner, uint32_t box_outer)
+// bf16 rows without swizzle (the self-conditioning table's tiles).
+int make_map_bf16_plain(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return DG_ERR_CUDA;
     const cuuint64_t d[2] = {inner, outer};
-    const cuuint64_t st[1] = {inner * 4};
+    const cuuint64_t st[1] = {inner * 2};
     const cuuint32_t b[2] = {box_inner, box_outer};
     const cuuint32_t e[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), d, st, b, e,
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), d, st, b, e,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
@@ -285,7 +285,7 @@ struct Fp8Operands {
 // Self-conditioning read-out of the step: the table E [V, kScDim], the
 // per-(row, unit) parts in the workspace and the read-out [M, kScDim].
 struct ScOperands {
-    const float *table;
+    const uint16_t *table;
     float *part;
     float *out;
 };
@@ -378,8 +378,8 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
             a.sc_table = sco->table;
             a.sc_part = sco->part;
             CUtensorMap me;
-            int rc = make_map_f32_plain(&me, sco->table, kScDim, static_cast<uint64_t>(p->V),
-                                        kScDim, kDuoScETileRows / 2);
+            int rc = make_map_bf16_plain(&me, sco->table, kScDim, static_cast<uint64_t>(p->V),
+                                         kScDim, kDuoScETileRows / 2);
             if (rc != DG_OK) return rc;
             DG_CUDA_TRY(launch_kernel(lm_head_duo_sc_kernel, dim3(plan.grid),
                                       dim3(DuoEpilogue<kDuoCGNarrow>::Threads), kDuoScSmemBytes,
@@ -727,7 +727,7 @@ size_t sc_ws_bytes(const dg_step_params *p, size_t *off_sc)
     return off + round_up(static_cast<size_t>(slots) * M * kScDim * 4, 256);
 }
 
-int sc_step(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+int sc_step(const uint16_t *hidden, const uint16_t *w, const uint16_t *sc_table,
             const dg_step_params *p, const dg_step_io *io, float *sc_out, void *workspace,
             size_t workspace_bytes, void *stream, bool lm_only)
 {
@@ -1032,14 +1032,14 @@ size_t dg_denoise_step_sc_workspace(const dg_step_params *p)
     return sc_ws_bytes(p, nullptr);
 }
 
-int dg_denoise_step_sc(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+int dg_denoise_step_sc(const uint16_t *hidden, const uint16_t *w, const uint16_t *sc_table,
                        const dg_step_params *p, const dg_step_io *io, float *sc_out,
                        void *workspace, size_t workspace_bytes, void *stream)
 {
     return sc_step(hidden, w, sc_table, p, io, sc_out, workspace, workspace_bytes, stream, false);
 }
 
-int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const uint16_t *sc_table,
                        const dg_step_params *p, void *workspace, size_t workspace_bytes,
                        void *stream)
 {

@@ -89,8 +89,8 @@ struct LmHeadArgs {
     // launches); null: not shared
     uint32_t *rowkey;
     // self-conditioning read-out (lm_head_duo_sc_kernel only): table E
-    // [V, kScDim] fp32 and the per-(row, unit) parts [M][units][kScDim]
-    const float *sc_table;
+    // [V, kScDim] bf16 and the per-(row, unit) parts [M][units][kScDim] fp32
+    const uint16_t *sc_table;
     float *sc_part;
 };
 
@@ -146,14 +146,15 @@ __global__ void lm_head_duo_wide_kernel(const __grid_constant__ CUtensorMap map_
 // The 8-epilogue-warp kernel with the self-conditioning read-out folded in:
 // its column groups merge kScDim more words per row through shared memory,
 // and the TMA producer stages the table rows of each tile's columns (one
-// box of kDuoScETileRows / 2 rows x kScDim fp32 per 128 columns) into one
-// of two buffers, so the fold reads them from shared memory; the ring has
+// box of kDuoScETileRows / 2 rows x kScDim bf16 per 128 columns) into one
+// of two buffers, so the fold reads them from shared memory; every epilogue
+// warp has a 1 KB staging buffer for its chunk's weights; the ring has
 // kDuoScStages stages to make room.
 constexpr int kDuoScStages = 4;
 constexpr int kDuoScETileRows = 256;
 constexpr int kDuoScSmemBytes = kDuoScStages * kDuoStageBytes + 1024 + 256 + kPairMergeBytes +
                                 (kDuoCGNarrow - 1) * kScDim * 128 * 4 +
-                                2 * kDuoScETileRows * kScDim * 4;
+                                2 * kDuoScETileRows * kScDim * 2 + 4 * kDuoCGNarrow * 32 * 16 * 2;
 __global__ void lm_head_duo_sc_kernel(const __grid_constant__ CUtensorMap map_x,
                                       const __grid_constant__ CUtensorMap map_w,
                                       const __grid_constant__ CUtensorMap map_e, LmHeadArgs a);

@@ -88,9 +88,11 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     const ScMerge sm{reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256 +
                                                kPairMergeBytes),
                      a.sc_part};
-    // kSC: two E buffers of kDuoScETileRows x kScDim fp32 each
-    float *ebuf = reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256 + kPairMergeBytes +
-                                            (kCG - 1) * kScDim * 128 * 4);
+    // kSC: two E buffers of kDuoScETileRows x kScDim bf16 each, then a 1 KB
+    // P staging buffer per epilogue warp
+    uint16_t *ebuf = reinterpret_cast<uint16_t *>(smem + Stages * kDuoStageBytes + 256 +
+                                                  kPairMergeBytes + (kCG - 1) * kScDim * 128 * 4);
+    uint16_t *pbuf_all = ebuf + 2 * kDuoScETileRows * kScDim;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = static_cast<int>(cluster_ctarank());          // row / column half
@@ -181,7 +183,7 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                     if (!mbar_wait(&e_empty[b], (eu & 1u) ^ 1u, a.ws, 408)) { ok = false; break; }
                     const int nbox = (bn + kDuoScETileRows / 2 - 1) / (kDuoScETileRows / 2);
                     mbar_arrive_expect_tx(&e_full[b],
-                                          static_cast<uint32_t>(nbox * (kDuoScETileRows / 2) * kScDim * 4));
+                                          static_cast<uint32_t>(nbox * (kDuoScETileRows / 2) * kScDim * 2));
                     for (int j = 0; j < nbox; ++j)
                         tma_load_2d(ebuf + (static_cast<size_t>(b) * kDuoScETileRows +
                                             j * (kDuoScETileRows / 2)) * kScDim,
@@ -332,9 +334,10 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                 const int b = i & 1;
                 const bool eok = mbar_wait(&e_full[b], (use & 1u), a.ws, 410);
                 if (!__all_sync(0xFFFFFFFFu, eok)) break;
-                fold_tile_sc(st, sc, ebuf + static_cast<size_t>(b) * kDuoScETileRows * kScDim, tb,
-                             16 * cg, 16 * CG, bn, static_cast<uint32_t>(n * a.BN),
-                             static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+                fold_tile_sc(st, sc, ebuf + static_cast<size_t>(b) * kDuoScETileRows * kScDim,
+                             pbuf_all + (warp - 4) * 32 * 16, tb, 16 * cg, 16 * CG, bn,
+                             static_cast<uint32_t>(n * a.BN), static_cast<uint32_t>(a.V),
+                             static_cast<uint32_t>(row), fc, live);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&e_empty[b]);
             } else if constexpr (kFp8) {

@@ -58,21 +58,36 @@ DG_DEVICE void row_state_init(RowState &s)
 
 // Self-conditioning read-out ("Parallel Denoising From an Autoregressive
 // Checkpoint", section "Finding": a 7.8M-parameter block feeds the previous
-// prediction back; its matmul runs in full precision in the sampling stage).
-// Per canvas row, sc = sum_v softmax(logits / T)_v E[v, :] over a table
-// E [V, kScDim] (fp32).  The fold keeps o = sum_v 2^(t_v - m) E[v, :] next to
-// S, rescaled with it whenever the running maximum m moves; a merge weighs
-// each part by 2^(m_part - m); the read-out is o / S.
+// prediction back; its matmul runs in the sampling stage next to the
+// full-vocabulary softmax).  Per canvas row, sc = sum_v softmax(logits /
+// T)_v E[v, :] over a table E [V, kScDim] (bf16).  The fold keeps
+// o = sum_v 2^(t_v - m) E[v, :] next to S, rescaled with it whenever the
+// running maximum m moves; a merge weighs each part by 2^(m_part - m); the
+// read-out is o / S.
+//
+// A warp folds 32 rows (one per lane) x 16 columns per chunk, so the chunk's
+// part of o is a 32 x 16 x 32 product P E with P = 2^(t - m): it runs on the
+// tensor cores as two m16 x four n8 mma.sync m16n8k16 (bf16 P and E, fp32
+// accumulate).  P goes through a 1 KB per-warp shared buffer (ldmatrix gives
+// the A fragments), E's 16 rows come from the tile's table rows in shared
+// memory (ldmatrix.trans gives the B fragments).  The accumulator is held in
+// the mma fragment layout: lane (g = lane / 4, t = lane % 4) holds rows g,
+// g + 8 (first m16 tile) and g + 16, g + 24 (second) at columns 8 j + 2 t,
+// 8 j + 2 t + 1 of n8 tile j.
 constexpr int kScDim = 32;
 
 struct ScAcc {
-    float2 o[kScDim / 2];
+    float c[2][4][4];   // [m16 tile][n8 tile][fragment register]
 };
 
 DG_DEVICE void sc_init(ScAcc &a)
 {
 #pragma unroll
-    for (int k = 0; k < kScDim / 2; ++k) a.o[k] = make_float2(0.f, 0.f);
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) a.c[mt][j][r] = 0.f;
 }
 
 DG_DEVICE float fast_exp2(float x)
@@ -82,43 +97,129 @@ DG_DEVICE float fast_exp2(float x)
     return y;
 }
 
-DG_DEVICE void sc_scale(ScAcc &a, float f)
+// Multiply row r of the accumulator by the factor lane r holds.  All 32
+// lanes call it together.
+DG_DEVICE void sc_scale_rows(ScAcc &a, float f)
 {
-    const float2 f2 = make_float2(f, f);
+    if (!__any_sync(0xFFFFFFFFu, f != 1.0f)) return;
+    const int g = (threadIdx.x & 31) >> 2;
+    const float f0 = __shfl_sync(0xFFFFFFFFu, f, g), f1 = __shfl_sync(0xFFFFFFFFu, f, g + 8);
+    const float f2 = __shfl_sync(0xFFFFFFFFu, f, g + 16), f3 = __shfl_sync(0xFFFFFFFFu, f, g + 24);
 #pragma unroll
-    for (int k = 0; k < kScDim / 2; ++k) a.o[k] = mul2(a.o[k], f2);
-}
-
-// o += e E[v, :] for one vocabulary row erow (kScDim fp32 in shared memory,
-// 16-byte aligned; every lane of a warp reads the same row, a broadcast).
-DG_DEVICE void sc_add_row(ScAcc &a, float e, const float *__restrict__ erow)
-{
-    const float4 *e4 = reinterpret_cast<const float4 *>(erow);
-    const float2 ev = make_float2(e, e);
-#pragma unroll
-    for (int q = 0; q < kScDim / 4; ++q) {
-        const float4 r = e4[q];
-        a.o[2 * q] = fma2(ev, make_float2(r.x, r.y), a.o[2 * q]);
-        a.o[2 * q + 1] = fma2(ev, make_float2(r.z, r.w), a.o[2 * q + 1]);
+    for (int j = 0; j < 4; ++j) {
+        a.c[0][j][0] *= f0;
+        a.c[0][j][1] *= f0;
+        a.c[0][j][2] *= f1;
+        a.c[0][j][3] *= f1;
+        a.c[1][j][0] *= f2;
+        a.c[1][j][1] *= f2;
+        a.c[1][j][2] *= f3;
+        a.c[1][j][3] *= f3;
     }
 }
 
-// Before the softmax states sa and sb merge (row_state_merge(sa, sb)), the
-// read-out parts follow them: a <- 2^(ma - m) a + 2^(mb - m) b with
-// m = max(ma, mb); a part whose S is 0 holds nothing.
+DG_DEVICE uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// o += P E for one chunk: es[q] = (P[row][2q], P[row][2q + 1]) of this
+// lane's row; Ec = the chunk's 16 table rows (bf16 [16][kScDim], shared,
+// 16-byte aligned); pbuf = this warp's 32 x 16 bf16 staging buffer (shared).
+// All 32 lanes call it together.
+DG_DEVICE void sc_add_chunk(ScAcc &a, const float2 (&es)[8], const uint16_t *Ec, uint16_t *pbuf)
+{
+    const int lane = threadIdx.x & 31;
+    uint4 lo, hi;
+    lo.x = pack_bf16x2(es[0].x, es[0].y);
+    lo.y = pack_bf16x2(es[1].x, es[1].y);
+    lo.z = pack_bf16x2(es[2].x, es[2].y);
+    lo.w = pack_bf16x2(es[3].x, es[3].y);
+    hi.x = pack_bf16x2(es[4].x, es[4].y);
+    hi.y = pack_bf16x2(es[5].x, es[5].y);
+    hi.z = pack_bf16x2(es[6].x, es[6].y);
+    hi.w = pack_bf16x2(es[7].x, es[7].y);
+    __syncwarp();   // the previous chunk's fragments were read
+    reinterpret_cast<uint4 *>(pbuf + lane * 16)[0] = lo;
+    reinterpret_cast<uint4 *>(pbuf + lane * 16)[1] = hi;
+    __syncwarp();
+    uint32_t af[2][4], bf[4][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        // matrices: rows 0-7 / 8-15 of the m16 tile at columns 0-7, then 8-15
+        const uint32_t addr = smem_u32(pbuf + (mt * 16 + (lane & 15)) * 16 + (lane >> 4) * 8);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(af[mt][0]), "=r"(af[mt][1]), "=r"(af[mt][2]), "=r"(af[mt][3])
+                     : "r"(addr)
+                     : "memory");
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        // matrices: k 0-7 / 8-15 of n8 tile 2h, then of n8 tile 2h + 1
+        const int mat = lane >> 3;
+        const int k = (lane & 7) + 8 * (mat & 1);
+        const int n0 = 16 * h + 8 * (mat >> 1);
+        const uint32_t addr = smem_u32(Ec + k * kScDim + n0);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(bf[2 * h][0]), "=r"(bf[2 * h][1]), "=r"(bf[2 * h + 1][0]),
+                       "=r"(bf[2 * h + 1][1])
+                     : "r"(addr)
+                     : "memory");
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                : "+f"(a.c[mt][j][0]), "+f"(a.c[mt][j][1]), "+f"(a.c[mt][j][2]),
+                  "+f"(a.c[mt][j][3])
+                : "r"(af[mt][0]), "r"(af[mt][1]), "r"(af[mt][2]), "r"(af[mt][3]),
+                  "r"(bf[j][0]), "r"(bf[j][1]));
+}
+
+// Before the softmax states of two parts merge (row_state_merge(sa, sb)),
+// their read-out parts follow: a <- 2^(ma - m) a + 2^(mb - m) b per row
+// (m = max(ma, mb); a part whose S is 0 holds nothing).  sa, sb are this
+// lane's row; all 32 lanes call it together.
 DG_DEVICE void sc_merge(ScAcc &a, const RowState &sa, const ScAcc &b, const RowState &sb)
 {
-    if (!(sb.S > 0.f)) return;
-    if (!(sa.S > 0.f)) {
-        a = b;
-        return;
+    float fa = 1.f, fb = 0.f;
+    if (sb.S > 0.f) {
+        if (sa.S > 0.f) {
+            const float m = fmaxf(sa.m, sb.m);
+            fa = fast_exp2(sa.m - m);
+            fb = fast_exp2(sb.m - m);
+        } else {
+            fa = 0.f;
+            fb = 1.f;
+        }
     }
-    const float m = fmaxf(sa.m, sb.m);
-    const float2 fa = make_float2(fast_exp2(sa.m - m), fast_exp2(sa.m - m));
-    const float2 fb = make_float2(fast_exp2(sb.m - m), fast_exp2(sb.m - m));
+    const int g = (threadIdx.x & 31) >> 2;
+    float fA[4], fB[4];
 #pragma unroll
-    for (int k = 0; k < kScDim / 2; ++k) a.o[k] = fma2(fa, a.o[k], mul2(fb, b.o[k]));
+    for (int i = 0; i < 4; ++i) {
+        fA[i] = __shfl_sync(0xFFFFFFFFu, fa, g + 8 * i);
+        fB[i] = __shfl_sync(0xFFFFFFFFu, fb, g + 8 * i);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = 2 * mt + (r >> 1);   // rows g, g + 8, g + 16, g + 24
+                a.c[mt][j][r] = fmaf(fA[i], a.c[mt][j][r], fB[i] * b.c[mt][j][r]);
+            }
 }
+
+// The positions of this lane's fragment values: row (0..31 within the warp's
+// rows) and column of register r of n8 tile j in m16 tile mt.
+DG_DEVICE int sc_frag_row(int mt, int r) { return mt * 16 + ((threadIdx.x & 31) >> 2) + 8 * (r >> 1); }
+DG_DEVICE int sc_frag_col(int j, int r) { return 8 * j + 2 * (threadIdx.x & 3) + (r & 1); }
 
 // Per-step constants of the fold.
 struct FoldConsts {
@@ -185,7 +286,7 @@ DG_DEVICE uint32_t gumbel_word_threshold(float t)
 template <bool kSC>
 DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
                         uint32_t row, const FoldConsts &fc, bool live, ScAcc *sc,
-                        const float *__restrict__ E)
+                        const uint16_t *__restrict__ E, uint16_t *pbuf)
 {
     const bool full = v0 + 16u <= V;
     float x[16];
@@ -216,15 +317,17 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
     }
     // softmax statistics in base 2 (c2 > 0, so the maximum maps through)
     const float mt = cmax * fc.c2;
+    float fsc = 1.0f;      // the factor this row's read-out part is rescaled by
     if (mt > st.m) {
         if (st.S > 0.f) {
             const float f = fast_exp2(st.m - mt);
             st.A = f * fmaf(st.m - mt, st.S, st.A);
             st.S = f * st.S;
-            if constexpr (kSC) sc_scale(*sc, f);
+            fsc = f;
         }
         st.m = mt;
     }
+    if constexpr (kSC) sc_scale_rows(*sc, fsc);
     // on pairs of columns (packed fp32: the same roundings as one column at
     // a time); the sums run as a fixed tree, column j with j + 8, then + 4,
     // + 2, + 1
@@ -237,17 +340,9 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
         es[q] = e;
         as[q] = mul2(e, dlt);
     }
-    if constexpr (kSC) {
-        // columns in order, each weighted by its 2^(t - m) (0 past V: not read)
-        if (live) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (full || v0 + 2 * q < V) sc_add_row(*sc, es[q].x, E + (2 * q) * kScDim);
-                if (full || v0 + 2 * q + 1 < V)
-                    sc_add_row(*sc, es[q].y, E + (2 * q + 1) * kScDim);
-            }
-        }
-    }
+    // the chunk's read-out part (columns past V and rows past M weigh 0; the
+    // table rows past V are zero-filled)
+    if constexpr (kSC) sc_add_chunk(*sc, es, E, pbuf);
 #pragma unroll
     for (int h = 4; h >= 1; h >>= 1) {
 #pragma unroll
@@ -383,7 +478,7 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
 DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
                       uint32_t row, const FoldConsts &fc, bool live)
 {
-    fold16_t<false>(st, lg, v0, V, row, fc, live, nullptr, nullptr);
+    fold16_t<false>(st, lg, v0, V, row, fc, live, nullptr, nullptr, nullptr);
 }
 
 // Resolve the kept column (evaluate it exactly) before the state is stored.
@@ -443,9 +538,10 @@ DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int B
 }
 
 // fold_tile with the self-conditioning part: Et holds the table rows of the
-// tile's columns vbase, vbase + 1, ... (kScDim floats each, shared memory).
-DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const float *__restrict__ Et, uint32_t tb,
-                            int first, int stride, int BN, uint32_t vbase, uint32_t V,
+// tile's columns vbase, vbase + 1, ... (kScDim bf16 each, shared memory);
+// pbuf is the warp's staging buffer.
+DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const uint16_t *__restrict__ Et, uint16_t *pbuf,
+                            uint32_t tb, int first, int stride, int BN, uint32_t vbase, uint32_t V,
                             uint32_t row, const FoldConsts &fc, bool live)
 {
 #pragma unroll 1
@@ -453,7 +549,7 @@ DG_DEVICE void fold_tile_sc(RowState &st, ScAcc &sc, const float *__restrict__ E
         float lg[16];
         tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
         const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
-        if (v0 < V) fold16_t<true>(st, lg, v0, V, row, fc, live, &sc, Et + c0 * kScDim);
+        if (v0 < V) fold16_t<true>(st, lg, v0, V, row, fc, live, &sc, Et + c0 * kScDim, pbuf);
     }
 }
 
@@ -588,19 +684,23 @@ DG_DEVICE void group_merge_store_t(RowState &st, int cg, int rix, uint32_t k,
             f[5 * gm.rows] = st.amax;
             f[6 * gm.rows] = __int_as_float(st.aidx);
             if constexpr (kSC) {
-                float *o = sm.buf + static_cast<size_t>(cg - 1) * kScDim * gm.rows + rix;
+                // [column][row] words; this lane's fragment positions
+                float *o = sm.buf + static_cast<size_t>(cg - 1) * kScDim * gm.rows + (rix & ~31);
 #pragma unroll
-                for (int j = 0; j < kScDim / 2; ++j) {
-                    o[(2 * j) * gm.rows] = sc->o[j].x;
-                    o[(2 * j + 1) * gm.rows] = sc->o[j].y;
-                }
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            o[sc_frag_col(j, r) * gm.rows + sc_frag_row(mt, r)] = sc->c[mt][j][r];
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(gm.ready);
         return;
     }
-    const bool ok = mbar_wait(gm.ready, k & 1u, ws, 121);
+    // (warp-uniform: the read-out merge below exchanges values between lanes)
+    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(gm.ready, k & 1u, ws, 121));
     if (ok) {
         for (int g = 1; g < gm.G; ++g) {
             const float *f = gm.buf + static_cast<size_t>(g - 1) * 7 * gm.rows + rix;
@@ -613,24 +713,39 @@ DG_DEVICE void group_merge_store_t(RowState &st, int cg, int rix, uint32_t k,
             o.amax = f[5 * gm.rows];
             o.aidx = __float_as_int(f[6 * gm.rows]);
             if constexpr (kSC) {
-                const float *ob = sm.buf + static_cast<size_t>(g - 1) * kScDim * gm.rows + rix;
+                const float *ob =
+                    sm.buf + static_cast<size_t>(g - 1) * kScDim * gm.rows + (rix & ~31);
                 ScAcc b;
 #pragma unroll
-                for (int j = 0; j < kScDim / 2; ++j)
-                    b.o[j] = make_float2(ob[(2 * j) * gm.rows], ob[(2 * j + 1) * gm.rows]);
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            b.c[mt][j][r] = ob[sc_frag_col(j, r) * gm.rows + sc_frag_row(mt, r)];
                 sc_merge(*sc, st, b, o);
             }
             row_state_merge(st, o);
         }
-        if (store) {
-            partial_store(p, idx, st);
-            if constexpr (kSC) {
-                float4 *dst = reinterpret_cast<float4 *>(sm.part + idx * kScDim);
+        if (store) partial_store(p, idx, st);
+        if constexpr (kSC) {
+            // the read-out part of row R sits in the lanes of its fragment
+            // positions: each stores its values under row R's slot index
 #pragma unroll
-                for (int j = 0; j < kScDim / 4; ++j)
-                    dst[j] = make_float4(sc->o[2 * j].x, sc->o[2 * j].y, sc->o[2 * j + 1].x,
-                                         sc->o[2 * j + 1].y);
-            }
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int R = sc_frag_row(mt, 2 * h);
+                    const unsigned long long iR = __shfl_sync(0xFFFFFFFFu,
+                                                              static_cast<unsigned long long>(idx), R);
+                    const int sR = __shfl_sync(0xFFFFFFFFu, store ? 1 : 0, R);
+                    if (sR) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<float2 *>(sm.part + iR * kScDim + sc_frag_col(j, 0)) =
+                                make_float2(sc->c[mt][j][2 * h], sc->c[mt][j][2 * h + 1]);
+                    }
+                }
         }
     }
     __syncwarp();

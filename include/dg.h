@@ -203,26 +203,29 @@ int dg_noalloc_read_device_status(int *status_out, int clear, void *stream);
 /* dg_denoise_step with the self-conditioning read-out folded into the LM    */
 /* head.  "Parallel Denoising From an Autoregressive Checkpoint", section    */
 /* "Finding": a 7.8M-parameter self-conditioning block feeds the previous    */
-/* step's prediction back into the model, and its matmul runs in full        */
-/* precision in the sampling stage next to the full-vocabulary softmax.      */
-/* The pages give no formula; this library reads the fed-back prediction as  */
-/* the expected embedding under the step's sampling distribution:            */
+/* step's prediction back into the model, and its matmul runs in the         */
+/* sampling stage next to the full-vocabulary softmax.  The pages give no   */
+/* formula; this library reads the fed-back prediction as the expected       */
+/* embedding under the step's sampling distribution:                         */
 /*   sc_out[r, j] = sum_v softmax(logits[r] / T)_v sc_table[v, j],  j < 32   */
 /* (V x 30 = 7.86M parameters at V = 262144; pad the table's rows with zero  */
-/* columns to 32).  fp32 arithmetic; the logits are never stored.  Turning   */
-/* sc_out into the next step's hidden states is the decoder body's work.     */
-/* Layouts: sc_table [V, 32] fp32 (device, 16-byte aligned), sc_out [B*L, 32] */
-/* fp32 (device, 16-byte aligned); the rest as dg_denoise_step.  Always runs  */
-/* the 2-SM LM-head kernel.  Same results as dg_denoise_step for every other  */
-/* output.  Errors as dg_denoise_step.                                        */
+/* columns to 32).  The weights 2^(t - m) of each 16-column chunk are rounded */
+/* to bf16 and multiplied with the table on the tensor cores (fp32           */
+/* accumulation); softmax statistics and the read-out sums are fp32; the      */
+/* logits are never stored.  Turning sc_out into the next step's hidden      */
+/* states is the decoder body's work.  Layouts: sc_table [V, 32] bf16         */
+/* (device, 16-byte aligned), sc_out [B*L, 32] fp32 (device, 16-byte          */
+/* aligned); the rest as dg_denoise_step.  Always runs the 2-SM LM-head       */
+/* kernel.  Every other output as dg_denoise_step.  Errors as                 */
+/* dg_denoise_step.                                                           */
 /* ------------------------------------------------------------------------ */
 size_t dg_denoise_step_sc_workspace(const dg_step_params *p);
-int dg_denoise_step_sc(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+int dg_denoise_step_sc(const uint16_t *hidden, const uint16_t *w, const uint16_t *sc_table,
                        const dg_step_params *p, const dg_step_io *io, float *sc_out,
                        void *workspace, size_t workspace_bytes, void *stream);
 /* Its LM-head kernel alone (partial states and read-out parts left in the   */
 /* workspace; for timing).                                                    */
-int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const float *sc_table,
+int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const uint16_t *sc_table,
                        const dg_step_params *p, void *workspace, size_t workspace_bytes,
                        void *stream);
 

@@ -5,9 +5,9 @@ section "Finding": the self-conditioning block's matmul runs next to the
 full-vocabulary softmax).
 
 Tolerance of the read-out, per row: max_j |sc_j - sc*_j| <= 2e-2 max_j |sc*_j|
-+ 2e-4 max |E| (the second term covers the fp32 summation over the
-vocabulary when the weighted rows cancel, e.g. uniform weights over a
-zero-mean table).  Every other output of the step is checked as for
++ 2e-4 max |E| (the second term covers the bf16 rounding of the weights and
+the fp32 summation over the vocabulary when the weighted rows cancel, e.g.
+uniform weights over a zero-mean table).  Every other output of the step is checked as for
 dg_denoise_step (entropies 1e-4, tokens where the margins allow).
 """
 import numpy as np
@@ -27,8 +27,10 @@ WORKERS = 8
 
 
 def _table(V, seed, R=dg.SC_DIM):
+    """A bf16 table (as its fp32 values: the oracle's input)."""
     rng = np.random.default_rng(seed)
-    return rng.standard_normal((V, R)).astype(np.float32)
+    return dg_synth.bf16_bits_to_f32(dg_synth.f32_to_bf16_bits(
+        rng.standard_normal((V, R)).astype(np.float32)))
 
 
 def _check_sc(got, ref, E):
@@ -40,7 +42,7 @@ def _check_sc(got, ref, E):
 
 def _run_sc(xb, wb, E, B, L, d, V, T, seed, k, canvas0=None, prev=None):
     x, w = to_dev(xb), to_dev(wb)
-    Et = torch.from_numpy(E).to(DEV)
+    Et = torch.from_numpy(E).to(DEV).to(torch.bfloat16)     # exact: E holds bf16 values
     p = dg.step_params(B, L, d, V, T, 0.1, 0.005, step=k, seed=seed)
     ws = dg.workspace(dg.denoise_step_sc_workspace(p), DEV)
     bufs = dg.StepBuffers(B, L, DEV)
