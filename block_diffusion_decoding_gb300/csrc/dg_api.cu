@@ -768,7 +768,8 @@ int moe_chunks_cap(int M, int E, int K)
 }
 
 struct MoeWs {
-    size_t logits, sel_e, sel_g, pos_of, tok, gate, items, counts, next, ready, xs, hs, ys, total;
+    size_t logits, sel_e, sel_g, pos_of, tok, gate, items, counts, next, ready, bits, xs, hs, ys,
+        total;
 };
 
 MoeWs moe_ws_layout(const dg_moe_params *p)
@@ -794,6 +795,7 @@ MoeWs moe_ws_layout(const dg_moe_params *p)
     w.counts = take(16);
     w.next = take(4);
     w.ready = take(static_cast<size_t>(kMoeMaxChunks) * 4);
+    w.bits = take(E * ((M + 31) / 32) * 4);
     w.xs = take(R * d * 2);
     w.hs = take(R * f * 2);
     w.ys = take(R * d * 4);
@@ -1090,6 +1092,7 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     a.counts = reinterpret_cast<int32_t *>(base + L.counts);
     a.next_item = reinterpret_cast<int32_t *>(base + L.next);
     a.ready = reinterpret_cast<uint32_t *>(base + L.ready);
+    a.bits = reinterpret_cast<uint32_t *>(base + L.bits);
     a.x_sorted = reinterpret_cast<uint16_t *>(base + L.xs);
     a.h_sorted = reinterpret_cast<uint16_t *>(base + L.hs);
     a.y_sorted = reinterpret_cast<float *>(base + L.ys);
@@ -1129,9 +1132,7 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     }
     cudaStream_t st = as_stream(stream);
     const bool pdl = use_pdl(st);
-    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3((M + 15) / 16, (E + 15) / 16), dim3(256), 0,
-                              st, pdl, x, w_router, M, d, E,
-                              reinterpret_cast<float *>(base + L.logits)));
+    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3(M), dim3(256), 0, st, pdl, a, w_router));
     DG_LAUNCHED();
     DG_CUDA_TRY(launch_kernel(moe_route_kernel, dim3(1), dim3(kMoeRouteThreads), 0, st, pdl, a));
     DG_LAUNCHED();

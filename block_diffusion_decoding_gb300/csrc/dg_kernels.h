@@ -252,7 +252,7 @@ constexpr int kMoeMaxChunks =
 struct MoeArgs {
     int M, d, f, E, top_k;
     const uint16_t *x;          // [M, d] bf16
-    const float *logits;        // [M, E] router logits
+    float *logits;              // [M, E] router logits
     int32_t *sel_expert;        // [M, top_k] chosen experts, best first
     float *sel_gate;            // [M, top_k] their gates
     int32_t *pos_of;            // [M, top_k] row of each assignment in the sorted order
@@ -262,6 +262,7 @@ struct MoeArgs {
     int32_t *counts;            // [4]: gate/up items, all items, sorted rows
     int32_t *next_item;         // work-list counter of the FFN kernel
     uint32_t *ready;            // [kMoeMaxChunks] H parts stored per chunk
+    uint32_t *bits;             // [E][ceil(M / 32)] token bitmaps of the experts (0 between calls)
     uint16_t *x_sorted;         // [M (top_k + 1), d] bf16
     uint16_t *h_sorted;         // [M (top_k + 1), f] bf16
     float *y_sorted;            // [M (top_k + 1), d] fp32, gate applied
@@ -269,8 +270,7 @@ struct MoeArgs {
     WsHeader *ws;
 };
 
-__global__ void moe_router_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wr,
-                                  int M, int d, int E, float *__restrict__ logits);
+__global__ void moe_router_kernel(MoeArgs a, const uint16_t *__restrict__ wr);
 __global__ void moe_route_kernel(MoeArgs a);
 __global__ void moe_gather_kernel(MoeArgs a);
 __global__ void moe_combine_kernel(MoeArgs a);

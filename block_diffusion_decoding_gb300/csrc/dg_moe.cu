@@ -16,11 +16,12 @@
 // intermediate activation is stored as bf16.
 //
 // Launches:
-//   moe_router_kernel   router logits [M, E] fp32 (CUDA cores, 16 x 16 tiles)
-//   moe_route_kernel    one CTA: top-k and gates per token, the tokens of each
-//                       expert in token order (per-expert bitmaps), their
-//                       positions in the expert-sorted order, and the work
-//                       list of the FFN kernel
+//   moe_router_kernel   a CTA per token: its router logits (CUDA cores), its
+//                       top-k experts and gates, a bit in each chosen
+//                       expert's token bitmap
+//   moe_route_kernel    one CTA: the tokens of each expert in token order
+//                       (the bitmaps), their positions in the expert-sorted
+//                       order, and the work list of the FFN kernel
 //   moe_gather_kernel   X_sorted[pos] = x[token of pos] (bf16 rows)
 //   moe_ffn_kernel      persistent tcgen05 GEMMs over the work list: gate/up
 //                       items (expert, 128 rows of f, <= 128 tokens) write
@@ -39,42 +40,90 @@
 
 namespace dg {
 
-// ------------------------------------------------------------------ router
-// grid (ceil(M / 16), ceil(E / 16)), 256 threads: thread (ty, tx) computes the
-// logit of token 16 bx + ty and expert 16 by + tx, summing k in order.
-__global__ void __launch_bounds__(256) moe_router_kernel(const uint16_t *__restrict__ x,
-                                                         const uint16_t *__restrict__ wr, int M,
-                                                         int d, int E, float *__restrict__ logits)
+// ------------------------------------------------------------------ router + top-k
+// One CTA of 256 threads per token: warp w computes the logits of experts
+// 16 w .. 16 w + 15 (each lane sums its 16-byte chunks of the row in order,
+// then a fixed butterfly), then warp 0 takes the top_k (k rounds of the
+// largest logit, ties to the lower expert index), their gates softmax(l[S])
+// and marks the token in each chosen expert's bitmap (zero between calls).
+__global__ void __launch_bounds__(256) moe_router_kernel(MoeArgs a, const uint16_t *__restrict__ wr)
 {
-    __shared__ float xs[16][65];
-    __shared__ float ws[16][65];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int t0 = blockIdx.x * 16, e0 = blockIdx.y * 16;
+    __shared__ float lg[kMoeMaxExperts];
+    const int t = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = a.d, E = a.E, K = a.top_k;
     griddep_wait();
     griddep_launch_dependents();
-    float acc = 0.f;
-    for (int k0 = 0; k0 < d; k0 += 64) {
-        // 16 rows x 64 values of each operand: 4 values per thread
-        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-            const int r = i >> 6, c = i & 63;
-            const int t = t0 + r, e = e0 + r;
-            xs[r][c] = t < M ? __uint_as_float(static_cast<uint32_t>(x[static_cast<size_t>(t) * d + k0 + c]) << 16) : 0.f;
-            ws[r][c] = e < E ? __uint_as_float(static_cast<uint32_t>(wr[static_cast<size_t>(e) * d + k0 + c]) << 16) : 0.f;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(t) * d);
+    const int nc = d / 8;
+    for (int i = 0; i < 16; ++i) {
+        const int e = warp * 16 + i;
+        if (e >= E) break;
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + static_cast<size_t>(e) * d);
+        float acc = 0.f;
+        for (int c = lane; c < nc; c += 32) {
+            const uint4 xv = __ldg(xr + c), wv = __ldg(wrow + c);
+            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc = fmaf(__uint_as_float(xs[q] << 16), __uint_as_float(ws[q] << 16), acc);
+                acc = fmaf(__uint_as_float(xs[q] & 0xFFFF0000u), __uint_as_float(ws[q] & 0xFFFF0000u),
+                           acc);
+            }
         }
-        __syncthreads();
-#pragma unroll 16
-        for (int c = 0; c < 64; ++c) acc = fmaf(xs[ty][c], ws[tx][c], acc);
-        __syncthreads();
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) lg[e] = acc;
     }
-    const int t = t0 + ty, e = e0 + tx;
-    if (t < M && e < E) logits[static_cast<size_t>(t) * E + e] = acc;
+    __syncthreads();
+    if (warp != 0) return;
+    for (int e = lane; e < E; e += 32) a.logits[static_cast<size_t>(t) * E + e] = lg[e];
+    float v[kMoeMaxExperts / 32];
+#pragma unroll
+    for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
+        const int e = q * 32 + lane;
+        v[q] = e < E ? lg[e] : -INFINITY;
+    }
+    const int words = (a.M + 31) >> 5;
+    float mx = 0.f, s = 0.f, my_l = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < K; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
+            const int e = q * 32 + lane;
+            if (e < E && (v[q] > bv || (v[q] == bv && e < be))) { bv = v[q]; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+#pragma unroll
+        for (int q = 0; q < kMoeMaxExperts / 32; ++q)
+            if (q * 32 + lane == be) v[q] = -INFINITY;
+        if (j == 0) mx = bv;
+        s += expf(bv - mx);          // the same sum in every lane, in selection order
+        if (lane == j) {
+            my_l = bv;
+            my_e = be;
+        }
+    }
+    if (lane < K) {
+        a.sel_expert[t * K + lane] = my_e;
+        a.sel_gate[t * K + lane] = expf(my_l - mx) / s;
+        atomicOr(a.bits + static_cast<size_t>(my_e) * words + (t >> 5), 1u << (t & 31));
+    }
 }
 
 // ------------------------------------------------------------------ route
 // One CTA of kMoeRouteThreads threads.  Positions in the expert-sorted order:
 // experts 0 .. E-1, then the shared expert E (every token), each expert's
-// tokens in increasing token order; its chunks of <= kMoeChunk tokens are the
-// FFN kernel's token tiles.
+// tokens in increasing token order (their rank in the expert's bitmap); its
+// chunks of <= kMoeChunk tokens are the FFN kernel's token tiles.  The
+// bitmaps are cleared again for the next call.
 __global__ void __launch_bounds__(kMoeRouteThreads) moe_route_kernel(MoeArgs a)
 {
     __shared__ uint32_t bits[(kMoeMaxExperts + 1) * (kMoeMaxTokens / 32)];
@@ -83,61 +132,16 @@ __global__ void __launch_bounds__(kMoeRouteThreads) moe_route_kernel(MoeArgs a)
     __shared__ int ch0[kMoeMaxExperts + 2];
     __shared__ int chunk_e[kMoeMaxChunks];
     __shared__ int nch_s;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int nw = blockDim.x >> 5;
+    const int tid = threadIdx.x;
     const int M = a.M, E = a.E, K = a.top_k;
     const int words = (M + 31) >> 5;
     griddep_wait();
     griddep_launch_dependents();
-    for (int i = tid; i < (E + 1) * words; i += blockDim.x) bits[i] = 0u;
-    if (tid == 0) *a.next_item = 0;
-    __syncthreads();
-    // top-k per token (a warp per token): k rounds of the warp's largest
-    // logit, ties to the lower expert index; gates = softmax of the chosen
-    for (int t = wid; t < M; t += nw) {
-        float v[kMoeMaxExperts / 32];
-#pragma unroll
-        for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
-            const int e = q * 32 + lane;
-            v[q] = e < E ? a.logits[static_cast<size_t>(t) * E + e] : -INFINITY;
-        }
-        float sel_l[kMoeMaxTopK];
-        int sel_e[kMoeMaxTopK];
-        for (int j = 0; j < K; ++j) {
-            float bv = -INFINITY;
-            int be = 0x7FFFFFFF;
-#pragma unroll
-            for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
-                const int e = q * 32 + lane;
-                if (e < E && (v[q] > bv || (v[q] == bv && e < be))) { bv = v[q]; be = e; }
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-            }
-            sel_l[j] = bv;
-            sel_e[j] = be;
-#pragma unroll
-            for (int q = 0; q < kMoeMaxExperts / 32; ++q)
-                if (q * 32 + lane == be) v[q] = -INFINITY;
-        }
-        if (lane == 0) {
-            const float mx = sel_l[0];
-            float s = 0.f;
-            float g[kMoeMaxTopK];
-            for (int j = 0; j < K; ++j) {
-                g[j] = expf(sel_l[j] - mx);
-                s += g[j];
-            }
-            for (int j = 0; j < K; ++j) {
-                a.sel_expert[t * K + j] = sel_e[j];
-                a.sel_gate[t * K + j] = g[j] / s;
-                atomicOr(&bits[sel_e[j] * words + (t >> 5)], 1u << (t & 31));
-            }
-        }
+    for (int i = tid; i < E * words; i += blockDim.x) {
+        bits[i] = __ldcg(a.bits + i);
+        a.bits[i] = 0u;
     }
+    if (tid == 0) *a.next_item = 0;
     __syncthreads();
     // tokens per expert; the shared expert takes every token
     for (int e = tid; e <= E; e += blockDim.x) {
