@@ -414,22 +414,20 @@ def run_ours(args, cfg, emit=True):
         else:
             dg.lm_head_fold(x, w, p0, sws)
 
-    # The canvas attention and the LM head read different inputs in this step
-    # (the hidden states are given), so the attention runs on a second stream
-    # forked from and joined back into the step's stream: the step ends when
-    # both have.
-    side = torch.cuda.Stream(dev)
-    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    # The bf16 step is one library call (dg_canvas_step: the canvas attention
+    # on a stream forked from the step's stream, the LM head planned on the SMs
+    # the attention leaves free); the FP8 and self-conditioning steps run the
+    # attention and then their step on the one stream.
+    cws = dg.workspace(dg.canvas_step_workspace(p0, P, Hq, Hkv, D), dev) if not (fp8 or sc) else None
 
     def step(k):
-        fork.record(stream)
-        side.wait_event(fork)
-        dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws, stream=side)
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold,
                            k, seed=rank)
-        lm_step(p)
-        join.record(side)
-        stream.wait_event(join)
+        if cws is not None:
+            dg.canvas_step(q, kp, vp, kc, vc, attn_out, scale, x, w, p, bufs, cws)
+        else:
+            dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws)
+            lm_step(p)
 
     def timed(fn, n, first):
         """Per-iteration CUDA-event times (ms) with an L2 flush before each iteration."""
@@ -461,7 +459,8 @@ def run_ours(args, cfg, emit=True):
         tdist.barrier()
     torch.cuda.synchronize(dev)
     step_ms = sum(ts) / len(ts)
-    status = dg.read_device_status(sws) | dg.read_device_status(aws)
+    status = dg.read_device_status(sws) | dg.read_device_status(aws) | (
+        dg.read_device_status(cws) if cws is not None else 0)
     step_ms = _reduce_max(step_ms, dev)
 
     # ---- per-kernel timings (same flush discipline) for the roofline

@@ -37,7 +37,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
             "dg_denoise_step_fp8_workspace", "dg_denoise_step_fp8", "dg_lm_head_fold_fp8",
             "dg_wait_timeout_probe", "dg_denoise_step_sc_workspace", "dg_denoise_step_sc",
             "dg_lm_head_fold_sc", "dg_moe_ffn_workspace", "dg_moe_ffn",
-            "dg_generate_block_fn", "dg_hidden_from_steps", "dg_hidden_embed_add"]
+            "dg_generate_block_fn", "dg_hidden_from_steps", "dg_hidden_embed_add",
+            "dg_canvas_step_workspace", "dg_canvas_step"]
 
 
 class DgError(RuntimeError):
@@ -127,6 +128,8 @@ def _lib():
             "dg_generate_block_fn": ([vp, vp, vp, vp, sp, bp, bi, vp, sz, vp], i32),
             "dg_hidden_from_steps": ([vp] * 5, i32),
             "dg_hidden_embed_add": ([vp] * 5, i32),
+            "dg_canvas_step_workspace": ([sp, i32, i32, i32, i32], sz),
+            "dg_canvas_step": ([vp] * 6 + [i32] * 4 + [f32, vp, vp, sp, si, vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -227,6 +230,24 @@ def denoise_step(hidden, w, p: StepParams, bufs: StepBuffers, workspace, stream=
     rc = _lib().dg_denoise_step(_p(hidden), _p(w), ctypes.byref(p), ctypes.byref(io),
                                 _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "dg_denoise_step")
+
+
+def canvas_step_workspace(p: StepParams, P, Hq, Hkv, D) -> int:
+    return int(_lib().dg_canvas_step_workspace(ctypes.byref(p), P, Hq, Hkv, D))
+
+
+def canvas_step(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, scale, hidden, w,
+                p: StepParams, bufs: StepBuffers, workspace, stream=None):
+    """dg_canvas_step: the canvas attention and the denoising step in one call."""
+    B, L, Hq, D = q.shape
+    P = k_prefix.shape[1] if k_prefix is not None else 0
+    Hkv = k_canvas.shape[2]
+    io = bufs.io()
+    rc = _lib().dg_canvas_step(_p(q), _p(k_prefix) if P else None, _p(v_prefix) if P else None,
+                               _p(k_canvas), _p(v_canvas), _p(attn_out), P, Hq, Hkv, D,
+                               float(scale), _p(hidden), _p(w), ctypes.byref(p), ctypes.byref(io),
+                               _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_canvas_step")
 
 
 def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):

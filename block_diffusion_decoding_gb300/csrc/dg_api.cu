@@ -1027,6 +1027,94 @@ int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas, int *
     return DG_OK;
 }
 
+// ---------------------------------------------------------------- the whole step
+namespace {
+
+// The second stream and the fork / join events of dg_canvas_step, one set per
+// device, made at the first call on it.
+struct ForkStreams {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::map<int, ForkStreams> g_fork;
+
+int fork_streams(ForkStreams **out)
+{
+    int dev = 0;
+    DG_CUDA_TRY(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lk(g_mu);
+    ForkStreams &f = g_fork[dev];
+    if (f.side == nullptr) {
+        DG_CUDA_TRY(cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking));
+        DG_CUDA_TRY(cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming));
+        DG_CUDA_TRY(cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming));
+    }
+    *out = &f;
+    return DG_OK;
+}
+
+// The attention's CTAs when they are few enough to set aside SMs for them
+// (the LM head is then planned on the rest), else 0.
+int attn_reserve(int B, int L, int P, int Hq, int Hkv, int D, int sms)
+{
+    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, sms);
+    const int ctas = ap.mtiles * Hkv * B * ap.nsplit;
+    return ctas <= sms / 8 ? ctas : 0;
+}
+
+}  // namespace
+
+size_t dg_canvas_step_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    const size_t a = dg_canvas_attn_workspace(p->B, p->L, P, Hq, Hkv, D);
+    if (a == 0) return 0;
+    return round_up(dg_denoise_step_workspace(p), 256) + a;
+}
+
+int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                   const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out, int P,
+                   int Hq, int Hkv, int D, float scale, const uint16_t *hidden, const uint16_t *w,
+                   const dg_step_params *p, const dg_step_io *io, void *workspace,
+                   size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if ((rc = check_io(io, true)) != DG_OK) return rc;
+    if (!hidden || !w) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(w) || !aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    const size_t need = dg_canvas_step_workspace(p, P, Hq, Hkv, D);
+    if (need == 0) return DG_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < need) return DG_ERR_WORKSPACE;
+    DeviceInfo *di = nullptr;
+    if ((rc = current_device_info(&di)) != DG_OK) return rc;
+    ForkStreams *fs = nullptr;
+    if ((rc = fork_streams(&fs)) != DG_OK) return rc;
+    const size_t step_bytes = round_up(dg_denoise_step_workspace(p), 256);
+    uint8_t *aws = static_cast<uint8_t *>(workspace) + step_bytes;
+    cudaStream_t st = as_stream(stream);
+    // attention on the second stream, forked from and joined back into `stream`
+    DG_CUDA_TRY(cudaEventRecord(fs->fork, st));
+    DG_CUDA_TRY(cudaStreamWaitEvent(fs->side, fs->fork, 0));
+    rc = attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, p->B, p->L, P, P, Hq, Hkv, D,
+                  scale, 0, aws, workspace_bytes - step_bytes, fs->side);
+    if (rc == DG_OK) {
+        const int M = p->B * p->L;
+        const int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, di->sms);
+        const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve);
+        StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
+        const StepSource src = step_source(p);
+        const AcceptArgs acc = accept_args(p, io);
+        rc = enqueue_step(hidden, 0, 1, nullptr, w, p, plan, ws, src, io->entropy, io->sample,
+                          io->argmax, acc, st);
+    }
+    // the join is recorded whatever happened, so `stream` never waits on a stale fork
+    DG_CUDA_TRY(cudaEventRecord(fs->join, fs->side));
+    DG_CUDA_TRY(cudaStreamWaitEvent(st, fs->join, 0));
+    return rc;
+}
+
 // ---------------------------------------------------------------- self-conditioning step
 size_t dg_denoise_step_sc_workspace(const dg_step_params *p)
 {

@@ -175,6 +175,28 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
                     const dg_step_io *io, void *workspace, size_t workspace_bytes,
                     void *stream);
 
+/* The whole step in one call: dg_canvas_attn (the canvas's attention over   */
+/* [cache ; canvas], into attn_out) and dg_denoise_step (the LM head, sampler, */
+/* acceptance and stop test on the given hidden states).  In this step the    */
+/* two read different inputs, so the attention runs on a second stream the     */
+/* library forks from `stream` and joins back into it (the call's work on      */
+/* `stream` ends when both have); when the attention needs few CTAs (at most  */
+/* an eighth of the SMs) the LM head is planned on the SMs it leaves free.    */
+/* The second stream is one per device, shared by all calls: calls on         */
+/* different streams are correct but their attentions run one after another.  */
+/* Arguments as the two calls (B, L of p; q / out [B, L, Hq, D]; caches       */
+/* [B, P, Hkv, D]); one workspace of dg_canvas_step_workspace bytes: the     */
+/* step's first (its status word at the start), then the attention's from    */
+/* offset round_up(dg_denoise_step_workspace(p), 256) (its own status word). */
+/* Errors as the two calls.  Capturable (the fork and join become graph       */
+/* edges).                                                                    */
+size_t dg_canvas_step_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D);
+int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                   const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out, int P,
+                   int Hq, int Hkv, int D, float scale, const uint16_t *hidden, const uint16_t *w,
+                   const dg_step_params *p, const dg_step_io *io, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
 /* dg_denoise_step for callers that cannot allocate device memory (an engine  */
 /* that owns every byte through its own pool, code that runs where allocation */
 /* is not allowed): no workspace argument.  The pages have no counterpart;    */

@@ -484,3 +484,40 @@ def test_block_converging_matches_oracle():
     assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
     last = ref["history"][-1]
     assert abs(float(bufs.mean_entropy[0]) - float(last["mean_entropy"][0])) < H_TOL
+
+
+@pytest.mark.parametrize("name", ["step_small", "batch4"])
+def test_canvas_step_matches_the_two_calls_and_the_oracle(name):
+    """dg_canvas_step (attention on a forked stream, the LM head planned around
+    it) gives the attention output of dg_canvas_attn bit for bit and a step
+    that matches the oracle."""
+    cfg = dg_synth.CONFIGS[name]
+    B, L, P, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.P, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
+    ai = dg_synth.attention_inputs(cfg)
+    t = {k: to_dev(v) for k, v in ai.items()}
+    xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    rng = np.random.default_rng(3)
+    canvas0 = rng.integers(0, V, B * L).astype(np.int32)
+    prev = rng.integers(0, V, B * L).astype(np.int32)
+    p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=2, seed=5)
+    bufs = dg.StepBuffers(B, L, DEV)
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    bufs.prev_argmax.copy_(torch.from_numpy(prev))
+    out = torch.empty_like(t["q"])
+    ws = dg.workspace(dg.canvas_step_workspace(p, P, Hq, Hkv, D), DEV)
+    for _ in range(2):       # the second call reuses the internal stream and events
+        bufs.canvas.copy_(torch.from_numpy(canvas0))
+        bufs.prev_argmax.copy_(torch.from_numpy(prev))
+        dg.canvas_step(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], out, scale, to_dev(xb),
+                       to_dev(wb), p, bufs, ws)
+        torch.cuda.synchronize()
+        status_ok(ws)
+    ref_out = torch.empty_like(out)
+    aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    dg.canvas_attn(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], ref_out, scale, aws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    ref = oracle.step(xb, wb, canvas0, prev, B, L, 0.8, 0.1, 5, 2, workers=8)
+    check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+    assert np.array_equal(np_i32(bufs.stop), ref["stop"])
