@@ -111,7 +111,10 @@ def test_selfcond_special_cases():
     bufs, sc = _run_sc(dg_synth.f32_to_bf16_bits(x), dg_synth.f32_to_bf16_bits(w), E, 1, L, d, V,
                        0.4, 1, 0)
     hot = (np.arange(L) % d) * 3
-    assert np.abs(sc - E[hot]).max() <= 1e-5 * float(np.abs(E).max())
+    # the row of E, up to the bf16 rounding of the chunk weights (the weight
+    # is 1 within 2^-9, the softmax sum it is divided by is fp32)
+    assert np.abs(sc - E[hot]).max() <= 2e-3 * float(np.abs(E).max())
+    _check_sc(sc, E[hot].astype(np.float64), E)
     assert np.array_equal(np_i32(bufs.argmax), hot)
 
 
