@@ -444,7 +444,8 @@ int attn_split_cap(int blocks, int nkt)
     return std::max(1, std::min(cap, nkt));
 }
 
-AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
+// max_ctas > 0: no split count that would launch more CTAs than that.
+AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms, int max_ctas = 0)
 {
     AttnPlan a{};
     // head dim 256: the 2-SM pair kernel (its 128-key S UMMAs replace 64-key
@@ -474,6 +475,7 @@ AttnPlan plan_attn(int B, int L, int P, int Hq, int Hkv, int D, int sms)
         const int real = (a.nkt + tps - 1) / tps;
         if (real != ns) continue;
         if (forced && ns != std::min(forced, a.nkt)) continue;
+        if (max_ctas > 0 && ns > 1 && static_cast<long>(a.blocks) * ns > max_ctas) continue;
         const long waves = (static_cast<long>(a.blocks) * ns + sms - 1) / sms;
         const long cost = (waves * (tps + 3) + (ns > 1 ? 4 : 0)) * 16 + ns;
         if (best < 0 || cost < best) {
@@ -533,7 +535,7 @@ size_t block_ws_layout(const dg_step_params *p, int slots, size_t *off_ctl, size
 static int attn_run(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
              const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *out, int B, int L, int P,
              int prefix_alloc, int Hq, int Hkv, int D, float scale, int causal, void *workspace,
-             size_t workspace_bytes, void *stream)
+             size_t workspace_bytes, void *stream, int max_ctas = 0)
 {
     if (!q || !k_canvas || !v_canvas || !out) return DG_ERR_INVALID_ARG;
     if (B < 1 || L < 1 || P < 0 || Hq < 1 || Hkv < 1) return DG_ERR_INVALID_ARG;
@@ -552,7 +554,7 @@ static int attn_run(const uint16_t *q, const uint16_t *k_prefix, const uint16_t 
     DeviceInfo *di = nullptr;
     int rc = current_device_info(&di);
     if (rc != DG_OK) return rc;
-    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms);
+    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, di->sms, max_ctas);
     cudaStream_t st = as_stream(stream);
 
     CUtensorMap mq, mkp, mvp, mkc, mvc;
@@ -1053,13 +1055,14 @@ int fork_streams(ForkStreams **out)
     return DG_OK;
 }
 
-// The attention's CTAs when they are few enough to set aside SMs for them
-// (the LM head is then planned on the rest), else 0.
+// SMs set aside for the attention of the step: when its query tiles need at
+// most an eighth of the SMs, its key splits are limited to that many CTAs
+// and the LM head is planned on the rest; else none (a long attention
+// shares the GPU with the LM head instead).
 int attn_reserve(int B, int L, int P, int Hq, int Hkv, int D, int sms)
 {
     const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, sms);
-    const int ctas = ap.mtiles * Hkv * B * ap.nsplit;
-    return ctas <= sms / 8 ? ctas : 0;
+    return ap.blocks <= sms / 8 ? sms / 8 : 0;
 }
 
 }  // namespace
@@ -1097,11 +1100,11 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     // attention on the second stream, forked from and joined back into `stream`
     DG_CUDA_TRY(cudaEventRecord(fs->fork, st));
     DG_CUDA_TRY(cudaStreamWaitEvent(fs->side, fs->fork, 0));
+    const int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, di->sms);
     rc = attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, p->B, p->L, P, P, Hq, Hkv, D,
-                  scale, 0, aws, workspace_bytes - step_bytes, fs->side);
+                  scale, 0, aws, workspace_bytes - step_bytes, fs->side, reserve);
     if (rc == DG_OK) {
         const int M = p->B * p->L;
-        const int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, di->sms);
         const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve);
         StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
         const StepSource src = step_source(p);
@@ -1220,7 +1223,8 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     }
     cudaStream_t st = as_stream(stream);
     const bool pdl = use_pdl(st);
-    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3(M), dim3(256), 0, st, pdl, a, w_router));
+    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3((M + kMoeRouterTokens - 1) / kMoeRouterTokens),
+                              dim3(256), 0, st, pdl, a, w_router));
     DG_LAUNCHED();
     DG_CUDA_TRY(launch_kernel(moe_route_kernel, dim3(1), dim3(kMoeRouteThreads), 0, st, pdl, a));
     DG_LAUNCHED();

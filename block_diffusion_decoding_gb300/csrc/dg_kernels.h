@@ -245,6 +245,7 @@ constexpr int kMoeMaxTopK = 8;
 constexpr int kMoeMaxTokens = 2048;    // canvas rows per call
 constexpr int kMoeChunk = 128;         // tokens per token tile of the expert GEMMs
 constexpr int kMoeRouteThreads = 1024;
+constexpr int kMoeRouterTokens = 2;    // tokens per router CTA (they share its router-weight loads)
 // token chunks of one call: every expert's tokens in chunks of kMoeChunk
 constexpr int kMoeMaxChunks =
     kMoeMaxExperts + 1 + (kMoeMaxTokens * (kMoeMaxTopK + 1) + kMoeChunk - 1) / kMoeChunk;

@@ -16,9 +16,9 @@
 // intermediate activation is stored as bf16.
 //
 // Launches:
-//   moe_router_kernel   a CTA per token: its router logits (CUDA cores), its
-//                       top-k experts and gates, a bit in each chosen
-//                       expert's token bitmap
+//   moe_router_kernel   a CTA per two tokens: their router logits (CUDA
+//                       cores), top-k experts and gates, a bit in each
+//                       chosen expert's token bitmap
 //   moe_route_kernel    one CTA: the tokens of each expert in token order
 //                       (the bitmaps), their positions in the expert-sorted
 //                       order, and the work list of the FFN kernel
@@ -41,50 +41,76 @@
 namespace dg {
 
 // ------------------------------------------------------------------ router + top-k
-// One CTA of 256 threads per token: warp w computes the logits of experts
-// 16 w .. 16 w + 15 (each lane sums its 16-byte chunks of the row in order,
-// then a fixed butterfly), then warp 0 takes the top_k (k rounds of the
-// largest logit, ties to the lower expert index), their gates softmax(l[S])
-// and marks the token in each chosen expert's bitmap (zero between calls).
+// One CTA of 256 threads per kMoeRouterTokens tokens: warp w computes the
+// logits of experts 16 w .. 16 w + 15 for each of the CTA's tokens (each lane
+// sums its 16-byte chunks of the rows in order, all 16 experts' loads of a
+// chunk in flight together, then a fixed butterfly); then warp j takes token
+// j's top_k (k rounds of the largest logit, ties to the lower expert index),
+// their gates softmax(l[S]) and marks the token in each chosen expert's
+// bitmap (zero between calls).
 __global__ void __launch_bounds__(256) moe_router_kernel(MoeArgs a, const uint16_t *__restrict__ wr)
 {
-    __shared__ float lg[kMoeMaxExperts];
-    const int t = blockIdx.x;
+    __shared__ float lg[kMoeRouterTokens][kMoeMaxExperts];
+    const int t0 = blockIdx.x * kMoeRouterTokens;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d = a.d, E = a.E, K = a.top_k;
+    const int d = a.d, E = a.E, K = a.top_k, M = a.M;
     griddep_wait();
     griddep_launch_dependents();
-    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(t) * d);
     const int nc = d / 8;
-    for (int i = 0; i < 16; ++i) {
-        const int e = warp * 16 + i;
-        if (e >= E) break;
-        const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + static_cast<size_t>(e) * d);
-        float acc = 0.f;
-        for (int c = lane; c < nc; c += 32) {
-            const uint4 xv = __ldg(xr + c), wv = __ldg(wrow + c);
-            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
+    const int e0 = warp * 16;
+    if (e0 < E) {
+        float acc[kMoeRouterTokens][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc = fmaf(__uint_as_float(xs[q] << 16), __uint_as_float(ws[q] << 16), acc);
-                acc = fmaf(__uint_as_float(xs[q] & 0xFFFF0000u), __uint_as_float(ws[q] & 0xFFFF0000u),
-                           acc);
+        for (int j = 0; j < kMoeRouterTokens; ++j)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[j][i] = 0.f;
+        for (int c = lane; c < nc; c += 32) {
+            uint4 xv[kMoeRouterTokens];
+#pragma unroll
+            for (int j = 0; j < kMoeRouterTokens; ++j)
+                xv[j] = t0 + j < M ? __ldg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(t0 + j) * d) + c)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            uint4 wv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                wv[i] = e0 + i < E ? __ldg(reinterpret_cast<const uint4 *>(wr + static_cast<size_t>(e0 + i) * d) + c)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t ws[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+                for (int j = 0; j < kMoeRouterTokens; ++j) {
+                    const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[j][i] = fmaf(__uint_as_float(xs[q] << 16), __uint_as_float(ws[q] << 16), acc[j][i]);
+                        acc[j][i] = fmaf(__uint_as_float(xs[q] & 0xFFFF0000u),
+                                         __uint_as_float(ws[q] & 0xFFFF0000u), acc[j][i]);
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-        if (lane == 0) lg[e] = acc;
+        for (int j = 0; j < kMoeRouterTokens; ++j)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float v = acc[j][i];
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (lane == 0 && e0 + i < E) lg[j][e0 + i] = v;
+            }
     }
     __syncthreads();
-    if (warp != 0) return;
-    for (int e = lane; e < E; e += 32) a.logits[static_cast<size_t>(t) * E + e] = lg[e];
+    const int t = t0 + warp;
+    if (warp >= kMoeRouterTokens || t >= M) return;
+    for (int e = lane; e < E; e += 32) a.logits[static_cast<size_t>(t) * E + e] = lg[warp][e];
     float v[kMoeMaxExperts / 32];
 #pragma unroll
     for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
         const int e = q * 32 + lane;
-        v[q] = e < E ? lg[e] : -INFINITY;
+        v[q] = e < E ? lg[warp][e] : -INFINITY;
     }
-    const int words = (a.M + 31) >> 5;
+    const int words = (M + 31) >> 5;
     float mx = 0.f, s = 0.f, my_l = 0.f;
     int my_e = 0;
     for (int j = 0; j < K; ++j) {
