@@ -83,6 +83,9 @@ int current_device_info(DeviceInfo **out)
         DG_CUDA_TRY(cudaFuncSetAttribute(lm_head_duo_fp8_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDuoSmemBytes));
+        DG_CUDA_TRY(cudaFuncSetAttribute(moe_router_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         moe_router_smem_bytes()));
         DG_CUDA_TRY(cudaFuncSetAttribute(moe_ffn_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          moe_ffn_smem_bytes()));
@@ -770,8 +773,8 @@ int moe_chunks_cap(int M, int E, int K)
 }
 
 struct MoeWs {
-    size_t logits, sel_e, sel_g, pos_of, tok, gate, items, counts, next, ready, bits, xs, hs, ys,
-        total;
+    size_t logits, sel_e, sel_g, pos_of, tok, gate, items, counts, next, ready, bits, rpart, xs, hs,
+        ys, total;
 };
 
 MoeWs moe_ws_layout(const dg_moe_params *p)
@@ -798,6 +801,7 @@ MoeWs moe_ws_layout(const dg_moe_params *p)
     w.next = take(4);
     w.ready = take(static_cast<size_t>(kMoeMaxChunks) * 4);
     w.bits = take(E * ((M + 31) / 32) * 4);
+    w.rpart = take((d / kMoeRouterKSlice) * M * E * 4);
     w.xs = take(R * d * 2);
     w.hs = take(R * f * 2);
     w.ys = take(R * d * 4);
@@ -813,7 +817,7 @@ int check_moe_params(const dg_moe_params *p)
     if (p->top_k > p->n_experts) return DG_ERR_INVALID_ARG;
     if (p->M > kMoeMaxTokens || p->n_experts > kMoeMaxExperts || p->top_k > kMoeMaxTopK)
         return DG_ERR_UNSUPPORTED;
-    if (p->d % 128 != 0 || p->d > 16384 || p->f % 128 != 0 || p->f > 16384)
+    if (p->d % kMoeRouterKSlice != 0 || p->d > 16384 || p->f % 128 != 0 || p->f > 16384)
         return DG_ERR_UNSUPPORTED;
     return DG_OK;
 }
@@ -1184,6 +1188,7 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     a.next_item = reinterpret_cast<int32_t *>(base + L.next);
     a.ready = reinterpret_cast<uint32_t *>(base + L.ready);
     a.bits = reinterpret_cast<uint32_t *>(base + L.bits);
+    a.router_part = reinterpret_cast<float *>(base + L.rpart);
     a.x_sorted = reinterpret_cast<uint16_t *>(base + L.xs);
     a.h_sorted = reinterpret_cast<uint16_t *>(base + L.hs);
     a.y_sorted = reinterpret_cast<float *>(base + L.ys);
@@ -1223,8 +1228,25 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     }
     cudaStream_t st = as_stream(stream);
     const bool pdl = use_pdl(st);
-    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3((M + kMoeRouterTokens - 1) / kMoeRouterTokens),
-                              dim3(256), 0, st, pdl, a, w_router));
+    CUtensorMap mwr, mx;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(E)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
+        const uint32_t box[2] = {64, 128};
+        if ((rc = make_map_bf16(&mwr, w_router, 2, dims, strides, box)) != DG_OK) return rc;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(M)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(d) * 2};
+        const uint32_t box[2] = {64, 128};
+        if ((rc = make_map_bf16(&mx, x, 2, dims, strides, box)) != DG_OK) return rc;
+    }
+    const int nslices = d / kMoeRouterKSlice;
+    DG_CUDA_TRY(launch_kernel(moe_router_kernel, dim3(nslices, (M + 127) / 128), dim3(128),
+                              moe_router_smem_bytes(), st, pdl, mwr, mx, a));
+    DG_LAUNCHED();
+    DG_CUDA_TRY(launch_kernel(moe_topk_kernel, dim3((M + 7) / 8), dim3(256), 0, st, pdl, a,
+                              nslices));
     DG_LAUNCHED();
     DG_CUDA_TRY(launch_kernel(moe_route_kernel, dim3(1), dim3(kMoeRouteThreads), 0, st, pdl, a));
     DG_LAUNCHED();

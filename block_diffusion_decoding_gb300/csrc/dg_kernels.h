@@ -245,7 +245,7 @@ constexpr int kMoeMaxTopK = 8;
 constexpr int kMoeMaxTokens = 2048;    // canvas rows per call
 constexpr int kMoeChunk = 128;         // tokens per token tile of the expert GEMMs
 constexpr int kMoeRouteThreads = 1024;
-constexpr int kMoeRouterTokens = 2;    // tokens per router CTA (they share its router-weight loads)
+constexpr int kMoeRouterKSlice = 256;  // k values per router CTA (d % 256 == 0)
 // token chunks of one call: every expert's tokens in chunks of kMoeChunk
 constexpr int kMoeMaxChunks =
     kMoeMaxExperts + 1 + (kMoeMaxTokens * (kMoeMaxTopK + 1) + kMoeChunk - 1) / kMoeChunk;
@@ -264,6 +264,7 @@ struct MoeArgs {
     int32_t *next_item;         // work-list counter of the FFN kernel
     uint32_t *ready;            // [kMoeMaxChunks] H parts stored per chunk
     uint32_t *bits;             // [E][ceil(M / 32)] token bitmaps of the experts (0 between calls)
+    float *router_part;         // [d / kMoeRouterKSlice][M][E] partial router logits
     uint16_t *x_sorted;         // [M (top_k + 1), d] bf16
     uint16_t *h_sorted;         // [M (top_k + 1), f] bf16
     float *y_sorted;            // [M (top_k + 1), d] fp32, gate applied
@@ -271,7 +272,11 @@ struct MoeArgs {
     WsHeader *ws;
 };
 
-__global__ void moe_router_kernel(MoeArgs a, const uint16_t *__restrict__ wr);
+// router: maps of the router weight [E, d] and of x [M, d], box {64, 128}
+__global__ void moe_router_kernel(const __grid_constant__ CUtensorMap map_wr,
+                                  const __grid_constant__ CUtensorMap map_x, MoeArgs a);
+int moe_router_smem_bytes();
+__global__ void moe_topk_kernel(MoeArgs a, int nslices);
 __global__ void moe_route_kernel(MoeArgs a);
 __global__ void moe_gather_kernel(MoeArgs a);
 __global__ void moe_combine_kernel(MoeArgs a);

@@ -16,9 +16,11 @@
 // intermediate activation is stored as bf16.
 //
 // Launches:
-//   moe_router_kernel   a CTA per two tokens: their router logits (CUDA
-//                       cores), top-k experts and gates, a bit in each
-//                       chosen expert's token bitmap
+//   moe_router_kernel   router logits on the tensor cores, split over k
+//                       (CTA = k slice x 128-token chunk, partial sums)
+//   moe_topk_kernel     a warp per token: the slices summed in order, top-k
+//                       experts and gates, a bit in each chosen expert's
+//                       token bitmap
 //   moe_route_kernel    one CTA: the tokens of each expert in token order
 //                       (the bitmaps), their positions in the expert-sorted
 //                       order, and the work list of the FFN kernel
@@ -40,75 +42,122 @@
 
 namespace dg {
 
-// ------------------------------------------------------------------ router + top-k
-// One CTA of 256 threads per kMoeRouterTokens tokens: warp w computes the
-// logits of experts 16 w .. 16 w + 15 for each of the CTA's tokens (each lane
-// sums its 16-byte chunks of the rows in order, all 16 experts' loads of a
-// chunk in flight together, then a fixed butterfly); then warp j takes token
-// j's top_k (k rounds of the largest logit, ties to the lower expert index),
-// their gates softmax(l[S]) and marks the token in each chosen expert's
-// bitmap (zero between calls).
-__global__ void __launch_bounds__(256) moe_router_kernel(MoeArgs a, const uint16_t *__restrict__ wr)
+// ------------------------------------------------------------------ router
+// Router logits on the tensor cores, split over k: CTA (ks, c) multiplies the
+// router weight rows (experts, K-major, A) by the rows of token chunk c
+// (K-major, B) over k slice ks (kMoeRouterKSlice values), one 128 x 128 x 16
+// UMMA per 16 k into TMEM, and stores its partial logits [ks][t][e] (fp32);
+// the top-k kernel sums the slices in order.  One thread loads the slice's
+// operands with TMA (all of it at once) and issues the UMMAs; the four warps
+// read TMEM (lane = expert, column = token) and store.
+__global__ void __launch_bounds__(128, 1)
+    moe_router_kernel(const __grid_constant__ CUtensorMap map_wr,
+                      const __grid_constant__ CUtensorMap map_x, MoeArgs a)
 {
-    __shared__ float lg[kMoeRouterTokens][kMoeMaxExperts];
-    const int t0 = blockIdx.x * kMoeRouterTokens;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr int kKB = kMoeRouterKSlice / 64;                 // k blocks of the slice
+    constexpr int kTile = 128 * 64 * 2;                        // 16 KB per operand block
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + 2 * kKB * kTile);
+    uint64_t *done = full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    __shared__ int s_ok;
+    const int ks = blockIdx.x, c = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d = a.d, E = a.E, K = a.top_k, M = a.M;
+    if (threadIdx.x == 0) {
+        s_ok = 0;
+        mbar_init(full, 1);
+        mbar_init(done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     griddep_wait();
     griddep_launch_dependents();
-    const int nc = d / 8;
-    const int e0 = warp * 16;
-    if (e0 < E) {
-        float acc[kMoeRouterTokens][16];
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(full, 2 * kKB * kTile);
+        for (int kb = 0; kb < kKB; ++kb) {
+            const int k = ks * kMoeRouterKSlice + kb * 64;
+            tma_load_2d(smem + kb * kTile, &map_wr, full, k, 0, policy_evict_last());
+            tma_load_2d(smem + (kKB + kb) * kTile, &map_x, full, k, c * 128, policy_evict_last());
+        }
+        ok = mbar_wait(full, 0, a.ws, 731);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t idesc = make_idesc_bf16(128, 128, 0);
+            const uint32_t sa = smem_u32(smem);
+            for (int kb = 0; kb < kKB; ++kb)
 #pragma unroll
-        for (int j = 0; j < kMoeRouterTokens; ++j)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[j][i] = 0.f;
-        for (int c = lane; c < nc; c += 32) {
-            uint4 xv[kMoeRouterTokens];
-#pragma unroll
-            for (int j = 0; j < kMoeRouterTokens; ++j)
-                xv[j] = t0 + j < M ? __ldg(reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(t0 + j) * d) + c)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-            uint4 wv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                wv[i] = e0 + i < E ? __ldg(reinterpret_cast<const uint4 *>(wr + static_cast<size_t>(e0 + i) * d) + c)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t ws[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-                for (int j = 0; j < kMoeRouterTokens; ++j) {
-                    const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[j][i] = fmaf(__uint_as_float(xs[q] << 16), __uint_as_float(ws[q] << 16), acc[j][i]);
-                        acc[j][i] = fmaf(__uint_as_float(xs[q] & 0xFFFF0000u),
-                                         __uint_as_float(ws[q] & 0xFFFF0000u), acc[j][i]);
-                    }
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = make_sdesc_sw128(sa + kb * kTile + kk * 32, 16, 1024);
+                    const uint64_t bd = make_sdesc_sw128(sa + (kKB + kb) * kTile + kk * 32, 16, 1024);
+                    umma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0);
                 }
+        }
+        s_ok = ok ? 1 : 0;
+        umma_commit(done);
+    }
+    __syncwarp();
+    const bool ok2 = __all_sync(0xFFFFFFFFu, mbar_wait(done, 0, a.ws, 732));
+    __syncthreads();
+    if (ok2 && s_ok != 0) {
+        tc_fence_after();
+        const int e = warp * 32 + lane;
+        const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float *part = a.router_part + static_cast<size_t>(ks) * a.M * a.E;
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+            float v[16];
+            tmem_ld16(tb + static_cast<uint32_t>(c0), v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = c * 128 + c0 + j;
+                if (t < a.M && e < a.E) part[static_cast<size_t>(t) * a.E + e] = v[j];
             }
         }
-#pragma unroll
-        for (int j = 0; j < kMoeRouterTokens; ++j)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float v = acc[j][i];
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (lane == 0 && e0 + i < E) lg[j][e0 + i] = v;
-            }
     }
+    tc_fence_before();
     __syncthreads();
-    const int t = t0 + warp;
-    if (warp >= kMoeRouterTokens || t >= M) return;
-    for (int e = lane; e < E; e += 32) a.logits[static_cast<size_t>(t) * E + e] = lg[warp][e];
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+int moe_router_smem_bytes() { return 2 * (kMoeRouterKSlice / 64) * 128 * 64 * 2 + 1024 + 256; }
+
+// ------------------------------------------------------------------ top-k
+// A warp per token: its logits are the sum of the k slices' parts in slice
+// order; then the top_k (k rounds of the largest logit, ties to the lower
+// expert index), their gates softmax(l[S]) and a bit in each chosen expert's
+// token bitmap (zero between calls).
+__global__ void __launch_bounds__(256) moe_topk_kernel(MoeArgs a, int nslices)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    const int E = a.E, K = a.top_k, M = a.M;
+    griddep_wait();
+    griddep_launch_dependents();
+    if (t >= M) return;
     float v[kMoeMaxExperts / 32];
 #pragma unroll
     for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
         const int e = q * 32 + lane;
-        v[q] = e < E ? lg[warp][e] : -INFINITY;
+        float l = -INFINITY;
+        if (e < E) {
+            l = 0.f;
+            for (int ks = 0; ks < nslices; ++ks)
+                l += __ldcg(a.router_part + (static_cast<size_t>(ks) * M + t) * E + e);
+            a.logits[static_cast<size_t>(t) * E + e] = l;
+        }
+        v[q] = l;
     }
     const int words = (M + 31) >> 5;
     float mx = 0.f, s = 0.f, my_l = 0.f;

@@ -269,7 +269,8 @@ int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const uint16_t
 /* w_up [E + 1, f, d]; w_down [E + 1, d, f] (index E = the shared expert);   */
 /* out [M, d] fp32.  experts_out [M, top_k] int32 and gates_out [M, top_k]   */
 /* fp32 receive the routing when not NULL.  Only the experts some row picks */
-/* are read.  Supported: 1 <= M <= 2048; d, f multiples of 128, <= 16384;     */
+/* are read.  Supported: 1 <= M <= 2048; d a multiple of 256, f of 128,      */
+/* both <= 16384;                                                             */
 /* 1 <= top_k <= min(8, E), E <= 128.  16-byte aligned pointers.  Errors as  */
 /* dg_denoise_step; device-side waits report through the workspace status.  */
 /* ------------------------------------------------------------------------ */
