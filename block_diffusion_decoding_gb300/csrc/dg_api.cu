@@ -1060,13 +1060,17 @@ int fork_streams(ForkStreams **out)
 }
 
 // SMs set aside for the attention of the step: when its query tiles need at
-// most an eighth of the SMs, its key splits are limited to that many CTAs
-// and the LM head is planned on the rest; else none (a long attention
-// shares the GPU with the LM head instead).
+// most an eighth of the SMs and, with its key splits limited to that many
+// CTAs, each CTA has at most kReserveTiles key tiles (a short attention that
+// hides under the LM head), the LM head is planned on the other SMs; else
+// none (a longer attention shares the GPU with the LM head instead).
+constexpr int kReserveTiles = 6;
 int attn_reserve(int B, int L, int P, int Hq, int Hkv, int D, int sms)
 {
-    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, sms);
-    return ap.blocks <= sms / 8 ? sms / 8 : 0;
+    const int cap = sms / 8;
+    const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, sms, cap);
+    if (ap.blocks > cap || ap.tps > kReserveTiles) return 0;
+    return cap;
 }
 
 }  // namespace
