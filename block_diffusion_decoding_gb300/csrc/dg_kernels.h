@@ -150,11 +150,13 @@ __global__ void lm_head_duo_wide_kernel(const __grid_constant__ CUtensorMap map_
 // of two buffers, so the fold reads them from shared memory; every epilogue
 // warp has a 1 KB staging buffer for its chunk's weights; the ring has
 // kDuoScStages stages to make room.
-constexpr int kDuoScStages = 4;
+constexpr int kDuoScStages = 5;
 constexpr int kDuoScETileRows = 256;
-constexpr int kDuoScSmemBytes = kDuoScStages * kDuoStageBytes + 1024 + 256 + kPairMergeBytes +
+constexpr int kDuoScSmemBytes = kDuoScStages * kDuoStageBytes + 1024 + 256 +
+                                (kDuoCGNarrow - 1) * 7 * 128 * 4 +
                                 (kDuoCGNarrow - 1) * kScDim * 128 * 4 +
                                 2 * kDuoScETileRows * kScDim * 2 + 4 * kDuoCGNarrow * 32 * 16 * 2;
+static_assert(kDuoScSmemBytes <= 227 * 1024, "self-conditioning LM head: shared memory");
 __global__ void lm_head_duo_sc_kernel(const __grid_constant__ CUtensorMap map_x,
                                       const __grid_constant__ CUtensorMap map_w,
                                       const __grid_constant__ CUtensorMap map_e, LmHeadArgs a);

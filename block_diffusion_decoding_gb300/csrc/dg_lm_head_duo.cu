@@ -85,13 +85,15 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
     constexpr int EpiWarps = DuoEpilogue<kCG>::Warps;
     const GroupMerge gm{reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256),
                         mrg_ready, mrg_done, CG, 128};
-    const ScMerge sm{reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256 +
-                                               kPairMergeBytes),
+    // the self-conditioning instance sizes the state merge for its 2 column
+    // groups (the others for up to 4)
+    constexpr int MergeBytes = kSC ? (kCG - 1) * 7 * 128 * 4 : kPairMergeBytes;
+    const ScMerge sm{reinterpret_cast<float *>(smem + Stages * kDuoStageBytes + 256 + MergeBytes),
                      a.sc_part};
     // kSC: two E buffers of kDuoScETileRows x kScDim bf16 each, then a 1 KB
     // P staging buffer per epilogue warp
     uint16_t *ebuf = reinterpret_cast<uint16_t *>(smem + Stages * kDuoStageBytes + 256 +
-                                                  kPairMergeBytes + (kCG - 1) * kScDim * 128 * 4);
+                                                  MergeBytes + (kCG - 1) * kScDim * 128 * 4);
     uint16_t *pbuf_all = ebuf + 2 * kDuoScETileRows * kScDim;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
