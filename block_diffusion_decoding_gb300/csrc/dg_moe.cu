@@ -148,16 +148,28 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(MoeArgs a, int nslices)
     if (t >= M) return;
     float v[kMoeMaxExperts / 32];
 #pragma unroll
+    for (int q = 0; q < kMoeMaxExperts / 32; ++q) v[q] = (q * 32 + lane < E) ? 0.f : -INFINITY;
+    // the slices in order, eight slices' loads of every expert in flight together
+    for (int k0 = 0; k0 < nslices; k0 += 8) {
+        float part[8][kMoeMaxExperts / 32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
+                const int e = q * 32 + lane;
+                part[u][q] = (k0 + u < nslices && e < E)
+                                 ? __ldcg(a.router_part + (static_cast<size_t>(k0 + u) * M + t) * E + e)
+                                 : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int q = 0; q < kMoeMaxExperts / 32; ++q) v[q] += part[u][q];
+    }
+#pragma unroll
     for (int q = 0; q < kMoeMaxExperts / 32; ++q) {
         const int e = q * 32 + lane;
-        float l = -INFINITY;
-        if (e < E) {
-            l = 0.f;
-            for (int ks = 0; ks < nslices; ++ks)
-                l += __ldcg(a.router_part + (static_cast<size_t>(ks) * M + t) * E + e);
-            a.logits[static_cast<size_t>(t) * E + e] = l;
-        }
-        v[q] = l;
+        if (e < E) a.logits[static_cast<size_t>(t) * E + e] = v[q];
     }
     const int words = (M + 31) >> 5;
     float mx = 0.f, s = 0.f, my_l = 0.f;
@@ -228,22 +240,41 @@ __global__ void __launch_bounds__(kMoeRouteThreads) moe_route_kernel(MoeArgs a)
         cnt[e] = c;
     }
     __syncthreads();
-    if (tid == 0) {
-        // row offsets and chunk ids (chunks of <= kMoeChunk tokens), experts in order
+    if (tid < 32) {
+        // row offsets and chunk ids (chunks of <= kMoeChunk tokens), experts in
+        // order: exclusive scans over the E + 1 experts, 32 at a time
+        const int lane = tid;
         int o = 0, ch = 0;
-        for (int e = 0; e <= E; ++e) {
-            off[e] = o;
-            ch0[e] = ch;
-            o += cnt[e];
-            ch += (cnt[e] + kMoeChunk - 1) / kMoeChunk;
+        for (int e0 = 0; e0 <= E; e0 += 32) {
+            const int e = e0 + lane;
+            const int c = e <= E ? cnt[e] : 0;
+            const int n = (c + kMoeChunk - 1) / kMoeChunk;
+            int ic = c, in = n;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int uc = __shfl_up_sync(0xFFFFFFFFu, ic, d);
+                const int un = __shfl_up_sync(0xFFFFFFFFu, in, d);
+                if (lane >= d) {
+                    ic += uc;
+                    in += un;
+                }
+            }
+            if (e <= E) {
+                off[e] = o + ic - c;
+                ch0[e] = ch + in - n;
+            }
+            o += __shfl_sync(0xFFFFFFFFu, ic, 31);
+            ch += __shfl_sync(0xFFFFFFFFu, in, 31);
         }
-        off[E + 1] = o;
-        ch0[E + 1] = ch;
-        nch_s = ch;
-        const int ft = a.f / 128, dt = a.d / 128;
-        a.counts[0] = ch * ft;          // gate/up items
-        a.counts[1] = ch * (ft + dt);   // all items
-        a.counts[2] = o;                // rows of the sorted order
+        if (lane == 0) {
+            off[E + 1] = o;
+            ch0[E + 1] = ch;
+            nch_s = ch;
+            const int ft = a.f / 128, dt = a.d / 128;
+            a.counts[0] = ch * ft;          // gate/up items
+            a.counts[1] = ch * (ft + dt);   // all items
+            a.counts[2] = o;                // rows of the sorted order
+        }
     }
     __syncthreads();
     // the work list: every chunk x f tile of gate/up items, then every chunk x
@@ -251,11 +282,8 @@ __global__ void __launch_bounds__(kMoeRouteThreads) moe_route_kernel(MoeArgs a)
     // tile | chunk id << 8, first row, tokens)
     {
         const int nch = nch_s, ft = a.f / 128, dt = a.d / 128;
-        for (int cid = tid; cid < nch; cid += blockDim.x) {
-            int e = 0;
-            while (ch0[e + 1] <= cid) ++e;
-            chunk_e[cid] = e;
-        }
+        for (int e = tid; e <= E; e += blockDim.x)
+            for (int cid = ch0[e]; cid < ch0[e + 1]; ++cid) chunk_e[cid] = e;
         __syncthreads();
         for (int i = tid; i < nch * (ft + dt); i += blockDim.x) {
             const bool up = i < nch * ft;
