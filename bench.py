@@ -1061,17 +1061,18 @@ def run_kernel_only(args, cfg):
 SWEEP = [
     # (name in the line, config, options): every configuration of the step, the
     # block loop, the encoder append and the widened rows, each in its own
-    # timed region of at least 200 steps (10 blocks for the loop)
-    ("step_small", "step_small", {}),
-    ("batch1", "batch1", {}),
-    ("batch4", "batch4", {}),
-    ("batch16", "batch16", {}),
-    ("long_context", "long_context", {}),
-    ("block_full", "block_full", {"steps": 10}),
-    ("step_full_fp8", "step_full", {"lm_dtype": "fp8"}),
-    ("step_full_self_cond", "step_full", {"self_cond": True}),
-    ("encoder_full", "encoder_full", {}),
-    ("moe_full", "moe_full", {}),
+    # timed region of about half a second or more (with the L2 flush before
+    # every step), so the clock sampler sees the GPU under load
+    ("step_small", "step_small", {"steps": 4000}),
+    ("batch1", "batch1", {"steps": 4000}),
+    ("batch4", "batch4", {"steps": 3000}),
+    ("batch16", "batch16", {"steps": 2000}),
+    ("long_context", "long_context", {"steps": 4000}),
+    ("block_full", "block_full", {"steps": 100}),
+    ("step_full_fp8", "step_full", {"lm_dtype": "fp8", "steps": 2000}),
+    ("step_full_self_cond", "step_full", {"self_cond": True, "steps": 1500}),
+    ("encoder_full", "encoder_full", {"steps": 4000}),
+    ("moe_full", "moe_full", {"steps": 2000}),
 ]
 
 
@@ -1103,7 +1104,7 @@ def run_sweep(args):
     res = {}
     for name, cname, opt in SWEEP:
         a = copy.copy(args)
-        a.steps = max(200, args.steps) if "steps" not in opt else opt["steps"]
+        a.steps = max(args.steps, opt.get("steps", 200))
         a.warmup = max(5, args.warmup)
         a.no_cpu_baseline = True
         a.lm_dtype = opt.get("lm_dtype", "bf16")
