@@ -1032,7 +1032,11 @@ def run_kernel_only(args, cfg):
             r1 = min(d, r0 + 256)
             w[r0:r1] = (torch.randn(r1 - r0, V, device=dev, generator=g) * cfg.w_std).to(bf)
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 1)
-        if args.lm_dtype == "fp8":
+        if args.self_cond:
+            sc_table = (torch.randn(V, 32, device=dev, generator=g) / math.sqrt(d)).to(bf)
+            ws = dg.workspace(dg.denoise_step_sc_workspace(p), dev)
+            fn = lambda: dg.lm_head_fold_sc(x, w, sc_table, p, ws)
+        elif args.lm_dtype == "fp8":
             w8 = torch.empty(V, d, dtype=torch.uint8, device=dev)
             w_scale = torch.empty(V, dtype=torch.float32, device=dev)
             dg.quantize_weight_e4m3(w, w8, w_scale)
