@@ -1113,7 +1113,15 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
                   scale, 0, aws, workspace_bytes - step_bytes, fs->side, reserve);
     if (rc == DG_OK) {
         const int M = p->B * p->L;
-        const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve);
+        LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve);
+        if (reserve > 0 && plan.kind != kLmSingle && std::getenv("DG_LM_KERNEL") == nullptr) {
+            // one tile per CTA on the SMs left: the single-CTA kernel (its 16
+            // epilogue warps fold a 256-row tile; measured faster than the
+            // 2-SM kernel's 8 at one tile per CTA)
+            const LmPlan single = plan_lm_head(M, p->d, p->V, di->sms - reserve, false, false,
+                                               kLmSingle);
+            if (single.units >= single.total) plan = single;
+        }
         StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
         const StepSource src = step_source(p);
         const AcceptArgs acc = accept_args(p, io);

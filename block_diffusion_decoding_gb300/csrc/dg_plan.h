@@ -46,7 +46,9 @@ struct LmPlan {
 // single 256-row block of bf16 operands, else 16.  DG_LM_KERNEL=single|duo|
 // fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
 // have the 2-SM UMMA kernel only.
-inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool sc = false)
+// only_kind >= 0 restricts the choice to that kernel (as DG_LM_KERNEL does).
+inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool sc = false,
+                           int only_kind = -1)
 {
     LmPlan best{};
     best.M = M;
@@ -64,7 +66,8 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool 
                                                          : -1;
     // a forced kernel FP8 operands or the self-conditioning read-out do not
     // have is ignored
-    const int only = (fp8 || sc) && only_env != kLmDuo && only_env != kLmDuoFused ? -1 : only_env;
+    const int only_req = only_kind >= 0 ? only_kind : only_env;
+    const int only = (fp8 || sc) && only_req != kLmDuo && only_req != kLmDuoFused ? -1 : only_req;
     long best_cost = -1;
     auto consider = [&](int kind, int bn) {
         if (forced_bn && bn != forced_bn) return;

@@ -231,3 +231,34 @@ def test_block_full_converging_final_steps_match_oracle():
                                            & (r_prev["argmax_margin"] >= MARGIN)
                                            & (r_pp["argmax_margin"] >= MARGIN)))
         assert argmax_moved_clearly or st["mean_entropy"] >= cfg.stop_threshold + 2 * H_TOL
+
+
+def test_canvas_step_full_width_equals_the_two_calls():
+    """dg_canvas_step at the full-width step (no SMs set aside at this shape,
+    the LM head on the same plan): the attention output and every step output
+    equal those of dg_canvas_attn and dg_denoise_step, bit for bit."""
+    cfg = dg_synth.CONFIGS["step_full"]
+    B, L, P, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.P, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
+    ai = dg_synth.attention_inputs(cfg)
+    t = {k: to_dev(v) for k, v in ai.items()}
+    x, w = to_dev(dg_synth.lm_hidden(cfg)), to_dev(_weight("step_full"))
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=4, seed=3)
+    rng = np.random.default_rng(8)
+    canvas0 = torch.from_numpy(rng.integers(0, V, B * L).astype(np.int32))
+    got, ref = dg.StepBuffers(B, L, DEV), dg.StepBuffers(B, L, DEV)
+    got.canvas.copy_(canvas0)
+    ref.canvas.copy_(canvas0)
+    out, ref_out = torch.empty_like(t["q"]), torch.empty_like(t["q"])
+    ws = dg.workspace(dg.canvas_step_workspace(p, P, Hq, Hkv, D), DEV)
+    dg.canvas_step(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], out, scale, x, w, p, got, ws)
+    aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    sws = dg.workspace(dg.denoise_step_workspace(p), DEV)
+    dg.canvas_attn(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], ref_out, scale, aws)
+    dg.denoise_step(x, w, p, ref, sws)
+    torch.cuda.synchronize()
+    status_ok(ws)
+    assert torch.equal(out, ref_out)
+    for name in ("canvas", "argmax", "sample", "n_accepted", "stop", "prev_argmax"):
+        assert np.array_equal(np_i32(getattr(got, name)), np_i32(getattr(ref, name))), name
+    assert torch.equal(got.entropy, ref.entropy)
