@@ -98,3 +98,15 @@ def test_moe_shared_expert_only_when_routed_down_weights_are_zero():
     (got,) = _run(a, M, d, f, E, K)
     err = np.abs(got[0] - ref["out"]).max(axis=1) / np.abs(ref["out"]).max(axis=1)
     assert err.max() < OUT_TOL
+
+
+@pytest.mark.parametrize("M,d,f,E,K", [(96, 256, 128, 8, 8), (2048, 256, 128, 16, 4)])
+def test_moe_edges(M, d, f, E, K):
+    """Every expert chosen by every row (top_k = E), and the largest M the
+    routing takes (2048 rows: eight 256-token canvases)."""
+    a = _small(M, d, f, E, K, seed=M + 3 * E)
+    ref = oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], K)
+    (got,) = _run(a, M, d, f, E, K)
+    if K == E:
+        assert (np.sort(got[1], axis=1) == np.arange(E)).all()
+    _check(got, ref, K)

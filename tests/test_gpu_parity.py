@@ -521,3 +521,31 @@ def test_canvas_step_matches_the_two_calls_and_the_oracle(name):
     ref = oracle.step(xb, wb, canvas0, prev, B, L, 0.8, 0.1, 5, 2, workers=8)
     check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
     assert np.array_equal(np_i32(bufs.stop), ref["stop"])
+
+
+def test_canvas_step_without_a_cache_and_ragged_canvases():
+    """dg_canvas_step with no cached keys (P = 0), two canvases of 100
+    positions (ragged against the 128-row tiles)."""
+    cfg = dg_synth.StepConfig("cs_edge", B=2, L=100, Hq=4, Hkv=1, D=128, P=0, d=256, V=4096,
+                              w_std=0.05, seed=12)
+    B, L, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
+    ai = dg_synth.attention_inputs(cfg)
+    q, kc, vc = to_dev(ai["q"]), to_dev(ai["kc"]), to_dev(ai["vc"])
+    xb, wb = dg_synth.lm_hidden(cfg), dg_synth.lm_weight(cfg)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    p = dg.step_params(B, L, d, V, 0.6, 0.1, 0.005, step=1, seed=2)
+    bufs = dg.StepBuffers(B, L, DEV)
+    canvas0 = oracle.init_canvas(B * L, V, 2)
+    bufs.canvas.copy_(torch.from_numpy(canvas0))
+    out = torch.full_like(q, float("nan"))
+    ws = dg.workspace(dg.canvas_step_workspace(p, 0, Hq, Hkv, D), DEV)
+    dg.canvas_step(q, None, None, kc, vc, out, scale, to_dev(xb), to_dev(wb), p, bufs, ws)
+    torch.cuda.synchronize()
+    status_ok(ws)
+    rows = np.arange(B * L * Hq)
+    ref_o = oracle.attention_rows(ai["q"], ai["kp"], ai["vp"], ai["kc"], ai["vc"], B, L, 0, Hq, Hkv,
+                                  D, scale, rows)
+    got_o = out.float().reshape(-1, D).cpu().numpy()
+    assert (np.abs(got_o - ref_o).max(axis=1) / np.abs(ref_o).max(axis=1)).max() < ATTN_TOL
+    ref = oracle.step(xb, wb, canvas0, np.full(B * L, -1, np.int32), B, L, 0.6, 0.1, 2, 1)
+    check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
