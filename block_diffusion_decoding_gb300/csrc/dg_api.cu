@@ -1067,6 +1067,11 @@ int fork_streams(ForkStreams **out)
 constexpr int kReserveTiles = 6;
 int attn_reserve(int B, int L, int P, int Hq, int Hkv, int D, int sms)
 {
+    // DG_ATTN_RESERVE=n forces n SMs (0: none) for the attention
+    if (const char *env = std::getenv("DG_ATTN_RESERVE")) {
+        const int n = std::atoi(env);
+        return n > 0 && n <= sms - 2 ? n & ~1 : 0;
+    }
     const int cap = sms / 8;
     const AttnPlan ap = plan_attn(B, L, P, Hq, Hkv, D, sms, cap);
     if (ap.blocks > cap || ap.tps > kReserveTiles) return 0;

@@ -247,7 +247,7 @@ constexpr int kMoeMaxTopK = 8;
 constexpr int kMoeMaxTokens = 2048;    // canvas rows per call
 constexpr int kMoeChunk = 128;         // tokens per token tile of the expert GEMMs
 constexpr int kMoeRouteThreads = 1024;
-constexpr int kMoeRouterKSlice = 256;  // k values per router CTA (d % 256 == 0)
+constexpr int kMoeRouterKSlice = 128;  // k values per router CTA (d % 128 == 0)
 // token chunks of one call: every expert's tokens in chunks of kMoeChunk
 constexpr int kMoeMaxChunks =
     kMoeMaxExperts + 1 + (kMoeMaxTokens * (kMoeMaxTopK + 1) + kMoeChunk - 1) / kMoeChunk;

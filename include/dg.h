@@ -41,7 +41,8 @@
  *     the LM-head choice).  For testing and tuning, the environment variables
  *     DG_LM_KERNEL (single | duo | fused), DG_LM_BN (tile width),
  *     DG_LM_EPI (8 | 16: epilogue warps of the 2-SM kernel, bf16 operands),
- *     DG_ATTN_KERNEL (single | pair) and DG_ATTN_SPLITS (key splits) force a
+ *     DG_ATTN_KERNEL (single | pair), DG_ATTN_SPLITS (key splits) and
+ *     DG_ATTN_RESERVE (SMs kept for the attention in dg_canvas_step) force a
  *     choice; a choice the shapes do not allow is ignored.  Results do not
  *     depend on the choice beyond floating-point summation order.
  */
@@ -269,8 +270,7 @@ int dg_lm_head_fold_sc(const uint16_t *hidden, const uint16_t *w, const uint16_t
 /* w_up [E + 1, f, d]; w_down [E + 1, d, f] (index E = the shared expert);   */
 /* out [M, d] fp32.  experts_out [M, top_k] int32 and gates_out [M, top_k]   */
 /* fp32 receive the routing when not NULL.  Only the experts some row picks */
-/* are read.  Supported: 1 <= M <= 2048; d a multiple of 256, f of 128,      */
-/* both <= 16384;                                                             */
+/* are read.  Supported: 1 <= M <= 2048; d, f multiples of 128, <= 16384;     */
 /* 1 <= top_k <= min(8, E), E <= 128.  16-byte aligned pointers.  Errors as  */
 /* dg_denoise_step; device-side waits report through the workspace status.  */
 /* ------------------------------------------------------------------------ */

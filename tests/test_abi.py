@@ -162,7 +162,7 @@ def test_moe_rejects_bad_arguments_before_launch(lib):
     p = dg.moe_params(256, 2816, 768, 128, 8)
     assert dg.moe_ffn_workspace(p) > 256 * 9 * 2816 * 4
     assert dg.moe_ffn_workspace(dg.moe_params(256, 2816, 700, 128, 8)) == 0    # f % 128
-    assert dg.moe_ffn_workspace(dg.moe_params(256, 384, 768, 128, 8)) == 0     # d % 256
+    assert dg.moe_ffn_workspace(dg.moe_params(256, 320, 768, 128, 8)) == 0     # d % 128
     assert dg.moe_ffn_workspace(dg.moe_params(4096, 2816, 768, 128, 8)) == 0   # M > 2048
     assert dg.moe_ffn_workspace(dg.moe_params(256, 2816, 768, 4, 8)) == 0      # top_k > E
     bad = dg.moe_params(256, 2816, 768, 256, 8)                                 # E > 128

@@ -64,7 +64,7 @@ def _small(M, d, f, E, K, seed, alpha=0.8):
     return dg_synth.moe_inputs(cfg)
 
 
-@pytest.mark.parametrize("M,d,f,E,K", [(64, 256, 256, 16, 4), (100, 512, 128, 20, 3),
+@pytest.mark.parametrize("M,d,f,E,K", [(64, 256, 256, 16, 4), (100, 384, 128, 20, 3),
                                        (300, 256, 384, 8, 4), (1, 256, 128, 4, 1),
                                        (17, 256, 256, 128, 8), (130, 768, 128, 40, 2)])
 def test_moe_matches_oracle_small(M, d, f, E, K):
