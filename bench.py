@@ -218,12 +218,13 @@ def run_reference(args, cfg):
     if rank != 0:
         return 0
     host = host_inputs_small_sample(cfg, seed=cfg.seed)
-    times = []
+    times, walls = [], []
     desc = ""
     for i in range(args.warmup + args.steps):
-        t, desc, _ = oracle_step_estimate(cfg, host, v_sample=2048, attn_rows=16, seed=i)
+        t, desc, parts = oracle_step_estimate(cfg, host, v_sample=2048, attn_rows=16, seed=i)
         if i >= args.warmup:
             times.append(t)
+            walls.append(sum(parts.values()))
     per = sum(times) / len(times)
     value = 1.0 / per
     line = dict(impl="reference", metric="denoise steps/s (256-tok canvas, bs=1)",
@@ -234,7 +235,10 @@ def run_reference(args, cfg):
                 cpu_baseline=dict(value=value, unit="steps/s", cores=1, kind="oracle",
                                   sample=desc),
                 e2e=dict(value=value, unit="steps/s", h2d_bytes_per_step=0,
-                         d2h_bytes_per_step=0))
+                         d2h_bytes_per_step=0),
+                # ms_per_step is the sample's time scaled to a whole step; the
+                # oracle actually ran this long per timed step
+                sample_wall_s_per_step=sum(walls) / len(walls))
     print(json.dumps(line), flush=True)
     return 0
 
@@ -250,12 +254,13 @@ def run_reference_moe(args, mcfg):
     sub = dg_synth.MoeConfig(mcfg.name + "_rows", M=64, d=mcfg.d, f=mcfg.f, E=mcfg.E,
                              top_k=mcfg.top_k, alpha=mcfg.alpha, seed=mcfg.seed)
     a = dg_synth.moe_inputs(sub)
-    times = []
+    times, walls = [], []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], sub.top_k)
         if i >= args.warmup:
-            times.append((time.perf_counter() - t0) * mcfg.M / sub.M)
+            walls.append(time.perf_counter() - t0)
+            times.append(walls[-1] * mcfg.M / sub.M)
     per = sum(times) / len(times)
     value = 1.0 / per
     desc = ("oracle (numpy fp64 matmuls + plain routing, 1 thread): the first %d of %d canvas "
@@ -272,7 +277,8 @@ def run_reference_moe(args, mcfg):
                 cpu_baseline=dict(value=value, unit="layers/s", cores=1, kind="oracle",
                                   sample=desc),
                 e2e=dict(value=value, unit="layers/s", h2d_bytes_per_step=0,
-                         d2h_bytes_per_step=0))
+                         d2h_bytes_per_step=0),
+                sample_wall_s_per_step=sum(walls) / len(walls))
     print(json.dumps(line), flush=True)
     return 0
 
