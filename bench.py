@@ -50,6 +50,30 @@ def _peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# nominal dense peaks of the part (HBM3e bandwidth, bf16 tensor rate), reported
+# beside the measured ones
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def _host_cpu():
+    """The host's CPU model (best effort) and logical core count."""
+    import platform
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k = line.split(":", 1)[0].strip().lower()
+                if k in ("model name", "model", "cpu model", "hardware"):
+                    v = line.split(":", 1)[1].strip()
+                    if v and not v.isdigit():
+                        model = v
+                        break
+    except OSError:
+        pass
+    return dict(cpu_model=model, machine=platform.machine(), nproc=os.cpu_count())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -232,7 +256,7 @@ def run_reference(args, cfg):
                 warmup=args.warmup, ms_per_step=per * 1e3, higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
                 config=_config_json(cfg, l2="n/a (CPU)"),
-                cpu_baseline=dict(value=value, unit="steps/s", cores=1, kind="oracle",
+                cpu_baseline=dict(value=value, unit="steps/s", cores=1, kind="oracle", **_host_cpu(),
                                   sample=desc),
                 e2e=dict(value=value, unit="steps/s", h2d_bytes_per_step=0,
                          d2h_bytes_per_step=0),
@@ -274,7 +298,7 @@ def run_reference_moe(args, mcfg):
                                                            mcfg.f, mcfg.top_k),
                         "global_batch": 1, "seq_len": mcfg.M, "parallelism": "replicas",
                         "l2": "n/a (CPU)"},
-                cpu_baseline=dict(value=value, unit="layers/s", cores=1, kind="oracle",
+                cpu_baseline=dict(value=value, unit="layers/s", cores=1, kind="oracle", **_host_cpu(),
                                   sample=desc),
                 e2e=dict(value=value, unit="layers/s", h2d_bytes_per_step=0,
                          d2h_bytes_per_step=0),
@@ -534,7 +558,7 @@ def run_ours(args, cfg, emit=True):
                                     sc_table=sc_host)[0] for _ in range(2)]
         _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8,
                                           sc_table=sc_host)
-        cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle",
+        cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle", **_host_cpu(),
                    sample=desc)
     if world > 1:
         tdist.destroy_process_group()
@@ -553,12 +577,13 @@ def run_ours(args, cfg, emit=True):
                     peak_source=peak_kind + (" (MEASURED_PEAKS.json bf16_tflops, burst, x2 for "
                                              "E4M3 by the nominal dense ratio)" if fp8 else
                                              " (MEASURED_PEAKS.json bf16_tflops, burst)"),
-                    algorithmic_flops=lm_flops)
+                    algorithmic_flops=lm_flops,
+                    frac_of_nominal=lm_tflops / (NOMINAL_BF16_TFLOPS * (2.0 if fp8 else 1.0)))
     else:
         roof = dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
                     frac=lm_gbs / hbm_peak, traffic=traffic, kernel=lm_plan["kernel"],
                     peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
-                    algorithmic_bytes=lm_bytes)
+                    algorithmic_bytes=lm_bytes, frac_of_nominal=lm_gbs / NOMINAL_HBM_GBS)
     line = dict(
         metric="denoise steps/s (256-tok canvas, bs=1)", value=value, unit="steps/s",
         n_gpus=world, steps=args.steps, warmup=args.warmup, ms_per_step=step_ms,
@@ -712,7 +737,7 @@ def run_block(args, cfg, emit=True):
                 "w": w[:, :16384].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)}
         est = [oracle_block_step_estimate(cfg, host)[0] for _ in range(2)]
         _, desc = oracle_block_step_estimate(cfg, host)
-        cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle",
+        cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle", **_host_cpu(),
                    sample=desc)
     if world > 1:
         tdist.destroy_process_group()
@@ -738,7 +763,7 @@ def run_block(args, cfg, emit=True):
         roofline=dict(bound="hbm", achieved=lm_gbs, peak=hbm_peak, unit="GB/s",
                       frac=lm_gbs / hbm_peak, traffic=traffic, kernel=lm_plan["kernel"],
                       peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
-                      algorithmic_bytes=lm_bytes),
+                      algorithmic_bytes=lm_bytes, frac_of_nominal=lm_gbs / NOMINAL_HBM_GBS),
         step_roofline_ms=lm_bytes / (hbm_peak * 1e9) * 1e3,
         step_frac_of_roofline=lm_bytes / (hbm_peak * 1e9) * 1e3 / step_ms,
         cpu_baseline=cpu,
@@ -830,7 +855,7 @@ def run_encoder(args, cfg, emit=True):
         roofline=dict(bound="tensor", achieved=tflops, peak=bf16_peak, unit="TFLOP/s",
                       frac=tflops / bf16_peak, traffic=None, kernel="attention (causal)",
                       peak_source=peak_kind + " (MEASURED_PEAKS.json bf16_tflops, burst)",
-                      algorithmic_flops=flops),
+                      algorithmic_flops=flops, frac_of_nominal=tflops / NOMINAL_BF16_TFLOPS),
         step_roofline_ms=roof_ms, step_frac_of_roofline=roof_ms / ms,
         clocks=clk.summary(), device_status=status)
     if not emit:
@@ -947,7 +972,7 @@ def run_moe(args, mcfg, emit=True):
         t0 = time.perf_counter()
         oracle.moe_ffn(host["x"], host["wr"], host["wg"], host["wu"], host["wd"], K)
         t_or = time.perf_counter() - t0
-        cpu = dict(value=1.0 / t_or, unit="layers/s", cores=1, kind="oracle",
+        cpu = dict(value=1.0 / t_or, unit="layers/s", cores=1, kind="oracle", **_host_cpu(),
                    sample="oracle (numpy fp64 matmuls + plain routing, 1 thread): the whole "
                           "layer, all %d rows" % M)
     if world > 1:
@@ -968,7 +993,7 @@ def run_moe(args, mcfg, emit=True):
                       achieved=gbs, peak=hbm_peak, unit="GB/s", frac=gbs / hbm_peak,
                       traffic=None, kernel="moe_ffn_kernel (+ router, route, gather, combine)",
                       peak_source=peak_kind + " (MEASURED_PEAKS.json hbm_gbs)",
-                      algorithmic_bytes=nbytes),
+                      algorithmic_bytes=nbytes, frac_of_nominal=gbs / NOMINAL_HBM_GBS),
         step_roofline_ms=roof_ms, step_frac_of_roofline=roof_ms / ms,
         TFLOP_per_s=flops / (ms * 1e-3) / 1e12,
         cpu_baseline=cpu,
