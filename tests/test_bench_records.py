@@ -31,7 +31,8 @@ def _fields(kernel):
 def test_records_are_consistent():
     # within 1% above the algorithmic bytes: W + X (bf16), codes + scales (FP8)
     algo = {"lm_head_duo_kernel": 2816 * 262144 * 2 + 256 * 2816 * 2,
-            "lm_head_duo_fp8_kernel": 2816 * 262144 + 4 * 262144 + 256 * 2816 + 4 * 256}
+            "lm_head_duo_fp8_kernel": 2816 * 262144 + 4 * 262144 + 256 * 2816 + 4 * 256,
+            "lm_head_duo_sc_kernel": 2816 * 262144 * 2 + 256 * 2816 * 2 + 262144 * 32 * 2}
     for kernel, a in algo.items():
         rec = _fields(kernel)
         assert rec["kernel"] == kernel and rec["shape"] == "256x2816x262144"
@@ -44,7 +45,7 @@ def test_records_match_the_current_sources():
     """Skipped (not failed) after a kernel change, until the records are
     captured again on a GPU; bench.py then reports traffic as null."""
     got = {k: bench._traffic_record(SRCS, k, FULL)
-           for k in ("lm_head_duo_kernel", "lm_head_duo_fp8_kernel")}
+           for k in ("lm_head_duo_kernel", "lm_head_duo_fp8_kernel", "lm_head_duo_sc_kernel")}
     if any(v is None for v in got.values()):
         pytest.skip("LM-head sources changed since the ncu records were taken")
     for k, v in got.items():
