@@ -56,21 +56,30 @@ NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 
 
+# Arm cores by (implementer, part) as /proc/cpuinfo gives them
+_ARM_PARTS = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+              ("0x41", "0xd0c"): "Arm Neoverse N1", ("0x41", "0xd49"): "Arm Neoverse N2"}
+
+
 def _host_cpu():
     """The host's CPU model (best effort) and logical core count."""
     import platform
     model = platform.processor() or platform.machine()
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                k = line.split(":", 1)[0].strip().lower()
-                if k in ("model name", "model", "cpu model", "hardware"):
-                    v = line.split(":", 1)[1].strip()
-                    if v and not v.isdigit():
-                        model = v
-                        break
+                if ":" not in line:
+                    continue
+                k, v = (x.strip() for x in line.split(":", 1))
+                fields.setdefault(k.lower(), v)
     except OSError:
         pass
+    if fields.get("model name"):
+        model = fields["model name"]
+    elif "cpu implementer" in fields and "cpu part" in fields:
+        imp, part = fields["cpu implementer"].lower(), fields["cpu part"].lower()
+        model = _ARM_PARTS.get((imp, part), "Arm implementer %s part %s" % (imp, part))
     return dict(cpu_model=model, machine=platform.machine(), nproc=os.cpu_count())
 
 
