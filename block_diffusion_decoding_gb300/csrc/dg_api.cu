@@ -1041,6 +1041,9 @@ namespace {
 struct ForkStreams {
     cudaStream_t side = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    // a step's fork, launches and join are enqueued under this lock, so calls
+    // from several host threads cannot interleave their event records
+    std::mutex mu;
 };
 std::map<int, ForkStreams> g_fork;
 
@@ -1107,6 +1110,7 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     ForkStreams *fs = nullptr;
     if ((rc = fork_streams(&fs)) != DG_OK) return rc;
+    std::lock_guard<std::mutex> fork_lock(fs->mu);
     const size_t step_bytes = round_up(dg_denoise_step_workspace(p), 256);
     uint8_t *aws = static_cast<uint8_t *>(workspace) + step_bytes;
     cudaStream_t st = as_stream(stream);

@@ -184,7 +184,9 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 /* `stream` ends when both have); when the attention needs few CTAs (at most  */
 /* an eighth of the SMs) the LM head is planned on the SMs it leaves free.    */
 /* The second stream is one per device, shared by all calls: calls on         */
-/* different streams are correct but their attentions run one after another.  */
+/* different streams, or from several host threads (the library enqueues a    */
+/* call's fork, launches and join under a lock), are correct but their        */
+/* attentions run one after another.                                          */
 /* Arguments as the two calls (B, L of p; q / out [B, L, Hq, D]; caches       */
 /* [B, P, Hkv, D]); one workspace of dg_canvas_step_workspace bytes: the     */
 /* step's first (its status word at the start), then the attention's from    */

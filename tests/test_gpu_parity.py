@@ -549,3 +549,59 @@ def test_canvas_step_without_a_cache_and_ragged_canvases():
     assert (np.abs(got_o - ref_o).max(axis=1) / np.abs(ref_o).max(axis=1)).max() < ATTN_TOL
     ref = oracle.step(xb, wb, canvas0, np.full(B * L, -1, np.int32), B, L, 0.6, 0.1, 2, 1)
     check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
+
+
+def test_canvas_step_from_several_host_threads():
+    """dg_canvas_step called from four host threads at once, each on its own
+    stream, buffers and workspace (the library's forked stream and events are
+    shared): every thread's repeated steps equal the same step made alone,
+    bit for bit."""
+    import threading
+    cfg = dg_synth.CONFIGS["step_small"]
+    B, L, P, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.P, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
+    ai = dg_synth.attention_inputs(cfg)
+    t = {k: to_dev(v) for k, v in ai.items()}
+    x, w = to_dev(dg_synth.lm_hidden(cfg)), to_dev(dg_synth.lm_weight(cfg))
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    canvas0 = oracle.init_canvas(B * L, V, 4)
+
+    def make(seed):
+        p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=1, seed=seed)
+        return dict(p=p, bufs=dg.StepBuffers(B, L, DEV), out=torch.empty_like(t["q"]),
+                    ws=dg.workspace(dg.canvas_step_workspace(p, P, Hq, Hkv, D), DEV),
+                    stream=torch.cuda.Stream())
+
+    def run(c, n):
+        with torch.cuda.stream(c["stream"]):
+            for _ in range(n):
+                c["bufs"].canvas.copy_(torch.from_numpy(canvas0))
+                c["bufs"].prev_argmax.fill_(-1)
+                dg.canvas_step(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], c["out"], scale, x, w,
+                               c["p"], c["bufs"], c["ws"], stream=c["stream"])
+        c["stream"].synchronize()
+
+    ctx = [make(10 + i) for i in range(4)]
+    alone = []
+    for c in ctx:
+        run(c, 1)
+        alone.append((c["bufs"].readback.clone(), c["out"].clone()))
+    torch.cuda.synchronize()
+    errs = []
+
+    def worker(c):
+        try:
+            run(c, 25)
+        except Exception as e:   # reported below
+            errs.append(e)
+
+    threads = [threading.Thread(target=worker, args=(c,)) for c in ctx]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errs
+    for c, (rb, o) in zip(ctx, alone):
+        status_ok(c["ws"])
+        assert torch.equal(c["bufs"].readback, rb)
+        assert torch.equal(c["out"], o)
