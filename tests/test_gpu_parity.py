@@ -486,11 +486,13 @@ def test_block_converging_matches_oracle():
     assert abs(float(bufs.mean_entropy[0]) - float(last["mean_entropy"][0])) < H_TOL
 
 
-@pytest.mark.parametrize("name", ["step_small", "batch4"])
+@pytest.mark.parametrize("name", ["step_small", "batch1", "batch4"])
 def test_canvas_step_matches_the_two_calls_and_the_oracle(name):
     """dg_canvas_step (attention on a forked stream, the LM head planned around
-    it) gives the attention output of dg_canvas_attn bit for bit and a step
-    that matches the oracle."""
+    it) gives the attention output of dg_canvas_attn (bit for bit where its key
+    splits are the same; capped to the SMs set aside for it, they can differ,
+    and the rows then agree to bf16 rounding) and a step that matches the
+    oracle."""
     cfg = dg_synth.CONFIGS[name]
     B, L, P, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.P, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
     ai = dg_synth.attention_inputs(cfg)
@@ -517,7 +519,12 @@ def test_canvas_step_matches_the_two_calls_and_the_oracle(name):
     aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
     dg.canvas_attn(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], ref_out, scale, aws)
     torch.cuda.synchronize()
-    assert torch.equal(out, ref_out)
+    if name == "step_small":
+        assert torch.equal(out, ref_out)
+    else:
+        a, r = out.float(), ref_out.float()
+        row_max = r.abs().amax(dim=-1, keepdim=True)
+        assert ((a - r).abs() <= 2.0 ** -6 * row_max + 1e-6).all()
     ref = oracle.step(xb, wb, canvas0, prev, B, L, 0.8, 0.1, 5, 2, workers=8)
     check_step_against_oracle(bufs, ref, B, L, exact_tokens=False)
     assert np.array_equal(np_i32(bufs.stop), ref["stop"])
