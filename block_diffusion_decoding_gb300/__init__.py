@@ -144,13 +144,15 @@ def lib():
     return _lib()
 
 
+# Every entry point has its argtypes set, so device pointers and streams go
+# through as plain integers (no ctypes object per argument).
 def _p(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def _check(rc: int, what: str):
@@ -217,8 +219,17 @@ class StepBuffers:
         self.n_accepted = torch.zeros(B, **i32)
         self.mean_entropy = torch.zeros(B, dtype=torch.float32, device=device)
 
+    def __setattr__(self, name, value):
+        # a replaced tensor invalidates the cached dg_step_io
+        object.__setattr__(self, name, value)
+        if name != "_io":
+            object.__setattr__(self, "_io", None)
+
     def io(self) -> StepIO:
-        return StepIO(*[ctypes.c_void_p(getattr(self, n).data_ptr()) for n, _ in StepIO._fields_])
+        if self._io is None:
+            self._io = StepIO(*[ctypes.c_void_p(getattr(self, n).data_ptr())
+                                for n, _ in StepIO._fields_])
+        return self._io
 
 
 def denoise_step_workspace(p: StepParams) -> int:
@@ -386,8 +397,17 @@ class BlockBuffers:
         self.mean_entropy = torch.zeros(B, dtype=torch.float32, device=device)
         self.n_accepted_hist = torch.zeros(max_steps * B, **i32)
 
+    def __setattr__(self, name, value):
+        # a replaced tensor invalidates the cached dg_block_io
+        object.__setattr__(self, name, value)
+        if name != "_io":
+            object.__setattr__(self, "_io", None)
+
     def io(self) -> BlockIO:
-        return BlockIO(*[ctypes.c_void_p(getattr(self, n).data_ptr()) for n, _ in BlockIO._fields_])
+        if self._io is None:
+            self._io = BlockIO(*[ctypes.c_void_p(getattr(self, n).data_ptr())
+                                 for n, _ in BlockIO._fields_])
+        return self._io
 
 
 class HiddenSteps(ctypes.Structure):
