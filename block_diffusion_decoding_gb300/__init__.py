@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_UNSUPPORTED",
                 6: "DG_ERR_TIMEOUT", 7: "DG_ERR_DEVICE"}
 
 # Functions include/dg.h declares (checked by the CPU test-suite).
-EXPORTED = ["dg_status_string", "dg_version", "dg_read_device_status",
+EXPORTED = ["dg_status_string", "dg_version", "dg_set_device_checks", "dg_device_checks",
+            "dg_read_device_status",
             "dg_canvas_attn_workspace", "dg_canvas_attn",
             "dg_encoder_append_workspace", "dg_encoder_append",
             "dg_denoise_step_workspace", "dg_denoise_step", "dg_denoise_step_noalloc",
@@ -94,6 +95,8 @@ def _lib():
         sig = {
             "dg_status_string": ([i32], ctypes.c_char_p),
             "dg_version": ([], i32),
+            "dg_set_device_checks": ([i32], i32),
+            "dg_device_checks": ([], i32),
             "dg_read_device_status": ([vp, ctypes.POINTER(ctypes.c_int), i32, vp], i32),
             "dg_canvas_attn_workspace": ([i32] * 6, sz),
             "dg_canvas_attn": ([vp] * 6 + [i32] * 6 + [f32, vp, sz, vp], i32),
@@ -481,6 +484,16 @@ def wait_timeout_probe(workspace, limit_ns: int, stream=None):
     """dg_wait_timeout_probe: a bounded wait that nothing completes, on purpose."""
     _check(_lib().dg_wait_timeout_probe(_p(workspace), workspace.numel(), int(limit_ns),
                                         _stream(stream)), "dg_wait_timeout_probe")
+
+
+def set_device_checks(on: bool) -> None:
+    """dg_set_device_checks: device-side index and finiteness checks (off by
+    default); a failed check reads back as DG_ERR_DEVICE."""
+    _check(_lib().dg_set_device_checks(1 if on else 0), "dg_set_device_checks")
+
+
+def device_checks() -> bool:
+    return bool(_lib().dg_device_checks())
 
 
 def read_device_status(workspace, clear=False, stream=None) -> int:

@@ -53,6 +53,8 @@ struct DeviceInfo {
 };
 
 std::mutex g_mu;
+// dg_set_device_checks: read when a call enqueues its kernels
+std::atomic<int> g_checks{0};
 std::map<int, DeviceInfo> g_dev;
 std::atomic<uint64_t> g_launches{0};
 
@@ -425,8 +427,11 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
         c.sc_part = sco->part;
         c.sc_out = sco->out;
     }
+    AcceptArgs acc_c = acc;
+    acc_c.ws = ws.hdr;
+    acc_c.checks = g_checks.load(std::memory_order_relaxed);
     DG_CUDA_TRY(launch_kernel(combine_accept_kernel, dim3((p->L + c.rows_per_cta - 1) / c.rows_per_cta, p->B), dim3(kAcceptThreads), 0, st,
-                              pdl, c, acc));
+                              pdl, c, acc_c));
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
@@ -612,6 +617,7 @@ static int attn_run(const uint16_t *q, const uint16_t *k_prefix, const uint16_t 
     a.tiles_per_split = ap.tps;
     a.scale_log2 = scale * 1.44269502162933349609375f;
     a.causal = causal;
+    a.checks = g_checks.load(std::memory_order_relaxed);
     a.q = q;
     a.out = out;
     a.ws = static_cast<WsHeader *>(workspace);
@@ -824,6 +830,8 @@ int check_moe_params(const dg_moe_params *p)
 
 }  // namespace
 
+int dg::device_checks() { return g_checks.load(std::memory_order_relaxed); }
+
 extern "C" {
 
 const char *dg_status_string(int status)
@@ -842,6 +850,14 @@ const char *dg_status_string(int status)
 }
 
 int dg_version(void) { return 100; }
+
+int dg_set_device_checks(int on)
+{
+    g_checks.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
+    return DG_OK;
+}
+
+int dg_device_checks(void) { return g_checks.load(std::memory_order_relaxed); }
 
 int dg_read_device_status(const void *workspace, int *status_out, int clear, void *stream)
 {
@@ -1199,6 +1215,7 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
     const int M = p->M, K = p->top_k, E = p->n_experts, d = p->d, f = p->f;
     const uint64_t R = static_cast<uint64_t>(M) * (K + 1);
     MoeArgs a{};
+    a.checks = g_checks.load(std::memory_order_relaxed);
     a.M = M;
     a.d = d;
     a.f = f;
@@ -1333,6 +1350,8 @@ int dg_accept_renoise(const float *entropy, const int32_t *sample, const int32_t
     if (!entropy || !sample || !argmax) return DG_ERR_INVALID_ARG;
     if (workspace == nullptr || workspace_bytes < sizeof(WsHeader)) return DG_ERR_WORKSPACE;
     AcceptArgs acc = accept_args(p, io);
+    acc.ws = static_cast<WsHeader *>(workspace);
+    acc.checks = g_checks.load(std::memory_order_relaxed);
     accept_only_kernel<<<p->B, kAcceptThreads, 0, as_stream(stream)>>>(entropy, sample, argmax, acc);
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());

@@ -361,12 +361,18 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
             tc_fence_after();
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;   // no visible key: zero row
             const size_t nrows = static_cast<size_t>(a.B) * a.L * a.Hq;
+            // device-side checks: a finite softmax sum and output row
+            bool bad = a.checks && live && !isfinite(l);
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32_nowait(tmem + lane_off + Gm::ColO + c0, o);
                 tmem_wait_ld();
                 if (!live) continue;
+                if (a.checks) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) bad |= !isfinite(__uint_as_float(o[k]));
+                }
                 // the output row, or (several key splits) this split's
                 // normalised partial row, as bf16
                 uint16_t *row_out = (a.nsplit == 1)
@@ -390,6 +396,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap *map_kp, const CUten
                 float2 *ml = reinterpret_cast<float2 *>(a.part_ml);
                 ml[static_cast<size_t>(split) * nrows + flat] = make_float2(m_ref, l);
             }
+            if (bad) report_error(a.ws, DG_ERR_DEVICE, 813);
         }
     }
     tc_fence_before();
@@ -484,6 +491,13 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a)
         }
     }
     const float inv = 1.f / den;
+    if (a.checks) {
+        // device-side checks: a positive finite sum over the splits, finite outputs
+        bool bad = !(den > 0.f) || !isfinite(den);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bad |= !isfinite(acc[e]);
+        if (bad) report_error(a.ws, DG_ERR_DEVICE, 811);
+    }
     uint16_t *dst = a.out + row * a.D + lane * per;
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {

@@ -20,6 +20,9 @@ inline int combine_rows_per_cta(int B, int L, int sms)
     return static_cast<int>(need < kCombineRowsMin ? kCombineRowsMin : need > 32 ? 32 : need);
 }
 
+// Host: whether the device-side checks are on (dg_set_device_checks).
+int device_checks();
+
 struct FoldArgs {
     int M, V, BN, ntn, total, n_slots;
     Partials part;
@@ -62,6 +65,10 @@ struct AcceptArgs {
     int32_t *out_argmax;
     int32_t *n_acc_hist;
     unsigned long long cond;   // cudaGraphConditionalHandle
+    // device-side checks (dg_set_device_checks): the combine and acceptance
+    // verify indices and finiteness and report DG_ERR_DEVICE to ws
+    WsHeader *ws;
+    int checks;
 };
 
 struct LmHeadArgs {
@@ -206,6 +213,7 @@ struct AttnArgs {
     int nkt_p, nkt_c;   // key tiles in the prefix / canvas
     int tiles_per_split;
     float scale_log2;   // scale * log2(e)
+    int checks;         // device-side checks (dg_set_device_checks)
     int causal;         // canvas keys after a query's position are masked (cache append)
     const uint16_t *q;  // [B, L, Hq, D]
     uint16_t *out;      // [B, L, Hq, D] (nsplit == 1)
@@ -254,6 +262,7 @@ constexpr int kMoeMaxChunks =
 
 struct MoeArgs {
     int M, d, f, E, top_k;
+    int checks;                 // device-side checks (dg_set_device_checks)
     const uint16_t *x;          // [M, d] bf16
     float *logits;              // [M, E] router logits
     int32_t *sel_expert;        // [M, top_k] chosen experts, best first

@@ -199,8 +199,14 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(MoeArgs a, int nslices)
         }
     }
     if (lane < K) {
+        const float gate = expf(my_l - mx) / s;
+        if (a.checks && (!isfinite(gate) || my_e < 0 || my_e >= E)) {
+            // device-side checks: a finite gate, an expert of the layer
+            report_error(a.ws, DG_ERR_DEVICE, 825);
+            if (my_e < 0 || my_e >= E) my_e = 0;
+        }
         a.sel_expert[t * K + lane] = my_e;
-        a.sel_gate[t * K + lane] = expf(my_l - mx) / s;
+        a.sel_gate[t * K + lane] = gate;
         atomicOr(a.bits + static_cast<size_t>(my_e) * words + (t >> 5), 1u << (t & 31));
     }
 }
@@ -240,6 +246,12 @@ __global__ void __launch_bounds__(kMoeRouteThreads) moe_route_kernel(MoeArgs a)
         cnt[e] = c;
     }
     __syncthreads();
+    if (a.checks && tid == 0) {
+        // device-side check: every token chose top_k distinct experts
+        int routed = 0;
+        for (int e = 0; e < E; ++e) routed += cnt[e];
+        if (routed != M * K) report_error(a.ws, DG_ERR_DEVICE, 821);
+    }
     if (tid < 32) {
         // row offsets and chunk ids (chunks of <= kMoeChunk tokens), experts in
         // order: exclusive scans over the E + 1 experts, 32 at a time
@@ -301,6 +313,10 @@ __global__ void __launch_bounds__(kMoeRouteThreads) moe_route_kernel(MoeArgs a)
     for (int i = tid; i < M * K; i += blockDim.x) {
         const int t = i / K;
         const int e = a.sel_expert[i];
+        if (a.checks && (e < 0 || e >= E)) {
+            report_error(a.ws, DG_ERR_DEVICE, 822);
+            continue;
+        }
         const int w = t >> 5;
         int r = __popc(bits[e * words + w] & ((1u << (t & 31)) - 1u));
         for (int q = 0; q < w; ++q) r += __popc(bits[e * words + q]);
@@ -352,7 +368,13 @@ __global__ void moe_combine_kernel(MoeArgs a)
         const float4 *y = reinterpret_cast<const float4 *>(a.y_sorted);
         float4 s = __ldcg(y + static_cast<size_t>(shared0 + t) * vec + c);
         for (int j = 0; j < K; ++j) {
-            const float4 v = __ldcg(y + static_cast<size_t>(a.pos_of[t * K + j]) * vec + c);
+            const int pj = a.pos_of[t * K + j];
+            if (a.checks && (pj < 0 || pj >= shared0)) {
+                // device-side check: a routed row of the sorted order
+                if (c == 0) report_error(a.ws, DG_ERR_DEVICE, 824);
+                continue;
+            }
+            const float4 v = __ldcg(y + static_cast<size_t>(pj) * vec + c);
             s.x += v.x;
             s.y += v.y;
             s.z += v.z;

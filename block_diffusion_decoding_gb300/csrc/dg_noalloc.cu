@@ -239,6 +239,8 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     acc.n_accepted = io->n_accepted;
     acc.mean_entropy = io->mean_entropy;
     acc.stop = io->stop;
+    acc.ws = hdr;
+    acc.checks = device_checks();
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool pdl = use_pdl(s);

@@ -110,6 +110,18 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
         am = __ldcg(argmax + base + tid);
         pa = a.prev_argmax[base + tid];
         smp = __ldcg(sample + base + tid);
+        if (a.checks) {
+            // device-side checks of the operands (the stage entry takes them from the caller)
+            if (!(h >= 0.f) || !isfinite(h)) report_error(a.ws, DG_ERR_DEVICE, 804);
+            if (smp < 0 || smp >= a.V) {
+                report_error(a.ws, DG_ERR_DEVICE, 805);
+                smp = 0;
+            }
+            if (am < 0 || am >= a.V) {
+                report_error(a.ws, DG_ERR_DEVICE, 806);
+                am = 0;
+            }
+        }
         keys[tid] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(tid);
     }
     __syncthreads();
@@ -134,6 +146,10 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
     int rank = 0;
     if (own) {
         for (int q = 0; q < nq; ++q) rank += prank[q * L + tid];
+        if (a.checks && (rank < 0 || rank >= L)) {
+            report_error(a.ws, DG_ERR_DEVICE, 807);
+            rank = L - 1;
+        }
         hsorted[rank] = h;
     }
     __syncthreads();
@@ -194,6 +210,7 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
         if (a.ctl != nullptr) a.out_argmax[base + tid] = am;
     }
     if (tid == 0) {
+        if (a.checks && !isfinite(total)) report_error(a.ws, DG_ERR_DEVICE, 808);
         const double mean = total / static_cast<double>(L);
         const int stop = (step >= 1 && all_same && mean < static_cast<double>(a.threshold)) ? 1 : 0;
         a.n_accepted[b] = kstar;
@@ -273,11 +290,24 @@ __global__ void __launch_bounds__(kAcceptThreads) combine_accept_kernel(CombineA
             row_state_merge(st, o);
         }
         if (lane == 0) {
-            float h = 0.6931471805599453f * (log2f(st.S) - st.A / st.S);
-            h = fmaxf(h, 0.f);
+            const float h_raw = 0.6931471805599453f * (log2f(st.S) - st.A / st.S);
+            const float h = fmaxf(h_raw, 0.f);
+            int gi = st.gidx, ai = st.aidx;
+            if (a.checks) {
+                // device-side checks: a finite entropy, indices inside the vocabulary
+                if (!isfinite(h_raw)) report_error(a.ws, DG_ERR_DEVICE, 801);
+                if (gi < 0 || gi >= a.V) {
+                    report_error(a.ws, DG_ERR_DEVICE, 802);
+                    gi = 0;
+                }
+                if (ai < 0 || ai >= a.V) {
+                    report_error(a.ws, DG_ERR_DEVICE, 803);
+                    ai = 0;
+                }
+            }
             c.H[r] = h;
-            c.sample[r] = st.gidx;
-            c.argmax[r] = st.aidx;
+            c.sample[r] = gi;
+            c.argmax[r] = ai;
         }
         if (c.sc_out != nullptr) {
             // self-conditioning read-out: lane k sums component k of the

@@ -73,6 +73,22 @@ const char *dg_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int dg_version(void);
 
+/* Device-side checks, off by default (a debugging aid; the pages describe   */
+/* no failure handling).  When on, the combine / acceptance kernels check    */
+/* every sampled and argmax index against [0, V), every entropy and the      */
+/* canvas total for finiteness and every rank against [0, L); the attention  */
+/* kernels and the split merge check each row's softmax sum and outputs for  */
+/* finiteness; the MoE routing checks expert ids, positions and the token    */
+/* count.  A failed check records DG_ERR_DEVICE (and a location code) in the */
+/* call's workspace status word, read with dg_read_device_status (or        */
+/* dg_noalloc_read_device_status), and an out-of-range index is replaced by  */
+/* 0 before it is stored; results are otherwise those of the unchecked       */
+/* kernels.  The setting is process-wide, read when a call enqueues its      */
+/* kernels (a captured graph keeps the setting of its capture).  Returns     */
+/* DG_OK.                                                                    */
+int dg_set_device_checks(int on);
+int dg_device_checks(void);
+
 /* Device status word kept in the first bytes of every workspace: 0 when no
  * kernel has reported a problem, else a DG_ERR_* code.  Reads it with a
  * synchronous copy on `stream` into *status_out (host).  Clears it when
