@@ -468,15 +468,18 @@ def run_ours(args, cfg, emit=True):
             dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws)
             lm_step(p)
 
-    def timed(fn, n, first):
-        """Per-iteration CUDA-event times (ms) with an L2 flush before each iteration."""
+    def timed(fn, n, first, label="step"):
+        """Per-iteration CUDA-event times (ms) with an L2 flush before each
+        iteration; each iteration is an NVTX range (for a timeline profiler)."""
         evs = []
         for i in range(n):
             flush.fill_(i & 0xFF)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.nvtx.range_push(label)
             s.record(stream)
             fn(first + i)
             e.record(stream)
+            torch.cuda.nvtx.range_pop()
             evs.append((s, e))
         torch.cuda.synchronize(dev)
         return [s.elapsed_time(e) for s, e in evs]
@@ -503,9 +506,9 @@ def run_ours(args, cfg, emit=True):
     step_ms = _reduce_max(step_ms, dev)
 
     # ---- per-kernel timings (same flush discipline) for the roofline
-    lm_ms = statistics.mean(timed(lambda k: lm_fold(), args.steps, 0))
+    lm_ms = statistics.mean(timed(lambda k: lm_fold(), args.steps, 0, "lm_head"))
     at_ms = statistics.mean(timed(lambda k: dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale,
-                                                           aws), args.steps, 0))
+                                                           aws), args.steps, 0, "canvas_attn"))
     # FP8: W codes + column scales, and the bf16 hidden states read by the row quantisation;
     # self-conditioning: + the bf16 table E [V, 32]
     lm_bytes = (d * V + 4 * V if fp8 else d * V * 2) + M * d * 2 + (V * 32 * 2 if sc else 0)
