@@ -1427,7 +1427,8 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
         static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(stride),
         static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.grid * 4 + plan.kind),
         static_cast<uint64_t>(dev), reinterpret_cast<uint64_t>(fn),
-        reinterpret_cast<uint64_t>(user)};
+        reinterpret_cast<uint64_t>(user),
+        static_cast<uint64_t>(g_checks.load(std::memory_order_relaxed))};
 
     BlockGraph *bgp = nullptr;
     {
@@ -1498,7 +1499,13 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
             return DG_ERR_CUDA;
         }
         std::lock_guard<std::mutex> lk(g_mu);
-        bgp = &(g_block_graphs[key] = bg);
+        auto ins = g_block_graphs.emplace(key, bg);
+        if (!ins.second) {
+            // another thread built the same graph meanwhile: keep that one
+            cudaGraphExecDestroy(bg.exec);
+            cudaGraphDestroy(bg.graph);
+        }
+        bgp = &ins.first->second;
     }
     loop_init_kernel<<<std::max(1, (M + 255) / 256), 256, 0, st>>>(
         ctl, bp->max_steps, bp->t_start, bp->t_end, p->B, done, io->steps_taken, io->canvas, prev,

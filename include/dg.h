@@ -84,8 +84,8 @@ int dg_version(void);
 /* dg_noalloc_read_device_status), and an out-of-range index is replaced by  */
 /* 0 before it is stored; results are otherwise those of the unchecked       */
 /* kernels.  The setting is process-wide, read when a call enqueues its      */
-/* kernels (a captured graph keeps the setting of its capture).  Returns     */
-/* DG_OK.                                                                    */
+/* kernels (a graph the caller captures keeps the setting of its capture;   */
+/* dg_generate_block keeps one graph per setting).  Returns DG_OK.          */
 int dg_set_device_checks(int on);
 int dg_device_checks(void);
 

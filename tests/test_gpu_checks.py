@@ -152,3 +152,32 @@ def test_sample_outside_the_vocabulary_is_reported_and_replaced(checks_on):
     assert dg.read_device_status(ws) == DG_ERR_DEVICE
     canvas = np_i32(bufs.canvas)
     assert canvas[4] == 0 and canvas[5] == 5
+
+
+def test_checked_block_loop_equals_unchecked():
+    """The block loop keeps one graph per setting of the checks: both give the
+    same run, and the checked one reports nothing."""
+    cfg = dg_synth.StepConfig("blk_chk", L=64, d=256, V=2048, w_std=0.02, seed=18)
+    wb = dg_synth.lm_weight(cfg)
+    tg = dg_synth.block_targets(cfg)
+    N = 48
+    hs = to_dev(np.stack([dg_synth.block_hidden(cfg, wb, tg, k) for k in range(N)]))
+    w = to_dev(wb)
+    p = dg.step_params(1, cfg.L, cfg.d, cfg.V, 0.8, 0.1, 0.005, step=0, seed=9)
+    bp = dg.block_params(N, 0.8, 0.4, cfg.L * cfg.d)
+    ws = dg.workspace(dg.generate_block_workspace(p, bp), DEV)
+    bufs = dg.BlockBuffers(1, cfg.L, N, DEV)   # the same buffers: one graph per setting
+    runs = []
+    for on in (False, True, False):
+        dg.set_device_checks(on)
+        try:
+            dg.generate_block(hs, w, p, bp, bufs, ws)
+            torch.cuda.synchronize()
+        finally:
+            dg.set_device_checks(False)
+        status_ok(ws)
+        runs.append({n: getattr(bufs, n).clone()
+                     for n in ("steps_taken", "canvas", "argmax", "n_accepted_hist")})
+    for r in runs[1:]:
+        for n, v in r.items():
+            assert torch.equal(v, runs[0][n]), n
