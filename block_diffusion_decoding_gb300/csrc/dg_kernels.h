@@ -134,9 +134,7 @@ constexpr int kDuoStages = 6;
 // (CG = 2) suffice and leave the producer and MMA warps more issue slots.
 // With several row blocks the W tiles come from L2, the tiles arrive at the
 // MMA rate and the fold's latency shows: 16 warps (CG = 4).  FP8 tiles carry
-// half the bytes; 8 warps measured faster there too (176.6-177.4 against
-// 180.1-180.2 us for 16, 178.1 for 12: the fewer epilogue warps leave the
-// MMA and producer warps more issue slots).
+// half the bytes and take 16 too.
 constexpr int kDuoCGNarrow = 2;
 constexpr int kDuoCGWide = 4;
 template <int kCG>

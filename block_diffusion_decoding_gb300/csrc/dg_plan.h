@@ -109,7 +109,7 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool 
     if (best.duo()) {
         const char *env_e = std::getenv("DG_LM_EPI");
         const int forced_e = env_e ? std::atoi(env_e) : 0;
-        best.epi_warps = fp8 ? 4 * kDuoCGNarrow
+        best.epi_warps = fp8 ? 4 * kDuoCGWide
                          : sc ? 4 * kDuoCGNarrow
                          : forced_e == 8 || forced_e == 16 ? forced_e
                          : best.mblocks == 1             ? 4 * kDuoCGNarrow
