@@ -66,11 +66,13 @@ def _small(M, d, f, E, K, seed, alpha=0.8):
 
 @pytest.mark.parametrize("M,d,f,E,K", [(64, 256, 256, 16, 4), (100, 384, 128, 20, 3),
                                        (300, 256, 384, 8, 4), (1, 256, 128, 4, 1),
-                                       (17, 256, 256, 128, 8), (130, 768, 128, 40, 2)])
+                                       (17, 256, 256, 128, 8), (130, 768, 128, 40, 2),
+                                       (5, 128, 128, 6, 2)])
 def test_moe_matches_oracle_small(M, d, f, E, K):
     """Several tiles of f and d and k slices of the router, ragged token counts,
     an expert with more than one 128-token chunk (300 rows over 8 experts),
-    a single row, 128 experts, two 128-row token chunks of the router."""
+    a single row, 128 experts, two 128-row token chunks of the router, and the
+    smallest hidden size (one k slice of the router, one d tile)."""
     a = _small(M, d, f, E, K, seed=M + E)
     ref = oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], K)
     got, again = _run(a, M, d, f, E, K, reps=2)
