@@ -76,27 +76,35 @@ __global__ void __launch_bounds__(256) logits_fold_kernel(const float *__restric
 }
 
 // ---------------------------------------------------------------- accept (one canvas)
-// Run by one CTA of kAcceptThreads threads (>= L).  The rank of every key
-// (H, position) among the L keys gives the ascending order without a sorting
-// network: each key is counted against up to kRankSplit slices of the keys
-// by separate threads, and the slice counts are summed.  The exclusive
-// prefix sums of the sorted entropies (fp64) never decrease, so k* = #{j :
-// sum of the first j sorted entropies <= b} (and k* >= 1); one warp scans
-// them 32 at a time and stops at the first chunk that passes b.  Position i
-// is accepted iff its rank is below k*.
+// Run by one CTA of kAcceptThreads threads (>= L).  Only the positions whose
+// entropy is within the bound b (the set C) need an exact order: a sorted
+// prefix that holds any larger entropy sums past b (an fp64 sum of
+// non-negative terms is at least each of its terms), so the accepted
+// positions are C's smallest keys (H, position) and at most one more, the
+// smallest key outside C, which sorts right after all of C.  C is compacted
+// in position order; the rank of every key of C among them gives the
+// ascending order without a sorting network: each key is counted against up
+// to kRankSplit slices of C's keys by separate threads, and the slice counts
+// are summed.  The exclusive prefix sums of the sorted entropies (fp64)
+// never decrease, so k* = #{j : sum of the first j sorted entropies <= b}
+// (and k* >= 1); one warp scans them 32 at a time and stops at the first
+// chunk that passes b.  Position i is accepted iff its rank is below k*.
 constexpr int kRankSplit = 4;
 
 __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float *__restrict__ H,
                               const int32_t *__restrict__ sample,
                               const int32_t *__restrict__ argmax)
 {
-    __shared__ __align__(16) uint64_t keys[kMaxCanvas];
-    __shared__ float hsorted[kMaxCanvas];
+    __shared__ __align__(16) uint64_t keys[kMaxCanvas];   // C's keys, in position order
+    __shared__ float hsorted[kMaxCanvas];                 // C sorted, then the first key past C
     __shared__ int prank[kRankSplit * kMaxCanvas];
+    __shared__ float hpos[kMaxCanvas];                    // the entropies, in position order
+    __shared__ int wcnt[kAcceptThreads / 32];
+    __shared__ uint64_t wmin[kAcceptThreads / 32];
     __shared__ double wsum[1];
     __shared__ int s_kstar;
     const int tid = threadIdx.x, nt = blockDim.x;
-    const int lane = tid & 31, wid = tid >> 5;
+    const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
     const int L = a.L;
     const size_t base = static_cast<size_t>(b) * L;
     const bool own = tid < L;    // this thread's position i = tid (nt >= L)
@@ -122,15 +130,47 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
                 am = 0;
             }
         }
-        keys[tid] = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(tid);
+    }
+    const uint64_t key = (static_cast<uint64_t>(__float_as_uint(h)) << 32) | static_cast<uint32_t>(tid);
+    const bool inC = own && h <= a.bound;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, inC);
+    // per warp: the smallest key outside C
+    uint64_t mo = (own && !inC) ? key : ~0ull;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, mo, off);
+        mo = o < mo ? o : mo;
+    }
+    if (own) hpos[tid] = h;
+    if (lane == 0) {
+        wcnt[wid] = __popc(bal);
+        wmin[wid] = mo;
     }
     __syncthreads();
-    // partial ranks: thread t counts key t % L against slice t / L (slices
-    // start on even keys, two keys per 16-byte shared load)
-    const int nq = max(1, min(kRankSplit, nt / L));
-    if (tid < nq * L) {
-        const int i = tid % L, q = tid / L;
-        const int j0 = (q * L / nq) & ~1, j1 = (q + 1 == nq) ? L : ((q + 1) * L / nq) & ~1;
+    // every warp combines the per-warp counts and minima (lane w: warp w's)
+    const int cw = lane < nw ? wcnt[lane] : 0;
+    int incl = cw;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int nC = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const int ci = __shfl_sync(0xFFFFFFFFu, incl - cw, wid) + __popc(bal & ((1u << lane) - 1u));
+    uint64_t mout = lane < nw ? wmin[lane] : ~0ull;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, mout, off);
+        mout = o < mout ? o : mout;
+    }
+    if (inC) keys[ci] = key;
+    __syncthreads();
+    // partial ranks within C: thread t counts key t % nC against slice
+    // t / nC (slices start on even keys, two keys per 16-byte shared load)
+    const int nq = nC > 0 ? max(1, min(kRankSplit, nt / nC)) : 0;
+    if (tid < nq * nC) {
+        const int i = tid % nC, q = tid / nC;
+        const int j0 = (q * nC / nq) & ~1, j1 = (q + 1 == nq) ? nC : ((q + 1) * nC / nq) & ~1;
         const uint64_t k = keys[i];
         int cnt = 0;
         int j = j0;
@@ -140,50 +180,54 @@ __device__ void accept_canvas(const AcceptArgs &a, int b, int step, const float 
             cnt += (kk.x < k ? 1 : 0) + (kk.y < k ? 1 : 0);
         }
         if (j < j1) cnt += (keys[j] < k) ? 1 : 0;
-        prank[q * L + i] = cnt;
+        prank[q * nC + i] = cnt;
     }
     __syncthreads();
-    int rank = 0;
-    if (own) {
-        for (int q = 0; q < nq; ++q) rank += prank[q * L + tid];
-        if (a.checks && (rank < 0 || rank >= L)) {
+    int rank = L;    // outside C and not its smallest key: never accepted
+    if (inC) {
+        rank = 0;
+        for (int q = 0; q < nq; ++q) rank += prank[q * nC + ci];
+        if (a.checks && (rank < 0 || rank >= nC)) {
             report_error(a.ws, DG_ERR_DEVICE, 807);
-            rank = L - 1;
+            rank = nC - 1;
         }
         hsorted[rank] = h;
+    } else if (own && key == mout) {
+        rank = nC;
+        hsorted[nC] = h;
     }
+    const int nS = nC + (mout != ~0ull ? 1 : 0);   // entries of hsorted
     __syncthreads();
     // k*: warp 0 scans the sorted entropies in chunks of 32 (exclusive sums)
     if (wid == 0) {
         double carry = 0.0;
         int kcount = 0;
-        for (int c0 = 0; c0 < L; c0 += 32) {
+        for (int c0 = 0; c0 < nS; c0 += 32) {
             const int j = c0 + lane;
-            const double hv = (j < L) ? static_cast<double>(hsorted[j]) : 0.0;
-            double incl = hv;
+            const double hv = (j < nS) ? static_cast<double>(hsorted[j]) : 0.0;
+            double inc = hv;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const double o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-                if (lane >= off) incl += o;
+                const double o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+                if (lane >= off) inc += o;
             }
-            const double prev = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+            const double prev = __shfl_up_sync(0xFFFFFFFFu, inc, 1);
             const double excl = carry + (lane == 0 ? 0.0 : prev);
-            kcount += __popc(__ballot_sync(0xFFFFFFFFu, j < L && excl <= static_cast<double>(a.bound)));
+            kcount += __popc(__ballot_sync(0xFFFFFFFFu, j < nS && excl <= static_cast<double>(a.bound)));
             const double last = __shfl_sync(0xFFFFFFFFu, excl, 31);
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            carry += __shfl_sync(0xFFFFFFFFu, inc, 31);
             if (last > static_cast<double>(a.bound)) break;   // the sums only grow
         }
-        // fp64 total of the entropies (mean for the stop test): lane l sums
-        // sorted entries l, l + 32, ... in order, then a fixed butterfly (fp64
-        // is slow here: one warp does it)
+        if (lane == 0) s_kstar = max(1, kcount);
+    } else if (wid == 1) {
+        // fp64 total of the entropies (mean for the stop test), beside the
+        // scan: lane l sums positions l, l + 32, ... in order, then a fixed
+        // butterfly (fp64 is slow here: one warp does it)
         double t = 0.0;
-        for (int j = lane; j < L; j += 32) t += static_cast<double>(hsorted[j]);
+        for (int j = lane; j < L; j += 32) t += static_cast<double>(hpos[j]);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-        if (lane == 0) {
-            s_kstar = max(1, kcount);
-            wsum[0] = t;
-        }
+        if (lane == 0) wsum[0] = t;
     }
     __syncthreads();
     const int kstar = s_kstar;
