@@ -105,6 +105,75 @@ def test_accept_renoise_stop_bit_exact(B, L, kind):
     status_ok(ws)
 
 
+def _edge_entropies(kind, L, b):
+    """Entropies around the acceptance's in-bound set {H <= b}: its edges."""
+    f = np.float32
+    bf = f(b)
+    h = np.full(L, f(2.0))
+    if kind == "at_bound":        # H exactly b (inside) and the next float up (outside)
+        h[::3] = bf
+        h[1::3] = np.nextafter(bf, f(1e9))
+        h[5] = f(0.0)
+    elif kind == "one_out_taken":   # all but one inside, summing to 0: the outside key commits too
+        h[:] = f(0.0)
+        h[L // 2] = f(7.5)
+    elif kind == "one_out_not":     # all but one inside, summing past b
+        h[:] = f(0.01)
+        h[L // 3] = f(7.5)
+    elif kind == "ties_out":        # none inside; ties among the smallest outside keys
+        h[:] = f(0.7)
+        h[[9, 4, 30]] = f(0.3)
+    elif kind == "all_inside":
+        h[:] = f(b / L)
+        h[::7] = f(0.0)
+    elif kind == "inside_ties":     # ties inside the set and at its last committed entry
+        h[:] = f(3.0)
+        h[:L // 2] = np.tile(np.array([0.02, 0.0, 0.02, 0.04], np.float32), L)[:L // 2]
+    elif kind == "zero_bound":      # b = 0: only exact zeros are inside
+        h[::4] = f(0.0)
+    else:
+        raise ValueError(kind)
+    return h
+
+
+@pytest.mark.parametrize("kind,L,b", [("at_bound", 256, 0.1), ("one_out_taken", 256, 0.1),
+                                      ("one_out_not", 256, 0.1), ("ties_out", 64, 0.1),
+                                      ("all_inside", 1024, 0.1), ("inside_ties", 100, 0.1),
+                                      ("zero_bound", 256, 0.0), ("at_bound", 33, 0.25)])
+def test_accept_in_bound_set_edges(kind, L, b):
+    """The acceptance orders only the positions within the bound (and the
+    smallest key past it): its membership edge, the outside key that commits
+    or not, ties inside and outside, and b = 0 -- against the oracle's full
+    sort, bit for bit."""
+    rng = np.random.default_rng(abs(hash((kind, L))) % (1 << 32))
+    V, seed, step = 4096, 5, 2
+    H = _edge_entropies(kind, L, b)[None, :]
+    sample = rng.integers(0, V, (1, L)).astype(np.int32)
+    argmax = rng.integers(0, V, (1, L)).astype(np.int32)
+    p = dg.step_params(1, L, 64, V, 0.8, b, 0.005, step=step, seed=seed)
+    bufs = dg.StepBuffers(1, L, DEV)
+    bufs.prev_argmax.copy_(torch.from_numpy(argmax.reshape(-1)))
+    ws = dg.workspace(4096, DEV)
+    dg.accept_renoise(torch.from_numpy(H.reshape(-1)).to(DEV),
+                      torch.from_numpy(sample.reshape(-1)).to(DEV),
+                      torch.from_numpy(argmax.reshape(-1)).to(DEV), p, bufs, ws)
+    torch.cuda.synchronize()
+    r = oracle.accept_renoise(H[0], sample[0], np.zeros(L, np.int32), V, np.float32(b), seed, 0, step)
+    s = oracle.stop(argmax[0], argmax[0], H[0], step)
+    assert int(bufs.n_accepted[0]) == r["n_accepted"]
+    assert np.array_equal(bufs.accepted.cpu().numpy(), r["accepted"])
+    assert np.array_equal(np_i32(bufs.canvas), r["canvas"])
+    assert int(bufs.stop[0]) == s["stop"]
+    assert abs(float(bufs.mean_entropy[0]) - s["mean_entropy"]) <= 1e-6 * max(1, s["mean_entropy"])
+    if kind == "one_out_taken":
+        assert r["n_accepted"] == L
+    if kind == "one_out_not":
+        assert r["accepted"][L // 3] == 0
+    if kind == "ties_out":
+        assert r["n_accepted"] == 1 and r["accepted"][4] == 1
+    status_ok(ws)
+
+
 def test_accept_step0_never_stops():
     L, V = 64, 1024
     p = dg.step_params(1, L, 64, V, 0.8, 0.1, 0.005, step=0, seed=1)
