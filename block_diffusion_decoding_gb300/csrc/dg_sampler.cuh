@@ -394,31 +394,42 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
 #pragma unroll
     for (int j = 0; j < 16; ++j) in |= (w[j] >= wthr ? 1u : 0u) << j;
     if (!live) in = 0;
-    float lz[16];
-    const float2 iv = make_float2(fc.invT, fc.invT);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float2 z = mul2(make_float2(x[2 * q], x[2 * q + 1]), iv);
-        lz[2 * q] = z.x;
-        lz[2 * q + 1] = z.y;
-    }
     // Stage 2: approximate scores lz + G~.  A column can end up as the chunk's
     // exact best only if its approximate score is within twice the estimate's
     // error of the chunk's best approximate score, and above the running best.
+    // Columns stage 1 or 1b ruled out score below lb (they cannot be the
+    // best); a group of four columns (one Philox block) that no lane of the
+    // warp let through is skipped whole.
     float ap[16];
     float amax = -INFINITY;
+    const uint32_t qin = ((in & 0x000Fu) ? 1u : 0u) | ((in & 0x00F0u) ? 2u : 0u) |
+                         ((in & 0x0F00u) ? 4u : 0u) | ((in & 0xF000u) ? 8u : 0u);
+    const uint32_t qany = __reduce_or_sync(0xFFFFFFFFu, qin);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        // u = ((x >> 9) + 1/2) 2^-23 = (1 + (x >> 9) 2^-23) - (1 - 2^-24), exact
-        const float u = __fadd_rn(__uint_as_float(0x3F800000u | (w[j] >> 9)), -0.99999994f);
-        const float om = 1.0f - u;   // exact
-        // -ln u: series near u = 1 (relative error < 3e-9), hardware log2 below
-        const float e1 = (u > 0.99f) ? fmaf(om * om, 0.5f + om * (1.0f / 3.0f), om)
-                                     : -0.69314718f * fast_log2(u);
-        const float g = -0.69314718f * fast_log2(e1);
-        // columns stage 1 or 1b ruled out score below lb: they cannot be the best
-        ap[j] = ((in >> j) & 1u) ? lz[j] + g : -INFINITY;
-        amax = fmaxf(amax, ap[j]);
+    for (int q = 0; q < 4; ++q) {
+        if ((qany >> q) & 1u) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j0 = 4 * q + 2 * h;
+                const float2 z = mul2(make_float2(x[j0], x[j0 + 1]), make_float2(fc.invT, fc.invT));
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int j = j0 + t;
+                    // u = ((x >> 9) + 1/2) 2^-23 = (1 + (x >> 9) 2^-23) - (1 - 2^-24), exact
+                    const float u = __fadd_rn(__uint_as_float(0x3F800000u | (w[j] >> 9)), -0.99999994f);
+                    const float om = 1.0f - u;   // exact
+                    // -ln u: series near u = 1 (relative error < 3e-9), hardware log2 below
+                    const float e1 = (u > 0.99f) ? fmaf(om * om, 0.5f + om * (1.0f / 3.0f), om)
+                                                 : -0.69314718f * fast_log2(u);
+                    const float g = -0.69314718f * fast_log2(e1);
+                    ap[j] = ((in >> j) & 1u) ? (t ? z.y : z.x) + g : -INFINITY;
+                    amax = fmaxf(amax, ap[j]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) ap[4 * q + t] = -INFINITY;
+        }
     }
     // Deferred exact evaluation.  Invariant: the exact best of the columns
     // seen so far is either among those evaluated exactly (gbest, gidx) or is
