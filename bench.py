@@ -316,16 +316,22 @@ def run_reference_moe(args, mcfg):
     return 0
 
 
-def _config_json(cfg, l2, lm_dtype="bf16", self_cond=False):
-    return {"workload": "%s: single denoising step, B=%d L=%d, attention Hq=%d Hkv=%d D=%d "
-                        "P=%d, LM head d=%d V=%d%s%s, T=%.1f b=%.1f" % (
-                            cfg.name, cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V,
-                            " (E4M3 operands, per-row / per-column scales)"
-                            if lm_dtype == "fp8" else "",
-                            " + self-conditioning read-out (bf16 table [V, 32])"
-                            if self_cond else "",
-                            cfg.temperature, cfg.entropy_bound),
-            "global_batch": cfg.B, "seq_len": cfg.L, "parallelism": "replicas", "l2": l2}
+W_LAYOUTS = {0: "row-major [d, V]", 1: "packed [ceil(V/128)][d][128] (dg_pack_lm_weight, at load)"}
+
+
+def _config_json(cfg, l2, lm_dtype="bf16", self_cond=False, w_layout=None):
+    out = {"workload": "%s: single denoising step, B=%d L=%d, attention Hq=%d Hkv=%d D=%d "
+                       "P=%d, LM head d=%d V=%d%s%s, T=%.1f b=%.1f" % (
+                           cfg.name, cfg.B, cfg.L, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.d, cfg.V,
+                           " (E4M3 operands, per-row / per-column scales)"
+                           if lm_dtype == "fp8" else "",
+                           " + self-conditioning read-out (bf16 table [V, 32])"
+                           if self_cond else "",
+                           cfg.temperature, cfg.entropy_bound),
+           "global_batch": cfg.B, "seq_len": cfg.L, "parallelism": "replicas", "l2": l2}
+    if w_layout is not None:
+        out["w_layout"] = W_LAYOUTS[w_layout]
+    return out
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -412,10 +418,15 @@ def run_ours(args, cfg, emit=True):
     aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), dev)
     bufs = dg.StepBuffers(B, L, dev)
     bufs.canvas.copy_(torch.randint(0, V, (M,), device=dev, generator=g, dtype=torch.int32))
-    p0 = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 0,
-                        seed=rank)
     fp8 = args.lm_dtype == "fp8"
     sc = args.self_cond
+    # load-time layout of the bf16 W (not timed): where the LM head runs on
+    # the 2-SM kernels, W is packed (dg_pack_lm_weight: one 16 KB stretch per
+    # 128 columns x 64 hidden dimensions); FP8 reads its own E4M3 copy
+    packed = not fp8 and dg.lm_head_plan(M, d, V)["kind"] >= 2
+    layout = dg.W_PACKED if packed else dg.W_ROWMAJOR
+    p0 = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 0,
+                        seed=rank, w_layout=layout)
     if sc:
         # the self-conditioning table E [V, 32] bf16 (30 meaningful columns,
         # V x 30 = 7.86M parameters at V = 262144) and the read-out [M, 32]
@@ -434,6 +445,9 @@ def run_ours(args, cfg, emit=True):
         sws = dg.workspace(dg.denoise_step_sc_workspace(p0), dev)
     else:
         sws = dg.workspace(dg.denoise_step_workspace(p0), dev)
+    if packed:
+        w = dg.pack_lm_weight(w)
+        torch.cuda.synchronize(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     stream = torch.cuda.current_stream(dev)
 
@@ -461,7 +475,7 @@ def run_ours(args, cfg, emit=True):
 
     def step(k):
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold,
-                           k, seed=rank)
+                           k, seed=rank, w_layout=layout)
         if cws is not None:
             dg.canvas_step(q, kp, vp, kc, vc, attn_out, scale, x, w, p, bufs, cws)
         else:
@@ -602,7 +616,8 @@ def run_ours(args, cfg, emit=True):
         higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="e4m3 LM head (fp32 accumulate), bf16 attention" if fp8 else "bf16",
         data="synthetic", config=_config_json(cfg, l2="flushed (256 MiB write) before every step",
-                                              lm_dtype=args.lm_dtype, self_cond=sc),
+                                              lm_dtype=args.lm_dtype, self_cond=sc,
+                                              w_layout=None if fp8 else layout),
         canvas_tokens_per_s=value * M,
         roofline=roof,
         kernels={lm_plan["kernel"]: {"ms": lm_ms, "GB_per_s": lm_gbs, "TFLOP_per_s": lm_tflops,
@@ -661,8 +676,13 @@ def run_block(args, cfg, emit=True):
         noise = torch.randn(M, d, device=dev, generator=g, dtype=torch.float64) / math.sqrt(d)
         hid[k] = (gk[:, None] * cols + noise).to(bf)
     del cols
+    # W packed for the 2-SM LM-head kernels (load time, not timed); the
+    # row-major copy stays for the oracle sample
+    packed = dg.lm_head_plan(M, d, V)["kind"] >= 2
+    layout = dg.W_PACKED if packed else dg.W_ROWMAJOR
+    wl = dg.pack_lm_weight(w) if packed else w
     p = dg.step_params(B, L, d, V, cfg.t_start, cfg.entropy_bound, cfg.stop_threshold, 0,
-                       seed=rank)
+                       seed=rank, w_layout=layout)
     bp = dg.block_params(N, cfg.t_start, cfg.t_end, M * d)
     bufs = dg.BlockBuffers(B, L, N, dev)
     bws = dg.workspace(dg.generate_block_workspace(p, bp), dev)
@@ -683,7 +703,7 @@ def run_block(args, cfg, emit=True):
         return [a.elapsed_time(b_) for a, b_ in evs]
 
     def block():
-        dg.generate_block(hid, w, p, bp, bufs, bws)
+        dg.generate_block(hid, wl, p, bp, bufs, bws)
 
     with ClockSampler(local) as clk:
         clk.wait_first()
@@ -709,13 +729,13 @@ def run_block(args, cfg, emit=True):
     flat = torch.zeros(M, d, device=dev, dtype=bf)
     fbp = dg.block_params(N, cfg.t_start, cfg.t_end, 0)
     fbufs = dg.BlockBuffers(B, L, N, dev)
-    dg.generate_block(flat, w, p, fbp, fbufs, bws)
+    dg.generate_block(flat, wl, p, fbp, fbufs, bws)
     torch.cuda.synchronize(dev)
     flat_ok = (int(fbufs.steps_taken.min().item()) == N and
                bool((fbufs.n_accepted_hist == 1).all().item()))
 
     # the LM-head kernel alone on the first step's hidden states (roofline)
-    lm_ms = statistics.mean(timed(lambda: dg.lm_head_fold(hid[0], w, p, sws), args.steps))
+    lm_ms = statistics.mean(timed(lambda: dg.lm_head_fold(hid[0], wl, p, sws), args.steps))
     lm_bytes = d * V * 2 + M * d * 2
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
     lm_plan = dg.lm_head_plan(M, d, V)
@@ -767,7 +787,7 @@ def run_block(args, cfg, emit=True):
                                                         cfg.t_end, N, cfg.entropy_bound,
                                                         cfg.stop_threshold),
                 "global_batch": B, "seq_len": L, "parallelism": "replicas",
-                "l2": "flushed (256 MiB write) before every block"},
+                "l2": "flushed (256 MiB write) before every block", "w_layout": W_LAYOUTS[layout]},
         block_ms=block_ms, steps_to_stop=steps,
         commits_per_step=float(hist.mean().item()),
         canvas_tokens_per_s=world * M / (block_ms * 1e-3),
@@ -1074,7 +1094,13 @@ def run_kernel_only(args, cfg):
         for r0 in range(0, d, 256):
             r1 = min(d, r0 + 256)
             w[r0:r1] = (torch.randn(r1 - r0, V, device=dev, generator=g) * cfg.w_std).to(bf)
-        p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 1)
+        # W as the benchmark holds it: packed where the 2-SM kernels run
+        layout = (dg.W_PACKED if args.lm_dtype != "fp8" and dg.lm_head_plan(M, d, V)["kind"] >= 2
+                  else dg.W_ROWMAJOR)
+        p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold, 1,
+                           w_layout=layout)
+        if layout == dg.W_PACKED:
+            w = dg.pack_lm_weight(w)
         if args.self_cond:
             sc_table = (torch.randn(V, 32, device=dev, generator=g) / math.sqrt(d)).to(bf)
             ws = dg.workspace(dg.denoise_step_sc_workspace(p), dev)

@@ -39,7 +39,8 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_set_device_checks", "dg_device
             "dg_wait_timeout_probe", "dg_denoise_step_sc_workspace", "dg_denoise_step_sc",
             "dg_lm_head_fold_sc", "dg_moe_ffn_workspace", "dg_moe_ffn",
             "dg_generate_block_fn", "dg_hidden_from_steps", "dg_hidden_embed_add",
-            "dg_canvas_step_workspace", "dg_canvas_step"]
+            "dg_canvas_step_workspace", "dg_canvas_step",
+            "dg_lm_weight_packed_bytes", "dg_pack_lm_weight"]
 
 
 class DgError(RuntimeError):
@@ -53,7 +54,10 @@ class StepParams(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int), ("V", ctypes.c_int),
                 ("temperature", ctypes.c_double), ("entropy_bound", ctypes.c_float),
                 ("stop_threshold", ctypes.c_float), ("step", ctypes.c_int),
-                ("seed", ctypes.c_uint64)]
+                ("seed", ctypes.c_uint64), ("w_layout", ctypes.c_int)]
+
+W_ROWMAJOR = 0   # the LM-head weight as [d, V]
+W_PACKED = 1     # as pack_lm_weight writes it
 
 
 class StepIO(ctypes.Structure):
@@ -119,6 +123,8 @@ def _lib():
             "dg_logf_eval": ([vp, vp, i32, vp], i32),
             "dg_quantize_rows_e4m3": ([vp, ctypes.c_int64, i32, vp, vp, vp], i32),
             "dg_quantize_weight_e4m3": ([vp, i32, i32, vp, vp, vp], i32),
+            "dg_lm_weight_packed_bytes": ([i32, i32], sz),
+            "dg_pack_lm_weight": ([vp, i32, i32, vp, vp], i32),
             "dg_denoise_step_fp8_workspace": ([sp], sz),
             "dg_denoise_step_fp8": ([vp, vp, vp, sp, si, vp, sz, vp], i32),
             "dg_lm_head_fold_fp8": ([vp, vp, vp, sp, vp, sz, vp], i32),
@@ -199,8 +205,8 @@ def encoder_append(q, k_cache, v_cache, P, k_new, v_new, out, scale, workspace, 
 
 # ---------------------------------------------------------------- step
 def step_params(B, L, d, V, temperature, entropy_bound=0.1, stop_threshold=0.005, step=0,
-                seed=0) -> StepParams:
-    return StepParams(B, L, d, V, temperature, entropy_bound, stop_threshold, step, seed)
+                seed=0, w_layout=W_ROWMAJOR) -> StepParams:
+    return StepParams(B, L, d, V, temperature, entropy_bound, stop_threshold, step, seed, w_layout)
 
 
 class StepBuffers:
@@ -336,6 +342,22 @@ def quantize_rows_e4m3(x, codes, scale, stream=None):
     rows, cols = x.shape
     rc = _lib().dg_quantize_rows_e4m3(_p(x), rows, cols, _p(codes), _p(scale), _stream(stream))
     _check(rc, "dg_quantize_rows_e4m3")
+
+
+def lm_weight_packed_bytes(d, V) -> int:
+    return int(_lib().dg_lm_weight_packed_bytes(d, V))
+
+
+def pack_lm_weight(w, out=None, stream=None):
+    """W [d, V] bf16 -> the packed LM-head weight (a 1-D bf16 tensor of
+    lm_weight_packed_bytes(d, V) bytes), for steps with w_layout=W_PACKED."""
+    import torch
+    d, V = w.shape
+    if out is None:
+        out = torch.empty(lm_weight_packed_bytes(d, V) // 2, dtype=w.dtype, device=w.device)
+    rc = _lib().dg_pack_lm_weight(_p(w), d, V, _p(out), _stream(stream))
+    _check(rc, "dg_pack_lm_weight")
+    return out
 
 
 def quantize_weight_e4m3(w, w8t, scale, stream=None):

@@ -233,6 +233,7 @@ int check_step_params(const dg_step_params *p)
     if (!(p->entropy_bound >= 0.f) || !std::isfinite(p->entropy_bound)) return DG_ERR_INVALID_ARG;
     if (!std::isfinite(p->stop_threshold)) return DG_ERR_INVALID_ARG;
     if (p->step < 0) return DG_ERR_INVALID_ARG;
+    if (p->w_layout != DG_W_ROWMAJOR && p->w_layout != DG_W_PACKED) return DG_ERR_INVALID_ARG;
     if (p->L > kMaxCanvas) return DG_ERR_UNSUPPORTED;
     if (p->V % 8 != 0 || p->V < 64) return DG_ERR_UNSUPPORTED;
     if (static_cast<long long>(p->B) * p->L > (1LL << 30)) return DG_ERR_UNSUPPORTED;
@@ -354,7 +355,16 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
             int rc = make_map_bf16(&mx, hidden, rank, dims, strides, box);
             if (rc != DG_OK) return rc;
         }
-        {
+        const bool packed = p->w_layout == DG_W_PACKED;
+        if (packed) {
+            // [ceil(V / 128)][d][128]: 64 x 64 boxes inside one 128-column tile
+            const uint64_t dims[3] = {128, static_cast<uint64_t>(p->d),
+                                      static_cast<uint64_t>((p->V + 127) / 128)};
+            const uint64_t strides[2] = {256, static_cast<uint64_t>(p->d) * 256};
+            const uint32_t box[3] = {64, 64, 1};
+            int rc = make_map_bf16(&mw, w, 3, dims, strides, box);
+            if (rc != DG_OK) return rc;
+        } else {
             const uint64_t dims[2] = {static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d)};
             const uint64_t strides[1] = {static_cast<uint64_t>(p->V) * 2};
             const uint32_t box[2] = {64, 64};
@@ -362,6 +372,7 @@ int enqueue_step(const uint16_t *hidden, int64_t hidden_stride, int x_steps, con
             if (rc != DG_OK) return rc;
         }
         LmHeadArgs a{};
+        a.w_packed = packed ? 1 : 0;
         a.M = M;
         a.d = p->d;
         a.V = p->V;
@@ -757,7 +768,8 @@ int sc_step(const uint16_t *hidden, const uint16_t *w, const uint16_t *sc_table,
     DeviceInfo *di = nullptr;
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
-    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, false, true);
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, false, true, -1,
+                                     p->w_layout == DG_W_PACKED);
     StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     ScOperands sco{sc_table, reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + off_sc),
                    sc_out};
@@ -954,7 +966,8 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     DeviceInfo *di = nullptr;
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
-    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, false, false, -1,
+                                     p->w_layout == DG_W_PACKED);
     StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     const StepSource src = step_source(p);
     const AcceptArgs acc = accept_args(p, io);
@@ -975,7 +988,8 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
     DeviceInfo *di = nullptr;
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
-    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, false, false, -1,
+                                     p->w_layout == DG_W_PACKED);
     StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
     const StepSource src = step_source(p);
     AcceptArgs acc{};
@@ -1008,6 +1022,30 @@ int dg_quantize_weight_e4m3(const uint16_t *w, int d, int V, uint8_t *w8t, float
                                                                                  w8t);
     DG_LAUNCHED();
     scale_from_amax_kernel<<<(V + 255) / 256, 256, 0, st>>>(scale, V);
+    DG_LAUNCHED();
+    DG_CUDA_TRY(cudaGetLastError());
+    return DG_OK;
+}
+
+size_t dg_lm_weight_packed_bytes(int d, int V)
+{
+    if (d < 1 || V < 1) return 0;
+    return static_cast<size_t>((V + 127) / 128) * static_cast<size_t>(d) * 128 * 2;
+}
+
+int dg_pack_lm_weight(const uint16_t *w, int d, int V, uint16_t *w_packed, void *stream)
+{
+    if (!w || !w_packed) return DG_ERR_INVALID_ARG;
+    if (d % 64 != 0 || d < 64 || d > 16384 || V % 8 != 0 || V < 64) return DG_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(w_packed)) return DG_ERR_ALIGNMENT;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(w);
+    const uintptr_t a1 = a0 + static_cast<size_t>(d) * V * 2;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(w_packed);
+    const uintptr_t b1 = b0 + dg_lm_weight_packed_bytes(d, V);
+    if (a0 < b1 && b0 < a1) return DG_ERR_INVALID_ARG;
+    const int64_t chunks = static_cast<int64_t>((V + 127) / 128) * d * 16;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((chunks + 255) / 256, 8192));
+    pack_lm_weight_kernel<<<grid, 256, 0, as_stream(stream)>>>(w, d, V, w_packed);
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     return DG_OK;
@@ -1145,8 +1183,10 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
                   scale, 0, aws, workspace_bytes - step_bytes, fs->side, reserve);
     if (rc == DG_OK) {
         const int M = p->B * p->L;
-        LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve);
-        if (reserve > 0 && plan.kind != kLmSingle && std::getenv("DG_LM_KERNEL") == nullptr) {
+        const bool packed = p->w_layout == DG_W_PACKED;
+        LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve, false, false, -1, packed);
+        if (reserve > 0 && !packed && plan.kind != kLmSingle &&
+            std::getenv("DG_LM_KERNEL") == nullptr) {
             // one tile per CTA on the SMs left: the single-CTA kernel (its 16
             // epilogue warps fold a 256-row tile; measured faster than the
             // 2-SM kernel's 8 at one tile per CTA)
@@ -1391,7 +1431,8 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
     DeviceInfo *di = nullptr;
     if ((rc = current_device_info(&di)) != DG_OK) return rc;
     const int M = p->B * p->L;
-    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms);
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms, false, false, -1,
+                                     p->w_layout == DG_W_PACKED);
     size_t off_ctl, off_scr;
     block_ws_layout(p, slot_bound(M, p->V), &off_ctl, &off_scr);
     uint8_t *base = static_cast<uint8_t *>(workspace);

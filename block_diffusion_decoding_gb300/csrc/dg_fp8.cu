@@ -158,4 +158,24 @@ __global__ void __launch_bounds__(256) quantize_cols_e4m3_kernel(const uint16_t 
     }
 }
 
+// W [d, V] -> the packed LM-head weight [ceil(V / 128)][d][128], zero past
+// V: one thread per 16 bytes (8 values; V % 8 == 0, so a chunk is all inside
+// or all past V); the 16 chunks of a packed row read one 256-byte stretch of
+// a row of W.
+__global__ void __launch_bounds__(256) pack_lm_weight_kernel(const uint16_t *__restrict__ w, int d,
+                                                             int V, uint16_t *__restrict__ wp)
+{
+    const int64_t n = static_cast<int64_t>((V + 127) / 128) * d * 16;
+    for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * 256) {
+        const int c8 = static_cast<int>(i & 15);
+        const int64_t row = i >> 4;                  // tile * d + k
+        const int t = static_cast<int>(row / d), k = static_cast<int>(row % d);
+        const int v = t * 128 + c8 * 8;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (v < V) val = *reinterpret_cast<const uint4 *>(w + static_cast<size_t>(k) * V + v);
+        reinterpret_cast<uint4 *>(wp)[i] = val;
+    }
+}
+
 }  // namespace dg

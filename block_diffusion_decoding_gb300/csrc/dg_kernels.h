@@ -95,6 +95,7 @@ struct LmHeadArgs {
     // one launch ([M] order-preserving keys, 0 = none; all 0 between
     // launches); null: not shared
     uint32_t *rowkey;
+    int w_packed;       // W as [ceil(V / 128)][d][128] (2-SM kernels only)
     // self-conditioning read-out (lm_head_duo_sc_kernel only): table E
     // [V, kScDim] bf16 and the per-(row, unit) parts [M][units][kScDim] fp32
     const uint16_t *sc_table;
@@ -178,6 +179,8 @@ __global__ void quantize_rows_e4m3_kernel(const uint16_t *__restrict__ x, int64_
 constexpr int kQuantVecs = 16;   // 16-byte vectors per thread of the vector row kernel
 __global__ void quantize_rows_e4m3_vec_kernel(const uint16_t *__restrict__ x, int cols,
                                               uint8_t *__restrict__ q, float *__restrict__ scale);
+__global__ void pack_lm_weight_kernel(const uint16_t *__restrict__ w, int d, int V,
+                                      uint16_t *__restrict__ wp);
 __global__ void column_amax_kernel(const uint16_t *__restrict__ w, int d, int V,
                                    float *__restrict__ amax);
 __global__ void quantize_cols_e4m3_kernel(const uint16_t *__restrict__ w, int d, int V,

@@ -213,6 +213,15 @@ DG_DEVICE void lm_head_duo_body(const CUtensorMap &map_x, const CUtensorMap &map
                         for (int j = 0; j < span; ++j)
                             tma_load_2d_pair(sb + j * w_half_bytes, &map_w, fb, kb * 128,
                                              n * a.BN + r * (bn / 2) + j * (a.BN / 2), pol_w);
+                    } else if (a.w_packed) {
+                        // packed W: the box of 64 columns x 64 rows starting at
+                        // column c0 (a multiple of 64) lies in 128-column tile
+                        // c0 / 128, at column c0 % 128 of its rows
+                        for (int j = 0; j < bn / 128; ++j) {
+                            const int c0 = n * a.BN + r * (bn / 2) + j * 64;
+                            tma_load_3d_pair(sb + j * kLmBBoxBytes, &map_w, fb, c0 & 127,
+                                             kb * kLmBK, c0 >> 7, pol_w);
+                        }
                     } else {
                         for (int j = 0; j < bn / 128; ++j)
                             tma_load_2d_pair(sb + j * kLmBBoxBytes, &map_w, fb,

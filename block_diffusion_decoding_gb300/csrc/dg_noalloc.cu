@@ -105,8 +105,10 @@ typedef CUresult (*NaEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, v
                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// A 2-D bf16 map [outer][inner], or with planes > 0 a 3-D one
+// [planes][outer][inner] (the packed LM-head weight), 128-byte swizzle.
 int na_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-           uint32_t box_outer)
+           uint32_t box_outer, uint64_t planes = 0)
 {
     static NaEncodeFn fn = nullptr;
     static std::once_flag once;
@@ -121,11 +123,11 @@ int na_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, u
             (void)cudaGetLastError();
     });
     if (fn == nullptr) return DG_ERR_CUDA;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t elem[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+    const cuuint64_t dims[3] = {inner, outer, planes};
+    const cuuint64_t strides[2] = {inner * 2, inner * 2 * outer};
+    const cuuint32_t box[3] = {box_inner, box_outer, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, planes > 0 ? 3 : 2, const_cast<void *>(base), dims,
                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
@@ -143,6 +145,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     if (!(p->temperature > 0.0) || !std::isfinite(p->temperature)) return DG_ERR_INVALID_ARG;
     if (!(p->entropy_bound >= 0.f) || !std::isfinite(p->entropy_bound)) return DG_ERR_INVALID_ARG;
     if (!std::isfinite(p->stop_threshold) || p->step < 0) return DG_ERR_INVALID_ARG;
+    if (p->w_layout != DG_W_ROWMAJOR && p->w_layout != DG_W_PACKED) return DG_ERR_INVALID_ARG;
     if (!io->canvas || !io->prev_argmax || !io->argmax || !io->sample || !io->entropy ||
         !io->accepted || !io->n_accepted || !io->mean_entropy || !io->stop)
         return DG_ERR_INVALID_ARG;
@@ -157,7 +160,8 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
 
     // ---- kernel and tile plan: the same choice as dg_denoise_step
     const int M = p->B * p->L;
-    const LmPlan plan = plan_lm_head(M, p->d, p->V, st->sms);
+    const bool packed = p->w_layout == DG_W_PACKED;
+    const LmPlan plan = plan_lm_head(M, p->d, p->V, st->sms, false, false, -1, packed);
     const int BN = plan.BN, ntn = plan.ntn, total = plan.total;
 
     // ---- scratch layout (as a workspace): header | partials | counters | row keys
@@ -185,8 +189,12 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     if ((rc = na_map(&mx, hidden, static_cast<uint64_t>(p->d), static_cast<uint64_t>(M), 64,
                      plan.cluster() ? 128u : 256u)) != DG_OK)
         return rc;
-    if ((rc = na_map(&mw, w, static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d), 64, 64)) != DG_OK)
-        return rc;
+    if (packed)
+        rc = na_map(&mw, w, 128, static_cast<uint64_t>(p->d), 64, 64,
+                    static_cast<uint64_t>((p->V + 127) / 128));
+    else
+        rc = na_map(&mw, w, static_cast<uint64_t>(p->V), static_cast<uint64_t>(p->d), 64, 64);
+    if (rc != DG_OK) return rc;
 
     StepSource src{};
     src.ctl = nullptr;
@@ -195,6 +203,7 @@ extern "C" int dg_denoise_step_noalloc(const uint16_t *hidden, const uint16_t *w
     src.step = p->step;
 
     LmHeadArgs a{};
+    a.w_packed = packed ? 1 : 0;
     a.M = M;
     a.d = p->d;
     a.V = p->V;

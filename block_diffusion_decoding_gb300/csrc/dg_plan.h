@@ -47,8 +47,9 @@ struct LmPlan {
 // fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
 // have the 2-SM UMMA kernel only.
 // only_kind >= 0 restricts the choice to that kernel (as DG_LM_KERNEL does).
+// A packed weight (dg_pack_lm_weight) is read by the 2-SM kernels only.
 inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool sc = false,
-                           int only_kind = -1)
+                           int only_kind = -1, bool packed = false)
 {
     LmPlan best{};
     best.M = M;
@@ -64,15 +65,16 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool 
                      : std::strcmp(env_k, "duo") == 0    ? kLmDuo
                      : std::strcmp(env_k, "fused") == 0  ? kLmDuoFused
                                                          : -1;
-    // a forced kernel FP8 operands or the self-conditioning read-out do not
-    // have is ignored
+    // a forced kernel FP8 operands, the self-conditioning read-out or a
+    // packed weight do not have is ignored
+    const bool duo_only = fp8 || sc || packed;
     const int only_req = only_kind >= 0 ? only_kind : only_env;
-    const int only = (fp8 || sc) && only_req != kLmDuo && only_req != kLmDuoFused ? -1 : only_req;
+    const int only = duo_only && only_req != kLmDuo && only_req != kLmDuoFused ? -1 : only_req;
     long best_cost = -1;
     auto consider = [&](int kind, int bn) {
         if (forced_bn && bn != forced_bn) return;
         if (only >= 0 && kind != only) return;
-        if ((fp8 || sc) && kind != kLmDuo && kind != kLmDuoFused) return;
+        if (duo_only && kind != kLmDuo && kind != kLmDuoFused) return;
         const bool pair = kind != kLmSingle;
         const int ntn = (V + bn - 1) / bn;
         const int total = ntn * best.mblocks;

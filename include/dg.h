@@ -159,10 +159,15 @@ int dg_encoder_append(const uint16_t *q, uint16_t *k_cache, uint16_t *v_cache, i
 /*   of counter (0, r, step, 1).                                              */
 /*   stop[b] = step >= 1 && argmax == prev_argmax over the canvas &&          */
 /*             mean entropy < stop_threshold; then prev_argmax <- argmax.     */
-/* Layouts: hidden [B*L, d] bf16; w [d, V] bf16 (vocabulary contiguous).      */
+/* Layouts: hidden [B*L, d] bf16; w [d, V] bf16 (vocabulary contiguous), or */
+/* with w_layout = DG_W_PACKED the same weight as dg_pack_lm_weight writes   */
+/* it (then only the 2-SM LM-head kernels run: w is read as one 16 KB        */
+/* stretch per 128 columns and 64 hidden dimensions).                        */
 /* Supported: d % 64 == 0, 64 <= d <= 16384; V % 8 == 0, 64 <= V < 2^31;      */
 /* 1 <= L <= 1024; B >= 1.                                                    */
 /* ------------------------------------------------------------------------ */
+#define DG_W_ROWMAJOR 0     /* w [d, V]                                        */
+#define DG_W_PACKED 1       /* w as dg_pack_lm_weight writes it                */
 typedef struct dg_step_params {
     int B;                  /* canvases in the batch                          */
     int L;                  /* canvas length (256)                            */
@@ -173,7 +178,22 @@ typedef struct dg_step_params {
     float stop_threshold;   /* mean-entropy stop threshold (0.005)            */
     int step;               /* step index k (Philox counter; k >= 1 arms stop)*/
     uint64_t seed;          /* Philox key                                     */
+    int w_layout;           /* DG_W_ROWMAJOR (0) or DG_W_PACKED               */
 } dg_step_params;
+
+/* The LM-head weight in the layout the 2-SM kernels stream fastest: the      */
+/* columns in tiles of 128, each tile's d rows of 128 values contiguous:      */
+/*   w_packed[t][k][c] = w[k][128 t + c]   (c < 128, t < ceil(V / 128)),      */
+/* zero where 128 t + c >= V.  A tile of 128 columns by 64 hidden dimensions  */
+/* is then one contiguous 16 KB stretch of memory instead of 64 rows of 256   */
+/* bytes a row of w apart.  w [d, V] bf16 (device), w_packed of               */
+/* dg_lm_weight_packed_bytes(d, V) bytes (device, caller-owned, not          */
+/* overlapping w); one kernel launch on `stream`.  Returns DG_ERR_INVALID_ARG */
+/* for null pointers or d, V outside the step's supported range, else        */
+/* DG_ERR_CUDA on a launch failure.  A layout choice only: the step's         */
+/* results are the same bit for bit with either layout.                       */
+size_t dg_lm_weight_packed_bytes(int d, int V);
+int dg_pack_lm_weight(const uint16_t *w, int d, int V, uint16_t *w_packed, void *stream);
 
 typedef struct dg_step_io {
     int32_t *canvas;        /* [B*L] in/out: current canvas tokens            */

@@ -41,9 +41,10 @@ def test_status_strings(lib):
 
 
 def test_struct_layouts_match_header(lib):
-    # int B, L, d, V; double T; float b, thr; int step; (pad) uint64 seed
-    assert ctypes.sizeof(dg.StepParams) == 48
+    # int B, L, d, V; double T; float b, thr; int step; (pad) uint64 seed; int w_layout (pad)
+    assert ctypes.sizeof(dg.StepParams) == 56
     assert dg.StepParams.seed.offset == 40
+    assert dg.StepParams.w_layout.offset == 48
     assert ctypes.sizeof(dg.StepIO) == 9 * 8
     assert ctypes.sizeof(dg.BlockParams) == 32
     assert ctypes.sizeof(dg.BlockIO) == 5 * 8
@@ -170,3 +171,22 @@ def test_moe_rejects_bad_arguments_before_launch(lib):
     assert rc == 2
     rc = lib.dg_moe_ffn(*([None] * 8), ctypes.byref(p), None, 0, None)
     assert rc == 1
+
+
+def test_packed_weight_size_and_argument_checks(lib):
+    """dg_pack_lm_weight: [ceil(V / 128)][d][128] bf16; the argument checks
+    answer before any device work."""
+    assert lib.dg_lm_weight_packed_bytes(2816, 262144) == 2048 * 2816 * 128 * 2
+    assert lib.dg_lm_weight_packed_bytes(64, 1000) == 8 * 64 * 128 * 2
+    assert lib.dg_lm_weight_packed_bytes(0, 1000) == 0
+    a, b = 1 << 20, 1 << 40
+    assert lib.dg_pack_lm_weight(None, 64, 1024, _vp(b), None) == 1
+    assert lib.dg_pack_lm_weight(_vp(a), 64, 1024, None, None) == 1
+    assert lib.dg_pack_lm_weight(_vp(a), 100, 1024, _vp(b), None) == 1    # d % 64
+    assert lib.dg_pack_lm_weight(_vp(a), 64, 1001, _vp(b), None) == 1     # V % 8
+    assert lib.dg_pack_lm_weight(_vp(a + 8), 64, 1024, _vp(b), None) == 3  # alignment
+    # the packed copy may not overlap the weight
+    assert lib.dg_pack_lm_weight(_vp(a), 64, 1024, _vp(a + 4096), None) == 1
+    # a step's layout is 0 (row-major) or 1 (packed)
+    assert dg.denoise_step_workspace(dg.step_params(1, 256, 1024, 16384, 0.8, w_layout=1)) > 0
+    assert dg.denoise_step_workspace(dg.step_params(1, 256, 1024, 16384, 0.8, w_layout=2)) == 0
