@@ -135,9 +135,12 @@ constexpr int kDuoStages = 6;
 // (CG = 2) suffice and leave the producer and MMA warps more issue slots.
 // With several row blocks the W tiles come from L2, the tiles arrive at the
 // MMA rate and the fold's latency shows: 16 warps (CG = 4).  FP8 tiles carry
-// half the bytes and take 16 too.
+// half the bytes and take the UMMA issue as their limit: 12 warps (CG = 3)
+// fold a tile well inside the MMA's time for it and leave the MMA warp more
+// issue slots than 16 do (measured: 8 warps fold too slowly, 16 slow the MMA).
 constexpr int kDuoCGNarrow = 2;
 constexpr int kDuoCGWide = 4;
+constexpr int kDuoCGFp8 = 3;
 template <int kCG>
 struct DuoEpilogue {
     static constexpr int CG = kCG;

@@ -430,11 +430,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGNa
     lm_head_duo_body<false, kDuoCGNarrow, true>(map_x, map_w, a, &map_e);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGWide>::Threads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(DuoEpilogue<kDuoCGFp8>::Threads, 1)
     lm_head_duo_fp8_kernel(const __grid_constant__ CUtensorMap map_x,
                            const __grid_constant__ CUtensorMap map_w, LmHeadArgs a)
 {
-    lm_head_duo_body<true, kDuoCGWide>(map_x, map_w, a);
+    lm_head_duo_body<true, kDuoCGFp8>(map_x, map_w, a);
 }
 
 }  // namespace dg

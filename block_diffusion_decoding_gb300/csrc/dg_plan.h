@@ -34,7 +34,7 @@ struct LmPlan {
                       // slots, one partial state per (row, unit)
     int grid;         // CTAs launched
     int sms;          // SMs of the device the plan was made for
-    int epi_warps;    // epilogue warps of the 2-SM kernel (8 or 16; 0 otherwise)
+    int epi_warps;    // epilogue warps of the 2-SM kernel (8 or 16, FP8 12; 0 otherwise)
     bool sc;          // the self-conditioning instance (lm_head_duo_sc_kernel)
     int part_slots() const { return units; }
     bool cluster() const { return kind != kLmSingle; }
@@ -43,9 +43,9 @@ struct LmPlan {
 
 // Choose the kernel and tile width: fewest tile columns per SM on the busiest
 // CTA, plus a per-tile overhead; the 2-SM kernel runs 8 epilogue warps on a
-// single 256-row block of bf16 operands, else 16.  DG_LM_KERNEL=single|duo|
-// fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8 operands
-// have the 2-SM UMMA kernel only.
+// single 256-row block of bf16 operands, else 16 (FP8: 12).  DG_LM_KERNEL=
+// single|duo|fused, DG_LM_BN and DG_LM_EPI=8|16 (bf16) force a choice.  FP8
+// operands have the 2-SM UMMA kernel only.
 // only_kind >= 0 restricts the choice to that kernel (as DG_LM_KERNEL does).
 // A packed weight (dg_pack_lm_weight) is read by the 2-SM kernels only.
 inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool sc = false,
@@ -111,7 +111,7 @@ inline LmPlan plan_lm_head(int M, int d, int V, int sms, bool fp8 = false, bool 
     if (best.duo()) {
         const char *env_e = std::getenv("DG_LM_EPI");
         const int forced_e = env_e ? std::atoi(env_e) : 0;
-        best.epi_warps = fp8 ? 4 * kDuoCGWide
+        best.epi_warps = fp8 ? 4 * kDuoCGFp8
                          : sc ? 4 * kDuoCGNarrow
                          : forced_e == 8 || forced_e == 16 ? forced_e
                          : best.mblocks == 1             ? 4 * kDuoCGNarrow
@@ -169,9 +169,10 @@ inline cudaError_t launch_lm_head(const LmPlan &plan, const CUtensorMap &mx, con
                 : plan.kind == kLmSingle ? lm_head_kernel
                 : wide                   ? lm_head_duo_wide_kernel   // kLmDuo, kLmDuoFused
                                          : lm_head_duo_kernel;
-    const int threads = !plan.duo() ? kLmThreads
-                        : wide      ? DuoEpilogue<kDuoCGWide>::Threads
-                                    : DuoEpilogue<kDuoCGNarrow>::Threads;
+    const int threads = fp8          ? DuoEpilogue<kDuoCGFp8>::Threads
+                        : !plan.duo() ? kLmThreads
+                        : wide        ? DuoEpilogue<kDuoCGWide>::Threads
+                                      : DuoEpilogue<kDuoCGNarrow>::Threads;
     return launch_kernel(kern, dim3(plan.grid), dim3(threads), smem, st, pdl, mx, mw, a);
 }
 

@@ -80,7 +80,7 @@ def check_step_against_oracle(bufs, ref, B, L, exact_tokens):
 
 def force_lm_kernel(monkeypatch, spec):
     """Force the LM-head choice: None = the planner's; "kind" or "kind/epi"
-    (kind single | pair | duo | fused; epi 8 | 16 epilogue warps of the
+    (kind single | duo | fused; epi 8 | 16 epilogue warps of the
     2-SM kernel)."""
     monkeypatch.delenv("DG_LM_KERNEL", raising=False)
     monkeypatch.delenv("DG_LM_EPI", raising=False)
