@@ -335,6 +335,14 @@ def _config_json(cfg, l2, lm_dtype="bf16", self_cond=False, w_layout=None):
 
 
 # ----------------------------------------------------------------------------- our arm
+def _w_columns(w, packed, d, ncols):
+    """The first ncols columns of the LM-head weight as [d, ncols] (row-major),
+    from W [d, V] or from its packed form [V/128][d][128] (ncols % 128 == 0)."""
+    if not packed:
+        return w[:, :ncols].contiguous()
+    return w.view(-1, d, 128)[:ncols // 128].permute(1, 0, 2).reshape(d, ncols)
+
+
 def _traffic_record(kernel_sources, kernel, shape):
     """Per-launch DRAM bytes of the LM-head kernel from its committed ncu summary
     (profiles/<kernel>_step_full.md), valid only while the kernel sources are
@@ -573,7 +581,8 @@ def run_ours(args, cfg, emit=True):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = {"x": x.view(torch.int16).cpu().numpy().view(np.uint16),
-                "w": w[:, :16384].contiguous().view(torch.int16).cpu().numpy().view(np.uint16),
+                "w": _w_columns(w, packed, d, 16384).view(torch.int16).cpu().numpy()
+                     .view(np.uint16),
                 "q": q.view(torch.int16).cpu().numpy().view(np.uint16),
                 "kp": kp.view(torch.int16).cpu().numpy().view(np.uint16),
                 "vp": vp.view(torch.int16).cpu().numpy().view(np.uint16),

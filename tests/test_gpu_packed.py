@@ -189,3 +189,30 @@ def test_noalloc_step_packed_equals_rowmajor(monkeypatch):
         torch.cuda.synchronize()
         res.append(bufs)
     _same_outputs(res[1], res[0])
+
+
+@pytest.mark.parametrize("B,L,d,V", [(1, 256, 256, 8200), (2, 130, 128, 4096)])
+def test_self_conditioning_step_packed_equals_rowmajor(B, L, d, V):
+    """The self-conditioning step (its own 2-SM instance, which also stages
+    the table rows of each tile) on the packed weight: the same step outputs
+    and the same read-out, bit for bit."""
+    cfg = dg_synth.StepConfig("packed_sc", B=B, L=L, d=d, V=V, w_std=0.05, seed=40 + B)
+    x, w = to_dev(dg_synth.lm_hidden(cfg)), to_dev(dg_synth.lm_weight(cfg))
+    wp = dg.pack_lm_weight(w)
+    g = torch.Generator(device=DEV).manual_seed(V)
+    table = (torch.randn(V, dg.SC_DIM, device=DEV, generator=g) / math.sqrt(d)).to(torch.bfloat16)
+    canvas0 = torch.from_numpy(np.random.default_rng(9).integers(0, V, B * L).astype(np.int32))
+    res = []
+    for layout, ww in ((dg.W_ROWMAJOR, w), (dg.W_PACKED, wp)):
+        p = dg.step_params(B, L, d, V, 0.75, 0.1, 0.005, step=2, seed=5, w_layout=layout)
+        ws = dg.workspace(dg.denoise_step_sc_workspace(p), DEV)
+        bufs = dg.StepBuffers(B, L, DEV)
+        bufs.canvas.copy_(canvas0)
+        sc = torch.full((B * L, dg.SC_DIM), float("nan"), device=DEV)
+        dg.denoise_step_sc(x, ww, table, p, bufs, sc, ws)
+        torch.cuda.synchronize()
+        status_ok(ws)
+        res.append((bufs, sc))
+    _same_outputs(res[1][0], res[0][0])
+    assert torch.equal(res[0][1], res[1][1])
+    assert bool(torch.isfinite(res[1][1]).all())
