@@ -352,6 +352,8 @@ def pack_lm_weight(w, out=None, stream=None):
     """W [d, V] bf16 -> the packed LM-head weight (a 1-D bf16 tensor of
     lm_weight_packed_bytes(d, V) bytes), for steps with w_layout=W_PACKED."""
     import torch
+    if w.dim() != 2 or w.dtype != torch.bfloat16 or not w.is_contiguous():
+        raise ValueError("pack_lm_weight: w must be a contiguous bf16 [d, V] tensor")
     d, V = w.shape
     if out is None:
         out = torch.empty(lm_weight_packed_bytes(d, V) // 2, dtype=w.dtype, device=w.device)

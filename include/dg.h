@@ -76,7 +76,8 @@ int dg_version(void);
 /* Device-side checks, off by default (a debugging aid; the pages describe   */
 /* no failure handling).  When on, the combine / acceptance kernels check    */
 /* every sampled and argmax index against [0, V), every entropy and the      */
-/* canvas total for finiteness and every rank against [0, L); the attention  */
+/* canvas total for finiteness and every rank of the acceptance's ordered    */
+/* positions against their count; the attention                               */
 /* kernels and the split merge check each row's softmax sum and outputs for  */
 /* finiteness; the MoE routing checks expert ids, positions and the token    */
 /* count.  A failed check records DG_ERR_DEVICE (and a location code) in the */
@@ -240,7 +241,8 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
 /* dg_denoise_step for callers that cannot allocate device memory (an engine  */
 /* that owns every byte through its own pool, code that runs where allocation */
 /* is not allowed): no workspace argument.  The pages have no counterpart;    */
-/* this is a deployment convenience.  Same kernels, same results; their       */
+/* this is a deployment convenience.  Same kernels, same results (w in either */
+/* layout of p->w_layout); their                                              */
 /* scratch lives in one 8 MiB array inside the library's device memory,      */
 /* held by every GPU that loads the library until the process exits.         */
 /* Limit: steps needing more than 8 MiB of scratch (256 B + 7 x 4 B x units  */

@@ -57,3 +57,14 @@ def test_records_do_not_carry_over():
     assert bench._traffic_record(SRCS, "lm_head_duo_wide_kernel", FULL) is None
     # another set of sources (here: one file short) hashes differently
     assert bench._traffic_record(SRCS[:-1], "lm_head_duo_kernel", FULL) is None
+
+
+def test_oracle_sample_columns_from_either_layout():
+    """bench.py's oracle sample takes the first columns of W from W [d, V] or
+    from its packed form [V/128][d][128] alike."""
+    import torch
+    d, V = 64, 1024
+    w = torch.arange(d * V, dtype=torch.float32).view(d, V)
+    wp = w.view(d, V // 128, 128).permute(1, 0, 2).contiguous().view(-1)
+    assert torch.equal(bench._w_columns(wp, True, d, 512), w[:, :512])
+    assert torch.equal(bench._w_columns(w, False, d, 512), w[:, :512])
