@@ -433,7 +433,9 @@ int dg_lm_head_fold(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 uint64_t dg_kernel_launches(void);
 
 /* The LM-head launch dg_denoise_step would make on the current device for    */
-/* rows = B*L canvas positions, hidden size d and vocabulary V (no launch).   */
+/* rows = B*L canvas positions, hidden size d and vocabulary V (no launch),  */
+/* with W [d, V] in its row-major layout (a packed W keeps the step on the   */
+/* kinds 2 and 3; the FP8 step runs kind 2/3 with 12 epilogue warps).       */
 /* *kind: 0 = single-CTA kernel, 2 = 2-CTA cluster issuing 2-SM UMMAs,      */
 /* 3 = the kind-2 kernel on a schedule of bn-column tiles whose adjacent     */
 /* pairs run as one tile of 2 bn columns (kind 1 is not used); *bn:          */
