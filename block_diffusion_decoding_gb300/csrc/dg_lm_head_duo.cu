@@ -18,7 +18,10 @@
 // MMA at this shape.
 //
 //   warp 0      TMA producer (both CTAs): X[128 rows, 64] and W[64, BN/2] of
-//               its own halves into a 6-stage ring; both CTAs' copies
+//               its own halves into a 6-stage ring (W from [d, V], or from
+//               the packed layout [V/128][d][128] through a 3-D map: the
+//               same boxes, each 64 x 64 pair one contiguous 16 KB); both
+//               CTAs' copies
 //               complete on the even CTA's full barrier (the even CTA expects
 //               the bytes of both halves); a stage is free once the pair MMAs
 //               that read it are done (the commit is multicast to both CTAs'
@@ -27,7 +30,7 @@
 //               CTA); the accumulator is free once the epilogues of both
 //               CTAs have read it (the odd CTA's warps arrive remotely);
 //   warps 4..   epilogue (4 x CG warps: CG = 2 in lm_head_duo_kernel, 4 in
-//               lm_head_duo_wide_kernel and the FP8 instance): warp w
+//               lm_head_duo_wide_kernel, 3 in the FP8 instance): warp w
 //               reads TMEM lanes 32 (w % 4) .. +31, every CG-th 16-column
 //               chunk starting at chunk (w - 4) / 4; the column groups merge
 //               in shared memory and one partial state per (row, cluster)
