@@ -145,7 +145,7 @@ def test_accept_in_bound_set_edges(kind, L, b):
     smallest key past it): its membership edge, the outside key that commits
     or not, ties inside and outside, and b = 0 -- against the oracle's full
     sort, bit for bit."""
-    rng = np.random.default_rng(abs(hash((kind, L))) % (1 << 32))
+    rng = np.random.default_rng(sum(map(ord, kind)) * 1009 + L)
     V, seed, step = 4096, 5, 2
     H = _edge_entropies(kind, L, b)[None, :]
     sample = rng.integers(0, V, (1, L)).astype(np.int32)
