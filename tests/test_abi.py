@@ -190,3 +190,13 @@ def test_packed_weight_size_and_argument_checks(lib):
     # a step's layout is 0 (row-major) or 1 (packed)
     assert dg.denoise_step_workspace(dg.step_params(1, 256, 1024, 16384, 0.8, w_layout=1)) > 0
     assert dg.denoise_step_workspace(dg.step_params(1, 256, 1024, 16384, 0.8, w_layout=2)) == 0
+
+
+def test_pack_lm_weight_binding_rejects_bad_tensors(lib):
+    """The binding packs only a contiguous bf16 [d, V] tensor (checked before
+    any call into the library)."""
+    import torch
+    w = torch.zeros(64, 256, dtype=torch.bfloat16)
+    for bad in (w.t(), w.float(), w.view(-1)):
+        with pytest.raises(ValueError):
+            dg.pack_lm_weight(bad)

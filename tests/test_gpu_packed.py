@@ -216,3 +216,32 @@ def test_self_conditioning_step_packed_equals_rowmajor(B, L, d, V):
     _same_outputs(res[1][0], res[0][0])
     assert torch.equal(res[0][1], res[1][1])
     assert bool(torch.isfinite(res[1][1]).all())
+
+
+def test_block_loop_with_producer_packed_equals_rowmajor(monkeypatch):
+    """The loop with the decoder body captured into it (the built-in
+    canvas-dependent producer, hidden_k = bf16(base_k + E[canvas])) on the
+    packed weight: the same run as on W [d, V] (both on the 2-SM kernel)."""
+    force_lm_kernel(monkeypatch, "fused")
+    B, L, d, V, steps = 1, 128, 256, 4096, 10
+    cfg = dg_synth.StepConfig("packed_fn", B=B, L=L, d=d, V=V, w_std=0.05, seed=14)
+    w = to_dev(dg_synth.lm_weight(cfg))
+    wp = dg.pack_lm_weight(w)
+    g = torch.Generator(device=DEV).manual_seed(8)
+    base = (torch.randn(steps, L, d, device=DEV, generator=g) * 2.0).to(torch.bfloat16)
+    table = (torch.randn(V, d, device=DEV, generator=g) * 0.05).to(torch.bfloat16)
+    user = dg.HiddenEmbed(base.data_ptr(), L * d, table.data_ptr(), L, d, V)
+    res = []
+    for layout, ww in ((dg.W_ROWMAJOR, w), (dg.W_PACKED, wp)):
+        p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=0, seed=6, w_layout=layout)
+        bp = dg.block_params(steps, 0.8, 0.4, 0)
+        bufs = dg.BlockBuffers(B, L, steps, DEV)
+        ws = dg.workspace(dg.generate_block_workspace(p, bp), DEV)
+        buf = torch.empty(L, d, dtype=torch.bfloat16, device=DEV)
+        dg.generate_block_fn(dg.hidden_producer("embed_add"), user, buf, ww, p, bp, bufs, ws)
+        torch.cuda.synchronize()
+        status_ok(ws)
+        res.append(bufs)
+    a, b = res
+    for name in ("canvas", "argmax", "steps_taken", "mean_entropy", "n_accepted_hist"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
