@@ -185,6 +185,32 @@ def test_block_full_three_step_schedule_matches_oracle():
         assert np.array_equal(np_i32(bufs.canvas), ref["canvas"])
 
 
+def test_block_full_packed_weight_equals_rowmajor():
+    """The full-size converging loop (48-step cap) as the benchmark runs it,
+    on the packed weight: the same run as on W [d, V], bit for bit."""
+    cfg = dg_synth.CONFIGS["block_full"]
+    wb = _weight("block_full")
+    hs, _ = _block_hidden_all(cfg, wb, cfg.max_steps)
+    B, L, d, V = cfg.B, cfg.L, cfg.d, cfg.V
+    w = to_dev(wb)
+    hid = to_dev(hs)
+    res = []
+    for layout, ww in ((dg.W_ROWMAJOR, w), (dg.W_PACKED, dg.pack_lm_weight(w))):
+        p = dg.step_params(B, L, d, V, cfg.t_start, cfg.entropy_bound, cfg.stop_threshold,
+                           step=0, seed=5, w_layout=layout)
+        bp = dg.block_params(cfg.max_steps, cfg.t_start, cfg.t_end, B * L * d)
+        bufs = dg.BlockBuffers(B, L, cfg.max_steps, DEV)
+        ws = dg.workspace(dg.generate_block_workspace(p, bp), DEV)
+        dg.generate_block(hid, ww, p, bp, bufs, ws)
+        torch.cuda.synchronize()
+        status_ok(ws)
+        res.append(bufs)
+    a, b = res
+    assert 2 <= int(a.steps_taken[0]) < cfg.max_steps
+    for name in ("canvas", "argmax", "steps_taken", "mean_entropy", "n_accepted_hist"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
 def test_block_full_converging_final_steps_match_oracle():
     """The 48-step converging loop at full size.  The loop must stop before the
     cap (entropies fall with the step); at the step it stopped on, the oracle's
