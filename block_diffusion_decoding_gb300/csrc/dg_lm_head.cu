@@ -26,7 +26,10 @@
 //               them (dg_sampler.cuh) while the MMA fills the other buffer;
 //               at each row-block boundary the two column groups merge
 //               their states in shared memory and one partial state per
-//               (row, CTA) goes to global memory (slot = CTA index).
+//               (row, CTA) goes to global memory (slot = CTA index).  A CTA
+//               with a single tile leaves accumulator buffer 1 unused: its
+//               epilogue warps fill it with the tile's Philox noise words
+//               while the MMA runs, and the fold loads them from there.
 #include "dg_kernels.h"
 
 namespace dg {
@@ -179,6 +182,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         RowState st;
         row_state_init(st);
         int cur_m = -1;
+        // one tile: accumulator buffer 1 stays free, so the tile's noise words
+        // are computed into it while the MMA runs and the fold loads them
+        const bool pre = ntiles == 1;
+        if (pre) {
+            const int m = t0 / a.ntn, n = t0 % a.ntn;
+            noise_to_tmem(tmem_base + lane_off + static_cast<uint32_t>(256 + h * 128), 16 * cg,
+                          16 * kLmColGroups, a.BN, static_cast<uint32_t>(n * a.BN),
+                          static_cast<uint32_t>(a.V),
+                          static_cast<uint32_t>(m * kRowsPerBlock + h * 128 + q * 32 + lane), fc);
+        }
         for (int i = 0; i < ntiles; ++i) {
             const int t = t0 + i;
             const int m = t / a.ntn, n = t % a.ntn;
@@ -201,7 +214,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const uint32_t tb = tmem_base + lane_off + static_cast<uint32_t>(acc * 256 + h * 128);
             const bool live = row < a.M;
             fold_tile(st, tb, 16 * cg, 16 * kLmColGroups, a.BN, static_cast<uint32_t>(n * a.BN),
-                      static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live);
+                      static_cast<uint32_t>(a.V), static_cast<uint32_t>(row), fc, live,
+                      pre ? tb + 256u : 0u);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);

@@ -286,7 +286,7 @@ DG_DEVICE uint32_t gumbel_word_threshold(float t)
 template <bool kSC>
 DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
                         uint32_t row, const FoldConsts &fc, bool live, ScAcc *sc,
-                        const uint16_t *__restrict__ E, uint16_t *pbuf)
+                        const uint16_t *__restrict__ E, uint16_t *pbuf, uint32_t wtm = 0u)
 {
     const bool full = v0 + 16u <= V;
     float x[16];
@@ -366,7 +366,11 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
     const float cz = cmax * fc.invT;
     if (!__any_sync(0xFFFFFFFFu, cz > lb - kGumbelMaxPlusSlack)) return;
     uint32_t w[16];
-    {
+    if (wtm != 0u) {
+        // the chunk's noise words, computed ahead into TMEM (same layout)
+        tmem_ld16_issue(wtm, w);
+        tmem_wait_ld16(w);
+    } else {
         uint4 r[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) r[q] = make_uint4((v0 >> 2) + q, row, fc.step, kStreamGumbel);
@@ -487,9 +491,37 @@ DG_DEVICE void fold16_t(RowState &st, const float (&lg)[16], uint32_t v0, uint32
 }
 
 DG_DEVICE void fold16(RowState &st, const float (&lg)[16], uint32_t v0, uint32_t V,
-                      uint32_t row, const FoldConsts &fc, bool live)
+                      uint32_t row, const FoldConsts &fc, bool live, uint32_t wtm = 0u)
 {
-    fold16_t<false>(st, lg, v0, V, row, fc, live, nullptr, nullptr, nullptr);
+    fold16_t<false>(st, lg, v0, V, row, fc, live, nullptr, nullptr, nullptr, wtm);
+}
+
+// The noise words of the chunks fold_tile visits (first, first + stride,
+// ... < BN, columns vbase + c), written to TMEM at wtb + c for this warp's
+// lanes, so that the fold loads them instead of running Philox.  All 32
+// lanes call it together.
+DG_DEVICE void noise_to_tmem(uint32_t wtb, int first, int stride, int BN, uint32_t vbase,
+                             uint32_t V, uint32_t row, const FoldConsts &fc)
+{
+#pragma unroll 1
+    for (int c0 = first; c0 < BN; c0 += stride) {
+        const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
+        if (v0 >= V) break;
+        uint4 r[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[q] = make_uint4((v0 >> 2) + q, row, fc.step, kStreamGumbel);
+        philox4x32_10_x4(r, fc.k0, fc.k1);
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            w[4 * q] = r[q].x;
+            w[4 * q + 1] = r[q].y;
+            w[4 * q + 2] = r[q].z;
+            w[4 * q + 3] = r[q].w;
+        }
+        tmem_st16(wtb + static_cast<uint32_t>(c0), w);
+    }
+    tmem_wait_st();
 }
 
 // Resolve the kept column (evaluate it exactly) before the state is stored.
@@ -536,7 +568,8 @@ DG_DEVICE void row_state_merge(RowState &a, const RowState &b)
 // is folded needs 16 more live registers than the 96 a thread has here and
 // spills; it measured slower.)
 DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int BN, uint32_t vbase,
-                         uint32_t V, uint32_t row, const FoldConsts &fc, bool live)
+                         uint32_t V, uint32_t row, const FoldConsts &fc, bool live,
+                         uint32_t wtb = 0u)
 {
 #pragma unroll 1
     for (int c0 = first; c0 < BN; c0 += stride) {
@@ -544,7 +577,7 @@ DG_DEVICE void fold_tile(RowState &st, uint32_t tb, int first, int stride, int B
         tmem_ld16(tb + static_cast<uint32_t>(c0), lg);
         const uint32_t v0 = vbase + static_cast<uint32_t>(c0);
         // one call site of the (large) fold keeps the loop in the instruction cache
-        if (v0 < V) fold16(st, lg, v0, V, row, fc, live);
+        if (v0 < V) fold16(st, lg, v0, V, row, fc, live, wtb ? wtb + static_cast<uint32_t>(c0) : 0u);
     }
 }
 
