@@ -459,14 +459,6 @@ def run_ours(args, cfg, emit=True):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     stream = torch.cuda.current_stream(dev)
 
-    def lm_step(p):
-        if fp8:
-            dg.denoise_step_fp8(x, w8, w_scale, p, bufs, sws)
-        elif sc:
-            dg.denoise_step_sc(x, w, sc_table, p, bufs, sc_out, sws)
-        else:
-            dg.denoise_step(x, w, p, bufs, sws)
-
     def lm_fold():
         if fp8:
             dg.lm_head_fold_fp8(x, w8, w_scale, p0, sws)
@@ -475,20 +467,27 @@ def run_ours(args, cfg, emit=True):
         else:
             dg.lm_head_fold(x, w, p0, sws)
 
-    # The bf16 step is one library call (dg_canvas_step: the canvas attention
-    # on a stream forked from the step's stream, the LM head planned on the SMs
-    # the attention leaves free); the FP8 and self-conditioning steps run the
-    # attention and then their step on the one stream.
-    cws = dg.workspace(dg.canvas_step_workspace(p0, P, Hq, Hkv, D), dev) if not (fp8 or sc) else None
+    # The step is one library call (dg_canvas_step and its FP8 and
+    # self-conditioning forms: the canvas attention on a stream forked from the
+    # step's stream; for the bf16 step the LM head is planned on the SMs a
+    # short attention leaves free).
+    if fp8:
+        cws = dg.workspace(dg.canvas_step_fp8_workspace(p0, P, Hq, Hkv, D), dev)
+    elif sc:
+        cws = dg.workspace(dg.canvas_step_sc_workspace(p0, P, Hq, Hkv, D), dev)
+    else:
+        cws = dg.workspace(dg.canvas_step_workspace(p0, P, Hq, Hkv, D), dev)
 
     def step(k):
         p = dg.step_params(B, L, d, V, cfg.temperature, cfg.entropy_bound, cfg.stop_threshold,
                            k, seed=rank, w_layout=layout)
-        if cws is not None:
-            dg.canvas_step(q, kp, vp, kc, vc, attn_out, scale, x, w, p, bufs, cws)
+        if fp8:
+            dg.canvas_step_fp8(q, kp, vp, kc, vc, attn_out, scale, x, w8, w_scale, p, bufs, cws)
+        elif sc:
+            dg.canvas_step_sc(q, kp, vp, kc, vc, attn_out, scale, x, w, sc_table, p, bufs, sc_out,
+                              cws)
         else:
-            dg.canvas_attn(q, kp, vp, kc, vc, attn_out, scale, aws)
-            lm_step(p)
+            dg.canvas_step(q, kp, vp, kc, vc, attn_out, scale, x, w, p, bufs, cws)
 
     def timed(fn, n, first, label="step"):
         """Per-iteration CUDA-event times (ms) with an L2 flush before each

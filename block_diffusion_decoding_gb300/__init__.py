@@ -40,7 +40,9 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_set_device_checks", "dg_device
             "dg_lm_head_fold_sc", "dg_moe_ffn_workspace", "dg_moe_ffn",
             "dg_generate_block_fn", "dg_hidden_from_steps", "dg_hidden_embed_add",
             "dg_canvas_step_workspace", "dg_canvas_step",
-            "dg_lm_weight_packed_bytes", "dg_pack_lm_weight"]
+            "dg_lm_weight_packed_bytes", "dg_pack_lm_weight",
+            "dg_canvas_step_fp8_workspace", "dg_canvas_step_fp8",
+            "dg_canvas_step_sc_workspace", "dg_canvas_step_sc"]
 
 
 class DgError(RuntimeError):
@@ -139,6 +141,12 @@ def _lib():
             "dg_hidden_embed_add": ([vp] * 5, i32),
             "dg_canvas_step_workspace": ([sp, i32, i32, i32, i32], sz),
             "dg_canvas_step": ([vp] * 6 + [i32] * 4 + [f32, vp, vp, sp, si, vp, sz, vp], i32),
+            "dg_canvas_step_fp8_workspace": ([sp, i32, i32, i32, i32], sz),
+            "dg_canvas_step_fp8": ([vp] * 6 + [i32] * 4 + [f32, vp, vp, vp, sp, si, vp, sz, vp],
+                                   i32),
+            "dg_canvas_step_sc_workspace": ([sp, i32, i32, i32, i32], sz),
+            "dg_canvas_step_sc": ([vp] * 6 + [i32] * 4 + [f32, vp, vp, vp, sp, si, vp, vp, sz, vp],
+                                  i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -268,6 +276,44 @@ def canvas_step(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, scale, hidd
                                float(scale), _p(hidden), _p(w), ctypes.byref(p), ctypes.byref(io),
                                _p(workspace), workspace.numel(), _stream(stream))
     _check(rc, "dg_canvas_step")
+
+
+def canvas_step_fp8_workspace(p: StepParams, P, Hq, Hkv, D) -> int:
+    return int(_lib().dg_canvas_step_fp8_workspace(ctypes.byref(p), P, Hq, Hkv, D))
+
+
+def canvas_step_fp8(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, scale, hidden, w8t,
+                    w_scale, p: StepParams, bufs: StepBuffers, workspace, stream=None):
+    """dg_canvas_step_fp8: the canvas attention beside the E4M3 denoising step."""
+    B, L, Hq, D = q.shape
+    P = k_prefix.shape[1] if k_prefix is not None else 0
+    Hkv = k_canvas.shape[2]
+    io = bufs.io()
+    rc = _lib().dg_canvas_step_fp8(_p(q), _p(k_prefix) if P else None,
+                                   _p(v_prefix) if P else None, _p(k_canvas), _p(v_canvas),
+                                   _p(attn_out), P, Hq, Hkv, D, float(scale), _p(hidden), _p(w8t),
+                                   _p(w_scale), ctypes.byref(p), ctypes.byref(io), _p(workspace),
+                                   workspace.numel(), _stream(stream))
+    _check(rc, "dg_canvas_step_fp8")
+
+
+def canvas_step_sc_workspace(p: StepParams, P, Hq, Hkv, D) -> int:
+    return int(_lib().dg_canvas_step_sc_workspace(ctypes.byref(p), P, Hq, Hkv, D))
+
+
+def canvas_step_sc(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, scale, hidden, w,
+                   sc_table, p: StepParams, bufs: StepBuffers, sc_out, workspace, stream=None):
+    """dg_canvas_step_sc: the canvas attention beside the self-conditioning step."""
+    B, L, Hq, D = q.shape
+    P = k_prefix.shape[1] if k_prefix is not None else 0
+    Hkv = k_canvas.shape[2]
+    io = bufs.io()
+    rc = _lib().dg_canvas_step_sc(_p(q), _p(k_prefix) if P else None,
+                                  _p(v_prefix) if P else None, _p(k_canvas), _p(v_canvas),
+                                  _p(attn_out), P, Hq, Hkv, D, float(scale), _p(hidden), _p(w),
+                                  _p(sc_table), ctypes.byref(p), ctypes.byref(io), _p(sc_out),
+                                  _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "dg_canvas_step_sc")
 
 
 def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):

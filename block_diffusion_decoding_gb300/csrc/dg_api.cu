@@ -1206,6 +1206,132 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     return rc;
 }
 
+// ---------------------------------------------------------------- whole step, FP8 / self-conditioning
+namespace {
+
+// The canvas attention on the library's second stream, forked from and joined
+// back into `stream`, beside step(stream, ctx) (the LM-head step; it gets the
+// first step_bytes of the workspace, the attention the rest from offset
+// step_bytes).  No SMs are set aside: the attention shares the GPU.
+typedef int (*ForkStepFn)(cudaStream_t st, void *ctx);
+int canvas_fork_run(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                    const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out, int P,
+                    int Hq, int Hkv, int D, float scale, const dg_step_params *p, size_t step_bytes,
+                    void *workspace, size_t workspace_bytes, void *stream, ForkStepFn step,
+                    void *ctx)
+{
+    ForkStreams *fs = nullptr;
+    int rc = fork_streams(&fs);
+    if (rc != DG_OK) return rc;
+    std::lock_guard<std::mutex> fork_lock(fs->mu);
+    uint8_t *aws = static_cast<uint8_t *>(workspace) + step_bytes;
+    cudaStream_t st = as_stream(stream);
+    DG_CUDA_TRY(cudaEventRecord(fs->fork, st));
+    DG_CUDA_TRY(cudaStreamWaitEvent(fs->side, fs->fork, 0));
+    rc = attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, p->B, p->L, P, P, Hq, Hkv, D,
+                  scale, 0, aws, workspace_bytes - step_bytes, fs->side, 0);
+    if (rc == DG_OK) rc = step(st, ctx);
+    // the join is recorded whatever happened, so `stream` never waits on a stale fork
+    DG_CUDA_TRY(cudaEventRecord(fs->join, fs->side));
+    DG_CUDA_TRY(cudaStreamWaitEvent(st, fs->join, 0));
+    return rc;
+}
+
+struct Fp8StepArgs {
+    const uint16_t *hidden;
+    const uint8_t *w8t;
+    const float *w_scale;
+    const dg_step_params *p;
+    const dg_step_io *io;
+    void *workspace;
+    size_t bytes;
+};
+
+int fp8_fork_step(cudaStream_t st, void *ctx)
+{
+    const Fp8StepArgs *a = static_cast<const Fp8StepArgs *>(ctx);
+    return fp8_step(a->hidden, a->w8t, a->w_scale, a->p, a->io, a->workspace, a->bytes, st, false);
+}
+
+struct ScStepArgs {
+    const uint16_t *hidden, *w, *sc_table;
+    const dg_step_params *p;
+    const dg_step_io *io;
+    float *sc_out;
+    void *workspace;
+    size_t bytes;
+};
+
+int sc_fork_step(cudaStream_t st, void *ctx)
+{
+    const ScStepArgs *a = static_cast<const ScStepArgs *>(ctx);
+    return sc_step(a->hidden, a->w, a->sc_table, a->p, a->io, a->sc_out, a->workspace, a->bytes,
+                   st, false);
+}
+
+}  // namespace
+
+size_t dg_canvas_step_fp8_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    const size_t a = dg_canvas_attn_workspace(p->B, p->L, P, Hq, Hkv, D);
+    if (a == 0) return 0;
+    return round_up(fp8_ws_bytes(p, nullptr, nullptr), 256) + a;
+}
+
+int dg_canvas_step_fp8(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                       const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out,
+                       int P, int Hq, int Hkv, int D, float scale, const uint16_t *hidden,
+                       const uint8_t *w8t, const float *w_scale, const dg_step_params *p,
+                       const dg_step_io *io, void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_fp8_step(hidden, w8t, w_scale, p);
+    if (rc != DG_OK) return rc;
+    if ((rc = check_io(io, true)) != DG_OK) return rc;
+    if (!aligned16(workspace)) return DG_ERR_ALIGNMENT;
+    const size_t need = dg_canvas_step_fp8_workspace(p, P, Hq, Hkv, D);
+    if (need == 0) return DG_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < need) return DG_ERR_WORKSPACE;
+    const size_t step_bytes = round_up(fp8_ws_bytes(p, nullptr, nullptr), 256);
+    Fp8StepArgs args{hidden, w8t, w_scale, p, io, workspace, step_bytes};
+    return canvas_fork_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, P, Hq, Hkv, D,
+                           scale, p, step_bytes, workspace, workspace_bytes, stream, fp8_fork_step,
+                           &args);
+}
+
+size_t dg_canvas_step_sc_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D)
+{
+    if (check_step_params(p) != DG_OK) return 0;
+    const size_t a = dg_canvas_attn_workspace(p->B, p->L, P, Hq, Hkv, D);
+    if (a == 0) return 0;
+    return round_up(sc_ws_bytes(p, nullptr), 256) + a;
+}
+
+int dg_canvas_step_sc(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                      const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out, int P,
+                      int Hq, int Hkv, int D, float scale, const uint16_t *hidden,
+                      const uint16_t *w, const uint16_t *sc_table, const dg_step_params *p,
+                      const dg_step_io *io, float *sc_out, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if ((rc = check_io(io, true)) != DG_OK) return rc;
+    if (!hidden || !w || !sc_table || !sc_out) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (!aligned16(hidden) || !aligned16(w) || !aligned16(sc_table) || !aligned16(sc_out) ||
+        !aligned16(workspace))
+        return DG_ERR_ALIGNMENT;
+    const size_t need = dg_canvas_step_sc_workspace(p, P, Hq, Hkv, D);
+    if (need == 0) return DG_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < need) return DG_ERR_WORKSPACE;
+    const size_t step_bytes = round_up(sc_ws_bytes(p, nullptr), 256);
+    ScStepArgs args{hidden, w, sc_table, p, io, sc_out, workspace, step_bytes};
+    return canvas_fork_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, P, Hq, Hkv, D,
+                           scale, p, step_bytes, workspace, workspace_bytes, stream, sc_fork_step,
+                           &args);
+}
+
 // ---------------------------------------------------------------- self-conditioning step
 size_t dg_denoise_step_sc_workspace(const dg_step_params *p)
 {

@@ -238,6 +238,30 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
                    const dg_step_params *p, const dg_step_io *io, void *workspace,
                    size_t workspace_bytes, void *stream);
 
+/* The whole step with the E4M3 LM head (dg_denoise_step_fp8) or with the     */
+/* self-conditioning read-out (dg_denoise_step_sc) in place of               */
+/* dg_denoise_step: the canvas attention on the library's second stream,     */
+/* forked from `stream` and joined back into it, beside that step on         */
+/* `stream`; no SMs are set aside for the attention.  Arguments and errors   */
+/* as dg_canvas_attn and the step they pair with; one workspace of the       */
+/* matching *_workspace bytes: the step's first (its status word at the      */
+/* start), the attention's from offset round_up(step workspace, 256).        */
+/* Same results as the two calls, bit for bit.                               */
+size_t dg_canvas_step_fp8_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D);
+int dg_canvas_step_fp8(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                       const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out,
+                       int P, int Hq, int Hkv, int D, float scale, const uint16_t *hidden,
+                       const uint8_t *w8t, const float *w_scale, const dg_step_params *p,
+                       const dg_step_io *io, void *workspace, size_t workspace_bytes,
+                       void *stream);
+size_t dg_canvas_step_sc_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D);
+int dg_canvas_step_sc(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
+                      const uint16_t *k_canvas, const uint16_t *v_canvas, uint16_t *attn_out,
+                      int P, int Hq, int Hkv, int D, float scale, const uint16_t *hidden,
+                      const uint16_t *w, const uint16_t *sc_table, const dg_step_params *p,
+                      const dg_step_io *io, float *sc_out, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
 /* dg_denoise_step for callers that cannot allocate device memory (an engine  */
 /* that owns every byte through its own pool, code that runs where allocation */
 /* is not allowed): no workspace argument.  The pages have no counterpart;    */

@@ -288,3 +288,76 @@ def test_canvas_step_full_width_equals_the_two_calls():
     for name in ("canvas", "argmax", "sample", "n_accepted", "stop", "prev_argmax"):
         assert np.array_equal(np_i32(getattr(got, name)), np_i32(getattr(ref, name))), name
     assert torch.equal(got.entropy, ref.entropy)
+
+
+def _attn_case(cfg):
+    ai = dg_synth.attention_inputs(cfg)
+    return {k: to_dev(v) for k, v in ai.items()}
+
+
+def test_canvas_step_fp8_full_width_equals_the_two_calls():
+    """dg_canvas_step_fp8 at the full-width step: the attention output and every
+    step output equal those of dg_canvas_attn and dg_denoise_step_fp8."""
+    cfg = dg_synth.CONFIGS["step_full"]
+    B, L, P, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.P, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
+    t = _attn_case(cfg)
+    x, w = to_dev(dg_synth.lm_hidden(cfg)), to_dev(_weight("step_full"))
+    w8 = torch.empty(V, d, dtype=torch.uint8, device=DEV)
+    ws8 = torch.empty(V, dtype=torch.float32, device=DEV)
+    dg.quantize_weight_e4m3(w, w8, ws8)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=2, seed=7)
+    canvas0 = torch.from_numpy(np.random.default_rng(4).integers(0, V, B * L).astype(np.int32))
+    got, ref = dg.StepBuffers(B, L, DEV), dg.StepBuffers(B, L, DEV)
+    got.canvas.copy_(canvas0)
+    ref.canvas.copy_(canvas0)
+    out, ref_out = torch.empty_like(t["q"]), torch.empty_like(t["q"])
+    ws = dg.workspace(dg.canvas_step_fp8_workspace(p, P, Hq, Hkv, D), DEV)
+    dg.canvas_step_fp8(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], out, scale, x, w8, ws8, p, got,
+                       ws)
+    aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    sws = dg.workspace(dg.denoise_step_fp8_workspace(p), DEV)
+    dg.canvas_attn(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], ref_out, scale, aws)
+    dg.denoise_step_fp8(x, w8, ws8, p, ref, sws)
+    torch.cuda.synchronize()
+    status_ok(ws)
+    assert torch.equal(out, ref_out)
+    for name in ("canvas", "argmax", "sample", "n_accepted", "stop", "prev_argmax"):
+        assert np.array_equal(np_i32(getattr(got, name)), np_i32(getattr(ref, name))), name
+    assert torch.equal(got.entropy, ref.entropy)
+
+
+def test_canvas_step_sc_full_width_equals_the_two_calls():
+    """dg_canvas_step_sc at the full-width step on the packed weight: the
+    attention output, every step output and the read-out equal those of
+    dg_canvas_attn and dg_denoise_step_sc."""
+    cfg = dg_synth.CONFIGS["step_full"]
+    B, L, P, Hq, Hkv, D, d, V = cfg.B, cfg.L, cfg.P, cfg.Hq, cfg.Hkv, cfg.D, cfg.d, cfg.V
+    t = _attn_case(cfg)
+    x = to_dev(dg_synth.lm_hidden(cfg))
+    wp = dg.pack_lm_weight(to_dev(_weight("step_full")))
+    g = torch.Generator(device=DEV).manual_seed(12)
+    table = (torch.randn(V, dg.SC_DIM, device=DEV, generator=g) / math.sqrt(d)).to(torch.bfloat16)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    p = dg.step_params(B, L, d, V, 0.8, 0.1, 0.005, step=3, seed=8, w_layout=dg.W_PACKED)
+    canvas0 = torch.from_numpy(np.random.default_rng(6).integers(0, V, B * L).astype(np.int32))
+    got, ref = dg.StepBuffers(B, L, DEV), dg.StepBuffers(B, L, DEV)
+    got.canvas.copy_(canvas0)
+    ref.canvas.copy_(canvas0)
+    out, ref_out = torch.empty_like(t["q"]), torch.empty_like(t["q"])
+    sc_got = torch.empty(B * L, dg.SC_DIM, device=DEV)
+    sc_ref = torch.empty(B * L, dg.SC_DIM, device=DEV)
+    ws = dg.workspace(dg.canvas_step_sc_workspace(p, P, Hq, Hkv, D), DEV)
+    dg.canvas_step_sc(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], out, scale, x, wp, table, p, got,
+                      sc_got, ws)
+    aws = dg.workspace(dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D), DEV)
+    sws = dg.workspace(dg.denoise_step_sc_workspace(p), DEV)
+    dg.canvas_attn(t["q"], t["kp"], t["vp"], t["kc"], t["vc"], ref_out, scale, aws)
+    dg.denoise_step_sc(x, wp, table, p, ref, sc_ref, sws)
+    torch.cuda.synchronize()
+    status_ok(ws)
+    assert torch.equal(out, ref_out)
+    for name in ("canvas", "argmax", "sample", "n_accepted", "stop", "prev_argmax"):
+        assert np.array_equal(np_i32(getattr(got, name)), np_i32(getattr(ref, name))), name
+    assert torch.equal(got.entropy, ref.entropy)
+    assert torch.equal(sc_got, sc_ref)
