@@ -200,3 +200,43 @@ def test_pack_lm_weight_binding_rejects_bad_tensors(lib):
     for bad in (w.t(), w.float(), w.view(-1)):
         with pytest.raises(ValueError):
             dg.pack_lm_weight(bad)
+
+
+def test_whole_step_fp8_and_sc_validate_before_launch(lib):
+    """dg_canvas_step_fp8 / dg_canvas_step_sc: the step's checks and the
+    workspace size are answered before anything is forked or launched."""
+    good = 1 << 20
+    p = dg.step_params(1, 256, 1024, 16384, 0.8)
+    io = dg.StepIO(*[_vp(good + 64 * i) for i in range(9)])
+    P, Hq, Hkv, D = 256, 4, 1, 128
+    a = dg.canvas_attn_workspace(1, 256, P, Hq, Hkv, D)
+    n8 = dg.canvas_step_fp8_workspace(p, P, Hq, Hkv, D)
+    nsc = dg.canvas_step_sc_workspace(p, P, Hq, Hkv, D)
+    # the step's workspace (rounded to 256 B), then the attention's
+    assert n8 == (dg.denoise_step_fp8_workspace(p) + 255) // 256 * 256 + a
+    assert nsc == (dg.denoise_step_sc_workspace(p) + 255) // 256 * 256 + a
+    assert dg.canvas_step_fp8_workspace(p, P, Hq, Hkv, 64) == 0          # head dim
+    assert dg.canvas_step_sc_workspace(dg.step_params(1, 256, 1024, 1001, 0.8), P, Hq, Hkv, D) == 0
+
+    def fp8(h=good, w8=good, sw=good, n=n8, ws=good):
+        return lib.dg_canvas_step_fp8(*[_vp(good)] * 6, P, Hq, Hkv, D, 0.1,
+                                      _vp(h) if h else None, _vp(w8) if w8 else None,
+                                      _vp(sw) if sw else None, ctypes.byref(p), ctypes.byref(io),
+                                      _vp(ws) if ws else None, n, None)
+
+    assert fp8(h=0) == 1                 # null hidden
+    assert fp8(sw=good + 4) == 3         # misaligned scales
+    assert fp8(n=n8 - 1) == 4            # workspace too small
+    assert fp8(ws=0) == 4                # no workspace
+
+    def sc(h=good, w=good, tab=good, out=good, n=nsc):
+        return lib.dg_canvas_step_sc(*[_vp(good)] * 6, P, Hq, Hkv, D, 0.1,
+                                     _vp(h) if h else None, _vp(w) if w else None,
+                                     _vp(tab) if tab else None, ctypes.byref(p),
+                                     ctypes.byref(io), _vp(out) if out else None, _vp(good), n,
+                                     None)
+
+    assert sc(tab=0) == 1                # null table
+    assert sc(out=0) == 1                # null read-out
+    assert sc(w=good + 2) == 3           # misaligned weight
+    assert sc(n=nsc - 1) == 4            # workspace too small
