@@ -1178,12 +1178,10 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     // attention on the second stream, forked from and joined back into `stream`
     DG_CUDA_TRY(cudaEventRecord(fs->fork, st));
     DG_CUDA_TRY(cudaStreamWaitEvent(fs->side, fs->fork, 0));
-    const int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, di->sms);
-    rc = attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, p->B, p->L, P, P, Hq, Hkv, D,
-                  scale, 0, aws, workspace_bytes - step_bytes, fs->side, reserve);
-    if (rc == DG_OK) {
-        const int M = p->B * p->L;
-        const bool packed = p->w_layout == DG_W_PACKED;
+    const int M = p->B * p->L;
+    const bool packed = p->w_layout == DG_W_PACKED;
+    // the LM head's plan on the SMs a reservation leaves
+    auto lm_plan = [&](int reserve) {
         LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve, false, false, -1, packed);
         if (reserve > 0 && !packed && plan.kind != kLmSingle &&
             std::getenv("DG_LM_KERNEL") == nullptr) {
@@ -1194,6 +1192,29 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
                                                kLmSingle);
             if (single.units >= single.total) plan = single;
         }
+        return plan;
+    };
+    int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, di->sms);
+    if (reserve > 0 && std::getenv("DG_ATTN_RESERVE") == nullptr) {
+        // fewer SMs for the attention when that lets the LM head run more,
+        // narrower tiles and each of them still has at most 2 kReserveTiles of
+        // the attention's key tiles to run (small step: 4 instead of 8 SMs,
+        // 147 LM-head CTAs of 112 columns instead of 128 of 128)
+        const AttnPlan ap = plan_attn(p->B, p->L, P, Hq, Hkv, D, di->sms, reserve);
+        const int ctas = ap.blocks * ap.nsplit;
+        const int units = lm_plan(reserve).units;
+        for (int r = 2; r < reserve; r += 2) {
+            if ((ctas + r - 1) / r * ap.tps > 2 * kReserveTiles) continue;
+            if (lm_plan(r).units > units) {
+                reserve = r;
+                break;
+            }
+        }
+    }
+    rc = attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, p->B, p->L, P, P, Hq, Hkv, D,
+                  scale, 0, aws, workspace_bytes - step_bytes, fs->side, reserve);
+    if (rc == DG_OK) {
+        const LmPlan plan = lm_plan(reserve);
         StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
         const StepSource src = step_source(p);
         const AcceptArgs acc = accept_args(p, io);

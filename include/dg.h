@@ -220,7 +220,9 @@ int dg_denoise_step(const uint16_t *hidden, const uint16_t *w, const dg_step_par
 /* library forks from `stream` and joins back into it (the call's work on      */
 /* `stream` ends when both have); when the attention is short on few CTAs    */
 /* (its key splits capped at an eighth of the SMs, else a sixth, leave at     */
-/* most 6 key tiles per CTA) the LM head is planned on the SMs it leaves.     */
+/* most 6 key tiles per CTA) the LM head is planned on the SMs it leaves --   */
+/* on fewer of them set aside when that gives the LM head more CTAs and the   */
+/* attention still at most 12 key tiles per reserved SM.                      */
 /* The second stream is one per device, shared by all calls: calls on         */
 /* different streams, or from several host threads (the library enqueues a    */
 /* call's fork, launches and join under a lock), are correct but their        */
