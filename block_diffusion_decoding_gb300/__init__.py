@@ -42,7 +42,7 @@ EXPORTED = ["dg_status_string", "dg_version", "dg_set_device_checks", "dg_device
             "dg_canvas_step_workspace", "dg_canvas_step",
             "dg_lm_weight_packed_bytes", "dg_pack_lm_weight",
             "dg_canvas_step_fp8_workspace", "dg_canvas_step_fp8",
-            "dg_canvas_step_sc_workspace", "dg_canvas_step_sc"]
+            "dg_canvas_step_sc_workspace", "dg_canvas_step_sc", "dg_canvas_step_plan"]
 
 
 class DgError(RuntimeError):
@@ -81,6 +81,13 @@ class BlockParams(ctypes.Structure):
 class BlockIO(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("canvas", "argmax", "steps_taken", "mean_entropy", "n_accepted_hist")]
+
+
+class CanvasStepPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("attn_reserved_sms", "attn_pair", "attn_ctas", "attn_splits", "attn_key_tiles",
+                 "attn_key_tile", "lm_kind", "lm_bn", "lm_ctas", "lm_tiles",
+                 "lm_epilogue_warps", "lm_sms")]
 
 
 _L = None
@@ -147,6 +154,7 @@ def _lib():
             "dg_canvas_step_sc_workspace": ([sp, i32, i32, i32, i32], sz),
             "dg_canvas_step_sc": ([vp] * 6 + [i32] * 4 + [f32, vp, vp, vp, sp, si, vp, vp, sz, vp],
                                   i32),
+            "dg_canvas_step_plan": ([sp] + [i32] * 5 + [ctypes.POINTER(CanvasStepPlan)], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -321,6 +329,15 @@ def lm_head_fold(hidden, w, p: StepParams, workspace, stream=None):
     rc = _lib().dg_lm_head_fold(_p(hidden), _p(w), ctypes.byref(p), _p(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "dg_lm_head_fold")
+
+
+def canvas_step_plan(p: StepParams, P: int, Hq: int, Hkv: int, D: int, sms: int = 0) -> dict:
+    """The launches canvas_step would make on a GPU with `sms` SMs (0: the
+    current device's); with sms > 0 no device is touched."""
+    out = CanvasStepPlan()
+    rc = _lib().dg_canvas_step_plan(ctypes.byref(p), P, Hq, Hkv, D, sms, ctypes.byref(out))
+    _check(rc, "dg_canvas_step_plan")
+    return {name: getattr(out, name) for name, _ in CanvasStepPlan._fields_}
 
 
 def lm_head_plan(rows: int, d: int, V: int) -> dict:

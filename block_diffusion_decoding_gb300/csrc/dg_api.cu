@@ -1142,6 +1142,57 @@ int attn_reserve(int B, int L, int P, int Hq, int Hkv, int D, int sms)
     return 0;
 }
 
+// The LM head's plan for the canvas step on the SMs a reservation leaves.
+LmPlan canvas_lm_plan(const dg_step_params *p, int sms, int reserve)
+{
+    const int M = p->B * p->L;
+    const bool packed = p->w_layout == DG_W_PACKED;
+    LmPlan plan = plan_lm_head(M, p->d, p->V, sms - reserve, false, false, -1, packed);
+    if (reserve > 0 && !packed && plan.kind != kLmSingle && std::getenv("DG_LM_KERNEL") == nullptr) {
+        // one tile per CTA on the SMs left: the single-CTA kernel (its 16
+        // epilogue warps fold a 256-row tile; measured faster than the 2-SM
+        // kernel's 8 at one tile per CTA)
+        const LmPlan single = plan_lm_head(M, p->d, p->V, sms - reserve, false, false, kLmSingle);
+        if (single.units >= single.total) plan = single;
+    }
+    return plan;
+}
+
+// The canvas step's plan on a GPU with `sms` SMs: the SMs set aside for the
+// attention (attn_reserve), the attention's plan on them and the LM head's on
+// the rest.
+struct CanvasStepPlan {
+    int reserve;
+    AttnPlan ap;
+    LmPlan lm;
+};
+
+CanvasStepPlan plan_canvas_step(const dg_step_params *p, int P, int Hq, int Hkv, int D, int sms)
+{
+    int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, sms);
+    if (reserve > 0 && std::getenv("DG_ATTN_RESERVE") == nullptr) {
+        // fewer SMs for the attention when that lets the LM head run more,
+        // narrower tiles and each of them still has at most 2 kReserveTiles of
+        // the attention's key tiles to run (small step: 4 instead of 8 SMs,
+        // 147 LM-head CTAs of 112 columns instead of 128 of 128)
+        const AttnPlan ap = plan_attn(p->B, p->L, P, Hq, Hkv, D, sms, reserve);
+        const int ctas = ap.blocks * ap.nsplit;
+        const int units = canvas_lm_plan(p, sms, reserve).units;
+        for (int r = 2; r < reserve; r += 2) {
+            if ((ctas + r - 1) / r * ap.tps > 2 * kReserveTiles) continue;
+            if (canvas_lm_plan(p, sms, r).units > units) {
+                reserve = r;
+                break;
+            }
+        }
+    }
+    CanvasStepPlan sp{};
+    sp.reserve = reserve;
+    sp.ap = plan_attn(p->B, p->L, P, Hq, Hkv, D, sms, reserve);
+    sp.lm = canvas_lm_plan(p, sms, reserve);
+    return sp;
+}
+
 }  // namespace
 
 size_t dg_canvas_step_workspace(const dg_step_params *p, int P, int Hq, int Hkv, int D)
@@ -1150,6 +1201,37 @@ size_t dg_canvas_step_workspace(const dg_step_params *p, int P, int Hq, int Hkv,
     const size_t a = dg_canvas_attn_workspace(p->B, p->L, P, Hq, Hkv, D);
     if (a == 0) return 0;
     return round_up(dg_denoise_step_workspace(p), 256) + a;
+}
+
+int dg_canvas_step_plan(const dg_step_params *p, int P, int Hq, int Hkv, int D, int sms,
+                        dg_canvas_step_plan_info *out)
+{
+    int rc = check_step_params(p);
+    if (rc != DG_OK) return rc;
+    if (out == nullptr || sms > kAssumedMaxSMs) return DG_ERR_INVALID_ARG;
+    if (p->d % 64 != 0 || p->d < 64 || p->d > 16384) return DG_ERR_UNSUPPORTED;
+    if (dg_canvas_step_workspace(p, P, Hq, Hkv, D) == 0) return DG_ERR_UNSUPPORTED;
+    if (sms <= 0) {
+        DeviceInfo *di = nullptr;
+        if ((rc = current_device_info(&di)) != DG_OK) return rc;
+        sms = di->sms;
+    }
+    const CanvasStepPlan sp = plan_canvas_step(p, P, Hq, Hkv, D, sms);
+    dg_canvas_step_plan_info o{};
+    o.attn_reserved_sms = sp.reserve;
+    o.attn_pair = sp.ap.pair ? 1 : 0;
+    o.attn_ctas = sp.ap.blocks * sp.ap.nsplit;
+    o.attn_splits = sp.ap.nsplit;
+    o.attn_key_tiles = sp.ap.tps;
+    o.attn_key_tile = sp.ap.BKV;
+    o.lm_kind = sp.lm.kind;
+    o.lm_bn = sp.lm.BN;
+    o.lm_ctas = sp.lm.grid;
+    o.lm_tiles = sp.lm.total;
+    o.lm_epilogue_warps = sp.lm.epi_warps;
+    o.lm_sms = sp.lm.sms;
+    *out = o;
+    return DG_OK;
 }
 
 int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *v_prefix,
@@ -1179,42 +1261,11 @@ int dg_canvas_step(const uint16_t *q, const uint16_t *k_prefix, const uint16_t *
     DG_CUDA_TRY(cudaEventRecord(fs->fork, st));
     DG_CUDA_TRY(cudaStreamWaitEvent(fs->side, fs->fork, 0));
     const int M = p->B * p->L;
-    const bool packed = p->w_layout == DG_W_PACKED;
-    // the LM head's plan on the SMs a reservation leaves
-    auto lm_plan = [&](int reserve) {
-        LmPlan plan = plan_lm_head(M, p->d, p->V, di->sms - reserve, false, false, -1, packed);
-        if (reserve > 0 && !packed && plan.kind != kLmSingle &&
-            std::getenv("DG_LM_KERNEL") == nullptr) {
-            // one tile per CTA on the SMs left: the single-CTA kernel (its 16
-            // epilogue warps fold a 256-row tile; measured faster than the
-            // 2-SM kernel's 8 at one tile per CTA)
-            const LmPlan single = plan_lm_head(M, p->d, p->V, di->sms - reserve, false, false,
-                                               kLmSingle);
-            if (single.units >= single.total) plan = single;
-        }
-        return plan;
-    };
-    int reserve = attn_reserve(p->B, p->L, P, Hq, Hkv, D, di->sms);
-    if (reserve > 0 && std::getenv("DG_ATTN_RESERVE") == nullptr) {
-        // fewer SMs for the attention when that lets the LM head run more,
-        // narrower tiles and each of them still has at most 2 kReserveTiles of
-        // the attention's key tiles to run (small step: 4 instead of 8 SMs,
-        // 147 LM-head CTAs of 112 columns instead of 128 of 128)
-        const AttnPlan ap = plan_attn(p->B, p->L, P, Hq, Hkv, D, di->sms, reserve);
-        const int ctas = ap.blocks * ap.nsplit;
-        const int units = lm_plan(reserve).units;
-        for (int r = 2; r < reserve; r += 2) {
-            if ((ctas + r - 1) / r * ap.tps > 2 * kReserveTiles) continue;
-            if (lm_plan(r).units > units) {
-                reserve = r;
-                break;
-            }
-        }
-    }
+    const CanvasStepPlan sp = plan_canvas_step(p, P, Hq, Hkv, D, di->sms);
     rc = attn_run(q, k_prefix, v_prefix, k_canvas, v_canvas, attn_out, p->B, p->L, P, P, Hq, Hkv, D,
-                  scale, 0, aws, workspace_bytes - step_bytes, fs->side, reserve);
+                  scale, 0, aws, workspace_bytes - step_bytes, fs->side, sp.reserve);
     if (rc == DG_OK) {
-        const LmPlan plan = lm_plan(reserve);
+        const LmPlan &plan = sp.lm;
         StepWs ws = carve_step_ws(workspace, M, p->B, plan.part_slots());
         const StepSource src = step_source(p);
         const AcceptArgs acc = accept_args(p, io);

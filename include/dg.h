@@ -473,6 +473,35 @@ uint64_t dg_kernel_launches(void);
 /* rejects, DG_ERR_CUDA without a device. */
 int dg_lm_head_plan(int rows, int d, int V, int *kind, int *bn, int *ctas, int *epilogue_warps);
 
+/* The launches dg_canvas_step would make for these arguments (same meaning  */
+/* as there) on a GPU with `sms` SMs, without launching anything.  sms > 0   */
+/* (at most 256) plans for that SM count and touches no device, so it runs   */
+/* on a host without a GPU; sms <= 0 takes the current device's count        */
+/* (DG_ERR_CUDA without a device).  The planner's environment overrides      */
+/* (DG_ATTN_*, DG_LM_*) apply as in the step.                                 */
+typedef struct dg_canvas_step_plan_info {
+    int attn_reserved_sms;  /* SMs set aside for the attention; 0: it shares */
+                            /* the GPU with the LM head                        */
+    int attn_pair;          /* 1: 2-CTA clusters issuing 2-SM UMMAs (adjacent */
+                            /* 128-row query tiles), 0: one CTA per tile      */
+    int attn_ctas;          /* CTAs of the attention kernel                    */
+    int attn_splits;        /* key splits per query tile (> 1: a merge kernel  */
+                            /* follows)                                         */
+    int attn_key_tiles;     /* key tiles per split, at most                    */
+    int attn_key_tile;      /* keys per key tile                               */
+    int lm_kind;            /* as *kind of dg_lm_head_plan                     */
+    int lm_bn;              /* vocabulary columns per (schedule) tile          */
+    int lm_ctas;            /* CTAs of the LM-head kernel                      */
+    int lm_tiles;           /* tiles of its schedule                           */
+    int lm_epilogue_warps;  /* as *epilogue_warps of dg_lm_head_plan           */
+    int lm_sms;             /* SMs the LM head was planned on                  */
+} dg_canvas_step_plan_info;
+/* Errors: DG_ERR_INVALID_ARG for a NULL p or out, invalid params or sms     */
+/* above 256; DG_ERR_UNSUPPORTED for shapes dg_canvas_step rejects.  *out is */
+/* written only on DG_OK. */
+int dg_canvas_step_plan(const dg_step_params *p, int P, int Hq, int Hkv, int D, int sms,
+                        dg_canvas_step_plan_info *out);
+
 /* ------------------------------------------------------------------------ */
 /* FP8 (E4M3) LM head.  The pages quote their throughput for an FP8 model     */
 /* ("DiffusionGemma Lab" section 1; "Parallel Denoising From an              */

@@ -240,3 +240,139 @@ def test_whole_step_fp8_and_sc_validate_before_launch(lib):
     assert sc(out=0) == 1                # null read-out
     assert sc(w=good + 2) == 3           # misaligned weight
     assert sc(n=nsc - 1) == 4            # workspace too small
+
+
+# ------------------------------------------------------------------ canvas step plan
+_SMALL = dict(B=1, L=256, d=1024, V=16384, P=256, Hq=4, Hkv=1, D=128)
+_FULL = dict(B=1, L=256, d=2816, V=262144, P=4096, Hq=16, Hkv=8, D=256)
+
+
+@pytest.fixture
+def planner_defaults(monkeypatch):
+    """No planner override from the caller's environment."""
+    for v in ("DG_ATTN_KERNEL", "DG_ATTN_SPLITS", "DG_ATTN_RESERVE", "DG_LM_KERNEL", "DG_LM_BN",
+              "DG_LM_EPI"):
+        monkeypatch.delenv(v, raising=False)
+
+
+def _plan(sms=152, w_layout=dg.W_ROWMAJOR, **kw):
+    c = dict(_SMALL, **kw)
+    p = dg.step_params(c["B"], c["L"], c["d"], c["V"], 0.8, w_layout=w_layout)
+    return dg.canvas_step_plan(p, c["P"], c["Hq"], c["Hkv"], c["D"], sms)
+
+
+def test_canvas_step_plan_of_the_measured_shapes(lib, planner_defaults):
+    """The plans the measured canvas steps run on a 152-SM GB300, computed on
+    the host: the small step sets 4 SMs aside for its 8 attention CTAs and
+    runs the single-CTA LM head as 147 tiles of 112 columns on the other 148;
+    with 2048 cached keys the attention keeps 24 SMs (3 key splits of at most
+    6 tiles) and the LM head runs 128 tiles of 128 columns; the full-width
+    step reserves nothing: the 2-SM attention on 128 CTAs (4 splits) shares
+    the GPU with the fused 2-SM LM head on all 152 SMs."""
+    assert _plan() == dict(attn_reserved_sms=4, attn_pair=0, attn_ctas=8, attn_splits=1,
+                           attn_key_tiles=4, attn_key_tile=128, lm_kind=0, lm_bn=112,
+                           lm_ctas=147, lm_tiles=147, lm_epilogue_warps=0, lm_sms=148)
+    b1 = _plan(P=2048)
+    assert (b1["attn_reserved_sms"], b1["attn_ctas"], b1["attn_splits"], b1["attn_key_tiles"]) \
+        == (24, 24, 3, 6)
+    assert (b1["lm_kind"], b1["lm_bn"], b1["lm_ctas"], b1["lm_sms"]) == (0, 128, 128, 128)
+    for layout in (dg.W_ROWMAJOR, dg.W_PACKED):
+        full = _plan(w_layout=layout, **_FULL)
+        assert full == dict(attn_reserved_sms=0, attn_pair=1, attn_ctas=128, attn_splits=4,
+                            attn_key_tiles=9, attn_key_tile=128, lm_kind=3, lm_bn=128,
+                            lm_ctas=152, lm_tiles=2048, lm_epilogue_warps=8, lm_sms=152)
+    # four canvases with 2048 cached keys: no reservation, the fused 2-SM LM
+    # head with 16 epilogue warps (four 256-row blocks)
+    b4 = _plan(B=4, P=2048)
+    assert (b4["attn_reserved_sms"], b4["lm_kind"], b4["lm_epilogue_warps"]) == (0, 3, 16)
+
+
+def test_canvas_step_plan_reservation_override(lib, planner_defaults, monkeypatch):
+    """DG_ATTN_RESERVE=n forces n SMs (rounded down to even; 0: none) and
+    skips the search for a smaller reservation."""
+    monkeypatch.setenv("DG_ATTN_RESERVE", "0")
+    p0 = _plan()
+    assert p0["attn_reserved_sms"] == 0 and p0["lm_sms"] == 152
+    monkeypatch.setenv("DG_ATTN_RESERVE", "9")
+    p8 = _plan()
+    assert p8["attn_reserved_sms"] == 8 and p8["lm_sms"] == 144
+    # one wave of 128-column tiles on 144 SMs
+    assert (p8["lm_kind"], p8["lm_bn"], p8["lm_ctas"]) == (0, 128, 128)
+
+
+def _ceil(a, b):
+    return -(-a // b)
+
+
+@pytest.mark.parametrize("sms", [16, 60, 132, 148, 152, 256])
+def test_canvas_step_plan_invariants(lib, planner_defaults, sms):
+    """Over a sweep of shapes and SM counts: the LM-head tiles cover the
+    vocabulary and rows once, its grid fits the SMs left to it, the key
+    splits cover every key tile, a reservation is even and leaves the LM head
+    the rest, and a packed W keeps the LM head on the 2-SM kernels."""
+    for B, L, P, Hq, Hkv, D, d, V in [
+            (1, 256, 256, 4, 1, 128, 1024, 16384), (1, 256, 2048, 4, 1, 128, 1024, 16384),
+            (4, 256, 2048, 4, 1, 128, 1024, 16384), (16, 256, 2048, 4, 1, 128, 1024, 16384),
+            (1, 256, 32768, 4, 1, 128, 1024, 16384), (1, 256, 4096, 16, 8, 256, 2816, 262144),
+            (2, 100, 0, 8, 2, 128, 512, 1000), (1, 17, 777, 16, 1, 256, 64, 64),
+            (3, 256, 130, 8, 8, 256, 2048, 50000), (1, 64, 1, 2, 1, 128, 128, 262144)]:
+        for layout in (dg.W_ROWMAJOR, dg.W_PACKED):
+            pl = _plan(sms, layout, B=B, L=L, P=P, Hq=Hq, Hkv=Hkv, D=D, d=d, V=V)
+            r = pl["attn_reserved_sms"]
+            assert r % 2 == 0 and 0 <= r <= sms // 6 + 1
+            assert pl["lm_sms"] == sms - r
+            # attention: every key tile of [cache ; canvas] in some split
+            bkv = pl["attn_key_tile"]
+            nkt = _ceil(P, bkv) + _ceil(L, bkv)
+            ns, tps = pl["attn_splits"], pl["attn_key_tiles"]
+            assert ns * tps >= nkt and (ns - 1) * tps < nkt
+            G = Hq // Hkv
+            mtiles = _ceil(L * G, 128)
+            if pl["attn_pair"]:
+                mtiles += mtiles & 1
+            assert pl["attn_ctas"] == mtiles * Hkv * B * ns
+            assert pl["attn_pair"] == (1 if D == 256 else 0)
+            if r > 0 and ns > 1:
+                assert pl["attn_ctas"] <= r
+            # LM head
+            kind, bn = pl["lm_kind"], pl["lm_bn"]
+            mblocks = _ceil(B * L, 256)
+            assert pl["lm_tiles"] == _ceil(V, bn) * mblocks
+            if layout == dg.W_PACKED:
+                assert kind in (2, 3)
+            if kind == 0:
+                assert bn % 16 == 0 and 64 <= bn <= 128
+                assert pl["lm_ctas"] <= min(pl["lm_sms"], pl["lm_tiles"])
+                assert pl["lm_epilogue_warps"] == 0
+            else:
+                assert kind in (2, 3) and bn in ((128, 256) if kind == 2 else (128,))
+                assert pl["lm_ctas"] % 2 == 0
+                assert pl["lm_ctas"] <= max(2, pl["lm_sms"] // 2 * 2)
+                assert pl["lm_ctas"] // 2 <= pl["lm_tiles"]
+                assert pl["lm_epilogue_warps"] == (8 if mblocks == 1 else 16)
+            assert pl["lm_ctas"] <= 256
+
+
+def test_canvas_step_plan_rejects_before_planning(lib, planner_defaults):
+    """Bad arguments are answered without touching a device, and the output
+    is left as it was."""
+    p = dg.step_params(1, 256, 1024, 16384, 0.8)
+    out = dg.CanvasStepPlan(*([-7] * len(dg.CanvasStepPlan._fields_)))
+
+    def call(pp=p, P=256, Hq=4, Hkv=1, D=128, sms=152, o=out):
+        return lib.dg_canvas_step_plan(ctypes.byref(pp) if pp is not None else None, P, Hq, Hkv,
+                                       D, sms, ctypes.byref(o) if o is not None else None)
+
+    assert call(pp=None) == 1
+    assert call(o=None) == 1
+    assert call(sms=257) == 1
+    assert call(pp=dg.step_params(1, 256, 1024, 16384, -1.0)) == 1     # temperature
+    assert call(D=64) == 2                                            # head dim
+    assert call(Hq=3, Hkv=2) == 2                                     # GQA group
+    assert call(pp=dg.step_params(1, 256, 1000, 16384, 0.8)) == 2     # d % 64
+    assert call(pp=dg.step_params(1, 256, 1024, 1001, 0.8)) == 2      # V % 8
+    assert [getattr(out, n) for n, _ in dg.CanvasStepPlan._fields_] == [-7] * 12
+    assert call() == 0 and out.lm_ctas == 147
+    import torch
+    if not torch.cuda.is_available():
+        assert call(sms=0) == 5                                       # no device

@@ -344,6 +344,18 @@ def test_lm_head_plan_epilogue_width(monkeypatch):
     assert dg.lm_head_plan(256, 2816, 262144)["epilogue_warps"] == 0
 
 
+def test_canvas_step_plan_on_the_device_equals_the_host_plan(monkeypatch):
+    """sms = 0 plans for the current device: the same plan as the host-side
+    query given the device's SM count."""
+    force_lm_kernel(monkeypatch, None)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for B, P, Hq, Hkv, D, d, V in [(1, 256, 4, 1, 128, 1024, 16384),
+                                   (1, 4096, 16, 8, 256, 2816, 262144)]:
+        p = dg.step_params(B, 256, d, V, 0.8)
+        assert dg.canvas_step_plan(p, P, Hq, Hkv, D, 0) == \
+            dg.canvas_step_plan(p, P, Hq, Hkv, D, sms)
+
+
 def test_denoise_step_uniform_and_one_hot_rows():
     """Zero hidden rows give uniform logits (H = ln V, argmax 0); a row aligned
     with one vocabulary column at large scale gives H ~ 0 at that column."""
