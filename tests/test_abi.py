@@ -376,3 +376,42 @@ def test_canvas_step_plan_rejects_before_planning(lib, planner_defaults):
     import torch
     if not torch.cuda.is_available():
         assert call(sms=0) == 5                                       # no device
+
+
+def _r256(n):
+    return (n + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("env", [{}, {"DG_ATTN_SPLITS": "1"}, {"DG_ATTN_SPLITS": "3"},
+                                 {"DG_ATTN_SPLITS": "64"}, {"DG_ATTN_KERNEL": "single"},
+                                 {"DG_ATTN_KERNEL": "pair"}, {"DG_LM_KERNEL": "single"},
+                                 {"DG_LM_KERNEL": "duo", "DG_LM_BN": "128"},
+                                 {"DG_LM_KERNEL": "fused"}, {"DG_LM_BN": "64"},
+                                 {"DG_ATTN_RESERVE": "40"}])
+def test_canvas_step_plans_fit_the_queried_workspace(lib, planner_defaults, monkeypatch, env):
+    """Whatever the SM count or a forced planner choice, the plan's partial
+    states fit the workspace the queries answered without knowing either:
+    the attention's key-split partials (bf16 outputs and fp32 max / sum per
+    split and query row, after a 256-byte header) and the LM head's per-unit
+    partial states (7 words per row and unit, at most one unit per 64-column
+    tile or 256 units)."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    for B, L, P, Hq, Hkv, D, d, V in [
+            (1, 256, 256, 4, 1, 128, 1024, 16384), (1, 256, 32768, 4, 1, 128, 1024, 16384),
+            (16, 256, 2048, 4, 1, 128, 1024, 16384), (1, 256, 4096, 16, 8, 256, 2816, 262144),
+            (1, 200, 3000, 16, 8, 256, 512, 4096), (1, 1, 100000, 2, 1, 256, 64, 64),
+            (3, 37, 129, 8, 1, 128, 128, 1000)]:
+        p = dg.step_params(B, L, d, V, 0.8)
+        attn_ws = dg.canvas_attn_workspace(B, L, P, Hq, Hkv, D)
+        step_ws = dg.denoise_step_workspace(p)
+        assert dg.canvas_step_workspace(p, P, Hq, Hkv, D) == _r256(step_ws) + attn_ws
+        M = B * L
+        for sms in (8, 24, 76, 148, 152, 200, 256):
+            pl = dg.canvas_step_plan(p, P, Hq, Hkv, D, sms)
+            ns = pl["attn_splits"]
+            need = 256 if ns == 1 else 256 + _r256(ns * M * Hq * D * 2) + _r256(ns * M * Hq * 8)
+            assert need <= attn_ws, (B, L, P, Hq, Hkv, D, sms, pl)
+            units = pl["lm_ctas"] // (1 if pl["lm_kind"] == 0 else 2)
+            assert units <= min(_ceil(M, 256) * _ceil(V, 64), 256)
+            assert 256 + _r256(7 * units * M * 4) + _r256(B * 4) + _r256(M * 4) <= step_ws
