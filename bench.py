@@ -234,11 +234,19 @@ def oracle_step_estimate(cfg, inputs_host, v_sample=8192, attn_rows=64, seed=0, 
     return full, desc, dict(t_lm=t_lm, t_attn=t_at, t_accept=t_acc)
 
 
+# The oracle's sample of a step, the same in the reference arm and in the GPU
+# arm's cpu_baseline: every canvas row against the first ORACLE_V_SAMPLE
+# vocabulary columns, ORACLE_ATTN_ROWS attention rows.
+ORACLE_V_SAMPLE = 16384
+ORACLE_ATTN_ROWS = 64
+
+
 def host_inputs_small_sample(cfg, seed=0):
     """Host (numpy, bf16 bits) inputs of the workload for the oracle sample; W is drawn
     only for the sampled columns to keep the reference arm bounded."""
     cfg_s = dg_synth.StepConfig(cfg.name + "_cols", B=cfg.B, L=cfg.L, Hq=cfg.Hq, Hkv=cfg.Hkv,
-                                D=cfg.D, P=cfg.P, d=cfg.d, V=min(cfg.V, 8192), w_std=cfg.w_std,
+                                D=cfg.D, P=cfg.P, d=cfg.d, V=min(cfg.V, ORACLE_V_SAMPLE),
+                                w_std=cfg.w_std,
                                 row_scale=cfg.row_scale, seed=seed)
     out = dict(dg_synth.attention_inputs(cfg_s))
     out["x"] = dg_synth.lm_hidden(cfg_s)
@@ -254,7 +262,8 @@ def run_reference(args, cfg):
     times, walls = [], []
     desc = ""
     for i in range(args.warmup + args.steps):
-        t, desc, parts = oracle_step_estimate(cfg, host, v_sample=2048, attn_rows=16, seed=i)
+        t, desc, parts = oracle_step_estimate(cfg, host, v_sample=ORACLE_V_SAMPLE,
+                                              attn_rows=ORACLE_ATTN_ROWS, seed=i)
         if i >= args.warmup:
             times.append(t)
             walls.append(sum(parts.values()))
@@ -580,17 +589,19 @@ def run_ours(args, cfg, emit=True):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = {"x": x.view(torch.int16).cpu().numpy().view(np.uint16),
-                "w": _w_columns(w, packed, d, 16384).view(torch.int16).cpu().numpy()
+                "w": _w_columns(w, packed, d, ORACLE_V_SAMPLE).view(torch.int16).cpu().numpy()
                      .view(np.uint16),
                 "q": q.view(torch.int16).cpu().numpy().view(np.uint16),
                 "kp": kp.view(torch.int16).cpu().numpy().view(np.uint16),
                 "vp": vp.view(torch.int16).cpu().numpy().view(np.uint16),
                 "kc": kc.view(torch.int16).cpu().numpy().view(np.uint16),
                 "vc": vc.view(torch.int16).cpu().numpy().view(np.uint16)}
-        sc_host = sc_table[:16384].float().cpu().numpy() if sc else None
-        est = [oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8,
+        sc_host = sc_table[:ORACLE_V_SAMPLE].float().cpu().numpy() if sc else None
+        est = [oracle_step_estimate(cfg, host, v_sample=ORACLE_V_SAMPLE,
+                                    attn_rows=ORACLE_ATTN_ROWS, fp8=fp8,
                                     sc_table=sc_host)[0] for _ in range(2)]
-        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=16384, attn_rows=64, fp8=fp8,
+        _, desc, _ = oracle_step_estimate(cfg, host, v_sample=ORACLE_V_SAMPLE,
+                                          attn_rows=ORACLE_ATTN_ROWS, fp8=fp8,
                                           sc_table=sc_host)
         cpu = dict(value=1.0 / statistics.median(est), unit="steps/s", cores=1, kind="oracle", **_host_cpu(),
                    sample=desc)
