@@ -286,27 +286,25 @@ def run_reference(args, cfg):
 
 
 def run_reference_moe(args, mcfg):
-    """The oracle on the MoE workload (host cores, one thread), on a bounded
-    sample: the first 64 canvas rows of the layer (their routing and
-    experts), scaled to the 256-row layer by rows."""
+    """The oracle on the MoE workload (host cores, one thread): the whole
+    layer, all canvas rows, as the GPU arm's cpu_baseline times it (a
+    couple of seconds per layer)."""
     ws_, rank, _ = _dist()
     if rank != 0:
         return 0
     import oracle
-    sub = dg_synth.MoeConfig(mcfg.name + "_rows", M=64, d=mcfg.d, f=mcfg.f, E=mcfg.E,
-                             top_k=mcfg.top_k, alpha=mcfg.alpha, seed=mcfg.seed)
-    a = dg_synth.moe_inputs(sub)
-    times, walls = [], []
+    a = dg_synth.moe_inputs(mcfg)
+    times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], sub.top_k)
+        oracle.moe_ffn(a["x"], a["wr"], a["wg"], a["wu"], a["wd"], mcfg.top_k)
         if i >= args.warmup:
-            walls.append(time.perf_counter() - t0)
-            times.append(walls[-1] * mcfg.M / sub.M)
+            times.append(time.perf_counter() - t0)
+    walls = times
     per = sum(times) / len(times)
     value = 1.0 / per
-    desc = ("oracle (numpy fp64 matmuls + plain routing, 1 thread): the first %d of %d canvas "
-            "rows, scaled by rows" % (sub.M, mcfg.M))
+    desc = ("oracle (numpy fp64 matmuls + plain routing, 1 thread): the whole layer, all %d "
+            "rows" % mcfg.M)
     line = dict(impl="reference", metric="MoE FFN layers/s (256-token canvas)", value=value,
                 unit="layers/s", n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
                 ms_per_step=per * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
