@@ -1665,6 +1665,7 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
         f2u(p->entropy_bound), f2u(p->stop_threshold), d2u(bp->t_start), d2u(bp->t_end), p->seed,
         static_cast<uint64_t>(bp->max_steps), static_cast<uint64_t>(stride),
         static_cast<uint64_t>(plan.BN), static_cast<uint64_t>(plan.grid * 4 + plan.kind),
+        static_cast<uint64_t>(plan.epi_warps), static_cast<uint64_t>(p->w_layout),
         static_cast<uint64_t>(dev), reinterpret_cast<uint64_t>(fn),
         reinterpret_cast<uint64_t>(user),
         static_cast<uint64_t>(g_checks.load(std::memory_order_relaxed))};
