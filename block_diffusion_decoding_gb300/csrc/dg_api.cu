@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -522,12 +523,36 @@ size_t attn_ws_bytes(int B, int L, int Hq, int D, int nsplit)
 }
 
 // ---------------------------------------------------------------- block-loop graph cache
+// One instantiated loop graph per key (pointers, shapes, parameters, plan,
+// producer); beyond kMaxBlockGraphs the least recently used is dropped.  A
+// call holds its own reference while it launches, and CUDA frees a dropped
+// executable graph that is still running when it completes.
 struct BlockGraph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
 };
 
-std::map<std::vector<uint64_t>, BlockGraph> g_block_graphs;
+void release_block_graph(BlockGraph *g)
+{
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+}
+
+struct BlockGraphEntry {
+    std::shared_ptr<BlockGraph> g;
+    uint64_t last_use = 0;
+};
+
+constexpr size_t kMaxBlockGraphs = 64;
+
+// guarded by g_mu; never destroyed, so no CUDA call runs at process exit
+std::map<std::vector<uint64_t>, BlockGraphEntry> &block_graphs()
+{
+    static auto *cache = new std::map<std::vector<uint64_t>, BlockGraphEntry>();
+    return *cache;
+}
+uint64_t g_block_graph_clock = 0;
 
 size_t block_ws_layout(const dg_step_params *p, int slots, size_t *off_ctl, size_t *off_scratch)
 {
@@ -1670,27 +1695,40 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
         reinterpret_cast<uint64_t>(user),
         static_cast<uint64_t>(g_checks.load(std::memory_order_relaxed))};
 
-    BlockGraph *bgp = nullptr;
+    std::shared_ptr<BlockGraph> bgp;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_block_graphs.find(key);
-        if (it != g_block_graphs.end()) bgp = &it->second;
+        auto &cache = block_graphs();
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            it->second.last_use = ++g_block_graph_clock;
+            bgp = it->second.g;
+        }
     }
-    if (bgp == nullptr) {
+    if (!bgp) {
         BlockGraph bg;
         DG_CUDA_TRY(cudaGraphCreate(&bg.graph, 0));
         cudaGraphConditionalHandle cond;
-        DG_CUDA_TRY(cudaGraphConditionalHandleCreate(&cond, bg.graph, 1, cudaGraphCondAssignDefault));
+        if (cudaGraphConditionalHandleCreate(&cond, bg.graph, 1, cudaGraphCondAssignDefault) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphDestroy(bg.graph);
+            return DG_ERR_CUDA;
+        }
         cudaGraphNodeParams np = {};
         np.type = cudaGraphNodeTypeConditional;
         np.conditional.handle = cond;
         np.conditional.type = cudaGraphCondTypeWhile;
         np.conditional.size = 1;
         cudaGraphNode_t wnode;
-        DG_CUDA_TRY(cudaGraphAddNode(&wnode, bg.graph, nullptr, nullptr, 0, &np));
+        cudaStream_t cap = nullptr;
+        if (cudaGraphAddNode(&wnode, bg.graph, nullptr, nullptr, 0, &np) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphDestroy(bg.graph);
+            return DG_ERR_CUDA;
+        }
         cudaGraph_t body = np.conditional.phGraph_out[0];
-        cudaStream_t cap;
-        DG_CUDA_TRY(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
         if (cudaStreamBeginCaptureToGraph(cap, body, nullptr, nullptr, 0,
                                           cudaStreamCaptureModeRelaxed) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -1738,14 +1776,21 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
             cudaGraphDestroy(bg.graph);
             return DG_ERR_CUDA;
         }
+        std::shared_ptr<BlockGraph> made(new BlockGraph(bg), release_block_graph);
         std::lock_guard<std::mutex> lk(g_mu);
-        auto ins = g_block_graphs.emplace(key, bg);
-        if (!ins.second) {
-            // another thread built the same graph meanwhile: keep that one
-            cudaGraphExecDestroy(bg.exec);
-            cudaGraphDestroy(bg.graph);
+        auto &cache = block_graphs();
+        // another thread may have built the same graph meanwhile: keep that
+        // one (this one is released when `made` goes out of scope)
+        auto ins = cache.emplace(key, BlockGraphEntry{made, 0});
+        ins.first->second.last_use = ++g_block_graph_clock;
+        bgp = ins.first->second.g;
+        if (cache.size() > kMaxBlockGraphs) {
+            auto lru = cache.end();
+            for (auto e = cache.begin(); e != cache.end(); ++e)
+                if (e != ins.first && (lru == cache.end() || e->second.last_use < lru->second.last_use))
+                    lru = e;
+            if (lru != cache.end()) cache.erase(lru);
         }
-        bgp = &ins.first->second;
     }
     loop_init_kernel<<<std::max(1, (M + 255) / 256), 256, 0, st>>>(
         ctl, bp->max_steps, bp->t_start, bp->t_end, p->B, done, io->steps_taken, io->canvas, prev,
