@@ -525,17 +525,23 @@ size_t attn_ws_bytes(int B, int L, int Hq, int D, int nsplit)
 // ---------------------------------------------------------------- block-loop graph cache
 // One instantiated loop graph per key (pointers, shapes, parameters, plan,
 // producer); beyond kMaxBlockGraphs the least recently used is dropped.  A
-// call holds its own reference while it launches, and CUDA frees a dropped
-// executable graph that is still running when it completes.
+// call holds its own reference while it launches and records `done` after
+// the launch; a dropped graph is freed once its last launch has completed.
 struct BlockGraph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
+    cudaEvent_t done = nullptr;
 };
 
 void release_block_graph(BlockGraph *g)
 {
+    if (g->done) {
+        cudaEventSynchronize(g->done);
+        cudaEventDestroy(g->done);
+    }
     if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
+    (void)cudaGetLastError();
     delete g;
 }
 
@@ -1776,7 +1782,16 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
             cudaGraphDestroy(bg.graph);
             return DG_ERR_CUDA;
         }
+        if (cudaEventCreateWithFlags(&bg.done, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cudaGraphExecDestroy(bg.exec);
+            cudaGraphDestroy(bg.graph);
+            return DG_ERR_CUDA;
+        }
+        // released after the lock below: a graph another thread built
+        // meanwhile, or the one dropped from the cache
         std::shared_ptr<BlockGraph> made(new BlockGraph(bg), release_block_graph);
+        std::shared_ptr<BlockGraph> dropped;
         std::lock_guard<std::mutex> lk(g_mu);
         auto &cache = block_graphs();
         // another thread may have built the same graph meanwhile: keep that
@@ -1789,7 +1804,10 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
             for (auto e = cache.begin(); e != cache.end(); ++e)
                 if (e != ins.first && (lru == cache.end() || e->second.last_use < lru->second.last_use))
                     lru = e;
-            if (lru != cache.end()) cache.erase(lru);
+            if (lru != cache.end()) {
+                dropped = lru->second.g;
+                cache.erase(lru);
+            }
         }
     }
     loop_init_kernel<<<std::max(1, (M + 255) / 256), 256, 0, st>>>(
@@ -1799,6 +1817,7 @@ static int block_run(const uint16_t *hidden_steps, dg_hidden_fn fn, void *user, 
     DG_LAUNCHED();
     DG_CUDA_TRY(cudaGetLastError());
     DG_CUDA_TRY(cudaGraphLaunch(bgp->exec, st));
+    DG_CUDA_TRY(cudaEventRecord(bgp->done, st));
     return DG_OK;
 }
 

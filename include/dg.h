@@ -368,9 +368,10 @@ int dg_moe_ffn(const uint16_t *x, const uint16_t *w_router, const uint16_t *w_ga
 /* host waits only at the end.  The library keeps the instantiated graph of   */
 /* each distinct (pointers, shapes, params incl. the seed, block params, W    */
 /* layout, LM-head plan, producer) and replays it on a repeated call; it      */
-/* keeps at most 64, dropping the least recently used (a dropped graph that   */
-/* is still running completes first).  A call with a new key captures and    */
-/* instantiates a graph on the host before it launches.                       */
+/* keeps at most 64, dropping the least recently used (the call that drops   */
+/* one waits on the host for that graph's last launch to complete before it  */
+/* frees it).  A call with a new key captures and instantiates a graph on     */
+/* the host before it launches.                                               */
 /* hidden_steps: device bf16, hidden_step_stride elements apart per step (0 = */
 /* the same hidden states every step); the decoder body that would produce    */
 /* them is outside this library.                                              */
