@@ -38,7 +38,8 @@
  *     DG_ERR_UNSUPPORTED without launching.
  *   - Kernel choice: the library picks the LM-head and attention kernels and
  *     their tilings from the shapes and the SM count (dg_lm_head_plan reports
- *     the LM-head choice).  For testing and tuning, the environment variables
+ *     the LM-head choice, dg_canvas_step_plan the whole step's, for any SM
+ *     count).  For testing and tuning, the environment variables
  *     DG_LM_KERNEL (single | duo | fused), DG_LM_BN (tile width),
  *     DG_LM_EPI (8 | 16: epilogue warps of the 2-SM kernel, bf16 operands),
  *     DG_ATTN_KERNEL (single | pair), DG_ATTN_SPLITS (key splits) and
